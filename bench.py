@@ -1,0 +1,440 @@
+"""Throughput benchmark of the gated delta rule forward pass on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--no-cpu-baseline]
+
+One step = one gdn_fwd call (every stage of the chunked forward pass) over the
+whole synthetic batch of the workload (default: B=4, H=16, T=4096,
+d_k=d_v=128, bf16 I/O, fp32 state).  Inputs are resident in HBM before the
+timed region; L2 is flushed (a 256 MiB write) before every timed step and
+each step is timed with CUDA events on the launching stream.  Rank 0 prints
+one JSON line.  Under torchrun every rank runs an independent replica of the
+workload (the path has no cross-GPU exchange), "scaling": "weak", and the
+slowest rank's time is reported.
+
+--impl reference times the fp64 CPU oracle on a bounded sample of the same
+workload on the host cores (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "GDN chunked fwd tokens/s (B·H·T/s) and % of roofline, bf16, d=128, 1×GB300"
+UNIT = "tokens/s"
+DEFAULT_WORKLOAD = "gdn_fwd_b4_h16_t4096_d128_bf16"
+L2_FLUSH_BYTES = 256 << 20
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target CPU time of the oracle sample")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world <= 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def workload_shape(name):
+    cfg = synth.WORKLOADS[name]
+    if "N" in cfg:
+        lens = synth.varlen_lengths(cfg["N"], cfg["len_min"], cfg["len_max"], cfg["seed"])
+        return dict(kind="varlen", H=cfg["H"], dk=cfg["dk"], dv=cfg["dv"], io=cfg["io"],
+                    lengths=lens, tokens=int(lens.sum()) * cfg["H"], N=cfg["N"],
+                    h0=cfg["h0_std"] > 0)
+    return dict(kind="dense", B=cfg["B"], H=cfg["H"], T=cfg["T"], dk=cfg["dk"], dv=cfg["dv"],
+                io=cfg["io"], tokens=cfg["B"] * cfg["H"] * cfg["T"], N=cfg["B"],
+                h0=cfg["h0_std"] > 0)
+
+
+def algorithmic(shape):
+    """Compulsory HBM bytes and chunked-algorithm FLOPs of one forward call.
+
+    Bytes: every q, k, v, o element once at the I/O width, two fp32 gates per
+    token-head, h0 (when given) read once and hT written once per
+    (sequence, head).  FLOPs per token-head, counting full 64x64 chunk tiles
+    as issued: 6*C*d_k + 4*C*d_v + 6*d_k*d_v (C = 64)."""
+    io = 2 if shape["io"] == "bf16" else 4
+    dk, dv, C = shape["dk"], shape["dv"], 64
+    th = shape["tokens"]
+    seqheads = shape["N"] * shape["H"]
+    state = seqheads * dk * dv * 4
+    by = th * ((2 * dk + 2 * dv) * io + 8) + state * (2 if shape["h0"] else 1)
+    flops = th * (6 * C * dk + 4 * C * dv + 6 * dk * dv)
+    return by, flops
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "gated_deltanet_recurrence_gdn_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    summary is missing or was taken on different kernel sources."""
+    p = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(p):
+        return None
+    want = kernel_source_hash()
+    for line in open(p):
+        parts = line.split()
+        if len(parts) >= 4 and not line.startswith("#"):
+            k, w, src_hash, traffic = parts[:4]
+            if k == kernel and w == workload and src_hash == want:
+                return float(traffic)
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.Q,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for nm, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        load = [x for x in sm if mx and x >= 0.5 * mx] or sm
+        return {"sm_mhz": statistics.median(load), "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------ our GPU arm
+
+
+def make_inputs(name, device):
+    return synth.make_workload(name, device=device)
+
+
+def call(gdn, x, out=None):
+    if x.cu_seqlens is not None:
+        return gdn.gdn_fwd_varlen(x.q, x.k, x.v, x.log_alpha, x.beta, x.cu_seqlens, x.h0,
+                                  out=out)
+    return gdn.gdn_fwd(x.q, x.k, x.v, x.log_alpha, x.beta, x.h0, out=out)
+
+
+def run_ours(args, world, rank, local):
+    import gated_deltanet_recurrence_gdn_gb300 as gdn
+    gdn.load()
+    dev = torch.device("cuda", local)
+    shape = workload_shape(args.workload)
+    x = make_inputs(args.workload, dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    for _ in range(max(args.warmup, 3)):
+        call(gdn, x)
+    gdn.sync_check(dev)
+
+    # ---- device-timed region: inputs resident, L2 flushed before each step
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    out = torch.empty_like(x.v)
+    launches0 = gdn.kernel_launches()
+    gdn.kernel_timer(True)
+    gdn.kernel_timer_read()
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t_wall = time.perf_counter()
+    with ClockSampler(local) as clocks:
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record(stream)
+            call(gdn, x, out=out)
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(world)
+    wall = time.perf_counter() - t_wall
+    launches = gdn.kernel_launches() - launches0
+    k_ms, k_n, k_name = gdn.kernel_timer_read()
+    gdn.kernel_timer(False)
+    gdn.sync_check(dev)
+    step_ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / args.steps
+    step_ms = max_over_ranks(step_ms, world)
+    kern_ms = max_over_ranks(k_ms / max(k_n, 1), world)
+
+    # ---- end to end: pinned host inputs -> device, forward, result -> host
+    host = {k: (None if t is None else t.cpu().pin_memory()) for k, t in x.tensors().items()}
+    dev_buf = {k: (None if t is None else torch.empty_like(t)) for k, t in x.tensors().items()}
+    o_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    hT_shape = ((shape["N"], shape["H"], shape["dv"], shape["dk"]) if shape["kind"] == "varlen"
+                else (shape["B"], shape["H"], shape["dv"], shape["dk"]))
+    h_host = torch.empty(hT_shape, dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values() if t is not None)
+    d2h = o_host.numel() * o_host.element_size() + h_host.numel() * 4
+    e2e_steps = max(3, min(args.steps, 10))
+
+    def e2e_step():
+        for k_, t in host.items():
+            if t is not None:
+                dev_buf[k_].copy_(t, non_blocking=True)
+        y = synth.Inputs(dev_buf["q"], dev_buf["k"], dev_buf["v"], dev_buf["log_alpha"],
+                         dev_buf["beta"], dev_buf["h0"], x.cu_seqlens)
+        o, hT = call(gdn, y, out=out)
+        o_host.copy_(o, non_blocking=True)
+        h_host.copy_(hT, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
+
+    by, flops = algorithmic(shape)
+    hbm, tf, src = load_peaks()
+    achieved = by / (kern_ms * 1e-3) / 1e9
+    res = {
+        "metric": METRIC,
+        "value": shape["tokens"] * world / (step_ms * 1e-3),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": step_ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if shape["io"] == "bf16" else "f32",
+        "data": "synthetic (seeded; q,k L2-normalised Gaussian, v Gaussian, sigmoid beta, "
+                "-softplus log-gates)",
+        "config": {"workload": args.workload, "token_heads": shape["tokens"],
+                   "d_k": shape["dk"], "d_v": shape["dv"], "chunk": 64,
+                   "l2": "flushed before every timed step (256 MiB write)",
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "wall_s_timed_region": wall},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "peak_source": src + " (MEASURED_PEAKS.json hbm_gbs)"
+                     if src == "measured" else "fallback 6.8 TB/s",
+                     "traffic": recorded_traffic(k_name, args.workload),
+                     "kernel": k_name, "kernel_ms": kern_ms,
+                     "algorithmic_bytes": by, "algorithmic_flops": flops,
+                     "tensor_frac_of_peak": flops / (kern_ms * 1e-3) / (tf * 1e12)},
+        "clocks": clocks.summary(),
+        "e2e": {"value": shape["tokens"] * world / (e2e_ms * 1e-3), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms},
+        "gpu_launches": launches,
+        "impl_used": {1: "simt", 2: "tc"}.get(gdn.last_impl(), "none"),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(args.workload, x, args.cpu_seconds)
+    elif rank == 0 and world == 1:
+        res["cpu_baseline"] = None
+    return res
+
+
+# ------------------------------------------------------------- the oracle
+
+
+def oracle_sample(name, x, budget_s, max_heads=None):
+    """Run the fp64 oracle (1 thread) on whole heads of the workload until
+    about budget_s seconds of CPU time; returns (token-heads, seconds, desc)."""
+    import oracle
+    oracle.build()
+    f64 = synth.to_f64
+    if x.cu_seqlens is not None:
+        cu = x.cu_seqlens.cpu().numpy()
+        units = [(n, h) for n in range(len(cu) - 1) for h in range(x.q.shape[0])]
+
+        def one(u):
+            n, h = u
+            a, b = int(cu[n]), int(cu[n + 1])
+            s = np.s_[h, a:b]
+            args = [f64(t[s])[None, None] for t in (x.q, x.k, x.v, x.log_alpha, x.beta)]
+            h0 = None if x.h0 is None else f64(x.h0[n, h])[None, None]
+            t0 = time.perf_counter()
+            oracle.gdn_fwd(*args, h0)
+            return b - a, time.perf_counter() - t0
+    else:
+        units = [(b, h) for b in range(x.q.shape[0]) for h in range(x.q.shape[1])]
+
+        def one(u):
+            b, h = u
+            args = [f64(t[b, h])[None, None] for t in (x.q, x.k, x.v, x.log_alpha, x.beta)]
+            h0 = None if x.h0 is None else f64(x.h0[b, h])[None, None]
+            t0 = time.perf_counter()
+            oracle.gdn_fwd(*args, h0)
+            return x.q.shape[2], time.perf_counter() - t0
+
+    toks, secs, used = 0, 0.0, 0
+    for u in units[: max_heads or len(units)]:
+        n, s = one(u)
+        toks += n
+        secs += s
+        used += 1
+        if secs >= budget_s:
+            break
+    return toks, secs, "%d of %d (sequence, head) problems, whole length each" % (used, len(units))
+
+
+def cpu_baseline(name, x, budget_s):
+    toks, secs, desc = oracle_sample(name, x, budget_s)
+    return {"value": toks / secs, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": desc + "; fp64 single-threaded C, %.1f s" % secs,
+            "host_cpus": os.cpu_count()}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return None
+    shape = workload_shape(args.workload)
+    x = make_inputs(args.workload, "cpu")
+    per_step = max(1.0, min(args.cpu_seconds, 60.0 / max(args.steps + args.warmup, 1)))
+    for _ in range(args.warmup):
+        oracle_sample(args.workload, x, per_step / 4, max_heads=1)
+    toks, secs = 0, 0.0
+    desc = ""
+    for _ in range(args.steps):
+        t, s, desc = oracle_sample(args.workload, x, per_step)
+        toks += t
+        secs += s
+    value = toks / secs
+    return {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)",
+        "config": {"workload": args.workload, "token_heads": shape["tokens"],
+                   "d_k": shape["dk"], "d_v": shape["dv"], "chunk": 64},
+        "impl": "reference",
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": "per step: " + desc + " (fp64 single-threaded C)"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        res = run_reference(args, world, rank)
+    else:
+        res = run_ours(args, world, rank, local)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,227 @@
+"""Thin Python binding of libgdn (the GB300 gated delta rule forward library).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of ``libgdn.so``.  PyTorch supplies device memory and the current
+stream.  If the library has not been built, importing works but every call
+raises -- there is no CPU fallback.
+
+    o, hT = gdn_fwd(q, k, v, log_alpha, beta, h0=None)
+    o, hT = gdn_fwd_varlen(q, k, v, log_alpha, beta, cu_seqlens, h0=None)
+
+Layouts follow ``include/gdn.h``: dense q, k [B,H,T,d_k], v [B,H,T,d_v]; packed
+q, k [H,T_total,d_k], v [H,T_total,d_v]; gates fp32; h0 / hT [.., H, d_v, d_k]
+fp32; q, k, v share one dtype (bf16 or fp32), which is also the dtype of o.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libgdn.so")
+
+GDN_OK = 0
+GDN_ERR_INVALID_ARG = 1
+GDN_ERR_UNSUPPORTED = 2
+GDN_ERR_ALIGNMENT = 3
+GDN_ERR_CUDA = 4
+GDN_ERR_DEVICE_TIMEOUT = 5
+GDN_F32 = 0
+GDN_BF16 = 1
+GDN_OPT_IMPL = 0
+GDN_OPT_SEGMENTS = 1
+GDN_OPT_WAIT_LIMIT = 2
+GDN_IMPL_AUTO = 0
+GDN_IMPL_SIMT = 1
+GDN_IMPL_TC = 2
+
+CHUNK = 64
+
+_lib = None
+
+_vp = ctypes.c_void_p
+_i = ctypes.c_int
+
+# (name, restype, argtypes) of every symbol include/gdn.h declares.
+ABI = [
+    ("gdn_fwd", _i, [_vp] * 8 + [_i] * 7 + [_vp]),
+    ("gdn_fwd_varlen", _i, [_vp] * 9 + [_i] * 7 + [_vp]),
+    ("gdn_status_string", ctypes.c_char_p, [_i]),
+    ("gdn_sync_check", _i, [_vp]),
+    ("gdn_set_option", _i, [_i, ctypes.c_longlong]),
+    ("gdn_get_option", ctypes.c_longlong, [_i]),
+    ("gdn_kernel_timer", _i, [_i]),
+    ("gdn_kernel_timer_read", _i, [ctypes.POINTER(ctypes.c_double),
+                                   ctypes.POINTER(ctypes.c_longlong),
+                                   ctypes.POINTER(ctypes.c_char_p)]),
+    ("gdn_kernel_launches", ctypes.c_uint64, []),
+    ("gdn_last_impl", _i, []),
+]
+
+
+class GdnError(RuntimeError):
+    def __init__(self, status, what=""):
+        self.status = status
+        super().__init__("%s%s" % (what + ": " if what else "", status_string(status)))
+
+
+def load(path: str | None = None):
+    """Load libgdn.so (built by ``_build.build()``) and declare its ABI."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise ImportError("libgdn.so is not built (%s); run __graft_entry__.build()" % p)
+    lib = ctypes.CDLL(p)
+    for name, res, args in ABI:
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    try:
+        return load().gdn_status_string(int(status)).decode()
+    except ImportError:
+        return "status %d" % status
+
+
+def _check(rc, what):
+    if rc != GDN_OK:
+        raise GdnError(rc, what)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+_DT = {torch.bfloat16: GDN_BF16, torch.float32: GDN_F32}
+
+
+def _prep_io(q, k, v, log_alpha, beta, h0):
+    for name, t in (("q", q), ("k", k), ("v", v), ("log_alpha", log_alpha), ("beta", beta)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise ValueError("%s must be a CUDA tensor" % name)
+        if not t.is_contiguous():
+            raise ValueError("%s must be contiguous" % name)
+    if q.dtype not in _DT or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v must share one dtype, bf16 or fp32")
+    if log_alpha.dtype != torch.float32 or beta.dtype != torch.float32:
+        raise ValueError("log_alpha and beta must be fp32")
+    if h0 is not None and (h0.dtype != torch.float32 or not h0.is_contiguous() or not h0.is_cuda):
+        raise ValueError("h0 must be a contiguous fp32 CUDA tensor")
+
+
+def gdn_fwd(q, k, v, log_alpha, beta, h0=None, *, chunk=CHUNK, out=None, final_state=True,
+            check=False):
+    """Dense forward: returns (o [B,H,T,d_v], hT [B,H,d_v,d_k] or None)."""
+    lib = load()
+    _prep_io(q, k, v, log_alpha, beta, h0)
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    if k.shape != q.shape or v.shape[:3] != (B, H, T) or log_alpha.shape != (B, H, T) \
+            or beta.shape != (B, H, T):
+        raise ValueError("shape mismatch")
+    if h0 is not None and h0.shape != (B, H, dv, dk):
+        raise ValueError("h0 must be [B,H,d_v,d_k]")
+    o = out if out is not None else torch.empty((B, H, T, dv), dtype=q.dtype, device=q.device)
+    hT = torch.empty((B, H, dv, dk), dtype=torch.float32, device=q.device) if final_state else None
+    with torch.cuda.device(q.device):
+        rc = lib.gdn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(h0),
+                         _ptr(o), _ptr(hT), B, H, T, dk, dv, chunk, _DT[q.dtype],
+                         _stream(q.device))
+        _check(rc, "gdn_fwd")
+        if check:
+            _check(lib.gdn_sync_check(_stream(q.device)), "gdn_fwd (device)")
+    return o, hT
+
+
+def gdn_fwd_varlen(q, k, v, log_alpha, beta, cu_seqlens, h0=None, *, chunk=CHUNK, out=None,
+                   final_state=True, check=False):
+    """Packed forward: returns (o [H,T_total,d_v], hT [N,H,d_v,d_k] or None)."""
+    lib = load()
+    _prep_io(q, k, v, log_alpha, beta, h0)
+    H, TT, dk = q.shape
+    dv = v.shape[-1]
+    if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda or cu_seqlens.dim() != 1:
+        raise ValueError("cu_seqlens must be a 1-D int32 CUDA tensor")
+    N = cu_seqlens.shape[0] - 1
+    if k.shape != q.shape or v.shape[:2] != (H, TT) or log_alpha.shape != (H, TT) \
+            or beta.shape != (H, TT):
+        raise ValueError("shape mismatch")
+    if h0 is not None and h0.shape != (N, H, dv, dk):
+        raise ValueError("h0 must be [N,H,d_v,d_k]")
+    o = out if out is not None else torch.empty((H, TT, dv), dtype=q.dtype, device=q.device)
+    hT = torch.empty((N, H, dv, dk), dtype=torch.float32, device=q.device) if final_state else None
+    with torch.cuda.device(q.device):
+        rc = lib.gdn_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
+                                _ptr(h0), _ptr(o), _ptr(hT), _ptr(cu_seqlens.contiguous()), N,
+                                H, TT, dk, dv, chunk, _DT[q.dtype], _stream(q.device))
+        _check(rc, "gdn_fwd_varlen")
+        if check:
+            _check(lib.gdn_sync_check(_stream(q.device)), "gdn_fwd_varlen (device)")
+    return o, hT
+
+
+def sync_check(device=None):
+    """Synchronise the current stream and raise if a kernel recorded an error."""
+    _check(load().gdn_sync_check(_stream(device)), "device")
+
+
+def set_option(key: int, value: int):
+    _check(load().gdn_set_option(int(key), int(value)), "gdn_set_option")
+
+
+def get_option(key: int) -> int:
+    return int(load().gdn_get_option(int(key)))
+
+
+def kernel_launches() -> int:
+    return int(load().gdn_kernel_launches())
+
+
+def kernel_timer(enable: bool):
+    _check(load().gdn_kernel_timer(1 if enable else 0), "gdn_kernel_timer")
+
+
+def kernel_timer_read():
+    """(total_ms, launches, kernel_name) of the dominant kernel since the last read."""
+    ms = ctypes.c_double(0.0)
+    n = ctypes.c_longlong(0)
+    name = ctypes.c_char_p()
+    _check(load().gdn_kernel_timer_read(ctypes.byref(ms), ctypes.byref(n), ctypes.byref(name)),
+           "gdn_kernel_timer_read")
+    return ms.value, n.value, (name.value or b"").decode()
+
+
+def last_impl() -> int:
+    return int(load().gdn_last_impl())
+
+
+class use_impl:
+    """Context manager forcing GDN_IMPL_SIMT / GDN_IMPL_TC / GDN_IMPL_AUTO."""
+
+    def __init__(self, impl: int, segments: int | None = None):
+        self.impl, self.segments = impl, segments
+
+    def __enter__(self):
+        self.prev = (get_option(GDN_OPT_IMPL), get_option(GDN_OPT_SEGMENTS))
+        set_option(GDN_OPT_IMPL, self.impl)
+        if self.segments is not None:
+            set_option(GDN_OPT_SEGMENTS, self.segments)
+        return self
+
+    def __exit__(self, *exc):
+        set_option(GDN_OPT_IMPL, self.prev[0])
+        set_option(GDN_OPT_SEGMENTS, self.prev[1])
+        return False

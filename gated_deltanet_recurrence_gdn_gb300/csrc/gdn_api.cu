@@ -1,0 +1,239 @@
+// gdn_api.cu -- the C ABI of libgdn: argument checks, dispatch, error word.
+#include <atomic>
+#include <cstdint>
+#include <mutex>
+#include <vector>
+
+#include "gdn_internal.h"
+
+namespace gdn {
+
+namespace {
+__device__ int g_error_word = 0;
+
+std::atomic<uint64_t> g_launches{0};
+std::atomic<long long> g_opt_impl{GDN_IMPL_AUTO};
+std::atomic<long long> g_opt_segments{0};
+std::atomic<long long> g_opt_wait_limit{0};
+std::atomic<int> g_last_impl{0};
+
+struct TimerState {
+    std::mutex mu;
+    bool enabled = false;
+    std::vector<cudaEvent_t> ev;  // pairs: ev[2i] start, ev[2i+1] stop
+    size_t used = 0;              // pairs recorded since the last read
+    const char *kernel = "";
+};
+TimerState &timer() {
+    static TimerState t;
+    return t;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+gdn_status check_common(const void *q, const void *k, const void *v, const float *la,
+                        const float *beta, const float *h0, const void *o, const float *hT,
+                        int H, int d_k, int d_v, int chunk, gdn_dtype dt, bool need_tokens) {
+    if (H < 0 || d_k <= 0 || d_v <= 0) return GDN_ERR_INVALID_ARG;
+    if (H > 65535) return GDN_ERR_UNSUPPORTED;  // heads form a grid dimension
+    if (dt != GDN_F32 && dt != GDN_BF16) return GDN_ERR_INVALID_ARG;
+    if (chunk != kChunk) return GDN_ERR_UNSUPPORTED;
+    if (d_k % 8 || d_v % 8 || d_k > 128 || d_v > 256) return GDN_ERR_UNSUPPORTED;
+    if (need_tokens && (!q || !k || !v || !la || !beta || !o)) return GDN_ERR_INVALID_ARG;
+    const void *ptrs[] = {q, k, v, la, beta, h0, o, hT};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return GDN_ERR_ALIGNMENT;
+    return GDN_OK;
+}
+
+gdn_status dispatch(FwdArgs &a) {
+    const long long impl = g_opt_impl.load();
+    gdn_status rc;
+    int used;
+    if (impl == GDN_IMPL_SIMT || (impl == GDN_IMPL_AUTO && !tc_supported(a))) {
+        rc = simt_forward(a);
+        used = GDN_IMPL_SIMT;
+    } else {
+        if (!tc_supported(a)) return GDN_ERR_UNSUPPORTED;
+        rc = tc_forward(a);
+        used = GDN_IMPL_TC;
+    }
+    if (rc == GDN_OK) g_last_impl.store(used);
+    return rc;
+}
+}  // namespace
+
+int *device_error_word() {
+    void *p = nullptr;
+    cudaGetSymbolAddress(&p, g_error_word);
+    return static_cast<int *>(p);
+}
+
+int timer_begin(cudaStream_t st, const char *kernel) {
+    TimerState &t = timer();
+    std::lock_guard<std::mutex> lk(t.mu);
+    if (!t.enabled) return -1;
+    if (t.used * 2 + 2 > t.ev.size()) {
+        cudaEvent_t a, b;
+        if (cudaEventCreate(&a) != cudaSuccess) return -1;
+        if (cudaEventCreate(&b) != cudaSuccess) {
+            cudaEventDestroy(a);
+            return -1;
+        }
+        t.ev.push_back(a);
+        t.ev.push_back(b);
+    }
+    const int slot = (int)t.used++;
+    t.kernel = kernel;
+    cudaEventRecord(t.ev[2 * slot], st);
+    return slot;
+}
+
+void timer_end(int slot, cudaStream_t st) {
+    if (slot < 0) return;
+    TimerState &t = timer();
+    std::lock_guard<std::mutex> lk(t.mu);
+    cudaEventRecord(t.ev[2 * slot + 1], st);
+}
+
+void count_launch(int n) { g_launches.fetch_add((uint64_t)n); }
+
+long long option(int key) {
+    switch (key) {
+        case GDN_OPT_IMPL: return g_opt_impl.load();
+        case GDN_OPT_SEGMENTS: return g_opt_segments.load();
+        case GDN_OPT_WAIT_LIMIT: return g_opt_wait_limit.load();
+        default: return -1;
+    }
+}
+
+}  // namespace gdn
+
+using namespace gdn;
+
+extern "C" {
+
+gdn_status gdn_fwd(const void *q, const void *k, const void *v, const float *log_alpha,
+                   const float *beta, const float *h0, void *o, float *hT, int B, int H, int T,
+                   int d_k, int d_v, int chunk, gdn_dtype dt, void *stream) {
+    if (B < 0 || T < 0) return GDN_ERR_INVALID_ARG;
+    const bool tokens = (long long)B * H * T > 0;
+    gdn_status rc = check_common(q, k, v, log_alpha, beta, h0, o, hT, H, d_k, d_v, chunk, dt,
+                                 tokens);
+    if (rc != GDN_OK) return rc;
+    if ((long long)B * H == 0) return GDN_OK;
+    FwdArgs a{};
+    a.q = q; a.k = k; a.v = v; a.log_alpha = log_alpha; a.beta = beta; a.h0 = h0;
+    a.o = o; a.hT = hT;
+    a.sm = SeqMap{nullptr, B, H, T, 0};
+    a.dk = d_k; a.dv = d_v; a.dt = dt;
+    a.rows = (long long)B * H * T;
+    a.max_chunks = (T + kChunk - 1) / kChunk;
+    a.chunk_slots = (int)((long long)B * a.max_chunks);
+    a.stream = static_cast<cudaStream_t>(stream);
+    if ((long long)B * a.max_chunks > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
+    return dispatch(a);
+}
+
+gdn_status gdn_fwd_varlen(const void *q, const void *k, const void *v, const float *log_alpha,
+                          const float *beta, const float *h0, void *o, float *hT,
+                          const int32_t *cu_seqlens, int N, int H, int T_total, int d_k,
+                          int d_v, int chunk, gdn_dtype dt, void *stream) {
+    if (N < 0 || T_total < 0) return GDN_ERR_INVALID_ARG;
+    if (N > 0 && !cu_seqlens) return GDN_ERR_INVALID_ARG;
+    if (N == 0 && T_total != 0) return GDN_ERR_INVALID_ARG;
+    const bool tokens = (long long)H * T_total > 0;
+    gdn_status rc = check_common(q, k, v, log_alpha, beta, h0, o, hT, H, d_k, d_v, chunk, dt,
+                                 tokens);
+    if (rc != GDN_OK) return rc;
+    if ((long long)N * H == 0) return GDN_OK;
+    FwdArgs a{};
+    a.q = q; a.k = k; a.v = v; a.log_alpha = log_alpha; a.beta = beta; a.h0 = h0;
+    a.o = o; a.hT = hT;
+    a.sm = SeqMap{cu_seqlens, N, H, 0, T_total};
+    a.dk = d_k; a.dv = d_v; a.dt = dt;
+    a.rows = (long long)H * T_total;
+    a.max_chunks = (T_total + kChunk - 1) / kChunk;
+    const long long slots = (long long)T_total / kChunk + N;
+    if (slots > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
+    a.chunk_slots = (int)slots;
+    a.stream = static_cast<cudaStream_t>(stream);
+    return dispatch(a);
+}
+
+const char *gdn_status_string(gdn_status s) {
+    switch (s) {
+        case GDN_OK: return "GDN_OK";
+        case GDN_ERR_INVALID_ARG: return "GDN_ERR_INVALID_ARG: invalid argument";
+        case GDN_ERR_UNSUPPORTED: return "GDN_ERR_UNSUPPORTED: unsupported chunk, width or implementation";
+        case GDN_ERR_ALIGNMENT: return "GDN_ERR_ALIGNMENT: pointer not 16-byte aligned";
+        case GDN_ERR_CUDA: return "GDN_ERR_CUDA: CUDA runtime error";
+        case GDN_ERR_DEVICE_TIMEOUT: return "GDN_ERR_DEVICE_TIMEOUT: bounded device wait gave up";
+        default: return "unknown gdn_status";
+    }
+}
+
+gdn_status gdn_sync_check(void *stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return GDN_ERR_CUDA;
+    int word = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&word, g_error_word, sizeof(int)) != cudaSuccess) return GDN_ERR_CUDA;
+    if (word != 0 && cudaMemcpyToSymbol(g_error_word, &zero, sizeof(int)) != cudaSuccess)
+        return GDN_ERR_CUDA;
+    if (word == kErrTimeout) return GDN_ERR_DEVICE_TIMEOUT;
+    if (word == kErrSeqlens) return GDN_ERR_INVALID_ARG;
+    return word == 0 ? GDN_OK : GDN_ERR_CUDA;
+}
+
+gdn_status gdn_set_option(int key, long long value) {
+    switch (key) {
+        case GDN_OPT_IMPL:
+            if (value < GDN_IMPL_AUTO || value > GDN_IMPL_TC) return GDN_ERR_INVALID_ARG;
+            g_opt_impl.store(value);
+            return GDN_OK;
+        case GDN_OPT_SEGMENTS:
+            if (value < 0 || value > 4096) return GDN_ERR_INVALID_ARG;
+            g_opt_segments.store(value);
+            return GDN_OK;
+        case GDN_OPT_WAIT_LIMIT:
+            if (value < 0) return GDN_ERR_INVALID_ARG;
+            g_opt_wait_limit.store(value);
+            return GDN_OK;
+        default:
+            return GDN_ERR_INVALID_ARG;
+    }
+}
+
+long long gdn_get_option(int key) { return option(key); }
+
+gdn_status gdn_kernel_timer(int enable) {
+    TimerState &t = timer();
+    std::lock_guard<std::mutex> lk(t.mu);
+    t.enabled = enable != 0;
+    t.used = 0;
+    return GDN_OK;
+}
+
+gdn_status gdn_kernel_timer_read(double *total_ms, long long *launches, const char **kernel) {
+    TimerState &t = timer();
+    std::lock_guard<std::mutex> lk(t.mu);
+    double sum = 0.0;
+    for (size_t i = 0; i < t.used; ++i) {
+        float ms = 0.f;
+        if (cudaEventSynchronize(t.ev[2 * i + 1]) != cudaSuccess ||
+            cudaEventElapsedTime(&ms, t.ev[2 * i], t.ev[2 * i + 1]) != cudaSuccess)
+            return GDN_ERR_CUDA;
+        sum += ms;
+    }
+    if (total_ms) *total_ms = sum;
+    if (launches) *launches = (long long)t.used;
+    if (kernel) *kernel = t.kernel;
+    t.used = 0;
+    return GDN_OK;
+}
+
+uint64_t gdn_kernel_launches(void) { return g_launches.load(); }
+
+int gdn_last_impl(void) { return g_last_impl.load(); }
+
+}  // extern "C"

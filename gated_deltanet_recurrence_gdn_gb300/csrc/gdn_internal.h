@@ -1,0 +1,69 @@
+// gdn_internal.h -- shared host/device declarations of libgdn (not installed).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gdn.h"
+
+namespace gdn {
+
+constexpr int kChunk = 64;
+
+// Device error word codes (first error wins).
+enum : int { kErrNone = 0, kErrTimeout = 1, kErrSeqlens = 2 };
+
+// Where the tokens of (sequence n, head h) live.  Dense tensors are
+// [B][H][T][d] (sequence n = batch index); packed tensors are [H][T_total][d]
+// with sequence n at tokens [cu[n], cu[n+1]).  Both reduce to "row0 + t" in a
+// [rows][d] view, rows = B*H*T or H*T_total.
+struct SeqMap {
+    const int32_t *cu;  // device, N+1 entries; nullptr for dense
+    int N;              // number of sequences (B for dense)
+    int H;
+    int T;              // dense sequence length
+    int T_total;        // packed token count
+
+    __device__ __forceinline__ void get(int n, int h, long long &row0, int &len) const {
+        if (cu) {
+            int a = __ldg(cu + n), b = __ldg(cu + n + 1);
+            row0 = (long long)h * T_total + a;
+            len = b - a;
+        } else {
+            row0 = ((long long)n * H + h) * (long long)T;
+            len = T;
+        }
+    }
+};
+
+struct FwdArgs {
+    const void *q, *k, *v;
+    const float *log_alpha, *beta, *h0;
+    void *o;
+    float *hT;
+    SeqMap sm;
+    int dk, dv;
+    gdn_dtype dt;
+    long long rows;       // rows of the [rows][d] views
+    int max_chunks;       // upper bound on chunks of one sequence
+    int chunk_slots;      // upper bound on chunks of all sequences
+    cudaStream_t stream;
+};
+
+// device error word helpers (defined in gdn_api.cu)
+int *device_error_word();
+// dominant-kernel timer: returns a slot (or -1 when timing is off)
+int timer_begin(cudaStream_t st, const char *kernel);
+void timer_end(int slot, cudaStream_t st);
+void count_launch(int n = 1);
+long long option(int key);
+
+// SIMT (CUDA-core, fp32 arithmetic) path: every supported shape and dtype.
+gdn_status simt_forward(const FwdArgs &a);
+
+// tcgen05 tensor-core path (bf16 I/O).  Returns GDN_ERR_UNSUPPORTED when the
+// call does not fit it; the caller then decides whether to fall back.
+bool tc_supported(const FwdArgs &a);
+gdn_status tc_forward(const FwdArgs &a);
+
+}  // namespace gdn

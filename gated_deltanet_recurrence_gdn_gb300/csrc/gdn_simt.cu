@@ -1,0 +1,357 @@
+// gdn_simt.cu -- chunked gated delta rule on CUDA cores, fp32 arithmetic.
+//
+// This is the path for fp32 I/O and for shapes the tensor-core kernels do not
+// cover.  It follows the chunked method of "Gated DeltaNet GPU并行实现"
+// section 3.2: inside a chunk everything is a small dense product, across
+// chunks a serial pass carries the state.  Two kernels:
+//
+//   prep  (one CTA per (chunk, head), all chunks in parallel):
+//         g_r   = sum_{i<=r} log_alpha_i inside the chunk        (gate cumsum)
+//         A_rs  = beta_r exp(g_r - g_s) (k_r . k_s),  s < r        (decayed Gram)
+//         T     = (I + A)^{-1}  by column-wise forward substitution
+//         W     = T diag(beta exp(g)) K,   U = T diag(beta) V       (WY factors)
+//   state (one CTA per (sequence, head, 32-wide d_v tile), chunks in order):
+//         with H = S^T (d_k x d_v) at the chunk start,
+//         V'    = U - W H
+//         O     = diag(exp(g)) Q H + [mask_{s<=r} exp(g_r - g_s) Q K^T] V'
+//         H    <- exp(g_C) H + K^T diag(exp(g_C - g_r)) V'
+//
+// Derivation (the affine form of section 2.2 unrolled over one chunk): with
+// u_r = beta_r (v_r - alpha_r S_{r-1} k_r) the update is S_r = alpha_r S_{r-1}
+// + u_r k_r^T, so S_r = gamma_r S_0 + sum_{s<=r} (gamma_r/gamma_s) u_s k_s^T
+// (gamma = exp(g)).  Substituting into u_r gives (I + A) U' = diag(beta) V -
+// diag(beta gamma) K S_0^T, i.e. U' = U - W S_0^T; the chunk-end state and the
+// outputs follow by summing the same expansion.
+//
+// Rows past the end of a sequence are padding with k = v = q = 0, beta = 0
+// and log_alpha = 0, which leaves every real row unchanged.
+#include <cuda_bf16.h>
+
+#include "gdn_internal.h"
+
+namespace gdn {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kDvt = 32;  // d_v columns per state-pass CTA
+
+__device__ __forceinline__ float ld_in(const float *p) { return __ldg(p); }
+__device__ __forceinline__ float ld_in(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
+__device__ __forceinline__ void st_out(float *p, float x) { *p = x; }
+__device__ __forceinline__ void st_out(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
+
+__device__ __forceinline__ void set_error(int *err, int code) { atomicCAS(err, 0, code); }
+
+// Validates one packed sequence's range; dense maps are valid by construction.
+__device__ __forceinline__ bool seq_ok(const SeqMap &sm, int n) {
+    if (!sm.cu) return true;
+    int a = __ldg(sm.cu + n), b = __ldg(sm.cu + n + 1);
+    return a >= 0 && a <= b && b <= sm.T_total;
+}
+
+// One block lists every (sequence, chunk) pair of a packed batch; unused
+// slots get n = -1.  Also validates cu_seqlens.
+__global__ void k_chunk_table(const int32_t *cu, int N, int T_total, int2 *table, int slots,
+                              int *err) {
+    __shared__ int s_scan[1024];
+    __shared__ int s_base;
+    __shared__ int s_bad;
+    const int tid = threadIdx.x;
+    if (tid == 0) {
+        s_base = 0;
+        s_bad = (__ldg(cu) != 0 || __ldg(cu + N) != T_total) ? 1 : 0;
+    }
+    __syncthreads();
+    for (int base = 0; base < N; base += 1024) {
+        const int n = base + tid;
+        int cnt = 0;
+        if (n < N) {
+            int a = __ldg(cu + n), b = __ldg(cu + n + 1);
+            if (b < a || a < 0 || b > T_total) atomicExch(&s_bad, 1);
+            else cnt = (b - a + kChunk - 1) / kChunk;
+        }
+        s_scan[tid] = cnt;
+        __syncthreads();
+        for (int off = 1; off < 1024; off <<= 1) {  // inclusive Hillis-Steele scan
+            int x = tid >= off ? s_scan[tid - off] : 0;
+            __syncthreads();
+            s_scan[tid] += x;
+            __syncthreads();
+        }
+        const int start = s_base + s_scan[tid] - cnt;
+        for (int c = 0; c < cnt; ++c)
+            if (start + c < slots) table[start + c] = make_int2(n, c);
+        __syncthreads();
+        if (tid == 1023) s_base += s_scan[1023];
+        __syncthreads();
+    }
+    const int used = s_bad ? 0 : min(s_base, slots);
+    for (int i = used + tid; i < slots; i += 1024) table[i] = make_int2(-1, -1);
+    if (tid == 0 && s_bad) set_error(err, kErrSeqlens);
+}
+
+template <typename TIn>
+__global__ void __launch_bounds__(kThreads)
+k_simt_prep(FwdArgs a, const int2 *__restrict__ table, float *__restrict__ W,
+            float *__restrict__ U, float *__restrict__ G, int *err) {
+    extern __shared__ float smem[];
+    const int dk = a.dk, dv = a.dv, tid = threadIdx.x;
+    int n, c;
+    if (table) {
+        int2 e = table[blockIdx.x];
+        n = e.x;
+        c = e.y;
+        if (n < 0) return;
+    } else {
+        n = blockIdx.x / a.max_chunks;
+        c = blockIdx.x % a.max_chunks;
+    }
+    const int h = blockIdx.y;
+    if (!seq_ok(a.sm, n)) {
+        if (tid == 0) set_error(err, kErrSeqlens);
+        return;
+    }
+    long long row0;
+    int len;
+    a.sm.get(n, h, row0, len);
+    const int t0 = c * kChunk;
+    if (t0 >= len) return;
+    const int L = min(kChunk, len - t0);
+    const long long r0 = row0 + t0;
+    const int ks = dk + 1, vs = dv + 1;
+    float *Ks = smem;                 // [64][dk+1]
+    float *Vs = Ks + kChunk * ks;     // [64][dv+1]
+    float *A = Vs + kChunk * vs;      // [64][65]
+    float *Tm = A + kChunk * 65;      // [64][65]
+    float *g = Tm + kChunk * 65;      // [64] gate cumsum
+    float *bb = g + kChunk;           // [64] beta
+    float *wb = bb + kChunk;          // [64] beta * exp(g)
+    const TIn *kp = static_cast<const TIn *>(a.k);
+    const TIn *vp = static_cast<const TIn *>(a.v);
+
+    if (tid < kChunk) {
+        const bool ok = tid < L;
+        g[tid] = ok ? __ldg(a.log_alpha + r0 + tid) : 0.f;
+        bb[tid] = ok ? __ldg(a.beta + r0 + tid) : 0.f;
+    }
+    for (int i = tid; i < kChunk * dk; i += kThreads) {
+        const int r = i / dk, j = i - r * dk;
+        Ks[r * ks + j] = r < L ? ld_in(kp + (r0 + r) * dk + j) : 0.f;
+    }
+    for (int i = tid; i < kChunk * dv; i += kThreads) {
+        const int r = i / dv, j = i - r * dv;
+        Vs[r * vs + j] = r < L ? ld_in(vp + (r0 + r) * dv + j) : 0.f;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        float s = 0.f;
+        for (int r = 0; r < kChunk; ++r) {
+            s += g[r];
+            g[r] = s;
+        }
+    }
+    __syncthreads();
+    for (int i = tid; i < kChunk * kChunk; i += kThreads) {
+        const int r = i >> 6, s = i & 63;
+        float val = 0.f;
+        if (s < r) {
+            float acc = 0.f;
+            for (int j = 0; j < dk; ++j) acc = fmaf(Ks[r * ks + j], Ks[s * ks + j], acc);
+            val = bb[r] * expf(g[r] - g[s]) * acc;  // s < r: g_r <= g_s, no overflow
+        }
+        A[r * 65 + s] = val;
+    }
+    if (tid < kChunk) wb[tid] = bb[tid] * expf(g[tid]);
+    __syncthreads();
+    if (tid < kChunk) {  // column tid of T = (I + A)^{-1}
+        const int cc = tid;
+        for (int r = 0; r <= cc; ++r) Tm[r * 65 + cc] = (r == cc) ? 1.f : 0.f;
+        for (int r = cc + 1; r < kChunk; ++r) {
+            float acc = 0.f;
+            for (int s = cc; s < r; ++s) acc = fmaf(A[r * 65 + s], Tm[s * 65 + cc], acc);
+            Tm[r * 65 + cc] = -acc;
+        }
+    }
+    __syncthreads();
+    for (int i = tid; i < L * dk; i += kThreads) {
+        const int r = i / dk, j = i - r * dk;
+        float acc = 0.f;
+        for (int s = 0; s <= r; ++s) acc = fmaf(Tm[r * 65 + s] * wb[s], Ks[s * ks + j], acc);
+        W[(r0 + r) * dk + j] = acc;
+    }
+    for (int i = tid; i < L * dv; i += kThreads) {
+        const int r = i / dv, j = i - r * dv;
+        float acc = 0.f;
+        for (int s = 0; s <= r; ++s) acc = fmaf(Tm[r * 65 + s] * bb[s], Vs[s * vs + j], acc);
+        U[(r0 + r) * dv + j] = acc;
+    }
+    if (tid < L) G[r0 + tid] = g[tid];
+}
+
+template <typename TIn>
+__global__ void __launch_bounds__(kThreads)
+k_simt_state(FwdArgs a, const float *__restrict__ W, const float *__restrict__ U,
+             const float *__restrict__ G, int *err) {
+    extern __shared__ float smem[];
+    const int dk = a.dk, dv = a.dv, tid = threadIdx.x;
+    const int n = blockIdx.x, h = blockIdx.y, dv0 = blockIdx.z * kDvt;
+    const int nv = min(kDvt, dv - dv0);
+    if (!seq_ok(a.sm, n)) {
+        if (tid == 0) set_error(err, kErrSeqlens);
+        return;
+    }
+    long long row0;
+    int len;
+    a.sm.get(n, h, row0, len);
+    const int ks = dk + 1, us = kDvt + 1;
+    float *Hs = smem;                    // [dk][32]   H = S^T tile
+    float *Ks = Hs + dk * kDvt;          // [64][dk+1]
+    float *Qs = Ks + kChunk * ks;        // [64][dk+1]
+    float *Ws = Qs + kChunk * ks;        // [64][dk+1]
+    float *Us = Ws + kChunk * ks;        // [64][33]
+    float *Vn = Us + kChunk * us;        // [64][33]
+    float *P = Vn + kChunk * us;         // [64][65]
+    float *g = P + kChunk * 65;          // [64]
+    float *e = g + kChunk;               // [64] exp(g_C - g_r)
+    const TIn *qp = static_cast<const TIn *>(a.q);
+    const TIn *kp = static_cast<const TIn *>(a.k);
+    TIn *op = static_cast<TIn *>(a.o);
+    const long long sbase = ((long long)n * a.sm.H + h) * dv;  // state row of (n, h)
+
+    for (int i = tid; i < dk * kDvt; i += kThreads) {
+        const int j = i / kDvt, cc = i - j * kDvt;
+        Hs[i] = (a.h0 && cc < nv) ? __ldg(a.h0 + (sbase + dv0 + cc) * dk + j) : 0.f;
+    }
+    const int nch = (len + kChunk - 1) / kChunk;
+    for (int c = 0; c < nch; ++c) {
+        const int t0 = c * kChunk, L = min(kChunk, len - t0);
+        const long long r0 = row0 + t0;
+        __syncthreads();  // previous chunk fully consumed
+        for (int i = tid; i < kChunk * dk; i += kThreads) {
+            const int r = i / dk, j = i - r * dk;
+            const bool ok = r < L;
+            Ks[r * ks + j] = ok ? ld_in(kp + (r0 + r) * dk + j) : 0.f;
+            Qs[r * ks + j] = ok ? ld_in(qp + (r0 + r) * dk + j) : 0.f;
+            Ws[r * ks + j] = ok ? __ldg(W + (r0 + r) * dk + j) : 0.f;
+        }
+        for (int i = tid; i < kChunk * kDvt; i += kThreads) {
+            const int r = i / kDvt, cc = i - r * kDvt;
+            Us[r * us + cc] = (r < L && cc < nv) ? __ldg(U + (r0 + r) * dv + dv0 + cc) : 0.f;
+        }
+        if (tid < kChunk) g[tid] = __ldg(G + r0 + min(tid, L - 1));
+        __syncthreads();
+        const float gl = g[kChunk - 1];
+        if (tid < kChunk) e[tid] = expf(gl - g[tid]);
+        for (int i = tid; i < kChunk * kChunk; i += kThreads) {
+            const int r = i >> 6, s = i & 63;
+            float val = 0.f;
+            if (s <= r) {
+                float acc = 0.f;
+                for (int j = 0; j < dk; ++j) acc = fmaf(Qs[r * ks + j], Ks[s * ks + j], acc);
+                val = expf(g[r] - g[s]) * acc;
+            }
+            P[r * 65 + s] = val;
+        }
+        for (int i = tid; i < kChunk * kDvt; i += kThreads) {
+            const int r = i / kDvt, cc = i - r * kDvt;
+            float acc = Us[r * us + cc];
+            for (int j = 0; j < dk; ++j) acc = fmaf(-Ws[r * ks + j], Hs[j * kDvt + cc], acc);
+            Vn[r * us + cc] = acc;
+        }
+        __syncthreads();
+        for (int i = tid; i < kChunk * kDvt; i += kThreads) {
+            const int r = i / kDvt, cc = i - r * kDvt;
+            if (r < L && cc < nv) {
+                float a1 = 0.f, a2 = 0.f;
+                for (int j = 0; j < dk; ++j) a1 = fmaf(Qs[r * ks + j], Hs[j * kDvt + cc], a1);
+                for (int s = 0; s <= r; ++s) a2 = fmaf(P[r * 65 + s], Vn[s * us + cc], a2);
+                st_out(op + (r0 + r) * dv + dv0 + cc, expf(g[r]) * a1 + a2);
+            }
+        }
+        __syncthreads();  // every read of H for this chunk is done
+        const float decay = expf(gl);
+        for (int i = tid; i < dk * kDvt; i += kThreads) {
+            const int j = i / kDvt, cc = i - j * kDvt;
+            float acc = 0.f;
+            for (int s = 0; s < kChunk; ++s) acc = fmaf(Ks[s * ks + j] * e[s], Vn[s * us + cc], acc);
+            Hs[i] = fmaf(decay, Hs[i], acc);
+        }
+    }
+    __syncthreads();
+    if (a.hT) {
+        for (int i = tid; i < dk * kDvt; i += kThreads) {
+            const int j = i / kDvt, cc = i - j * kDvt;
+            if (cc < nv) a.hT[(sbase + dv0 + cc) * dk + j] = Hs[i];
+        }
+    }
+}
+
+size_t prep_smem(int dk, int dv) {
+    return sizeof(float) * ((size_t)kChunk * (dk + 1) + (size_t)kChunk * (dv + 1) +
+                            2 * kChunk * 65 + 3 * kChunk);
+}
+size_t state_smem(int dk) {
+    return sizeof(float) * ((size_t)dk * kDvt + 3 * (size_t)kChunk * (dk + 1) +
+                            2 * kChunk * (kDvt + 1) + kChunk * 65 + 2 * kChunk);
+}
+
+template <typename TIn>
+gdn_status launch(const FwdArgs &a) {
+    int *err = device_error_word();
+    cudaStream_t st = a.stream;
+    const size_t psm = prep_smem(a.dk, a.dv), ssm = state_smem(a.dk);
+    if (cudaFuncSetAttribute(k_simt_prep<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)psm) != cudaSuccess ||
+        cudaFuncSetAttribute(k_simt_state<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)ssm) != cudaSuccess)
+        return GDN_ERR_CUDA;
+    float *W = nullptr, *U = nullptr, *G = nullptr;
+    int2 *table = nullptr;
+    const size_t rows = (size_t)a.rows > 0 ? (size_t)a.rows : 1;
+    if (cudaMallocAsync((void **)&W, rows * a.dk * sizeof(float), st) != cudaSuccess ||
+        cudaMallocAsync((void **)&U, rows * a.dv * sizeof(float), st) != cudaSuccess ||
+        cudaMallocAsync((void **)&G, rows * sizeof(float), st) != cudaSuccess) {
+        if (W) cudaFreeAsync(W, st);
+        if (U) cudaFreeAsync(U, st);
+        return GDN_ERR_CUDA;
+    }
+    gdn_status rc = GDN_OK;
+    if (a.chunk_slots > 0) {
+        if (a.sm.cu) {
+            if (cudaMallocAsync((void **)&table, sizeof(int2) * (size_t)a.chunk_slots, st) !=
+                cudaSuccess) {
+                rc = GDN_ERR_CUDA;
+            } else {
+                k_chunk_table<<<1, 1024, 0, st>>>(a.sm.cu, a.sm.N, a.sm.T_total, table,
+                                                 a.chunk_slots, err);
+                count_launch();
+            }
+        }
+        if (rc == GDN_OK) {
+            dim3 grid(a.chunk_slots, a.sm.H);
+            k_simt_prep<TIn><<<grid, kThreads, psm, st>>>(a, table, W, U, G, err);
+            count_launch();
+        }
+    }
+    if (rc == GDN_OK && a.sm.N > 0 && a.sm.H > 0) {
+        dim3 grid(a.sm.N, a.sm.H, (a.dv + kDvt - 1) / kDvt);
+        const int slot = timer_begin(st, "k_simt_state");
+        k_simt_state<TIn><<<grid, kThreads, ssm, st>>>(a, W, U, G, err);
+        timer_end(slot, st);
+        count_launch();
+    }
+    if (rc == GDN_OK && cudaGetLastError() != cudaSuccess) rc = GDN_ERR_CUDA;
+    cudaFreeAsync(W, st);
+    cudaFreeAsync(U, st);
+    cudaFreeAsync(G, st);
+    if (table) cudaFreeAsync(table, st);
+    return rc;
+}
+
+}  // namespace
+
+gdn_status simt_forward(const FwdArgs &a) {
+    return a.dt == GDN_F32 ? launch<float>(a) : launch<__nv_bfloat16>(a);
+}
+
+}  // namespace gdn

@@ -1,0 +1,143 @@
+/*
+ * gdn.h -- C ABI of the GB300 (sm_103a) gated delta rule forward library
+ * (libgdn.so).
+ *
+ * The operation ("Gated DeltaNet GPU并行实现", sections 2.1-2.2): for every
+ * (sequence, head) a state S of shape d_v x d_k evolves over tokens as
+ *
+ *     S_t = alpha_t * S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,
+ *     o_t = S_t q_t,            alpha_t = exp(log_alpha_t),
+ *
+ * starting from h0 (or zero) and ending in hT.  The library computes it in the
+ * chunked form of section 3.2 (chunks of `chunk` tokens: matrix products inside
+ * a chunk, a serial state pass across chunks), with the dual-parallel
+ * segment scan of section 3.3 over the affine maps of section 2.3 when there
+ * are too few independent (sequence, head) problems to fill the GPU.
+ *
+ * Layouts (all row-major, innermost dimension contiguous, section 4.1):
+ *   dense:  q, k [B][H][T][d_k]; v, o [B][H][T][d_v];
+ *           log_alpha, beta [B][H][T] (fp32); h0, hT [B][H][d_v][d_k] (fp32).
+ *   packed: q, k [H][T_total][d_k]; v, o [H][T_total][d_v];
+ *           log_alpha, beta [H][T_total] (fp32); h0, hT [N][H][d_v][d_k] (fp32);
+ *           sequence n occupies tokens [cu_seqlens[n], cu_seqlens[n+1]).
+ *   hT[.., i, j] is S_{i j}: i indexes d_v, j indexes d_k.
+ *
+ * Ownership: every pointer argument is a DEVICE pointer owned by the caller;
+ * the library keeps no reference after the call returns.  Scratch memory is
+ * taken from the stream-ordered allocator (cudaMallocAsync / cudaFreeAsync
+ * on `stream`).  All work is enqueued on `stream` (a cudaStream_t; NULL is
+ * the legacy default stream); calls return before the GPU finishes.
+ *
+ * Errors: arguments are checked synchronously and a non-GDN_OK status is
+ * returned before anything is enqueued.  Pointers must be 16-byte aligned
+ * (section 5.2, second pitfall: misaligned or non-contiguous inputs break
+ * bulk tensor copies), otherwise GDN_ERR_ALIGNMENT.  A failed launch returns
+ * GDN_ERR_CUDA.  Errors found by the kernels while running (a bounded wait
+ * that gave up, an invalid cu_seqlens entry) are recorded in a device error
+ * word and reported by gdn_sync_check().  Values are not checked for NaN.
+ * There is no CPU fallback.
+ */
+#ifndef GDN_H
+#define GDN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GDN_OK = 0,
+    GDN_ERR_INVALID_ARG = 1,    /* NULL pointer, bad size, bad cu_seqlens */
+    GDN_ERR_UNSUPPORTED = 2,    /* chunk != 64, d_k / d_v outside the supported set */
+    GDN_ERR_ALIGNMENT = 3,      /* a pointer is not 16-byte aligned */
+    GDN_ERR_CUDA = 4,           /* a CUDA runtime call or launch failed */
+    GDN_ERR_DEVICE_TIMEOUT = 5  /* a bounded device-side wait gave up */
+} gdn_status;
+
+typedef enum {
+    GDN_F32 = 0,   /* q, k, v, o are fp32 */
+    GDN_BF16 = 1   /* q, k, v, o are bf16 */
+} gdn_dtype;
+
+/*
+ * Dense forward pass.  See the layouts above.
+ *   q, k, v     inputs of `dt`; log_alpha, beta fp32 gates (alpha = exp(log_alpha)).
+ *   h0          initial state or NULL (= zero state).
+ *   o           output of `dt`, [B][H][T][d_v].
+ *   hT          final state or NULL (= not written).
+ *   B, H, T     batch, heads, tokens per sequence (T = 0 gives hT = h0).
+ *   d_k, d_v    key and value widths: multiples of 8 with 8 <= d_k <= 128 and
+ *               8 <= d_v <= 256.
+ *   chunk       chunk length; only 64 is supported (GDN_ERR_UNSUPPORTED else).
+ *   stream      cudaStream_t to enqueue on.
+ */
+gdn_status gdn_fwd(const void *q, const void *k, const void *v,
+                   const float *log_alpha, const float *beta, const float *h0,
+                   void *o, float *hT,
+                   int B, int H, int T, int d_k, int d_v, int chunk,
+                   gdn_dtype dt, void *stream);
+
+/*
+ * Packed variable-length forward pass.  cu_seqlens is a DEVICE int32 array of
+ * N+1 non-decreasing offsets with cu_seqlens[0] = 0 and cu_seqlens[N] =
+ * T_total (checked on the device; a violation is reported by
+ * gdn_sync_check() as GDN_ERR_INVALID_ARG and leaves o / hT unspecified).
+ * Sequences never interact; each starts from its own h0[n] (or zero).
+ */
+gdn_status gdn_fwd_varlen(const void *q, const void *k, const void *v,
+                          const float *log_alpha, const float *beta, const float *h0,
+                          void *o, float *hT, const int32_t *cu_seqlens,
+                          int N, int H, int T_total, int d_k, int d_v, int chunk,
+                          gdn_dtype dt, void *stream);
+
+/* Static, human-readable name of a status. */
+const char *gdn_status_string(gdn_status s);
+
+/*
+ * Synchronises `stream`, then reads and clears the device error word of the
+ * current device.  Returns GDN_OK, GDN_ERR_DEVICE_TIMEOUT, GDN_ERR_INVALID_ARG
+ * (bad cu_seqlens seen by a kernel) or GDN_ERR_CUDA.
+ */
+gdn_status gdn_sync_check(void *stream);
+
+/*
+ * Implementation selection (process-wide; for tests and benchmarks).
+ *   GDN_OPT_IMPL:      GDN_IMPL_AUTO (default), GDN_IMPL_SIMT (fp32 CUDA-core
+ *                      kernels, every supported shape), GDN_IMPL_TC (tcgen05
+ *                      tensor-core kernels; GDN_ERR_UNSUPPORTED when the call
+ *                      does not fit them).
+ *   GDN_OPT_SEGMENTS:  0 = automatic; s > 0 forces s sequence segments per
+ *                      (sequence, head) in the tensor-core path's segment scan;
+ *                      1 disables the scan.
+ *   GDN_OPT_WAIT_LIMIT: iteration cap of device-side bounded waits (0 = default).
+ * Returns GDN_ERR_INVALID_ARG for an unknown key or value.
+ */
+enum { GDN_OPT_IMPL = 0, GDN_OPT_SEGMENTS = 1, GDN_OPT_WAIT_LIMIT = 2 };
+enum { GDN_IMPL_AUTO = 0, GDN_IMPL_SIMT = 1, GDN_IMPL_TC = 2 };
+gdn_status gdn_set_option(int key, long long value);
+long long gdn_get_option(int key);
+
+/*
+ * Live timing of the dominant kernel, for benchmarks.  While enabled, every
+ * forward call records a pair of CUDA events around the launch of its most
+ * expensive kernel, on the call's stream.  gdn_kernel_timer_read() waits for
+ * those events, returns the summed duration in milliseconds, the number of
+ * timed launches and the kernel's name (a static string), and clears the
+ * record.  Not thread-safe; meant for one benchmarking thread.
+ */
+gdn_status gdn_kernel_timer(int enable);
+gdn_status gdn_kernel_timer_read(double *total_ms, long long *launches, const char **kernel);
+
+/* Number of kernels this library has launched since it was loaded. */
+uint64_t gdn_kernel_launches(void);
+
+/* Implementation the last successful gdn_fwd / gdn_fwd_varlen call used
+ * (GDN_IMPL_SIMT or GDN_IMPL_TC), 0 before the first call. */
+int gdn_last_impl(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H */

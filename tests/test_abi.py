@@ -1,0 +1,91 @@
+"""The C-ABI library loads and exports every function include/gdn.h declares,
+and its host-side argument checks answer without touching a GPU (CPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import gated_deltanet_recurrence_gdn_gb300 as gdn
+from gated_deltanet_recurrence_gdn_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return gdn.load()
+
+
+def declared_functions():
+    names = set()
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if h.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", h)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(gdn_[a-z0-9_]+)\s*\(", src))
+    return sorted(names)
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ("gdn_fwd", "gdn_fwd_varlen", "gdn_status_string", "gdn_sync_check"):
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    # and the binding declares a prototype for each of them
+    bound = {n for n, _, _ in gdn.ABI}
+    assert set(declared_functions()) <= bound
+
+
+def test_status_strings(lib):
+    for s in range(6):
+        assert lib.gdn_status_string(s).decode().startswith("GDN_")
+    assert lib.gdn_status_string(99) == b"unknown gdn_status"
+
+
+def test_options_roundtrip(lib):
+    assert lib.gdn_set_option(gdn.GDN_OPT_IMPL, gdn.GDN_IMPL_SIMT) == gdn.GDN_OK
+    assert lib.gdn_get_option(gdn.GDN_OPT_IMPL) == gdn.GDN_IMPL_SIMT
+    assert lib.gdn_set_option(gdn.GDN_OPT_IMPL, 9) == gdn.GDN_ERR_INVALID_ARG
+    assert lib.gdn_set_option(77, 0) == gdn.GDN_ERR_INVALID_ARG
+    assert lib.gdn_set_option(gdn.GDN_OPT_IMPL, gdn.GDN_IMPL_AUTO) == gdn.GDN_OK
+
+
+# Host-only validation: these calls must return before any CUDA call, so fake
+# (never dereferenced) device addresses are fine.
+FAKE = 0x10000
+
+
+def _args(off=0):
+    return [FAKE + off, FAKE, FAKE, FAKE, FAKE, None, FAKE, None]
+
+
+def test_host_checks(lib):
+    f = lib.gdn_fwd
+    assert f(*_args(), 1, 1, 64, 64, 64, 128, 1, None) == gdn.GDN_ERR_UNSUPPORTED  # chunk
+    assert f(*_args(), 1, 1, 64, 60, 64, 64, 1, None) == gdn.GDN_ERR_UNSUPPORTED   # d_k % 8
+    assert f(*_args(), 1, 1, 64, 256, 64, 64, 1, None) == gdn.GDN_ERR_UNSUPPORTED  # d_k > 128
+    assert f(*_args(), 1, 1, 64, 64, 512, 64, 1, None) == gdn.GDN_ERR_UNSUPPORTED  # d_v > 256
+    assert f(*_args(8), 1, 1, 64, 64, 64, 64, 1, None) == gdn.GDN_ERR_ALIGNMENT
+    assert f(*_args(), -1, 1, 64, 64, 64, 64, 1, None) == gdn.GDN_ERR_INVALID_ARG
+    assert f(*_args(), 1, 1, 64, 64, 64, 64, 3, None) == gdn.GDN_ERR_INVALID_ARG   # dtype
+    nul = _args()
+    nul[2] = None
+    assert f(*nul, 1, 1, 64, 64, 64, 64, 1, None) == gdn.GDN_ERR_INVALID_ARG
+    # nothing to do: zero heads / zero batch returns OK without launching
+    assert f(*_args(), 0, 4, 64, 64, 64, 64, 1, None) == gdn.GDN_OK
+    assert f(*_args(), 2, 0, 64, 64, 64, 64, 1, None) == gdn.GDN_OK
+    g = lib.gdn_fwd_varlen
+    assert g(*_args(), None, 2, 1, 10, 64, 64, 64, 1, None) == gdn.GDN_ERR_INVALID_ARG
+    assert g(*_args(), FAKE, 0, 1, 10, 64, 64, 64, 1, None) == gdn.GDN_ERR_INVALID_ARG
+    assert g(*_args(), FAKE, 0, 1, 0, 64, 64, 64, 1, None) == gdn.GDN_OK
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    with pytest.raises(ImportError):
+        gdn.load(str(tmp_path / "missing.so"))

@@ -1,0 +1,240 @@
+"""CUDA path vs the fp64 oracle, element by element, on the same seeded inputs.
+
+Small cases span several 64-token chunks and a ragged tail; the workload
+cases run at full size in the launch configuration the benchmark times and
+compare either every output (when the oracle finishes in seconds) or a
+sampled subset of heads / sequences / a causal prefix.
+"""
+import numpy as np
+import pytest
+import torch
+
+import gated_deltanet_recurrence_gdn_gb300 as gdn
+import synth
+from tests import gpu_util as U
+
+pytestmark = pytest.mark.gpu
+
+IMPLS = {"simt": gdn.GDN_IMPL_SIMT, "tc": gdn.GDN_IMPL_TC, "auto": gdn.GDN_IMPL_AUTO}
+
+
+def run_dense(x, impl, **kw):
+    with gdn.use_impl(IMPLS[impl], kw.pop("segments", None)):
+        try:
+            o, hT = gdn.gdn_fwd(x.q, x.k, x.v, x.log_alpha, x.beta, x.h0, check=True, **kw)
+        except gdn.GdnError as e:
+            if e.status == gdn.GDN_ERR_UNSUPPORTED and impl == "tc":
+                pytest.skip("shape not covered by the tensor-core path")
+            raise
+        used = gdn.last_impl()
+    if impl != "auto":
+        assert used == IMPLS[impl]
+    U.sync()
+    return o, hT
+
+
+def run_varlen(y, impl, **kw):
+    with gdn.use_impl(IMPLS[impl], kw.pop("segments", None)):
+        try:
+            o, hT = gdn.gdn_fwd_varlen(y.q, y.k, y.v, y.log_alpha, y.beta, y.cu_seqlens, y.h0,
+                                       check=True, **kw)
+        except gdn.GdnError as e:
+            if e.status == gdn.GDN_ERR_UNSUPPORTED and impl == "tc":
+                pytest.skip("shape not covered by the tensor-core path")
+            raise
+    U.sync()
+    return o, hT
+
+
+def check(o, hT, o_ref, h_ref, io):
+    to, th = U.TOL[io]
+    eo, eh = U.rel(U.f64(o), o_ref), U.rel(U.f64(hT), h_ref)
+    assert eo <= to and eh <= th, (eo, eh)
+    assert np.isfinite(U.f64(o)).all()
+    return eo, eh
+
+
+DENSE_CASES = [
+    # B, H, T, dk, dv, io, h0_std, decay
+    (1, 1, 1, 64, 64, "f32", 0.02, "fast"),
+    (2, 3, 63, 64, 64, "bf16", 0.02, "fast"),
+    (2, 2, 64, 128, 128, "bf16", 0.0, "fast"),
+    (1, 3, 65, 128, 128, "bf16", 0.5, "slow"),
+    (2, 2, 3 * 64 + 17, 128, 128, "bf16", 0.02, "fast"),
+    (2, 2, 3 * 64 + 17, 128, 128, "f32", 0.02, "fast"),
+    (1, 2, 5 * 64 + 3, 64, 64, "bf16", 0.02, "slow"),
+    (1, 2, 2 * 64 + 40, 128, 256, "bf16", 0.02, "fast"),
+    (1, 2, 2 * 64 + 40, 64, 128, "bf16", 0.0, "fast"),
+    (1, 1, 130, 32, 48, "f32", 0.1, "fast"),
+    (1, 2, 4 * 64, 128, 64, "bf16", 0.02, "none"),
+]
+
+
+@pytest.mark.parametrize("impl", ["simt", "tc"])
+@pytest.mark.parametrize("case", DENSE_CASES, ids=lambda c: "b%dh%dt%d_k%dv%d_%s_%s" % (
+    c[0], c[1], c[2], c[3], c[4], c[5], c[7]))
+def test_dense_small(impl, case):
+    B, H, T, dk, dv, io, h0s, decay = case
+    x = synth.make_dense(B, H, T, dk, dv, io=io, h0_std=h0s, decay=decay, seed=100 + T,
+                         device="cuda")
+    o, hT = run_dense(x, impl)
+    o_ref, h_ref = U.oracle_dense(x)
+    check(o, hT, o_ref.reshape(o.shape), h_ref.reshape(hT.shape), io)
+
+
+VARLEN_CASES = [
+    ([70, 0, 5, 130, 64], 2, 64, 64, "f32"),
+    ([1, 63, 64, 65, 200, 0], 3, 128, 128, "bf16"),
+    ([300, 17, 128], 2, 128, 256, "bf16"),
+    ([0, 0], 1, 64, 64, "bf16"),
+]
+
+
+@pytest.mark.parametrize("impl", ["simt", "tc"])
+@pytest.mark.parametrize("case", VARLEN_CASES, ids=lambda c: "n%d_k%dv%d_%s" % (
+    len(c[0]), c[2], c[3], c[4]))
+def test_varlen_small(impl, case):
+    lens, H, dk, dv, io = case
+    y = synth.make_varlen(lens, H, dk, dv, io=io, h0_std=0.02, seed=200 + len(lens),
+                          device="cuda")
+    o, hT = run_varlen(y, impl)
+    import oracle
+    o_ref, h_ref = oracle.gdn_fwd_varlen(U.f64(y.q), U.f64(y.k), U.f64(y.v),
+                                         U.f64(y.log_alpha), U.f64(y.beta),
+                                         y.cu_seqlens.cpu().numpy(), U.f64(y.h0))
+    check(o, hT, o_ref, h_ref, io)
+
+
+@pytest.mark.parametrize("impl", ["simt", "tc"])
+def test_varlen_equals_dense(impl):
+    # equal lengths: the packed call must reproduce the dense call bit for bit
+    # up to the different memory layout
+    B, H, T, dk, dv = 3, 2, 150, 128, 128
+    x = synth.make_dense(B, H, T, dk, dv, io="bf16", h0_std=0.02, seed=5, device="cuda")
+    od, hd = run_dense(x, impl)
+    pack = lambda t: t.permute(1, 0, 2, 3).reshape(H, B * T, t.shape[-1]).contiguous()  # noqa
+    packg = lambda t: t.permute(1, 0, 2).reshape(H, B * T).contiguous()  # noqa
+    cu = torch.arange(0, B * T + 1, T, dtype=torch.int32, device="cuda")
+    y = synth.Inputs(pack(x.q), pack(x.k), pack(x.v), packg(x.log_alpha), packg(x.beta), x.h0,
+                     cu)
+    ov, hv = run_varlen(y, impl)
+    assert torch.equal(ov, pack(od)) and torch.equal(hv, hd)
+
+
+@pytest.mark.parametrize("impl", ["simt", "tc"])
+def test_continuation(impl):
+    B, H, T1, T2, dk, dv = 1, 4, 192, 137, 128, 128
+    x = synth.make_dense(B, H, T1 + T2, dk, dv, io="bf16", h0_std=0.02, seed=9, device="cuda")
+    o, hT = run_dense(x, impl)
+    s1, s2 = np.s_[:, :, :T1], np.s_[:, :, T1:]
+    part = lambda s, h0: synth.Inputs(*(t[s].contiguous() for t in (x.q, x.k, x.v,  # noqa
+                                                                  x.log_alpha, x.beta)), h0)
+    o1, h1 = run_dense(part(s1, x.h0), impl)
+    o2, h2 = run_dense(part(s2, h1), impl)
+    o12 = torch.cat([o1, o2], dim=2)
+    assert U.rel(U.f64(o12), U.f64(o)) <= 1e-2
+    assert U.rel(U.f64(h2), U.f64(hT)) <= 2e-2
+
+
+@pytest.mark.parametrize("impl", ["simt", "tc"])
+def test_empty_sequence_gives_h0(impl):
+    x = synth.make_dense(2, 3, 0, 64, 64, io="bf16", h0_std=0.3, seed=1, device="cuda")
+    o, hT = run_dense(x, impl)
+    assert o.numel() == 0 and torch.equal(hT, x.h0)
+
+
+# ----------------------------------------------------------------- workloads
+
+
+def test_workload_fp32_small_full():
+    x = synth.make_workload("gdn_fwd_b1_h1_t256_d64_fp32", device="cuda")
+    o, hT = run_dense(x, "auto")
+    o_ref, h_ref = U.oracle_dense(x)
+    check(o, hT, o_ref.reshape(o.shape), h_ref.reshape(hT.shape), "f32")
+
+
+@pytest.mark.parametrize("impl", ["auto", "simt"])
+def test_workload_b4_h16_t4096_d128_full(impl):
+    x = synth.make_workload("gdn_fwd_b4_h16_t4096_d128_bf16", device="cuda")
+    o, hT = run_dense(x, impl)
+    o_ref, h_ref = U.oracle_dense(x)           # every head, every token
+    check(o, hT, o_ref.reshape(o.shape), h_ref.reshape(hT.shape), "bf16")
+
+
+def test_workload_b8_h8_t8192_d64_h0_full():
+    x = synth.make_workload("gdn_fwd_b8_h8_t8192_d64_bf16_h0", device="cuda")
+    o, hT = run_dense(x, "auto")
+    o_ref, h_ref = U.oracle_dense(x)
+    check(o, hT, o_ref.reshape(o.shape), h_ref.reshape(hT.shape), "bf16")
+
+
+def test_workload_long_context_sampled():
+    name = "gdn_fwd_b1_h16_t131072_d128_bf16"
+    x = synth.make_workload(name, device="cuda")
+    o, hT = run_dense(x, "auto")
+    # causal prefix of every head
+    P = 8192
+    o_ref, _ = U.oracle_dense_prefix_gpu(x, P)
+    assert U.rel(U.f64(o[:, :, :P]), o_ref) <= U.TOL["bf16"][0]
+    # full length (every output and hT) of two heads
+    heads = [(0, 0), (0, 11)]
+    o_ref, h_ref = U.oracle_dense_heads_gpu(x, heads)
+    for i, (b, h) in enumerate(heads):
+        assert U.rel(U.f64(o[b, h]), o_ref[i]) <= U.TOL["bf16"][0]
+        assert U.rel(U.f64(hT[b, h]), h_ref[i]) <= U.TOL["bf16"][1]
+
+
+def test_workload_varlen_sampled():
+    name = "gdn_fwd_varlen_n64_h32_dk128_dv256_bf16"
+    y = synth.make_workload(name, device="cuda")
+    o, hT = run_varlen(y, "auto")
+    cu = y.cu_seqlens.cpu().numpy()
+    lens = np.diff(cu)
+    order = np.argsort(lens)
+    pairs = [(int(order[0]), 0), (int(order[-1]), 31), (int(order[-2]), 7),
+             (int(order[len(order) // 2]), 16), (5, 3), (63, 30)]
+    ref = U.oracle_varlen_pairs_gpu(y, pairs)
+    for (n, h), (o_ref, h_ref) in ref.items():
+        a, b = int(cu[n]), int(cu[n + 1])
+        assert U.rel(U.f64(o[h, a:b]), o_ref) <= U.TOL["bf16"][0], (n, h)
+        assert U.rel(U.f64(hT[n, h]), h_ref) <= U.TOL["bf16"][1], (n, h)
+
+
+# ------------------------------------------------------------ error handling
+
+
+def test_argument_errors():
+    x = synth.make_dense(1, 2, 70, 64, 64, io="bf16", seed=3, device="cuda")
+    lib = gdn.load()
+    s = torch.cuda.current_stream().cuda_stream
+    p = lambda t: t.data_ptr()  # noqa: E731
+    o = torch.empty_like(x.v)
+    args = [p(x.q), p(x.k), p(x.v), p(x.log_alpha), p(x.beta), None, p(o), None]
+    assert lib.gdn_fwd(*args, 1, 2, 70, 64, 64, 32, 1, s) == gdn.GDN_ERR_UNSUPPORTED
+    assert lib.gdn_fwd(*args, 1, 2, 70, 100, 64, 64, 1, s) == gdn.GDN_ERR_UNSUPPORTED
+    bad = list(args)
+    bad[0] = p(x.q) + 2
+    assert lib.gdn_fwd(*bad, 1, 2, 70, 64, 64, 64, 1, s) == gdn.GDN_ERR_ALIGNMENT
+    bad = list(args)
+    bad[1] = None
+    assert lib.gdn_fwd(*bad, 1, 2, 70, 64, 64, 64, 1, s) == gdn.GDN_ERR_INVALID_ARG
+    assert lib.gdn_fwd(*args, 1, 2, 70, 64, 64, 64, 7, s) == gdn.GDN_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("impl", ["simt", "tc"])
+def test_bad_cu_seqlens_reported(impl):
+    # a decreasing / out-of-range offset table is caught by the kernels and
+    # reported on the host; nothing is read out of bounds
+    y = synth.make_varlen([40, 50], 2, 64, 64, io="bf16", seed=4, device="cuda")
+    bad = torch.tensor([0, 95, 90], dtype=torch.int32, device="cuda")
+    with gdn.use_impl(IMPLS[impl]):
+        try:
+            gdn.gdn_fwd_varlen(y.q, y.k, y.v, y.log_alpha, y.beta, bad, None)
+        except gdn.GdnError as e:
+            if e.status == gdn.GDN_ERR_UNSUPPORTED and impl == "tc":
+                pytest.skip("shape not covered by the tensor-core path")
+            raise
+    lib = gdn.load()
+    assert lib.gdn_sync_check(torch.cuda.current_stream().cuda_stream) == gdn.GDN_ERR_INVALID_ARG
+    # the error word is cleared by reading it
+    assert lib.gdn_sync_check(torch.cuda.current_stream().cuda_stream) == gdn.GDN_OK
