@@ -28,6 +28,7 @@ GDN_ERR_UNSUPPORTED = 2
 GDN_ERR_ALIGNMENT = 3
 GDN_ERR_CUDA = 4
 GDN_ERR_DEVICE_TIMEOUT = 5
+GDN_ERR_TOO_LARGE = 6
 GDN_F32 = 0
 GDN_BF16 = 1
 GDN_OPT_IMPL = 0
@@ -48,6 +49,7 @@ _i = ctypes.c_int
 ABI = [
     ("gdn_fwd", _i, [_vp] * 8 + [_i] * 7 + [_vp]),
     ("gdn_fwd_varlen", _i, [_vp] * 9 + [_i] * 7 + [_vp]),
+    ("gdn_fwd_noalloc", _i, [_vp] * 8 + [_i] * 7 + [_vp]),
     ("gdn_status_string", ctypes.c_char_p, [_i]),
     ("gdn_sync_check", _i, [_vp]),
     ("gdn_set_option", _i, [_i, ctypes.c_longlong]),
@@ -170,6 +172,29 @@ def gdn_fwd_varlen(q, k, v, log_alpha, beta, cu_seqlens, h0=None, *, chunk=CHUNK
         _check(rc, "gdn_fwd_varlen")
         if check:
             _check(lib.gdn_sync_check(_stream(q.device)), "gdn_fwd_varlen (device)")
+    return o, hT
+
+
+def gdn_fwd_noalloc(q, k, v, log_alpha, beta, h0=None, *, chunk=CHUNK, out=None,
+                    final_state=None, check=False):
+    """Dense forward through the allocation-free entry point: the library
+    allocates nothing (its scratch is a fixed 32 MiB device array); the
+    caller passes the outputs (`out`, `final_state`) or they are created here
+    with torch.  Returns (o, hT)."""
+    lib = load()
+    _prep_io(q, k, v, log_alpha, beta, h0)
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    o = out if out is not None else torch.empty((B, H, T, dv), dtype=q.dtype, device=q.device)
+    hT = final_state if final_state is not None else torch.empty(
+        (B, H, dv, dk), dtype=torch.float32, device=q.device)
+    with torch.cuda.device(q.device):
+        rc = lib.gdn_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
+                                 _ptr(h0), _ptr(o), _ptr(hT), B, H, T, dk, dv, chunk,
+                                 _DT[q.dtype], _stream(q.device))
+        _check(rc, "gdn_fwd_noalloc")
+        if check:
+            _check(lib.gdn_sync_check(_stream(q.device)), "gdn_fwd_noalloc (device)")
     return o, hT
 
 

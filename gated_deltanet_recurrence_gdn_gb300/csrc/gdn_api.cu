@@ -161,6 +161,29 @@ gdn_status gdn_fwd_varlen(const void *q, const void *k, const void *v, const flo
     return dispatch(a);
 }
 
+gdn_status gdn_fwd_noalloc(const void *q, const void *k, const void *v, const float *log_alpha,
+                           const float *beta, const float *h0, void *o, float *hT, int B, int H,
+                           int T, int d_k, int d_v, int chunk, gdn_dtype dt, void *stream) {
+    if (B < 0 || T < 0) return GDN_ERR_INVALID_ARG;
+    const bool tokens = (long long)B * H * T > 0;
+    gdn_status rc = check_common(q, k, v, log_alpha, beta, h0, o, hT, H, d_k, d_v, chunk, dt,
+                                 tokens);
+    if (rc != GDN_OK) return rc;
+    if ((long long)B * H == 0) return GDN_OK;
+    if ((long long)B * H * T * (d_k + d_v + 1) * 4 > (long long)kNoallocScratchBytes)
+        return GDN_ERR_TOO_LARGE;
+    FwdArgs a{};
+    a.q = q; a.k = k; a.v = v; a.log_alpha = log_alpha; a.beta = beta; a.h0 = h0;
+    a.o = o; a.hT = hT;
+    a.sm = SeqMap{nullptr, B, H, T, 0};
+    a.dk = d_k; a.dv = d_v; a.dt = dt;
+    a.rows = (long long)B * H * T;
+    a.max_chunks = (T + kChunk - 1) / kChunk;
+    a.chunk_slots = (int)((long long)B * a.max_chunks);
+    a.stream = static_cast<cudaStream_t>(stream);
+    return simt_forward_noalloc(a);
+}
+
 const char *gdn_status_string(gdn_status s) {
     switch (s) {
         case GDN_OK: return "GDN_OK";
@@ -169,6 +192,7 @@ const char *gdn_status_string(gdn_status s) {
         case GDN_ERR_ALIGNMENT: return "GDN_ERR_ALIGNMENT: pointer not 16-byte aligned";
         case GDN_ERR_CUDA: return "GDN_ERR_CUDA: CUDA runtime error";
         case GDN_ERR_DEVICE_TIMEOUT: return "GDN_ERR_DEVICE_TIMEOUT: bounded device wait gave up";
+        case GDN_ERR_TOO_LARGE: return "GDN_ERR_TOO_LARGE: call needs more than the fixed scratch of gdn_fwd_noalloc (32 MiB)";
         default: return "unknown gdn_status";
     }
 }

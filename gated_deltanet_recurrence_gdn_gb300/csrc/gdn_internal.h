@@ -61,6 +61,11 @@ long long option(int key);
 // SIMT (CUDA-core, fp32 arithmetic) path: every supported shape and dtype.
 gdn_status simt_forward(const FwdArgs &a);
 
+// The same path on a dense batch with its scratch in a fixed device array of
+// kNoallocScratchBytes (needs rows * (d_k + d_v + 1) * 4 bytes); no allocation.
+constexpr size_t kNoallocScratchBytes = size_t(32) << 20;
+gdn_status simt_forward_noalloc(const FwdArgs &a);
+
 // tcgen05 tensor-core path (bf16 I/O).  Returns GDN_ERR_UNSUPPORTED when the
 // call does not fit it; the caller then decides whether to fall back.
 bool tc_supported(const FwdArgs &a);

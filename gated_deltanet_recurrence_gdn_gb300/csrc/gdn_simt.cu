@@ -27,6 +27,8 @@
 // and log_alpha = 0, which leaves every real row unchanged.
 #include <cuda_bf16.h>
 
+#include <mutex>
+
 #include "gdn_internal.h"
 
 namespace gdn {
@@ -352,6 +354,83 @@ gdn_status launch(const FwdArgs &a) {
 
 gdn_status simt_forward(const FwdArgs &a) {
     return a.dt == GDN_F32 ? launch<float>(a) : launch<__nv_bfloat16>(a);
+}
+
+}  // namespace gdn
+
+// ------------------------------------------------- allocation-free variant
+//
+// gdn_fwd_noalloc runs the same two CUDA-core kernels (prep, state pass) on a
+// dense batch, but its W / U / gate-cumsum scratch lives in this fixed device
+// array instead of coming from cudaMallocAsync.  The array belongs to every
+// GPU that loads the library, for as long as the library stays loaded.  All
+// calls share it and it keeps whatever the previous call left: nothing in it
+// needs to start at zero, because the prep kernel writes every row the state
+// kernel later reads.  Two calls whose kernels overlap on the GPU (different
+// streams, or different host threads) race on it and may both be wrong.
+static __device__ __align__(256) float gdn_noalloc_scratch[gdn::kNoallocScratchBytes / sizeof(float)];
+
+namespace gdn {
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+float *g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device.  In host code
+// the array's name only stands in for the symbol, so the address is looked
+// up once per device (with that device current) and cached.
+gdn_status noalloc_scratch(float **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return GDN_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return GDN_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, gdn_noalloc_scratch) != cudaSuccess || !p)
+            return GDN_ERR_CUDA;
+        g_noalloc_ptr[dev] = static_cast<float *>(p);
+    }
+    *out = g_noalloc_ptr[dev];
+    return GDN_OK;
+}
+
+template <typename TIn>
+gdn_status launch_noalloc(const FwdArgs &a, float *scratch) {
+    int *err = device_error_word();
+    cudaStream_t st = a.stream;
+    const size_t psm = prep_smem(a.dk, a.dv), ssm = state_smem(a.dk);
+    if (cudaFuncSetAttribute(k_simt_prep<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)psm) != cudaSuccess ||
+        cudaFuncSetAttribute(k_simt_state<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)ssm) != cudaSuccess)
+        return GDN_ERR_CUDA;
+    const size_t rows = (size_t)a.rows;
+    float *W = scratch;
+    float *U = W + rows * a.dk;
+    float *G = U + rows * a.dv;
+    if (a.chunk_slots > 0) {
+        dim3 grid(a.chunk_slots, a.sm.H);
+        k_simt_prep<TIn><<<grid, kThreads, psm, st>>>(a, nullptr, W, U, G, err);
+        count_launch();
+    }
+    dim3 grid(a.sm.N, a.sm.H, (a.dv + kDvt - 1) / kDvt);
+    k_simt_state<TIn><<<grid, kThreads, ssm, st>>>(a, W, U, G, err);
+    count_launch();
+    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+}  // namespace
+
+gdn_status simt_forward_noalloc(const FwdArgs &a) {
+    if (a.sm.cu) return GDN_ERR_UNSUPPORTED;   // dense batches only
+    const size_t need = (size_t)a.rows * (size_t)(a.dk + a.dv + 1) * sizeof(float);
+    if (need > kNoallocScratchBytes) return GDN_ERR_TOO_LARGE;
+    float *scratch = nullptr;
+    gdn_status rc = noalloc_scratch(&scratch);
+    if (rc != GDN_OK) return rc;
+    return a.dt == GDN_F32 ? launch_noalloc<float>(a, scratch)
+                           : launch_noalloc<__nv_bfloat16>(a, scratch);
 }
 
 }  // namespace gdn

@@ -52,7 +52,8 @@ typedef enum {
     GDN_ERR_UNSUPPORTED = 2,    /* chunk != 64, d_k / d_v outside the supported set */
     GDN_ERR_ALIGNMENT = 3,      /* a pointer is not 16-byte aligned */
     GDN_ERR_CUDA = 4,           /* a CUDA runtime call or launch failed */
-    GDN_ERR_DEVICE_TIMEOUT = 5  /* a bounded device-side wait gave up */
+    GDN_ERR_DEVICE_TIMEOUT = 5, /* a bounded device-side wait gave up */
+    GDN_ERR_TOO_LARGE = 6       /* gdn_fwd_noalloc: the call needs more than its fixed scratch */
 } gdn_status;
 
 typedef enum {
@@ -90,6 +91,34 @@ gdn_status gdn_fwd_varlen(const void *q, const void *k, const void *v,
                           void *o, float *hT, const int32_t *cu_seqlens,
                           int N, int H, int T_total, int d_k, int d_v, int chunk,
                           gdn_dtype dt, void *stream);
+
+/*
+ * Dense forward pass that allocates no device memory (the paper has no
+ * counterpart: this is a deployment variant of the same computation).
+ *
+ * Some callers cannot allocate while they run: a serving process that hands
+ * all of the GPU's memory to its own pool at start-up and forbids any other
+ * allocation afterwards, or a latency-critical loop in which an allocation
+ * that stalls or fails is not acceptable.  gdn_fwd_noalloc takes the same
+ * arguments and has the same layouts as gdn_fwd, but keeps its scratch in a
+ * fixed 32 MiB array that the library places in every GPU's memory when it
+ * is loaded; it never calls an allocator.
+ *
+ *   Limit: B*H*T*(d_k + d_v + 1)*4 bytes must not exceed 32 MiB (for
+ *   d_k = d_v = 128, about 32 000 token-heads), otherwise GDN_ERR_TOO_LARGE
+ *   is returned and nothing is enqueued.  It always runs the fp32 CUDA-core
+ *   kernels (bf16 or fp32 I/O).
+ *   Set-up: the first call on each device looks up the array's device address
+ *   with that device current; make that first call before any stream capture.
+ *   Sharing: every call uses the same array.  Calls whose kernels overlap on
+ *   the GPU (other streams, other host threads) race on it and give wrong
+ *   results; serialise them.
+ */
+gdn_status gdn_fwd_noalloc(const void *q, const void *k, const void *v,
+                           const float *log_alpha, const float *beta, const float *h0,
+                           void *o, float *hT,
+                           int B, int H, int T, int d_k, int d_v, int chunk,
+                           gdn_dtype dt, void *stream);
 
 /* Static, human-readable name of a status. */
 const char *gdn_status_string(gdn_status s);
