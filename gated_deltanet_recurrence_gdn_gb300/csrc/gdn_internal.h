@@ -1,6 +1,7 @@
 // gdn_internal.h -- shared host/device declarations of libgdn (not installed).
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -65,6 +66,15 @@ gdn_status simt_forward(const FwdArgs &a);
 // kNoallocScratchBytes (needs rows * (d_k + d_v + 1) * 4 bytes); no allocation.
 constexpr size_t kNoallocScratchBytes = size_t(32) << 20;
 gdn_status simt_forward_noalloc(const FwdArgs &a);
+
+// Lists every (sequence, chunk) of a packed batch into table[chunk_slots]
+// (unused slots get n = -1) and validates cu_seqlens.
+gdn_status enqueue_chunk_table(const FwdArgs &a, int2 *table);
+
+// Chunk-prep kernel of the tensor-core path: T = (I + A)^{-1} per chunk, bf16
+// rows [rows][64] in Tout (table: packed batches only, else nullptr).
+size_t tc_prep_smem(int dk);
+gdn_status enqueue_tc_prep(const FwdArgs &a, const int2 *table, __nv_bfloat16 *Tout);
 
 // tcgen05 tensor-core path (bf16 I/O).  Returns GDN_ERR_UNSUPPORTED when the
 // call does not fit it; the caller then decides whether to fall back.

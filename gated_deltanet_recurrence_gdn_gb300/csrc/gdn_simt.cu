@@ -356,6 +356,13 @@ gdn_status simt_forward(const FwdArgs &a) {
     return a.dt == GDN_F32 ? launch<float>(a) : launch<__nv_bfloat16>(a);
 }
 
+gdn_status enqueue_chunk_table(const FwdArgs &a, int2 *table) {
+    k_chunk_table<<<1, 1024, 0, a.stream>>>(a.sm.cu, a.sm.N, a.sm.T_total, table, a.chunk_slots,
+                                             device_error_word());
+    count_launch();
+    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
 }  // namespace gdn
 
 // ------------------------------------------------- allocation-free variant

@@ -19,14 +19,16 @@
 //   O     = diag(gamma) Q H + P V'                      (tcgen05, accumulates)
 //   H    <- exp(g_C) H + dH
 //
-// Warp roles (320 threads):
+// Warp roles (352 threads):
 //   warps 0-3  chain warpgroup: owns H (thread t = row t = d_k index t), forms
-//              V', updates H, stores O.
-//   warps 4-7  prep warpgroup: gates, G epilogue (A, P), the inverse, the WY
-//              factors as bf16 operands, gamma-scaled Q.  Runs one chunk ahead
-//              of the chain.
+//              V', updates H, stores O (a chunk late, from a second TMEM
+//              accumulator, so the store is off the state's critical path).
+//   warps 4-7  prep warpgroup: gates (prefetched a chunk ahead), G epilogue
+//              (A, P), the inverse, the WY factors as bf16 operands,
+//              gamma-scaled Q.  Runs one chunk ahead of the chain.
 //   warp 8     TMA producer (one lane): K, Q, V tiles, 128-byte swizzled.
-//   warp 9     MMA issuer (one lane) and TMEM owner.
+//   warp 9     chain MMA issuer (one lane): [W; gamma Q] H, K^T V~, P V'; TMEM owner.
+//   warp 10    prep MMA issuer (one lane): [K; Q] K^T, [T_u; T_w] [V | K].
 // Every mbarrier wait is bounded; a wait that gives up sets the device error
 // word and makes every role leave its loop, after which in-flight MMAs are
 // drained and TMEM is freed.
@@ -40,6 +42,25 @@
 #include "gdn_internal.h"
 #include "tc_ptx.cuh"
 
+// Optional per-phase timeline of CTA (0,0,0) for profiling builds
+// (-DGDN_TRACE_TIMELINE): clock64() stamps by role, chunk and event, read back
+// with gdn_trace_read().  Compiled out otherwise.
+#ifdef GDN_TRACE_TIMELINE
+__device__ long long g_gdn_trace[4][128][16];
+extern "C" int gdn_trace_read(long long *out) {
+    return (int)cudaMemcpyFromSymbol(out, g_gdn_trace, sizeof(g_gdn_trace));
+}
+#define TRACE(role, jj, ev, cond)                                                          \
+    do {                                                                                   \
+        if ((cond) && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && (jj) < 128) \
+            g_gdn_trace[role][jj][ev] = clock64();                                         \
+    } while (0)
+#else
+#define TRACE(role, jj, ev, cond) \
+    do {                          \
+    } while (0)
+#endif
+
 namespace gdn {
 namespace {
 
@@ -48,54 +69,56 @@ using namespace ptx;
 constexpr int kC = 64;         // chunk length
 constexpr int kNV = 64;        // d_v columns per CTA
 constexpr int kNS = 2;         // input stages
-constexpr int kThreadsTC = 320;
+constexpr int kThreadsTC = 352;
 
 // mbarrier slots
 enum {
     B_FULL = 0,                 // + stage: TMA bytes landed
     B_READY = B_FULL + kNS,     // + stage: pad rows cleared, stage usable by MMA
-    B_FREE = B_READY + kNS,     // + stage: consumers done (MMA commit + prep)
-    B_G = B_FREE + kNS,         // M1 done (G in TMEM)
+    B_FREE = B_READY + kNS,     // + stage: consumers done (chain MMA commit + prep)
+    B_PFREE = B_FREE + kNS,     // + (chunk & 1): P buffer read by the output MMA
+    B_G = B_PFREE + 2,          // Gram MMA done (G in TMEM)
     B_GFREE,                    // prep has read G
     B_T,                        // T_u / T_w in smem
     B_UW,                       // U and W in TMEM
     B_WQ,                       // W and gamma*Q in smem
     B_M2,                       // chain MMA done
     B_H,                        // H (bf16) in smem, TMEM results consumed
-    B_VN,                       // V' (bf16) in smem
+    B_VN,                       // V' (bf16) in smem, U consumed
     B_M34,                      // dH and O done
-    B_DRAIN,
+    B_DRAIN,                    // chain MMA issuer drained
+    B_DRAIN2,                   // prep MMA issuer drained
     B_COUNT
 };
 
 template <int DK>
 struct Lay {
     static constexpr int KB = DK / 64;                 // 64-column blocks of K / Q / W
-    static constexpr int STAGE = KB * 16384 + 8192;    // per block [K | Q], then V
-    static constexpr int OFF_V = KB * 16384;
+    static constexpr int OFF_V = KB * 16384;           // stage: per block [K | Q], then V, T
+    static constexpr int OFF_TI = OFF_V + 8192;        // chunk's T = (I + A)^{-1}, bf16
+    static constexpr int STAGE = OFF_TI + 8192;
     static constexpr int OFF_STAGE = 0;
     static constexpr int OFF_WQ = kNS * STAGE;         // per block [W | gamma Q]
     static constexpr int OFF_H = OFF_WQ + KB * 16384;  // DK rows x 128 B
     static constexpr int OFF_R0 = OFF_H + DK * 128;    // [V~ | P0]
     static constexpr int OFF_R1 = OFF_R0 + 16384;      // [V' | P1]
     static constexpr int OFF_TT = OFF_R1 + 16384;      // [T_u ; T_w], 128 rows x 128 B
-    static constexpr int LDA = 68;                     // fp32 row stride of A / T
-    static constexpr int OFF_A = OFF_TT + 16384;
-    static constexpr int OFF_T = OFF_A + 64 * LDA * 4;
-    static constexpr int LDX = 36;
-    static constexpr int OFF_X = OFF_T + 64 * LDA * 4; // fp32 [32][36]
-    static constexpr int OFF_G = OFF_X + 32 * LDX * 4; // 2 x {g, beta, gamma, 1/gamma}
-    static constexpr int OFF_BAR = OFF_G + 2 * 4 * 64 * 4;
+    static constexpr int GSZ = 5 * 64;                 // g, beta, gamma, 1/gamma, beta*gamma
+    static constexpr int OFF_G = OFF_TT + 16384;       // 2 x GSZ floats
+    static constexpr int OFF_GS = OFF_G + 2 * GSZ * 4;  // per stage raw gates: log_alpha, beta
+    static constexpr int OFF_BAR = OFF_GS + kNS * 128 * 4;
     static constexpr int OFF_MISC = OFF_BAR + B_COUNT * 8;
     static constexpr int TOTAL = OFF_MISC + 64;
     static constexpr int ALLOC = TOTAL + 1024;
     static_assert(OFF_WQ % 1024 == 0 && OFF_H % 1024 == 0 && OFF_R0 % 1024 == 0, "align");
-    static_assert(OFF_TT % 1024 == 0 && OFF_A % 16 == 0, "align");
+    static_assert(OFF_TT % 1024 == 0 && OFF_G % 16 == 0, "align");
     static_assert(ALLOC <= 227 * 1024, "shared memory budget");
 };
 
-// TMEM column map (512 allocated)
-constexpr uint32_t TM_G = 0, TM_U = 64, TM_M2 = 128, TM_H = 192, TM_W = 256;
+// TMEM column map (512 allocated): G, two chain / output accumulators, dH, and
+// the WY product [T_u; T_w] [K | V]: W in its first d_k columns (lanes 64-127),
+// U in the next 64 (lanes 0-63).
+constexpr uint32_t TM_G = 0, TM_M2 = 128, TM_H = 256, TM_W = 320;
 
 struct TcParams {
     SeqMap sm;
@@ -120,81 +143,46 @@ struct Ctl {
         atomicCAS(err, 0, kErrTimeout);
         return false;
     }
-};
-
-__device__ __forceinline__ float tf32(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return __uint_as_float(r);
-}
-
-// D += A(16x8, row) * B(8x8, col), tf32 inputs, fp32 accumulate.
-__device__ __forceinline__ void mma_tf32(float (&d)[4], const float (&a)[4], const float (&b)[2]) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(__float_as_uint(a[0])), "r"(__float_as_uint(a[1])), "r"(__float_as_uint(a[2])),
-          "r"(__float_as_uint(a[3])), "r"(__float_as_uint(b[0])), "r"(__float_as_uint(b[1])));
-}
-
-// One 16x8 output tile of  Y = Am * Bm  over k = 0..K-1, operands fp32 in smem
-// (row-major with strides lda / ldb).  Returns the C fragment.
-template <int K>
-__device__ __forceinline__ void tile_mma(float (&c)[4], const float *Am, int lda, const float *Bm,
-                                         int ldb, int lane) {
-    const int g = lane >> 2, t = lane & 3;
-    c[0] = c[1] = c[2] = c[3] = 0.f;
-#pragma unroll
-    for (int k0 = 0; k0 < K; k0 += 8) {
-        float a[4], b[2];
-        a[0] = tf32(Am[g * lda + k0 + t]);
-        a[1] = tf32(Am[(g + 8) * lda + k0 + t]);
-        a[2] = tf32(Am[g * lda + k0 + t + 4]);
-        a[3] = tf32(Am[(g + 8) * lda + k0 + t + 4]);
-        b[0] = tf32(Bm[(k0 + t) * ldb + g]);
-        b[1] = tf32(Bm[(k0 + t + 4) * ldb + g]);
-        mma_tf32(c, a, b);
+    // Same, by busy polling (single-thread issuer roles).
+    __device__ __forceinline__ bool spin(int b, uint32_t parity) const {
+        if (*abort) return false;
+        if (mbar_spin(bar + b, parity, limit)) return true;
+        *abort = 1;
+        atomicCAS(err, 0, kErrTimeout);
+        return false;
     }
-}
-
-__device__ __forceinline__ void store_tile(float *D, int ldd, const float (&c)[4], int lane,
-                                           float scale) {
-    const int g = lane >> 2, t = lane & 3;
-    D[g * ldd + 2 * t] = scale * c[0];
-    D[g * ldd + 2 * t + 1] = scale * c[1];
-    D[(g + 8) * ldd + 2 * t] = scale * c[2];
-    D[(g + 8) * ldd + 2 * t + 1] = scale * c[3];
-}
+};
 
 __device__ __forceinline__ void st16(uint8_t *p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     *reinterpret_cast<uint4 *>(p) = make_uint4(a, b, c, d);
 }
 
-// Writes 16 fp32 values (x[0..15], columns c0..c0+15 of a 64-wide row) as bf16
-// into a 128-byte-swizzled row.
-__device__ __forceinline__ void put_row16(uint8_t *tile, int row, int c0, const float (&x)[16]) {
-    const int ch = c0 >> 3;
+// Writes 8 fp32 values (columns 8*ch .. 8*ch+7 of a 64-wide row) as bf16 into
+// chunk `ch` of a 128-byte-swizzled row.
+__device__ __forceinline__ void put8(uint8_t *tile, int row, int ch, const float *x) {
     st16(tile + sw128_offset(row, ch), pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]),
          pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
-    st16(tile + sw128_offset(row, ch + 1), pack_bf16(x[8], x[9]), pack_bf16(x[10], x[11]),
-         pack_bf16(x[12], x[13]), pack_bf16(x[14], x[15]));
 }
+
+__device__ __forceinline__ void put_row64(uint8_t *tile, int row, const float (&x)[64]) {
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch) put8(tile, row, ch, x + 8 * ch);
+}
+
+__device__ __forceinline__ float f32(uint32_t u) { return __uint_as_float(u); }
 
 template <int DK>
 __global__ void __launch_bounds__(kThreadsTC, 1)
 k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-         const __grid_constant__ CUtensorMap tm_v, TcParams p) {
+         const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_t,
+         TcParams p) {
     using L = Lay<DK>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + L::OFF_BAR);
     uint32_t *misc = reinterpret_cast<uint32_t *>(sm + L::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(misc + 1);
-    float *gb = reinterpret_cast<float *>(sm + L::OFF_G);   // [2][4][64]
-    float *Ab = reinterpret_cast<float *>(sm + L::OFF_A);
-    float *Tb = reinterpret_cast<float *>(sm + L::OFF_T);
-    float *Xb = reinterpret_cast<float *>(sm + L::OFF_X);
+    float *gb = reinterpret_cast<float *>(sm + L::OFF_G);   // [2][GSZ]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int dv0 = blockIdx.x * kNV, h = blockIdx.y, n = blockIdx.z;
@@ -230,6 +218,7 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
     if (tid == 0) {
         for (int i = 0; i < B_COUNT; ++i) mbar_init(bar + i, 1);
         for (int s = 0; s < kNS; ++s) mbar_init(bar + B_FREE + s, 2);
+        for (int s = 0; s < kNS; ++s) mbar_init(bar + B_FULL + s, 33);   // TMA tx + 32 gate lanes
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -248,84 +237,111 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
         for (int c = 0; c < kNV; ++c)
             hreg[c] = (t < DK && p.h0) ? __ldg(p.h0 + (srow + dv0 + c) * DK + t) : 0.f;
         uint8_t *Hs = sm + L::OFF_H;
-        for (int j = 0; j < nch; ++j) {
-            // (i) publish H as the bf16 B operand of the chain MMA
-            if (t < DK) {
+        uint8_t *VT = sm + L::OFF_R0, *VN = sm + L::OFF_R1;
+        // Output rows of chunk jj (lanes 64-127 of its accumulator) to global.
+        auto store_o = [&](int jj) {
+            const int r = t - 64;
+            const int Lj = min(kC, len - jj * kC);
+            uint32_t o0[32], o1[32];
+            const uint32_t acc = tmem + lane_base + TM_M2 + (jj & 1) * 64;
+            tmem_ld32(acc, o0);
+            tmem_ld32(acc + 32, o1);
+            tmem_wait32(o0);
+            tmem_wait32(o1);
+            if (r < Lj) {
+                uint4 *dst = reinterpret_cast<uint4 *>(p.o + (row0 + (long long)jj * kC + r) *
+                                                                 p.dv + dv0);
 #pragma unroll
-                for (int c0 = 0; c0 < kNV; c0 += 16) {
-                    float x[16];
+                for (int q = 0; q < 4; ++q)
+                    dst[q] = make_uint4(pack_bf16(f32(o0[8 * q]), f32(o0[8 * q + 1])),
+                                        pack_bf16(f32(o0[8 * q + 2]), f32(o0[8 * q + 3])),
+                                        pack_bf16(f32(o0[8 * q + 4]), f32(o0[8 * q + 5])),
+                                        pack_bf16(f32(o0[8 * q + 6]), f32(o0[8 * q + 7])));
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) x[i] = hreg[c0 + i];
-                    put_row16(Hs, t, c0, x);
-                }
+                for (int q = 0; q < 4; ++q)
+                    dst[4 + q] = make_uint4(pack_bf16(f32(o1[8 * q]), f32(o1[8 * q + 1])),
+                                            pack_bf16(f32(o1[8 * q + 2]), f32(o1[8 * q + 3])),
+                                            pack_bf16(f32(o1[8 * q + 4]), f32(o1[8 * q + 5])),
+                                            pack_bf16(f32(o1[8 * q + 6]), f32(o1[8 * q + 7])));
             }
+        };
+        bool alive = true;
+        for (int j = 0; j < nch; ++j) {
+            TRACE(0, j, 0, t == 0);
+            // (i) publish H as the bf16 B operand of the chain MMA
+            if (t < DK) put_row64(Hs, t, hreg);
             fence_proxy_async_smem();
             tc_fence_before();
             named_bar(1, 128);
             if (t == 0) mbar_arrive(bar + B_H);
+            TRACE(0, j, 1, t == 0);
+            // (i') previous chunk's output rows, off the state's critical path
+            if (j > 0 && t >= 64) store_o(j - 1);
+            TRACE(0, j, 2, t == 64);
             // (ii) V' = U - W H, and its decayed copy for the state update
             {
                 bool ok = ctl.wait(B_WQ, j & 1);   // orders this chunk's gates too
                 ok = ok && ctl.wait(B_M2, j & 1);
-                if (!named_bar_and(1, 128, ok)) break;
+                if (!named_bar_and(1, 128, ok)) {
+                    alive = false;
+                    break;
+                }
             }
+            TRACE(0, j, 3, t == 0);
             tc_fence_after();
-            const float *gj = gb + (j & 1) * 256;
+            const float *gj = gb + (j & 1) * L::GSZ;
             const float gC = gj[63];
             const float decayC = __expf(gC);
             if (t < 64) {
                 const float ev = __expf(gC - gj[t]);
-                uint8_t *VT = sm + L::OFF_R0, *VN = sm + L::OFF_R1;
+                const uint32_t acc = tmem + lane_base + TM_M2 + (j & 1) * 64;
 #pragma unroll
-                for (int c0 = 0; c0 < kNV; c0 += 16) {
-                    float wh[16], u[16], vt[16];
-                    tmem_ld16f(tmem + lane_base + TM_M2 + c0, wh);
-                    tmem_ld16f(tmem + lane_base + TM_U + c0, u);
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t wh[32], u[32];
+                    tmem_ld32(acc + 32 * half, wh);
+                    tmem_ld32(tmem + lane_base + TM_W + DK + 32 * half, u);
+                    tmem_wait32(wh);
+                    tmem_wait32(u);
+                    float vn[32], vt[32];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        u[i] -= wh[i];
-                        vt[i] = u[i] * ev;
+                    for (int i = 0; i < 32; ++i) {
+                        vn[i] = f32(u[i]) - f32(wh[i]);
+                        vt[i] = vn[i] * ev;
                     }
-                    put_row16(VN, t, c0, u);
-                    put_row16(VT, t, c0, vt);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        put8(VN, t, 4 * half + q, vn + 8 * q);
+                        put8(VT, t, 4 * half + q, vt + 8 * q);
+                    }
                 }
             }
             fence_proxy_async_smem();
             tc_fence_before();
             named_bar(1, 128);
             if (t == 0) mbar_arrive(bar + B_VN);
-            // (iii) H <- exp(g_C) H + dH;  O rows out
-            if (!named_bar_and(1, 128, ctl.wait(B_M34, j & 1))) break;
+            TRACE(0, j, 4, t == 0);
+            // (iii) H <- exp(g_C) H + dH
+            if (!named_bar_and(1, 128, ctl.wait(B_M34, j & 1))) {
+                alive = false;
+                break;
+            }
+            TRACE(0, j, 5, t == 0);
             tc_fence_after();
             if (t < DK) {
+                uint32_t d0[32], d1[32];
+                tmem_ld32(tmem + lane_base + TM_H, d0);
+                tmem_ld32(tmem + lane_base + TM_H + 32, d1);
+                tmem_wait32(d0);
+                tmem_wait32(d1);
 #pragma unroll
-                for (int c0 = 0; c0 < kNV; c0 += 16) {
-                    float dh[16];
-                    tmem_ld16f(tmem + lane_base + TM_H + c0, dh);
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) hreg[c0 + i] = fmaf(decayC, hreg[c0 + i], dh[i]);
-                }
-            }
-            if (t >= 64) {
-                const int r = t - 64;
-                const int L_ = min(kC, len - j * kC);
-                __nv_bfloat16 *orow = p.o + (row0 + (long long)j * kC + r) * p.dv + dv0;
-#pragma unroll
-                for (int c0 = 0; c0 < kNV; c0 += 16) {
-                    float ov[16];
-                    tmem_ld16f(tmem + lane_base + TM_M2 + c0, ov);
-                    if (r < L_) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(orow + c0);
-                        dst[0] = make_uint4(pack_bf16(ov[0], ov[1]), pack_bf16(ov[2], ov[3]),
-                                            pack_bf16(ov[4], ov[5]), pack_bf16(ov[6], ov[7]));
-                        dst[1] = make_uint4(pack_bf16(ov[8], ov[9]), pack_bf16(ov[10], ov[11]),
-                                            pack_bf16(ov[12], ov[13]),
-                                            pack_bf16(ov[14], ov[15]));
-                    }
+                for (int i = 0; i < 32; ++i) {
+                    hreg[i] = fmaf(decayC, hreg[i], f32(d0[i]));
+                    hreg[32 + i] = fmaf(decayC, hreg[32 + i], f32(d1[i]));
                 }
             }
         }
-        if (!*abort_flag && p.hT && t < DK) {
+        if (alive && nch > 0 && t >= 64) store_o(nch - 1);
+        if (alive && p.hT && t < DK) {
 #pragma unroll
             for (int c = 0; c < kNV; ++c) p.hT[(srow + dv0 + c) * DK + t] = hreg[c];
         }
@@ -338,14 +354,15 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
             const int s = j % kNS;
             uint8_t *stg = sm + L::OFF_STAGE + s * L::STAGE;
             const int L_ = min(kC, len - j * kC);
-            float *gj = gb + (j & 1) * 256;   // g, beta, gamma, 1/gamma
-            // (a) gates and their in-chunk cumulative sum
+            float *gj = gb + (j & 1) * L::GSZ;   // g, beta, gamma, 1/gamma, beta*gamma
+            TRACE(1, j, 0, t == 0);
+            if (!named_bar_and(2, 128, ctl.wait(B_FULL + s, (j / kNS) & 1))) break;
+            TRACE(1, j, 1, t == 0);
+            // (a) in-chunk cumulative log gate from the staged gates
             if (w == 0) {
-                const long long r0 = row0 + (long long)j * kC;
-                float la0 = lane < L_ ? __ldg(p.log_alpha + r0 + lane) : 0.f;
-                float la1 = lane + 32 < L_ ? __ldg(p.log_alpha + r0 + lane + 32) : 0.f;
-                const float b0 = lane < L_ ? __ldg(p.beta + r0 + lane) : 0.f;
-                const float b1 = lane + 32 < L_ ? __ldg(p.beta + r0 + lane + 32) : 0.f;
+                const float *gs = reinterpret_cast<const float *>(sm + L::OFF_GS) + s * 128;
+                float la0 = gs[lane], la1 = gs[32 + lane];
+                const float b0 = gs[64 + lane], b1 = gs[96 + lane];
 #pragma unroll
                 for (int off = 1; off < 32; off <<= 1) {
                     const float y0 = __shfl_up_sync(0xffffffffu, la0, off);
@@ -356,19 +373,21 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
                     }
                 }
                 la1 += __shfl_sync(0xffffffffu, la0, 31);
+                const float e0 = __expf(la0), e1 = __expf(la1);
                 gj[lane] = la0;
                 gj[lane + 32] = la1;
                 gj[64 + lane] = b0;
                 gj[64 + lane + 32] = b1;
-                gj[128 + lane] = __expf(la0);
-                gj[128 + lane + 32] = __expf(la1);
+                gj[128 + lane] = e0;
+                gj[128 + lane + 32] = e1;
                 gj[192 + lane] = __expf(-la0);   // used only when the chunk's span is < 80
                 gj[192 + lane + 32] = __expf(-la1);
+                gj[256 + lane] = b0 * e0;
+                gj[256 + lane + 32] = b1 * e1;
             }
-            if (!named_bar_and(2, 128, ctl.wait(B_FULL + s, (j / kNS) & 1))) break;
             if (p.sm.cu && L_ < kC) {
                 // rows past this sequence belong to the next one: clear them
-                const int per_row = 2 * DK / 8 + kNV / 8;   // 16-byte pieces per row
+                constexpr int per_row = 2 * DK / 8 + 16;   // 16-byte pieces: K, Q, V, T
                 for (int i = t; i < (kC - L_) * per_row; i += 128) {
                     const int r = L_ + i / per_row, q = i % per_row;
                     uint8_t *base;
@@ -377,140 +396,99 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
                         const int blk = q / 16, which = (q / 8) & 1;   // per block: K, then Q
                         base = stg + blk * 16384 + which * 8192;
                         chn = q & 7;
-                    } else {
+                    } else if (q < 2 * DK / 8 + 8) {
                         base = stg + L::OFF_V;
                         chn = q - 2 * DK / 8;
+                    } else {
+                        base = stg + L::OFF_TI;
+                        chn = q - 2 * DK / 8 - 8;
                     }
                     st16(base + sw128_offset(r, chn), 0u, 0u, 0u, 0u);
                 }
+                fence_proxy_async_smem();
             }
-            fence_proxy_async_smem();
             named_bar(2, 128);
             if (t == 0) mbar_arrive(bar + B_READY + s);
-            // (b) G epilogue: A (fp32, for the inverse) and P (bf16 operand)
-            if (!named_bar_and(2, 128, ctl.wait(B_G, j & 1))) break;
-            tc_fence_after();
             {
+                // (b) T_u = T diag(beta) (TT rows 0-63), T_w = T diag(beta gamma)
+                //     (TT rows 64-127) from the chunk's T, same swizzled positions
+                const int r = t & 63;
+                const uint8_t *Ti = stg + L::OFF_TI;
+                uint8_t *TT = sm + L::OFF_TT;
+                const float4 *sc = reinterpret_cast<const float4 *>(gj + (t < 64 ? 64 : 256));
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {
+                    const uint4 v = *reinterpret_cast<const uint4 *>(Ti + sw128_offset(r, ch));
+                    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+                    float x[8];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 f2 = __bfloat1622float2(
+                            *reinterpret_cast<const __nv_bfloat162 *>(&wv[e]));
+                        x[2 * e] = f2.x;
+                        x[2 * e + 1] = f2.y;
+                    }
+                    const float4 c0 = sc[2 * ch], c1 = sc[2 * ch + 1];
+                    st16(TT + sw128_offset(t, ch), pack_bf16(x[0] * c0.x, x[1] * c0.y),
+                         pack_bf16(x[2] * c0.z, x[3] * c0.w), pack_bf16(x[4] * c1.x, x[5] * c1.y),
+                         pack_bf16(x[6] * c1.z, x[7] * c1.w));
+                }
+                TRACE(1, j, 7, t == 0);
+                fence_proxy_async_smem();
+                named_bar(2, 128);
+                if (t == 0) mbar_arrive(bar + B_T);
+                TRACE(1, j, 2, t == 0);
+            }
+            {
+                // (b') P = mask_{s<=r}(Q K^T) * exp(g_r - g_s).  The Q K^T MMA has
+                //      M = 64: row 16w + i sits in lane i (< 16) of warp w's lanes.
+                bool okg = ctl.wait(B_G, j & 1);
+                if (j >= 2) okg = okg && ctl.wait(B_PFREE + (j & 1), ((j - 2) >> 1) & 1);
+                if (!named_bar_and(2, 128, okg)) break;
+                tc_fence_after();
+                const int r = 16 * w + (lane & 15);
+                uint32_t g0[32], g1[32];
+                tmem_ld32(tmem + lane_base + TM_G, g0);
+                tmem_ld32(tmem + lane_base + TM_G + 32, g1);
                 const float gC = gj[63];
                 const bool span_ok = gC > -80.f;
-                const int r = t & 63;
                 const float gr = gj[r];
-                float fr = span_ok ? gj[128 + r] : 0.f;
-                if (t < 64) fr *= gj[64 + r];   // beta_r folded into A
+                const float fr = span_ok ? gj[128 + r] : 0.f;
                 uint8_t *Pt = sm + ((j & 1) ? L::OFF_R1 : L::OFF_R0) + 8192;
+                tmem_wait32(g0);
+                tmem_wait32(g1);
+                TRACE(1, j, 8, t == 0);
+                if (lane < 16) {
 #pragma unroll
-                for (int c0 = 0; c0 < kC; c0 += 16) {
-                    float gv[16];
-                    tmem_ld16f(tmem + lane_base + TM_G + c0, gv);
+                    for (int half = 0; half < 2; ++half) {
+                        float x[32];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int sidx = c0 + i;
-                        const bool keep = (t < 64) ? (sidx < r) : (sidx <= r);
-                        float f;
-                        if (span_ok) f = fr * gj[192 + sidx];
-                        else f = (t < 64 ? gj[64 + r] : 1.f) * __expf(keep ? gr - gj[sidx] : 0.f);
-                        gv[i] = keep ? f * gv[i] : 0.f;
-                    }
-                    if (t < 64) {
-                        float4 *dst = reinterpret_cast<float4 *>(Ab + r * L::LDA + c0);
-                        dst[0] = make_float4(gv[0], gv[1], gv[2], gv[3]);
-                        dst[1] = make_float4(gv[4], gv[5], gv[6], gv[7]);
-                        dst[2] = make_float4(gv[8], gv[9], gv[10], gv[11]);
-                        dst[3] = make_float4(gv[12], gv[13], gv[14], gv[15]);
-                    } else {
-                        put_row16(Pt, r, c0, gv);
+                        for (int i = 0; i < 32; ++i) {
+                            const int sidx = 32 * half + i;
+                            const float gv = f32(half == 0 ? g0[i] : g1[i]);
+                            const bool keep = sidx <= r;
+                            const float f = span_ok ? fr * gj[192 + sidx]
+                                                    : __expf(keep ? gr - gj[sidx] : 0.f);
+                            x[i] = keep ? f * gv : 0.f;
+                        }
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) put8(Pt, r, 4 * half + q, x + 8 * q);
                     }
                 }
-            }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            named_bar(2, 128);
-            if (t == 0) mbar_arrive(bar + B_GFREE);
-            // (c) T = (I + A)^{-1}
-            if (w < 2) {
-                // 16x16 diagonal blocks, one column per thread, right-looking
-                const int blk = t >> 4, c = t & 15, o = blk * 16;
-                float x[16];
-#pragma unroll
-                for (int r = 0; r < 16; ++r) x[r] = (r == c) ? 1.f : 0.f;
-#pragma unroll
-                for (int s2 = 0; s2 < 16; ++s2) {
-#pragma unroll
-                    for (int r = s2 + 1; r < 16; ++r)
-                        x[r] = fmaf(-Ab[(o + r) * L::LDA + o + s2], x[s2], x[r]);
-                }
-#pragma unroll
-                for (int r = 0; r < 16; ++r) Tb[(o + r) * L::LDA + o + c] = x[r];
-            } else {
-                // zero the six strictly upper 16x16 blocks
-                for (int i = t - 64; i < 6 * 256; i += 64) {
-                    const int b = i >> 8, e = i & 255;
-                    const int bi = b < 3 ? 0 : (b < 5 ? 1 : 2);
-                    const int bj = b < 3 ? b + 1 : (b < 5 ? b - 1 : 3);
-                    Tb[(bi * 16 + (e >> 4)) * L::LDA + bj * 16 + (e & 15)] = 0.f;
-                }
-            }
-            named_bar(2, 128);
-            {
-                // 16 -> 32: T_{2p+1,2p} = -D_{2p+1} A_{2p+1,2p} D_{2p}
-                const int pr = w >> 1, nh = w & 1;
-                const int ro = 32 * pr + 16, co = 32 * pr;
-                float *Xw = Xb + w * 16 * 9;
-                float c4[4];
-                tile_mma<16>(c4, Ab + ro * L::LDA + co, L::LDA, Tb + co * L::LDA + co + 8 * nh,
-                             L::LDA, lane);
-                store_tile(Xw, 9, c4, lane, 1.f);
-                __syncwarp();
-                tile_mma<16>(c4, Tb + ro * L::LDA + ro, L::LDA, Xw, 9, lane);
-                __syncwarp();
-                store_tile(Tb + ro * L::LDA + co + 8 * nh, L::LDA, c4, lane, -1.f);
-            }
-            named_bar(2, 128);
-            {
-                // 32 -> 64: T_{1,0} = -E1 (A_{1,0} E0), 32x32 blocks
-                const int mt = w >> 1, nt0 = 2 * (w & 1);
-#pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    float c4[4];
-                    tile_mma<32>(c4, Ab + (32 + 16 * mt) * L::LDA, L::LDA, Tb + 8 * (nt0 + q),
-                                 L::LDA, lane);
-                    store_tile(Xb + 16 * mt * L::LDX + 8 * (nt0 + q), L::LDX, c4, lane, 1.f);
-                }
+                TRACE(1, j, 9, t == 0);
+                fence_proxy_async_smem();
+                tc_fence_before();
                 named_bar(2, 128);
-#pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    float c4[4];
-                    tile_mma<32>(c4, Tb + (32 + 16 * mt) * L::LDA + 32, L::LDA,
-                                 Xb + 8 * (nt0 + q), L::LDX, lane);
-                    store_tile(Tb + (32 + 16 * mt) * L::LDA + 8 * (nt0 + q), L::LDA, c4, lane,
-                               -1.f);
-                }
+                if (t == 0) mbar_arrive(bar + B_GFREE);
+                TRACE(1, j, 3, t == 0);
             }
-            named_bar(2, 128);
-            {
-                // T_u = T diag(beta) (rows 0-63), T_w = T diag(beta gamma) (rows 64-127)
-                const int r = t & 63;
-                uint8_t *TT = sm + L::OFF_TT;
-                const float *Tr = Tb + r * L::LDA;
-#pragma unroll
-                for (int c0 = 0; c0 < kC; c0 += 16) {
-                    float x[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int sidx = c0 + i;
-                        float sc = gj[64 + sidx];
-                        if (t >= 64) sc *= gj[128 + sidx];
-                        x[i] = sidx <= r ? Tr[sidx] * sc : 0.f;
-                    }
-                    put_row16(TT, t, c0, x);
-                }
-            }
-            fence_proxy_async_smem();
-            named_bar(2, 128);
-            if (t == 0) mbar_arrive(bar + B_T);
-            // (d) gamma-scaled Q into the chain operand (after the previous
-            //     chain MMA has read it)
-            if (!named_bar_and(2, 128, j == 0 || ctl.wait(B_M2, (j - 1) & 1))) break;
+            bool ok = true;
+            // (c) the chain operand [W; gamma Q] is free once the previous chain
+            //     MMA has read it: warps 4-5 write gamma*Q, warps 6-7 (TMEM lanes
+            //     64-127) write the W rows as soon as the WY MMA is done.
+            if (!named_bar_and(2, 128, ok && (j == 0 || ctl.wait(B_M2, (j - 1) & 1)))) break;
+            TRACE(1, j, 4, t == 0);
+            bool okw = true;
             if (t < 64) {
                 const float gam = gj[128 + t];
 #pragma unroll
@@ -531,150 +509,167 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
                         st16(dst + off, wv[0], wv[1], wv[2], wv[3]);
                     }
                 }
-            }
-            // (e) W rows (TMEM lanes 64-127) into the chain operand
-            if (!named_bar_and(2, 128, ctl.wait(B_UW, j & 1))) break;
-            tc_fence_after();
-            if (t >= 64) {
-                const int r = t - 64;
+            } else {
+                okw = named_bar_and(3, 64, ctl.wait(B_UW, j & 1));
+                if (okw) {
+                    tc_fence_after();
+                    const int r = t - 64;
 #pragma unroll
-                for (int blk = 0; blk < L::KB; ++blk) {
-                    uint8_t *dst = sm + L::OFF_WQ + blk * 16384;
+                    for (int blk = 0; blk < L::KB; ++blk) {
+                        uint8_t *dst = sm + L::OFF_WQ + blk * 16384;
+                        uint32_t w0[32], w1[32];
+                        tmem_ld32(tmem + lane_base + TM_W + blk * 64, w0);
+                        tmem_ld32(tmem + lane_base + TM_W + blk * 64 + 32, w1);
+                        tmem_wait32(w0);
+                        tmem_wait32(w1);
+                        float x[8];
 #pragma unroll
-                    for (int c0 = 0; c0 < 64; c0 += 16) {
-                        float x[16];
-                        tmem_ld16f(tmem + lane_base + TM_W + blk * 64 + c0, x);
-                        put_row16(dst, r, c0, x);
+                        for (int ch = 0; ch < 8; ++ch) {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+                                x[e] = f32(ch < 4 ? w0[8 * ch + e] : w1[8 * (ch - 4) + e]);
+                            put8(dst, r, ch, x);
+                        }
                     }
                 }
             }
             fence_proxy_async_smem();
             tc_fence_before();
-            named_bar(2, 128);
+            if (!named_bar_and(2, 128, okw)) break;
             if (t == 0) {
                 mbar_arrive(bar + B_WQ);
                 mbar_arrive(bar + B_FREE + s);
             }
+            TRACE(1, j, 5, t == 0);
         }
     } else if (warp == 8) {
         // ================================================= TMA producer
+        // lane 0 issues the bulk tensor copies; all lanes stage the chunk's
+        // gates (log_alpha, beta; zero past the sequence) next to them
         if (lane == 0) {
             prefetch_tmap(&tm_q);
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_v);
-            int issued = 0;
-            for (int j = 0; j < nch; ++j) {
-                const int s = j % kNS;
-                if (j >= kNS && !ctl.wait(B_FREE + s, ((j / kNS) - 1) & 1)) break;
-                uint8_t *stg = sm + L::OFF_STAGE + s * L::STAGE;
-                uint64_t *fb = bar + B_FULL + s;
+            prefetch_tmap(&tm_t);
+        }
+        int issued = 0;
+        for (int j = 0; j < nch; ++j) {
+            const int s = j % kNS;
+            const bool ok = j < kNS || ctl.wait(B_FREE + s, ((j / kNS) - 1) & 1);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            uint8_t *stg = sm + L::OFF_STAGE + s * L::STAGE;
+            uint64_t *fb = bar + B_FULL + s;
+            const int y = ytok0 + j * kC;
+            if (lane == 0) {
                 mbar_arrive_expect_tx(fb, (uint32_t)L::STAGE);
-                const int y = ytok0 + j * kC;
 #pragma unroll
                 for (int blk = 0; blk < L::KB; ++blk) {
                     tma_load_3d(stg + blk * 16384, &tm_k, fb, blk * 64, y, zcoord);
                     tma_load_3d(stg + blk * 16384 + 8192, &tm_q, fb, blk * 64, y, zcoord);
                 }
                 tma_load_3d(stg + L::OFF_V, &tm_v, fb, dv0, y, zcoord);
-                issued = j + 1;
+                tma_load_3d(stg + L::OFF_TI, &tm_t, fb, 0, y, zcoord);
             }
-            // on abort, let copies still in flight land before the CTA exits
-            if (*abort_flag) {
-                for (int j = max(0, issued - kNS); j < issued; ++j)
-                    mbar_wait(bar + B_FULL + j % kNS, (j / kNS) & 1, ctl.limit);
+            {
+                float *gs = reinterpret_cast<float *>(sm + L::OFF_GS) + s * 128;
+                const long long r0 = row0 + (long long)j * kC;
+                const int Lj = min(kC, len - j * kC);
+                gs[lane] = lane < Lj ? __ldg(p.log_alpha + r0 + lane) : 0.f;
+                gs[32 + lane] = lane + 32 < Lj ? __ldg(p.log_alpha + r0 + lane + 32) : 0.f;
+                gs[64 + lane] = lane < Lj ? __ldg(p.beta + r0 + lane) : 0.f;
+                gs[96 + lane] = lane + 32 < Lj ? __ldg(p.beta + r0 + lane + 32) : 0.f;
+                mbar_arrive(fb);
             }
+            issued = j + 1;
         }
-    } else {
-        // ==================================================== MMA issuer
+        // on abort, let copies still in flight land before the CTA exits
+        if (lane == 0 && *abort_flag) {
+            for (int j = max(0, issued - kNS); j < issued; ++j)
+                mbar_wait(bar + B_FULL + j % kNS, (j / kNS) & 1, ctl.limit);
+        }
+    } else if (warp == 9) {
+        // ===================================== chain MMA issuer (and TMEM owner)
         if (lane == 0 && nch > 0) {
-            constexpr uint32_t idG = make_idesc_bf16(128, 64, false, false);   // [K;Q] K^T
-            constexpr uint32_t idU = make_idesc_bf16(128, 64, false, true);    // TT V
-            constexpr uint32_t idW = make_idesc_bf16(128, DK, false, true);    // TT K
             constexpr uint32_t idM2 = make_idesc_bf16(128, kNV, false, true);  // [W;gQ] H
             constexpr uint32_t idM3 = make_idesc_bf16(128, kNV, true, true);   // K^T V~
             constexpr uint32_t idM4 = make_idesc_bf16(128, kNV, false, true);  // [x;P] V'
             const uint32_t sbase = smem_u32(sm);
-            auto stage_addr = [&](int j) { return sbase + L::OFF_STAGE + (j % kNS) * L::STAGE; };
-            auto issue_m1 = [&](int j) {
-                const uint32_t st = stage_addr(j);
+            // descriptor bases; an operand at base + off is base_desc + (off >> 4)
+            const uint64_t dWQ = make_sdesc(sbase + L::OFF_WQ, 16, 1024, kSwizzle128B);
+            const uint64_t dH = make_sdesc(sbase + L::OFF_H, 16, 1024, kSwizzle128B);
+            const uint64_t dVT = make_sdesc(sbase + L::OFF_R0, 16, 1024, kSwizzle128B);
+            const uint64_t dVN = make_sdesc(sbase + L::OFF_R1, 16, 1024, kSwizzle128B);
+            const uint64_t dKT = make_sdesc(sbase + L::OFF_STAGE, 16384, 1024, kSwizzle128B);
+            for (int j = 0; j < nch; ++j) {
+                const uint32_t soff = (j % kNS) * L::STAGE;
+                const uint32_t acc = tmem + TM_M2 + (j & 1) * 64;
+                if (!ctl.spin(B_H, j & 1) || !ctl.spin(B_WQ, j & 1)) break;
+                TRACE(2, j, 0, true);
+                tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < DK / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                    mma_bf16(tmem + TM_G, make_sdesc(st + off, 16, 1024, kSwizzle128B),
-                             make_sdesc(st + off, 16, 1024, kSwizzle128B), idG, kk > 0);
+                    mma_bf16(acc, dWQ + (off >> 4), dH + (kk * 2048 >> 4), idM2, kk > 0);
                 }
-                mma_commit(bar + B_G);
-            };
-            auto issue_uw = [&](int j) {
-                const uint32_t st = stage_addr(j);
-                const uint32_t tt = sbase + L::OFF_TT;
+                mma_commit(bar + B_M2);
+                TRACE(2, j, 1, true);
+                if (!ctl.spin(B_VN, j & 1)) break;
+                TRACE(2, j, 2, true);
+                tc_fence_after();
+                const uint64_t dP = (j & 1) ? dVN : dVT;   // [x; P] starts at the region base
 #pragma unroll
                 for (int kk = 0; kk < kC / 16; ++kk) {
-                    const uint64_t a = make_sdesc(tt + kk * 32, 16, 1024, kSwizzle128B);
-                    mma_bf16(tmem + TM_U,
-                             a, make_sdesc(st + L::OFF_V + kk * 2048, 16, 1024, kSwizzle128B),
-                             idU, kk > 0);
-                    mma_bf16(tmem + TM_W,
-                             a, make_sdesc(st + kk * 2048, 16384, 1024, kSwizzle128B), idW,
-                             kk > 0);
+                    mma_bf16(tmem + TM_H, dKT + ((soff + kk * 2048) >> 4), dVT + (kk * 2048 >> 4),
+                             idM3, kk > 0);
+                    mma_bf16(acc, dP + (kk * 32 >> 4), dVN + (kk * 2048 >> 4), idM4, 1u);
                 }
-                mma_commit(bar + B_UW);
-            };
-            if (ctl.wait(B_READY, 0)) issue_m1(0);
-            if (ctl.wait(B_T, 0)) issue_uw(0);
-            for (int j = 0; j < nch; ++j) {
-                if (*abort_flag) break;
-                const uint32_t st = stage_addr(j);
-                // 1. chain MMA  [W; gamma Q] H
-                if (!ctl.wait(B_H, j & 1) || !ctl.wait(B_WQ, j & 1)) break;
-                tc_fence_after();
-                {
-                    const uint32_t wq = sbase + L::OFF_WQ, hs = sbase + L::OFF_H;
-#pragma unroll
-                    for (int kk = 0; kk < DK / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                        mma_bf16(tmem + TM_M2, make_sdesc(wq + off, 16, 1024, kSwizzle128B),
-                                 make_sdesc(hs + kk * 2048, 16, 1024, kSwizzle128B), idM2,
-                                 kk > 0);
-                    }
-                    mma_commit(bar + B_M2);
-                }
-                // 2. next chunk's Gram
-                if (j + 1 < nch) {
-                    if (!ctl.wait(B_READY + (j + 1) % kNS, ((j + 1) / kNS) & 1) ||
-                        !ctl.wait(B_GFREE, j & 1))
-                        break;
-                    tc_fence_after();
-                    issue_m1(j + 1);
-                }
-                // 3. dH = K^T V~ and O += P V'
-                if (!ctl.wait(B_VN, j & 1)) break;
-                tc_fence_after();
-                {
-                    const uint32_t vt = sbase + L::OFF_R0, vn = sbase + L::OFF_R1;
-                    const uint32_t pr = sbase + ((j & 1) ? L::OFF_R1 : L::OFF_R0);
-#pragma unroll
-                    for (int kk = 0; kk < kC / 16; ++kk) {
-                        mma_bf16(tmem + TM_H,
-                                 make_sdesc(st + kk * 2048, 16384, 1024, kSwizzle128B),
-                                 make_sdesc(vt + kk * 2048, 16, 1024, kSwizzle128B), idM3,
-                                 kk > 0);
-                        mma_bf16(tmem + TM_M2, make_sdesc(pr + kk * 32, 16, 1024, kSwizzle128B),
-                                 make_sdesc(vn + kk * 2048, 16, 1024, kSwizzle128B), idM4, 1u);
-                    }
-                    mma_commit(bar + B_M34);
-                    mma_commit(bar + B_FREE + (j % kNS));
-                }
-                // 4. next chunk's WY factors
-                if (j + 1 < nch) {
-                    if (!ctl.wait(B_T, (j + 1) & 1)) break;
-                    tc_fence_after();
-                    issue_uw(j + 1);
-                }
+                mma_commit(bar + B_M34);
+                mma_commit(bar + B_PFREE + (j & 1));
+                mma_commit(bar + B_FREE + (j % kNS));
+                TRACE(2, j, 3, true);
             }
             // every issued MMA has finished before TMEM is released
             mma_commit(bar + B_DRAIN);
             mbar_wait(bar + B_DRAIN, 0, ctl.limit);
+        }
+    } else {
+        // ============================================== prep MMA issuer
+        if (lane == 0 && nch > 0) {
+            constexpr uint32_t idG = make_idesc_bf16(64, 64, false, false);      // Q K^T
+            constexpr uint32_t idUW = make_idesc_bf16(128, DK + 64, false, true);  // TT [K|V]
+            const uint32_t sbase = smem_u32(sm);
+            const uint64_t dS = make_sdesc(sbase + L::OFF_STAGE, 16, 1024, kSwizzle128B);
+            const uint64_t dKV = make_sdesc(sbase + L::OFF_STAGE, 16384, 1024, kSwizzle128B);
+            const uint64_t dTT = make_sdesc(sbase + L::OFF_TT, 16, 1024, kSwizzle128B);
+            for (int j = 0; j < nch; ++j) {
+                const int s = j % kNS;
+                const uint32_t soff = s * L::STAGE;
+                if (!ctl.spin(B_READY + s, (j / kNS) & 1)) break;
+                if (j > 0 && !ctl.spin(B_GFREE, (j - 1) & 1)) break;
+                TRACE(3, j, 0, true);
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < DK / 16; ++kk) {
+                    const uint32_t off = soff + (kk >> 2) * 16384 + (kk & 3) * 32;
+                    mma_bf16(tmem + TM_G, dS + ((off + 8192) >> 4), dS + (off >> 4), idG, kk > 0);
+                }
+                mma_commit(bar + B_G);
+                TRACE(3, j, 1, true);
+                if (!ctl.spin(B_T, j & 1)) break;
+                if (j > 0 && !ctl.spin(B_VN, (j - 1) & 1)) break;   // U of j-1 consumed
+                TRACE(3, j, 2, true);
+                tc_fence_after();
+                // [K | V] as one MN-major operand: K blocks and the V tile sit
+                // 16 KiB apart in the stage
+#pragma unroll
+                for (int kk = 0; kk < kC / 16; ++kk)
+                    mma_bf16(tmem + TM_W, dTT + (kk * 32 >> 4), dKV + ((soff + kk * 2048) >> 4),
+                             idUW, kk > 0);
+                mma_commit(bar + B_UW);
+                TRACE(3, j, 3, true);
+            }
+            mma_commit(bar + B_DRAIN2);
+            mbar_wait(bar + B_DRAIN2, 0, ctl.limit);
         }
     }
     tc_fence_before();
@@ -729,13 +724,13 @@ bool device_is_sm10x() {
 }
 
 template <int DK>
-gdn_status launch_tc(const FwdArgs &a) {
+gdn_status launch_tc(const FwdArgs &a, const __nv_bfloat16 *Tin) {
     using L = Lay<DK>;
     const long long ydim = a.sm.cu ? a.sm.T_total : a.sm.T;
     const long long zdim = a.sm.cu ? a.sm.H : (long long)a.sm.N * a.sm.H;
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mq, mk, mv, mt;
     if (!make_map(&mq, a.q, DK, ydim, zdim) || !make_map(&mk, a.k, DK, ydim, zdim) ||
-        !make_map(&mv, a.v, a.dv, ydim, zdim))
+        !make_map(&mv, a.v, a.dv, ydim, zdim) || !make_map(&mt, Tin, 64, ydim, zdim))
         return GDN_ERR_CUDA;
     static bool attr_set = false;
     if (!attr_set) {
@@ -757,7 +752,7 @@ gdn_status launch_tc(const FwdArgs &a) {
     p.wait_limit = lim > 0 ? (uint32_t)(lim > 0x7fffffffLL ? 0x7fffffffLL : lim) : (1u << 22);
     dim3 grid(a.dv / kNV, a.sm.H, a.sm.N);
     const int slot = timer_begin(a.stream, "k_gdn_tc");
-    k_gdn_tc<DK><<<grid, kThreadsTC, L::ALLOC, a.stream>>>(mq, mk, mv, p);
+    k_gdn_tc<DK><<<grid, kThreadsTC, L::ALLOC, a.stream>>>(mq, mk, mv, mt, p);
     timer_end(slot, a.stream);
     count_launch();
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
@@ -777,7 +772,27 @@ bool tc_supported(const FwdArgs &a) {
 }
 
 gdn_status tc_forward(const FwdArgs &a) {
-    return a.dk == 128 ? launch_tc<128>(a) : launch_tc<64>(a);
+    // Scratch: T per token row (bf16, rows x 64) and, for packed batches, the
+    // (sequence, chunk) table; stream-ordered, released after the launches.
+    cudaStream_t st = a.stream;
+    __nv_bfloat16 *Tbuf = nullptr;
+    int2 *table = nullptr;
+    if (cudaMallocAsync((void **)&Tbuf, (size_t)a.rows * 64 * sizeof(__nv_bfloat16), st) !=
+        cudaSuccess)
+        return GDN_ERR_CUDA;
+    gdn_status rc = GDN_OK;
+    if (a.sm.cu) {
+        if (cudaMallocAsync((void **)&table, sizeof(int2) * (size_t)a.chunk_slots, st) !=
+            cudaSuccess)
+            rc = GDN_ERR_CUDA;
+        else
+            rc = enqueue_chunk_table(a, table);
+    }
+    if (rc == GDN_OK) rc = enqueue_tc_prep(a, table, Tbuf);
+    if (rc == GDN_OK) rc = a.dk == 128 ? launch_tc<128>(a, Tbuf) : launch_tc<64>(a, Tbuf);
+    cudaFreeAsync(Tbuf, st);
+    if (table) cudaFreeAsync(table, st);
+    return rc;
 }
 
 }  // namespace gdn
