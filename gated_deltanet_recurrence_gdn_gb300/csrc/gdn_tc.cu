@@ -128,6 +128,14 @@ struct TcParams {
     int *err;
     int dv;
     uint32_t wait_limit;
+    // Segment scan (dense batches): sequence n = b * segs + segment, covering
+    // tokens [segment * seglen, min(T, (segment + 1) * seglen)); segs = 0: off.
+    int segs, seglen;
+    int no_output;   // 1: skip o (state-only pass)
+    // CTAs with blockIdx.x >= xsplit run the map's linear part instead: v = 0,
+    // h0 = identity (d_k x d_k state), final state into hT2 with width dv2.
+    int xsplit, dv2;
+    float *hT2;
 };
 
 struct Ctl {
@@ -185,12 +193,15 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
     float *gb = reinterpret_cast<float *>(sm + L::OFF_G);   // [2][GSZ]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int dv0 = blockIdx.x * kNV, h = blockIdx.y, n = blockIdx.z;
+    const int dv0 = ((int)blockIdx.x >= p.xsplit ? (int)blockIdx.x - p.xsplit : (int)blockIdx.x) *
+                    kNV;
+    const int h = blockIdx.y, n = blockIdx.z;
 
     // ---- sequence bounds (validated; an invalid packed range is an error)
     long long row0 = 0;
     int len = 0;
     bool ok_seq = true;
+    int ytok0 = 0, zcoord = 0;   // bulk-copy coordinates of chunk 0
     if (p.sm.cu) {
         const int a = __ldg(p.sm.cu + n), b = __ldg(p.sm.cu + n + 1);
         ok_seq = a >= 0 && a <= b && b <= p.sm.T_total;
@@ -198,18 +209,29 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
             row0 = (long long)h * p.sm.T_total + a;
             len = b - a;
         }
+        ytok0 = a;
+        zcoord = h;
+    } else if (p.segs > 0) {
+        const int b = n / p.segs, sg = n - b * p.segs;
+        const int t0 = sg * p.seglen;
+        row0 = ((long long)b * p.sm.H + h) * (long long)p.sm.T + t0;
+        len = max(0, min(p.seglen, p.sm.T - t0));
+        ytok0 = t0;
+        zcoord = b * p.sm.H + h;
     } else {
         row0 = ((long long)n * p.sm.H + h) * (long long)p.sm.T;
         len = p.sm.T;
+        zcoord = n * p.sm.H + h;
     }
     if (!ok_seq) {
         if (tid == 0) atomicCAS(p.err, 0, kErrSeqlens);
         return;  // before any barrier or TMEM use
     }
-    const int ytok0 = p.sm.cu ? __ldg(p.sm.cu + n) : 0;   // token coordinate of chunk 0
-    const int zcoord = p.sm.cu ? h : n * p.sm.H + h;
     const int nch = (len + kC - 1) / kC;
-    const long long srow = ((long long)n * p.sm.H + h) * p.dv;   // state row of (n, h)
+    const bool lin = (int)blockIdx.x >= p.xsplit;        // linear-part CTA (v = 0, h0 = I)
+    const int dvs = lin ? p.dv2 : p.dv;                  // width of this CTA's state
+    float *hTp = lin ? p.hT2 : p.hT;
+    const long long srow = ((long long)n * p.sm.H + h) * dvs;   // state row of (n, h)
 
     if (warp == 9) {
         tmem_alloc(misc, 512);
@@ -235,7 +257,8 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
         float hreg[kNV];
 #pragma unroll
         for (int c = 0; c < kNV; ++c)
-            hreg[c] = (t < DK && p.h0) ? __ldg(p.h0 + (srow + dv0 + c) * DK + t) : 0.f;
+            hreg[c] = lin ? ((t < DK && dv0 + c == t) ? 1.f : 0.f)
+                          : ((t < DK && p.h0) ? __ldg(p.h0 + (srow + dv0 + c) * DK + t) : 0.f);
         uint8_t *Hs = sm + L::OFF_H;
         uint8_t *VT = sm + L::OFF_R0, *VN = sm + L::OFF_R1;
         // Output rows of chunk jj (lanes 64-127 of its accumulator) to global.
@@ -276,7 +299,7 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
             if (t == 0) mbar_arrive(bar + B_H);
             TRACE(0, j, 1, t == 0);
             // (i') previous chunk's output rows, off the state's critical path
-            if (j > 0 && t >= 64) store_o(j - 1);
+            if (j > 0 && t >= 64 && !p.no_output && !lin) store_o(j - 1);
             TRACE(0, j, 2, t == 64);
             // (ii) V' = U - W H, and its decayed copy for the state update
             {
@@ -340,16 +363,23 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
                 }
             }
         }
-        if (alive && nch > 0 && t >= 64) store_o(nch - 1);
-        if (alive && p.hT && t < DK) {
+        if (alive && nch > 0 && t >= 64 && !p.no_output && !lin) store_o(nch - 1);
+        if (alive && hTp && t < DK) {
 #pragma unroll
-            for (int c = 0; c < kNV; ++c) p.hT[(srow + dv0 + c) * DK + t] = hreg[c];
+            for (int c = 0; c < kNV; ++c) hTp[(srow + dv0 + c) * DK + t] = hreg[c];
         }
     } else if (warp < 8) {
         // ================================================== prep warpgroup
         const int t = tid - 128;
         const int w = warp - 4;
         const uint32_t lane_base = (uint32_t)(w * 32) << 16;
+        if (lin) {
+            // v = 0: the V tiles are never loaded, so clear them once
+            for (int i = t; i < kNS * 512; i += 128)
+                st16(sm + L::OFF_STAGE + (i >> 9) * L::STAGE + L::OFF_V + (i & 511) * 16, 0u, 0u,
+                     0u, 0u);
+            fence_proxy_async_smem();
+        }
         for (int j = 0; j < nch; ++j) {
             const int s = j % kNS;
             uint8_t *stg = sm + L::OFF_STAGE + s * L::STAGE;
@@ -561,13 +591,13 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
             uint64_t *fb = bar + B_FULL + s;
             const int y = ytok0 + j * kC;
             if (lane == 0) {
-                mbar_arrive_expect_tx(fb, (uint32_t)L::STAGE);
+                mbar_arrive_expect_tx(fb, (uint32_t)(lin ? L::STAGE - 8192 : L::STAGE));
 #pragma unroll
                 for (int blk = 0; blk < L::KB; ++blk) {
                     tma_load_3d(stg + blk * 16384, &tm_k, fb, blk * 64, y, zcoord);
                     tma_load_3d(stg + blk * 16384 + 8192, &tm_q, fb, blk * 64, y, zcoord);
                 }
-                tma_load_3d(stg + L::OFF_V, &tm_v, fb, dv0, y, zcoord);
+                if (!lin) tma_load_3d(stg + L::OFF_V, &tm_v, fb, dv0, y, zcoord);
                 tma_load_3d(stg + L::OFF_TI, &tm_t, fb, 0, y, zcoord);
             }
             {
@@ -723,8 +753,22 @@ bool device_is_sm10x() {
     return major == 10;
 }
 
+// One launch of the fused kernel.  `seq` says how the grid's z axis maps to
+// token ranges (plain batch, or b * segs + segment); `lin_tiles` > 0 adds CTAs
+// that compute the segments' linear parts (v = 0, h0 = I) into hT2.
+struct LaunchCfg {
+    int nseq;             // grid.z
+    int segs, seglen;     // segment scan view (segs = 0: off)
+    int no_output;
+    const float *h0;
+    float *hT;
+    int lin_tiles;
+    float *hT2;
+    bool timed;
+};
+
 template <int DK>
-gdn_status launch_tc(const FwdArgs &a, const __nv_bfloat16 *Tin) {
+gdn_status launch_tc(const FwdArgs &a, const __nv_bfloat16 *Tin, const LaunchCfg &c) {
     using L = Lay<DK>;
     const long long ydim = a.sm.cu ? a.sm.T_total : a.sm.T;
     const long long zdim = a.sm.cu ? a.sm.H : (long long)a.sm.N * a.sm.H;
@@ -743,19 +787,155 @@ gdn_status launch_tc(const FwdArgs &a, const __nv_bfloat16 *Tin) {
     p.sm = a.sm;
     p.log_alpha = a.log_alpha;
     p.beta = a.beta;
-    p.h0 = a.h0;
+    p.h0 = c.h0;
     p.o = static_cast<__nv_bfloat16 *>(a.o);
-    p.hT = a.hT;
+    p.hT = c.hT;
     p.err = device_error_word();
     p.dv = a.dv;
     const long long lim = option(GDN_OPT_WAIT_LIMIT);
     p.wait_limit = lim > 0 ? (uint32_t)(lim > 0x7fffffffLL ? 0x7fffffffLL : lim) : (1u << 22);
-    dim3 grid(a.dv / kNV, a.sm.H, a.sm.N);
-    const int slot = timer_begin(a.stream, "k_gdn_tc");
+    p.segs = c.segs;
+    p.seglen = c.seglen;
+    p.no_output = c.no_output;
+    p.xsplit = a.dv / kNV;
+    p.dv2 = DK;
+    p.hT2 = c.hT2;
+    dim3 grid(a.dv / kNV + c.lin_tiles, a.sm.H, c.nseq);
+    const int slot = c.timed ? timer_begin(a.stream, "k_gdn_tc") : -1;
     k_gdn_tc<DK><<<grid, kThreadsTC, L::ALLOC, a.stream>>>(mq, mk, mv, mt, p);
     timer_end(slot, a.stream);
     count_launch();
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+// Exclusive fold of the segment maps ("Gated DeltaNet GPU并行实现", sections
+// 2.3 and 3.3): with S -> S A_i + B_i the map of segment i (earlier map
+// first), the state entering segment i+1 is S_in[i] A_i + B_i, S_in[0] = h0.
+// One CTA per (batch, head, 16 state rows), fp32.
+__global__ void __launch_bounds__(256)
+k_seg_fold(const float *__restrict__ h0, const float *__restrict__ Aseg,
+           const float *__restrict__ Bseg, float *__restrict__ Sin, int B, int H, int segs,
+           int dv, int dk) {
+    extern __shared__ float Sr[];   // [16][dk]
+    const int tid = threadIdx.x;
+    const int bh = blockIdx.x, b = bh / H, h = bh - b * H, r0 = blockIdx.y * 16;
+    const int tot = 16 * dk;
+    for (int i = tid; i < tot; i += 256) {
+        const int r = i / dk, cc = i - r * dk;
+        Sr[i] = h0 ? h0[((long long)bh * dv + r0 + r) * dk + cc] : 0.f;
+    }
+    __syncthreads();
+    for (int sg = 0; sg < segs; ++sg) {
+        const long long n = (long long)b * segs + sg;
+        for (int i = tid; i < tot; i += 256) {
+            const int r = i / dk, cc = i - r * dk;
+            Sin[((n * H + h) * dv + r0 + r) * dk + cc] = Sr[i];
+        }
+        if (sg == segs - 1) break;
+        const long long m = (long long)b * (segs - 1) + sg;
+        const float *Am = Aseg + (m * H + h) * (long long)dk * dk;
+        const float *Bm = Bseg + ((m * H + h) * dv + r0) * (long long)dk;
+        float acc[8];   // 16 * dk / 256 <= 8 entries per thread
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const int i = tid + 256 * e;
+            if (i < tot) {
+                const int r = i / dk, cc = i - r * dk;
+                float x = Bm[(long long)r * dk + cc];
+                for (int kk = 0; kk < dk; ++kk) x = fmaf(Sr[r * dk + kk], Am[kk * dk + cc], x);
+                acc[e] = x;
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const int i = tid + 256 * e;
+            if (i < tot) Sr[i] = acc[e];
+        }
+        __syncthreads();
+    }
+}
+
+int sm_count() {
+    static int n = 0;
+    if (n == 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            n = 148;
+    }
+    return n;
+}
+
+// Number of sequence segments for the segment scan (1 = none).  Automatic:
+// dense batches whose (batch, head, d_v tile) count leaves most SMs idle and
+// that have enough chunks per sequence.
+int choose_segments(const FwdArgs &a) {
+    if (a.sm.cu) return 1;
+    const int nch = a.max_chunks;
+    const long long opt = option(GDN_OPT_SEGMENTS);
+    int S;
+    if (opt >= 1) {
+        S = (int)opt;
+    } else {
+        const long long base = (long long)a.sm.N * a.sm.H * (a.dv / kNV);
+        if (base * 3 > sm_count() || nch < 64) return 1;
+        const long long per = (long long)a.sm.N * a.sm.H * (a.dv / kNV + a.dk / kNV);
+        S = 1 + (int)(sm_count() / per);
+    }
+    S = max(1, min(S, nch));
+    return S;
+}
+
+gdn_status tc_segmented(const FwdArgs &a, const __nv_bfloat16 *Tbuf, int S) {
+    cudaStream_t st = a.stream;
+    const int nch = a.max_chunks;
+    const int seglen = ((nch + S - 1) / S) * kC;
+    S = (a.sm.T + seglen - 1) / seglen;   // no empty segments
+    const int B = a.sm.N, H = a.sm.H, dv = a.dv, dk = a.dk;
+    if (S < 2 || (long long)B * S > 65535) {
+        LaunchCfg c{B, 0, 0, 0, a.h0, a.hT, 0, nullptr, true};
+        return dk == 128 ? launch_tc<128>(a, Tbuf, c) : launch_tc<64>(a, Tbuf, c);
+    }
+    const size_t st_dv = (size_t)H * dv * dk, st_dk = (size_t)H * dk * dk;
+    float *Aseg = nullptr, *Bseg = nullptr, *Sin = nullptr, *Hout = nullptr;
+    gdn_status rc = GDN_OK;
+    if (cudaMallocAsync((void **)&Aseg, sizeof(float) * st_dk * B * (S - 1), st) != cudaSuccess ||
+        cudaMallocAsync((void **)&Bseg, sizeof(float) * st_dv * B * (S - 1), st) != cudaSuccess ||
+        cudaMallocAsync((void **)&Sin, sizeof(float) * st_dv * B * S, st) != cudaSuccess ||
+        (a.hT && cudaMallocAsync((void **)&Hout, sizeof(float) * st_dv * B * S, st) != cudaSuccess))
+        rc = GDN_ERR_CUDA;
+    if (rc == GDN_OK) {
+        // pass 1: per segment but the last, the map's affine part (final state
+        // from zero) and linear part (final state from the identity, v = 0)
+        LaunchCfg c1{B * (S - 1), S - 1, seglen, 1, nullptr, Bseg, dk / kNV, Aseg, false};
+        rc = dk == 128 ? launch_tc<128>(a, Tbuf, c1) : launch_tc<64>(a, Tbuf, c1);
+    }
+    if (rc == GDN_OK) {
+        // pass 2: fold the maps into every segment's initial state
+        dim3 grid(B * H, dv / 16);
+        k_seg_fold<<<grid, 256, 16 * dk * sizeof(float), st>>>(a.h0, Aseg, Bseg, Sin, B, H, S,
+                                                               dv, dk);
+        count_launch();
+        if (cudaGetLastError() != cudaSuccess) rc = GDN_ERR_CUDA;
+    }
+    if (rc == GDN_OK) {
+        // pass 3: every segment from its true initial state, with outputs
+        LaunchCfg c3{B * S, S, seglen, 0, Sin, Hout, 0, nullptr, true};
+        rc = dk == 128 ? launch_tc<128>(a, Tbuf, c3) : launch_tc<64>(a, Tbuf, c3);
+    }
+    if (rc == GDN_OK && a.hT) {
+        for (int b = 0; b < B && rc == GDN_OK; ++b)
+            if (cudaMemcpyAsync(a.hT + (size_t)b * st_dv, Hout + ((size_t)b * S + S - 1) * st_dv,
+                                sizeof(float) * st_dv, cudaMemcpyDeviceToDevice,
+                                st) != cudaSuccess)
+                rc = GDN_ERR_CUDA;
+    }
+    if (Aseg) cudaFreeAsync(Aseg, st);
+    if (Bseg) cudaFreeAsync(Bseg, st);
+    if (Sin) cudaFreeAsync(Sin, st);
+    if (Hout) cudaFreeAsync(Hout, st);
+    return rc;
 }
 
 }  // namespace
@@ -789,7 +969,13 @@ gdn_status tc_forward(const FwdArgs &a) {
             rc = enqueue_chunk_table(a, table);
     }
     if (rc == GDN_OK) rc = enqueue_tc_prep(a, table, Tbuf);
-    if (rc == GDN_OK) rc = a.dk == 128 ? launch_tc<128>(a, Tbuf) : launch_tc<64>(a, Tbuf);
+    const int S = choose_segments(a);
+    if (rc == GDN_OK && S > 1) {
+        rc = tc_segmented(a, Tbuf, S);
+    } else if (rc == GDN_OK) {
+        LaunchCfg c{a.sm.N, 0, 0, 0, a.h0, a.hT, 0, nullptr, true};
+        rc = a.dk == 128 ? launch_tc<128>(a, Tbuf, c) : launch_tc<64>(a, Tbuf, c);
+    }
     cudaFreeAsync(Tbuf, st);
     if (table) cudaFreeAsync(table, st);
     return rc;
