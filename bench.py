@@ -61,13 +61,18 @@ def parse():
 
 
 def dist_setup(n_gpus):
+    """One process per GPU (torchrun env).  NCCL on GPUs; gloo when there is
+    no GPU (the CPU tests of this path)."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        else:
+            dist.init_process_group("gloo")
     elif torch.cuda.is_available():
         torch.cuda.set_device(0)
     return world, rank, local
@@ -80,12 +85,20 @@ def barrier(world):
 
 
 def max_over_ranks(x, world):
+    """Largest value over all ranks (the slowest rank's time)."""
     if world <= 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(tokens_per_rank, world, step_ms):
+    """Whole-job tokens/s: every rank runs its own replica of the workload
+    (weak scaling), timed by the slowest rank."""
+    return tokens_per_rank * world / (step_ms * 1e-3)
 
 
 def workload_shape(name):
@@ -303,7 +316,7 @@ def run_ours(args, world, rank, local):
     achieved = by / (kern_ms * 1e-3) / 1e9
     res = {
         "metric": METRIC,
-        "value": shape["tokens"] * world / (step_ms * 1e-3),
+        "value": job_throughput(shape["tokens"], world, step_ms),
         "unit": UNIT,
         "n_gpus": world,
         "steps": args.steps,
@@ -328,7 +341,7 @@ def run_ours(args, world, rank, local):
                      "algorithmic_bytes": by, "algorithmic_flops": flops,
                      "tensor_frac_of_peak": flops / (kern_ms * 1e-3) / (tf * 1e12)},
         "clocks": clocks.summary(),
-        "e2e": {"value": shape["tokens"] * world / (e2e_ms * 1e-3), "unit": UNIT,
+        "e2e": {"value": job_throughput(shape["tokens"], world, e2e_ms), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms},
         "gpu_launches": launches,
