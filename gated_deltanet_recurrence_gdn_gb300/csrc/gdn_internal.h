@@ -71,8 +71,9 @@ gdn_status simt_forward_noalloc(const FwdArgs &a);
 // (unused slots get n = -1) and validates cu_seqlens.
 gdn_status enqueue_chunk_table(const FwdArgs &a, int2 *table);
 
-// Chunk-prep kernel of the tensor-core path: T = (I + A)^{-1} per chunk, bf16
-// rows [rows][64] in Tout (table: packed batches only, else nullptr).
+// Chunk-prep kernel of the tensor-core path: T = (I + A)^{-1} per chunk, written
+// as bf16 rows [rows][128] = [T diag(beta) | T diag(beta gamma)] into Tout
+// (table: packed batches only, else nullptr).
 size_t tc_prep_smem(int dk);
 gdn_status enqueue_tc_prep(const FwdArgs &a, const int2 *table, __nv_bfloat16 *Tout);
 

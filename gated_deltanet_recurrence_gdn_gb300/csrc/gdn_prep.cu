@@ -7,13 +7,14 @@
 //   A_rs = beta_r exp(g_r - g_s) (k_r . k_s)   for s < r, else 0
 //   T    = (I + A)^{-1}
 //
-// T is the matrix that turns the chunk's delta-rule updates into the WY form
-// used by the fused kernel (U = T diag(beta) V, W = T diag(beta gamma) K); it
-// depends on no state, so all chunks are independent ("Gated DeltaNet GPU并行实现",
-// section 3.2: everything inside a chunk is parallel, only the state pass is
-// serial).  T is written as bf16 rows indexed like the token rows of the
-// inputs, [rows][64], so the fused kernel loads a chunk's T with the same kind
-// of bulk tensor copy as K.
+// T turns the chunk's delta-rule updates into the WY form used by the fused
+// kernel, U = T diag(beta) V and W = T diag(beta gamma) K; it depends on no
+// state, so all chunks are independent ("Gated DeltaNet GPU并行实现", section
+// 3.2: everything inside a chunk is parallel, only the state pass is serial).
+// The kernel writes the two column-scaled copies T_u = T diag(beta) and
+// T_w = T diag(beta gamma) as bf16 rows indexed like the token rows of the
+// inputs, [rows][128] = [T_u row | T_w row], so the fused kernel loads them
+// with the same kind of bulk tensor copy as K.
 //
 // Arithmetic: the Gram runs on bf16 mma.sync tiles with fp32 accumulation
 // (the inputs are bf16 already); the inverse solves the four 16x16 diagonal
@@ -35,13 +36,16 @@ constexpr int LDX = 36;
 template <int DK>
 struct PrepLay {
     static constexpr int LDK = DK + 8;                   // bf16 row stride of the K tile
+    static constexpr int KBYTES = kCp * LDK * 2;
+    static constexpr int TBYTES = kCp * LDA * 4;
+    // the K tile is dead once the Gram is formed: T reuses its space
     static constexpr int OFF_K = 0;
-    static constexpr int OFF_A = OFF_K + kCp * LDK * 2;  // fp32 [64][68]
-    static constexpr int OFF_T = OFF_A + kCp * LDA * 4;  // fp32 [64][68]
-    static constexpr int OFF_X = OFF_T + kCp * LDA * 4;  // fp32 [32][36]
+    static constexpr int OFF_T = 0;                      // fp32 [64][68]
+    static constexpr int OFF_A = (KBYTES > TBYTES ? KBYTES : TBYTES);   // fp32 [64][68]
+    static constexpr int OFF_X = OFF_A + TBYTES;         // fp32 [32][36]
     static constexpr int OFF_G = OFF_X + 32 * LDX * 4;   // g, beta, gamma, 1/gamma
     static constexpr int TOTAL = OFF_G + 4 * kCp * 4;
-    static_assert(OFF_A % 16 == 0 && OFF_T % 16 == 0 && OFF_X % 16 == 0, "align");
+    static_assert(OFF_A % 16 == 0 && OFF_X % 16 == 0, "align");
 };
 
 __device__ __forceinline__ float tf32(float x) {
@@ -277,17 +281,26 @@ k_gdn_prep(const __nv_bfloat16 *__restrict__ k, const float *__restrict__ log_al
     }
     __syncthreads();
 
-    // ---- T rows of the real tokens, bf16: thread = (row, 32-column half)
+    // ---- [T_u | T_w] rows of the real tokens, bf16: thread = (row, half),
+    //      half 0 writes T_u = T diag(beta), half 1 writes T_w = T diag(beta gamma)
     {
         const int r = tid >> 1, hf = tid & 1;
         if (r < Lc) {
-            const float4 *src = reinterpret_cast<const float4 *>(Tb + r * LDA + 32 * hf);
-            uint4 *dst = reinterpret_cast<uint4 *>(Tout + (r0 + r) * kCp + 32 * hf);
+            const float4 *src = reinterpret_cast<const float4 *>(Tb + r * LDA);
+            const float4 *sb = reinterpret_cast<const float4 *>(gs + 64);
+            const float4 *sg = reinterpret_cast<const float4 *>(gs + 128);
+            uint4 *dst = reinterpret_cast<uint4 *>(Tout + (r0 + r) * (2 * kCp) + kCp * hf);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
+            for (int q = 0; q < 8; ++q) {
                 const float4 a = src[2 * q], b = src[2 * q + 1];
-                dst[q] = make_uint4(pack2(a.x, a.y), pack2(a.z, a.w), pack2(b.x, b.y),
-                                    pack2(b.z, b.w));
+                float4 s0 = sb[2 * q], s1 = sb[2 * q + 1];
+                if (hf) {
+                    const float4 g0 = sg[2 * q], g1 = sg[2 * q + 1];
+                    s0 = make_float4(s0.x * g0.x, s0.y * g0.y, s0.z * g0.z, s0.w * g0.w);
+                    s1 = make_float4(s1.x * g1.x, s1.y * g1.y, s1.z * g1.z, s1.w * g1.w);
+                }
+                dst[q] = make_uint4(pack2(a.x * s0.x, a.y * s0.y), pack2(a.z * s0.z, a.w * s0.w),
+                                    pack2(b.x * s1.x, b.y * s1.y), pack2(b.z * s1.z, b.w * s1.w));
             }
         }
     }

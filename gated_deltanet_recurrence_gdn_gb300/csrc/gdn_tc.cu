@@ -79,7 +79,6 @@ enum {
     B_PFREE = B_FREE + kNS,     // + (chunk & 1): P buffer read by the output MMA
     B_G = B_PFREE + 2,          // Gram MMA done (G in TMEM)
     B_GFREE,                    // prep has read G
-    B_T,                        // T_u / T_w in smem
     B_UW,                       // U and W in TMEM
     B_WQ,                       // W and gamma*Q in smem
     B_M2,                       // chain MMA done
@@ -94,24 +93,27 @@ enum {
 template <int DK>
 struct Lay {
     static constexpr int KB = DK / 64;                 // 64-column blocks of K / Q / W
-    static constexpr int OFF_V = KB * 16384;           // stage: per block [K | Q], then V, T
-    static constexpr int OFF_TI = OFF_V + 8192;        // chunk's T = (I + A)^{-1}, bf16
-    static constexpr int STAGE = OFF_TI + 8192;
+    // One input stage (all tiles 64 rows x 128 B, 128-byte swizzled):
+    //   K blocks, then V (so [K | V] is one operand with 8 KiB block stride),
+    //   per block [W | Q] (so [W; gamma Q] is one 128-row operand; Q is scaled
+    //   in place once the Gram has read it), then [T_u; T_w] from the prep kernel.
+    static constexpr int OFF_V = KB * 8192;
+    static constexpr int OFF_WQ = OFF_V + 8192;
+    static constexpr int OFF_TT = OFF_WQ + KB * 16384;
+    static constexpr int STAGE = OFF_TT + 16384;
     static constexpr int OFF_STAGE = 0;
-    static constexpr int OFF_WQ = kNS * STAGE;         // per block [W | gamma Q]
-    static constexpr int OFF_H = OFF_WQ + KB * 16384;  // DK rows x 128 B
+    static constexpr int OFF_H = OFF_STAGE + kNS * STAGE;   // DK rows x 128 B
     static constexpr int OFF_R0 = OFF_H + DK * 128;    // [V~ | P0]
     static constexpr int OFF_R1 = OFF_R0 + 16384;      // [V' | P1]
-    static constexpr int OFF_TT = OFF_R1 + 16384;      // [T_u ; T_w], 128 rows x 128 B
     static constexpr int GSZ = 5 * 64;                 // g, beta, gamma, 1/gamma, beta*gamma
-    static constexpr int OFF_G = OFF_TT + 16384;       // 2 x GSZ floats
+    static constexpr int OFF_G = OFF_R1 + 16384;       // 2 x GSZ floats
     static constexpr int OFF_GS = OFF_G + 2 * GSZ * 4;  // per stage raw gates: log_alpha, beta
     static constexpr int OFF_BAR = OFF_GS + kNS * 128 * 4;
     static constexpr int OFF_MISC = OFF_BAR + B_COUNT * 8;
     static constexpr int TOTAL = OFF_MISC + 64;
     static constexpr int ALLOC = TOTAL + 1024;
-    static_assert(OFF_WQ % 1024 == 0 && OFF_H % 1024 == 0 && OFF_R0 % 1024 == 0, "align");
-    static_assert(OFF_TT % 1024 == 0 && OFF_G % 16 == 0, "align");
+    static_assert(OFF_WQ % 1024 == 0 && OFF_TT % 1024 == 0 && STAGE % 1024 == 0, "align");
+    static_assert(OFF_H % 1024 == 0 && OFF_R0 % 1024 == 0 && OFF_G % 16 == 0, "align");
     static_assert(ALLOC <= 227 * 1024, "shared memory budget");
 };
 
@@ -417,61 +419,82 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
             }
             if (p.sm.cu && L_ < kC) {
                 // rows past this sequence belong to the next one: clear them
-                constexpr int per_row = 2 * DK / 8 + 16;   // 16-byte pieces: K, Q, V, T
+                constexpr int per_row = 2 * DK / 8 + 24;   // 16-byte pieces: K, Q, V, T_u, T_w
                 for (int i = t; i < (kC - L_) * per_row; i += 128) {
                     const int r = L_ + i / per_row, q = i % per_row;
                     uint8_t *base;
-                    int chn;
-                    if (q < 2 * DK / 8) {
-                        const int blk = q / 16, which = (q / 8) & 1;   // per block: K, then Q
-                        base = stg + blk * 16384 + which * 8192;
-                        chn = q & 7;
-                    } else if (q < 2 * DK / 8 + 8) {
+                    if (q < DK / 8)  // K
+                        base = stg + (q >> 3) * 8192;
+                    else if (q < 2 * DK / 8)  // Q
+                        base = stg + L::OFF_WQ + ((q - DK / 8) >> 3) * 16384 + 8192;
+                    else if (q < 2 * DK / 8 + 8)  // V
                         base = stg + L::OFF_V;
-                        chn = q - 2 * DK / 8;
-                    } else {
-                        base = stg + L::OFF_TI;
-                        chn = q - 2 * DK / 8 - 8;
-                    }
-                    st16(base + sw128_offset(r, chn), 0u, 0u, 0u, 0u);
+                    else  // T_u, T_w
+                        base = stg + L::OFF_TT + ((q - 2 * DK / 8 - 8) >> 3) * 8192;
+                    st16(base + sw128_offset(r, q & 7), 0u, 0u, 0u, 0u);
                 }
                 fence_proxy_async_smem();
             }
             named_bar(2, 128);
             if (t == 0) mbar_arrive(bar + B_READY + s);
-            {
-                // (b) T_u = T diag(beta) (TT rows 0-63), T_w = T diag(beta gamma)
-                //     (TT rows 64-127) from the chunk's T, same swizzled positions
-                const int r = t & 63;
-                const uint8_t *Ti = stg + L::OFF_TI;
-                uint8_t *TT = sm + L::OFF_TT;
-                const float4 *sc = reinterpret_cast<const float4 *>(gj + (t < 64 ? 64 : 256));
+            // (b) the chain operand [W; gamma Q] of this stage: warps 6-7 (TMEM
+            //     lanes 64-127) write the W rows once the WY MMA is done, warps
+            //     4-5 scale Q by gamma in place once the Gram has read it
+            bool okb;
+            if (t >= 64) {
+                okb = named_bar_and(3, 64, ctl.wait(B_UW, j & 1));
+                if (okb) {
+                    tc_fence_after();
+                    const int r = t - 64;
 #pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
-                    const uint4 v = *reinterpret_cast<const uint4 *>(Ti + sw128_offset(r, ch));
-                    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-                    float x[8];
+                    for (int blk = 0; blk < L::KB; ++blk) {
+                        uint8_t *dst = stg + L::OFF_WQ + blk * 16384;
+                        uint32_t w0[32], w1[32];
+                        tmem_ld32(tmem + lane_base + TM_W + blk * 64, w0);
+                        tmem_ld32(tmem + lane_base + TM_W + blk * 64 + 32, w1);
+                        tmem_wait32(w0);
+                        tmem_wait32(w1);
+                        float x[8];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 f2 = __bfloat1622float2(
-                            *reinterpret_cast<const __nv_bfloat162 *>(&wv[e]));
-                        x[2 * e] = f2.x;
-                        x[2 * e + 1] = f2.y;
+                        for (int ch = 0; ch < 8; ++ch) {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+                                x[e] = f32(ch < 4 ? w0[8 * ch + e] : w1[8 * (ch - 4) + e]);
+                            put8(dst, r, ch, x);
+                        }
                     }
-                    const float4 c0 = sc[2 * ch], c1 = sc[2 * ch + 1];
-                    st16(TT + sw128_offset(t, ch), pack_bf16(x[0] * c0.x, x[1] * c0.y),
-                         pack_bf16(x[2] * c0.z, x[3] * c0.w), pack_bf16(x[4] * c1.x, x[5] * c1.y),
-                         pack_bf16(x[6] * c1.z, x[7] * c1.w));
                 }
-                TRACE(1, j, 7, t == 0);
-                fence_proxy_async_smem();
-                named_bar(2, 128);
-                if (t == 0) mbar_arrive(bar + B_T);
-                TRACE(1, j, 2, t == 0);
+            } else {
+                okb = named_bar_and(4, 64, ctl.wait(B_G, j & 1));
+                if (okb) {
+                    const float gam = gj[128 + t];
+#pragma unroll
+                    for (int blk = 0; blk < L::KB; ++blk) {
+                        uint8_t *qs = stg + L::OFF_WQ + blk * 16384 + 8192;
+#pragma unroll
+                        for (int ch = 0; ch < 8; ++ch) {
+                            const uint32_t off = sw128_offset(t, ch);
+                            uint4 v = *reinterpret_cast<const uint4 *>(qs + off);
+                            uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                __nv_bfloat162 b2 = *reinterpret_cast<__nv_bfloat162 *>(&wv[e]);
+                                float2 f2 = __bfloat1622float2(b2);
+                                wv[e] = pack_bf16(f2.x * gam, f2.y * gam);
+                            }
+                            st16(qs + off, wv[0], wv[1], wv[2], wv[3]);
+                        }
+                    }
+                }
             }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            if (!named_bar_and(2, 128, okb)) break;
+            if (t == 0) mbar_arrive(bar + B_WQ);
+            TRACE(1, j, 5, t == 0);
             {
-                // (b') P = mask_{s<=r}(Q K^T) * exp(g_r - g_s).  The Q K^T MMA has
-                //      M = 64: row 16w + i sits in lane i (< 16) of warp w's lanes.
+                // (c) P = mask_{s<=r}(Q K^T) * exp(g_r - g_s).  The Q K^T MMA has
+                //     M = 64: row 16w + i sits in lane i (< 16) of warp w's lanes.
                 bool okg = ctl.wait(B_G, j & 1);
                 if (j >= 2) okg = okg && ctl.wait(B_PFREE + (j & 1), ((j - 2) >> 1) & 1);
                 if (!named_bar_and(2, 128, okg)) break;
@@ -509,68 +532,12 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
                 fence_proxy_async_smem();
                 tc_fence_before();
                 named_bar(2, 128);
-                if (t == 0) mbar_arrive(bar + B_GFREE);
+                if (t == 0) {
+                    mbar_arrive(bar + B_GFREE);
+                    mbar_arrive(bar + B_FREE + s);
+                }
                 TRACE(1, j, 3, t == 0);
             }
-            bool ok = true;
-            // (c) the chain operand [W; gamma Q] is free once the previous chain
-            //     MMA has read it: warps 4-5 write gamma*Q, warps 6-7 (TMEM lanes
-            //     64-127) write the W rows as soon as the WY MMA is done.
-            if (!named_bar_and(2, 128, ok && (j == 0 || ctl.wait(B_M2, (j - 1) & 1)))) break;
-            TRACE(1, j, 4, t == 0);
-            bool okw = true;
-            if (t < 64) {
-                const float gam = gj[128 + t];
-#pragma unroll
-                for (int blk = 0; blk < L::KB; ++blk) {
-                    const uint8_t *src = stg + blk * 16384 + 8192;
-                    uint8_t *dst = sm + L::OFF_WQ + blk * 16384 + 8192;
-#pragma unroll
-                    for (int ch = 0; ch < 8; ++ch) {
-                        const uint32_t off = sw128_offset(t, ch);
-                        uint4 v = *reinterpret_cast<const uint4 *>(src + off);
-                        uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            __nv_bfloat162 b2 = *reinterpret_cast<__nv_bfloat162 *>(&wv[e]);
-                            float2 f2 = __bfloat1622float2(b2);
-                            wv[e] = pack_bf16(f2.x * gam, f2.y * gam);
-                        }
-                        st16(dst + off, wv[0], wv[1], wv[2], wv[3]);
-                    }
-                }
-            } else {
-                okw = named_bar_and(3, 64, ctl.wait(B_UW, j & 1));
-                if (okw) {
-                    tc_fence_after();
-                    const int r = t - 64;
-#pragma unroll
-                    for (int blk = 0; blk < L::KB; ++blk) {
-                        uint8_t *dst = sm + L::OFF_WQ + blk * 16384;
-                        uint32_t w0[32], w1[32];
-                        tmem_ld32(tmem + lane_base + TM_W + blk * 64, w0);
-                        tmem_ld32(tmem + lane_base + TM_W + blk * 64 + 32, w1);
-                        tmem_wait32(w0);
-                        tmem_wait32(w1);
-                        float x[8];
-#pragma unroll
-                        for (int ch = 0; ch < 8; ++ch) {
-#pragma unroll
-                            for (int e = 0; e < 8; ++e)
-                                x[e] = f32(ch < 4 ? w0[8 * ch + e] : w1[8 * (ch - 4) + e]);
-                            put8(dst, r, ch, x);
-                        }
-                    }
-                }
-            }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            if (!named_bar_and(2, 128, okw)) break;
-            if (t == 0) {
-                mbar_arrive(bar + B_WQ);
-                mbar_arrive(bar + B_FREE + s);
-            }
-            TRACE(1, j, 5, t == 0);
         }
     } else if (warp == 8) {
         // ================================================= TMA producer
@@ -591,14 +558,17 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
             uint64_t *fb = bar + B_FULL + s;
             const int y = ytok0 + j * kC;
             if (lane == 0) {
-                mbar_arrive_expect_tx(fb, (uint32_t)(lin ? L::STAGE - 8192 : L::STAGE));
+                // K, Q, V and [T_u; T_w] tiles arrive; the W halves are written locally
+                mbar_arrive_expect_tx(fb, (uint32_t)(L::STAGE - L::KB * 8192 - (lin ? 8192 : 0)));
 #pragma unroll
                 for (int blk = 0; blk < L::KB; ++blk) {
-                    tma_load_3d(stg + blk * 16384, &tm_k, fb, blk * 64, y, zcoord);
-                    tma_load_3d(stg + blk * 16384 + 8192, &tm_q, fb, blk * 64, y, zcoord);
+                    tma_load_3d(stg + blk * 8192, &tm_k, fb, blk * 64, y, zcoord);
+                    tma_load_3d(stg + L::OFF_WQ + blk * 16384 + 8192, &tm_q, fb, blk * 64, y,
+                                zcoord);
                 }
                 if (!lin) tma_load_3d(stg + L::OFF_V, &tm_v, fb, dv0, y, zcoord);
-                tma_load_3d(stg + L::OFF_TI, &tm_t, fb, 0, y, zcoord);
+                tma_load_3d(stg + L::OFF_TT, &tm_t, fb, 0, y, zcoord);
+                tma_load_3d(stg + L::OFF_TT + 8192, &tm_t, fb, 64, y, zcoord);
             }
             {
                 float *gs = reinterpret_cast<float *>(sm + L::OFF_GS) + s * 128;
@@ -625,11 +595,12 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
             constexpr uint32_t idM4 = make_idesc_bf16(128, kNV, false, true);  // [x;P] V'
             const uint32_t sbase = smem_u32(sm);
             // descriptor bases; an operand at base + off is base_desc + (off >> 4)
-            const uint64_t dWQ = make_sdesc(sbase + L::OFF_WQ, 16, 1024, kSwizzle128B);
+            const uint64_t dWQ = make_sdesc(sbase + L::OFF_STAGE + L::OFF_WQ, 16, 1024,
+                                            kSwizzle128B);
             const uint64_t dH = make_sdesc(sbase + L::OFF_H, 16, 1024, kSwizzle128B);
             const uint64_t dVT = make_sdesc(sbase + L::OFF_R0, 16, 1024, kSwizzle128B);
             const uint64_t dVN = make_sdesc(sbase + L::OFF_R1, 16, 1024, kSwizzle128B);
-            const uint64_t dKT = make_sdesc(sbase + L::OFF_STAGE, 16384, 1024, kSwizzle128B);
+            const uint64_t dKT = make_sdesc(sbase + L::OFF_STAGE, 8192, 1024, kSwizzle128B);
             for (int j = 0; j < nch; ++j) {
                 const uint32_t soff = (j % kNS) * L::STAGE;
                 const uint32_t acc = tmem + TM_M2 + (j & 1) * 64;
@@ -638,7 +609,7 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < DK / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                    const uint32_t off = soff + (kk >> 2) * 16384 + (kk & 3) * 32;
                     mma_bf16(acc, dWQ + (off >> 4), dH + (kk * 2048 >> 4), idM2, kk > 0);
                 }
                 mma_commit(bar + B_M2);
@@ -669,33 +640,34 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
             constexpr uint32_t idUW = make_idesc_bf16(128, DK + 64, false, true);  // TT [K|V]
             const uint32_t sbase = smem_u32(sm);
             const uint64_t dS = make_sdesc(sbase + L::OFF_STAGE, 16, 1024, kSwizzle128B);
-            const uint64_t dKV = make_sdesc(sbase + L::OFF_STAGE, 16384, 1024, kSwizzle128B);
-            const uint64_t dTT = make_sdesc(sbase + L::OFF_TT, 16, 1024, kSwizzle128B);
+            const uint64_t dKV = make_sdesc(sbase + L::OFF_STAGE, 8192, 1024, kSwizzle128B);
+            const uint64_t dTT = make_sdesc(sbase + L::OFF_STAGE + L::OFF_TT, 16, 1024,
+                                            kSwizzle128B);
             for (int j = 0; j < nch; ++j) {
                 const int s = j % kNS;
                 const uint32_t soff = s * L::STAGE;
                 if (!ctl.spin(B_READY + s, (j / kNS) & 1)) break;
-                if (j > 0 && !ctl.spin(B_GFREE, (j - 1) & 1)) break;
+                if (j > 0 && !ctl.spin(B_VN, (j - 1) & 1)) break;   // U of j-1 consumed
                 TRACE(3, j, 0, true);
+                tc_fence_after();
+                // [K | V] as one MN-major operand: K blocks and the V tile sit
+                // 8 KiB apart in the stage
+#pragma unroll
+                for (int kk = 0; kk < kC / 16; ++kk)
+                    mma_bf16(tmem + TM_W, dTT + ((soff + kk * 32) >> 4),
+                             dKV + ((soff + kk * 2048) >> 4), idUW, kk > 0);
+                mma_commit(bar + B_UW);
+                TRACE(3, j, 1, true);
+                if (j > 0 && !ctl.spin(B_GFREE, (j - 1) & 1)) break;
+                TRACE(3, j, 2, true);
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < DK / 16; ++kk) {
-                    const uint32_t off = soff + (kk >> 2) * 16384 + (kk & 3) * 32;
-                    mma_bf16(tmem + TM_G, dS + ((off + 8192) >> 4), dS + (off >> 4), idG, kk > 0);
+                    const uint32_t kof = soff + (kk >> 2) * 8192 + (kk & 3) * 32;
+                    const uint32_t qof = soff + L::OFF_WQ + (kk >> 2) * 16384 + 8192 + (kk & 3) * 32;
+                    mma_bf16(tmem + TM_G, dS + (qof >> 4), dS + (kof >> 4), idG, kk > 0);
                 }
                 mma_commit(bar + B_G);
-                TRACE(3, j, 1, true);
-                if (!ctl.spin(B_T, j & 1)) break;
-                if (j > 0 && !ctl.spin(B_VN, (j - 1) & 1)) break;   // U of j-1 consumed
-                TRACE(3, j, 2, true);
-                tc_fence_after();
-                // [K | V] as one MN-major operand: K blocks and the V tile sit
-                // 16 KiB apart in the stage
-#pragma unroll
-                for (int kk = 0; kk < kC / 16; ++kk)
-                    mma_bf16(tmem + TM_W, dTT + (kk * 32 >> 4), dKV + ((soff + kk * 2048) >> 4),
-                             idUW, kk > 0);
-                mma_commit(bar + B_UW);
                 TRACE(3, j, 3, true);
             }
             mma_commit(bar + B_DRAIN2);
@@ -774,7 +746,7 @@ gdn_status launch_tc(const FwdArgs &a, const __nv_bfloat16 *Tin, const LaunchCfg
     const long long zdim = a.sm.cu ? a.sm.H : (long long)a.sm.N * a.sm.H;
     CUtensorMap mq, mk, mv, mt;
     if (!make_map(&mq, a.q, DK, ydim, zdim) || !make_map(&mk, a.k, DK, ydim, zdim) ||
-        !make_map(&mv, a.v, a.dv, ydim, zdim) || !make_map(&mt, Tin, 64, ydim, zdim))
+        !make_map(&mv, a.v, a.dv, ydim, zdim) || !make_map(&mt, Tin, 128, ydim, zdim))
         return GDN_ERR_CUDA;
     static bool attr_set = false;
     if (!attr_set) {
@@ -952,12 +924,12 @@ bool tc_supported(const FwdArgs &a) {
 }
 
 gdn_status tc_forward(const FwdArgs &a) {
-    // Scratch: T per token row (bf16, rows x 64) and, for packed batches, the
+    // Scratch: [T_u | T_w] per token row (bf16, rows x 128) and, for packed batches, the
     // (sequence, chunk) table; stream-ordered, released after the launches.
     cudaStream_t st = a.stream;
     __nv_bfloat16 *Tbuf = nullptr;
     int2 *table = nullptr;
-    if (cudaMallocAsync((void **)&Tbuf, (size_t)a.rows * 64 * sizeof(__nv_bfloat16), st) !=
+    if (cudaMallocAsync((void **)&Tbuf, (size_t)a.rows * 128 * sizeof(__nv_bfloat16), st) !=
         cudaSuccess)
         return GDN_ERR_CUDA;
     gdn_status rc = GDN_OK;
