@@ -71,11 +71,13 @@ gdn_status simt_forward_noalloc(const FwdArgs &a);
 // (unused slots get n = -1) and validates cu_seqlens.
 gdn_status enqueue_chunk_table(const FwdArgs &a, int2 *table);
 
-// Chunk-prep kernel of the tensor-core path: T = (I + A)^{-1} per chunk, written
-// as bf16 rows [rows][128] = [T diag(beta) | T diag(beta gamma)] into Tout
+// Chunk-prep kernel of the tensor-core path: with T = (I + A)^{-1} per chunk,
+// writes T diag(beta) as bf16 rows [rows][64] into Tu and
+// W = T diag(beta gamma) K as bf16 rows [rows][d_k] into W
 // (table: packed batches only, else nullptr).
 size_t tc_prep_smem(int dk);
-gdn_status enqueue_tc_prep(const FwdArgs &a, const int2 *table, __nv_bfloat16 *Tout);
+gdn_status enqueue_tc_prep(const FwdArgs &a, const int2 *table, __nv_bfloat16 *Tu,
+                           __nv_bfloat16 *W);
 
 // tcgen05 tensor-core path (bf16 I/O).  Returns GDN_ERR_UNSUPPORTED when the
 // call does not fit it; the caller then decides whether to fall back.

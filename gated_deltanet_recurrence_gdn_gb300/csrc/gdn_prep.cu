@@ -8,13 +8,13 @@
 //   T    = (I + A)^{-1}
 //
 // T turns the chunk's delta-rule updates into the WY form used by the fused
-// kernel, U = T diag(beta) V and W = T diag(beta gamma) K; it depends on no
-// state, so all chunks are independent ("Gated DeltaNet GPU并行实现", section
-// 3.2: everything inside a chunk is parallel, only the state pass is serial).
-// The kernel writes the two column-scaled copies T_u = T diag(beta) and
-// T_w = T diag(beta gamma) as bf16 rows indexed like the token rows of the
-// inputs, [rows][128] = [T_u row | T_w row], so the fused kernel loads them
-// with the same kind of bulk tensor copy as K.
+// kernel, U = T diag(beta) V and W = T diag(beta gamma) K; neither depends on
+// the state, so all chunks are independent ("Gated DeltaNet GPU并行实现",
+// section 3.2: everything inside a chunk is parallel, only the state pass is
+// serial).  The kernel writes T_u = T diag(beta) ([rows][64]) and
+// W = T diag(beta gamma) K ([rows][d_k]) as bf16 rows indexed like the token
+// rows of the inputs, so the fused kernel loads them with the same kind of
+// bulk tensor copy as K.
 //
 // Arithmetic: the Gram runs on bf16 mma.sync tiles with fp32 accumulation
 // (the inputs are bf16 already); the inverse solves the four 16x16 diagonal
@@ -38,10 +38,11 @@ struct PrepLay {
     static constexpr int LDK = DK + 8;                   // bf16 row stride of the K tile
     static constexpr int KBYTES = kCp * LDK * 2;
     static constexpr int TBYTES = kCp * LDA * 4;
-    // the K tile is dead once the Gram is formed: T reuses its space
+    // K stays for W = T_w K; once T is final, A's space holds bf16 T_w and
+    // T's space holds the bf16 W tile on its way out
     static constexpr int OFF_K = 0;
-    static constexpr int OFF_T = 0;                      // fp32 [64][68]
-    static constexpr int OFF_A = (KBYTES > TBYTES ? KBYTES : TBYTES);   // fp32 [64][68]
+    static constexpr int OFF_T = KBYTES;                 // fp32 [64][68]
+    static constexpr int OFF_A = OFF_T + TBYTES;         // fp32 [64][68]
     static constexpr int OFF_X = OFF_A + TBYTES;         // fp32 [32][36]
     static constexpr int OFF_G = OFF_X + 32 * LDX * 4;   // g, beta, gamma, 1/gamma
     static constexpr int TOTAL = OFF_G + 4 * kCp * 4;
@@ -113,7 +114,8 @@ template <int DK>
 __global__ void __launch_bounds__(128)
 k_gdn_prep(const __nv_bfloat16 *__restrict__ k, const float *__restrict__ log_alpha,
            const float *__restrict__ beta, SeqMap sm, const int2 *__restrict__ table,
-           int max_chunks, __nv_bfloat16 *__restrict__ Tout, int *err) {
+           int max_chunks, __nv_bfloat16 *__restrict__ Tu_out, __nv_bfloat16 *__restrict__ W_out,
+           int *err) {
     using L = PrepLay<DK>;
     extern __shared__ __align__(16) uint8_t smem[];
     __nv_bfloat16 *Ks = reinterpret_cast<__nv_bfloat16 *>(smem + L::OFF_K);
@@ -281,28 +283,83 @@ k_gdn_prep(const __nv_bfloat16 *__restrict__ k, const float *__restrict__ log_al
     }
     __syncthreads();
 
-    // ---- [T_u | T_w] rows of the real tokens, bf16: thread = (row, half),
-    //      half 0 writes T_u = T diag(beta), half 1 writes T_w = T diag(beta gamma)
+    // ---- T_u = T diag(beta) rows out (bf16), and T_w = T diag(beta gamma) as
+    //      the bf16 A operand of W = T_w K (in A's space, row stride LDK)
+    __nv_bfloat16 *Tw = reinterpret_cast<__nv_bfloat16 *>(smem + L::OFF_A);
     {
         const int r = tid >> 1, hf = tid & 1;
-        if (r < Lc) {
-            const float4 *src = reinterpret_cast<const float4 *>(Tb + r * LDA);
-            const float4 *sb = reinterpret_cast<const float4 *>(gs + 64);
-            const float4 *sg = reinterpret_cast<const float4 *>(gs + 128);
-            uint4 *dst = reinterpret_cast<uint4 *>(Tout + (r0 + r) * (2 * kCp) + kCp * hf);
+        const float4 *src = reinterpret_cast<const float4 *>(Tb + r * LDA + 32 * hf);
+        const float4 *sb = reinterpret_cast<const float4 *>(gs + 64 + 32 * hf);
+        const float4 *sg = reinterpret_cast<const float4 *>(gs + 128 + 32 * hf);
+        uint32_t u[16], wv[16];
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const float4 a = src[2 * q], b = src[2 * q + 1];
-                float4 s0 = sb[2 * q], s1 = sb[2 * q + 1];
-                if (hf) {
-                    const float4 g0 = sg[2 * q], g1 = sg[2 * q + 1];
-                    s0 = make_float4(s0.x * g0.x, s0.y * g0.y, s0.z * g0.z, s0.w * g0.w);
-                    s1 = make_float4(s1.x * g1.x, s1.y * g1.y, s1.z * g1.z, s1.w * g1.w);
-                }
-                dst[q] = make_uint4(pack2(a.x * s0.x, a.y * s0.y), pack2(a.z * s0.z, a.w * s0.w),
-                                    pack2(b.x * s1.x, b.y * s1.y), pack2(b.z * s1.z, b.w * s1.w));
-            }
+        for (int q = 0; q < 4; ++q) {
+            const float4 a = src[2 * q], b = src[2 * q + 1];
+            const float4 s0 = sb[2 * q], s1 = sb[2 * q + 1];
+            const float4 g0 = sg[2 * q], g1 = sg[2 * q + 1];
+            u[4 * q] = pack2(a.x * s0.x, a.y * s0.y);
+            u[4 * q + 1] = pack2(a.z * s0.z, a.w * s0.w);
+            u[4 * q + 2] = pack2(b.x * s1.x, b.y * s1.y);
+            u[4 * q + 3] = pack2(b.z * s1.z, b.w * s1.w);
+            wv[4 * q] = pack2(a.x * s0.x * g0.x, a.y * s0.y * g0.y);
+            wv[4 * q + 1] = pack2(a.z * s0.z * g0.z, a.w * s0.w * g0.w);
+            wv[4 * q + 2] = pack2(b.x * s1.x * g1.x, b.y * s1.y * g1.y);
+            wv[4 * q + 3] = pack2(b.z * s1.z * g1.z, b.w * s1.w * g1.w);
         }
+        if (r < Lc) {
+            uint4 *dst = reinterpret_cast<uint4 *>(Tu_out + (r0 + r) * kCp + 32 * hf);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                dst[q] = make_uint4(u[4 * q], u[4 * q + 1], u[4 * q + 2], u[4 * q + 3]);
+        }
+        uint4 *tw = reinterpret_cast<uint4 *>(Tw + r * L::LDK + 32 * hf);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            tw[q] = make_uint4(wv[4 * q], wv[4 * q + 1], wv[4 * q + 2], wv[4 * q + 3]);
+    }
+    __syncthreads();
+    // ---- W = T_w K (64 x d_k): warp w owns rows 16w..16w+15; bf16 mma.sync,
+    //      fp32 accumulation, result staged as bf16 in T's space
+    __nv_bfloat16 *Ws = reinterpret_cast<__nv_bfloat16 *>(smem + L::OFF_T);
+    {
+        const int g = lane >> 2, t = lane & 3;
+        const int ra = 16 * w + g, rb = ra + 8;
+        uint32_t af[4][4];
+#pragma unroll
+        for (int kq = 0; kq < 4; ++kq) {
+            const int k0 = 16 * kq;
+            af[kq][0] = *reinterpret_cast<const uint32_t *>(Tw + ra * L::LDK + k0 + 2 * t);
+            af[kq][1] = *reinterpret_cast<const uint32_t *>(Tw + rb * L::LDK + k0 + 2 * t);
+            af[kq][2] = *reinterpret_cast<const uint32_t *>(Tw + ra * L::LDK + k0 + 2 * t + 8);
+            af[kq][3] = *reinterpret_cast<const uint32_t *>(Tw + rb * L::LDK + k0 + 2 * t + 8);
+        }
+        const unsigned short *Ku = reinterpret_cast<const unsigned short *>(Ks);
+#pragma unroll
+        for (int nt = 0; nt < DK / 8; ++nt) {
+            const int n = 8 * nt + g;
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int kq = 0; kq < 4; ++kq) {
+                const int k0 = 16 * kq;
+                uint32_t b[2];
+                b[0] = (uint32_t)Ku[(k0 + 2 * t) * L::LDK + n] |
+                       ((uint32_t)Ku[(k0 + 2 * t + 1) * L::LDK + n] << 16);
+                b[1] = (uint32_t)Ku[(k0 + 2 * t + 8) * L::LDK + n] |
+                       ((uint32_t)Ku[(k0 + 2 * t + 9) * L::LDK + n] << 16);
+                mma_bf16x16(acc, af[kq], b);
+            }
+            const int col = 8 * nt + 2 * t;
+            *reinterpret_cast<uint32_t *>(Ws + ra * L::LDK + col) = pack2(acc[0], acc[1]);
+            *reinterpret_cast<uint32_t *>(Ws + rb * L::LDK + col) = pack2(acc[2], acc[3]);
+        }
+    }
+    __syncthreads();
+    // ---- W rows of the real tokens out, 16-byte vectors
+    for (int i = tid; i < kCp * (DK / 8); i += 128) {
+        const int r = i / (DK / 8), q = i % (DK / 8);
+        if (r < Lc)
+            *reinterpret_cast<uint4 *>(W_out + (r0 + r) * DK + 8 * q) =
+                *reinterpret_cast<const uint4 *>(Ws + r * L::LDK + 8 * q);
     }
 }
 
@@ -312,7 +369,8 @@ size_t tc_prep_smem(int dk) {
     return dk == 128 ? (size_t)PrepLay<128>::TOTAL : (size_t)PrepLay<64>::TOTAL;
 }
 
-gdn_status enqueue_tc_prep(const FwdArgs &a, const int2 *table, __nv_bfloat16 *Tout) {
+gdn_status enqueue_tc_prep(const FwdArgs &a, const int2 *table, __nv_bfloat16 *Tu,
+                           __nv_bfloat16 *W) {
     if (a.chunk_slots <= 0) return GDN_OK;
     int *err = device_error_word();
     const size_t smem = tc_prep_smem(a.dk);
@@ -323,13 +381,13 @@ gdn_status enqueue_tc_prep(const FwdArgs &a, const int2 *table, __nv_bfloat16 *T
                                  (int)smem) != cudaSuccess)
             return GDN_ERR_CUDA;
         k_gdn_prep<128><<<grid, 128, smem, a.stream>>>(k, a.log_alpha, a.beta, a.sm, table,
-                                                        a.max_chunks, Tout, err);
+                                                        a.max_chunks, Tu, W, err);
     } else {
         if (cudaFuncSetAttribute(k_gdn_prep<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem) != cudaSuccess)
             return GDN_ERR_CUDA;
         k_gdn_prep<64><<<grid, 128, smem, a.stream>>>(k, a.log_alpha, a.beta, a.sm, table,
-                                                       a.max_chunks, Tout, err);
+                                                       a.max_chunks, Tu, W, err);
     }
     count_launch();
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;

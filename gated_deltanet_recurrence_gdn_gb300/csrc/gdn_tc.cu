@@ -77,7 +77,8 @@ enum {
     B_READY = B_FULL + kNS,     // + stage: pad rows cleared, stage usable by MMA
     B_FREE = B_READY + kNS,     // + stage: consumers done (chain MMA commit + prep)
     B_PFREE = B_FREE + kNS,     // + (chunk & 1): P buffer read by the output MMA
-    B_G = B_PFREE + 2,          // Gram MMA done (G in TMEM)
+    B_PREADY = B_PFREE + 2,     // + (chunk & 1): P buffer written
+    B_G = B_PREADY + 2,         // Gram MMA done (G in TMEM)
     B_GFREE,                    // prep has read G
     B_UW,                       // U and W in TMEM
     B_WQ,                       // W and gamma*Q in smem
@@ -94,13 +95,13 @@ template <int DK>
 struct Lay {
     static constexpr int KB = DK / 64;                 // 64-column blocks of K / Q / W
     // One input stage (all tiles 64 rows x 128 B, 128-byte swizzled):
-    //   K blocks, then V (so [K | V] is one operand with 8 KiB block stride),
-    //   per block [W | Q] (so [W; gamma Q] is one 128-row operand; Q is scaled
-    //   in place once the Gram has read it), then [T_u; T_w] from the prep kernel.
+    //   K blocks, then V (so [K | V] would be one operand with 8 KiB block
+    //   stride and K^T is one MN-major operand), per block [W | Q] (so
+    //   [W; gamma Q] is one 128-row operand; Q is scaled in place), then T_u.
     static constexpr int OFF_V = KB * 8192;
     static constexpr int OFF_WQ = OFF_V + 8192;
-    static constexpr int OFF_TT = OFF_WQ + KB * 16384;
-    static constexpr int STAGE = OFF_TT + 16384;
+    static constexpr int OFF_TU = OFF_WQ + KB * 16384;
+    static constexpr int STAGE = OFF_TU + 8192;
     static constexpr int OFF_STAGE = 0;
     static constexpr int OFF_H = OFF_STAGE + kNS * STAGE;   // DK rows x 128 B
     static constexpr int OFF_R0 = OFF_H + DK * 128;    // [V~ | P0]
@@ -112,15 +113,14 @@ struct Lay {
     static constexpr int OFF_MISC = OFF_BAR + B_COUNT * 8;
     static constexpr int TOTAL = OFF_MISC + 64;
     static constexpr int ALLOC = TOTAL + 1024;
-    static_assert(OFF_WQ % 1024 == 0 && OFF_TT % 1024 == 0 && STAGE % 1024 == 0, "align");
+    static_assert(OFF_WQ % 1024 == 0 && OFF_TU % 1024 == 0 && STAGE % 1024 == 0, "align");
     static_assert(OFF_H % 1024 == 0 && OFF_R0 % 1024 == 0 && OFF_G % 16 == 0, "align");
     static_assert(ALLOC <= 227 * 1024, "shared memory budget");
 };
 
-// TMEM column map (512 allocated): G, two chain / output accumulators, dH, and
-// the WY product [T_u; T_w] [K | V]: W in its first d_k columns (lanes 64-127),
-// U in the next 64 (lanes 0-63).
-constexpr uint32_t TM_G = 0, TM_M2 = 128, TM_H = 256, TM_W = 320;
+// TMEM column map (512 allocated): [W; gamma Q] K^T (its lanes 64-127 hold
+// gamma Q K^T), two chain / output accumulators, dH, and U = T_u V (lanes 0-63).
+constexpr uint32_t TM_G = 0, TM_M2 = 64, TM_H = 192, TM_U = 256;
 
 struct TcParams {
     SeqMap sm;
@@ -185,7 +185,7 @@ template <int DK>
 __global__ void __launch_bounds__(kThreadsTC, 1)
 k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
          const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_t,
-         TcParams p) {
+         const __grid_constant__ CUtensorMap tm_w, TcParams p) {
     using L = Lay<DK>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -241,7 +241,7 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
     }
     if (tid == 0) {
         for (int i = 0; i < B_COUNT; ++i) mbar_init(bar + i, 1);
-        for (int s = 0; s < kNS; ++s) mbar_init(bar + B_FREE + s, 2);
+        for (int s = 0; s < kNS; ++s) mbar_init(bar + B_FREE + s, 3);   // chain MMA + 2 prep groups
         for (int s = 0; s < kNS; ++s) mbar_init(bar + B_FULL + s, 33);   // TMA tx + 32 gate lanes
         *abort_flag = 0;
         fence_mbar_init();
@@ -305,8 +305,9 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
             TRACE(0, j, 2, t == 64);
             // (ii) V' = U - W H, and its decayed copy for the state update
             {
-                bool ok = ctl.wait(B_WQ, j & 1);   // orders this chunk's gates too
-                ok = ok && ctl.wait(B_M2, j & 1);
+                // READY orders this chunk's gates; UW and M2 bring U and W H
+                bool ok = ctl.wait(B_READY + (j % kNS), (j / kNS) & 1);
+                ok = ok && ctl.wait(B_UW, j & 1) && ctl.wait(B_M2, j & 1);
                 if (!named_bar_and(1, 128, ok)) {
                     alive = false;
                     break;
@@ -324,7 +325,7 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
                 for (int half = 0; half < 2; ++half) {
                     uint32_t wh[32], u[32];
                     tmem_ld32(acc + 32 * half, wh);
-                    tmem_ld32(tmem + lane_base + TM_W + DK + 32 * half, u);
+                    tmem_ld32(tmem + lane_base + TM_U + 32 * half, u);
                     tmem_wait32(wh);
                     tmem_wait32(u);
                     float vn[32], vt[32];
@@ -371,102 +372,77 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
             for (int c = 0; c < kNV; ++c) hTp[(srow + dv0 + c) * DK + t] = hreg[c];
         }
     } else if (warp < 8) {
-        // ================================================== prep warpgroup
+        // ================================================== prep warpgroups
+        // Two independent 64-thread pipelines over the chunks:
+        //   warps 4-5: gates, clearing of packed-batch tails, gamma * Q in place
+        //              (before the Gram when the chunk's decay span allows, else
+        //              after it), publishing [W; gamma Q]
+        //   warps 6-7: P = causal decayed (Q K^T) from TMEM lanes 64-127
         const int t = tid - 128;
         const int w = warp - 4;
         const uint32_t lane_base = (uint32_t)(w * 32) << 16;
-        if (lin) {
-            // v = 0: the V tiles are never loaded, so clear them once
-            for (int i = t; i < kNS * 512; i += 128)
-                st16(sm + L::OFF_STAGE + (i >> 9) * L::STAGE + L::OFF_V + (i & 511) * 16, 0u, 0u,
-                     0u, 0u);
-            fence_proxy_async_smem();
-        }
-        for (int j = 0; j < nch; ++j) {
-            const int s = j % kNS;
-            uint8_t *stg = sm + L::OFF_STAGE + s * L::STAGE;
-            const int L_ = min(kC, len - j * kC);
-            float *gj = gb + (j & 1) * L::GSZ;   // g, beta, gamma, 1/gamma, beta*gamma
-            TRACE(1, j, 0, t == 0);
-            if (!named_bar_and(2, 128, ctl.wait(B_FULL + s, (j / kNS) & 1))) break;
-            TRACE(1, j, 1, t == 0);
-            // (a) in-chunk cumulative log gate from the staged gates
-            if (w == 0) {
-                const float *gs = reinterpret_cast<const float *>(sm + L::OFF_GS) + s * 128;
-                float la0 = gs[lane], la1 = gs[32 + lane];
-                const float b0 = gs[64 + lane], b1 = gs[96 + lane];
-#pragma unroll
-                for (int off = 1; off < 32; off <<= 1) {
-                    const float y0 = __shfl_up_sync(0xffffffffu, la0, off);
-                    const float y1 = __shfl_up_sync(0xffffffffu, la1, off);
-                    if (lane >= off) {
-                        la0 += y0;
-                        la1 += y1;
-                    }
-                }
-                la1 += __shfl_sync(0xffffffffu, la0, 31);
-                const float e0 = __expf(la0), e1 = __expf(la1);
-                gj[lane] = la0;
-                gj[lane + 32] = la1;
-                gj[64 + lane] = b0;
-                gj[64 + lane + 32] = b1;
-                gj[128 + lane] = e0;
-                gj[128 + lane + 32] = e1;
-                gj[192 + lane] = __expf(-la0);   // used only when the chunk's span is < 80
-                gj[192 + lane + 32] = __expf(-la1);
-                gj[256 + lane] = b0 * e0;
-                gj[256 + lane + 32] = b1 * e1;
-            }
-            if (p.sm.cu && L_ < kC) {
-                // rows past this sequence belong to the next one: clear them
-                constexpr int per_row = 2 * DK / 8 + 24;   // 16-byte pieces: K, Q, V, T_u, T_w
-                for (int i = t; i < (kC - L_) * per_row; i += 128) {
-                    const int r = L_ + i / per_row, q = i % per_row;
-                    uint8_t *base;
-                    if (q < DK / 8)  // K
-                        base = stg + (q >> 3) * 8192;
-                    else if (q < 2 * DK / 8)  // Q
-                        base = stg + L::OFF_WQ + ((q - DK / 8) >> 3) * 16384 + 8192;
-                    else if (q < 2 * DK / 8 + 8)  // V
-                        base = stg + L::OFF_V;
-                    else  // T_u, T_w
-                        base = stg + L::OFF_TT + ((q - 2 * DK / 8 - 8) >> 3) * 8192;
-                    st16(base + sw128_offset(r, q & 7), 0u, 0u, 0u, 0u);
-                }
+        if (t < 64) {
+            if (lin) {
+                // v = 0: the V tiles are never loaded, so clear them once
+                for (int i = t; i < kNS * 512; i += 64)
+                    st16(sm + L::OFF_STAGE + (i >> 9) * L::STAGE + L::OFF_V + (i & 511) * 16, 0u,
+                         0u, 0u, 0u);
                 fence_proxy_async_smem();
             }
-            named_bar(2, 128);
-            if (t == 0) mbar_arrive(bar + B_READY + s);
-            // (b) the chain operand [W; gamma Q] of this stage: warps 6-7 (TMEM
-            //     lanes 64-127) write the W rows once the WY MMA is done, warps
-            //     4-5 scale Q by gamma in place once the Gram has read it
-            bool okb;
-            if (t >= 64) {
-                okb = named_bar_and(3, 64, ctl.wait(B_UW, j & 1));
-                if (okb) {
-                    tc_fence_after();
-                    const int r = t - 64;
+            for (int j = 0; j < nch; ++j) {
+                const int s = j % kNS;
+                uint8_t *stg = sm + L::OFF_STAGE + s * L::STAGE;
+                const int L_ = min(kC, len - j * kC);
+                float *gj = gb + (j & 1) * L::GSZ;
+                TRACE(1, j, 0, t == 0);
+                if (!named_bar_and(4, 64, ctl.wait(B_FULL + s, (j / kNS) & 1))) break;
+                TRACE(1, j, 1, t == 0);
+                if (w == 0) {
+                    const float *gs = reinterpret_cast<const float *>(sm + L::OFF_GS) + s * 128;
+                    float la0 = gs[lane], la1 = gs[32 + lane];
+                    const float b0 = gs[64 + lane], b1 = gs[96 + lane];
 #pragma unroll
-                    for (int blk = 0; blk < L::KB; ++blk) {
-                        uint8_t *dst = stg + L::OFF_WQ + blk * 16384;
-                        uint32_t w0[32], w1[32];
-                        tmem_ld32(tmem + lane_base + TM_W + blk * 64, w0);
-                        tmem_ld32(tmem + lane_base + TM_W + blk * 64 + 32, w1);
-                        tmem_wait32(w0);
-                        tmem_wait32(w1);
-                        float x[8];
-#pragma unroll
-                        for (int ch = 0; ch < 8; ++ch) {
-#pragma unroll
-                            for (int e = 0; e < 8; ++e)
-                                x[e] = f32(ch < 4 ? w0[8 * ch + e] : w1[8 * (ch - 4) + e]);
-                            put8(dst, r, ch, x);
+                    for (int off = 1; off < 32; off <<= 1) {
+                        const float y0 = __shfl_up_sync(0xffffffffu, la0, off);
+                        const float y1 = __shfl_up_sync(0xffffffffu, la1, off);
+                        if (lane >= off) {
+                            la0 += y0;
+                            la1 += y1;
                         }
                     }
+                    la1 += __shfl_sync(0xffffffffu, la0, 31);
+                    const float e0 = __expf(la0), e1 = __expf(la1);
+                    gj[lane] = la0;
+                    gj[lane + 32] = la1;
+                    gj[64 + lane] = b0;
+                    gj[64 + lane + 32] = b1;
+                    gj[128 + lane] = e0;
+                    gj[128 + lane + 32] = e1;
+                    gj[192 + lane] = __expf(-la0);   // used only when the span is < 80
+                    gj[192 + lane + 32] = __expf(-la1);
+                    gj[256 + lane] = b0 * e0;
+                    gj[256 + lane + 32] = b1 * e1;
                 }
-            } else {
-                okb = named_bar_and(4, 64, ctl.wait(B_G, j & 1));
-                if (okb) {
+                if (p.sm.cu && L_ < kC) {
+                    // rows past this sequence belong to the next one: clear them
+                    constexpr int per_row = 3 * DK / 8 + 16;   // 16-byte pieces: K, W, Q, V, T_u
+                    for (int i = t; i < (kC - L_) * per_row; i += 64) {
+                        const int r = L_ + i / per_row, q = i % per_row;
+                        uint8_t *base;
+                        if (q < DK / 8)  // K
+                            base = stg + (q >> 3) * 8192;
+                        else if (q < 3 * DK / 8)  // W, Q blocks
+                            base = stg + L::OFF_WQ + ((q - DK / 8) >> 3) * 8192;
+                        else if (q < 3 * DK / 8 + 8)  // V
+                            base = stg + L::OFF_V;
+                        else  // T_u
+                            base = stg + L::OFF_TU;
+                        st16(base + sw128_offset(r, q & 7), 0u, 0u, 0u, 0u);
+                    }
+                }
+                named_bar(4, 64);
+                const bool span_ok = gj[63] > -80.f;
+                auto scale_q = [&]() {
                     const float gam = gj[128 + t];
 #pragma unroll
                     for (int blk = 0; blk < L::KB; ++blk) {
@@ -485,58 +461,70 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
                             st16(qs + off, wv[0], wv[1], wv[2], wv[3]);
                         }
                     }
+                };
+                if (span_ok) scale_q();
+                fence_proxy_async_smem();
+                named_bar(4, 64);
+                if (t == 0) mbar_arrive(bar + B_READY + s);
+                if (!span_ok) {
+                    // the Gram must read the unscaled Q first
+                    if (!named_bar_and(4, 64, ctl.wait(B_G, j & 1))) break;
+                    scale_q();
+                    fence_proxy_async_smem();
+                    named_bar(4, 64);
                 }
+                // publish [W; gamma Q] only once the previous chunk's chain MMA has
+                // read its own copy: the barrier then never runs two phases ahead
+                // of the chain MMA issuer waiting on it
+                if (!named_bar_and(4, 64, j == 0 || ctl.wait(B_M2, (j - 1) & 1))) break;
+                if (t == 0) mbar_arrive(bar + B_WQ);
+                if (t == 0) mbar_arrive(bar + B_FREE + s);
+                TRACE(1, j, 2, t == 0);
             }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            if (!named_bar_and(2, 128, okb)) break;
-            if (t == 0) mbar_arrive(bar + B_WQ);
-            TRACE(1, j, 5, t == 0);
-            {
-                // (c) P = mask_{s<=r}(Q K^T) * exp(g_r - g_s).  The Q K^T MMA has
-                //     M = 64: row 16w + i sits in lane i (< 16) of warp w's lanes.
-                bool okg = ctl.wait(B_G, j & 1);
+        } else {
+            for (int j = 0; j < nch; ++j) {
+                const int s = j % kNS;
+                float *gj = gb + (j & 1) * L::GSZ;
+                bool okg = ctl.wait(B_READY + s, (j / kNS) & 1);   // orders this chunk's gates
+                okg = okg && ctl.wait(B_G, j & 1);
                 if (j >= 2) okg = okg && ctl.wait(B_PFREE + (j & 1), ((j - 2) >> 1) & 1);
-                if (!named_bar_and(2, 128, okg)) break;
+                if (!named_bar_and(3, 64, okg)) break;
+                TRACE(1, j, 3, t == 64);
                 tc_fence_after();
-                const int r = 16 * w + (lane & 15);
+                const int r = t - 64;
                 uint32_t g0[32], g1[32];
                 tmem_ld32(tmem + lane_base + TM_G, g0);
                 tmem_ld32(tmem + lane_base + TM_G + 32, g1);
-                const float gC = gj[63];
-                const bool span_ok = gC > -80.f;
+                const bool span_ok = gj[63] > -80.f;
                 const float gr = gj[r];
-                const float fr = span_ok ? gj[128 + r] : 0.f;
                 uint8_t *Pt = sm + ((j & 1) ? L::OFF_R1 : L::OFF_R0) + 8192;
                 tmem_wait32(g0);
                 tmem_wait32(g1);
-                TRACE(1, j, 8, t == 0);
-                if (lane < 16) {
 #pragma unroll
-                    for (int half = 0; half < 2; ++half) {
-                        float x[32];
+                for (int half = 0; half < 2; ++half) {
+                    float x[32];
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            const int sidx = 32 * half + i;
-                            const float gv = f32(half == 0 ? g0[i] : g1[i]);
-                            const bool keep = sidx <= r;
-                            const float f = span_ok ? fr * gj[192 + sidx]
-                                                    : __expf(keep ? gr - gj[sidx] : 0.f);
-                            x[i] = keep ? f * gv : 0.f;
-                        }
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) put8(Pt, r, 4 * half + q, x + 8 * q);
+                    for (int i = 0; i < 32; ++i) {
+                        const int sidx = 32 * half + i;
+                        const float gv = f32(half == 0 ? g0[i] : g1[i]);
+                        const bool keep = sidx <= r;
+                        // span_ok: G already carries gamma_r (Q scaled before the Gram)
+                        const float f = span_ok ? gj[192 + sidx]
+                                                : __expf(keep ? gr - gj[sidx] : 0.f);
+                        x[i] = keep ? f * gv : 0.f;
                     }
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) put8(Pt, r, 4 * half + q, x + 8 * q);
                 }
-                TRACE(1, j, 9, t == 0);
                 fence_proxy_async_smem();
                 tc_fence_before();
-                named_bar(2, 128);
-                if (t == 0) {
+                named_bar(3, 64);
+                if (t == 64) {
+                    mbar_arrive(bar + B_PREADY + (j & 1));
                     mbar_arrive(bar + B_GFREE);
                     mbar_arrive(bar + B_FREE + s);
                 }
-                TRACE(1, j, 3, t == 0);
+                TRACE(1, j, 4, t == 64);
             }
         }
     } else if (warp == 8) {
@@ -548,6 +536,7 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_v);
             prefetch_tmap(&tm_t);
+            prefetch_tmap(&tm_w);
         }
         int issued = 0;
         for (int j = 0; j < nch; ++j) {
@@ -558,17 +547,17 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
             uint64_t *fb = bar + B_FULL + s;
             const int y = ytok0 + j * kC;
             if (lane == 0) {
-                // K, Q, V and [T_u; T_w] tiles arrive; the W halves are written locally
-                mbar_arrive_expect_tx(fb, (uint32_t)(L::STAGE - L::KB * 8192 - (lin ? 8192 : 0)));
+                // K, W, Q, V and T_u tiles
+                mbar_arrive_expect_tx(fb, (uint32_t)(L::STAGE - (lin ? 8192 : 0)));
 #pragma unroll
                 for (int blk = 0; blk < L::KB; ++blk) {
                     tma_load_3d(stg + blk * 8192, &tm_k, fb, blk * 64, y, zcoord);
+                    tma_load_3d(stg + L::OFF_WQ + blk * 16384, &tm_w, fb, blk * 64, y, zcoord);
                     tma_load_3d(stg + L::OFF_WQ + blk * 16384 + 8192, &tm_q, fb, blk * 64, y,
                                 zcoord);
                 }
                 if (!lin) tma_load_3d(stg + L::OFF_V, &tm_v, fb, dv0, y, zcoord);
-                tma_load_3d(stg + L::OFF_TT, &tm_t, fb, 0, y, zcoord);
-                tma_load_3d(stg + L::OFF_TT + 8192, &tm_t, fb, 64, y, zcoord);
+                tma_load_3d(stg + L::OFF_TU, &tm_t, fb, 0, y, zcoord);
             }
             {
                 float *gs = reinterpret_cast<float *>(sm + L::OFF_GS) + s * 128;
@@ -604,7 +593,7 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
             for (int j = 0; j < nch; ++j) {
                 const uint32_t soff = (j % kNS) * L::STAGE;
                 const uint32_t acc = tmem + TM_M2 + (j & 1) * 64;
-                if (!ctl.spin(B_H, j & 1) || !ctl.spin(B_WQ, j & 1)) break;
+                if (!ctl.wait(B_H, j & 1) || !ctl.wait(B_WQ, j & 1)) break;
                 TRACE(2, j, 0, true);
                 tc_fence_after();
 #pragma unroll
@@ -614,7 +603,8 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
                 }
                 mma_commit(bar + B_M2);
                 TRACE(2, j, 1, true);
-                if (!ctl.spin(B_VN, j & 1)) break;
+                if (!ctl.wait(B_VN, j & 1)) break;
+                if (!ctl.wait(B_PREADY + (j & 1), (j >> 1) & 1)) break;   // P of this chunk
                 TRACE(2, j, 2, true);
                 tc_fence_after();
                 const uint64_t dP = (j & 1) ? dVN : dVT;   // [x; P] starts at the region base
@@ -636,36 +626,32 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
     } else {
         // ============================================== prep MMA issuer
         if (lane == 0 && nch > 0) {
-            constexpr uint32_t idG = make_idesc_bf16(64, 64, false, false);      // Q K^T
-            constexpr uint32_t idUW = make_idesc_bf16(128, DK + 64, false, true);  // TT [K|V]
+            constexpr uint32_t idG = make_idesc_bf16(128, 64, false, false);   // [W;gQ] K^T
+            constexpr uint32_t idU = make_idesc_bf16(128, 64, false, true);    // [T_u;x] V
             const uint32_t sbase = smem_u32(sm);
             const uint64_t dS = make_sdesc(sbase + L::OFF_STAGE, 16, 1024, kSwizzle128B);
-            const uint64_t dKV = make_sdesc(sbase + L::OFF_STAGE, 8192, 1024, kSwizzle128B);
-            const uint64_t dTT = make_sdesc(sbase + L::OFF_STAGE + L::OFF_TT, 16, 1024,
-                                            kSwizzle128B);
             for (int j = 0; j < nch; ++j) {
                 const int s = j % kNS;
                 const uint32_t soff = s * L::STAGE;
-                if (!ctl.spin(B_READY + s, (j / kNS) & 1)) break;
-                if (j > 0 && !ctl.spin(B_VN, (j - 1) & 1)) break;   // U of j-1 consumed
+                if (!ctl.wait(B_READY + s, (j / kNS) & 1)) break;
+                if (j > 0 && !ctl.wait(B_VN, (j - 1) & 1)) break;   // U of j-1 consumed
                 TRACE(3, j, 0, true);
                 tc_fence_after();
-                // [K | V] as one MN-major operand: K blocks and the V tile sit
-                // 8 KiB apart in the stage
+                // U = T_u V; rows 64-127 of the A operand are whatever follows T_u
 #pragma unroll
                 for (int kk = 0; kk < kC / 16; ++kk)
-                    mma_bf16(tmem + TM_W, dTT + ((soff + kk * 32) >> 4),
-                             dKV + ((soff + kk * 2048) >> 4), idUW, kk > 0);
+                    mma_bf16(tmem + TM_U, dS + ((soff + L::OFF_TU + kk * 32) >> 4),
+                             dS + ((soff + L::OFF_V + kk * 2048) >> 4), idU, kk > 0);
                 mma_commit(bar + B_UW);
                 TRACE(3, j, 1, true);
-                if (j > 0 && !ctl.spin(B_GFREE, (j - 1) & 1)) break;
+                if (j > 0 && !ctl.wait(B_GFREE, (j - 1) & 1)) break;
                 TRACE(3, j, 2, true);
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < DK / 16; ++kk) {
                     const uint32_t kof = soff + (kk >> 2) * 8192 + (kk & 3) * 32;
-                    const uint32_t qof = soff + L::OFF_WQ + (kk >> 2) * 16384 + 8192 + (kk & 3) * 32;
-                    mma_bf16(tmem + TM_G, dS + (qof >> 4), dS + (kof >> 4), idG, kk > 0);
+                    const uint32_t aof = soff + L::OFF_WQ + (kk >> 2) * 16384 + (kk & 3) * 32;
+                    mma_bf16(tmem + TM_G, dS + (aof >> 4), dS + (kof >> 4), idG, kk > 0);
                 }
                 mma_commit(bar + B_G);
                 TRACE(3, j, 3, true);
@@ -744,9 +730,11 @@ gdn_status launch_tc(const FwdArgs &a, const __nv_bfloat16 *Tin, const LaunchCfg
     using L = Lay<DK>;
     const long long ydim = a.sm.cu ? a.sm.T_total : a.sm.T;
     const long long zdim = a.sm.cu ? a.sm.H : (long long)a.sm.N * a.sm.H;
-    CUtensorMap mq, mk, mv, mt;
+    CUtensorMap mq, mk, mv, mt, mw;
+    const __nv_bfloat16 *Win = Tin + (size_t)a.rows * 64;
     if (!make_map(&mq, a.q, DK, ydim, zdim) || !make_map(&mk, a.k, DK, ydim, zdim) ||
-        !make_map(&mv, a.v, a.dv, ydim, zdim) || !make_map(&mt, Tin, 128, ydim, zdim))
+        !make_map(&mv, a.v, a.dv, ydim, zdim) || !make_map(&mt, Tin, 64, ydim, zdim) ||
+        !make_map(&mw, Win, DK, ydim, zdim))
         return GDN_ERR_CUDA;
     static bool attr_set = false;
     if (!attr_set) {
@@ -774,7 +762,7 @@ gdn_status launch_tc(const FwdArgs &a, const __nv_bfloat16 *Tin, const LaunchCfg
     p.hT2 = c.hT2;
     dim3 grid(a.dv / kNV + c.lin_tiles, a.sm.H, c.nseq);
     const int slot = c.timed ? timer_begin(a.stream, "k_gdn_tc") : -1;
-    k_gdn_tc<DK><<<grid, kThreadsTC, L::ALLOC, a.stream>>>(mq, mk, mv, mt, p);
+    k_gdn_tc<DK><<<grid, kThreadsTC, L::ALLOC, a.stream>>>(mq, mk, mv, mt, mw, p);
     timer_end(slot, a.stream);
     count_launch();
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
@@ -924,12 +912,13 @@ bool tc_supported(const FwdArgs &a) {
 }
 
 gdn_status tc_forward(const FwdArgs &a) {
-    // Scratch: [T_u | T_w] per token row (bf16, rows x 128) and, for packed batches, the
+    // Scratch: T_u (bf16, rows x 64) and W (bf16, rows x d_k) and, for packed batches, the
     // (sequence, chunk) table; stream-ordered, released after the launches.
     cudaStream_t st = a.stream;
     __nv_bfloat16 *Tbuf = nullptr;
     int2 *table = nullptr;
-    if (cudaMallocAsync((void **)&Tbuf, (size_t)a.rows * 128 * sizeof(__nv_bfloat16), st) !=
+    if (cudaMallocAsync((void **)&Tbuf, (size_t)a.rows * (64 + a.dk) * sizeof(__nv_bfloat16),
+                        st) !=
         cudaSuccess)
         return GDN_ERR_CUDA;
     gdn_status rc = GDN_OK;
@@ -940,7 +929,7 @@ gdn_status tc_forward(const FwdArgs &a) {
         else
             rc = enqueue_chunk_table(a, table);
     }
-    if (rc == GDN_OK) rc = enqueue_tc_prep(a, table, Tbuf);
+    if (rc == GDN_OK) rc = enqueue_tc_prep(a, table, Tbuf, Tbuf + (size_t)a.rows * 64);
     const int S = choose_segments(a);
     if (rc == GDN_OK && S > 1) {
         rc = tc_segmented(a, Tbuf, S);
