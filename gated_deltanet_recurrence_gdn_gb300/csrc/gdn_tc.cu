@@ -441,31 +441,42 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
                     }
                 }
                 named_bar(4, 64);
+                TRACE(1, j, 5, t == 0);
                 const bool span_ok = gj[63] > -80.f;
                 auto scale_q = [&]() {
+                    // row t of every Q block: all loads first, then all stores (a
+                    // store may alias a later load, so interleaving them would
+                    // serialise every round trip)
                     const float gam = gj[128 + t];
 #pragma unroll
                     for (int blk = 0; blk < L::KB; ++blk) {
                         uint8_t *qs = stg + L::OFF_WQ + blk * 16384 + 8192;
+                        uint4 v[8];
+#pragma unroll
+                        for (int ch = 0; ch < 8; ++ch)
+                            v[ch] = *reinterpret_cast<const uint4 *>(qs + sw128_offset(t, ch));
 #pragma unroll
                         for (int ch = 0; ch < 8; ++ch) {
-                            const uint32_t off = sw128_offset(t, ch);
-                            uint4 v = *reinterpret_cast<const uint4 *>(qs + off);
-                            uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+                            uint32_t wv[4] = {v[ch].x, v[ch].y, v[ch].z, v[ch].w};
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
                                 __nv_bfloat162 b2 = *reinterpret_cast<__nv_bfloat162 *>(&wv[e]);
                                 float2 f2 = __bfloat1622float2(b2);
                                 wv[e] = pack_bf16(f2.x * gam, f2.y * gam);
                             }
-                            st16(qs + off, wv[0], wv[1], wv[2], wv[3]);
+                            v[ch] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
                         }
+#pragma unroll
+                        for (int ch = 0; ch < 8; ++ch)
+                            *reinterpret_cast<uint4 *>(qs + sw128_offset(t, ch)) = v[ch];
                     }
                 };
                 if (span_ok) scale_q();
+                TRACE(1, j, 6, t == 0);
                 fence_proxy_async_smem();
                 named_bar(4, 64);
                 if (t == 0) mbar_arrive(bar + B_READY + s);
+                TRACE(1, j, 7, t == 0);
                 if (!span_ok) {
                     // the Gram must read the unscaled Q first
                     if (!named_bar_and(4, 64, ctl.wait(B_G, j & 1))) break;
@@ -539,6 +550,18 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
             prefetch_tmap(&tm_w);
         }
         int issued = 0;
+        // gates of the next chunk, loaded one chunk ahead so their latency hides
+        // behind the wait for a free stage
+        float pla0 = 0.f, pla1 = 0.f, pb0 = 0.f, pb1 = 0.f;
+        auto load_gates = [&](int jj) {
+            const long long r0 = row0 + (long long)jj * kC;
+            const int Lj = min(kC, len - jj * kC);
+            pla0 = lane < Lj ? __ldg(p.log_alpha + r0 + lane) : 0.f;
+            pla1 = lane + 32 < Lj ? __ldg(p.log_alpha + r0 + lane + 32) : 0.f;
+            pb0 = lane < Lj ? __ldg(p.beta + r0 + lane) : 0.f;
+            pb1 = lane + 32 < Lj ? __ldg(p.beta + r0 + lane + 32) : 0.f;
+        };
+        if (nch > 0) load_gates(0);
         for (int j = 0; j < nch; ++j) {
             const int s = j % kNS;
             const bool ok = j < kNS || ctl.wait(B_FREE + s, ((j / kNS) - 1) & 1);
@@ -561,13 +584,12 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
             }
             {
                 float *gs = reinterpret_cast<float *>(sm + L::OFF_GS) + s * 128;
-                const long long r0 = row0 + (long long)j * kC;
-                const int Lj = min(kC, len - j * kC);
-                gs[lane] = lane < Lj ? __ldg(p.log_alpha + r0 + lane) : 0.f;
-                gs[32 + lane] = lane + 32 < Lj ? __ldg(p.log_alpha + r0 + lane + 32) : 0.f;
-                gs[64 + lane] = lane < Lj ? __ldg(p.beta + r0 + lane) : 0.f;
-                gs[96 + lane] = lane + 32 < Lj ? __ldg(p.beta + r0 + lane + 32) : 0.f;
+                gs[lane] = pla0;
+                gs[32 + lane] = pla1;
+                gs[64 + lane] = pb0;
+                gs[96 + lane] = pb1;
                 mbar_arrive(fb);
+                if (j + 1 < nch) load_gates(j + 1);
             }
             issued = j + 1;
         }
@@ -634,19 +656,10 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
                 const int s = j % kNS;
                 const uint32_t soff = s * L::STAGE;
                 if (!ctl.wait(B_READY + s, (j / kNS) & 1)) break;
-                if (j > 0 && !ctl.wait(B_VN, (j - 1) & 1)) break;   // U of j-1 consumed
+                if (j > 0 && !ctl.wait(B_GFREE, (j - 1) & 1)) break;   // G of j-1 consumed
                 TRACE(3, j, 0, true);
                 tc_fence_after();
-                // U = T_u V; rows 64-127 of the A operand are whatever follows T_u
-#pragma unroll
-                for (int kk = 0; kk < kC / 16; ++kk)
-                    mma_bf16(tmem + TM_U, dS + ((soff + L::OFF_TU + kk * 32) >> 4),
-                             dS + ((soff + L::OFF_V + kk * 2048) >> 4), idU, kk > 0);
-                mma_commit(bar + B_UW);
-                TRACE(3, j, 1, true);
-                if (j > 0 && !ctl.wait(B_GFREE, (j - 1) & 1)) break;
-                TRACE(3, j, 2, true);
-                tc_fence_after();
+                // the Gram first: P is the longer path to the output MMA
 #pragma unroll
                 for (int kk = 0; kk < DK / 16; ++kk) {
                     const uint32_t kof = soff + (kk >> 2) * 8192 + (kk & 3) * 32;
@@ -654,6 +667,16 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
                     mma_bf16(tmem + TM_G, dS + (aof >> 4), dS + (kof >> 4), idG, kk > 0);
                 }
                 mma_commit(bar + B_G);
+                TRACE(3, j, 1, true);
+                if (j > 0 && !ctl.wait(B_VN, (j - 1) & 1)) break;   // U of j-1 consumed
+                TRACE(3, j, 2, true);
+                tc_fence_after();
+                // U = T_u V; rows 64-127 of the A operand are whatever follows T_u
+#pragma unroll
+                for (int kk = 0; kk < kC / 16; ++kk)
+                    mma_bf16(tmem + TM_U, dS + ((soff + L::OFF_TU + kk * 32) >> 4),
+                             dS + ((soff + L::OFF_V + kk * 2048) >> 4), idU, kk > 0);
+                mma_commit(bar + B_UW);
                 TRACE(3, j, 3, true);
             }
             mma_commit(bar + B_DRAIN2);
