@@ -16,12 +16,18 @@
 // rows of the inputs, so the fused kernel loads them with the same kind of
 // bulk tensor copy as K.
 //
-// Arithmetic: the Gram runs on bf16 mma.sync tiles with fp32 accumulation
-// (the inputs are bf16 already); the inverse solves the four 16x16 diagonal
-// blocks by forward substitution in fp32 and merges them (16 -> 32 -> 64) with
-// tf32 mma.sync products, T_{10} = -T_11 A_10 T_00 at each level.  The decay
-// exp(g_r - g_s) is formed only where s < r (never overflows); when the chunk's
-// total decay is moderate it is factored as exp(g_r) exp(-g_s).
+// Arithmetic: the Gram and W run on bf16 mma.sync tiles (fragments by
+// ldmatrix) with fp32 accumulation (the inputs are bf16 already); the inverse
+// solves the four 16x16 diagonal blocks by forward substitution in fp32 and
+// merges them (16 -> 32 -> 64) with tf32 mma.sync products,
+// T_{10} = -T_11 A_10 T_00 at each level.  The decay exp(g_r - g_s) is formed
+// only where s < r (never overflows); when the chunk's total decay is moderate
+// it is factored as exp(g_r) exp(-g_s).
+//
+// The work is small and latency-bound, so the kernel is persistent with four
+// CTAs per SM (52 KB of shared memory each at d_k = 128), and every CTA loads
+// its next chunk's K tile and gates into registers while it computes the
+// current one.
 #include <cuda_bf16.h>
 
 #include "gdn_internal.h"
@@ -31,22 +37,25 @@ namespace {
 
 constexpr int kCp = 64;
 constexpr int LDA = 68;   // fp32 row stride of A / T
-constexpr int LDX = 36;
+constexpr int LDT = 72;   // bf16 row stride of the T_w tile
 
 template <int DK>
 struct PrepLay {
     static constexpr int LDK = DK + 8;                   // bf16 row stride of the K tile
     static constexpr int KBYTES = kCp * LDK * 2;
     static constexpr int TBYTES = kCp * LDA * 4;
-    // K stays for W = T_w K; once T is final, A's space holds bf16 T_w and
-    // T's space holds the bf16 W tile on its way out
+    // K stays for W = T_w K.  T's upper-right 32x32 block is never part of
+    // T (T is lower triangular and the merges read only its two diagonal
+    // 32x32 blocks), so it holds the merge products; once T is final, A's
+    // space holds bf16 T_w and T's space the bf16 W tile on its way out.
     static constexpr int OFF_K = 0;
     static constexpr int OFF_T = KBYTES;                 // fp32 [64][68]
     static constexpr int OFF_A = OFF_T + TBYTES;         // fp32 [64][68]
-    static constexpr int OFF_X = OFF_A + TBYTES;         // fp32 [32][36]
-    static constexpr int OFF_G = OFF_X + 32 * LDX * 4;   // g, beta, gamma, 1/gamma
+    static constexpr int OFF_G = OFF_A + TBYTES;         // g, beta, beta gamma, 1/gamma
     static constexpr int TOTAL = OFF_G + 4 * kCp * 4;
-    static_assert(OFF_A % 16 == 0 && OFF_X % 16 == 0, "align");
+    static constexpr int KV = kCp * DK / 8 / 128;        // 16-byte K vectors per thread
+    static_assert(OFF_A % 16 == 0 && OFF_G % 16 == 0, "align");
+    static_assert(kCp * LDT * 2 <= TBYTES && kCp * LDK * 2 <= TBYTES, "staging fits");
 };
 
 __device__ __forceinline__ float tf32(float x) {
@@ -56,52 +65,75 @@ __device__ __forceinline__ float tf32(float x) {
 }
 
 // D += A(16x8, row) * B(8x8, col), tf32 inputs, fp32 accumulate.
-__device__ __forceinline__ void mma_tf32(float (&d)[4], const float (&a)[4], const float (&b)[2]) {
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], const float (&b)[2]) {
     asm volatile(
         "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
         "{%8,%9}, {%0,%1,%2,%3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(__float_as_uint(a[0])), "r"(__float_as_uint(a[1])), "r"(__float_as_uint(a[2])),
-          "r"(__float_as_uint(a[3])), "r"(__float_as_uint(b[0])), "r"(__float_as_uint(b[1])));
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(__float_as_uint(b[0])),
+          "r"(__float_as_uint(b[1])));
 }
 
 // D += A(16x16, row) * B(16x8, col), bf16 inputs (two per register), fp32 accumulate.
-__device__ __forceinline__ void mma_bf16x16(float (&d)[4], const uint32_t (&a)[4],
-                                            const uint32_t (&b)[2]) {
+__device__ __forceinline__ void mma_bf16x16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                            uint32_t b1) {
     asm volatile(
         "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
         "{%8,%9}, {%0,%1,%2,%3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// One 16x8 output tile of  Y = Am * Bm  over k = 0..K-1, operands fp32 in smem
-// (row-major with strides lda / ldb).  Returns the C fragment.
+__device__ __forceinline__ uint32_t saddr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// Four 8x8 bf16 matrices from shared memory (lanes 8i..8i+7 give the row
+// addresses of matrix i); .trans hands each thread a column pair instead.
+__device__ __forceinline__ void ldsm4(uint32_t (&r)[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr)
+                 : "memory");
+}
+__device__ __forceinline__ void ldsm4t(uint32_t (&r)[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr)
+                 : "memory");
+}
+
+// One 16x8 output tile of  Y = Am * Bm  over the 8-wide k steps [kb, ke),
+// operands tf32 values stored as fp32 in smem (row-major, strides lda / ldb;
+// Am 16-byte aligned with lda a multiple of 4).  The A fragment of a k step is
+// one ldmatrix: its 8x8 b16 matrices are 8x4 fp32 blocks, which hand thread
+// (g, t) element (g, t) -- the tf32 fragment layout.
 template <int K>
 __device__ __forceinline__ void tile_mma(float (&c)[4], const float *Am, int lda, const float *Bm,
-                                         int ldb, int lane) {
+                                         int ldb, int lane, int kb = 0, int ke = K / 8) {
     const int g = lane >> 2, t = lane & 3;
     c[0] = c[1] = c[2] = c[3] = 0.f;
+    const uint32_t a_addr = saddr(Am + (lane & 15) * lda + 4 * (lane >> 4));
 #pragma unroll
-    for (int k0 = 0; k0 < K; k0 += 8) {
-        float a[4], b[2];
-        a[0] = tf32(Am[g * lda + k0 + t]);
-        a[1] = tf32(Am[(g + 8) * lda + k0 + t]);
-        a[2] = tf32(Am[g * lda + k0 + t + 4]);
-        a[3] = tf32(Am[(g + 8) * lda + k0 + t + 4]);
-        b[0] = tf32(Bm[(k0 + t) * ldb + g]);
-        b[1] = tf32(Bm[(k0 + t + 4) * ldb + g]);
+    for (int ks = 0; ks < K / 8; ++ks) {
+        if (ks < kb || ks >= ke) continue;
+        const int k0 = 8 * ks;
+        uint32_t a[4];
+        ldsm4(a, a_addr + 4 * k0);
+        const float b[2] = {Bm[(k0 + t) * ldb + g], Bm[(k0 + t + 4) * ldb + g]};
         mma_tf32(c, a, b);
     }
 }
 
+// Stores scale * C rounded to tf32 (every fp32 matrix in smem holds tf32
+// values, so the products read it without conversion).
 __device__ __forceinline__ void store_tile(float *D, int ldd, const float (&c)[4], int lane,
                                            float scale) {
     const int g = lane >> 2, t = lane & 3;
-    D[g * ldd + 2 * t] = scale * c[0];
-    D[g * ldd + 2 * t + 1] = scale * c[1];
-    D[(g + 8) * ldd + 2 * t] = scale * c[2];
-    D[(g + 8) * ldd + 2 * t + 1] = scale * c[3];
+    *reinterpret_cast<float2 *>(D + g * ldd + 2 * t) =
+        make_float2(tf32(scale * c[0]), tf32(scale * c[1]));
+    *reinterpret_cast<float2 *>(D + (g + 8) * ldd + 2 * t) =
+        make_float2(tf32(scale * c[2]), tf32(scale * c[3]));
 }
 
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
@@ -110,256 +142,327 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     return r;
 }
 
+// Persistent: CTA b takes the (chunk slot, head) units b, b + grid, ...  The
+// next unit's K tile and gates are loaded into registers while the current
+// one is computed.
 template <int DK>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(128, 4)
 k_gdn_prep(const __nv_bfloat16 *__restrict__ k, const float *__restrict__ log_alpha,
            const float *__restrict__ beta, SeqMap sm, const int2 *__restrict__ table,
-           int max_chunks, __nv_bfloat16 *__restrict__ Tu_out, __nv_bfloat16 *__restrict__ W_out,
-           int *err) {
+           int max_chunks, int slots, int units, __nv_bfloat16 *__restrict__ Tu_out,
+           __nv_bfloat16 *__restrict__ W_out, int *err) {
     using L = PrepLay<DK>;
     extern __shared__ __align__(16) uint8_t smem[];
     __nv_bfloat16 *Ks = reinterpret_cast<__nv_bfloat16 *>(smem + L::OFF_K);
     float *Ab = reinterpret_cast<float *>(smem + L::OFF_A);
     float *Tb = reinterpret_cast<float *>(smem + L::OFF_T);
-    float *Xb = reinterpret_cast<float *>(smem + L::OFF_X);
-    float *gs = reinterpret_cast<float *>(smem + L::OFF_G);   // g, beta, gamma, 1/gamma
+    float *gs = reinterpret_cast<float *>(smem + L::OFF_G);   // g, beta, beta gamma, 1/gamma
+    __nv_bfloat16 *Tw = reinterpret_cast<__nv_bfloat16 *>(smem + L::OFF_A);
+    __nv_bfloat16 *Ws = reinterpret_cast<__nv_bfloat16 *>(smem + L::OFF_T);
 
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
-    int n, c;
-    if (table) {
-        const int2 e = table[blockIdx.x];
-        n = e.x;
-        c = e.y;
-        if (n < 0) return;
-    } else {
-        n = blockIdx.x / max_chunks;
-        c = blockIdx.x % max_chunks;
-    }
-    const int h = blockIdx.y;
-    long long row0;
-    int len;
-    if (sm.cu) {
-        const int a = __ldg(sm.cu + n), b = __ldg(sm.cu + n + 1);
-        if (!(a >= 0 && a <= b && b <= sm.T_total)) {
-            if (tid == 0) atomicCAS(err, 0, kErrSeqlens);
-            return;
-        }
-        row0 = (long long)h * sm.T_total + a;
-        len = b - a;
-    } else {
-        row0 = ((long long)n * sm.H + h) * (long long)sm.T;
-        len = sm.T;
-    }
-    const int t0 = c * kCp;
-    if (t0 >= len) return;
-    const int Lc = min(kCp, len - t0);
-    const long long r0 = row0 + t0;
+    const int g = lane >> 2, t = lane & 3;
+    constexpr int VPR = DK / 8;   // 16-byte vectors per K row
 
-    // ---- K tile (rows past the sequence are zero) and gates
-    constexpr int VPR = DK / 8;   // 16-byte vectors per row
-    for (int i = tid; i < kCp * VPR; i += 128) {
-        const int r = i / VPR, q = i % VPR;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (r < Lc) v = __ldg(reinterpret_cast<const uint4 *>(k + (r0 + r) * DK) + q);
-        *reinterpret_cast<uint4 *>(Ks + r * L::LDK + 8 * q) = v;
-    }
-    if (w == 0) {
-        float la0 = lane < Lc ? __ldg(log_alpha + r0 + lane) : 0.f;
-        float la1 = lane + 32 < Lc ? __ldg(log_alpha + r0 + lane + 32) : 0.f;
-        const float b0 = lane < Lc ? __ldg(beta + r0 + lane) : 0.f;
-        const float b1 = lane + 32 < Lc ? __ldg(beta + r0 + lane + 32) : 0.f;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const float y0 = __shfl_up_sync(0xffffffffu, la0, off);
-            const float y1 = __shfl_up_sync(0xffffffffu, la1, off);
-            if (lane >= off) {
-                la0 += y0;
-                la1 += y1;
-            }
+    // unit u -> first token row r0 and token count Lc (0: nothing to do)
+    auto decode = [&](long long u, long long &r0, int &Lc) {
+        r0 = 0;
+        Lc = 0;
+        if (u >= units) return;
+        const int slot = (int)(u % slots), h = (int)(u / slots);
+        int n, c;
+        if (table) {
+            const int2 e = table[slot];
+            n = e.x;
+            c = e.y;
+            if (n < 0) return;
+        } else {
+            n = slot / max_chunks;
+            c = slot % max_chunks;
         }
-        la1 += __shfl_sync(0xffffffffu, la0, 31);
-        gs[lane] = la0;
-        gs[lane + 32] = la1;
-        gs[64 + lane] = b0;
-        gs[96 + lane] = b1;
-        gs[128 + lane] = __expf(la0);
-        gs[160 + lane] = __expf(la1);
-        gs[192 + lane] = __expf(-la0);
-        gs[224 + lane] = __expf(-la1);
-    }
-    __syncthreads();
-
-    // ---- A = strictly lower (beta_r exp(g_r - g_s) K K^T): warp w owns rows
-    //      16w..16w+15 and the column tiles left of its diagonal block's end
-    {
-        const int g = lane >> 2, t = lane & 3;
-        const float gC = gs[63];
-        const bool span_ok = gC > -80.f;
-        const int ra = 16 * w + g, rb = ra + 8;
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt) {
-            if (nt > 2 * w + 1) break;
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int k0 = 0; k0 < DK; k0 += 16) {
-                uint32_t a[4], b[2];
-                a[0] = *reinterpret_cast<const uint32_t *>(Ks + ra * L::LDK + k0 + 2 * t);
-                a[1] = *reinterpret_cast<const uint32_t *>(Ks + rb * L::LDK + k0 + 2 * t);
-                a[2] = *reinterpret_cast<const uint32_t *>(Ks + ra * L::LDK + k0 + 2 * t + 8);
-                a[3] = *reinterpret_cast<const uint32_t *>(Ks + rb * L::LDK + k0 + 2 * t + 8);
-                const int nrow = 8 * nt + g;
-                b[0] = *reinterpret_cast<const uint32_t *>(Ks + nrow * L::LDK + k0 + 2 * t);
-                b[1] = *reinterpret_cast<const uint32_t *>(Ks + nrow * L::LDK + k0 + 2 * t + 8);
-                mma_bf16x16(acc, a, b);
+        long long row0;
+        int len;
+        if (sm.cu) {
+            const int a = __ldg(sm.cu + n), b = __ldg(sm.cu + n + 1);
+            if (!(a >= 0 && a <= b && b <= sm.T_total)) {
+                if (tid == 0) atomicCAS(err, 0, kErrSeqlens);
+                return;
             }
+            row0 = (long long)h * sm.T_total + a;
+            len = b - a;
+        } else {
+            row0 = ((long long)n * sm.H + h) * (long long)sm.T;
+            len = sm.T;
+        }
+        const int t0 = c * kCp;
+        if (t0 >= len) return;
+        Lc = min(kCp, len - t0);
+        r0 = row0 + t0;
+    };
+
+    uint4 kr[L::KV];
+    float la0 = 0.f, la1 = 0.f, b0 = 0.f, b1 = 0.f;
+    // K rows past the chunk and the gates there read as zero
+    auto fetch = [&](long long r0, int Lc) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int r = (e < 2) ? ra : rb;
-                const int s = 8 * nt + 2 * t + (e & 1);
-                float v = 0.f;
-                if (s < r) {
-                    const float f = span_ok ? gs[128 + r] * gs[192 + s] : __expf(gs[r] - gs[s]);
-                    v = gs[64 + r] * f * acc[e];
+        for (int j = 0; j < L::KV; ++j) {
+            const int i = tid + 128 * j, r = i / VPR, q = i % VPR;
+            kr[j] = r < Lc ? __ldg(reinterpret_cast<const uint4 *>(k + (r0 + r) * DK) + q)
+                           : make_uint4(0u, 0u, 0u, 0u);
+        }
+        if (w == 0) {
+            la0 = lane < Lc ? __ldg(log_alpha + r0 + lane) : 0.f;
+            la1 = lane + 32 < Lc ? __ldg(log_alpha + r0 + lane + 32) : 0.f;
+            b0 = lane < Lc ? __ldg(beta + r0 + lane) : 0.f;
+            b1 = lane + 32 < Lc ? __ldg(beta + r0 + lane + 32) : 0.f;
+        }
+    };
+
+    long long u = blockIdx.x;
+    long long r0;
+    int Lc;
+    decode(u, r0, Lc);
+    fetch(r0, Lc);
+    for (; u < units; u += gridDim.x) {
+        // ---- this unit's K tile and gates into shared memory (every thread
+        //      finished the previous unit's reads of Ks, gs and A's space
+        //      before the barrier that ended its W product)
+#pragma unroll
+        for (int j = 0; j < L::KV; ++j) {
+            const int i = tid + 128 * j, r = i / VPR, q = i % VPR;
+            *reinterpret_cast<uint4 *>(Ks + r * L::LDK + 8 * q) = kr[j];
+        }
+        if (w == 0) {
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float y0 = __shfl_up_sync(0xffffffffu, la0, off);
+                const float y1 = __shfl_up_sync(0xffffffffu, la1, off);
+                if (lane >= off) {
+                    la0 += y0;
+                    la1 += y1;
                 }
-                Ab[r * LDA + s] = v;
             }
-        }
-    }
-    __syncthreads();
-
-    // ---- T = (I + A)^{-1}
-    if (w < 2) {
-        // 16x16 diagonal blocks, one column per thread, right-looking
-        const int blk = tid >> 4, cc = tid & 15, o = blk * 16;
-        float x[16];
-#pragma unroll
-        for (int r = 0; r < 16; ++r) x[r] = (r == cc) ? 1.f : 0.f;
-#pragma unroll
-        for (int s2 = 0; s2 < 16; ++s2) {
-#pragma unroll
-            for (int r = s2 + 1; r < 16; ++r) x[r] = fmaf(-Ab[(o + r) * LDA + o + s2], x[s2], x[r]);
-        }
-#pragma unroll
-        for (int r = 0; r < 16; ++r) Tb[(o + r) * LDA + o + cc] = x[r];
-    } else {
-        // zero the six strictly upper 16x16 blocks
-        for (int i = tid - 64; i < 6 * 256; i += 64) {
-            const int b = i >> 8, e = i & 255;
-            const int bi = b < 3 ? 0 : (b < 5 ? 1 : 2);
-            const int bj = b < 3 ? b + 1 : (b < 5 ? b - 1 : 3);
-            Tb[(bi * 16 + (e >> 4)) * LDA + bj * 16 + (e & 15)] = 0.f;
-        }
-    }
-    __syncthreads();
-    {
-        // 16 -> 32: T_{2p+1,2p} = -D_{2p+1} A_{2p+1,2p} D_{2p}
-        const int pr = w >> 1, nh = w & 1;
-        const int ro = 32 * pr + 16, co = 32 * pr;
-        float *Xw = Xb + w * 16 * 9;
-        float c4[4];
-        tile_mma<16>(c4, Ab + ro * LDA + co, LDA, Tb + co * LDA + co + 8 * nh, LDA, lane);
-        store_tile(Xw, 9, c4, lane, 1.f);
-        __syncwarp();
-        tile_mma<16>(c4, Tb + ro * LDA + ro, LDA, Xw, 9, lane);
-        store_tile(Tb + ro * LDA + co + 8 * nh, LDA, c4, lane, -1.f);
-    }
-    __syncthreads();
-    {
-        // 32 -> 64: T_{1,0} = -E1 (A_{1,0} E0), 32x32 blocks
-        const int mt = w >> 1, nt0 = 2 * (w & 1);
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-            float c4[4];
-            tile_mma<32>(c4, Ab + (32 + 16 * mt) * LDA, LDA, Tb + 8 * (nt0 + q), LDA, lane);
-            store_tile(Xb + 16 * mt * LDX + 8 * (nt0 + q), LDX, c4, lane, 1.f);
+            la1 += __shfl_sync(0xffffffffu, la0, 31);
+            gs[lane] = la0;
+            gs[lane + 32] = la1;
+            gs[64 + lane] = b0;
+            gs[96 + lane] = b1;
+            gs[128 + lane] = b0 * __expf(la0);
+            gs[160 + lane] = b1 * __expf(la1);
+            gs[192 + lane] = __expf(-la0);
+            gs[224 + lane] = __expf(-la1);
         }
         __syncthreads();
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-            float c4[4];
-            tile_mma<32>(c4, Tb + (32 + 16 * mt) * LDA + 32, LDA, Xb + 8 * (nt0 + q), LDX, lane);
-            store_tile(Tb + (32 + 16 * mt) * LDA + 8 * (nt0 + q), LDA, c4, lane, -1.f);
-        }
-    }
-    __syncthreads();
+        long long r0n;
+        int Lcn;
+        decode(u + gridDim.x, r0n, Lcn);
+        const bool live = Lc > 0;   // uniform over the CTA
 
-    // ---- T_u = T diag(beta) rows out (bf16), and T_w = T diag(beta gamma) as
-    //      the bf16 A operand of W = T_w K (in A's space, row stride LDK)
-    __nv_bfloat16 *Tw = reinterpret_cast<__nv_bfloat16 *>(smem + L::OFF_A);
-    {
-        const int r = tid >> 1, hf = tid & 1;
-        const float4 *src = reinterpret_cast<const float4 *>(Tb + r * LDA + 32 * hf);
-        const float4 *sb = reinterpret_cast<const float4 *>(gs + 64 + 32 * hf);
-        const float4 *sg = reinterpret_cast<const float4 *>(gs + 128 + 32 * hf);
-        uint32_t u[16], wv[16];
+        // ---- A = strictly lower (beta_r exp(g_r - g_s) K K^T) from the three
+        //      32x32 blocks of the Gram on or below the diagonal: warp 0 rows
+        //      and columns 0-31, warp 1 rows 32-63 x columns 0-31, warp 2 rows
+        //      and columns 32-63.  A is stored tf32-rounded outside its 16x16
+        //      diagonal blocks (only the merges read it there).  Warp 3 zeroes
+        //      the upper 16x16 blocks inside T's two diagonal 32x32 blocks.
+        if (live && w < 3) {
+            const float gC = gs[63];
+            const bool span_ok = gC > -80.f;
+            const int rb0 = w == 0 ? 0 : 32, cb0 = w == 2 ? 32 : 0;
+            const bool diag = w != 1;   // rows 0-15 x columns 16-31 of the block are zero
+            const uint32_t a_addr = saddr(Ks + (rb0 + (lane & 15)) * L::LDK + 8 * (lane >> 4));
+            const uint32_t b_addr =
+                saddr(Ks + (cb0 + (lane & 7) + 8 * (lane >> 4)) * L::LDK + 8 * ((lane >> 3) & 1));
+            float acc[2][4][4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const float4 a = src[2 * q], b = src[2 * q + 1];
-            const float4 s0 = sb[2 * q], s1 = sb[2 * q + 1];
-            const float4 g0 = sg[2 * q], g1 = sg[2 * q + 1];
-            u[4 * q] = pack2(a.x * s0.x, a.y * s0.y);
-            u[4 * q + 1] = pack2(a.z * s0.z, a.w * s0.w);
-            u[4 * q + 2] = pack2(b.x * s1.x, b.y * s1.y);
-            u[4 * q + 3] = pack2(b.z * s1.z, b.w * s1.w);
-            wv[4 * q] = pack2(a.x * s0.x * g0.x, a.y * s0.y * g0.y);
-            wv[4 * q + 1] = pack2(a.z * s0.z * g0.z, a.w * s0.w * g0.w);
-            wv[4 * q + 2] = pack2(b.x * s1.x * g1.x, b.y * s1.y * g1.y);
-            wv[4 * q + 3] = pack2(b.z * s1.z * g1.z, b.w * s1.w * g1.w);
-        }
-        if (r < Lc) {
-            uint4 *dst = reinterpret_cast<uint4 *>(Tu_out + (r0 + r) * kCp + 32 * hf);
+            for (int i = 0; i < 2; ++i)
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-                dst[q] = make_uint4(u[4 * q], u[4 * q + 1], u[4 * q + 2], u[4 * q + 3]);
-        }
-        uint4 *tw = reinterpret_cast<uint4 *>(Tw + r * L::LDK + 32 * hf);
+                for (int j = 0; j < 4; ++j) acc[i][j][0] = acc[i][j][1] = acc[i][j][2] = acc[i][j][3] = 0.f;
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-            tw[q] = make_uint4(wv[4 * q], wv[4 * q + 1], wv[4 * q + 2], wv[4 * q + 3]);
-    }
-    __syncthreads();
-    // ---- W = T_w K (64 x d_k): warp w owns rows 16w..16w+15; bf16 mma.sync,
-    //      fp32 accumulation, result staged as bf16 in T's space
-    __nv_bfloat16 *Ws = reinterpret_cast<__nv_bfloat16 *>(smem + L::OFF_T);
-    {
-        const int g = lane >> 2, t = lane & 3;
-        const int ra = 16 * w + g, rb = ra + 8;
-        uint32_t af[4][4];
+            for (int k0 = 0; k0 < DK; k0 += 16) {
+                uint32_t af[2][4], bf[2][4];
+                ldsm4(af[0], a_addr + 2 * k0);
+                ldsm4(af[1], a_addr + 2 * (k0 + 16 * L::LDK));
+                ldsm4(bf[0], b_addr + 2 * k0);
+                ldsm4(bf[1], b_addr + 2 * (k0 + 16 * L::LDK));
 #pragma unroll
-        for (int kq = 0; kq < 4; ++kq) {
-            const int k0 = 16 * kq;
-            af[kq][0] = *reinterpret_cast<const uint32_t *>(Tw + ra * L::LDK + k0 + 2 * t);
-            af[kq][1] = *reinterpret_cast<const uint32_t *>(Tw + rb * L::LDK + k0 + 2 * t);
-            af[kq][2] = *reinterpret_cast<const uint32_t *>(Tw + ra * L::LDK + k0 + 2 * t + 8);
-            af[kq][3] = *reinterpret_cast<const uint32_t *>(Tw + rb * L::LDK + k0 + 2 * t + 8);
-        }
-        const unsigned short *Ku = reinterpret_cast<const unsigned short *>(Ks);
+                for (int i = 0; i < 2; ++i)
 #pragma unroll
-        for (int nt = 0; nt < DK / 8; ++nt) {
-            const int n = 8 * nt + g;
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int kq = 0; kq < 4; ++kq) {
-                const int k0 = 16 * kq;
-                uint32_t b[2];
-                b[0] = (uint32_t)Ku[(k0 + 2 * t) * L::LDK + n] |
-                       ((uint32_t)Ku[(k0 + 2 * t + 1) * L::LDK + n] << 16);
-                b[1] = (uint32_t)Ku[(k0 + 2 * t + 8) * L::LDK + n] |
-                       ((uint32_t)Ku[(k0 + 2 * t + 9) * L::LDK + n] << 16);
-                mma_bf16x16(acc, af[kq], b);
+                    for (int j = 0; j < 4; ++j) {
+                        if (diag && i == 0 && j >= 2) continue;
+                        mma_bf16x16(acc[i][j], af[i], bf[j >> 1][2 * (j & 1)],
+                                    bf[j >> 1][2 * (j & 1) + 1]);
+                    }
             }
-            const int col = 8 * nt + 2 * t;
-            *reinterpret_cast<uint32_t *>(Ws + ra * L::LDK + col) = pack2(acc[0], acc[1]);
-            *reinterpret_cast<uint32_t *>(Ws + rb * L::LDK + col) = pack2(acc[2], acc[3]);
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+#pragma unroll
+                for (int hr = 0; hr < 2; ++hr) {
+                    const int r = rb0 + 16 * i + g + 8 * hr;
+                    const float br = gs[64 + r], bgr = gs[128 + r], gr = gs[r];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int s = cb0 + 8 * j + 2 * t;
+                        const float2 ig = *reinterpret_cast<const float2 *>(gs + 192 + s);
+                        float v[2];
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            v[e] = 0.f;
+                            if (s + e < r) {
+                                const float f = span_ok ? bgr * (e ? ig.y : ig.x)
+                                                        : br * __expf(gr - gs[s + e]);
+                                v[e] = f * acc[i][j][2 * hr + e];
+                                if ((r >> 4) != ((s + e) >> 4)) v[e] = tf32(v[e]);
+                            }
+                        }
+                        *reinterpret_cast<float2 *>(Ab + r * LDA + s) = make_float2(v[0], v[1]);
+                    }
+                }
+        } else if (live) {
+            for (int i = lane; i < 2 * 256; i += 32) {
+                const int b = i >> 8, e = i & 255;
+                Tb[(32 * b + (e >> 4)) * LDA + 32 * b + 16 + (e & 15)] = 0.f;
+            }
         }
-    }
-    __syncthreads();
-    // ---- W rows of the real tokens out, 16-byte vectors
-    for (int i = tid; i < kCp * (DK / 8); i += 128) {
-        const int r = i / (DK / 8), q = i % (DK / 8);
-        if (r < Lc)
-            *reinterpret_cast<uint4 *>(W_out + (r0 + r) * DK + 8 * q) =
-                *reinterpret_cast<const uint4 *>(Ws + r * L::LDK + 8 * q);
+        fetch(r0n, Lcn);   // next unit's loads fly during the rest of this one
+        if (live) {
+            __syncthreads();
+
+            // ---- T = (I + A)^{-1}
+            if (w < 2) {
+                // 16x16 diagonal blocks, one column cc per thread: row by row,
+                // x_r = delta_{r,cc} - sum_{s<r} A_rs x_s, A's rows read as
+                // float4 broadcasts
+                const int blk = tid >> 4, cc = tid & 15, o = blk * 16;
+                float x[16];
+#pragma unroll
+                for (int r = 0; r < 16; ++r) {
+                    const float4 *row = reinterpret_cast<const float4 *>(Ab + (o + r) * LDA + o);
+                    float acc = (r == cc) ? 1.f : 0.f;
+#pragma unroll
+                    for (int q = 0; 4 * q < r; ++q) {
+                        const float4 a4 = row[q];
+                        const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            if (4 * q + e < r) acc = fmaf(-av[e], x[4 * q + e], acc);
+                    }
+                    x[r] = acc;
+                }
+#pragma unroll
+                for (int r = 0; r < 16; ++r) Tb[(o + r) * LDA + o + cc] = tf32(x[r]);
+            }
+            __syncthreads();
+            {
+                // 16 -> 32: T_{2p+1,2p} = -D_{2p+1} A_{2p+1,2p} D_{2p}  (D_{2p} is
+                // lower triangular: its columns 8-15 have zero rows 0-7)
+                const int pr = w >> 1, nh = w & 1;
+                const int ro = 32 * pr + 16, co = 32 * pr;
+                float *Xw = Tb + (16 * pr) * LDA + 32 + 8 * nh;
+                float c4[4];
+                tile_mma<16>(c4, Ab + ro * LDA + co, LDA, Tb + co * LDA + co + 8 * nh, LDA, lane, nh);
+                store_tile(Xw, LDA, c4, lane, 1.f);
+                __syncwarp();
+                tile_mma<16>(c4, Tb + ro * LDA + ro, LDA, Xw, LDA, lane);
+                store_tile(Tb + ro * LDA + co + 8 * nh, LDA, c4, lane, -1.f);
+            }
+            __syncthreads();
+            {
+                // 32 -> 64: T_{1,0} = -E1 (A_{1,0} E0), 32x32 blocks; E0 and E1
+                // are lower triangular, so k steps of zero operand rows or
+                // columns are skipped
+                float *Xb = Tb + 32;
+                const int mt = w >> 1, nt0 = 2 * (w & 1);
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    float c4[4];
+                    tile_mma<32>(c4, Ab + (32 + 16 * mt) * LDA, LDA, Tb + 8 * (nt0 + q), LDA, lane,
+                                 nt0 + q);
+                    store_tile(Xb + 16 * mt * LDA + 8 * (nt0 + q), LDA, c4, lane, 1.f);
+                }
+                __syncthreads();
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    float c4[4];
+                    tile_mma<32>(c4, Tb + (32 + 16 * mt) * LDA + 32, LDA, Xb + 8 * (nt0 + q), LDA,
+                                 lane, 0, 2 + 2 * mt);
+                    store_tile(Tb + (32 + 16 * mt) * LDA + 8 * (nt0 + q), LDA, c4, lane, -1.f);
+                }
+            }
+            __syncthreads();
+
+            // ---- T_u = T diag(beta) rows out (bf16), and T_w = T diag(beta gamma)
+            //      as the bf16 A operand of W = T_w K (in A's space): lane l
+            //      takes columns 2l, 2l+1 of rows 16w..16w+15
+            {
+                const int s = 2 * lane;
+                const float2 bs = *reinterpret_cast<const float2 *>(gs + 64 + s);
+                const float2 bg = *reinterpret_cast<const float2 *>(gs + 128 + s);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int r = 16 * w + i;
+                    float2 tv = *reinterpret_cast<const float2 *>(Tb + r * LDA + s);
+                    if (r < 32 && s >= 32) tv = make_float2(0.f, 0.f);   // T's upper-right block
+                    if (r < Lc)
+                        *reinterpret_cast<uint32_t *>(Tu_out + (r0 + r) * kCp + s) =
+                            pack2(tv.x * bs.x, tv.y * bs.y);
+                    *reinterpret_cast<uint32_t *>(Tw + r * LDT + s) = pack2(tv.x * bg.x, tv.y * bg.y);
+                }
+            }
+            __syncthreads();
+
+            // ---- W = T_w K (64 x d_k): warp w owns columns [w d_k/4, (w+1) d_k/4)
+            //      for all rows; T_w is lower triangular, so row block mb only
+            //      needs k blocks 0..mb.  Result staged as bf16 in T's space.
+            {
+                constexpr int NP = DK / 64;   // 16-column pairs of n-tiles per warp
+#pragma unroll
+                for (int np = 0; np < NP; ++np) {
+                    const int c0 = w * (DK / 4) + 16 * np;
+                    float acc[4][2][4];
+#pragma unroll
+                    for (int mb = 0; mb < 4; ++mb)
+#pragma unroll
+                        for (int h2 = 0; h2 < 2; ++h2)
+                            acc[mb][h2][0] = acc[mb][h2][1] = acc[mb][h2][2] = acc[mb][h2][3] = 0.f;
+#pragma unroll
+                    for (int kq = 0; kq < 4; ++kq) {
+                        uint32_t bf[4];
+                        ldsm4t(bf, saddr(Ks + (16 * kq + (lane & 7) + 8 * ((lane >> 3) & 1)) * L::LDK +
+                                         c0 + 8 * (lane >> 4)));
+#pragma unroll
+                        for (int mb = kq; mb < 4; ++mb) {
+                            uint32_t af[4];
+                            ldsm4(af, saddr(Tw + (16 * mb + (lane & 15)) * LDT + 16 * kq +
+                                            8 * (lane >> 4)));
+                            mma_bf16x16(acc[mb][0], af, bf[0], bf[1]);
+                            mma_bf16x16(acc[mb][1], af, bf[2], bf[3]);
+                        }
+                    }
+#pragma unroll
+                    for (int mb = 0; mb < 4; ++mb)
+#pragma unroll
+                        for (int h2 = 0; h2 < 2; ++h2) {
+                            const int col = c0 + 8 * h2 + 2 * t;
+                            const int ra = 16 * mb + g;
+                            *reinterpret_cast<uint32_t *>(Ws + ra * L::LDK + col) =
+                                pack2(acc[mb][h2][0], acc[mb][h2][1]);
+                            *reinterpret_cast<uint32_t *>(Ws + (ra + 8) * L::LDK + col) =
+                                pack2(acc[mb][h2][2], acc[mb][h2][3]);
+                        }
+                }
+            }
+            __syncthreads();
+            // ---- W rows of the real tokens out, 16-byte vectors
+#pragma unroll
+            for (int j = 0; j < L::KV; ++j) {
+                const int i = tid + 128 * j, r = i / VPR, q = i % VPR;
+                if (r < Lc)
+                    *reinterpret_cast<uint4 *>(W_out + (r0 + r) * DK + 8 * q) =
+                        *reinterpret_cast<const uint4 *>(Ws + r * L::LDK + 8 * q);
+            }
+        }
+        r0 = r0n;
+        Lc = Lcn;
     }
 }
 
@@ -369,28 +472,40 @@ size_t tc_prep_smem(int dk) {
     return dk == 128 ? (size_t)PrepLay<128>::TOTAL : (size_t)PrepLay<64>::TOTAL;
 }
 
-gdn_status enqueue_tc_prep(const FwdArgs &a, const int2 *table, __nv_bfloat16 *Tu,
-                           __nv_bfloat16 *W) {
-    if (a.chunk_slots <= 0) return GDN_OK;
-    int *err = device_error_word();
-    const size_t smem = tc_prep_smem(a.dk);
-    dim3 grid(a.chunk_slots, a.sm.H);
-    const __nv_bfloat16 *k = static_cast<const __nv_bfloat16 *>(a.k);
-    if (a.dk == 128) {
-        if (cudaFuncSetAttribute(k_gdn_prep<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem) != cudaSuccess)
+namespace {
+template <int DK>
+gdn_status launch_prep(const FwdArgs &a, const int2 *table, __nv_bfloat16 *Tu,
+                       __nv_bfloat16 *W) {
+    static int blocks_per_sm[64] = {};   // per device, filled on first use
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return GDN_ERR_CUDA;
+    const int smem = PrepLay<DK>::TOTAL;
+    if (cudaFuncSetAttribute(k_gdn_prep<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        cudaSuccess)
+        return GDN_ERR_CUDA;
+    if (blocks_per_sm[dev] == 0) {
+        int nb = 0, nsm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, k_gdn_prep<DK>, 128, smem) !=
+                cudaSuccess ||
+            cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             return GDN_ERR_CUDA;
-        k_gdn_prep<128><<<grid, 128, smem, a.stream>>>(k, a.log_alpha, a.beta, a.sm, table,
-                                                        a.max_chunks, Tu, W, err);
-    } else {
-        if (cudaFuncSetAttribute(k_gdn_prep<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem) != cudaSuccess)
-            return GDN_ERR_CUDA;
-        k_gdn_prep<64><<<grid, 128, smem, a.stream>>>(k, a.log_alpha, a.beta, a.sm, table,
-                                                       a.max_chunks, Tu, W, err);
+        blocks_per_sm[dev] = max(1, nb) * max(1, nsm);
     }
+    const long long units = (long long)a.chunk_slots * a.sm.H;
+    if (units > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
+    const int grid = (int)(units < blocks_per_sm[dev] ? units : (long long)blocks_per_sm[dev]);
+    k_gdn_prep<DK><<<grid, 128, smem, a.stream>>>(
+        static_cast<const __nv_bfloat16 *>(a.k), a.log_alpha, a.beta, a.sm, table, a.max_chunks,
+        a.chunk_slots, (int)units, Tu, W, device_error_word());
     count_launch();
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+}  // namespace
+
+gdn_status enqueue_tc_prep(const FwdArgs &a, const int2 *table, __nv_bfloat16 *Tu,
+                           __nv_bfloat16 *W) {
+    if (a.chunk_slots <= 0 || a.sm.H <= 0) return GDN_OK;
+    return a.dk == 128 ? launch_prep<128>(a, table, Tu, W) : launch_prep<64>(a, table, Tu, W);
 }
 
 }  // namespace gdn
