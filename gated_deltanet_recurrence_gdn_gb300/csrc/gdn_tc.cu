@@ -83,7 +83,6 @@ enum {
     B_UW,                       // U and W in TMEM
     B_WQ,                       // W and gamma*Q in smem
     B_M2,                       // chain MMA done
-    B_H,                        // H (bf16) in smem, TMEM results consumed
     B_VN,                       // V' (bf16) in smem, U consumed
     B_M34,                      // dH and O done
     B_DRAIN,                    // chain MMA issuer drained
@@ -153,6 +152,14 @@ struct Ctl {
         atomicCAS(err, 0, kErrTimeout);
         return false;
     }
+    // Bounded poll of a release/acquire counter until it reaches `target`.
+    __device__ __forceinline__ bool flag(const uint32_t *f, uint32_t target) const {
+        if (*abort) return false;
+        if (flag_wait(f, target, limit)) return true;
+        *abort = 1;
+        atomicCAS(err, 0, kErrTimeout);
+        return false;
+    }
     // Same, by busy polling (single-thread issuer roles).
     __device__ __forceinline__ bool spin(int b, uint32_t parity) const {
         if (*abort) return false;
@@ -192,6 +199,9 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + L::OFF_BAR);
     uint32_t *misc = reinterpret_cast<uint32_t *>(sm + L::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(misc + 1);
+    // chunk index + 1 of the last H / V' the chain published (read by the
+    // output MMA issuer)
+    uint32_t *h_flag = misc + 2, *vn_flag = misc + 3;
     float *gb = reinterpret_cast<float *>(sm + L::OFF_G);   // [2][GSZ]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -244,6 +254,8 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
         for (int s = 0; s < kNS; ++s) mbar_init(bar + B_FREE + s, 3);   // chain MMA + 2 prep groups
         for (int s = 0; s < kNS; ++s) mbar_init(bar + B_FULL + s, 33);   // TMA tx + 32 gate lanes
         *abort_flag = 0;
+        *h_flag = 0;
+        *vn_flag = 0;
         fence_mbar_init();
     }
     tc_fence_before();
@@ -298,7 +310,7 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
             fence_proxy_async_smem();
             tc_fence_before();
             named_bar(1, 128);
-            if (t == 0) mbar_arrive(bar + B_H);
+            if (t == 0) st_release_cta(h_flag, (uint32_t)j + 1);
             TRACE(0, j, 1, t == 0);
             // (i') previous chunk's output rows, off the state's critical path
             if (j > 0 && t >= 64 && !p.no_output && !lin) store_o(j - 1);
@@ -344,7 +356,10 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
             fence_proxy_async_smem();
             tc_fence_before();
             named_bar(1, 128);
-            if (t == 0) mbar_arrive(bar + B_VN);
+            if (t == 0) {
+                st_release_cta(vn_flag, (uint32_t)j + 1);
+                mbar_arrive(bar + B_VN);
+            }
             TRACE(0, j, 4, t == 0);
             // (iii) H <- exp(g_C) H + dH
             if (!named_bar_and(1, 128, ctl.wait(B_M34, j & 1))) {
@@ -615,7 +630,7 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
             for (int j = 0; j < nch; ++j) {
                 const uint32_t soff = (j % kNS) * L::STAGE;
                 const uint32_t acc = tmem + TM_M2 + (j & 1) * 64;
-                if (!ctl.wait(B_H, j & 1) || !ctl.wait(B_WQ, j & 1)) break;
+                if (!ctl.wait(B_WQ, j & 1) || !ctl.flag(h_flag, (uint32_t)j + 1)) break;
                 TRACE(2, j, 0, true);
                 tc_fence_after();
 #pragma unroll
@@ -625,8 +640,8 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
                 }
                 mma_commit(bar + B_M2);
                 TRACE(2, j, 1, true);
-                if (!ctl.wait(B_VN, j & 1)) break;
                 if (!ctl.wait(B_PREADY + (j & 1), (j >> 1) & 1)) break;   // P of this chunk
+                if (!ctl.flag(vn_flag, (uint32_t)j + 1)) break;
                 TRACE(2, j, 2, true);
                 tc_fence_after();
                 const uint64_t dP = (j & 1) ? dVN : dVT;   // [x; P] starts at the region base

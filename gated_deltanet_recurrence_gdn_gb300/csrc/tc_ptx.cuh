@@ -79,6 +79,24 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32
     return false;
 }
 
+// Release / acquire on a CTA-shared 32-bit word: a cheaper one-way hand-off
+// than an mbarrier arrive for a single waiting thread.  A counter that only
+// grows (chunk index + 1) has no phase to confuse.
+__device__ __forceinline__ void st_release_cta(uint32_t *p, uint32_t v) {
+    asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire_cta(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+    return v;
+}
+// Bounded poll until *p >= target; false if it never got there.
+__device__ __forceinline__ bool flag_wait(const uint32_t *p, uint32_t target, uint32_t limit) {
+    for (uint32_t i = 0; i < 4u * limit; ++i)
+        if (ld_acquire_cta(p) >= target) return true;
+    return false;
+}
+
 // ----------------------------------------------------------------- fences
 
 // Generic-proxy writes to shared memory -> visible to the async proxy
