@@ -275,7 +275,10 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
                           : ((t < DK && p.h0) ? __ldg(p.h0 + (srow + dv0 + c) * DK + t) : 0.f);
         uint8_t *Hs = sm + L::OFF_H;
         uint8_t *VT = sm + L::OFF_R0, *VN = sm + L::OFF_R1;
-        // Output rows of chunk jj (lanes 64-127 of its accumulator) to global.
+        // Output rows of chunk jj (lanes 64-127 of its accumulator) to global,
+        // times osc: gamma_r when the chunk's accumulator holds
+        // Q H + (P / gamma_r) V' (Q left unscaled), else 1.
+        float osc = 1.f;
         auto store_o = [&](int jj) {
             const int r = t - 64;
             const int Lj = min(kC, len - jj * kC);
@@ -285,6 +288,11 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
             tmem_ld32(acc + 32, o1);
             tmem_wait32(o0);
             tmem_wait32(o1);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                o0[i] = __float_as_uint(f32(o0[i]) * osc);
+                o1[i] = __float_as_uint(f32(o1[i]) * osc);
+            }
             if (r < Lj) {
                 uint4 *dst = reinterpret_cast<uint4 *>(p.o + (row0 + (long long)jj * kC + r) *
                                                                  p.dv + dv0);
@@ -330,6 +338,9 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
             const float *gj = gb + (j & 1) * L::GSZ;
             const float gC = gj[63];
             const float decayC = __expf(gC);
+            // this chunk's output scale, kept in a register: its gate buffer
+            // may be refilled before the rows are stored during chunk j + 1
+            const float osc_j = (t >= 64 && gC > -80.f) ? gj[128 + t - 64] : 1.f;
             if (t < 64) {
                 const float ev = __expf(gC - gj[t]);
                 const uint32_t acc = tmem + lane_base + TM_M2 + (j & 1) * 64;
@@ -368,6 +379,7 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
             }
             TRACE(0, j, 5, t == 0);
             tc_fence_after();
+            osc = osc_j;
             if (t < DK) {
                 uint32_t d0[32], d1[32];
                 tmem_ld32(tmem + lane_base + TM_H, d0);
@@ -389,9 +401,9 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
     } else if (warp < 8) {
         // ================================================== prep warpgroups
         // Two independent 64-thread pipelines over the chunks:
-        //   warps 4-5: gates, clearing of packed-batch tails, gamma * Q in place
-        //              (before the Gram when the chunk's decay span allows, else
-        //              after it), publishing [W; gamma Q]
+        //   warps 4-5: gates, clearing of packed-batch tails, and -- only when
+        //              the chunk's decay span is too wide for exp(-g_s) -- gamma * Q
+        //              in place after the Gram; publishing [W; Q] (or [W; gamma Q])
         //   warps 6-7: P = causal decayed (Q K^T) from TMEM lanes 64-127
         const int t = tid - 128;
         const int w = warp - 4;
@@ -486,7 +498,8 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
                             *reinterpret_cast<uint4 *>(qs + sw128_offset(t, ch)) = v[ch];
                     }
                 };
-                if (span_ok) scale_q();
+                // span_ok: Q stays unscaled (the output rows take gamma_r at the
+                // end, and P is formed divided by gamma_r)
                 TRACE(1, j, 6, t == 0);
                 fence_proxy_async_smem();
                 named_bar(4, 64);
@@ -534,7 +547,8 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
                         const int sidx = 32 * half + i;
                         const float gv = f32(half == 0 ? g0[i] : g1[i]);
                         const bool keep = sidx <= r;
-                        // span_ok: G already carries gamma_r (Q scaled before the Gram)
+                        // span_ok: P / gamma_r = exp(-g_s) (q_r . k_s), to pair with the
+                        // unscaled Q of the chain MMA; else P itself
                         const float f = span_ok ? gj[192 + sidx]
                                                 : __expf(keep ? gr - gj[sidx] : 0.f);
                         x[i] = keep ? f * gv : 0.f;
