@@ -2,39 +2,41 @@
 //
 // One CTA owns one (sequence, head, 64-wide d_v tile) and walks its chunks of
 // C = 64 tokens in order ("Gated DeltaNet GPU并行实现", section 3.2: matrix
-// products inside a chunk, a serial state pass across chunks).  With
-// H = S^T (d_k x 64 tile of the state, fp32, kept in registers of the chain
-// warpgroup) and g_r the in-chunk cumulative log gate (gamma_r = exp(g_r)):
+// products inside a chunk, a serial state pass across chunks).  The chunk-prep
+// kernel (gdn_prep.cu) has already written, per chunk, T_u = T diag(beta) and
+// W = T diag(beta gamma) K with T = (I + A)^{-1}.  With H = S^T (d_k x 64 tile
+// of the state, fp32, kept in registers of the chain warpgroup), g_r the
+// in-chunk cumulative log gate and gamma_r = exp(g_r):
 //
-//   G     = [K; Q] K^T                                  (tcgen05, M = 128)
-//   A_rs  = beta_r exp(g_r - g_s) (K K^T)_rs,  s < r     (masked before exp)
-//   P_rs  = exp(g_r - g_s) (Q K^T)_rs,         s <= r
-//   T     = (I + A)^{-1}                                (16x16 diagonal blocks by
-//                                                         forward substitution, merged
-//                                                         with tf32 mma.sync)
-//   U     = T diag(beta) V,  W = T diag(beta gamma) K   (tcgen05, [T_u; T_w] stacked)
-//   [W H; gammaQ H]  = [W; diag(gamma) Q] H             (tcgen05, the chain MMA)
+//   G     = [W; Q] K^T                         (tcgen05, M = 128; rows 64-127 used)
+//   P'_rs = exp(-g_s) (Q K^T)_rs,  s <= r      (= P_rs / gamma_r)
+//   U     = T_u V                              (tcgen05)
+//   [W H; Q H] = [W; Q] H                      (tcgen05, the chain MMA)
 //   V'    = U - W H
-//   dH    = K^T diag(exp(g_C - g_r)) V'                 (tcgen05)
-//   O     = diag(gamma) Q H + P V'                      (tcgen05, accumulates)
+//   dH    = K^T diag(exp(g_C - g_r)) V'        (tcgen05)
+//   O     = diag(gamma) (Q H + P' V')          (tcgen05 accumulate; gamma on store)
 //   H    <- exp(g_C) H + dH
+//
+// When a chunk's total log decay g_C is below -80, exp(-g_s) could overflow:
+// that chunk instead scales Q by gamma in place after the Gram, forms
+// P_rs = exp(g_r - g_s) (Q K^T)_rs directly and stores O unscaled.
 //
 // Warp roles (352 threads):
 //   warps 0-3  chain warpgroup: owns H (thread t = row t = d_k index t), forms
-//              V', updates H, stores O (a chunk late, from a second TMEM
-//              accumulator, so the store is off the state's critical path).
-//   warps 4-7  prep warpgroup: gates (prefetched a chunk ahead), G epilogue
-//              (A, P), the inverse, the WY factors as bf16 operands,
-//              gamma-scaled Q.  Runs one chunk ahead of the chain.
-//   warp 8     TMA producer (one lane): K, Q, V tiles, 128-byte swizzled.
-//   warp 9     chain MMA issuer (one lane): [W; gamma Q] H, K^T V~, P V'; TMEM owner.
-//   warp 10    prep MMA issuer (one lane): [K; Q] K^T, [T_u; T_w] [V | K].
-// Every mbarrier wait is bounded; a wait that gives up sets the device error
-// word and makes every role leave its loop, after which in-flight MMAs are
-// drained and TMEM is freed.
+//              V', updates H, stores O a chunk late from a second TMEM
+//              accumulator, off the state's critical path.
+//   warps 4-5  gates of the chunk, clearing of packed-batch tails.
+//   warps 6-7  P' from the Gram in TMEM, as the bf16 operand of P' V'.
+//   warp 8     bulk tensor copies (one lane) of K, W, Q, V and T_u tiles, and
+//              the next chunk's gates (all lanes, prefetched in registers).
+//   warp 9     chain MMA issuer (one lane): [W; Q] H, K^T V~, P' V'; TMEM owner.
+//   warp 10    prep MMA issuer (one lane): [W; Q] K^T, T_u V.
+// Every wait is bounded; a wait that gives up sets the device error word and
+// makes every role leave its loop, after which in-flight MMAs are drained and
+// TMEM is freed.
 //
-// Rows past the end of a sequence are zero (bulk-copy fill, or cleared by the
-// prep warpgroup when they belong to the next packed sequence) with
+// Rows past the end of a sequence are zero (bulk-copy fill, or cleared by
+// warps 4-5 when they belong to the next packed sequence) with
 // beta = log_alpha = 0, which leaves every real row unchanged.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -81,7 +83,7 @@ enum {
     B_G = B_PREADY + 2,         // Gram MMA done (G in TMEM)
     B_GFREE,                    // prep has read G
     B_UW,                       // U and W in TMEM
-    B_WQ,                       // W and gamma*Q in smem
+    B_WQ,                       // [W; Q] (or [W; gamma Q]) in smem for the chain MMA
     B_M2,                       // chain MMA done
     B_VN,                       // V' (bf16) in smem, U consumed
     B_M34,                      // dH and O done
@@ -96,7 +98,7 @@ struct Lay {
     // One input stage (all tiles 64 rows x 128 B, 128-byte swizzled):
     //   K blocks, then V (so [K | V] would be one operand with 8 KiB block
     //   stride and K^T is one MN-major operand), per block [W | Q] (so
-    //   [W; gamma Q] is one 128-row operand; Q is scaled in place), then T_u.
+    //   [W; Q] is one 128-row operand), then T_u.
     static constexpr int OFF_V = KB * 8192;
     static constexpr int OFF_WQ = OFF_V + 8192;
     static constexpr int OFF_TU = OFF_WQ + KB * 16384;
@@ -117,8 +119,8 @@ struct Lay {
     static_assert(ALLOC <= 227 * 1024, "shared memory budget");
 };
 
-// TMEM column map (512 allocated): [W; gamma Q] K^T (its lanes 64-127 hold
-// gamma Q K^T), two chain / output accumulators, dH, and U = T_u V (lanes 0-63).
+// TMEM column map (512 allocated): [W; Q] K^T (its lanes 64-127 hold Q K^T),
+// two chain / output accumulators, dH, and U = T_u V (lanes 0-63).
 constexpr uint32_t TM_G = 0, TM_M2 = 64, TM_H = 192, TM_U = 256;
 
 struct TcParams {
@@ -512,7 +514,7 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
                     fence_proxy_async_smem();
                     named_bar(4, 64);
                 }
-                // publish [W; gamma Q] only once the previous chunk's chain MMA has
+                // publish [W; Q] only once the previous chunk's chain MMA has
                 // read its own copy: the barrier then never runs two phases ahead
                 // of the chain MMA issuer waiting on it
                 if (!named_bar_and(4, 64, j == 0 || ctl.wait(B_M2, (j - 1) & 1))) break;
@@ -630,7 +632,7 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
     } else if (warp == 9) {
         // ===================================== chain MMA issuer (and TMEM owner)
         if (lane == 0 && nch > 0) {
-            constexpr uint32_t idM2 = make_idesc_bf16(128, kNV, false, true);  // [W;gQ] H
+            constexpr uint32_t idM2 = make_idesc_bf16(128, kNV, false, true);  // [W;Q] H
             constexpr uint32_t idM3 = make_idesc_bf16(128, kNV, true, true);   // K^T V~
             constexpr uint32_t idM4 = make_idesc_bf16(128, kNV, false, true);  // [x;P] V'
             const uint32_t sbase = smem_u32(sm);
@@ -677,7 +679,7 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
     } else {
         // ============================================== prep MMA issuer
         if (lane == 0 && nch > 0) {
-            constexpr uint32_t idG = make_idesc_bf16(128, 64, false, false);   // [W;gQ] K^T
+            constexpr uint32_t idG = make_idesc_bf16(128, 64, false, false);   // [W;Q] K^T
             constexpr uint32_t idU = make_idesc_bf16(128, 64, false, true);    // [T_u;x] V
             const uint32_t sbase = smem_u32(sm);
             const uint64_t dS = make_sdesc(sbase + L::OFF_STAGE, 16, 1024, kSwizzle128B);
