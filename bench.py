@@ -339,6 +339,7 @@ def run_ours(args, world, rank, local):
                      "traffic": recorded_traffic(k_name, args.workload),
                      "kernel": k_name, "kernel_ms": kern_ms,
                      "algorithmic_bytes": by, "algorithmic_flops": flops,
+                     "step_frac": by / (step_ms * 1e-3) / 1e9 / hbm,
                      "tensor_frac_of_peak": flops / (kern_ms * 1e-3) / (tf * 1e12)},
         "clocks": clocks.summary(),
         "e2e": {"value": job_throughput(shape["tokens"], world, e2e_ms), "unit": UNIT,
