@@ -60,6 +60,7 @@ ABI = [
                                    ctypes.POINTER(ctypes.c_char_p)]),
     ("gdn_kernel_launches", ctypes.c_uint64, []),
     ("gdn_last_impl", _i, []),
+    ("gdn_release_scratch", _i, []),
 ]
 
 
@@ -231,6 +232,13 @@ def kernel_timer_read():
 
 def last_impl() -> int:
     return int(load().gdn_last_impl())
+
+
+def release_scratch(device=None) -> None:
+    """Hand the scratch memory the library's pool keeps on `device` (default:
+    the current one) back to the driver."""
+    with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
+        _check(load().gdn_release_scratch(), "gdn_release_scratch")
 
 
 class use_impl:

@@ -63,6 +63,46 @@ gdn_status dispatch(FwdArgs &a) {
 }
 }  // namespace
 
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_pool_mu;
+cudaMemPool_t g_pools[kMaxDevices] = {};
+
+cudaError_t scratch_pool(cudaMemPool_t *out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(g_pool_mu);
+    if (!g_pools[dev]) {
+        cudaMemPoolProps props = {};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        cudaMemPool_t pool;
+        if ((e = cudaMemPoolCreate(&pool, &props)) != cudaSuccess) return e;
+        uint64_t keep = UINT64_MAX;   // never hand freed blocks back on its own
+        if ((e = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep)) !=
+            cudaSuccess) {
+            cudaMemPoolDestroy(pool);
+            return e;
+        }
+        g_pools[dev] = pool;
+    }
+    *out = g_pools[dev];
+    return cudaSuccess;
+}
+}  // namespace
+
+cudaError_t scratch_alloc(void **p, size_t bytes, cudaStream_t st) {
+    cudaMemPool_t pool;
+    cudaError_t e = scratch_pool(&pool);
+    if (e != cudaSuccess) return e;
+    return cudaMallocFromPoolAsync(p, bytes, pool, st);
+}
+
+cudaError_t scratch_free(void *p, cudaStream_t st) { return cudaFreeAsync(p, st); }
+
 int *device_error_word() {
     void *p = nullptr;
     cudaGetSymbolAddress(&p, g_error_word);
@@ -259,5 +299,11 @@ gdn_status gdn_kernel_timer_read(double *total_ms, long long *launches, const ch
 uint64_t gdn_kernel_launches(void) { return g_launches.load(); }
 
 int gdn_last_impl(void) { return g_last_impl.load(); }
+
+gdn_status gdn_release_scratch(void) {
+    cudaMemPool_t pool;
+    if (gdn::scratch_pool(&pool) != cudaSuccess) return GDN_ERR_CUDA;
+    return cudaMemPoolTrimTo(pool, 0) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
 
 }  // extern "C"

@@ -51,6 +51,11 @@ struct FwdArgs {
     cudaStream_t stream;
 };
 
+// Stream-ordered scratch from the library's per-device pool, which keeps
+// freed memory mapped (defined in gdn_api.cu).
+cudaError_t scratch_alloc(void **p, size_t bytes, cudaStream_t st);
+cudaError_t scratch_free(void *p, cudaStream_t st);
+
 // device error word helpers (defined in gdn_api.cu)
 int *device_error_word();
 // dominant-kernel timer: returns a slot (or -1 when timing is off)

@@ -31,9 +31,12 @@
 #include <cuda_bf16.h>
 
 #include "gdn_internal.h"
+#include "tc_ptx.cuh"
 
 namespace gdn {
 namespace {
+
+using ptx::griddep_launch_dependents;
 
 constexpr int kCp = 64;
 constexpr int LDA = 68;   // fp32 row stride of A / T
@@ -160,6 +163,9 @@ k_gdn_prep(const __nv_bfloat16 *__restrict__ k, const float *__restrict__ log_al
     __nv_bfloat16 *Tw = reinterpret_cast<__nv_bfloat16 *>(smem + L::OFF_A);
     __nv_bfloat16 *Ws = reinterpret_cast<__nv_bfloat16 *>(smem + L::OFF_T);
 
+    // the fused kernel that follows may be scheduled on SMs this grid leaves
+    // (it waits for this grid's completion before reading T_u / W)
+    griddep_launch_dependents();
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, t = lane & 3;
     constexpr int VPR = DK / 8;   // 16-byte vectors per K row

@@ -310,17 +310,17 @@ gdn_status launch(const FwdArgs &a) {
     float *W = nullptr, *U = nullptr, *G = nullptr;
     int2 *table = nullptr;
     const size_t rows = (size_t)a.rows > 0 ? (size_t)a.rows : 1;
-    if (cudaMallocAsync((void **)&W, rows * a.dk * sizeof(float), st) != cudaSuccess ||
-        cudaMallocAsync((void **)&U, rows * a.dv * sizeof(float), st) != cudaSuccess ||
-        cudaMallocAsync((void **)&G, rows * sizeof(float), st) != cudaSuccess) {
-        if (W) cudaFreeAsync(W, st);
-        if (U) cudaFreeAsync(U, st);
+    if (scratch_alloc((void **)&W, rows * a.dk * sizeof(float), st) != cudaSuccess ||
+        scratch_alloc((void **)&U, rows * a.dv * sizeof(float), st) != cudaSuccess ||
+        scratch_alloc((void **)&G, rows * sizeof(float), st) != cudaSuccess) {
+        if (W) scratch_free(W, st);
+        if (U) scratch_free(U, st);
         return GDN_ERR_CUDA;
     }
     gdn_status rc = GDN_OK;
     if (a.chunk_slots > 0) {
         if (a.sm.cu) {
-            if (cudaMallocAsync((void **)&table, sizeof(int2) * (size_t)a.chunk_slots, st) !=
+            if (scratch_alloc((void **)&table, sizeof(int2) * (size_t)a.chunk_slots, st) !=
                 cudaSuccess) {
                 rc = GDN_ERR_CUDA;
             } else {
@@ -343,10 +343,10 @@ gdn_status launch(const FwdArgs &a) {
         count_launch();
     }
     if (rc == GDN_OK && cudaGetLastError() != cudaSuccess) rc = GDN_ERR_CUDA;
-    cudaFreeAsync(W, st);
-    cudaFreeAsync(U, st);
-    cudaFreeAsync(G, st);
-    if (table) cudaFreeAsync(table, st);
+    scratch_free(W, st);
+    scratch_free(U, st);
+    scratch_free(G, st);
+    if (table) scratch_free(table, st);
     return rc;
 }
 
@@ -369,7 +369,7 @@ gdn_status enqueue_chunk_table(const FwdArgs &a, int2 *table) {
 //
 // gdn_fwd_noalloc runs the same two CUDA-core kernels (prep, state pass) on a
 // dense batch, but its W / U / gate-cumsum scratch lives in this fixed device
-// array instead of coming from cudaMallocAsync.  The array belongs to every
+// array instead of the library's scratch pool.  The array belongs to every
 // GPU that loads the library, for as long as the library stays loaded.  All
 // calls share it and it keeps whatever the previous call left: nothing in it
 // needs to start at zero, because the prep kernel writes every row the state

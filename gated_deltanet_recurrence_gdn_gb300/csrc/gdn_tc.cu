@@ -264,6 +264,10 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = misc[0];
+    // everything above touched only this CTA's shared memory and TMEM; global
+    // data written by the previous kernel in the stream (T_u / W, segment
+    // initial states) is read only from here on
+    griddep_wait();
     const Ctl ctl{bar, abort_flag, p.err, p.wait_limit};
 
     if (warp < 4) {
@@ -816,8 +820,21 @@ gdn_status launch_tc(const FwdArgs &a, const __nv_bfloat16 *Tin, const LaunchCfg
     p.hT2 = c.hT2;
     dim3 grid(a.dv / kNV + c.lin_tiles, a.sm.H, c.nseq);
     const int slot = c.timed ? timer_begin(a.stream, "k_gdn_tc") : -1;
-    k_gdn_tc<DK><<<grid, kThreadsTC, L::ALLOC, a.stream>>>(mq, mk, mv, mt, mw, p);
+    // launched as a programmatic dependent of the previous kernel: its
+    // prologue (barriers, TMEM) overlaps that kernel's tail
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreadsTC);
+    cfg.dynamicSmemBytes = L::ALLOC;
+    cfg.stream = a.stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t le = cudaLaunchKernelEx(&cfg, k_gdn_tc<DK>, mq, mk, mv, mt, mw, p);
     timer_end(slot, a.stream);
+    if (le != cudaSuccess) return GDN_ERR_CUDA;
     count_launch();
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
@@ -914,10 +931,10 @@ gdn_status tc_segmented(const FwdArgs &a, const __nv_bfloat16 *Tbuf, int S) {
     const size_t st_dv = (size_t)H * dv * dk, st_dk = (size_t)H * dk * dk;
     float *Aseg = nullptr, *Bseg = nullptr, *Sin = nullptr, *Hout = nullptr;
     gdn_status rc = GDN_OK;
-    if (cudaMallocAsync((void **)&Aseg, sizeof(float) * st_dk * B * (S - 1), st) != cudaSuccess ||
-        cudaMallocAsync((void **)&Bseg, sizeof(float) * st_dv * B * (S - 1), st) != cudaSuccess ||
-        cudaMallocAsync((void **)&Sin, sizeof(float) * st_dv * B * S, st) != cudaSuccess ||
-        (a.hT && cudaMallocAsync((void **)&Hout, sizeof(float) * st_dv * B * S, st) != cudaSuccess))
+    if (scratch_alloc((void **)&Aseg, sizeof(float) * st_dk * B * (S - 1), st) != cudaSuccess ||
+        scratch_alloc((void **)&Bseg, sizeof(float) * st_dv * B * (S - 1), st) != cudaSuccess ||
+        scratch_alloc((void **)&Sin, sizeof(float) * st_dv * B * S, st) != cudaSuccess ||
+        (a.hT && scratch_alloc((void **)&Hout, sizeof(float) * st_dv * B * S, st) != cudaSuccess))
         rc = GDN_ERR_CUDA;
     if (rc == GDN_OK) {
         // pass 1: per segment but the last, the map's affine part (final state
@@ -945,10 +962,10 @@ gdn_status tc_segmented(const FwdArgs &a, const __nv_bfloat16 *Tbuf, int S) {
                                 st) != cudaSuccess)
                 rc = GDN_ERR_CUDA;
     }
-    if (Aseg) cudaFreeAsync(Aseg, st);
-    if (Bseg) cudaFreeAsync(Bseg, st);
-    if (Sin) cudaFreeAsync(Sin, st);
-    if (Hout) cudaFreeAsync(Hout, st);
+    if (Aseg) scratch_free(Aseg, st);
+    if (Bseg) scratch_free(Bseg, st);
+    if (Sin) scratch_free(Sin, st);
+    if (Hout) scratch_free(Hout, st);
     return rc;
 }
 
@@ -971,13 +988,13 @@ gdn_status tc_forward(const FwdArgs &a) {
     cudaStream_t st = a.stream;
     __nv_bfloat16 *Tbuf = nullptr;
     int2 *table = nullptr;
-    if (cudaMallocAsync((void **)&Tbuf, (size_t)a.rows * (64 + a.dk) * sizeof(__nv_bfloat16),
+    if (scratch_alloc((void **)&Tbuf, (size_t)a.rows * (64 + a.dk) * sizeof(__nv_bfloat16),
                         st) !=
         cudaSuccess)
         return GDN_ERR_CUDA;
     gdn_status rc = GDN_OK;
     if (a.sm.cu) {
-        if (cudaMallocAsync((void **)&table, sizeof(int2) * (size_t)a.chunk_slots, st) !=
+        if (scratch_alloc((void **)&table, sizeof(int2) * (size_t)a.chunk_slots, st) !=
             cudaSuccess)
             rc = GDN_ERR_CUDA;
         else
@@ -991,8 +1008,8 @@ gdn_status tc_forward(const FwdArgs &a) {
         LaunchCfg c{a.sm.N, 0, 0, 0, a.h0, a.hT, 0, nullptr, true};
         rc = a.dk == 128 ? launch_tc<128>(a, Tbuf, c) : launch_tc<64>(a, Tbuf, c);
     }
-    cudaFreeAsync(Tbuf, st);
-    if (table) cudaFreeAsync(table, st);
+    scratch_free(Tbuf, st);
+    if (table) scratch_free(table, st);
     return rc;
 }
 

@@ -97,6 +97,16 @@ __device__ __forceinline__ bool flag_wait(const uint32_t *p, uint32_t target, ui
     return false;
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialisation may start while the previous kernel in the stream runs;
+// griddep_wait() blocks until that kernel has completed and its memory is
+// visible (a no-op without the launch attribute).  griddep_launch_dependents()
+// lets the next such kernel be scheduled before this one ends.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ----------------------------------------------------------------- fences
 
 // Generic-proxy writes to shared memory -> visible to the async proxy

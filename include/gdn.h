@@ -24,8 +24,10 @@
  *
  * Ownership: every pointer argument is a DEVICE pointer owned by the caller;
  * the library keeps no reference after the call returns.  Scratch memory is
- * taken from the stream-ordered allocator (cudaMallocAsync / cudaFreeAsync
- * on `stream`).  All work is enqueued on `stream` (a cudaStream_t; NULL is
+ * taken, stream-ordered on `stream`, from a memory pool the library creates
+ * per device on first use; the pool keeps freed memory mapped, so a call
+ * after a synchronisation reuses it instead of mapping it again
+ * (gdn_release_scratch gives it back).  All work is enqueued on `stream` (a cudaStream_t; NULL is
  * the legacy default stream); calls return before the GPU finishes.
  *
  * Errors: arguments are checked synchronously and a non-GDN_OK status is
@@ -164,6 +166,11 @@ uint64_t gdn_kernel_launches(void);
 /* Implementation the last successful gdn_fwd / gdn_fwd_varlen call used
  * (GDN_IMPL_SIMT or GDN_IMPL_TC), 0 before the first call. */
 int gdn_last_impl(void);
+
+/* Returns the scratch memory the current device's pool holds (memory of
+ * calls still in flight stays until they finish) to the driver.  No paper
+ * counterpart: a memory-management hook.  GDN_OK, or GDN_ERR_CUDA. */
+gdn_status gdn_release_scratch(void);
 
 #ifdef __cplusplus
 }

@@ -143,6 +143,20 @@ def test_empty_sequence_gives_h0(impl):
     assert o.numel() == 0 and torch.equal(hT, x.h0)
 
 
+@pytest.mark.parametrize("impl", ["simt", "tc"])
+def test_scratch_pool_release_and_reuse(impl):
+    # scratch comes from the library's own pool: results do not depend on
+    # whether the pool was just emptied or still holds the previous call's
+    # blocks
+    x = synth.make_dense(2, 2, 333, 128, 128, io="bf16", h0_std=0.02, seed=21, device="cuda")
+    o1, h1 = run_dense(x, impl)
+    gdn.release_scratch()
+    o2, h2 = run_dense(x, impl)
+    o3, h3 = run_dense(x, impl)
+    assert torch.equal(o1, o2) and torch.equal(h1, h2)
+    assert torch.equal(o1, o3) and torch.equal(h1, h3)
+
+
 # ------------------------------------------------------------ segment scan
 
 
