@@ -38,6 +38,7 @@ import synth  # noqa: E402
 
 METRIC = "GDN chunked fwd tokens/s (B·H·T/s) and % of roofline, bf16, d=128, 1×GB300"
 UNIT = "tokens/s"
+DECODE_METRIC = "GDN decode step tokens/s (B·H/s) and % of roofline, bf16, d=128, 1×GB300"
 DEFAULT_WORKLOAD = "gdn_fwd_b4_h16_t4096_d128_bf16"
 L2_FLUSH_BYTES = 256 << 20
 FALLBACK_HBM_GBS = 6800.0
@@ -103,6 +104,9 @@ def job_throughput(tokens_per_rank, world, step_ms):
 
 def workload_shape(name):
     cfg = synth.WORKLOADS[name]
+    if cfg.get("kind") == "decode":
+        return dict(kind="decode", B=cfg["B"], H=cfg["H"], dk=cfg["dk"], dv=cfg["dv"],
+                    io=cfg["io"], tokens=cfg["B"] * cfg["H"], N=cfg["B"], h0=True)
     if "N" in cfg:
         lens = synth.varlen_lengths(cfg["N"], cfg["len_min"], cfg["len_max"], cfg["seed"])
         return dict(kind="varlen", H=cfg["H"], dk=cfg["dk"], dv=cfg["dv"], io=cfg["io"],
@@ -123,6 +127,10 @@ def algorithmic(shape):
     io = 2 if shape["io"] == "bf16" else 4
     dk, dv, C = shape["dk"], shape["dv"], 64
     th = shape["tokens"]
+    if shape["kind"] == "decode":
+        # one token per (sequence, head): its q, k, v, o and gates, and the
+        # fp32 state read and written once; 6 d_k d_v FLOPs (S k, S q, update)
+        return th * ((2 * dk + 2 * dv) * io + 8 + 2 * dk * dv * 4), th * 6 * dk * dv
     seqheads = shape["N"] * shape["H"]
     state = seqheads * dk * dv * 4
     by = th * ((2 * dk + 2 * dv) * io + 8) + state * (2 if shape["h0"] else 1)
@@ -231,7 +239,18 @@ def make_inputs(name, device):
     return synth.make_workload(name, device=device)
 
 
+def is_decode(x):
+    return x.meta.get("kind") == "decode"
+
+
+def metric_for(shape):
+    return DECODE_METRIC if shape["kind"] == "decode" else METRIC
+
+
 def call(gdn, x, out=None):
+    if is_decode(x):
+        return gdn.gdn_decode(x.q, x.k, x.v, x.log_alpha, x.beta, x.h0, slots=x.slots,
+                              out=out), x.h0
     if x.cu_seqlens is not None:
         return gdn.gdn_fwd_varlen(x.q, x.k, x.v, x.log_alpha, x.beta, x.cu_seqlens, x.h0,
                                   out=out)
@@ -278,15 +297,19 @@ def run_ours(args, world, rank, local):
     step_ms = max_over_ranks(step_ms, world)
     kern_ms = max_over_ranks(k_ms / max(k_n, 1), world)
 
-    # ---- end to end: pinned host inputs -> device, forward, result -> host
-    host = {k: (None if t is None else t.cpu().pin_memory()) for k, t in x.tensors().items()}
-    dev_buf = {k: (None if t is None else torch.empty_like(t)) for k, t in x.tensors().items()}
+    # ---- end to end: pinned host inputs -> device, forward, result -> host.
+    # A decode step keeps its states resident in device memory (a serving
+    # loop's state cache): only the token's inputs go in and o comes back.
+    dec = is_decode(x)
+    src = {k: t for k, t in x.tensors().items() if not (dec and k == "h0")}
+    host = {k: (None if t is None else t.cpu().pin_memory()) for k, t in src.items()}
+    dev_buf = {k: (None if t is None else torch.empty_like(t)) for k, t in src.items()}
     o_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     hT_shape = ((shape["N"], shape["H"], shape["dv"], shape["dk"]) if shape["kind"] == "varlen"
                 else (shape["B"], shape["H"], shape["dv"], shape["dk"]))
-    h_host = torch.empty(hT_shape, dtype=torch.float32).pin_memory()
+    h_host = None if dec else torch.empty(hT_shape, dtype=torch.float32).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in host.values() if t is not None)
-    d2h = o_host.numel() * o_host.element_size() + h_host.numel() * 4
+    d2h = o_host.numel() * o_host.element_size() + (0 if dec else h_host.numel() * 4)
     e2e_steps = max(3, min(args.steps, 10))
 
     def e2e_step():
@@ -294,10 +317,12 @@ def run_ours(args, world, rank, local):
             if t is not None:
                 dev_buf[k_].copy_(t, non_blocking=True)
         y = synth.Inputs(dev_buf["q"], dev_buf["k"], dev_buf["v"], dev_buf["log_alpha"],
-                         dev_buf["beta"], dev_buf["h0"], x.cu_seqlens)
+                         dev_buf["beta"], x.h0 if dec else dev_buf["h0"], x.cu_seqlens, x.meta,
+                         x.slots)
         o, hT = call(gdn, y, out=out)
         o_host.copy_(o, non_blocking=True)
-        h_host.copy_(hT, non_blocking=True)
+        if not dec:
+            h_host.copy_(hT, non_blocking=True)
 
     e2e_step()
     torch.cuda.synchronize(dev)
@@ -315,7 +340,7 @@ def run_ours(args, world, rank, local):
     hbm, tf, src = load_peaks()
     achieved = by / (kern_ms * 1e-3) / 1e9
     res = {
-        "metric": METRIC,
+        "metric": metric_for(shape),
         "value": job_throughput(shape["tokens"], world, step_ms),
         "unit": UNIT,
         "n_gpus": world,
@@ -329,7 +354,8 @@ def run_ours(args, world, rank, local):
         "data": "synthetic (seeded; q,k L2-normalised Gaussian, v Gaussian, sigmoid beta, "
                 "-softplus log-gates)",
         "config": {"workload": args.workload, "token_heads": shape["tokens"],
-                   "d_k": shape["dk"], "d_v": shape["dv"], "chunk": 64,
+                   "d_k": shape["dk"], "d_v": shape["dv"],
+                   "chunk": None if shape["kind"] == "decode" else 64,
                    "l2": "flushed before every timed step (256 MiB write)",
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "wall_s_timed_region": wall},
@@ -346,7 +372,8 @@ def run_ours(args, world, rank, local):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms},
         "gpu_launches": launches,
-        "impl_used": {1: "simt", 2: "tc"}.get(gdn.last_impl(), "none"),
+        "impl_used": "decode" if shape["kind"] == "decode" else
+                     {1: "simt", 2: "tc"}.get(gdn.last_impl(), "none"),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(args.workload, x, args.cpu_seconds)
@@ -364,7 +391,17 @@ def oracle_sample(name, x, budget_s, max_heads=None):
     import oracle
     oracle.build()
     f64 = synth.to_f64
-    if x.cu_seqlens is not None:
+    if is_decode(x):
+        units = [(b, h) for b in range(x.q.shape[0]) for h in range(x.q.shape[1])]
+
+        def one(u):
+            b, h = u
+            args = [f64(t[b, h])[None, None, None] for t in (x.q, x.k, x.v)]
+            args += [f64(t[b, h]).reshape(1, 1, 1) for t in (x.log_alpha, x.beta)]
+            t0 = time.perf_counter()
+            oracle.gdn_fwd(*args, f64(x.h0[b, h])[None, None])
+            return 1, time.perf_counter() - t0
+    elif x.cu_seqlens is not None:
         cu = x.cu_seqlens.cpu().numpy()
         units = [(n, h) for n in range(len(cu) - 1) for h in range(x.q.shape[0])]
 
@@ -422,12 +459,14 @@ def run_reference(args, world, rank):
         secs += s
     value = toks / secs
     return {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "metric": metric_for(shape), "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded)",
         "config": {"workload": args.workload, "token_heads": shape["tokens"],
-                   "d_k": shape["dk"], "d_v": shape["dv"], "chunk": 64},
+                   "d_k": shape["dk"], "d_v": shape["dv"],
+                   "chunk": None if shape["kind"] == "decode" else 64},
         "impl": "reference",
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": "per step: " + desc + " (fp64 single-threaded C)"},

@@ -50,6 +50,7 @@ ABI = [
     ("gdn_fwd", _i, [_vp] * 8 + [_i] * 7 + [_vp]),
     ("gdn_fwd_varlen", _i, [_vp] * 9 + [_i] * 7 + [_vp]),
     ("gdn_fwd_noalloc", _i, [_vp] * 8 + [_i] * 7 + [_vp]),
+    ("gdn_decode", _i, [_vp] * 7 + [_i] + [_vp] + [_i] * 5 + [_vp]),
     ("gdn_status_string", ctypes.c_char_p, [_i]),
     ("gdn_sync_check", _i, [_vp]),
     ("gdn_set_option", _i, [_i, ctypes.c_longlong]),
@@ -197,6 +198,41 @@ def gdn_fwd_noalloc(q, k, v, log_alpha, beta, h0=None, *, chunk=CHUNK, out=None,
         if check:
             _check(lib.gdn_sync_check(_stream(q.device)), "gdn_fwd_noalloc (device)")
     return o, hT
+
+
+def gdn_decode(q, k, v, log_alpha, beta, state, *, slots=None, out=None, check=False):
+    """One decode step for every (sequence, head), the state updated in place.
+
+    q, k [B,H,d_k] and v [B,H,d_v] (bf16 or fp32, one dtype); log_alpha, beta
+    [B,H] fp32; state fp32 [B,H,d_v,d_k], or a pool [P,H,d_v,d_k] indexed by
+    `slots` (int32 [B] on the device, distinct).  Returns o [B,H,d_v]."""
+    lib = load()
+    _prep_io(q, k, v, log_alpha, beta, None)
+    if state.dtype != torch.float32 or not state.is_contiguous() or not state.is_cuda:
+        raise ValueError("state must be a contiguous fp32 CUDA tensor")
+    B, H, dk = q.shape
+    dv = v.shape[-1]
+    if k.shape != q.shape or v.shape[:2] != (B, H) or log_alpha.shape != (B, H) \
+            or beta.shape != (B, H):
+        raise ValueError("shape mismatch")
+    if slots is not None:
+        if slots.dtype != torch.int32 or not slots.is_cuda or slots.shape != (B,):
+            raise ValueError("slots must be an int32 CUDA tensor of shape [B]")
+        slots = slots.contiguous()
+        n_slots = state.shape[0]
+    else:
+        n_slots = B
+    if state.shape[1:] != (H, dv, dk) or state.shape[0] != n_slots:
+        raise ValueError("state must be [B or P, H, d_v, d_k]")
+    o = out if out is not None else torch.empty((B, H, dv), dtype=q.dtype, device=q.device)
+    with torch.cuda.device(q.device):
+        rc = lib.gdn_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
+                            _ptr(state), _ptr(slots), n_slots, _ptr(o), B, H, dk, dv,
+                            _DT[q.dtype], _stream(q.device))
+        _check(rc, "gdn_decode")
+        if check:
+            _check(lib.gdn_sync_check(_stream(q.device)), "gdn_decode (device)")
+    return o
 
 
 def sync_check(device=None):

@@ -245,7 +245,7 @@ gdn_status gdn_sync_check(void *stream) {
     if (word != 0 && cudaMemcpyToSymbol(g_error_word, &zero, sizeof(int)) != cudaSuccess)
         return GDN_ERR_CUDA;
     if (word == kErrTimeout) return GDN_ERR_DEVICE_TIMEOUT;
-    if (word == kErrSeqlens) return GDN_ERR_INVALID_ARG;
+    if (word == kErrBadIndex) return GDN_ERR_INVALID_ARG;
     return word == 0 ? GDN_OK : GDN_ERR_CUDA;
 }
 

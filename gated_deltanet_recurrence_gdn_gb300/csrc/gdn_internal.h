@@ -12,7 +12,9 @@ namespace gdn {
 constexpr int kChunk = 64;
 
 // Device error word codes (first error wins).
-enum : int { kErrNone = 0, kErrTimeout = 1, kErrSeqlens = 2 };
+// kErrBadIndex: an index read on the device (packed offsets, state slots) is out
+// of range; the work that needed it is skipped.
+enum : int { kErrNone = 0, kErrTimeout = 1, kErrBadIndex = 2 };
 
 // Where the tokens of (sequence n, head h) live.  Dense tensors are
 // [B][H][T][d] (sequence n = batch index); packed tensors are [H][T_total][d]

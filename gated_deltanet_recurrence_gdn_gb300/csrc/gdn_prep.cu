@@ -191,7 +191,7 @@ k_gdn_prep(const __nv_bfloat16 *__restrict__ k, const float *__restrict__ log_al
         if (sm.cu) {
             const int a = __ldg(sm.cu + n), b = __ldg(sm.cu + n + 1);
             if (!(a >= 0 && a <= b && b <= sm.T_total)) {
-                if (tid == 0) atomicCAS(err, 0, kErrSeqlens);
+                if (tid == 0) atomicCAS(err, 0, kErrBadIndex);
                 return;
             }
             row0 = (long long)h * sm.T_total + a;

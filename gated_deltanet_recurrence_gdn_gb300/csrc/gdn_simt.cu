@@ -89,7 +89,7 @@ __global__ void k_chunk_table(const int32_t *cu, int N, int T_total, int2 *table
     }
     const int used = s_bad ? 0 : min(s_base, slots);
     for (int i = used + tid; i < slots; i += 1024) table[i] = make_int2(-1, -1);
-    if (tid == 0 && s_bad) set_error(err, kErrSeqlens);
+    if (tid == 0 && s_bad) set_error(err, kErrBadIndex);
 }
 
 template <typename TIn>
@@ -110,7 +110,7 @@ k_simt_prep(FwdArgs a, const int2 *__restrict__ table, float *__restrict__ W,
     }
     const int h = blockIdx.y;
     if (!seq_ok(a.sm, n)) {
-        if (tid == 0) set_error(err, kErrSeqlens);
+        if (tid == 0) set_error(err, kErrBadIndex);
         return;
     }
     long long row0;
@@ -199,7 +199,7 @@ k_simt_state(FwdArgs a, const float *__restrict__ W, const float *__restrict__ U
     const int n = blockIdx.x, h = blockIdx.y, dv0 = blockIdx.z * kDvt;
     const int nv = min(kDvt, dv - dv0);
     if (!seq_ok(a.sm, n)) {
-        if (tid == 0) set_error(err, kErrSeqlens);
+        if (tid == 0) set_error(err, kErrBadIndex);
         return;
     }
     long long row0;

@@ -238,7 +238,7 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
         zcoord = n * p.sm.H + h;
     }
     if (!ok_seq) {
-        if (tid == 0) atomicCAS(p.err, 0, kErrSeqlens);
+        if (tid == 0) atomicCAS(p.err, 0, kErrBadIndex);
         return;  // before any barrier or TMEM use
     }
     const int nch = (len + kC - 1) / kC;

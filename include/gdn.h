@@ -167,6 +167,31 @@ uint64_t gdn_kernel_launches(void);
  * (GDN_IMPL_SIMT or GDN_IMPL_TC), 0 before the first call. */
 int gdn_last_impl(void);
 
+/*
+ * One decode step for a batch of sequences ("Gated DeltaNet GPU并行实现",
+ * sections 2.1-2.2: the per-token update with the scalar gate absorbed into
+ * the state): for every (sequence b, head h), with S the d_v x d_k state and
+ * one new token,
+ *     S <- alpha S (I - beta k k^T) + beta v k^T,    o = S q,
+ * alpha = exp(log_alpha) -- gdn_fwd with T = 1 and h0 = hT = the state.
+ * Each row of S is updated independently (row i needs only its own S k and
+ * S q), so the step is one read and one write of the state: bound by HBM.
+ *   q, k        [B][H][d_k] of `dt`;   v, o  [B][H][d_v] of `dt`.
+ *   log_alpha, beta  [B][H] fp32.
+ *   state       fp32 states, read and overwritten in place: [B][H][d_v][d_k]
+ *               when slots is NULL, else a pool [n_slots][H][d_v][d_k] in
+ *               which sequence b uses state slots[b] (slots: DEVICE int32
+ *               [B], distinct; a slot outside [0, n_slots) is reported by
+ *               gdn_sync_check() as GDN_ERR_INVALID_ARG and that sequence is
+ *               left untouched).
+ *   d_k         32, 64 or 128 (GDN_ERR_UNSUPPORTED else); d_v >= 1.
+ * Pointers 16-byte aligned (GDN_ERR_ALIGNMENT).  No scratch memory.
+ */
+gdn_status gdn_decode(const void *q, const void *k, const void *v,
+                      const float *log_alpha, const float *beta, float *state,
+                      const int32_t *slots, int n_slots, void *o,
+                      int B, int H, int d_k, int d_v, gdn_dtype dt, void *stream);
+
 /* Returns the scratch memory the current device's pool holds (memory of
  * calls still in flight stays until they finish) to the driver.  No paper
  * counterpart: a memory-management hook.  GDN_OK, or GDN_ERR_CUDA. */

@@ -26,7 +26,8 @@ import numpy as np
 import torch
 
 # The workloads, by name.  "gdn_fwd_b4_h16_t4096_d128_bf16" is the headline
-# throughput workload; the rest are parity cases.
+# throughput workload; the other gdn_fwd ones are parity cases, and the
+# gdn_decode one times the single-token step.
 WORKLOADS = {
     "gdn_fwd_b1_h1_t256_d64_fp32": dict(B=1, H=1, T=256, dk=64, dv=64, io="f32",
                                         decay="fast", h0_std=0.0, seed=1),
@@ -39,6 +40,9 @@ WORKLOADS = {
     "gdn_fwd_varlen_n64_h32_dk128_dv256_bf16": dict(N=64, len_min=128, len_max=16384, H=32,
                                                     dk=128, dv=256, io="bf16", decay="fast",
                                                     h0_std=0.02, seed=5),
+    # one decode step over 256 sequences x 32 heads: 537 MB of fp32 state
+    "gdn_decode_b256_h32_d128_bf16": dict(kind="decode", B=256, H=32, dk=128, dv=128,
+                                          io="bf16", decay="fast", state_std=0.02, seed=6),
 }
 
 IO_DTYPES = {"f32": torch.float32, "bf16": torch.bfloat16}
@@ -54,6 +58,7 @@ class Inputs:
     h0: torch.Tensor | None
     cu_seqlens: torch.Tensor | None = None   # int32, packed batches only
     meta: dict = field(default_factory=dict)
+    slots: torch.Tensor | None = None        # int32 state slots, decode steps only
 
     def tensors(self):
         return dict(q=self.q, k=self.k, v=self.v, log_alpha=self.log_alpha, beta=self.beta,
@@ -131,9 +136,35 @@ def make_varlen(lengths, H, dk, dv, *, io="bf16", decay="fast", h0_std=0.0, seed
                        h0_std=h0_std, seed=seed))
 
 
+def make_decode(B, H, dk, dv, *, io="bf16", decay="fast", state_std=0.02, n_slots=None,
+                seed=0, device="cpu") -> Inputs:
+    """One decode step: q,k [B,H,dk], v [B,H,dv], gates [B,H], and the fp32
+    states in `h0`: [B,H,dv,dk], or a pool [n_slots,H,dv,dk] with `slots` a
+    seeded choice of B distinct slots (int32 [B])."""
+    g = _gen(device, seed)
+    dt = IO_DTYPES[io]
+    q = _unit_rows(_normal((B, H, dk), g, device)).to(dt)
+    k = _unit_rows(_normal((B, H, dk), g, device)).to(dt)
+    v = _normal((B, H, dv), g, device).to(dt)
+    la, beta = _gates((B, H), g, device, decay)
+    P = B if n_slots is None else n_slots
+    state = _normal((P, H, dv, dk), g, device, std=state_std)
+    slots = None
+    if n_slots is not None:
+        perm = np.random.default_rng(int(seed)).permutation(n_slots)[:B]
+        slots = torch.tensor(perm, dtype=torch.int32, device=device)
+    return Inputs(q, k, v, la, beta, state, None,
+                  dict(kind="decode", B=B, H=H, dk=dk, dv=dv, io=io, decay=decay,
+                       state_std=state_std, n_slots=n_slots, seed=seed), slots)
+
+
 def make_workload(name, device="cpu", **override) -> Inputs:
     cfg = dict(WORKLOADS[name])
     cfg.update(override)
+    if cfg.get("kind") == "decode":
+        return make_decode(cfg["B"], cfg["H"], cfg["dk"], cfg["dv"], io=cfg["io"],
+                           decay=cfg["decay"], state_std=cfg["state_std"], seed=cfg["seed"],
+                           device=device)
     if "N" in cfg:
         lengths = cfg.pop("lengths", None)
         if lengths is None:

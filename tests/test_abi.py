@@ -86,6 +86,21 @@ def test_host_checks(lib):
     assert g(*_args(), FAKE, 0, 1, 0, 64, 64, 64, 1, None) == gdn.GDN_OK
 
 
+def test_decode_host_checks(lib):
+    f = lib.gdn_decode
+    a = [FAKE] * 6 + [None, 0, FAKE]
+    assert f(*a, 2, 2, 48, 64, 1, None) == gdn.GDN_ERR_UNSUPPORTED    # d_k
+    assert f(*a, 2, 2, 64, 0, 1, None) == gdn.GDN_ERR_INVALID_ARG     # d_v
+    assert f(*a, 2, 2, 64, 64, 3, None) == gdn.GDN_ERR_INVALID_ARG    # dtype
+    assert f(*a, -1, 2, 64, 64, 1, None) == gdn.GDN_ERR_INVALID_ARG   # B
+    assert f(*a, 0, 2, 64, 64, 1, None) == gdn.GDN_OK                 # nothing to do
+    slots = [FAKE] * 6 + [FAKE, 0, FAKE]
+    assert f(*slots, 2, 2, 64, 64, 1, None) == gdn.GDN_ERR_INVALID_ARG  # empty pool
+    mis = list(a)
+    mis[5] = FAKE + 8
+    assert f(*mis, 2, 2, 64, 64, 1, None) == gdn.GDN_ERR_ALIGNMENT
+
+
 def test_binding_fails_loudly_without_library(tmp_path):
     with pytest.raises(ImportError):
         gdn.load(str(tmp_path / "missing.so"))
