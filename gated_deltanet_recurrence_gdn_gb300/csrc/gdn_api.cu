@@ -15,6 +15,7 @@ std::atomic<uint64_t> g_launches{0};
 std::atomic<long long> g_opt_impl{GDN_IMPL_AUTO};
 std::atomic<long long> g_opt_segments{0};
 std::atomic<long long> g_opt_wait_limit{0};
+std::atomic<long long> g_opt_poison{0};
 std::atomic<int> g_last_impl{0};
 
 struct TimerState {
@@ -98,7 +99,9 @@ cudaError_t scratch_alloc(void **p, size_t bytes, cudaStream_t st) {
     cudaMemPool_t pool;
     cudaError_t e = scratch_pool(&pool);
     if (e != cudaSuccess) return e;
-    return cudaMallocFromPoolAsync(p, bytes, pool, st);
+    if ((e = cudaMallocFromPoolAsync(p, bytes, pool, st)) != cudaSuccess) return e;
+    if (g_opt_poison.load()) e = cudaMemsetAsync(*p, 0xFF, bytes, st);
+    return e;
 }
 
 cudaError_t scratch_free(void *p, cudaStream_t st) { return cudaFreeAsync(p, st); }
@@ -143,6 +146,7 @@ long long option(int key) {
         case GDN_OPT_IMPL: return g_opt_impl.load();
         case GDN_OPT_SEGMENTS: return g_opt_segments.load();
         case GDN_OPT_WAIT_LIMIT: return g_opt_wait_limit.load();
+        case GDN_OPT_POISON_SCRATCH: return g_opt_poison.load();
         default: return -1;
     }
 }
@@ -262,6 +266,10 @@ gdn_status gdn_set_option(int key, long long value) {
         case GDN_OPT_WAIT_LIMIT:
             if (value < 0) return GDN_ERR_INVALID_ARG;
             g_opt_wait_limit.store(value);
+            return GDN_OK;
+        case GDN_OPT_POISON_SCRATCH:
+            if (value != 0 && value != 1) return GDN_ERR_INVALID_ARG;
+            g_opt_poison.store(value);
             return GDN_OK;
         default:
             return GDN_ERR_INVALID_ARG;

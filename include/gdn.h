@@ -142,9 +142,13 @@ gdn_status gdn_sync_check(void *stream);
  *                      (sequence, head) in the tensor-core path's segment scan;
  *                      1 disables the scan.
  *   GDN_OPT_WAIT_LIMIT: iteration cap of device-side bounded waits (0 = default).
+ *   GDN_OPT_POISON_SCRATCH: 1 fills every scratch block with 0xFF bytes (NaN
+ *                      in bf16 and fp32) when it is handed out, so that a read
+ *                      of scratch no kernel wrote shows up in the results; 0
+ *                      (default) leaves it as the pool returns it.
  * Returns GDN_ERR_INVALID_ARG for an unknown key or value.
  */
-enum { GDN_OPT_IMPL = 0, GDN_OPT_SEGMENTS = 1, GDN_OPT_WAIT_LIMIT = 2 };
+enum { GDN_OPT_IMPL = 0, GDN_OPT_SEGMENTS = 1, GDN_OPT_WAIT_LIMIT = 2, GDN_OPT_POISON_SCRATCH = 3 };
 enum { GDN_IMPL_AUTO = 0, GDN_IMPL_SIMT = 1, GDN_IMPL_TC = 2 };
 gdn_status gdn_set_option(int key, long long value);
 long long gdn_get_option(int key);

@@ -6,8 +6,14 @@ from __future__ import annotations
 import numpy as np
 import torch
 
+import gated_deltanet_recurrence_gdn_gb300 as gdn
 import oracle
 import synth
+
+# Every GPU test runs with poisoned scratch: blocks the library hands out are
+# filled with NaN bytes first, so a kernel that reads scratch nobody wrote
+# fails its parity check instead of passing on leftovers of an earlier call.
+gdn.set_option(gdn.GDN_OPT_POISON_SCRATCH, 1)
 
 # fp32 I/O: 1e-4 on o and hT; bf16 I/O: 1e-2 on o, 2e-2 on hT.
 TOL = {"f32": (1e-4, 1e-4), "bf16": (1e-2, 2e-2)}

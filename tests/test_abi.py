@@ -54,6 +54,11 @@ def test_options_roundtrip(lib):
     assert lib.gdn_set_option(gdn.GDN_OPT_IMPL, 9) == gdn.GDN_ERR_INVALID_ARG
     assert lib.gdn_set_option(77, 0) == gdn.GDN_ERR_INVALID_ARG
     assert lib.gdn_set_option(gdn.GDN_OPT_IMPL, gdn.GDN_IMPL_AUTO) == gdn.GDN_OK
+    prev = lib.gdn_get_option(gdn.GDN_OPT_POISON_SCRATCH)
+    assert lib.gdn_set_option(gdn.GDN_OPT_POISON_SCRATCH, 1) == gdn.GDN_OK
+    assert lib.gdn_get_option(gdn.GDN_OPT_POISON_SCRATCH) == 1
+    assert lib.gdn_set_option(gdn.GDN_OPT_POISON_SCRATCH, 2) == gdn.GDN_ERR_INVALID_ARG
+    assert lib.gdn_set_option(gdn.GDN_OPT_POISON_SCRATCH, prev) == gdn.GDN_OK
 
 
 # Host-only validation: these calls must return before any CUDA call, so fake
