@@ -52,6 +52,7 @@ ABI = [
     ("gdn_fwd_varlen", _i, [_vp] * 9 + [_i] * 7 + [_vp]),
     ("gdn_fwd_noalloc", _i, [_vp] * 8 + [_i] * 7 + [_vp]),
     ("gdn_decode", _i, [_vp] * 7 + [_i] + [_vp] + [_i] * 5 + [_vp]),
+    ("gdn_fwd_host", _i, [_vp] * 8 + [_i] * 7 + [_vp]),
     ("gdn_status_string", ctypes.c_char_p, [_i]),
     ("gdn_sync_check", _i, [_vp]),
     ("gdn_set_option", _i, [_i, ctypes.c_longlong]),
@@ -198,6 +199,43 @@ def gdn_fwd_noalloc(q, k, v, log_alpha, beta, h0=None, *, chunk=CHUNK, out=None,
         _check(rc, "gdn_fwd_noalloc")
         if check:
             _check(lib.gdn_sync_check(_stream(q.device)), "gdn_fwd_noalloc (device)")
+    return o, hT
+
+
+def gdn_fwd_host(q, k, v, log_alpha, beta, h0=None, *, chunk=CHUNK, out=None, final_state=True,
+                 final_out=None, sync=True, device=None):
+    """Dense forward on HOST tensors (page-locked for overlapped copies): the
+    library uploads, computes and downloads in a pipeline over time slices.
+    Returns host (o, hT); `out` / `final_out` receive them when given.  With
+    sync=False the caller synchronises the current stream of `device` before
+    reading the results."""
+    lib = load()
+    for name, t in (("q", q), ("k", k), ("v", v), ("log_alpha", log_alpha), ("beta", beta)):
+        if not isinstance(t, torch.Tensor) or t.is_cuda or not t.is_contiguous():
+            raise ValueError("%s must be a contiguous host tensor" % name)
+    if q.dtype not in _DT or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v must share one dtype, bf16 or fp32")
+    if log_alpha.dtype != torch.float32 or beta.dtype != torch.float32:
+        raise ValueError("log_alpha and beta must be fp32")
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    if k.shape != q.shape or v.shape[:3] != (B, H, T) or log_alpha.shape != (B, H, T) \
+            or beta.shape != (B, H, T):
+        raise ValueError("shape mismatch")
+    if h0 is not None and (h0.is_cuda or h0.dtype != torch.float32 or not h0.is_contiguous()
+                           or h0.shape != (B, H, dv, dk)):
+        raise ValueError("h0 must be a contiguous fp32 host tensor [B,H,d_v,d_k]")
+    o = out if out is not None else torch.empty((B, H, T, dv), dtype=q.dtype).pin_memory()
+    hT = final_out if final_out is not None else (
+        torch.empty((B, H, dv, dk), dtype=torch.float32).pin_memory() if final_state else None)
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    with torch.cuda.device(dev):
+        rc = lib.gdn_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(h0),
+                              _ptr(o), _ptr(hT), B, H, T, dk, dv, chunk, _DT[q.dtype],
+                              _stream(dev))
+        _check(rc, "gdn_fwd_host")
+        if sync:
+            _check(lib.gdn_sync_check(_stream(dev)), "gdn_fwd_host (device)")
     return o, hT
 
 

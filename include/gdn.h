@@ -172,6 +172,26 @@ uint64_t gdn_kernel_launches(void);
 int gdn_last_impl(void);
 
 /*
+ * Dense forward pass on HOST buffers (no paper counterpart: the same
+ * computation as gdn_fwd with the host <-> device traffic inside the call).
+ * Arguments and layouts as gdn_fwd, but q, k, v, log_alpha, beta, h0 (or
+ * NULL) are host inputs and o, hT (or NULL) host outputs.  The call cuts T
+ * into chunk-aligned slices of about 512 tokens and pipelines, on internal
+ * streams, the upload of slice i + 1, the device pass over slice i (the fp32
+ * state handed over in device memory) and the download of slice i - 1; it
+ * returns once everything is enqueued, with `stream` made to wait for the
+ * last download: synchronise `stream` before reading o / hT, and keep every
+ * buffer alive and unchanged until then.  Page-locked host memory lets the
+ * copies overlap; pageable memory works without overlap.  Device scratch
+ * (three slice buffers and two states) comes from the library's pool.
+ */
+gdn_status gdn_fwd_host(const void *q, const void *k, const void *v,
+                        const float *log_alpha, const float *beta, const float *h0,
+                        void *o, float *hT,
+                        int B, int H, int T, int d_k, int d_v, int chunk,
+                        gdn_dtype dt, void *stream);
+
+/*
  * One decode step for a batch of sequences ("Gated DeltaNet GPU并行实现",
  * sections 2.1-2.2: the per-token update with the scalar gate absorbed into
  * the state): for every (sequence b, head h), with S the d_v x d_k state and
