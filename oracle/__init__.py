@@ -64,6 +64,10 @@ def load_library(path: str):
     lib.gdn_oracle_fwd.argtypes = [_dp] * 8 + [ctypes.c_long] * 5
     lib.gdn_oracle_fwd_varlen.restype = ctypes.c_int
     lib.gdn_oracle_fwd_varlen.argtypes = [_dp] * 8 + [_lp] + [ctypes.c_long] * 5
+    lib.gdn_oracle_gla_fwd.restype = ctypes.c_int
+    lib.gdn_oracle_gla_fwd.argtypes = [_dp] * 8 + [ctypes.c_long] * 5
+    lib.gdn_oracle_gla_fwd_varlen.restype = ctypes.c_int
+    lib.gdn_oracle_gla_fwd_varlen.argtypes = [_dp] * 8 + [_lp] + [ctypes.c_long] * 5
     return lib
 
 
@@ -82,10 +86,13 @@ def _ptr(a):
     return None if a is None else a.ctypes.data_as(_dp)
 
 
-def gdn_fwd(q, k, v, log_alpha, beta, h0=None, *, threads: int = 1, lib=None):
+def gdn_fwd(q, k, v, log_alpha, beta, h0=None, *, threads: int = 1, lib=None, erase=True):
     """Dense oracle.  q,k [B,H,T,dk]; v [B,H,T,dv]; log_alpha, beta [B,H,T];
-    h0 [B,H,dv,dk] or None.  Returns (o [B,H,T,dv], hT [B,H,dv,dk]) in fp64."""
+    h0 [B,H,dv,dk] or None.  Returns (o [B,H,T,dv], hT [B,H,dv,dk]) in fp64.
+    erase=False runs gated linear attention (the recurrence without the
+    delta rule's erase term)."""
     lib = lib or _get()
+    fwd = lib.gdn_oracle_fwd if erase else lib.gdn_oracle_gla_fwd
     q, k, v = _f64(q), _f64(k), _f64(v)
     la, be = _f64(log_alpha), _f64(beta)
     B, H, T, dk = q.shape
@@ -99,7 +106,7 @@ def gdn_fwd(q, k, v, log_alpha, beta, h0=None, *, threads: int = 1, lib=None):
     hT = np.zeros((B, H, dv, dk), dtype=np.float64)
 
     def run(b, h):
-        rc = lib.gdn_oracle_fwd(_ptr(q[b, h]), _ptr(k[b, h]), _ptr(v[b, h]),
+        rc = fwd(_ptr(q[b, h]), _ptr(k[b, h]), _ptr(v[b, h]),
                                 _ptr(la[b, h]), _ptr(be[b, h]),
                                 None if h0 is None else _ptr(h0[b, h]),
                                 _ptr(o[b, h]), _ptr(hT[b, h]), 1, 1, T, dk, dv)
@@ -117,11 +124,14 @@ def gdn_fwd(q, k, v, log_alpha, beta, h0=None, *, threads: int = 1, lib=None):
 
 
 def gdn_fwd_varlen(q, k, v, log_alpha, beta, cu_seqlens, h0=None, *, threads: int = 1,
-                   lib=None):
+                   lib=None, erase=True):
     """Packed oracle.  q,k [H,T_total,dk]; v [H,T_total,dv]; log_alpha, beta
     [H,T_total]; cu_seqlens [N+1]; h0 [N,H,dv,dk] or None.
-    Returns (o [H,T_total,dv], hT [N,H,dv,dk]) in fp64."""
+    Returns (o [H,T_total,dv], hT [N,H,dv,dk]) in fp64.  erase=False runs
+    gated linear attention."""
     lib = lib or _get()
+    fwd = lib.gdn_oracle_fwd if erase else lib.gdn_oracle_gla_fwd
+    fwd_varlen = lib.gdn_oracle_fwd_varlen if erase else lib.gdn_oracle_gla_fwd_varlen
     q, k, v = _f64(q), _f64(k), _f64(v)
     la, be = _f64(log_alpha), _f64(beta)
     cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int64))
@@ -134,7 +144,7 @@ def gdn_fwd_varlen(q, k, v, log_alpha, beta, cu_seqlens, h0=None, *, threads: in
     o = np.zeros((H, TT, dv), dtype=np.float64)
     hT = np.zeros((N, H, dv, dk), dtype=np.float64)
     if threads <= 1 or N * H <= 1:
-        rc = lib.gdn_oracle_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(la), _ptr(be),
+        rc = fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(la), _ptr(be),
                                        _ptr(h0), _ptr(o), _ptr(hT),
                                        cu.ctypes.data_as(_lp), N, H, TT, dk, dv)
         if rc != 0:
@@ -147,7 +157,7 @@ def gdn_fwd_varlen(q, k, v, log_alpha, beta, cu_seqlens, h0=None, *, threads: in
         t0, t1 = int(cu[n]), int(cu[n + 1])
         ob = np.zeros((t1 - t0, dv), dtype=np.float64)
         hb = np.zeros((dv, dk), dtype=np.float64)
-        rc = lib.gdn_oracle_fwd(_ptr(np.ascontiguousarray(q[h, t0:t1])),
+        rc = fwd(_ptr(np.ascontiguousarray(q[h, t0:t1])),
                                 _ptr(np.ascontiguousarray(k[h, t0:t1])),
                                 _ptr(np.ascontiguousarray(v[h, t0:t1])),
                                 _ptr(np.ascontiguousarray(la[h, t0:t1])),

@@ -25,6 +25,16 @@
  * page's own expansion gives, so that is the form used here.  No 1/sqrt(d)
  * scaling is applied to q; the output is inclusive (o_t sees token t).
  *
+ * The second half of the file is gated linear attention, the same
+ * recurrence without the delta rule's erase term ("线性注意力机制与Gated
+ * DeltaNet的优化实践", sections 2.2-2.3: the linear-attention state
+ * S_i = S_{i-1} + k_i v_i^T and its gated form with a forget gate and an
+ * update gate, both scalars here):
+ *
+ *     S_t = alpha_t * S_{t-1} + beta_t v_t k_t^T,     o_t = S_t q_t
+ *
+ * (alpha = beta = 1 is plain linear attention), in the same layouts.
+ *
  * Parity pins for this file (closed forms, invariants, reductions to linear
  * attention, planted-mistake checks) live in tests/test_oracle_pins.py.
  */
@@ -163,5 +173,101 @@ int gdn_oracle_fwd_varlen(const double *q, const double *k, const double *v,
     }
     free(S);
     free(kS);
+    return 0;
+}
+
+/*
+ * Gated linear attention, one (sequence, head): the loop above with the
+ * erase term left out.  Same arguments; S is caller scratch of dv*dk doubles.
+ */
+static void oracle_one_gla(const double *q, const double *k, const double *v,
+                           const double *la, const double *beta,
+                           const double *h0, double *o, double *hT,
+                           long T, long dk, long dv, double *S)
+{
+    long t, i, j;
+    if (h0)
+        memcpy(S, h0, sizeof(double) * (size_t)(dv * dk));
+    else
+        memset(S, 0, sizeof(double) * (size_t)(dv * dk));
+    for (t = 0; t < T; ++t) {
+        const double *kt = k + t * dk;
+        const double *vt = v + t * dv;
+        const double *qt = q + t * dk;
+        const double g = exp(la[t]);
+        const double w = beta[t];
+        for (i = 0; i < dv; ++i)
+            for (j = 0; j < dk; ++j)
+                S[i * dk + j] = g * S[i * dk + j] + w * vt[i] * kt[j];
+        if (o) {
+            for (i = 0; i < dv; ++i) {
+                double sum = 0.0;
+                for (j = 0; j < dk; ++j)
+                    sum += S[i * dk + j] * qt[j];
+                o[t * dv + i] = sum;
+            }
+        }
+    }
+    if (hT)
+        memcpy(hT, S, sizeof(double) * (size_t)(dv * dk));
+}
+
+/* Dense batch, gated linear attention (layouts as gdn_oracle_fwd). */
+int gdn_oracle_gla_fwd(const double *q, const double *k, const double *v,
+                       const double *log_alpha, const double *beta,
+                       const double *h0, double *o, double *hT,
+                       long B, long H, long T, long dk, long dv)
+{
+    long bh;
+    double *S;
+    if (B < 0 || H < 0 || T < 0 || dk <= 0 || dv <= 0)
+        return -1;
+    S = (double *)malloc(sizeof(double) * (size_t)(dv * dk));
+    if (!S)
+        return -1;
+    for (bh = 0; bh < B * H; ++bh)
+        oracle_one_gla(q + bh * T * dk, k + bh * T * dk, v + bh * T * dv,
+                       log_alpha + bh * T, beta + bh * T,
+                       h0 ? h0 + bh * dv * dk : NULL,
+                       o ? o + bh * T * dv : NULL,
+                       hT ? hT + bh * dv * dk : NULL,
+                       T, dk, dv, S);
+    free(S);
+    return 0;
+}
+
+/* Packed batch, gated linear attention (layouts as gdn_oracle_fwd_varlen). */
+int gdn_oracle_gla_fwd_varlen(const double *q, const double *k, const double *v,
+                              const double *log_alpha, const double *beta,
+                              const double *h0, double *o, double *hT,
+                              const long *cu_seqlens, long N, long H, long T_total,
+                              long dk, long dv)
+{
+    long n, h;
+    double *S;
+    if (N < 0 || H < 0 || T_total < 0 || dk <= 0 || dv <= 0)
+        return -1;
+    if (N > 0 && (cu_seqlens[0] != 0 || cu_seqlens[N] != T_total))
+        return -1;
+    for (n = 0; n < N; ++n)
+        if (cu_seqlens[n + 1] < cu_seqlens[n])
+            return -1;
+    S = (double *)malloc(sizeof(double) * (size_t)(dv * dk));
+    if (!S)
+        return -1;
+    for (n = 0; n < N; ++n) {
+        long s0 = cu_seqlens[n];
+        long len = cu_seqlens[n + 1] - s0;
+        for (h = 0; h < H; ++h) {
+            long rw = h * T_total + s0;
+            oracle_one_gla(q + rw * dk, k + rw * dk, v + rw * dv,
+                           log_alpha + rw, beta + rw,
+                           h0 ? h0 + (n * H + h) * dv * dk : NULL,
+                           o ? o + rw * dv : NULL,
+                           hT ? hT + (n * H + h) * dv * dk : NULL,
+                           len, dk, dv, S);
+        }
+    }
+    free(S);
     return 0;
 }

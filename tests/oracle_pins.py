@@ -11,7 +11,10 @@ in the wrong order is the classic bug and recommends checking tiny random
 problems (d = 2) against the naive loop.  The reduction to (gated) linear
 attention follows the linear-attention recurrence of "线性注意力机制与Gated
 DeltaNet的优化实践" sections 2.2-2.3, with the erase term vanishing for
-mutually orthogonal keys.
+mutually orthogonal keys.  The gated-linear-attention loop (the recurrence
+without the erase term, same page sections 2.2-2.3) is pinned to its
+unrolled closed form, to plain linear attention, and to the delta rule where
+the two coincide.
 """
 from __future__ import annotations
 
@@ -246,6 +249,89 @@ def pin_norm_bound(lib, dk=6, dv=4, T=25, seed=9):
     return max(worst, 0.0)
 
 
+def _gla_closed_form(q, k, v, la, be, h0):
+    """Gated linear attention written out as masked decayed attention
+    ("线性注意力机制与Gated DeltaNet的优化实践" sections 2.2-2.3 unrolled):
+    o_t = sum_{s<=t} exp(G_t - G_s) beta_s (q_t . k_s) v_s + exp(G_t) h0 q_t,
+    hT = exp(G_T) h0 + sum_s exp(G_T - G_s) beta_s v_s k_s^T, G the
+    cumulative log gate."""
+    T = la.shape[-1]
+    if T == 0:
+        dv, dk = v.shape[-1], q.shape[-1]
+        o = np.zeros(q.shape[:-1] + (dv,))
+        hT = np.zeros(q.shape[:2] + (dv, dk)) if h0 is None else h0.copy()
+        return o, hT
+    G = np.cumsum(la, axis=-1)                                     # [B,H,T]
+    mask = np.tril(np.ones((T, T)))
+    dec = np.exp(G[..., :, None] - G[..., None, :]) * mask         # [B,H,T,T]
+    P = np.einsum("bhtd,bhsd->bhts", q, k) * dec * be[..., None, :]
+    o = np.einsum("bhts,bhsi->bhti", P, v)
+    hT = np.einsum("bhs,bhsi,bhsj->bhij", np.exp(G[..., -1:] - G) * be, v, k)
+    if h0 is not None:
+        o = o + np.exp(G)[..., None] * np.einsum("bhij,bhtj->bhti", h0, q)
+        hT = hT + np.exp(G[..., -1])[..., None, None] * h0
+    return o, hT
+
+
+def pin_gla_closed_form(lib, dk=5, dv=4, T=13, seed=21):
+    """The oracle's gated linear attention equals its unrolled closed form,
+    with an initial state, gates and write strengths drawn at random."""
+    rng = np.random.default_rng(seed)
+    q, k, v, la, be = _rand_inputs(rng, 2, 2, T, dk, dv, unit_k=False)
+    h0 = rng.standard_normal((2, 2, dv, dk))
+    o, hT = oracle.gdn_fwd(q, k, v, la, be, h0, lib=lib, erase=False)
+    o_ref, hT_ref = _gla_closed_form(q, k, v, la, be, h0)
+    return max(_rel(o, o_ref), _rel(hT, hT_ref))
+
+
+def pin_gla_linear_attention(lib, dk=4, dv=6, T=11, seed=22):
+    """alpha = beta = 1, no initial state: plain linear attention,
+    z_i = sum_{j<=i} (q_i . k_j) v_j (the first formula of section 2.2),
+    i.e. the causally masked (Q K^T) V."""
+    rng = np.random.default_rng(seed)
+    q, k, v, _, _ = _rand_inputs(rng, 1, 1, T, dk, dv, unit_k=False)
+    ones = np.ones((1, 1, T))
+    o, hT = oracle.gdn_fwd(q, k, v, 0 * ones, ones, None, lib=lib, erase=False)
+    o_ref = np.tril(q[0, 0] @ k[0, 0].T) @ v[0, 0]
+    hT_ref = v[0, 0].T @ k[0, 0]
+    return max(_rel(o[0, 0], o_ref), _rel(hT[0, 0], hT_ref))
+
+
+def pin_gla_equals_delta_on_orthogonal_keys(lib, dk=8, dv=5, T=8, seed=23):
+    """With a zero initial state and mutually orthogonal keys the delta rule
+    never erases anything (S_{t-1} k_t = 0), so both loops must agree."""
+    rng = np.random.default_rng(seed)
+    q, _, v, la, be = _rand_inputs(rng, 1, 1, T, dk, dv)
+    k = _orthogonal_keys(rng, T, dk)[None, None]
+    a = oracle.gdn_fwd(q, k, v, la, be, None, lib=lib)
+    b = oracle.gdn_fwd(q, k, v, la, be, None, lib=lib, erase=False)
+    return max(_rel(b[0], a[0]), _rel(b[1], a[1]))
+
+
+def pin_gla_varlen_split(lib, dk=4, dv=3, H=2, seed=24):
+    """Packed gated linear attention equals per-sequence dense calls."""
+    rng = np.random.default_rng(seed)
+    lens = [5, 0, 9, 1]
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    TT = int(cu[-1])
+    q = rng.standard_normal((H, TT, dk))
+    k = rng.standard_normal((H, TT, dk))
+    v = rng.standard_normal((H, TT, dv))
+    la = -rng.uniform(0, 1, (H, TT))
+    be = rng.uniform(0, 1, (H, TT))
+    h0 = rng.standard_normal((len(lens), H, dv, dk))
+    o, hT = oracle.gdn_fwd_varlen(q, k, v, la, be, cu, h0, lib=lib, erase=False)
+    worst = 0.0
+    for n, (a, b) in enumerate(zip(cu[:-1], cu[1:])):
+        s = np.s_[:, a:b]
+        od, hd = _gla_closed_form(q[s][None], k[s][None], v[s][None], la[s][None],
+                                  be[s][None], h0[n][None])
+        worst = max(worst, _rel(hT[n], hd[0]))
+        if b > a:
+            worst = max(worst, _rel(o[:, a:b], od[0]))
+    return worst
+
+
 ALL_PINS = {
     "beta_zero": pin_beta_zero,
     "exact_recall": pin_exact_recall,
@@ -256,4 +342,8 @@ ALL_PINS = {
     "continuation": pin_continuation,
     "varlen_split": pin_varlen_split,
     "norm_bound": pin_norm_bound,
+    "gla_closed_form": pin_gla_closed_form,
+    "gla_linear_attention": pin_gla_linear_attention,
+    "gla_equals_delta_on_orthogonal_keys": pin_gla_equals_delta_on_orthogonal_keys,
+    "gla_varlen_split": pin_gla_varlen_split,
 }

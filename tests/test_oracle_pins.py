@@ -81,6 +81,15 @@ MUTANTS = {
     "gate_not_exponentiated": ("const double a = exp(la[t]);", "const double a = 1.0 + la[t];"),
     "h0_ignored": ("if (h0)\n        memcpy", "if (0)\n        memcpy"),
     "varlen_offset": ("long row = h * T_total + t0;", "long row = h * T_total + t0 / 2;"),
+    # the gated-linear-attention loop
+    "gla_alpha_dropped": ("g * S[i * dk + j] + w", "S[i * dk + j] + w"),
+    "gla_beta_dropped": ("+ w * vt[i] * kt[j];", "+ vt[i] * kt[j];"),
+    "gla_alpha_on_write": ("+ w * vt[i] * kt[j];", "+ g * w * vt[i] * kt[j];"),
+    "gla_gate_not_exponentiated": ("const double g = exp(la[t]);", "const double g = 1.0 + la[t];"),
+    "gla_output_transposed": ("sum += S[i * dk + j] * qt[j];", "sum += S[j * dk + i] * qt[j];"),
+    "gla_h0_ignored": ("if (h0)\n        memcpy(S, h0, sizeof(double) * (size_t)(dv * dk));\n    else\n        memset(S, 0, sizeof(double) * (size_t)(dv * dk));\n    for (t = 0; t < T; ++t) {\n        const double *kt = k + t * dk;\n        const double *vt = v + t * dv;\n        const double *qt = q + t * dk;\n        const double g",
+                       "if (0)\n        memcpy(S, h0, sizeof(double) * (size_t)(dv * dk));\n    else\n        memset(S, 0, sizeof(double) * (size_t)(dv * dk));\n    for (t = 0; t < T; ++t) {\n        const double *kt = k + t * dk;\n        const double *vt = v + t * dv;\n        const double *qt = q + t * dk;\n        const double g"),
+    "gla_varlen_offset": ("long rw = h * T_total + s0;", "long rw = h * T_total + s0 / 2;"),
 }
 
 
@@ -109,5 +118,8 @@ def test_planted_mistake_is_caught(mutant_dir, name):
         "linear_attention": P.pin_linear_attention(mlib, dk=8, dv=8),
         "continuation": P.pin_continuation(mlib, **square),
         "varlen": P.pin_varlen_split(mlib, dk=5, dv=5),
+        "gla_closed_form": P.pin_gla_closed_form(mlib, **square),
+        "gla_linear_attention": P.pin_gla_linear_attention(mlib, **square),
+        "gla_varlen": P.pin_gla_varlen_split(mlib, dk=5, dv=5),
     }
     assert max(errs.values()) > 1e-6, errs
