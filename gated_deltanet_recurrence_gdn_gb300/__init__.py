@@ -53,6 +53,8 @@ ABI = [
     ("gdn_fwd_noalloc", _i, [_vp] * 8 + [_i] * 7 + [_vp]),
     ("gdn_decode", _i, [_vp] * 7 + [_i] + [_vp] + [_i] * 5 + [_vp]),
     ("gdn_fwd_host", _i, [_vp] * 8 + [_i] * 7 + [_vp]),
+    ("gdn_fwd_ex", _i, [_vp] * 8 + [_i] * 7 + [ctypes.c_uint, _vp]),
+    ("gdn_fwd_varlen_ex", _i, [_vp] * 9 + [_i] * 7 + [ctypes.c_uint, _vp]),
     ("gdn_status_string", ctypes.c_char_p, [_i]),
     ("gdn_sync_check", _i, [_vp]),
     ("gdn_set_option", _i, [_i, ctypes.c_longlong]),
@@ -128,9 +130,13 @@ def _prep_io(q, k, v, log_alpha, beta, h0):
         raise ValueError("h0 must be a contiguous fp32 CUDA tensor")
 
 
+GDN_FLAG_NO_ERASE = 1
+
+
 def gdn_fwd(q, k, v, log_alpha, beta, h0=None, *, chunk=CHUNK, out=None, final_state=True,
-            check=False):
-    """Dense forward: returns (o [B,H,T,d_v], hT [B,H,d_v,d_k] or None)."""
+            check=False, erase=True):
+    """Dense forward: returns (o [B,H,T,d_v], hT [B,H,d_v,d_k] or None).
+    erase=False: gated linear attention (no delta-rule erase term)."""
     lib = load()
     _prep_io(q, k, v, log_alpha, beta, h0)
     B, H, T, dk = q.shape
@@ -143,9 +149,10 @@ def gdn_fwd(q, k, v, log_alpha, beta, h0=None, *, chunk=CHUNK, out=None, final_s
     o = out if out is not None else torch.empty((B, H, T, dv), dtype=q.dtype, device=q.device)
     hT = torch.empty((B, H, dv, dk), dtype=torch.float32, device=q.device) if final_state else None
     with torch.cuda.device(q.device):
-        rc = lib.gdn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(h0),
-                         _ptr(o), _ptr(hT), B, H, T, dk, dv, chunk, _DT[q.dtype],
-                         _stream(q.device))
+        args = (_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(h0),
+                _ptr(o), _ptr(hT), B, H, T, dk, dv, chunk, _DT[q.dtype])
+        rc = (lib.gdn_fwd(*args, _stream(q.device)) if erase else
+              lib.gdn_fwd_ex(*args, GDN_FLAG_NO_ERASE, _stream(q.device)))
         _check(rc, "gdn_fwd")
         if check:
             _check(lib.gdn_sync_check(_stream(q.device)), "gdn_fwd (device)")
@@ -153,8 +160,9 @@ def gdn_fwd(q, k, v, log_alpha, beta, h0=None, *, chunk=CHUNK, out=None, final_s
 
 
 def gdn_fwd_varlen(q, k, v, log_alpha, beta, cu_seqlens, h0=None, *, chunk=CHUNK, out=None,
-                   final_state=True, check=False):
-    """Packed forward: returns (o [H,T_total,d_v], hT [N,H,d_v,d_k] or None)."""
+                   final_state=True, check=False, erase=True):
+    """Packed forward: returns (o [H,T_total,d_v], hT [N,H,d_v,d_k] or None).
+    erase=False: gated linear attention (no delta-rule erase term)."""
     lib = load()
     _prep_io(q, k, v, log_alpha, beta, h0)
     H, TT, dk = q.shape
@@ -170,9 +178,11 @@ def gdn_fwd_varlen(q, k, v, log_alpha, beta, cu_seqlens, h0=None, *, chunk=CHUNK
     o = out if out is not None else torch.empty((H, TT, dv), dtype=q.dtype, device=q.device)
     hT = torch.empty((N, H, dv, dk), dtype=torch.float32, device=q.device) if final_state else None
     with torch.cuda.device(q.device):
-        rc = lib.gdn_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
-                                _ptr(h0), _ptr(o), _ptr(hT), _ptr(cu_seqlens.contiguous()), N,
-                                H, TT, dk, dv, chunk, _DT[q.dtype], _stream(q.device))
+        args = (_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(h0), _ptr(o),
+                _ptr(hT), _ptr(cu_seqlens.contiguous()), N, H, TT, dk, dv, chunk,
+                _DT[q.dtype])
+        rc = (lib.gdn_fwd_varlen(*args, _stream(q.device)) if erase else
+              lib.gdn_fwd_varlen_ex(*args, GDN_FLAG_NO_ERASE, _stream(q.device)))
         _check(rc, "gdn_fwd_varlen")
         if check:
             _check(lib.gdn_sync_check(_stream(q.device)), "gdn_fwd_varlen (device)")

@@ -160,6 +160,15 @@ extern "C" {
 gdn_status gdn_fwd(const void *q, const void *k, const void *v, const float *log_alpha,
                    const float *beta, const float *h0, void *o, float *hT, int B, int H, int T,
                    int d_k, int d_v, int chunk, gdn_dtype dt, void *stream) {
+    return gdn_fwd_ex(q, k, v, log_alpha, beta, h0, o, hT, B, H, T, d_k, d_v, chunk, dt, 0u,
+                      stream);
+}
+
+gdn_status gdn_fwd_ex(const void *q, const void *k, const void *v, const float *log_alpha,
+                      const float *beta, const float *h0, void *o, float *hT, int B, int H,
+                      int T, int d_k, int d_v, int chunk, gdn_dtype dt, unsigned flags,
+                      void *stream) {
+    if (flags & ~(unsigned)GDN_FLAG_NO_ERASE) return GDN_ERR_INVALID_ARG;
     if (B < 0 || T < 0) return GDN_ERR_INVALID_ARG;
     const bool tokens = (long long)B * H * T > 0;
     gdn_status rc = check_common(q, k, v, log_alpha, beta, h0, o, hT, H, d_k, d_v, chunk, dt,
@@ -175,6 +184,7 @@ gdn_status gdn_fwd(const void *q, const void *k, const void *v, const float *log
     a.max_chunks = (T + kChunk - 1) / kChunk;
     a.chunk_slots = (int)((long long)B * a.max_chunks);
     a.stream = static_cast<cudaStream_t>(stream);
+    a.no_erase = (flags & GDN_FLAG_NO_ERASE) != 0;
     if ((long long)B * a.max_chunks > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
     return dispatch(a);
 }
@@ -183,6 +193,16 @@ gdn_status gdn_fwd_varlen(const void *q, const void *k, const void *v, const flo
                           const float *beta, const float *h0, void *o, float *hT,
                           const int32_t *cu_seqlens, int N, int H, int T_total, int d_k,
                           int d_v, int chunk, gdn_dtype dt, void *stream) {
+    return gdn_fwd_varlen_ex(q, k, v, log_alpha, beta, h0, o, hT, cu_seqlens, N, H, T_total,
+                             d_k, d_v, chunk, dt, 0u, stream);
+}
+
+gdn_status gdn_fwd_varlen_ex(const void *q, const void *k, const void *v,
+                             const float *log_alpha, const float *beta, const float *h0,
+                             void *o, float *hT, const int32_t *cu_seqlens, int N, int H,
+                             int T_total, int d_k, int d_v, int chunk, gdn_dtype dt,
+                             unsigned flags, void *stream) {
+    if (flags & ~(unsigned)GDN_FLAG_NO_ERASE) return GDN_ERR_INVALID_ARG;
     if (N < 0 || T_total < 0) return GDN_ERR_INVALID_ARG;
     if (N > 0 && !cu_seqlens) return GDN_ERR_INVALID_ARG;
     if (N == 0 && T_total != 0) return GDN_ERR_INVALID_ARG;
@@ -202,6 +222,7 @@ gdn_status gdn_fwd_varlen(const void *q, const void *k, const void *v, const flo
     if (slots > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
     a.chunk_slots = (int)slots;
     a.stream = static_cast<cudaStream_t>(stream);
+    a.no_erase = (flags & GDN_FLAG_NO_ERASE) != 0;
     return dispatch(a);
 }
 

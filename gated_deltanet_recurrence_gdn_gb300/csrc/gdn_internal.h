@@ -51,6 +51,7 @@ struct FwdArgs {
     int max_chunks;       // upper bound on chunks of one sequence
     int chunk_slots;      // upper bound on chunks of all sequences
     cudaStream_t stream;
+    bool no_erase;        // gated linear attention: A = 0, T = I, W = 0
 };
 
 // Stream-ordered scratch from the library's per-device pool, which keeps

@@ -472,6 +472,56 @@ k_gdn_prep(const __nv_bfloat16 *__restrict__ k, const float *__restrict__ log_al
     }
 }
 
+// Gated linear attention (no erase term): A = 0, so T = I, T_u = diag(beta)
+// and W = 0.  One CTA of 64 threads per (chunk slot, head); thread r writes
+// row r of the chunk.
+template <int DK>
+__global__ void __launch_bounds__(64)
+k_gla_prep(const float *__restrict__ beta, SeqMap sm, const int2 *__restrict__ table,
+           int max_chunks, __nv_bfloat16 *__restrict__ Tu_out, __nv_bfloat16 *__restrict__ W_out,
+           int *err) {
+    int n, c;
+    if (table) {
+        const int2 e = table[blockIdx.x];
+        n = e.x;
+        c = e.y;
+        if (n < 0) return;
+    } else {
+        n = blockIdx.x / max_chunks;
+        c = blockIdx.x % max_chunks;
+    }
+    const int h = blockIdx.y, r = threadIdx.x;
+    long long row0;
+    int len;
+    if (sm.cu) {
+        const int a = __ldg(sm.cu + n), b = __ldg(sm.cu + n + 1);
+        if (!(a >= 0 && a <= b && b <= sm.T_total)) {
+            if (r == 0) atomicCAS(err, 0, kErrBadIndex);
+            return;
+        }
+        row0 = (long long)h * sm.T_total + a;
+        len = b - a;
+    } else {
+        row0 = ((long long)n * sm.H + h) * (long long)sm.T;
+        len = sm.T;
+    }
+    const int t0 = c * kCp;
+    if (t0 + r >= len) return;
+    const long long row = row0 + t0 + r;
+    const uint32_t bb = pack2(__ldg(beta + row), 0.f) & 0xffffu;   // bf16 beta in the low half
+    uint4 *tu = reinterpret_cast<uint4 *>(Tu_out + row * kCp);
+#pragma unroll
+    for (int q = 0; q < kCp / 8; ++q) {
+        uint32_t w[4] = {0u, 0u, 0u, 0u};
+        const int e = r - 8 * q;   // position of the diagonal element in this 8-wide piece
+        if (e >= 0 && e < 8) w[e >> 1] = (e & 1) ? (bb << 16) : bb;
+        tu[q] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    uint4 *wr = reinterpret_cast<uint4 *>(W_out + row * DK);
+#pragma unroll
+    for (int q = 0; q < DK / 8; ++q) wr[q] = make_uint4(0u, 0u, 0u, 0u);
+}
+
 }  // namespace
 
 size_t tc_prep_smem(int dk) {
@@ -511,6 +561,17 @@ gdn_status launch_prep(const FwdArgs &a, const int2 *table, __nv_bfloat16 *Tu,
 gdn_status enqueue_tc_prep(const FwdArgs &a, const int2 *table, __nv_bfloat16 *Tu,
                            __nv_bfloat16 *W) {
     if (a.chunk_slots <= 0 || a.sm.H <= 0) return GDN_OK;
+    if (a.no_erase) {
+        dim3 grid(a.chunk_slots, a.sm.H);
+        if (a.dk == 128)
+            k_gla_prep<128><<<grid, 64, 0, a.stream>>>(a.beta, a.sm, table, a.max_chunks, Tu, W,
+                                                        device_error_word());
+        else
+            k_gla_prep<64><<<grid, 64, 0, a.stream>>>(a.beta, a.sm, table, a.max_chunks, Tu, W,
+                                                       device_error_word());
+        count_launch();
+        return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+    }
     return a.dk == 128 ? launch_prep<128>(a, table, Tu, W) : launch_prep<64>(a, table, Tu, W);
 }
 

@@ -153,10 +153,12 @@ k_simt_prep(FwdArgs a, const int2 *__restrict__ table, float *__restrict__ W,
         }
     }
     __syncthreads();
+    // A: the beta-weighted decayed Gram of the erase term (zero without it,
+    // which leaves T = I, U = diag(beta) V and W = 0)
     for (int i = tid; i < kChunk * kChunk; i += kThreads) {
         const int r = i >> 6, s = i & 63;
         float val = 0.f;
-        if (s < r) {
+        if (s < r && !a.no_erase) {
             float acc = 0.f;
             for (int j = 0; j < dk; ++j) acc = fmaf(Ks[r * ks + j], Ks[s * ks + j], acc);
             val = bb[r] * expf(g[r] - g[s]) * acc;  // s < r: g_r <= g_s, no overflow
@@ -178,7 +180,8 @@ k_simt_prep(FwdArgs a, const int2 *__restrict__ table, float *__restrict__ W,
     for (int i = tid; i < L * dk; i += kThreads) {
         const int r = i / dk, j = i - r * dk;
         float acc = 0.f;
-        for (int s = 0; s <= r; ++s) acc = fmaf(Tm[r * 65 + s] * wb[s], Ks[s * ks + j], acc);
+        if (!a.no_erase)
+            for (int s = 0; s <= r; ++s) acc = fmaf(Tm[r * 65 + s] * wb[s], Ks[s * ks + j], acc);
         W[(r0 + r) * dk + j] = acc;
     }
     for (int i = tid; i < L * dv; i += kThreads) {

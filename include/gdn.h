@@ -172,6 +172,29 @@ uint64_t gdn_kernel_launches(void);
 int gdn_last_impl(void);
 
 /*
+ * Forward passes with variant flags (otherwise as gdn_fwd / gdn_fwd_varlen).
+ *   GDN_FLAG_NO_ERASE: gated linear attention -- the recurrence without the
+ *   delta rule's erase term ("线性注意力机制与Gated DeltaNet的优化实践",
+ *   sections 2.2-2.3, with a scalar forget gate alpha and update gate beta):
+ *       S_t = alpha_t S_{t-1} + beta_t v_t k_t^T,    o_t = S_t q_t;
+ *   alpha = beta = 1 is plain linear attention.  In the chunked form the
+ *   erase term is what makes A, T and W; without it T = I and W = 0, and the
+ *   same kernels run with the in-chunk inverse skipped.
+ * Unknown flag bits give GDN_ERR_INVALID_ARG.
+ */
+enum { GDN_FLAG_NO_ERASE = 1 };
+gdn_status gdn_fwd_ex(const void *q, const void *k, const void *v,
+                      const float *log_alpha, const float *beta, const float *h0,
+                      void *o, float *hT,
+                      int B, int H, int T, int d_k, int d_v, int chunk,
+                      gdn_dtype dt, unsigned flags, void *stream);
+gdn_status gdn_fwd_varlen_ex(const void *q, const void *k, const void *v,
+                             const float *log_alpha, const float *beta, const float *h0,
+                             void *o, float *hT, const int32_t *cu_seqlens,
+                             int N, int H, int T_total, int d_k, int d_v, int chunk,
+                             gdn_dtype dt, unsigned flags, void *stream);
+
+/*
  * Dense forward pass on HOST buffers (no paper counterpart: the same
  * computation as gdn_fwd with the host <-> device traffic inside the call).
  * Arguments and layouts as gdn_fwd, but q, k, v, log_alpha, beta, h0 (or

@@ -277,3 +277,60 @@ def test_bad_cu_seqlens_reported(impl):
     assert lib.gdn_sync_check(torch.cuda.current_stream().cuda_stream) == gdn.GDN_ERR_INVALID_ARG
     # the error word is cleared by reading it
     assert lib.gdn_sync_check(torch.cuda.current_stream().cuda_stream) == gdn.GDN_OK
+
+
+# ------------------------------------------------- gated linear attention
+
+
+@pytest.mark.parametrize("impl", ["simt", "tc"])
+@pytest.mark.parametrize("B,H,T,dk,dv,io", [(2, 2, 300, 128, 128, "bf16"),
+                                            (1, 3, 200, 64, 64, "bf16"),
+                                            (2, 1, 150, 64, 64, "f32")])
+def test_no_erase_matches_oracle(impl, B, H, T, dk, dv, io):
+    # the recurrence without the erase term (gated linear attention)
+    x = synth.make_dense(B, H, T, dk, dv, io=io, h0_std=0.02, seed=T + 3, device="cuda")
+    with gdn.use_impl(IMPLS[impl]):
+        try:
+            o, hT = gdn.gdn_fwd(x.q, x.k, x.v, x.log_alpha, x.beta, x.h0, check=True, erase=False)
+        except gdn.GdnError as e:
+            if e.status == gdn.GDN_ERR_UNSUPPORTED and impl == "tc":
+                pytest.skip("shape not covered by the tensor-core path")
+            raise
+    U.sync()
+    import oracle
+    o_ref, h_ref = oracle.gdn_fwd(U.f64(x.q), U.f64(x.k), U.f64(x.v), U.f64(x.log_alpha),
+                                  U.f64(x.beta), U.f64(x.h0), threads=U.ORACLE_THREADS,
+                                  erase=False)
+    check(o, hT, o_ref, h_ref, io)
+
+
+@pytest.mark.parametrize("impl", ["simt", "tc"])
+def test_no_erase_varlen_matches_oracle(impl):
+    y = synth.make_varlen([1, 63, 64, 65, 200, 0, 129], 2, 128, 128, io="bf16", h0_std=0.02,
+                          seed=17, device="cuda")
+    with gdn.use_impl(IMPLS[impl]):
+        o, hT = gdn.gdn_fwd_varlen(y.q, y.k, y.v, y.log_alpha, y.beta, y.cu_seqlens, y.h0,
+                                   check=True, erase=False)
+    U.sync()
+    import oracle
+    o_ref, h_ref = oracle.gdn_fwd_varlen(U.f64(y.q), U.f64(y.k), U.f64(y.v),
+                                         U.f64(y.log_alpha), U.f64(y.beta),
+                                         y.cu_seqlens.cpu().numpy(), U.f64(y.h0),
+                                         erase=False)
+    check(o, hT, o_ref, h_ref, "bf16")
+
+
+@pytest.mark.parametrize("impl", ["simt", "tc"])
+def test_no_erase_plain_linear_attention(impl):
+    # alpha = beta = 1, no initial state: causally masked (Q K^T) V
+    B, H, T, d = 1, 2, 192, 64
+    x = synth.make_dense(B, H, T, d, d, io="bf16", seed=19, device="cuda")
+    la = torch.zeros_like(x.log_alpha)
+    be = torch.ones_like(x.beta)
+    with gdn.use_impl(IMPLS[impl]):
+        o, _ = gdn.gdn_fwd(x.q, x.k, x.v, la, be, None, check=True, erase=False)
+    U.sync()
+    qf, kf, vf = (t.double() for t in (x.q, x.k, x.v))
+    mask = torch.tril(torch.ones(T, T, dtype=torch.float64, device="cuda"))
+    ref = ((qf @ kf.transpose(-1, -2)) * mask) @ vf
+    assert U.rel(U.f64(o), U.f64(ref)) <= 1e-2
