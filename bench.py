@@ -39,6 +39,8 @@ import synth  # noqa: E402
 METRIC = "GDN chunked fwd tokens/s (B·H·T/s) and % of roofline, bf16, d=128, 1×GB300"
 UNIT = "tokens/s"
 DECODE_METRIC = "GDN decode step tokens/s (B·H/s) and % of roofline, bf16, d=128, 1×GB300"
+GLA_METRIC = ("gated linear attention (no erase term) chunked fwd tokens/s (B·H·T/s) and % of "
+              "roofline, bf16, d=128, 1×GB300")
 DEFAULT_WORKLOAD = "gdn_fwd_b4_h16_t4096_d128_bf16"
 L2_FLUSH_BYTES = 256 << 20
 FALLBACK_HBM_GBS = 6800.0
@@ -53,6 +55,8 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-erase", action="store_true",
+                    help="gated linear attention: the recurrence without the erase term")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle sample")
     return ap.parse_args()
@@ -244,10 +248,20 @@ def is_decode(x):
 
 
 def metric_for(shape):
+    if NO_ERASE:
+        return GLA_METRIC
     return DECODE_METRIC if shape["kind"] == "decode" else METRIC
 
 
+NO_ERASE = False   # set from --no-erase
+
+
 def call(gdn, x, out=None):
+    if NO_ERASE:
+        if x.cu_seqlens is not None:
+            return gdn.gdn_fwd_varlen(x.q, x.k, x.v, x.log_alpha, x.beta, x.cu_seqlens, x.h0,
+                                      out=out, erase=False)
+        return gdn.gdn_fwd(x.q, x.k, x.v, x.log_alpha, x.beta, x.h0, out=out, erase=False)
     if is_decode(x):
         return gdn.gdn_decode(x.q, x.k, x.v, x.log_alpha, x.beta, x.h0, slots=x.slots,
                               out=out), x.h0
@@ -312,7 +326,7 @@ def run_ours(args, world, rank, local):
     d2h = o_host.numel() * o_host.element_size() + (0 if dec else h_host.numel() * 4)
     e2e_steps = max(3, min(args.steps, 10))
 
-    dense = shape["kind"] == "dense"
+    dense = shape["kind"] == "dense" and not NO_ERASE
 
     def e2e_step():
         if dense:
@@ -420,7 +434,7 @@ def oracle_sample(name, x, budget_s, max_heads=None):
             args = [f64(t[s])[None, None] for t in (x.q, x.k, x.v, x.log_alpha, x.beta)]
             h0 = None if x.h0 is None else f64(x.h0[n, h])[None, None]
             t0 = time.perf_counter()
-            oracle.gdn_fwd(*args, h0)
+            oracle.gdn_fwd(*args, h0, erase=not NO_ERASE)
             return b - a, time.perf_counter() - t0
     else:
         units = [(b, h) for b in range(x.q.shape[0]) for h in range(x.q.shape[1])]
@@ -430,7 +444,7 @@ def oracle_sample(name, x, budget_s, max_heads=None):
             args = [f64(t[b, h])[None, None] for t in (x.q, x.k, x.v, x.log_alpha, x.beta)]
             h0 = None if x.h0 is None else f64(x.h0[b, h])[None, None]
             t0 = time.perf_counter()
-            oracle.gdn_fwd(*args, h0)
+            oracle.gdn_fwd(*args, h0, erase=not NO_ERASE)
             return x.q.shape[2], time.perf_counter() - t0
 
     toks, secs, used = 0, 0.0, 0
@@ -484,7 +498,9 @@ def run_reference(args, world, rank):
 
 
 def main():
+    global NO_ERASE
     args = parse()
+    NO_ERASE = args.no_erase
     world, rank, local = dist_setup(args.gpus)
     if args.impl == "reference":
         res = run_reference(args, world, rank)
