@@ -151,12 +151,21 @@ def load_peaks():
         return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
 
 
-def kernel_source_hash():
+# the sources each timed kernel is built from (its file and the headers it includes)
+KERNEL_SOURCES = {
+    "k_gdn_tc": ["gdn_tc.cu", "tc_ptx.cuh", "gdn_internal.h"],
+    "k_gdn_prep": ["gdn_prep.cu", "tc_ptx.cuh", "gdn_internal.h"],
+    "k_gdn_decode": ["gdn_decode.cu", "gdn_internal.h"],
+}
+
+
+def kernel_source_hash(kernel):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "gated_deltanet_recurrence_gdn_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            h.update(open(os.path.join(csrc, f), "rb").read())
+    files = KERNEL_SOURCES.get(kernel) or sorted(
+        f for f in os.listdir(csrc) if f.endswith((".cu", ".cuh", ".h")))
+    for f in files + ["../../include/gdn.h"]:
+        h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -166,7 +175,7 @@ def recorded_traffic(kernel, workload):
     p = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(p):
         return None
-    want = kernel_source_hash()
+    want = kernel_source_hash(kernel)
     for line in open(p):
         parts = line.split()
         if len(parts) >= 4 and not line.startswith("#"):
