@@ -68,6 +68,10 @@ def load_library(path: str):
     lib.gdn_oracle_gla_fwd.argtypes = [_dp] * 8 + [ctypes.c_long] * 5
     lib.gdn_oracle_gla_fwd_varlen.restype = ctypes.c_int
     lib.gdn_oracle_gla_fwd_varlen.argtypes = [_dp] * 8 + [_lp] + [ctypes.c_long] * 5
+    lib.gdn_oracle_vg_fwd.restype = ctypes.c_int
+    lib.gdn_oracle_vg_fwd.argtypes = [_dp] * 8 + [ctypes.c_long] * 6
+    lib.gdn_oracle_vg_fwd_varlen.restype = ctypes.c_int
+    lib.gdn_oracle_vg_fwd_varlen.argtypes = [_dp] * 8 + [_lp] + [ctypes.c_long] * 6
     return lib
 
 
@@ -86,19 +90,25 @@ def _ptr(a):
     return None if a is None else a.ctypes.data_as(_dp)
 
 
-def gdn_fwd(q, k, v, log_alpha, beta, h0=None, *, threads: int = 1, lib=None, erase=True):
+def gdn_fwd(q, k, v, log_alpha, beta, h0=None, *, threads: int = 1, lib=None, erase=True,
+            vector_gate=False):
     """Dense oracle.  q,k [B,H,T,dk]; v [B,H,T,dv]; log_alpha, beta [B,H,T];
     h0 [B,H,dv,dk] or None.  Returns (o [B,H,T,dv], hT [B,H,dv,dk]) in fp64.
     erase=False runs gated linear attention (the recurrence without the
-    delta rule's erase term)."""
+    delta rule's erase term); vector_gate=True takes log_alpha [B,H,T,dk], a
+    gate per key dimension."""
     lib = lib or _get()
-    fwd = lib.gdn_oracle_fwd if erase else lib.gdn_oracle_gla_fwd
+    if vector_gate:
+        def fwd(*a):
+            return lib.gdn_oracle_vg_fwd(*a, 1 if erase else 0)
+    else:
+        fwd = lib.gdn_oracle_fwd if erase else lib.gdn_oracle_gla_fwd
     q, k, v = _f64(q), _f64(k), _f64(v)
     la, be = _f64(log_alpha), _f64(beta)
     B, H, T, dk = q.shape
     dv = v.shape[-1]
     assert k.shape == q.shape and v.shape == (B, H, T, dv)
-    assert la.shape == (B, H, T) and be.shape == (B, H, T)
+    assert la.shape == ((B, H, T, dk) if vector_gate else (B, H, T)) and be.shape == (B, H, T)
     if h0 is not None:
         h0 = _f64(h0)
         assert h0.shape == (B, H, dv, dk)
@@ -124,14 +134,21 @@ def gdn_fwd(q, k, v, log_alpha, beta, h0=None, *, threads: int = 1, lib=None, er
 
 
 def gdn_fwd_varlen(q, k, v, log_alpha, beta, cu_seqlens, h0=None, *, threads: int = 1,
-                   lib=None, erase=True):
+                   lib=None, erase=True, vector_gate=False):
     """Packed oracle.  q,k [H,T_total,dk]; v [H,T_total,dv]; log_alpha, beta
-    [H,T_total]; cu_seqlens [N+1]; h0 [N,H,dv,dk] or None.
-    Returns (o [H,T_total,dv], hT [N,H,dv,dk]) in fp64.  erase=False runs
-    gated linear attention."""
+    [H,T_total] (log_alpha [H,T_total,dk] with vector_gate); cu_seqlens [N+1];
+    h0 [N,H,dv,dk] or None.  Returns (o [H,T_total,dv], hT [N,H,dv,dk]) in
+    fp64.  erase=False runs gated linear attention."""
     lib = lib or _get()
-    fwd = lib.gdn_oracle_fwd if erase else lib.gdn_oracle_gla_fwd
-    fwd_varlen = lib.gdn_oracle_fwd_varlen if erase else lib.gdn_oracle_gla_fwd_varlen
+    if vector_gate:
+        def fwd(*a):
+            return lib.gdn_oracle_vg_fwd(*a, 1 if erase else 0)
+
+        def fwd_varlen(*a):
+            return lib.gdn_oracle_vg_fwd_varlen(*a, 1 if erase else 0)
+    else:
+        fwd = lib.gdn_oracle_fwd if erase else lib.gdn_oracle_gla_fwd
+        fwd_varlen = lib.gdn_oracle_fwd_varlen if erase else lib.gdn_oracle_gla_fwd_varlen
     q, k, v = _f64(q), _f64(k), _f64(v)
     la, be = _f64(log_alpha), _f64(beta)
     cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int64))

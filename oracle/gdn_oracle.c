@@ -35,6 +35,16 @@
  *
  * (alpha = beta = 1 is plain linear attention), in the same layouts.
  *
+ * The third part takes a gate per key dimension ("Gated DeltaNet GPU并行实现",
+ * section 2.2: with a per-dimension or diagonal gate the affine map's
+ * coefficient matrix gains a diagonal factor).  Reading: the diagonal factor
+ * acts on the old state first, as the scalar gate does,
+ *
+ *     S_t = (S_{t-1} diag(alpha_t)) (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,
+ *
+ * alpha_t = exp(log_alpha_t) with log_alpha_t a d_k-vector; with the erase
+ * term off it is gated linear attention with a vector gate.
+ *
  * Parity pins for this file (closed forms, invariants, reductions to linear
  * attention, planted-mistake checks) live in tests/test_oracle_pins.py.
  */
@@ -269,5 +279,122 @@ int gdn_oracle_gla_fwd_varlen(const double *q, const double *k, const double *v,
         }
     }
     free(S);
+    return 0;
+}
+
+/*
+ * Per-dimension gate, one (sequence, head).  la: [T][dk]; erase = 0 leaves
+ * the erase term out.  Otherwise as oracle_one.
+ */
+static void oracle_one_vg(const double *q, const double *k, const double *v,
+                          const double *la, const double *beta,
+                          const double *h0, double *o, double *hT,
+                          long T, long dk, long dv, long erase, double *S, double *Sk)
+{
+    long t, i, j;
+    if (h0)
+        memcpy(S, h0, sizeof(double) * (size_t)(dv * dk));
+    else
+        memset(S, 0, sizeof(double) * (size_t)(dv * dk));
+    for (t = 0; t < T; ++t) {
+        const double *kt = k + t * dk;
+        const double *vt = v + t * dv;
+        const double *qt = q + t * dk;
+        const double *lat = la + t * dk;
+        const double bt = beta[t];
+        /* S <- S diag(alpha_t): column j scaled by exp(la_t[j]) */
+        for (i = 0; i < dv; ++i)
+            for (j = 0; j < dk; ++j)
+                S[i * dk + j] *= exp(lat[j]);
+        /* S <- S (I - b k k^T) + b v k^T */
+        for (i = 0; i < dv; ++i) {
+            double dot = 0.0;
+            for (j = 0; j < dk; ++j)
+                dot += S[i * dk + j] * kt[j];
+            Sk[i] = erase ? dot : 0.0;
+        }
+        for (i = 0; i < dv; ++i)
+            for (j = 0; j < dk; ++j)
+                S[i * dk + j] += bt * (vt[i] - Sk[i]) * kt[j];
+        if (o) {
+            for (i = 0; i < dv; ++i) {
+                double out = 0.0;
+                for (j = 0; j < dk; ++j)
+                    out += S[i * dk + j] * qt[j];
+                o[t * dv + i] = out;
+            }
+        }
+    }
+    if (hT)
+        memcpy(hT, S, sizeof(double) * (size_t)(dv * dk));
+}
+
+/* Dense batch, per-dimension gate: log_alpha [B][H][T][dk], rest as gdn_oracle_fwd. */
+int gdn_oracle_vg_fwd(const double *q, const double *k, const double *v,
+                      const double *log_alpha, const double *beta,
+                      const double *h0, double *o, double *hT,
+                      long B, long H, long T, long dk, long dv, long erase)
+{
+    long bh;
+    double *S, *Sk;
+    if (B < 0 || H < 0 || T < 0 || dk <= 0 || dv <= 0)
+        return -1;
+    S = (double *)malloc(sizeof(double) * (size_t)(dv * dk));
+    Sk = (double *)malloc(sizeof(double) * (size_t)dv);
+    if (!S || !Sk) {
+        free(S);
+        free(Sk);
+        return -1;
+    }
+    for (bh = 0; bh < B * H; ++bh)
+        oracle_one_vg(q + bh * T * dk, k + bh * T * dk, v + bh * T * dv,
+                      log_alpha + bh * T * dk, beta + bh * T,
+                      h0 ? h0 + bh * dv * dk : NULL,
+                      o ? o + bh * T * dv : NULL,
+                      hT ? hT + bh * dv * dk : NULL,
+                      T, dk, dv, erase, S, Sk);
+    free(S);
+    free(Sk);
+    return 0;
+}
+
+/* Packed batch, per-dimension gate: log_alpha [H][T_total][dk]. */
+int gdn_oracle_vg_fwd_varlen(const double *q, const double *k, const double *v,
+                             const double *log_alpha, const double *beta,
+                             const double *h0, double *o, double *hT,
+                             const long *cu_seqlens, long N, long H, long T_total,
+                             long dk, long dv, long erase)
+{
+    long n, h;
+    double *S, *Sk;
+    if (N < 0 || H < 0 || T_total < 0 || dk <= 0 || dv <= 0)
+        return -1;
+    if (N > 0 && (cu_seqlens[0] != 0 || cu_seqlens[N] != T_total))
+        return -1;
+    for (n = 0; n < N; ++n)
+        if (cu_seqlens[n + 1] < cu_seqlens[n])
+            return -1;
+    S = (double *)malloc(sizeof(double) * (size_t)(dv * dk));
+    Sk = (double *)malloc(sizeof(double) * (size_t)dv);
+    if (!S || !Sk) {
+        free(S);
+        free(Sk);
+        return -1;
+    }
+    for (n = 0; n < N; ++n) {
+        long first = cu_seqlens[n];
+        long len = cu_seqlens[n + 1] - first;
+        for (h = 0; h < H; ++h) {
+            long at = h * T_total + first;
+            oracle_one_vg(q + at * dk, k + at * dk, v + at * dv,
+                          log_alpha + at * dk, beta + at,
+                          h0 ? h0 + (n * H + h) * dv * dk : NULL,
+                          o ? o + at * dv : NULL,
+                          hT ? hT + (n * H + h) * dv * dk : NULL,
+                          len, dk, dv, erase, S, Sk);
+        }
+    }
+    free(S);
+    free(Sk);
     return 0;
 }

@@ -14,7 +14,11 @@ DeltaNet的优化实践" sections 2.2-2.3, with the erase term vanishing for
 mutually orthogonal keys.  The gated-linear-attention loop (the recurrence
 without the erase term, same page sections 2.2-2.3) is pinned to its
 unrolled closed form, to plain linear attention, and to the delta rule where
-the two coincide.
+the two coincide.  The per-key-dimension gate loop (section 2.2's diagonal
+factor) is pinned to the scalar loops when its entries are equal, to the
+explicit affine maps diag(alpha_t)(I - beta_t k k^T), beta_t v k^T composed in
+random bracketings (which fixes that the decay acts before the erase), and to
+its beta = 0 closed form.
 """
 from __future__ import annotations
 
@@ -332,6 +336,102 @@ def pin_gla_varlen_split(lib, dk=4, dv=3, H=2, seed=24):
     return worst
 
 
+def _vg_inputs(rng, B, H, T, dk, dv):
+    q, k, v, _, be = _rand_inputs(rng, B, H, T, dk, dv)
+    la = -np.log1p(np.exp(rng.standard_normal((B, H, T, dk)))) * 0.5   # a gate per key dimension
+    return q, k, v, la, be
+
+
+def pin_vg_scalar_reduction(lib, dk=5, dv=4, T=12, seed=31):
+    """A per-dimension gate whose entries are all equal is the scalar gate:
+    the vector-gate loop must agree with the scalar loops, with and without
+    the erase term."""
+    rng = np.random.default_rng(seed)
+    q, k, v, la, be = _rand_inputs(rng, 1, 2, T, dk, dv)
+    h0 = rng.standard_normal((1, 2, dv, dk))
+    lav = np.repeat(la[..., None], dk, axis=-1)
+    worst = 0.0
+    for erase in (True, False):
+        a = oracle.gdn_fwd(q, k, v, la, be, h0, lib=lib, erase=erase)
+        b = oracle.gdn_fwd(q, k, v, lav, be, h0, lib=lib, erase=erase, vector_gate=True)
+        worst = max(worst, _rel(b[0], a[0]), _rel(b[1], a[1]))
+    return worst
+
+
+def _vg_affine_maps(k, v, la, be, erase=True):
+    """Per-token maps S -> S A_t + B_t with a diagonal gate: A_t =
+    diag(alpha_t) (I - beta_t k k^T) (the decay acts on the old state first),
+    B_t = beta_t v_t k_t^T; section 2.2's extra diagonal factor."""
+    T, dk = k.shape
+    A = np.empty((T, dk, dk))
+    Bm = np.empty((T, v.shape[1], dk))
+    for t in range(T):
+        E = np.eye(dk) - (be[t] * np.outer(k[t], k[t]) if erase else 0.0)
+        A[t] = np.diag(np.exp(la[t])) @ E
+        Bm[t] = be[t] * np.outer(v[t], k[t])
+    return A, Bm
+
+
+def pin_vg_bracketing(lib, dk=4, dv=3, T=11, seed=32, trials=4):
+    """Section 2.3 with the diagonal factor: any bracketing of the explicit
+    affine maps equals the vector-gate loop, at every prefix, with and
+    without the erase term."""
+    rng = np.random.default_rng(seed)
+    q, k, v, la, be = _vg_inputs(rng, 1, 1, T, dk, dv)
+    h0 = rng.standard_normal((1, 1, dv, dk))
+    err = 0.0
+    for erase in (True, False):
+        o, hT = oracle.gdn_fwd(q, k, v, la, be, h0, lib=lib, erase=erase, vector_gate=True)
+        A, Bm = _vg_affine_maps(k[0, 0], v[0, 0], la[0, 0], be[0, 0], erase)
+        for _ in range(trials):
+            for t in range(1, T + 1):
+                At, Bt = _fold(A, Bm, 0, t, rng)
+                St = h0[0, 0] @ At + Bt
+                err = max(err, _rel(St @ q[0, 0, t - 1], o[0, 0, t - 1]))
+                if t == T:
+                    err = max(err, _rel(St, hT[0, 0]))
+    return err
+
+
+def pin_vg_beta_zero(lib, dk=5, dv=3, T=9, seed=33):
+    """beta = 0: each key dimension j of the state only decays,
+    S_t[:, j] = exp(sum_{i<=t} log_alpha_i[j]) h0[:, j]."""
+    rng = np.random.default_rng(seed)
+    q, k, v, la, _ = _vg_inputs(rng, 1, 2, T, dk, dv)
+    be = np.zeros(la.shape[:-1])
+    h0 = rng.standard_normal((1, 2, dv, dk))
+    o, hT = oracle.gdn_fwd(q, k, v, la, be, h0, lib=lib, vector_gate=True)
+    cum = np.exp(np.cumsum(la, axis=2))                               # [1,2,T,dk]
+    o_ref = np.einsum("bhij,bhtj,bhtj->bhti", h0, cum, q)
+    hT_ref = h0 * cum[:, :, -1][:, :, None, :]
+    return max(_rel(o, o_ref), _rel(hT, hT_ref))
+
+
+def pin_vg_varlen_split(lib, dk=4, dv=3, H=2, seed=34):
+    """Packed vector-gate batches equal per-sequence dense calls."""
+    rng = np.random.default_rng(seed)
+    lens = [6, 0, 8, 1]
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    TT = int(cu[-1])
+    q = rng.standard_normal((H, TT, dk))
+    k = rng.standard_normal((H, TT, dk))
+    k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = rng.standard_normal((H, TT, dv))
+    la = -rng.uniform(0, 1, (H, TT, dk))
+    be = rng.uniform(0, 1, (H, TT))
+    h0 = rng.standard_normal((len(lens), H, dv, dk))
+    o, hT = oracle.gdn_fwd_varlen(q, k, v, la, be, cu, h0, lib=lib, vector_gate=True)
+    worst = 0.0
+    for n, (a, b) in enumerate(zip(cu[:-1], cu[1:])):
+        s = np.s_[:, a:b]
+        od, hd = oracle.gdn_fwd(q[s][None], k[s][None], v[s][None], la[s][None], be[s][None],
+                                h0[n][None], lib=lib, vector_gate=True)
+        worst = max(worst, _rel(hT[n], hd[0]))
+        if b > a:
+            worst = max(worst, _rel(o[:, a:b], od[0]))
+    return worst
+
+
 ALL_PINS = {
     "beta_zero": pin_beta_zero,
     "exact_recall": pin_exact_recall,
@@ -346,4 +446,8 @@ ALL_PINS = {
     "gla_linear_attention": pin_gla_linear_attention,
     "gla_equals_delta_on_orthogonal_keys": pin_gla_equals_delta_on_orthogonal_keys,
     "gla_varlen_split": pin_gla_varlen_split,
+    "vg_scalar_reduction": pin_vg_scalar_reduction,
+    "vg_bracketing": pin_vg_bracketing,
+    "vg_beta_zero": pin_vg_beta_zero,
+    "vg_varlen_split": pin_vg_varlen_split,
 }

@@ -90,6 +90,14 @@ MUTANTS = {
     "gla_h0_ignored": ("if (h0)\n        memcpy(S, h0, sizeof(double) * (size_t)(dv * dk));\n    else\n        memset(S, 0, sizeof(double) * (size_t)(dv * dk));\n    for (t = 0; t < T; ++t) {\n        const double *kt = k + t * dk;\n        const double *vt = v + t * dv;\n        const double *qt = q + t * dk;\n        const double g",
                        "if (0)\n        memcpy(S, h0, sizeof(double) * (size_t)(dv * dk));\n    else\n        memset(S, 0, sizeof(double) * (size_t)(dv * dk));\n    for (t = 0; t < T; ++t) {\n        const double *kt = k + t * dk;\n        const double *vt = v + t * dv;\n        const double *qt = q + t * dk;\n        const double g"),
     "gla_varlen_offset": ("long rw = h * T_total + s0;", "long rw = h * T_total + s0 / 2;"),
+    # the per-dimension-gate loop
+    "vg_gate_wrong_axis": ("S[i * dk + j] *= exp(lat[j]);", "S[i * dk + j] *= exp(lat[i % dk]);"),
+    "vg_gate_not_exponentiated": ("S[i * dk + j] *= exp(lat[j]);", "S[i * dk + j] *= 1.0 + lat[j];"),
+    "vg_beta_dropped": ("+= bt * (vt[i] - Sk[i]) * kt[j];", "+= (vt[i] - Sk[i]) * kt[j];"),
+    "vg_erase_sign": ("+= bt * (vt[i] - Sk[i]) * kt[j];", "+= bt * (vt[i] + Sk[i]) * kt[j];"),
+    "vg_erase_ignored": ("Sk[i] = erase ? dot : 0.0;", "Sk[i] = 0.0;"),
+    "vg_output_transposed": ("out += S[i * dk + j] * qt[j];", "out += S[j * dk + i] * qt[j];"),
+    "vg_varlen_offset": ("long at = h * T_total + first;", "long at = h * T_total + first / 2;"),
 }
 
 
@@ -121,5 +129,9 @@ def test_planted_mistake_is_caught(mutant_dir, name):
         "gla_closed_form": P.pin_gla_closed_form(mlib, **square),
         "gla_linear_attention": P.pin_gla_linear_attention(mlib, **square),
         "gla_varlen": P.pin_gla_varlen_split(mlib, dk=5, dv=5),
+        "vg_scalar": P.pin_vg_scalar_reduction(mlib, **square),
+        "vg_bracketing": P.pin_vg_bracketing(mlib, **square),
+        "vg_beta_zero": P.pin_vg_beta_zero(mlib, **square),
+        "vg_varlen": P.pin_vg_varlen_split(mlib, dk=5, dv=5),
     }
     assert max(errs.values()) > 1e-6, errs
