@@ -131,18 +131,21 @@ def _prep_io(q, k, v, log_alpha, beta, h0):
 
 
 GDN_FLAG_NO_ERASE = 1
+GDN_FLAG_VECTOR_GATE = 2
 
 
 def gdn_fwd(q, k, v, log_alpha, beta, h0=None, *, chunk=CHUNK, out=None, final_state=True,
             check=False, erase=True):
     """Dense forward: returns (o [B,H,T,d_v], hT [B,H,d_v,d_k] or None).
-    erase=False: gated linear attention (no delta-rule erase term)."""
+    erase=False: gated linear attention (no delta-rule erase term).
+    A log_alpha of shape [B,H,T,d_k] is a gate per key dimension."""
     lib = load()
     _prep_io(q, k, v, log_alpha, beta, h0)
     B, H, T, dk = q.shape
     dv = v.shape[-1]
-    if k.shape != q.shape or v.shape[:3] != (B, H, T) or log_alpha.shape != (B, H, T) \
-            or beta.shape != (B, H, T):
+    vector_gate = log_alpha.dim() == 4
+    if k.shape != q.shape or v.shape[:3] != (B, H, T) or beta.shape != (B, H, T) \
+            or log_alpha.shape != ((B, H, T, dk) if vector_gate else (B, H, T)):
         raise ValueError("shape mismatch")
     if h0 is not None and h0.shape != (B, H, dv, dk):
         raise ValueError("h0 must be [B,H,d_v,d_k]")
@@ -151,8 +154,9 @@ def gdn_fwd(q, k, v, log_alpha, beta, h0=None, *, chunk=CHUNK, out=None, final_s
     with torch.cuda.device(q.device):
         args = (_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(h0),
                 _ptr(o), _ptr(hT), B, H, T, dk, dv, chunk, _DT[q.dtype])
-        rc = (lib.gdn_fwd(*args, _stream(q.device)) if erase else
-              lib.gdn_fwd_ex(*args, GDN_FLAG_NO_ERASE, _stream(q.device)))
+        flags = (0 if erase else GDN_FLAG_NO_ERASE) | (GDN_FLAG_VECTOR_GATE if vector_gate else 0)
+        rc = (lib.gdn_fwd_ex(*args, flags, _stream(q.device)) if flags else
+              lib.gdn_fwd(*args, _stream(q.device)))
         _check(rc, "gdn_fwd")
         if check:
             _check(lib.gdn_sync_check(_stream(q.device)), "gdn_fwd (device)")
@@ -162,7 +166,8 @@ def gdn_fwd(q, k, v, log_alpha, beta, h0=None, *, chunk=CHUNK, out=None, final_s
 def gdn_fwd_varlen(q, k, v, log_alpha, beta, cu_seqlens, h0=None, *, chunk=CHUNK, out=None,
                    final_state=True, check=False, erase=True):
     """Packed forward: returns (o [H,T_total,d_v], hT [N,H,d_v,d_k] or None).
-    erase=False: gated linear attention (no delta-rule erase term)."""
+    erase=False: gated linear attention (no delta-rule erase term).
+    A log_alpha of shape [H,T_total,d_k] is a gate per key dimension."""
     lib = load()
     _prep_io(q, k, v, log_alpha, beta, h0)
     H, TT, dk = q.shape
@@ -170,8 +175,9 @@ def gdn_fwd_varlen(q, k, v, log_alpha, beta, cu_seqlens, h0=None, *, chunk=CHUNK
     if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda or cu_seqlens.dim() != 1:
         raise ValueError("cu_seqlens must be a 1-D int32 CUDA tensor")
     N = cu_seqlens.shape[0] - 1
-    if k.shape != q.shape or v.shape[:2] != (H, TT) or log_alpha.shape != (H, TT) \
-            or beta.shape != (H, TT):
+    vector_gate = log_alpha.dim() == 3
+    if k.shape != q.shape or v.shape[:2] != (H, TT) or beta.shape != (H, TT) \
+            or log_alpha.shape != ((H, TT, dk) if vector_gate else (H, TT)):
         raise ValueError("shape mismatch")
     if h0 is not None and h0.shape != (N, H, dv, dk):
         raise ValueError("h0 must be [N,H,d_v,d_k]")
@@ -181,8 +187,9 @@ def gdn_fwd_varlen(q, k, v, log_alpha, beta, cu_seqlens, h0=None, *, chunk=CHUNK
         args = (_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(h0), _ptr(o),
                 _ptr(hT), _ptr(cu_seqlens.contiguous()), N, H, TT, dk, dv, chunk,
                 _DT[q.dtype])
-        rc = (lib.gdn_fwd_varlen(*args, _stream(q.device)) if erase else
-              lib.gdn_fwd_varlen_ex(*args, GDN_FLAG_NO_ERASE, _stream(q.device)))
+        flags = (0 if erase else GDN_FLAG_NO_ERASE) | (GDN_FLAG_VECTOR_GATE if vector_gate else 0)
+        rc = (lib.gdn_fwd_varlen_ex(*args, flags, _stream(q.device)) if flags else
+              lib.gdn_fwd_varlen(*args, _stream(q.device)))
         _check(rc, "gdn_fwd_varlen")
         if check:
             _check(lib.gdn_sync_check(_stream(q.device)), "gdn_fwd_varlen (device)")

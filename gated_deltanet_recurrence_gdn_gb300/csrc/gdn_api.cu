@@ -168,7 +168,7 @@ gdn_status gdn_fwd_ex(const void *q, const void *k, const void *v, const float *
                       const float *beta, const float *h0, void *o, float *hT, int B, int H,
                       int T, int d_k, int d_v, int chunk, gdn_dtype dt, unsigned flags,
                       void *stream) {
-    if (flags & ~(unsigned)GDN_FLAG_NO_ERASE) return GDN_ERR_INVALID_ARG;
+    if (flags & ~(unsigned)(GDN_FLAG_NO_ERASE | GDN_FLAG_VECTOR_GATE)) return GDN_ERR_INVALID_ARG;
     if (B < 0 || T < 0) return GDN_ERR_INVALID_ARG;
     const bool tokens = (long long)B * H * T > 0;
     gdn_status rc = check_common(q, k, v, log_alpha, beta, h0, o, hT, H, d_k, d_v, chunk, dt,
@@ -185,6 +185,7 @@ gdn_status gdn_fwd_ex(const void *q, const void *k, const void *v, const float *
     a.chunk_slots = (int)((long long)B * a.max_chunks);
     a.stream = static_cast<cudaStream_t>(stream);
     a.no_erase = (flags & GDN_FLAG_NO_ERASE) != 0;
+    a.vector_gate = (flags & GDN_FLAG_VECTOR_GATE) != 0;
     if ((long long)B * a.max_chunks > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
     return dispatch(a);
 }
@@ -202,7 +203,7 @@ gdn_status gdn_fwd_varlen_ex(const void *q, const void *k, const void *v,
                              void *o, float *hT, const int32_t *cu_seqlens, int N, int H,
                              int T_total, int d_k, int d_v, int chunk, gdn_dtype dt,
                              unsigned flags, void *stream) {
-    if (flags & ~(unsigned)GDN_FLAG_NO_ERASE) return GDN_ERR_INVALID_ARG;
+    if (flags & ~(unsigned)(GDN_FLAG_NO_ERASE | GDN_FLAG_VECTOR_GATE)) return GDN_ERR_INVALID_ARG;
     if (N < 0 || T_total < 0) return GDN_ERR_INVALID_ARG;
     if (N > 0 && !cu_seqlens) return GDN_ERR_INVALID_ARG;
     if (N == 0 && T_total != 0) return GDN_ERR_INVALID_ARG;
@@ -223,6 +224,7 @@ gdn_status gdn_fwd_varlen_ex(const void *q, const void *k, const void *v,
     a.chunk_slots = (int)slots;
     a.stream = static_cast<cudaStream_t>(stream);
     a.no_erase = (flags & GDN_FLAG_NO_ERASE) != 0;
+    a.vector_gate = (flags & GDN_FLAG_VECTOR_GATE) != 0;
     return dispatch(a);
 }
 

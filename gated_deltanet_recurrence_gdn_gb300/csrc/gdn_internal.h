@@ -52,6 +52,7 @@ struct FwdArgs {
     int chunk_slots;      // upper bound on chunks of all sequences
     cudaStream_t stream;
     bool no_erase;        // gated linear attention: A = 0, T = I, W = 0
+    bool vector_gate;     // log_alpha [rows][d_k]: a gate per key dimension
 };
 
 // Stream-ordered scratch from the library's per-device pool, which keeps

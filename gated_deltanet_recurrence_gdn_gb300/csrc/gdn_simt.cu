@@ -128,14 +128,21 @@ k_simt_prep(FwdArgs a, const int2 *__restrict__ table, float *__restrict__ W,
     float *g = Tm + kChunk * 65;      // [64] gate cumsum
     float *bb = g + kChunk;           // [64] beta
     float *wb = bb + kChunk;          // [64] beta * exp(g)
+    float *Gv = wb + kChunk;          // [64][dk+1] per-dimension gate cumsum (vector gate)
+    const bool vg = a.vector_gate;
     const TIn *kp = static_cast<const TIn *>(a.k);
     const TIn *vp = static_cast<const TIn *>(a.v);
 
     if (tid < kChunk) {
         const bool ok = tid < L;
-        g[tid] = ok ? __ldg(a.log_alpha + r0 + tid) : 0.f;
+        g[tid] = (ok && !vg) ? __ldg(a.log_alpha + r0 + tid) : 0.f;
         bb[tid] = ok ? __ldg(a.beta + r0 + tid) : 0.f;
     }
+    if (vg)
+        for (int i = tid; i < kChunk * dk; i += kThreads) {
+            const int r = i / dk, j = i - r * dk;
+            Gv[r * ks + j] = r < L ? __ldg(a.log_alpha + (r0 + r) * dk + j) : 0.f;
+        }
     for (int i = tid; i < kChunk * dk; i += kThreads) {
         const int r = i / dk, j = i - r * dk;
         Ks[r * ks + j] = r < L ? ld_in(kp + (r0 + r) * dk + j) : 0.f;
@@ -152,6 +159,13 @@ k_simt_prep(FwdArgs a, const int2 *__restrict__ table, float *__restrict__ W,
             g[r] = s;
         }
     }
+    if (vg && tid < dk) {   // column tid of the per-dimension cumsum
+        float s = 0.f;
+        for (int r = 0; r < kChunk; ++r) {
+            s += Gv[r * ks + tid];
+            Gv[r * ks + tid] = s;
+        }
+    }
     __syncthreads();
     // A: the beta-weighted decayed Gram of the erase term (zero without it,
     // which leaves T = I, U = diag(beta) V and W = 0)
@@ -160,8 +174,15 @@ k_simt_prep(FwdArgs a, const int2 *__restrict__ table, float *__restrict__ W,
         float val = 0.f;
         if (s < r && !a.no_erase) {
             float acc = 0.f;
-            for (int j = 0; j < dk; ++j) acc = fmaf(Ks[r * ks + j], Ks[s * ks + j], acc);
-            val = bb[r] * expf(g[r] - g[s]) * acc;  // s < r: g_r <= g_s, no overflow
+            if (vg) {   // the decay from s to r taken per key dimension
+                for (int j = 0; j < dk; ++j)
+                    acc = fmaf(Ks[r * ks + j] * expf(Gv[r * ks + j] - Gv[s * ks + j]),
+                               Ks[s * ks + j], acc);
+                val = bb[r] * acc;
+            } else {
+                for (int j = 0; j < dk; ++j) acc = fmaf(Ks[r * ks + j], Ks[s * ks + j], acc);
+                val = bb[r] * expf(g[r] - g[s]) * acc;  // s < r: g_r <= g_s, no overflow
+            }
         }
         A[r * 65 + s] = val;
     }
@@ -180,8 +201,14 @@ k_simt_prep(FwdArgs a, const int2 *__restrict__ table, float *__restrict__ W,
     for (int i = tid; i < L * dk; i += kThreads) {
         const int r = i / dk, j = i - r * dk;
         float acc = 0.f;
-        if (!a.no_erase)
-            for (int s = 0; s <= r; ++s) acc = fmaf(Tm[r * 65 + s] * wb[s], Ks[s * ks + j], acc);
+        if (!a.no_erase) {
+            if (vg)   // W = T diag(beta) (K * gamma), gamma per key dimension
+                for (int s = 0; s <= r; ++s)
+                    acc = fmaf(Tm[r * 65 + s] * bb[s] * expf(Gv[s * ks + j]), Ks[s * ks + j], acc);
+            else
+                for (int s = 0; s <= r; ++s)
+                    acc = fmaf(Tm[r * 65 + s] * wb[s], Ks[s * ks + j], acc);
+        }
         W[(r0 + r) * dk + j] = acc;
     }
     for (int i = tid; i < L * dv; i += kThreads) {
@@ -190,7 +217,14 @@ k_simt_prep(FwdArgs a, const int2 *__restrict__ table, float *__restrict__ W,
         for (int s = 0; s <= r; ++s) acc = fmaf(Tm[r * 65 + s] * bb[s], Vs[s * vs + j], acc);
         U[(r0 + r) * dv + j] = acc;
     }
-    if (tid < L) G[r0 + tid] = g[tid];
+    if (vg) {
+        for (int i = tid; i < L * dk; i += kThreads) {
+            const int r = i / dk, j = i - r * dk;
+            G[(r0 + r) * dk + j] = Gv[r * ks + j];
+        }
+    } else if (tid < L) {
+        G[r0 + tid] = g[tid];
+    }
 }
 
 template <typename TIn>
@@ -218,6 +252,8 @@ k_simt_state(FwdArgs a, const float *__restrict__ W, const float *__restrict__ U
     float *P = Vn + kChunk * us;         // [64][65]
     float *g = P + kChunk * 65;          // [64]
     float *e = g + kChunk;               // [64] exp(g_C - g_r)
+    float *Gv = e + kChunk;              // [64][dk+1] per-dimension cumsum (vector gate)
+    const bool vg = a.vector_gate;
     const TIn *qp = static_cast<const TIn *>(a.q);
     const TIn *kp = static_cast<const TIn *>(a.k);
     TIn *op = static_cast<TIn *>(a.o);
@@ -243,17 +279,31 @@ k_simt_state(FwdArgs a, const float *__restrict__ W, const float *__restrict__ U
             const int r = i / kDvt, cc = i - r * kDvt;
             Us[r * us + cc] = (r < L && cc < nv) ? __ldg(U + (r0 + r) * dv + dv0 + cc) : 0.f;
         }
-        if (tid < kChunk) g[tid] = __ldg(G + r0 + min(tid, L - 1));
+        if (vg) {   // rows past the sequence repeat its last cumulative gate
+            for (int i = tid; i < kChunk * dk; i += kThreads) {
+                const int r = i / dk, j = i - r * dk;
+                Gv[r * ks + j] = __ldg(G + (r0 + min(r, L - 1)) * dk + j);
+            }
+        } else if (tid < kChunk) {
+            g[tid] = __ldg(G + r0 + min(tid, L - 1));
+        }
         __syncthreads();
-        const float gl = g[kChunk - 1];
-        if (tid < kChunk) e[tid] = expf(gl - g[tid]);
+        const float gl = vg ? 0.f : g[kChunk - 1];
+        if (tid < kChunk && !vg) e[tid] = expf(gl - g[tid]);
         for (int i = tid; i < kChunk * kChunk; i += kThreads) {
             const int r = i >> 6, s = i & 63;
             float val = 0.f;
             if (s <= r) {
                 float acc = 0.f;
-                for (int j = 0; j < dk; ++j) acc = fmaf(Qs[r * ks + j], Ks[s * ks + j], acc);
-                val = expf(g[r] - g[s]) * acc;
+                if (vg) {
+                    for (int j = 0; j < dk; ++j)
+                        acc = fmaf(Qs[r * ks + j] * expf(Gv[r * ks + j] - Gv[s * ks + j]),
+                                   Ks[s * ks + j], acc);
+                    val = acc;
+                } else {
+                    for (int j = 0; j < dk; ++j) acc = fmaf(Qs[r * ks + j], Ks[s * ks + j], acc);
+                    val = expf(g[r] - g[s]) * acc;
+                }
             }
             P[r * 65 + s] = val;
         }
@@ -268,9 +318,13 @@ k_simt_state(FwdArgs a, const float *__restrict__ W, const float *__restrict__ U
             const int r = i / kDvt, cc = i - r * kDvt;
             if (r < L && cc < nv) {
                 float a1 = 0.f, a2 = 0.f;
-                for (int j = 0; j < dk; ++j) a1 = fmaf(Qs[r * ks + j], Hs[j * kDvt + cc], a1);
+                if (vg)   // (Q * gamma) H with gamma per key dimension
+                    for (int j = 0; j < dk; ++j)
+                        a1 = fmaf(Qs[r * ks + j] * expf(Gv[r * ks + j]), Hs[j * kDvt + cc], a1);
+                else
+                    for (int j = 0; j < dk; ++j) a1 = fmaf(Qs[r * ks + j], Hs[j * kDvt + cc], a1);
                 for (int s = 0; s <= r; ++s) a2 = fmaf(P[r * 65 + s], Vn[s * us + cc], a2);
-                st_out(op + (r0 + r) * dv + dv0 + cc, expf(g[r]) * a1 + a2);
+                st_out(op + (r0 + r) * dv + dv0 + cc, (vg ? a1 : expf(g[r]) * a1) + a2);
             }
         }
         __syncthreads();  // every read of H for this chunk is done
@@ -278,8 +332,16 @@ k_simt_state(FwdArgs a, const float *__restrict__ W, const float *__restrict__ U
         for (int i = tid; i < dk * kDvt; i += kThreads) {
             const int j = i / kDvt, cc = i - j * kDvt;
             float acc = 0.f;
-            for (int s = 0; s < kChunk; ++s) acc = fmaf(Ks[s * ks + j] * e[s], Vn[s * us + cc], acc);
-            Hs[i] = fmaf(decay, Hs[i], acc);
+            if (vg) {   // row j of H decays by its own dimension's gate
+                const float glj = Gv[(kChunk - 1) * ks + j];
+                for (int s = 0; s < kChunk; ++s)
+                    acc = fmaf(Ks[s * ks + j] * expf(glj - Gv[s * ks + j]), Vn[s * us + cc], acc);
+                Hs[i] = fmaf(expf(glj), Hs[i], acc);
+            } else {
+                for (int s = 0; s < kChunk; ++s)
+                    acc = fmaf(Ks[s * ks + j] * e[s], Vn[s * us + cc], acc);
+                Hs[i] = fmaf(decay, Hs[i], acc);
+            }
         }
     }
     __syncthreads();
@@ -291,20 +353,22 @@ k_simt_state(FwdArgs a, const float *__restrict__ W, const float *__restrict__ U
     }
 }
 
-size_t prep_smem(int dk, int dv) {
+size_t prep_smem(int dk, int dv, bool vg) {
     return sizeof(float) * ((size_t)kChunk * (dk + 1) + (size_t)kChunk * (dv + 1) +
-                            2 * kChunk * 65 + 3 * kChunk);
+                            2 * kChunk * 65 + 3 * kChunk + (vg ? (size_t)kChunk * (dk + 1) : 0));
 }
-size_t state_smem(int dk) {
+size_t state_smem(int dk, bool vg) {
     return sizeof(float) * ((size_t)dk * kDvt + 3 * (size_t)kChunk * (dk + 1) +
-                            2 * kChunk * (kDvt + 1) + kChunk * 65 + 2 * kChunk);
+                            2 * kChunk * (kDvt + 1) + kChunk * 65 + 2 * kChunk +
+                            (vg ? (size_t)kChunk * (dk + 1) : 0));
 }
 
 template <typename TIn>
 gdn_status launch(const FwdArgs &a) {
     int *err = device_error_word();
     cudaStream_t st = a.stream;
-    const size_t psm = prep_smem(a.dk, a.dv), ssm = state_smem(a.dk);
+    const size_t psm = prep_smem(a.dk, a.dv, a.vector_gate),
+                 ssm = state_smem(a.dk, a.vector_gate);
     if (cudaFuncSetAttribute(k_simt_prep<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)psm) != cudaSuccess ||
         cudaFuncSetAttribute(k_simt_state<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -315,7 +379,8 @@ gdn_status launch(const FwdArgs &a) {
     const size_t rows = (size_t)a.rows > 0 ? (size_t)a.rows : 1;
     if (scratch_alloc((void **)&W, rows * a.dk * sizeof(float), st) != cudaSuccess ||
         scratch_alloc((void **)&U, rows * a.dv * sizeof(float), st) != cudaSuccess ||
-        scratch_alloc((void **)&G, rows * sizeof(float), st) != cudaSuccess) {
+        scratch_alloc((void **)&G, rows * (a.vector_gate ? a.dk : 1) * sizeof(float), st) !=
+            cudaSuccess) {
         if (W) scratch_free(W, st);
         if (U) scratch_free(U, st);
         return GDN_ERR_CUDA;
@@ -409,7 +474,8 @@ template <typename TIn>
 gdn_status launch_noalloc(const FwdArgs &a, float *scratch) {
     int *err = device_error_word();
     cudaStream_t st = a.stream;
-    const size_t psm = prep_smem(a.dk, a.dv), ssm = state_smem(a.dk);
+    const size_t psm = prep_smem(a.dk, a.dv, a.vector_gate),
+                 ssm = state_smem(a.dk, a.vector_gate);
     if (cudaFuncSetAttribute(k_simt_prep<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)psm) != cudaSuccess ||
         cudaFuncSetAttribute(k_simt_state<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -434,7 +500,8 @@ gdn_status launch_noalloc(const FwdArgs &a, float *scratch) {
 
 gdn_status simt_forward_noalloc(const FwdArgs &a) {
     if (a.sm.cu) return GDN_ERR_UNSUPPORTED;   // dense batches only
-    const size_t need = (size_t)a.rows * (size_t)(a.dk + a.dv + 1) * sizeof(float);
+    const size_t need =
+        (size_t)a.rows * (size_t)(a.dk + a.dv + (a.vector_gate ? a.dk : 1)) * sizeof(float);
     if (need > kNoallocScratchBytes) return GDN_ERR_TOO_LARGE;
     float *scratch = nullptr;
     gdn_status rc = noalloc_scratch(&scratch);

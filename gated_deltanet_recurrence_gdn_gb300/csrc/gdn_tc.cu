@@ -972,7 +972,7 @@ gdn_status tc_segmented(const FwdArgs &a, const __nv_bfloat16 *Tbuf, int S) {
 }  // namespace
 
 bool tc_supported(const FwdArgs &a) {
-    if (a.dt != GDN_BF16) return false;
+    if (a.dt != GDN_BF16 || a.vector_gate) return false;
     if (a.dk != 64 && a.dk != 128) return false;
     if (a.dv % kNV != 0 || a.dv > 256) return false;
     if (a.sm.N > 65535 || a.sm.H > 65535) return false;

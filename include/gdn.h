@@ -180,9 +180,19 @@ int gdn_last_impl(void);
  *   alpha = beta = 1 is plain linear attention.  In the chunked form the
  *   erase term is what makes A, T and W; without it T = I and W = 0, and the
  *   same kernels run with the in-chunk inverse skipped.
+ *   GDN_FLAG_VECTOR_GATE: the forget gate is a vector over the key dimension
+ *   ("Gated DeltaNet GPU并行实现：拆解线性注意力循环的两种高效方案", section
+ *   2.2: a per-dimension gate puts an extra diagonal factor in the affine
+ *   map).  log_alpha is then [B][H][T][d_k] (varlen: [H][T_total][d_k]),
+ *   and the step decays the state's key columns before the erase:
+ *       S_t = (S_{t-1} diag(alpha_t)) (I - beta_t k_t k_t^T) + beta_t v_t k_t^T.
+ *   With all d_k entries of a row equal this is the scalar-gate recurrence.
+ *   Both flags together give gated linear attention with a vector gate.
+ *   Vector gates run on the CUDA-core path only: with GDN_IMPL_TC forced the
+ *   call returns GDN_ERR_UNSUPPORTED, with GDN_IMPL_AUTO it takes that path.
  * Unknown flag bits give GDN_ERR_INVALID_ARG.
  */
-enum { GDN_FLAG_NO_ERASE = 1 };
+enum { GDN_FLAG_NO_ERASE = 1, GDN_FLAG_VECTOR_GATE = 2 };
 gdn_status gdn_fwd_ex(const void *q, const void *k, const void *v,
                       const float *log_alpha, const float *beta, const float *h0,
                       void *o, float *hT,

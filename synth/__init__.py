@@ -8,6 +8,8 @@ holds none of the method's arithmetic, only the input recipe:
 * beta = sigmoid(N(0, 1));
 * log_alpha = -0.5 * softplus(N(0, 1))        ("fast" decay), or
   log_alpha = -softplus(N(-1, 1))              ("slow" decay, long context);
+* with a gate per key dimension (vector_gate=True) log_alpha gets a trailing
+  d_k axis, each entry drawn by the same rule independently;
 * h0 = 0, or h0 ~ N(0, std^2) per (sequence, head);
 * packed variable-length batches draw their lengths uniformly from
   [len_min, len_max] with a seeded numpy generator.
@@ -82,8 +84,9 @@ def _unit_rows(x):
     return x / x.norm(dim=-1, keepdim=True).clamp_min(1e-30)
 
 
-def _gates(shape, g, device, decay):
+def _gates(shape, g, device, decay, la_shape=None):
     beta = torch.sigmoid(_normal(shape, g, device))
+    shape = la_shape if la_shape is not None else shape
     if decay == "fast":
         la = -0.5 * torch.nn.functional.softplus(_normal(shape, g, device))
     elif decay == "slow":
@@ -96,18 +99,19 @@ def _gates(shape, g, device, decay):
 
 
 def make_dense(B, H, T, dk, dv, *, io="bf16", decay="fast", h0_std=0.0, seed=0,
-               device="cpu") -> Inputs:
-    """Dense batch: q,k [B,H,T,dk], v [B,H,T,dv], gates [B,H,T], h0 [B,H,dv,dk]."""
+               device="cpu", vector_gate=False) -> Inputs:
+    """Dense batch: q,k [B,H,T,dk], v [B,H,T,dv], gates [B,H,T], h0 [B,H,dv,dk]
+    (log_alpha [B,H,T,dk] with vector_gate)."""
     g = _gen(device, seed)
     dt = IO_DTYPES[io]
     q = _unit_rows(_normal((B, H, T, dk), g, device)).to(dt)
     k = _unit_rows(_normal((B, H, T, dk), g, device)).to(dt)
     v = _normal((B, H, T, dv), g, device).to(dt)
-    la, beta = _gates((B, H, T), g, device, decay)
+    la, beta = _gates((B, H, T), g, device, decay, (B, H, T, dk) if vector_gate else None)
     h0 = _normal((B, H, dv, dk), g, device, std=h0_std) if h0_std > 0 else None
     return Inputs(q, k, v, la, beta, h0, None,
                   dict(B=B, H=H, T=T, dk=dk, dv=dv, io=io, decay=decay, h0_std=h0_std,
-                       seed=seed))
+                       seed=seed, vector_gate=vector_gate))
 
 
 def varlen_lengths(N, len_min, len_max, seed):
@@ -116,9 +120,10 @@ def varlen_lengths(N, len_min, len_max, seed):
 
 
 def make_varlen(lengths, H, dk, dv, *, io="bf16", decay="fast", h0_std=0.0, seed=0,
-                device="cpu") -> Inputs:
+                device="cpu", vector_gate=False) -> Inputs:
     """Packed batch: q,k [H,T_total,dk], v [H,T_total,dv], gates [H,T_total],
-    cu_seqlens int32 [N+1], h0 [N,H,dv,dk]."""
+    cu_seqlens int32 [N+1], h0 [N,H,dv,dk] (log_alpha [H,T_total,dk] with
+    vector_gate)."""
     lengths = np.asarray(lengths, dtype=np.int64)
     cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int64)
     TT = int(cu[-1])
@@ -128,12 +133,12 @@ def make_varlen(lengths, H, dk, dv, *, io="bf16", decay="fast", h0_std=0.0, seed
     q = _unit_rows(_normal((H, TT, dk), g, device)).to(dt)
     k = _unit_rows(_normal((H, TT, dk), g, device)).to(dt)
     v = _normal((H, TT, dv), g, device).to(dt)
-    la, beta = _gates((H, TT), g, device, decay)
+    la, beta = _gates((H, TT), g, device, decay, (H, TT, dk) if vector_gate else None)
     h0 = _normal((N, H, dv, dk), g, device, std=h0_std) if h0_std > 0 else None
     cu_t = torch.tensor(cu, dtype=torch.int32, device=device)
     return Inputs(q, k, v, la, beta, h0, cu_t,
                   dict(N=N, H=H, T_total=TT, dk=dk, dv=dv, io=io, decay=decay,
-                       h0_std=h0_std, seed=seed))
+                       h0_std=h0_std, seed=seed, vector_gate=vector_gate))
 
 
 def make_decode(B, H, dk, dv, *, io="bf16", decay="fast", state_std=0.02, n_slots=None,

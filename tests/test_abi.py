@@ -89,6 +89,13 @@ def test_host_checks(lib):
     assert g(*_args(), None, 2, 1, 10, 64, 64, 64, 1, None) == gdn.GDN_ERR_INVALID_ARG
     assert g(*_args(), FAKE, 0, 1, 10, 64, 64, 64, 1, None) == gdn.GDN_ERR_INVALID_ARG
     assert g(*_args(), FAKE, 0, 1, 0, 64, 64, 64, 1, None) == gdn.GDN_OK
+    # variant flags: both known bits pass the checks, any other bit is refused
+    fx, gx = lib.gdn_fwd_ex, lib.gdn_fwd_varlen_ex
+    both = gdn.GDN_FLAG_NO_ERASE | gdn.GDN_FLAG_VECTOR_GATE
+    assert fx(*_args(), 0, 4, 64, 64, 64, 64, 1, both, None) == gdn.GDN_OK
+    assert fx(*_args(), 0, 4, 64, 64, 64, 64, 1, 4, None) == gdn.GDN_ERR_INVALID_ARG
+    assert gx(*_args(), FAKE, 0, 1, 0, 64, 64, 64, 1, both, None) == gdn.GDN_OK
+    assert gx(*_args(), FAKE, 0, 1, 0, 64, 64, 64, 1, 8, None) == gdn.GDN_ERR_INVALID_ARG
 
 
 def test_decode_host_checks(lib):

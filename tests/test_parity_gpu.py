@@ -334,3 +334,62 @@ def test_no_erase_plain_linear_attention(impl):
     mask = torch.tril(torch.ones(T, T, dtype=torch.float64, device="cuda"))
     ref = ((qf @ kf.transpose(-1, -2)) * mask) @ vf
     assert U.rel(U.f64(o), U.f64(ref)) <= 1e-2
+
+
+# ------------------------------------------------- a forget gate per key dimension
+
+
+@pytest.mark.parametrize("erase", [True, False])
+@pytest.mark.parametrize("B,H,T,dk,dv,io", [(2, 2, 300, 128, 128, "bf16"),
+                                            (1, 3, 200, 64, 64, "bf16"),
+                                            (2, 1, 150, 32, 48, "f32")])
+def test_vector_gate_matches_oracle(erase, B, H, T, dk, dv, io):
+    x = synth.make_dense(B, H, T, dk, dv, io=io, h0_std=0.02, seed=T + 5, device="cuda",
+                         vector_gate=True)
+    assert x.log_alpha.shape == (B, H, T, dk)
+    with gdn.use_impl(gdn.GDN_IMPL_AUTO):
+        o, hT = gdn.gdn_fwd(x.q, x.k, x.v, x.log_alpha, x.beta, x.h0, check=True, erase=erase)
+    assert gdn.load().gdn_last_impl() == gdn.GDN_IMPL_SIMT
+    U.sync()
+    import oracle
+    o_ref, h_ref = oracle.gdn_fwd(U.f64(x.q), U.f64(x.k), U.f64(x.v), U.f64(x.log_alpha),
+                                  U.f64(x.beta), U.f64(x.h0), threads=U.ORACLE_THREADS,
+                                  erase=erase, vector_gate=True)
+    check(o, hT, o_ref, h_ref, io)
+
+
+@pytest.mark.parametrize("erase", [True, False])
+def test_vector_gate_varlen_matches_oracle(erase):
+    y = synth.make_varlen([1, 63, 64, 65, 200, 0, 129], 2, 128, 128, io="bf16", h0_std=0.02,
+                          seed=23, device="cuda", vector_gate=True)
+    o, hT = gdn.gdn_fwd_varlen(y.q, y.k, y.v, y.log_alpha, y.beta, y.cu_seqlens, y.h0,
+                               check=True, erase=erase)
+    U.sync()
+    import oracle
+    o_ref, h_ref = oracle.gdn_fwd_varlen(U.f64(y.q), U.f64(y.k), U.f64(y.v),
+                                         U.f64(y.log_alpha), U.f64(y.beta),
+                                         y.cu_seqlens.cpu().numpy(), U.f64(y.h0),
+                                         erase=erase, vector_gate=True)
+    check(o, hT, o_ref, h_ref, "bf16")
+
+
+def test_vector_gate_uniform_rows_equal_scalar_gate():
+    # a per-dimension gate whose d_k entries are all equal is the scalar gate:
+    # the vector-gate kernels must agree with the tensor-core scalar path
+    x = synth.make_dense(2, 2, 300, 128, 128, io="bf16", h0_std=0.02, seed=41, device="cuda")
+    la_vec = x.log_alpha[..., None].expand(-1, -1, -1, 128).contiguous()
+    with gdn.use_impl(gdn.GDN_IMPL_TC):
+        o_s, h_s = gdn.gdn_fwd(x.q, x.k, x.v, x.log_alpha, x.beta, x.h0, check=True)
+    o_v, h_v = gdn.gdn_fwd(x.q, x.k, x.v, la_vec, x.beta, x.h0, check=True)
+    U.sync()
+    assert U.rel(U.f64(o_v), U.f64(o_s)) <= 1e-2
+    assert U.rel(U.f64(h_v), U.f64(h_s)) <= 2e-2
+
+
+def test_vector_gate_not_on_tensor_core_path():
+    x = synth.make_dense(1, 1, 128, 128, 128, io="bf16", seed=43, device="cuda",
+                         vector_gate=True)
+    with gdn.use_impl(gdn.GDN_IMPL_TC):
+        with pytest.raises(gdn.GdnError) as e:
+            gdn.gdn_fwd(x.q, x.k, x.v, x.log_alpha, x.beta, None)
+    assert e.value.status == gdn.GDN_ERR_UNSUPPORTED
