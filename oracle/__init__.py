@@ -11,11 +11,17 @@ sections 2.1-2.2).  This file only compiles it with gcc and marshals numpy
 arrays.  ``threads > 1`` runs independent (sequence, head) problems on several
 host threads; each problem is still the same single-threaded loop.
 
+``gdn_bwd`` / ``gdn_bwd_varlen`` return the gradient of
+L = sum(dO * o) + sum(dhT * hT) with respect to every input (reverse-mode
+differentiation of the same loop, the forward states kept).
+
 Parity status: pinned by closed forms and invariants in
 tests/test_oracle_pins.py (beta = 0 decay, exact recall S k = v for
 alpha = beta = 1, affine-map bracketing, the T = 1 closed form, reduction to
-(gated) linear attention, linearity, continuation, varlen splitting) and by
-planted-mistake checks that each of those pins catches.
+(gated) linear attention, linearity, continuation, varlen splitting; for the
+gradient: central finite differences of the forward loop, the exact adjoint
+identities of its linear arguments) and by planted-mistake checks that each
+of those pins catches.
 """
 from __future__ import annotations
 
@@ -72,6 +78,10 @@ def load_library(path: str):
     lib.gdn_oracle_vg_fwd.argtypes = [_dp] * 8 + [ctypes.c_long] * 6
     lib.gdn_oracle_vg_fwd_varlen.restype = ctypes.c_int
     lib.gdn_oracle_vg_fwd_varlen.argtypes = [_dp] * 8 + [_lp] + [ctypes.c_long] * 6
+    lib.gdn_oracle_bwd.restype = ctypes.c_int
+    lib.gdn_oracle_bwd.argtypes = [_dp] * 14 + [ctypes.c_long] * 6
+    lib.gdn_oracle_bwd_varlen.restype = ctypes.c_int
+    lib.gdn_oracle_bwd_varlen.argtypes = [_dp] * 14 + [_lp] + [ctypes.c_long] * 6
     return lib
 
 
@@ -189,3 +199,65 @@ def gdn_fwd_varlen(q, k, v, log_alpha, beta, cu_seqlens, h0=None, *, threads: in
     with ThreadPoolExecutor(max_workers=threads) as ex:
         list(ex.map(lambda j: run(*j), [(n, h) for n in range(N) for h in range(H)]))
     return o, hT
+
+
+def gdn_bwd(q, k, v, log_alpha, beta, h0, dout, dhT=None, *, threads: int = 1, lib=None,
+            erase=True):
+    """Dense gradient oracle.  Inputs as gdn_fwd; dout [B,H,T,dv]; dhT
+    [B,H,dv,dk] or None (zero).  Returns (dq, dk, dv, dlog_alpha, dbeta, dh0)
+    in fp64, each in its input's layout (dh0 [B,H,dv,dk] even when h0 is None:
+    the gradient at the zero state)."""
+    lib = lib or _get()
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    la, be, do = _f64(log_alpha), _f64(beta), _f64(dout)
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    assert k.shape == q.shape and v.shape == (B, H, T, dv) and do.shape == v.shape
+    assert la.shape == (B, H, T) and be.shape == (B, H, T)
+    h0 = None if h0 is None else _f64(h0)
+    dhT = None if dhT is None else _f64(dhT)
+    for t in (h0, dhT):
+        assert t is None or t.shape == (B, H, dv, dk)
+    out = [np.zeros(q.shape), np.zeros(k.shape), np.zeros(v.shape), np.zeros(la.shape),
+           np.zeros(be.shape), np.zeros((B, H, dv, dk))]
+
+    def run(b, h):
+        def sl(a):
+            return None if a is None else _ptr(a[b, h])
+        rc = lib.gdn_oracle_bwd(sl(q), sl(k), sl(v), sl(la), sl(be), sl(h0), sl(do), sl(dhT),
+                                *(sl(x) for x in out), 1, 1, T, dk, dv, 1 if erase else 0)
+        if rc != 0:
+            raise ValueError("oracle rejected its arguments")
+
+    jobs = [(b, h) for b in range(B) for h in range(H)]
+    if threads <= 1 or len(jobs) <= 1:
+        for j in jobs:
+            run(*j)
+    else:
+        with ThreadPoolExecutor(max_workers=threads) as ex:
+            list(ex.map(lambda j: run(*j), jobs))
+    return tuple(out)
+
+
+def gdn_bwd_varlen(q, k, v, log_alpha, beta, cu_seqlens, h0, dout, dhT=None, *, lib=None,
+                   erase=True):
+    """Packed gradient oracle.  Inputs as gdn_fwd_varlen; dout [H,T_total,dv];
+    dhT [N,H,dv,dk] or None.  Returns (dq, dk, dv, dlog_alpha, dbeta, dh0)."""
+    lib = lib or _get()
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    la, be, do = _f64(log_alpha), _f64(beta), _f64(dout)
+    cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int64))
+    H, TT, dk = q.shape
+    dv = v.shape[-1]
+    N = cu.shape[0] - 1
+    h0 = None if h0 is None else _f64(h0)
+    dhT = None if dhT is None else _f64(dhT)
+    out = [np.zeros(q.shape), np.zeros(k.shape), np.zeros(v.shape), np.zeros(la.shape),
+           np.zeros(be.shape), np.zeros((N, H, dv, dk))]
+    rc = lib.gdn_oracle_bwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(la), _ptr(be), _ptr(h0),
+                                   _ptr(do), _ptr(dhT), *(_ptr(x) for x in out),
+                                   cu.ctypes.data_as(_lp), N, H, TT, dk, dv,
+                                   1 if erase else 0)
+    if rc != 0:
+        raise ValueError("oracle rejected its arguments")
+    return tuple(out)

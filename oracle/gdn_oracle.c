@@ -45,8 +45,23 @@
  * alpha_t = exp(log_alpha_t) with log_alpha_t a d_k-vector; with the erase
  * term off it is gated linear attention with a vector gate.
  *
+ * The last part is the gradient of the first two loops.  No page writes the
+ * backward pass of the delta rule out; "企业官网建设流程全解析" (a page on
+ * linear-attention training) recomputes the recurrent state in the backward
+ * pass instead of storing it (sections 2 and 4.3) and checks gradients
+ * numerically (section 5.3).  The gradient here is the plain definition: for
+ * output weights dO [T][dv] and dhT [dv][dk] it returns the gradient of
+ *
+ *     L = sum_t dO_t . o_t + <dhT, hT>
+ *
+ * with respect to q, k, v, log_alpha, beta and h0, by reverse-mode
+ * differentiation of the token loop: the forward states S_{-1..T-1} are kept,
+ * then the tokens are walked backwards with the adjoint dS of the current
+ * state.
+ *
  * Parity pins for this file (closed forms, invariants, reductions to linear
- * attention, planted-mistake checks) live in tests/test_oracle_pins.py.
+ * attention, finite differences, planted-mistake checks) live in
+ * tests/test_oracle_pins.py.
  */
 #include <math.h>
 #include <stddef.h>
@@ -396,5 +411,180 @@ int gdn_oracle_vg_fwd_varlen(const double *q, const double *k, const double *v,
     }
     free(S);
     free(Sk);
+    return 0;
+}
+
+/*
+ * Gradient of one (sequence, head); erase = 0 differentiates the gated
+ * linear attention loop instead.  Layouts as oracle_one; dout [T][dv];
+ * dhT, h0 and dh0 may be NULL (zero weight / zero state / not written).
+ * Per token t, with X = S_{t-1}, a = alpha_t, b = beta_t and dS the adjoint
+ * of S_t (which already holds dO_t q_t^T from o_t = S_t q_t):
+ *     dq_t       = S_t^T dO_t
+ *     dv_t       = b dS k_t
+ *     dbeta_t    = (dS k_t) . (v_t - a X k_t)            [erase]
+ *                  (dS k_t) . v_t                        [no erase]
+ *     dalpha_t   = <dS, X> - b (dS k_t) . (X k_t)        [no erase: <dS, X>]
+ *     dk_t       = b dS^T v_t - a b (X^T dS k_t + dS^T X k_t)   [no erase: b dS^T v_t]
+ *     dS_{t-1}   = a dS (I - b k_t k_t^T)                [no erase: a dS]
+ *     dlog_alpha_t = a dalpha_t
+ * Returns 0, or -1 when the state history cannot be allocated.
+ */
+static int oracle_one_bwd(const double *q, const double *k, const double *v,
+                          const double *la, const double *beta, const double *h0,
+                          const double *dout, const double *dhT,
+                          double *dq, double *dk_, double *dv_, double *dla,
+                          double *dbeta, double *dh0,
+                          long T, long dk, long dv, long erase)
+{
+    const long n = dv * dk;
+    long t, i, j;
+    double *St = (double *)malloc(sizeof(double) * (size_t)((T + 1) * n));
+    double *dS = (double *)malloc(sizeof(double) * (size_t)n);
+    double *Xk = (double *)malloc(sizeof(double) * (size_t)dv);
+    double *dSk = (double *)malloc(sizeof(double) * (size_t)dv);
+    if (!St || !dS || !Xk || !dSk) {
+        free(St);
+        free(dS);
+        free(Xk);
+        free(dSk);
+        return -1;
+    }
+    /* forward, keeping every state: St + (t+1)*n holds S_t, St holds S_{-1} */
+    if (h0)
+        memcpy(St, h0, sizeof(double) * (size_t)n);
+    else
+        memset(St, 0, sizeof(double) * (size_t)n);
+    for (t = 0; t < T; ++t) {
+        const double *X = St + t * n;
+        double *Y = St + (t + 1) * n;
+        const double *kt = k + t * dk, *vt = v + t * dv;
+        const double a = exp(la[t]), b = beta[t];
+        for (i = 0; i < dv; ++i) {
+            double acc = 0.0;
+            for (j = 0; j < dk; ++j)
+                acc += X[i * dk + j] * kt[j];
+            Xk[i] = erase ? acc : 0.0;
+        }
+        for (i = 0; i < dv; ++i)
+            for (j = 0; j < dk; ++j)
+                Y[i * dk + j] = a * (X[i * dk + j] - b * Xk[i] * kt[j]) + b * vt[i] * kt[j];
+    }
+    /* backward */
+    if (dhT)
+        memcpy(dS, dhT, sizeof(double) * (size_t)n);
+    else
+        memset(dS, 0, sizeof(double) * (size_t)n);
+    for (t = T - 1; t >= 0; --t) {
+        const double *X = St + t * n;
+        const double *Y = St + (t + 1) * n;
+        const double *kt = k + t * dk, *vt = v + t * dv, *qt = q + t * dk;
+        const double *dot = dout + t * dv;
+        const double a = exp(la[t]), b = beta[t];
+        double sx = 0.0, db = 0.0, cross = 0.0;
+        /* o_t = S_t q_t */
+        for (i = 0; i < dv; ++i)
+            for (j = 0; j < dk; ++j)
+                dS[i * dk + j] += dot[i] * qt[j];
+        for (j = 0; j < dk; ++j) {
+            double acc = 0.0;
+            for (i = 0; i < dv; ++i)
+                acc += Y[i * dk + j] * dot[i];
+            dq[t * dk + j] = acc;
+        }
+        for (i = 0; i < dv; ++i) {
+            double a1 = 0.0, a2 = 0.0;
+            for (j = 0; j < dk; ++j) {
+                a1 += dS[i * dk + j] * kt[j];
+                a2 += X[i * dk + j] * kt[j];
+                sx += dS[i * dk + j] * X[i * dk + j];
+            }
+            dSk[i] = a1;
+            Xk[i] = a2;
+        }
+        for (i = 0; i < dv; ++i) {
+            dv_[t * dv + i] = b * dSk[i];
+            db += dSk[i] * (erase ? vt[i] - a * Xk[i] : vt[i]);
+            cross += dSk[i] * Xk[i];
+        }
+        dbeta[t] = db;
+        dla[t] = a * (erase ? sx - b * cross : sx);
+        for (j = 0; j < dk; ++j) {
+            double acc = 0.0;
+            for (i = 0; i < dv; ++i) {
+                acc += b * dS[i * dk + j] * vt[i];
+                if (erase)
+                    acc -= a * b * (X[i * dk + j] * dSk[i] + dS[i * dk + j] * Xk[i]);
+            }
+            dk_[t * dk + j] = acc;
+        }
+        for (i = 0; i < dv; ++i)
+            for (j = 0; j < dk; ++j)
+                dS[i * dk + j] = a * (dS[i * dk + j] - (erase ? b * dSk[i] * kt[j] : 0.0));
+    }
+    if (dh0)
+        memcpy(dh0, dS, sizeof(double) * (size_t)n);
+    free(St);
+    free(dS);
+    free(Xk);
+    free(dSk);
+    return 0;
+}
+
+/*
+ * Dense batch gradient: inputs as gdn_oracle_fwd, dout [B][H][T][dv], dhT
+ * [B][H][dv][dk] (or NULL); gradients in the layouts of their inputs.
+ */
+int gdn_oracle_bwd(const double *q, const double *k, const double *v,
+                   const double *log_alpha, const double *beta, const double *h0,
+                   const double *dout, const double *dhT,
+                   double *dq, double *dk_, double *dv_, double *dla, double *dbeta,
+                   double *dh0, long B, long H, long T, long dk, long dv, long erase)
+{
+    long bh;
+    if (B < 0 || H < 0 || T < 0 || dk <= 0 || dv <= 0)
+        return -1;
+    for (bh = 0; bh < B * H; ++bh)
+        if (oracle_one_bwd(q + bh * T * dk, k + bh * T * dk, v + bh * T * dv,
+                           log_alpha + bh * T, beta + bh * T,
+                           h0 ? h0 + bh * dv * dk : NULL, dout + bh * T * dv,
+                           dhT ? dhT + bh * dv * dk : NULL,
+                           dq + bh * T * dk, dk_ + bh * T * dk, dv_ + bh * T * dv,
+                           dla + bh * T, dbeta + bh * T,
+                           dh0 ? dh0 + bh * dv * dk : NULL, T, dk, dv, erase))
+            return -1;
+    return 0;
+}
+
+/* Packed batch gradient: layouts as gdn_oracle_fwd_varlen. */
+int gdn_oracle_bwd_varlen(const double *q, const double *k, const double *v,
+                          const double *log_alpha, const double *beta, const double *h0,
+                          const double *dout, const double *dhT,
+                          double *dq, double *dk_, double *dv_, double *dla, double *dbeta,
+                          double *dh0, const long *cu_seqlens, long N, long H, long T_total,
+                          long dk, long dv, long erase)
+{
+    long n, h;
+    if (N < 0 || H < 0 || T_total < 0 || dk <= 0 || dv <= 0)
+        return -1;
+    if (N > 0 && (cu_seqlens[0] != 0 || cu_seqlens[N] != T_total))
+        return -1;
+    for (n = 0; n < N; ++n)
+        if (cu_seqlens[n + 1] < cu_seqlens[n])
+            return -1;
+    for (n = 0; n < N; ++n) {
+        long s0 = cu_seqlens[n];
+        long len = cu_seqlens[n + 1] - s0;
+        for (h = 0; h < H; ++h) {
+            long rw = h * T_total + s0;
+            long st = (n * H + h) * dv * dk;
+            if (oracle_one_bwd(q + rw * dk, k + rw * dk, v + rw * dv, log_alpha + rw,
+                               beta + rw, h0 ? h0 + st : NULL, dout + rw * dv,
+                               dhT ? dhT + st : NULL, dq + rw * dk, dk_ + rw * dk,
+                               dv_ + rw * dv, dla + rw, dbeta + rw, dh0 ? dh0 + st : NULL,
+                               len, dk, dv, erase))
+                return -1;
+        }
+    }
     return 0;
 }

@@ -19,6 +19,16 @@ factor) is pinned to the scalar loops when its entries are equal, to the
 explicit affine maps diag(alpha_t)(I - beta_t k k^T), beta_t v k^T composed in
 random bracketings (which fixes that the decay acts before the erase), and to
 its beta = 0 closed form.
+
+The gradient oracle (no page writes the delta rule's backward pass out; the
+page "企业官网建设流程全解析" recomputes the state in the backward pass,
+sections 2 and 4.3, and checks gradients numerically, section 5.3) is pinned
+to central finite differences of the forward loops (a five-point stencil in
+fp64, every input along a random direction), to the exact adjoint identities
+of the forward's linear arguments -- L = <dO, O> + <dhT, hT> is linear in
+(h0, V) jointly, so L = <dV, V> + <dh0, h0>, and O is linear in q while hT
+does not depend on it, so <dO, O> = <dq, q> -- and to per-sequence calls for
+packed batches.
 """
 from __future__ import annotations
 
@@ -432,6 +442,101 @@ def pin_vg_varlen_split(lib, dk=4, dv=3, H=2, seed=34):
     return worst
 
 
+
+# ------------------------------------------------------------------ gradient
+
+_FD_STEP = 1e-3
+_FD_TOL = 1e-9     # five-point stencil: truncation O(h^4), rounding ~1e-13 / h
+
+
+def _bwd_inputs(rng, T, dk, dv, H=1):
+    q, k, v, la, be = _rand_inputs(rng, 1, H, T, dk, dv)
+    h0 = rng.standard_normal((1, H, dv, dk))
+    dO = rng.standard_normal((1, H, T, dv))
+    dhT = rng.standard_normal((1, H, dv, dk))
+    return q, k, v, la, be, h0, dO, dhT
+
+
+def _loss(lib, xs, dO, dhT, erase):
+    q, k, v, la, be, h0 = xs
+    if erase:
+        o, hT = oracle.gdn_fwd(q, k, v, la, be, h0, lib=lib)
+    else:
+        o, hT = oracle.gdn_fwd(q, k, v, la, be, h0, lib=lib, erase=False)
+    return float(np.sum(dO * o) + np.sum(dhT * hT))
+
+
+def pin_bwd_finite_differences(lib, dk=4, dv=3, T=7, seed=51, erase=True):
+    """Each gradient against the five-point central difference of the
+    forward loss along a random direction: (-L(x+2hD) + 8L(x+hD) - 8L(x-hD)
+    + L(x-2hD)) / 12h  =  <grad, D>."""
+    rng = np.random.default_rng(seed)
+    q, k, v, la, be, h0, dO, dhT = _bwd_inputs(rng, T, dk, dv)
+    xs = [q, k, v, la, be, h0]
+    grads = oracle.gdn_bwd(q, k, v, la, be, h0, dO, dhT, lib=lib, erase=erase)
+    worst = 0.0
+    for i, x in enumerate(xs):
+        D = rng.standard_normal(x.shape)
+        f = []
+        for m in (2, 1, -1, -2):
+            ys = list(xs)
+            ys[i] = x + m * _FD_STEP * D
+            f.append(_loss(lib, ys, dO, dhT, erase))
+        fd = (-f[0] + 8 * f[1] - 8 * f[2] + f[3]) / (12 * _FD_STEP)
+        an = float(np.sum(grads[i] * D))
+        err = abs(fd - an) / max(abs(an), abs(fd), 1e-3)
+        worst = max(worst, err / _FD_TOL * PIN_TOL)   # reported on the PIN_TOL scale
+    return worst
+
+
+def pin_bwd_fd_no_erase(lib, **kw):
+    return pin_bwd_finite_differences(lib, erase=False, seed=52, **kw)
+
+
+def pin_bwd_adjoint(lib, dk=5, dv=4, T=11, seed=53):
+    """L = <dO, O> + <dhT, hT> is linear in (h0, V), so L = <dV, V> + <dh0, h0>;
+    O is linear in q and hT does not depend on it, so <dO, O> = <dq, q>.
+    Both modes (with and without the erase term)."""
+    rng = np.random.default_rng(seed)
+    q, k, v, la, be, h0, dO, dhT = _bwd_inputs(rng, T, dk, dv, H=2)
+    worst = 0.0
+    for erase in (True, False):
+        o, hT = oracle.gdn_fwd(q, k, v, la, be, h0, lib=lib, erase=erase)
+        dq, _, dv_, _, _, dh0 = oracle.gdn_bwd(q, k, v, la, be, h0, dO, dhT, lib=lib,
+                                              erase=erase)
+        L_o, L_h = float(np.sum(dO * o)), float(np.sum(dhT * hT))
+        scale = max(abs(L_o) + abs(L_h), 1e-300)
+        worst = max(worst,
+                    abs(L_o + L_h - float(np.sum(dv_ * v) + np.sum(dh0 * h0))) / scale,
+                    abs(L_o - float(np.sum(dq * q))) / max(abs(L_o), 1e-300))
+    return worst
+
+
+def pin_bwd_varlen_split(lib, dk=4, dv=3, H=2, seed=54):
+    """Packed gradients equal the per-sequence dense gradients (both modes)."""
+    rng = np.random.default_rng(seed)
+    lens = [3, 0, 7, 1, 5]
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    TT = int(cu[-1])
+    q, k, v, la, be = (x[0] for x in _rand_inputs(rng, 1, H, TT, dk, dv))
+    dO = rng.standard_normal((H, TT, dv))
+    h0 = rng.standard_normal((len(lens), H, dv, dk))
+    dhT = rng.standard_normal((len(lens), H, dv, dk))
+    worst = 0.0
+    for erase in (True, False):
+        g = oracle.gdn_bwd_varlen(q, k, v, la, be, cu, h0, dO, dhT, lib=lib, erase=erase)
+        for n in range(len(lens)):
+            a, b = int(cu[n]), int(cu[n + 1])
+            gd = oracle.gdn_bwd(q[None, :, a:b], k[None, :, a:b], v[None, :, a:b],
+                                la[None, :, a:b], be[None, :, a:b], h0[n][None],
+                                dO[None, :, a:b], dhT[n][None], lib=lib, erase=erase)
+            for i in range(5):
+                if b > a:
+                    worst = max(worst, _rel(g[i][:, a:b], gd[i][0]))
+            worst = max(worst, _rel(g[5][n], gd[5][0]))
+    return worst
+
+
 ALL_PINS = {
     "beta_zero": pin_beta_zero,
     "exact_recall": pin_exact_recall,
@@ -450,4 +555,8 @@ ALL_PINS = {
     "vg_bracketing": pin_vg_bracketing,
     "vg_beta_zero": pin_vg_beta_zero,
     "vg_varlen_split": pin_vg_varlen_split,
+    "bwd_finite_differences": pin_bwd_finite_differences,
+    "bwd_fd_no_erase": pin_bwd_fd_no_erase,
+    "bwd_adjoint": pin_bwd_adjoint,
+    "bwd_varlen_split": pin_bwd_varlen_split,
 }

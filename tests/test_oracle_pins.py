@@ -98,6 +98,19 @@ MUTANTS = {
     "vg_erase_ignored": ("Sk[i] = erase ? dot : 0.0;", "Sk[i] = 0.0;"),
     "vg_output_transposed": ("out += S[i * dk + j] * qt[j];", "out += S[j * dk + i] * qt[j];"),
     "vg_varlen_offset": ("long at = h * T_total + first;", "long at = h * T_total + first / 2;"),
+    # gradient loop
+    "bwd_output_term_dropped": ("dS[i * dk + j] += dot[i] * qt[j];",
+                                "dS[i * dk + j] += 0.0 * dot[i] * qt[j];"),
+    "bwd_dq_from_old_state": ("acc += Y[i * dk + j] * dot[i];", "acc += X[i * dk + j] * dot[i];"),
+    "bwd_dbeta_sign": ("(erase ? vt[i] - a * Xk[i] : vt[i])", "(erase ? vt[i] + a * Xk[i] : vt[i])"),
+    "bwd_dlog_alpha_unscaled": ("dla[t] = a * (erase ? sx - b * cross : sx);",
+                                "dla[t] = (erase ? sx - b * cross : sx);"),
+    "bwd_dk_cross_term_dropped": ("(X[i * dk + j] * dSk[i] + dS[i * dk + j] * Xk[i])",
+                                  "(X[i * dk + j] * dSk[i])"),
+    "bwd_adjoint_erase_dropped": ("(erase ? b * dSk[i] * kt[j] : 0.0)", "0.0"),
+    "bwd_dv_beta_dropped": ("dv_[t * dv + i] = b * dSk[i];", "dv_[t * dv + i] = dSk[i];"),
+    "bwd_varlen_state_offset": ("long st = (n * H + h) * dv * dk;",
+                                "long st = (h * N + n) * dv * dk;"),
 }
 
 
@@ -133,5 +146,20 @@ def test_planted_mistake_is_caught(mutant_dir, name):
         "vg_bracketing": P.pin_vg_bracketing(mlib, **square),
         "vg_beta_zero": P.pin_vg_beta_zero(mlib, **square),
         "vg_varlen": P.pin_vg_varlen_split(mlib, dk=5, dv=5),
+        "bwd_fd": P.pin_bwd_finite_differences(mlib),
+        "bwd_fd_no_erase": P.pin_bwd_fd_no_erase(mlib),
+        "bwd_adjoint": P.pin_bwd_adjoint(mlib),
+        "bwd_varlen": P.pin_bwd_varlen_split(mlib),
     }
     assert max(errs.values()) > 1e-6, errs
+
+
+def test_bwd_empty_sequence_passes_dhT_through(lib):
+    # T = 0: hT = h0, so dh0 = dhT and there are no token gradients
+    rng = np.random.default_rng(3)
+    h0 = rng.standard_normal((1, 2, 3, 4))
+    dhT = rng.standard_normal((1, 2, 3, 4))
+    z = np.zeros((1, 2, 0, 4))
+    g = oracle.gdn_bwd(z, z, np.zeros((1, 2, 0, 3)), np.zeros((1, 2, 0)), np.zeros((1, 2, 0)),
+                       h0, np.zeros((1, 2, 0, 3)), dhT, lib=lib)
+    assert g[0].shape == (1, 2, 0, 4) and np.array_equal(g[5], dhT)
