@@ -7,6 +7,7 @@ raises -- there is no CPU fallback.
 
     o, hT = gdn_fwd(q, k, v, log_alpha, beta, h0=None)
     o, hT = gdn_fwd_varlen(q, k, v, log_alpha, beta, cu_seqlens, h0=None)
+    dq, dk, dv, dlog_alpha, dbeta, dh0 = gdn_bwd(q, k, v, log_alpha, beta, h0, dout, dhT)
 
 Layouts follow ``include/gdn.h``: dense q, k [B,H,T,d_k], v [B,H,T,d_v]; packed
 q, k [H,T_total,d_k], v [H,T_total,d_v]; gates fp32; h0 / hT [.., H, d_v, d_k]
@@ -55,6 +56,8 @@ ABI = [
     ("gdn_fwd_host", _i, [_vp] * 8 + [_i] * 7 + [_vp]),
     ("gdn_fwd_ex", _i, [_vp] * 8 + [_i] * 7 + [ctypes.c_uint, _vp]),
     ("gdn_fwd_varlen_ex", _i, [_vp] * 9 + [_i] * 7 + [ctypes.c_uint, _vp]),
+    ("gdn_bwd", _i, [_vp] * 14 + [_i] * 7 + [ctypes.c_uint, _vp]),
+    ("gdn_bwd_varlen", _i, [_vp] * 15 + [_i] * 7 + [ctypes.c_uint, _vp]),
     ("gdn_status_string", ctypes.c_char_p, [_i]),
     ("gdn_sync_check", _i, [_vp]),
     ("gdn_set_option", _i, [_i, ctypes.c_longlong]),
@@ -194,6 +197,75 @@ def gdn_fwd_varlen(q, k, v, log_alpha, beta, cu_seqlens, h0=None, *, chunk=CHUNK
         if check:
             _check(lib.gdn_sync_check(_stream(q.device)), "gdn_fwd_varlen (device)")
     return o, hT
+
+
+def _bwd_common(q, k, v, log_alpha, beta, h0, dout, dhT, n_states, dv_shape):
+    _prep_io(q, k, v, log_alpha, beta, h0)
+    if not isinstance(dout, torch.Tensor) or not dout.is_cuda or not dout.is_contiguous() \
+            or dout.dtype != q.dtype or dout.shape != dv_shape:
+        raise ValueError("dout must be a contiguous CUDA tensor shaped and typed like o")
+    dk, dv = q.shape[-1], v.shape[-1]
+    if dhT is not None and (dhT.dtype != torch.float32 or not dhT.is_contiguous()
+                            or not dhT.is_cuda or dhT.shape != (*n_states, dv, dk)):
+        raise ValueError("dhT must be a contiguous fp32 CUDA tensor shaped like hT")
+    if log_alpha.shape != beta.shape:
+        raise ValueError("vector gates have no backward pass")
+    return (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v),
+            torch.empty_like(log_alpha), torch.empty_like(beta),
+            torch.empty((*n_states, dv, dk), dtype=torch.float32, device=q.device))
+
+
+def gdn_bwd(q, k, v, log_alpha, beta, h0, dout, dhT=None, *, chunk=CHUNK, erase=True,
+            check=False):
+    """Dense backward pass: the gradient of sum(dout * o) + sum(dhT * hT) for
+    the forward gdn_fwd(q, k, v, log_alpha, beta, h0, erase=erase).  Returns
+    (dq, dk, dv, dlog_alpha, dbeta, dh0); dh0 [B,H,d_v,d_k] is the gradient
+    at the zero state when h0 is None."""
+    lib = load()
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    if k.shape != q.shape or v.shape[:3] != (B, H, T) or log_alpha.shape != (B, H, T) \
+            or beta.shape != (B, H, T):
+        raise ValueError("shape mismatch")
+    if h0 is not None and h0.shape != (B, H, dv, dk):
+        raise ValueError("h0 must be [B,H,d_v,d_k]")
+    g = _bwd_common(q, k, v, log_alpha, beta, h0, dout, dhT, (B, H), (B, H, T, dv))
+    with torch.cuda.device(q.device):
+        rc = lib.gdn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(h0),
+                         _ptr(dout), _ptr(dhT), *(_ptr(t) for t in g), B, H, T, dk, dv, chunk,
+                         _DT[q.dtype], 0 if erase else GDN_FLAG_NO_ERASE, _stream(q.device))
+        _check(rc, "gdn_bwd")
+        if check:
+            _check(lib.gdn_sync_check(_stream(q.device)), "gdn_bwd (device)")
+    return g
+
+
+def gdn_bwd_varlen(q, k, v, log_alpha, beta, cu_seqlens, h0, dout, dhT=None, *, chunk=CHUNK,
+                   erase=True, check=False):
+    """Packed backward pass (layouts as gdn_fwd_varlen).  Returns
+    (dq, dk, dv, dlog_alpha, dbeta, dh0 [N,H,d_v,d_k])."""
+    lib = load()
+    H, TT, dk = q.shape
+    dv = v.shape[-1]
+    if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda or cu_seqlens.dim() != 1:
+        raise ValueError("cu_seqlens must be a 1-D int32 CUDA tensor")
+    N = cu_seqlens.shape[0] - 1
+    if k.shape != q.shape or v.shape[:2] != (H, TT) or log_alpha.shape != (H, TT) \
+            or beta.shape != (H, TT):
+        raise ValueError("shape mismatch")
+    if h0 is not None and h0.shape != (N, H, dv, dk):
+        raise ValueError("h0 must be [N,H,d_v,d_k]")
+    g = _bwd_common(q, k, v, log_alpha, beta, h0, dout, dhT, (N, H), (H, TT, dv))
+    with torch.cuda.device(q.device):
+        rc = lib.gdn_bwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
+                                _ptr(h0), _ptr(dout), _ptr(dhT), *(_ptr(t) for t in g),
+                                _ptr(cu_seqlens.contiguous()), N, H, TT, dk, dv, chunk,
+                                _DT[q.dtype], 0 if erase else GDN_FLAG_NO_ERASE,
+                                _stream(q.device))
+        _check(rc, "gdn_bwd_varlen")
+        if check:
+            _check(lib.gdn_sync_check(_stream(q.device)), "gdn_bwd_varlen (device)")
+    return g
 
 
 def gdn_fwd_noalloc(q, k, v, log_alpha, beta, h0=None, *, chunk=CHUNK, out=None,

@@ -251,6 +251,87 @@ gdn_status gdn_fwd_noalloc(const void *q, const void *k, const void *v, const fl
     return simt_forward_noalloc(a);
 }
 
+namespace {
+gdn_status check_bwd(const void *dout, const float *dhT, const void *dq, const void *dk,
+                     const void *dv, const float *dla, const float *dbeta, const float *dh0,
+                     bool tokens, unsigned flags) {
+    if (flags & ~(unsigned)(GDN_FLAG_NO_ERASE | GDN_FLAG_VECTOR_GATE)) return GDN_ERR_INVALID_ARG;
+    if (flags & GDN_FLAG_VECTOR_GATE) return GDN_ERR_UNSUPPORTED;
+    if (g_opt_impl.load() == GDN_IMPL_TC) return GDN_ERR_UNSUPPORTED;
+    if (tokens && (!dout || !dq || !dk || !dv || !dla || !dbeta)) return GDN_ERR_INVALID_ARG;
+    const void *ptrs[] = {dout, dhT, dq, dk, dv, dla, dbeta, dh0};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return GDN_ERR_ALIGNMENT;
+    return GDN_OK;
+}
+
+gdn_status run_bwd(FwdArgs &a, const void *dout, const float *dhT, void *dq, void *dk, void *dv,
+                   float *dla, float *dbeta, float *dh0) {
+    BwdArgs b{};
+    b.dout = dout; b.dhT = dhT; b.dq = dq; b.dk = dk; b.dv = dv;
+    b.dlog_alpha = dla; b.dbeta = dbeta; b.dh0 = dh0;
+    const gdn_status rc = simt_backward(a, b);
+    if (rc == GDN_OK) g_last_impl.store(GDN_IMPL_SIMT);
+    return rc;
+}
+}  // namespace
+
+gdn_status gdn_bwd(const void *q, const void *k, const void *v, const float *log_alpha,
+                   const float *beta, const float *h0, const void *dout, const float *dhT,
+                   void *dq, void *dk, void *dv, float *dlog_alpha, float *dbeta, float *dh0,
+                   int B, int H, int T, int d_k, int d_v, int chunk, gdn_dtype dt,
+                   unsigned flags, void *stream) {
+    if (B < 0 || T < 0) return GDN_ERR_INVALID_ARG;
+    const bool tokens = (long long)B * H * T > 0;
+    gdn_status rc = check_common(q, k, v, log_alpha, beta, h0, dout, dhT, H, d_k, d_v, chunk,
+                                 dt, tokens);
+    if (rc == GDN_OK)
+        rc = check_bwd(dout, dhT, dq, dk, dv, dlog_alpha, dbeta, dh0, tokens, flags);
+    if (rc != GDN_OK) return rc;
+    if ((long long)B * H == 0) return GDN_OK;
+    FwdArgs a{};
+    a.q = q; a.k = k; a.v = v; a.log_alpha = log_alpha; a.beta = beta; a.h0 = h0;
+    a.sm = SeqMap{nullptr, B, H, T, 0};
+    a.dk = d_k; a.dv = d_v; a.dt = dt;
+    a.rows = (long long)B * H * T;
+    a.max_chunks = (T + kChunk - 1) / kChunk;
+    if ((long long)B * a.max_chunks > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
+    a.chunk_slots = (int)((long long)B * a.max_chunks);
+    a.stream = static_cast<cudaStream_t>(stream);
+    a.no_erase = (flags & GDN_FLAG_NO_ERASE) != 0;
+    return run_bwd(a, dout, dhT, dq, dk, dv, dlog_alpha, dbeta, dh0);
+}
+
+gdn_status gdn_bwd_varlen(const void *q, const void *k, const void *v, const float *log_alpha,
+                          const float *beta, const float *h0, const void *dout,
+                          const float *dhT, void *dq, void *dk, void *dv, float *dlog_alpha,
+                          float *dbeta, float *dh0, const int32_t *cu_seqlens, int N, int H,
+                          int T_total, int d_k, int d_v, int chunk, gdn_dtype dt,
+                          unsigned flags, void *stream) {
+    if (N < 0 || T_total < 0) return GDN_ERR_INVALID_ARG;
+    if (N > 0 && !cu_seqlens) return GDN_ERR_INVALID_ARG;
+    if (N == 0 && T_total != 0) return GDN_ERR_INVALID_ARG;
+    const bool tokens = (long long)H * T_total > 0;
+    gdn_status rc = check_common(q, k, v, log_alpha, beta, h0, dout, dhT, H, d_k, d_v, chunk,
+                                 dt, tokens);
+    if (rc == GDN_OK)
+        rc = check_bwd(dout, dhT, dq, dk, dv, dlog_alpha, dbeta, dh0, tokens, flags);
+    if (rc != GDN_OK) return rc;
+    if ((long long)N * H == 0) return GDN_OK;
+    FwdArgs a{};
+    a.q = q; a.k = k; a.v = v; a.log_alpha = log_alpha; a.beta = beta; a.h0 = h0;
+    a.sm = SeqMap{cu_seqlens, N, H, 0, T_total};
+    a.dk = d_k; a.dv = d_v; a.dt = dt;
+    a.rows = (long long)H * T_total;
+    a.max_chunks = (T_total + kChunk - 1) / kChunk;
+    const long long slots = (long long)T_total / kChunk + N;
+    if (slots > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
+    a.chunk_slots = (int)slots;
+    a.stream = static_cast<cudaStream_t>(stream);
+    a.no_erase = (flags & GDN_FLAG_NO_ERASE) != 0;
+    return run_bwd(a, dout, dhT, dq, dk, dv, dlog_alpha, dbeta, dh0);
+}
+
 const char *gdn_status_string(gdn_status s) {
     switch (s) {
         case GDN_OK: return "GDN_OK";

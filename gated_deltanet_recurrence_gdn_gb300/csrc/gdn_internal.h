@@ -53,6 +53,24 @@ struct FwdArgs {
     cudaStream_t stream;
     bool no_erase;        // gated linear attention: A = 0, T = I, W = 0
     bool vector_gate;     // log_alpha [rows][d_k]: a gate per key dimension
+
+    // Index of chunk c of sequence n among the chunk_slots per head: dense
+    // batches n * max_chunks + c; packed ones floor(cu[n] / 64) + n + c, which
+    // is unique because sequence n has at most (cu[n+1] - cu[n] + 63) / 64
+    // chunks and floor(cu[n] / 64) + ceil(len / 64) <= floor(cu[n+1] / 64) + 1.
+    __device__ __forceinline__ long long chunk_slot(int n, int c) const {
+        if (sm.cu) return (long long)(__ldg(sm.cu + n) / kChunk) + n + c;
+        return (long long)n * max_chunks + c;
+    }
+};
+
+// Gradient pointers of a backward pass (the forward arguments say the rest).
+struct BwdArgs {
+    const void *dout;     // dO [rows][d_v], I/O dtype
+    const float *dhT;     // [seq][H][d_v][d_k] or nullptr (zero)
+    void *dq, *dk, *dv;   // [rows][d], I/O dtype
+    float *dlog_alpha, *dbeta;  // [rows]
+    float *dh0;           // [seq][H][d_v][d_k] or nullptr (not written)
 };
 
 // Stream-ordered scratch from the library's per-device pool, which keeps
@@ -70,6 +88,21 @@ long long option(int key);
 
 // SIMT (CUDA-core, fp32 arithmetic) path: every supported shape and dtype.
 gdn_status simt_forward(const FwdArgs &a);
+
+// Pieces of that path the backward pass reuses.  Prep: W [rows][d_k], U
+// [rows][d_v], gate cumsum G [rows] (table: packed batches only).  State
+// pass: with Hst non-null it also stores each chunk's starting state
+// H = S^T as [H][chunk_slots][d_k][d_v] and with Vn non-null the rows of
+// V' = U - W H as [rows][d_v]; with a.o null it writes no output.
+size_t simt_prep_smem(const FwdArgs &a);
+size_t simt_state_smem(const FwdArgs &a);
+gdn_status enqueue_simt_prep(const FwdArgs &a, const int2 *table, float *W, float *U, float *G);
+gdn_status enqueue_simt_state(const FwdArgs &a, const float *W, const float *U, const float *G,
+                              float *Hst, float *Vn);
+
+// Backward pass of the scalar-gate recurrence (with or without the erase
+// term) on CUDA cores, fp32 arithmetic; defined in gdn_bwd.cu.
+gdn_status simt_backward(const FwdArgs &a, const BwdArgs &b);
 
 // The same path on a dense batch with its scratch in a fixed device array of
 // kNoallocScratchBytes (needs rows * (d_k + d_v + 1) * 4 bytes); no allocation.

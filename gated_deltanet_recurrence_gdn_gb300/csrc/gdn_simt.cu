@@ -230,7 +230,8 @@ k_simt_prep(FwdArgs a, const int2 *__restrict__ table, float *__restrict__ W,
 template <typename TIn>
 __global__ void __launch_bounds__(kThreads)
 k_simt_state(FwdArgs a, const float *__restrict__ W, const float *__restrict__ U,
-             const float *__restrict__ G, int *err) {
+             const float *__restrict__ G, float *__restrict__ Hst, float *__restrict__ Vout,
+             int *err) {
     extern __shared__ float smem[];
     const int dk = a.dk, dv = a.dv, tid = threadIdx.x;
     const int n = blockIdx.x, h = blockIdx.y, dv0 = blockIdx.z * kDvt;
@@ -268,6 +269,13 @@ k_simt_state(FwdArgs a, const float *__restrict__ W, const float *__restrict__ U
         const int t0 = c * kChunk, L = min(kChunk, len - t0);
         const long long r0 = row0 + t0;
         __syncthreads();  // previous chunk fully consumed
+        if (Hst) {   // the chunk's starting state, [d_k][d_v] per chunk slot
+            float *dst = Hst + ((long long)h * a.chunk_slots + a.chunk_slot(n, c)) * dk * dv;
+            for (int i = tid; i < dk * kDvt; i += kThreads) {
+                const int j = i / kDvt, cc = i - j * kDvt;
+                if (cc < nv) dst[(long long)j * dv + dv0 + cc] = Hs[i];
+            }
+        }
         for (int i = tid; i < kChunk * dk; i += kThreads) {
             const int r = i / dk, j = i - r * dk;
             const bool ok = r < L;
@@ -312,11 +320,12 @@ k_simt_state(FwdArgs a, const float *__restrict__ W, const float *__restrict__ U
             float acc = Us[r * us + cc];
             for (int j = 0; j < dk; ++j) acc = fmaf(-Ws[r * ks + j], Hs[j * kDvt + cc], acc);
             Vn[r * us + cc] = acc;
+            if (Vout && r < L && cc < nv) Vout[(r0 + r) * dv + dv0 + cc] = acc;
         }
         __syncthreads();
         for (int i = tid; i < kChunk * kDvt; i += kThreads) {
             const int r = i / kDvt, cc = i - r * kDvt;
-            if (r < L && cc < nv) {
+            if (op && r < L && cc < nv) {
                 float a1 = 0.f, a2 = 0.f;
                 if (vg)   // (Q * gamma) H with gamma per key dimension
                     for (int j = 0; j < dk; ++j)
@@ -406,7 +415,7 @@ gdn_status launch(const FwdArgs &a) {
     if (rc == GDN_OK && a.sm.N > 0 && a.sm.H > 0) {
         dim3 grid(a.sm.N, a.sm.H, (a.dv + kDvt - 1) / kDvt);
         const int slot = timer_begin(st, "k_simt_state");
-        k_simt_state<TIn><<<grid, kThreads, ssm, st>>>(a, W, U, G, err);
+        k_simt_state<TIn><<<grid, kThreads, ssm, st>>>(a, W, U, G, nullptr, nullptr, err);
         timer_end(slot, st);
         count_launch();
     }
@@ -422,6 +431,49 @@ gdn_status launch(const FwdArgs &a) {
 
 gdn_status simt_forward(const FwdArgs &a) {
     return a.dt == GDN_F32 ? launch<float>(a) : launch<__nv_bfloat16>(a);
+}
+
+size_t simt_prep_smem(const FwdArgs &a) { return prep_smem(a.dk, a.dv, a.vector_gate); }
+size_t simt_state_smem(const FwdArgs &a) { return state_smem(a.dk, a.vector_gate); }
+
+template <typename TIn>
+gdn_status enqueue_prep_t(const FwdArgs &a, const int2 *table, float *W, float *U, float *G) {
+    const size_t psm = prep_smem(a.dk, a.dv, a.vector_gate);
+    if (cudaFuncSetAttribute(k_simt_prep<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)psm) != cudaSuccess)
+        return GDN_ERR_CUDA;
+    if (a.chunk_slots > 0 && a.sm.H > 0) {
+        k_simt_prep<TIn><<<dim3(a.chunk_slots, a.sm.H), kThreads, psm, a.stream>>>(
+            a, table, W, U, G, device_error_word());
+        count_launch();
+    }
+    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+template <typename TIn>
+gdn_status enqueue_state_t(const FwdArgs &a, const float *W, const float *U, const float *G,
+                           float *Hst, float *Vn) {
+    const size_t ssm = state_smem(a.dk, a.vector_gate);
+    if (cudaFuncSetAttribute(k_simt_state<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)ssm) != cudaSuccess)
+        return GDN_ERR_CUDA;
+    if (a.sm.N > 0 && a.sm.H > 0) {
+        k_simt_state<TIn><<<dim3(a.sm.N, a.sm.H, (a.dv + kDvt - 1) / kDvt), kThreads, ssm,
+                            a.stream>>>(a, W, U, G, Hst, Vn, device_error_word());
+        count_launch();
+    }
+    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+gdn_status enqueue_simt_prep(const FwdArgs &a, const int2 *table, float *W, float *U, float *G) {
+    return a.dt == GDN_F32 ? enqueue_prep_t<float>(a, table, W, U, G)
+                           : enqueue_prep_t<__nv_bfloat16>(a, table, W, U, G);
+}
+
+gdn_status enqueue_simt_state(const FwdArgs &a, const float *W, const float *U, const float *G,
+                              float *Hst, float *Vn) {
+    return a.dt == GDN_F32 ? enqueue_state_t<float>(a, W, U, G, Hst, Vn)
+                           : enqueue_state_t<__nv_bfloat16>(a, W, U, G, Hst, Vn);
 }
 
 gdn_status enqueue_chunk_table(const FwdArgs &a, int2 *table) {
@@ -491,7 +543,7 @@ gdn_status launch_noalloc(const FwdArgs &a, float *scratch) {
         count_launch();
     }
     dim3 grid(a.sm.N, a.sm.H, (a.dv + kDvt - 1) / kDvt);
-    k_simt_state<TIn><<<grid, kThreads, ssm, st>>>(a, W, U, G, err);
+    k_simt_state<TIn><<<grid, kThreads, ssm, st>>>(a, W, U, G, nullptr, nullptr, err);
     count_launch();
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }

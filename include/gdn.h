@@ -205,6 +205,50 @@ gdn_status gdn_fwd_varlen_ex(const void *q, const void *k, const void *v,
                              gdn_dtype dt, unsigned flags, void *stream);
 
 /*
+ * Backward pass: the gradient of
+ *     L = sum_t dO_t . o_t + sum <dhT, hT>
+ * with respect to q, k, v, log_alpha, beta and h0, for the forward pass
+ * gdn_fwd_ex computes with the same inputs and flags.  No page writes the
+ * delta rule's gradient out; the one on linear-attention training
+ * ("企业官网建设流程全解析", sections 2 and 4.3) recomputes the recurrent state
+ * in the backward pass rather than storing it, and so does this call: it
+ * reruns the chunked forward (without writing o), carries the adjoint of the
+ * state backwards chunk by chunk, then forms every chunk's gradients in
+ * parallel.  CUDA cores, fp32 arithmetic.
+ *   q, k, v, log_alpha, beta, h0, B, H, T, d_k, d_v, chunk, dt: as gdn_fwd.
+ *   dout   [B][H][T][d_v] dtype dt: the weights dO of the outputs.
+ *   dhT    [B][H][d_v][d_k] fp32, or NULL for zero weight on the final state.
+ *   dq, dk [B][H][T][d_k] and dv [B][H][T][d_v], dtype dt (outputs).
+ *   dlog_alpha, dbeta [B][H][T] fp32 (outputs).
+ *   dh0    [B][H][d_v][d_k] fp32 (output; the gradient at the zero state when
+ *          h0 is NULL), or NULL to skip it.
+ *   flags  GDN_FLAG_NO_ERASE differentiates gated linear attention;
+ *          GDN_FLAG_VECTOR_GATE gives GDN_ERR_UNSUPPORTED (not built).
+ * Device memory, caller-owned; scratch (about 4 (d_k + 3 d_v + 1) bytes
+ * per token-head plus 8 d_k d_v bytes per chunk-head) comes from the
+ * library's pool.  Errors as gdn_fwd; with GDN_IMPL_TC forced the call
+ * returns GDN_ERR_UNSUPPORTED (there is no tensor-core backward).
+ */
+gdn_status gdn_bwd(const void *q, const void *k, const void *v,
+                   const float *log_alpha, const float *beta, const float *h0,
+                   const void *dout, const float *dhT,
+                   void *dq, void *dk, void *dv, float *dlog_alpha, float *dbeta,
+                   float *dh0,
+                   int B, int H, int T, int d_k, int d_v, int chunk,
+                   gdn_dtype dt, unsigned flags, void *stream);
+
+/* Packed backward pass: layouts as gdn_fwd_varlen ([H][T_total][d] tokens,
+ * [H][T_total] gates, [N][H][d_v][d_k] states), otherwise as gdn_bwd. */
+gdn_status gdn_bwd_varlen(const void *q, const void *k, const void *v,
+                          const float *log_alpha, const float *beta, const float *h0,
+                          const void *dout, const float *dhT,
+                          void *dq, void *dk, void *dv, float *dlog_alpha,
+                          float *dbeta, float *dh0,
+                          const int32_t *cu_seqlens, int N, int H, int T_total,
+                          int d_k, int d_v, int chunk, gdn_dtype dt,
+                          unsigned flags, void *stream);
+
+/*
  * Dense forward pass on HOST buffers (no paper counterpart: the same
  * computation as gdn_fwd with the host <-> device traffic inside the call).
  * Arguments and layouts as gdn_fwd, but q, k, v, log_alpha, beta, h0 (or

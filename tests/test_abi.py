@@ -98,6 +98,25 @@ def test_host_checks(lib):
     assert gx(*_args(), FAKE, 0, 1, 0, 64, 64, 64, 1, 8, None) == gdn.GDN_ERR_INVALID_ARG
 
 
+def test_bwd_host_checks(lib):
+    f = lib.gdn_bwd
+    a = [FAKE] * 14
+    assert f(*a, 0, 2, 64, 64, 64, 64, 1, 0, None) == gdn.GDN_OK                 # nothing to do
+    assert f(*a, 0, 2, 64, 64, 64, 64, 1, 4, None) == gdn.GDN_ERR_INVALID_ARG    # flag bit
+    assert f(*a, 0, 2, 64, 64, 64, 64, 1, gdn.GDN_FLAG_VECTOR_GATE, None) == \
+        gdn.GDN_ERR_UNSUPPORTED
+    assert f(*a, 1, 1, 64, 64, 64, 128, 1, 0, None) == gdn.GDN_ERR_UNSUPPORTED   # chunk
+    nul = list(a)
+    nul[8] = None                                                                # dq
+    assert f(*nul, 1, 1, 64, 64, 64, 64, 1, 0, None) == gdn.GDN_ERR_INVALID_ARG
+    mis = list(a)
+    mis[11] = FAKE + 4                                                           # dlog_alpha
+    assert f(*mis, 1, 1, 64, 64, 64, 64, 1, 0, None) == gdn.GDN_ERR_ALIGNMENT
+    g = lib.gdn_bwd_varlen
+    assert g(*a, None, 2, 1, 10, 64, 64, 64, 1, 0, None) == gdn.GDN_ERR_INVALID_ARG
+    assert g(*a, FAKE, 0, 1, 0, 64, 64, 64, 1, 0, None) == gdn.GDN_OK
+
+
 def test_decode_host_checks(lib):
     f = lib.gdn_decode
     a = [FAKE] * 6 + [None, 0, FAKE]
