@@ -1,7 +1,7 @@
 """Throughput benchmark of the gated delta rule forward pass on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--no-cpu-baseline]
+                    [--workload NAME] [--no-cpu-baseline] [--no-erase] [--backward]
 
 One step = one gdn_fwd call (every stage of the chunked forward pass) over the
 whole synthetic batch of the workload (default: B=4, H=16, T=4096,
@@ -14,6 +14,10 @@ slowest rank's time is reported.
 
 --impl reference times the fp64 CPU oracle on a bounded sample of the same
 workload on the host cores (rank 0 only).
+
+--no-erase times gated linear attention (the recurrence without the erase
+term); --backward times the backward pass (gdn_bwd: the gradient of
+sum(dO * o) + sum(dhT * hT) for fixed seeded weights dO, dhT) instead.
 """
 from __future__ import annotations
 
@@ -41,7 +45,10 @@ UNIT = "tokens/s"
 DECODE_METRIC = "GDN decode step tokens/s (B·H/s) and % of roofline, bf16, d=128, 1×GB300"
 GLA_METRIC = ("gated linear attention (no erase term) chunked fwd tokens/s (B·H·T/s) and % of "
               "roofline, bf16, d=128, 1×GB300")
+BWD_METRIC = "GDN chunked bwd tokens/s (B·H·T/s) and % of roofline, bf16, d=128, 1×GB300"
 DEFAULT_WORKLOAD = "gdn_fwd_b4_h16_t4096_d128_bf16"
+# fp32 FMA rate of the CUDA cores: 152 SMs x 128 lanes x 2 FLOP x 2.07 GHz
+ALU_FP32_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 L2_FLUSH_BYTES = 256 << 20
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
@@ -55,6 +62,8 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--backward", action="store_true",
+                    help="time the backward pass (gdn_bwd) instead of the forward")
     ap.add_argument("--no-erase", action="store_true",
                     help="gated linear attention: the recurrence without the erase term")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -142,6 +151,29 @@ def algorithmic(shape):
     return by, flops
 
 
+def algorithmic_bwd(shape):
+    """Compulsory HBM bytes of one backward call and the FLOPs its per-chunk
+    gradient kernel issues.
+
+    Bytes: q, k, v, dO read and dq, dk, dv written once at the I/O width, the
+    two gates read and their two gradients written (fp32), h0 and dhT read and
+    dh0 written once per (sequence, head).  FLOPs of k_bwd_chunk per
+    chunk-head (C = 64), as its loops issue them: the three d_v contractions
+    against the chunk states (3 C d_k d_v), the two C x C ones over d_v and
+    T^T dV' (2.5 C^2 d_v), eight C x C x d_k products of the gradient algebra
+    (about 4 C^2 d_k) and the inverse and its adjoint (about C^3 / 2); two
+    FLOPs per multiply-add."""
+    io = 2 if shape["io"] == "bf16" else 4
+    dk, dv, C = shape["dk"], shape["dv"], 64
+    th = shape["tokens"]
+    seqheads = shape["N"] * shape["H"]
+    state = seqheads * dk * dv * 4
+    by = th * ((4 * dk + 3 * dv) * io + 16) + state * (3 if shape["h0"] else 2)
+    chunks = -(-th // C)
+    fma = 3 * C * dk * dv + 2.5 * C * C * dv + 4 * C * C * dk + C ** 3 / 2
+    return by, chunks * fma * 2
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -156,6 +188,7 @@ KERNEL_SOURCES = {
     "k_gdn_tc": ["gdn_tc.cu", "tc_ptx.cuh", "gdn_internal.h"],
     "k_gdn_prep": ["gdn_prep.cu", "tc_ptx.cuh", "gdn_internal.h"],
     "k_gdn_decode": ["gdn_decode.cu", "gdn_internal.h"],
+    "k_bwd_chunk": ["gdn_bwd.cu", "gdn_internal.h"],
 }
 
 
@@ -257,15 +290,42 @@ def is_decode(x):
 
 
 def metric_for(shape):
+    if BACKWARD:
+        return BWD_METRIC
     if NO_ERASE:
         return GLA_METRIC
     return DECODE_METRIC if shape["kind"] == "decode" else METRIC
 
 
 NO_ERASE = False   # set from --no-erase
+BACKWARD = False   # set from --backward
+_BWD_WEIGHTS = {}
+
+
+def bwd_weights(x):
+    """Seeded output weights dO (I/O dtype) and dhT (fp32) of the backward."""
+    key = (x.q.device, tuple(x.v.shape))
+    if key not in _BWD_WEIGHTS:
+        g = torch.Generator(device=x.q.device).manual_seed(1234)
+        n_states = x.h0.shape[:2] if x.h0 is not None else (
+            (x.meta["N"], x.meta["H"]) if x.cu_seqlens is not None else x.q.shape[:2])
+        dout = torch.randn(x.v.shape, generator=g, device=x.q.device).to(x.q.dtype)
+        dhT = torch.randn((*n_states, x.v.shape[-1], x.q.shape[-1]), generator=g,
+                          device=x.q.device)
+        _BWD_WEIGHTS[key] = (dout, dhT)
+    return _BWD_WEIGHTS[key]
 
 
 def call(gdn, x, out=None):
+    if BACKWARD:
+        dout, dhT = bwd_weights(x)
+        if x.cu_seqlens is not None:
+            g = gdn.gdn_bwd_varlen(x.q, x.k, x.v, x.log_alpha, x.beta, x.cu_seqlens, x.h0,
+                                   dout, dhT, erase=not NO_ERASE)
+        else:
+            g = gdn.gdn_bwd(x.q, x.k, x.v, x.log_alpha, x.beta, x.h0, dout, dhT,
+                            erase=not NO_ERASE)
+        return g[0], g[5]
     if NO_ERASE:
         if x.cu_seqlens is not None:
             return gdn.gdn_fwd_varlen(x.q, x.k, x.v, x.log_alpha, x.beta, x.cu_seqlens, x.h0,
@@ -325,6 +385,8 @@ def run_ours(args, world, rank, local):
     # loop's state cache): only the token's inputs go in and o comes back.
     dec = is_decode(x)
     src = {k: t for k, t in x.tensors().items() if not (dec and k == "h0")}
+    if BACKWARD:
+        src["dout"], src["dhT"] = bwd_weights(x)
     host = {k: (None if t is None else t.cpu().pin_memory()) for k, t in src.items()}
     dev_buf = {k: (None if t is None else torch.empty_like(t)) for k, t in src.items()}
     o_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
@@ -333,11 +395,33 @@ def run_ours(args, world, rank, local):
     h_host = None if dec else torch.empty(hT_shape, dtype=torch.float32).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in host.values() if t is not None)
     d2h = o_host.numel() * o_host.element_size() + (0 if dec else h_host.numel() * 4)
+    g_host = None
+    if BACKWARD:
+        like = [x.q, x.k, x.v, x.log_alpha, x.beta]
+        g_host = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in like]
+        g_host.append(torch.empty(hT_shape, dtype=torch.float32).pin_memory())
+        d2h = sum(t.numel() * t.element_size() for t in g_host)
     e2e_steps = max(3, min(args.steps, 10))
 
-    dense = shape["kind"] == "dense" and not NO_ERASE
+    dense = shape["kind"] == "dense" and not NO_ERASE and not BACKWARD
 
     def e2e_step():
+        if BACKWARD:
+            for k_, t in host.items():
+                if t is not None:
+                    dev_buf[k_].copy_(t, non_blocking=True)
+            kw = dict(erase=not NO_ERASE)
+            if x.cu_seqlens is not None:
+                g = gdn.gdn_bwd_varlen(dev_buf["q"], dev_buf["k"], dev_buf["v"],
+                                       dev_buf["log_alpha"], dev_buf["beta"], x.cu_seqlens,
+                                       dev_buf["h0"], dev_buf["dout"], dev_buf["dhT"], **kw)
+            else:
+                g = gdn.gdn_bwd(dev_buf["q"], dev_buf["k"], dev_buf["v"], dev_buf["log_alpha"],
+                                dev_buf["beta"], dev_buf["h0"], dev_buf["dout"], dev_buf["dhT"],
+                                **kw)
+            for hb, t in zip(g_host, g):
+                hb.copy_(t, non_blocking=True)
+            return
         if dense:
             # the library's host-buffer entry point: it uploads, computes and
             # downloads, pipelined over time slices
@@ -367,7 +451,7 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize(dev)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
 
-    by, flops = algorithmic(shape)
+    by, flops = algorithmic_bwd(shape) if BACKWARD else algorithmic(shape)
     hbm, tf, src = load_peaks()
     achieved = by / (kern_ms * 1e-3) / 1e9
     res = {
@@ -406,6 +490,19 @@ def run_ours(args, world, rank, local):
         "impl_used": "decode" if shape["kind"] == "decode" else
                      {1: "simt", 2: "tc"}.get(gdn.last_impl(), "none"),
     }
+    if BACKWARD:
+        # CUDA-core fp32 kernels: the roof of the dominant one is the fp32 FMA rate
+        alu = flops / (kern_ms * 1e-3) / 1e12
+        res["roofline"] = {
+            "bound": "alu", "achieved": alu, "peak": ALU_FP32_TFLOPS, "unit": "TFLOP/s",
+            "frac": alu / ALU_FP32_TFLOPS,
+            "peak_source": "fp32 FMA: 152 SMs x 128 lanes x 2 FLOP x 2.07 GHz (nominal)",
+            "traffic": recorded_traffic(k_name, args.workload),
+            "kernel": k_name, "kernel_ms": kern_ms, "algorithmic_flops": flops,
+            "algorithmic_bytes": by,
+            "step_hbm_frac": by / (step_ms * 1e-3) / 1e9 / hbm,
+        }
+        res["config"]["pass"] = "backward (state recomputed)"
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(args.workload, x, args.cpu_seconds)
     elif rank == 0 and world == 1:
@@ -432,6 +529,18 @@ def oracle_sample(name, x, budget_s, max_heads=None):
             t0 = time.perf_counter()
             oracle.gdn_fwd(*args, f64(x.h0[b, h])[None, None])
             return 1, time.perf_counter() - t0
+    elif BACKWARD and x.cu_seqlens is None:
+        dout, dhT = (t.cpu() for t in bwd_weights(x))
+        units = [(b, h) for b in range(x.q.shape[0]) for h in range(x.q.shape[1])]
+
+        def one(u):
+            b, h = u
+            args = [f64(t[b, h])[None, None] for t in (x.q, x.k, x.v, x.log_alpha, x.beta)]
+            h0 = None if x.h0 is None else f64(x.h0[b, h])[None, None]
+            t0 = time.perf_counter()
+            oracle.gdn_bwd(*args, h0, f64(dout[b, h])[None, None], f64(dhT[b, h])[None, None],
+                           erase=not NO_ERASE)
+            return x.q.shape[2], time.perf_counter() - t0
     elif x.cu_seqlens is not None:
         cu = x.cu_seqlens.cpu().numpy()
         units = [(n, h) for n in range(len(cu) - 1) for h in range(x.q.shape[0])]
@@ -443,7 +552,12 @@ def oracle_sample(name, x, budget_s, max_heads=None):
             args = [f64(t[s])[None, None] for t in (x.q, x.k, x.v, x.log_alpha, x.beta)]
             h0 = None if x.h0 is None else f64(x.h0[n, h])[None, None]
             t0 = time.perf_counter()
-            oracle.gdn_fwd(*args, h0, erase=not NO_ERASE)
+            if BACKWARD:
+                dout, dhT = (t.cpu() for t in bwd_weights(x))
+                oracle.gdn_bwd(*args, h0, f64(dout[s])[None, None], f64(dhT[n, h])[None, None],
+                               erase=not NO_ERASE)
+            else:
+                oracle.gdn_fwd(*args, h0, erase=not NO_ERASE)
             return b - a, time.perf_counter() - t0
     else:
         units = [(b, h) for b in range(x.q.shape[0]) for h in range(x.q.shape[1])]
@@ -507,9 +621,12 @@ def run_reference(args, world, rank):
 
 
 def main():
-    global NO_ERASE
+    global NO_ERASE, BACKWARD
     args = parse()
     NO_ERASE = args.no_erase
+    BACKWARD = args.backward
+    if BACKWARD and synth.WORKLOADS[args.workload].get("kind") == "decode":
+        raise SystemExit("--backward needs a chunked workload")
     world, rank, local = dist_setup(args.gpus)
     if args.impl == "reference":
         res = run_reference(args, world, rank)
