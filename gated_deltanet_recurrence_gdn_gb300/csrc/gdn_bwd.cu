@@ -36,14 +36,17 @@
 // Without the erase term A = 0, T = I and W = 0, and the A and W terms drop.
 #include <cuda_bf16.h>
 
+#include <type_traits>
+
 #include "gdn_internal.h"
+#include "gdn_mma.cuh"
+#include "gdn_tile.cuh"
 
 namespace gdn {
 namespace {
 
 constexpr int kThreads = 256;
 constexpr int kDvt = 32;     // d_v columns per tile
-constexpr int kRegJ = 32;    // key columns a thread owns in k_bwd_chunk (d_k <= 128)
 
 __device__ __forceinline__ float ld_in(const float *p) { return __ldg(p); }
 __device__ __forceinline__ float ld_in(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
@@ -59,24 +62,33 @@ __device__ __forceinline__ bool seq_ok(const SeqMap &sm, int n) {
 
 // ---------------------------------------------------------------- dS pass
 //
-// One CTA per (sequence, head, 32-wide d_v tile), chunks in reverse order.
-// dH = dS^T (d_k x 32) lives in shared memory.  For each chunk it stores
+// One CTA per (sequence, head, 64-wide d_v tile), chunks in reverse order.
+// dH = dS^T (d_k x 64) lives in shared memory.  For each chunk it stores
 // dH (the adjoint of the chunk's end state) as [H][chunk_slots][d_k][d_v]
-// and the rows of dV', then steps dH back to the chunk's start.
+// and the rows of dV', then steps dH back to the chunk's start.  The products
+// run on the tensor cores (mma.sync tf32, gdn_mma.cuh); the next (earlier)
+// chunk's K, Q, W and dO are loaded into registers while the current one is
+// computed.
+
+constexpr int kDvm = 64;           // d_v columns per dS-pass CTA
+constexpr int kLdh = kDvm + 8;     // d_k x 64 state tiles: transposed reads conflict-free
+constexpr int kLdc = kChunk + 4;   // 64 x 64 tiles
+constexpr int kLdt = kDvt + 4;     // 64 x 32 tiles (chunk kernel)
 
 size_t dstate_smem(int dk) {
-    return sizeof(float) * ((size_t)dk * kDvt + 3 * (size_t)kChunk * (dk + 1) +
-                            2 * kChunk * (kDvt + 1) + kChunk * 65 + 3 * kChunk);
+    return sizeof(float) * ((size_t)dk * kLdh + 3 * (size_t)kChunk * (dk + 4) +
+                            3 * kChunk * kLdc + 3 * kChunk);
 }
 
-template <typename TIn>
-__global__ void __launch_bounds__(kThreads)
+template <typename TIn, bool SPLIT>
+__global__ void __launch_bounds__(kThreads, 1)
 k_bwd_dstate(FwdArgs a, BwdArgs b, const float *__restrict__ W, const float *__restrict__ G,
              float *__restrict__ dVn, float *__restrict__ dHc, int *err) {
     extern __shared__ float smem[];
     const int dk = a.dk, dv = a.dv, tid = threadIdx.x;
-    const int n = blockIdx.x, h = blockIdx.y, dv0 = blockIdx.z * kDvt;
-    const int nv = min(kDvt, dv - dv0);
+    const int lane = tid & 31, warp = tid >> 5;
+    const int n = blockIdx.x, h = blockIdx.y, dv0 = blockIdx.z * kDvm;
+    const int nv = min(kDvm, dv - dv0);
     if (!seq_ok(a.sm, n)) {
         if (tid == 0) set_error(err, kErrBadIndex);
         return;
@@ -84,131 +96,210 @@ k_bwd_dstate(FwdArgs a, BwdArgs b, const float *__restrict__ W, const float *__r
     long long row0;
     int len;
     a.sm.get(n, h, row0, len);
-    const int ks = dk + 1, us = kDvt + 1;
-    float *dH = smem;                    // [dk][32]
-    float *Ks = dH + dk * kDvt;          // [64][dk+1]
-    float *Qs = Ks + kChunk * ks;        // [64][dk+1]
-    float *Ws = Qs + kChunk * ks;        // [64][dk+1]
-    float *dOs = Ws + kChunk * ks;       // [64][33]
-    float *dVs = dOs + kChunk * us;      // [64][33]
-    float *P = dVs + kChunk * us;        // [64][65]  P_rs = G_rs q_r . k_s, s <= r
-    float *g = P + kChunk * 65;          // [64]
+    const int ldk = dk + 4;
+    float *dH = smem;                    // [dk][72]
+    float *Ks = dH + dk * kLdh;          // [64][dk+4]
+    float *Qs = Ks + kChunk * ldk;       // [64][dk+4]
+    float *Ws = Qs + kChunk * ldk;       // [64][dk+4]
+    float *dOs = Ws + kChunk * ldk;      // [64][68]
+    float *dVs = dOs + kChunk * kLdc;    // [64][68]
+    float *P = dVs + kChunk * kLdc;      // [64][68]  P_rs = G_rs q_r . k_s, s <= r
+    float *g = P + kChunk * kLdc;        // [64]
     float *e = g + kChunk;               // [64] exp(g_C - g_r)
     float *gm = e + kChunk;              // [64] exp(g_r)
     const TIn *qp = static_cast<const TIn *>(a.q);
     const TIn *kp = static_cast<const TIn *>(a.k);
     const TIn *dop = static_cast<const TIn *>(b.dout);
     const long long sbase = ((long long)n * a.sm.H + h) * dv;
+    const int m0 = 16 * (warp >> 1), nh = warp & 1;
+    const int ntask = 2 * ((dk + 15) / 16);   // (16-row block, column half) tasks of d_k x 64
 
-    for (int i = tid; i < dk * kDvt; i += kThreads) {
-        const int j = i / kDvt, cc = i - j * kDvt;
-        dH[i] = (b.dhT && cc < nv) ? __ldg(b.dhT + (sbase + dv0 + cc) * dk + j) : 0.f;
+    for (int i = tid; i < dk * kDvm; i += kThreads) {
+        const int j = i / kDvm, cc = i - j * kDvm;
+        dH[j * kLdh + cc] = (b.dhT && cc < nv) ? __ldg(b.dhT + (sbase + dv0 + cc) * dk + j) : 0.f;
     }
+    TileRegs<4> rk, rq, rw;
+    TileRegs<2> ro;
+    float gnext = 0.f;
+    auto issue = [&](int c) {
+        const int L = min(kChunk, len - c * kChunk);
+        const long long r0 = row0 + (long long)c * kChunk;
+        rk.load(kp + r0 * dk, dk, dk, L, dk, tid);
+        rq.load(qp + r0 * dk, dk, dk, L, dk, tid);
+        rw.load(W + r0 * dk, dk, dk, L, dk, tid);
+        ro.load(dop + r0 * dv + dv0, dv, kDvm, L, nv, tid);
+        if (tid < kChunk) gnext = __ldg(G + r0 + min(tid, L - 1));
+    };
     const int nch = (len + kChunk - 1) / kChunk;
+    if (nch > 0) issue(nch - 1);
     for (int c = nch - 1; c >= 0; --c) {
         const int t0 = c * kChunk, L = min(kChunk, len - t0);
         const long long r0 = row0 + t0;
         __syncthreads();  // the previous (later) chunk is fully consumed
         float *dst = dHc + ((long long)h * a.chunk_slots + a.chunk_slot(n, c)) * dk * dv;
-        for (int i = tid; i < dk * kDvt; i += kThreads) {
-            const int j = i / kDvt, cc = i - j * kDvt;
-            if (cc < nv) dst[(long long)j * dv + dv0 + cc] = dH[i];
+        for (int i = tid; i < dk * kDvm; i += kThreads) {
+            const int j = i / kDvm, cc = i - j * kDvm;
+            if (cc < nv) dst[(long long)j * dv + dv0 + cc] = dH[j * kLdh + cc];
         }
-        for (int i = tid; i < kChunk * dk; i += kThreads) {
-            const int r = i / dk, j = i - r * dk;
-            const bool ok = r < L;
-            Ks[r * ks + j] = ok ? ld_in(kp + (r0 + r) * dk + j) : 0.f;
-            Qs[r * ks + j] = ok ? ld_in(qp + (r0 + r) * dk + j) : 0.f;
-            Ws[r * ks + j] = ok ? __ldg(W + (r0 + r) * dk + j) : 0.f;
-        }
-        for (int i = tid; i < kChunk * kDvt; i += kThreads) {
-            const int r = i / kDvt, cc = i - r * kDvt;
-            dOs[r * us + cc] = (r < L && cc < nv) ? ld_in(dop + (r0 + r) * dv + dv0 + cc) : 0.f;
-        }
-        if (tid < kChunk) g[tid] = __ldg(G + r0 + min(tid, L - 1));
+        rk.store(Ks, ldk, dk, tid);
+        rq.store(Qs, ldk, dk, tid);
+        rw.store(Ws, ldk, dk, tid);
+        ro.store(dOs, kLdc, kDvm, tid);
+        if (tid < kChunk) g[tid] = gnext;
+        if (c > 0) issue(c - 1);
         __syncthreads();
         const float gl = g[kChunk - 1];
         if (tid < kChunk) {
             e[tid] = expf(gl - g[tid]);
             gm[tid] = expf(g[tid]);
         }
-        for (int i = tid; i < kChunk * kChunk; i += kThreads) {
-            const int r = i >> 6, s = i & 63;
-            float val = 0.f;
-            if (s <= r) {
-                float acc = 0.f;
-                for (int j = 0; j < dk; ++j) acc = fmaf(Qs[r * ks + j], Ks[s * ks + j], acc);
-                val = expf(g[r] - g[s]) * acc;
-            }
-            P[r * 65 + s] = val;
+        {
+            float acc[4][4];
+            mma::zero(acc);
+            mma::warp_gemm<4, SPLIT>(
+                acc, [&](int m, int k) { return Qs[m * ldk + k]; },
+                [&](int k, int nn) { return Ks[nn * ldk + k]; }, m0, nh, 2, kChunk, dk, lane);
+            mma::for_each(acc, m0, nh, 2, kChunk, lane, [&](int r, int s, float &x) {
+                P[r * kLdc + s] = s <= r ? expf(g[r] - g[s]) * x : 0.f;
+            });
         }
         __syncthreads();
-        // dV'_r = sum_{s >= r} P_sr dO_s + e_r dS k_r
-        for (int i = tid; i < kChunk * kDvt; i += kThreads) {
-            const int r = i / kDvt, cc = i - r * kDvt;
-            float a1 = 0.f, a2 = 0.f;
-            for (int s = r; s < kChunk; ++s) a1 = fmaf(P[s * 65 + r], dOs[s * us + cc], a1);
-            for (int j = 0; j < dk; ++j) a2 = fmaf(Ks[r * ks + j], dH[j * kDvt + cc], a2);
-            const float val = r < L ? fmaf(e[r], a2, a1) : 0.f;
-            dVs[r * us + cc] = val;
-            if (r < L && cc < nv) dVn[(r0 + r) * dv + dv0 + cc] = val;
+        {   // dV'_r = sum_{s >= r} P_sr dO_s + e_r dS k_r
+            float a1[4][4], a2[4][4];
+            mma::zero(a1);
+            mma::zero(a2);
+            mma::warp_gemm<4, SPLIT>(
+                a1, [&](int m, int k) { return P[k * kLdc + m]; },
+                [&](int k, int nn) { return dOs[k * kLdc + nn]; }, m0, nh, 2, kDvm, kChunk, lane);
+            mma::warp_gemm<4, SPLIT>(
+                a2, [&](int m, int k) { return Ks[m * ldk + k]; },
+                [&](int k, int nn) { return dH[k * kLdh + nn]; }, m0, nh, 2, kDvm, dk, lane);
+            const int gl4 = lane >> 2, tl = lane & 3;
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int r = m0 + gl4 + 8 * (q >> 1), cc = 8 * (nh + 2 * i) + 2 * tl + (q & 1);
+                    const float val = r < L ? fmaf(e[r], a2[i][q], a1[i][q]) : 0.f;
+                    dVs[r * kLdc + cc] = val;
+                    if (r < L && cc < nv) dVn[(r0 + r) * dv + dv0 + cc] = val;
+                }
         }
         __syncthreads();
         // dS <- gamma_C dS + dO^T diag(gamma) Q - dV'^T W   (as dH = dS^T)
         const float decay = expf(gl);
-        for (int i = tid; i < dk * kDvt; i += kThreads) {
-            const int j = i / kDvt, cc = i - j * kDvt;
-            float acc = 0.f;
-            for (int r = 0; r < kChunk; ++r) {
-                acc = fmaf(gm[r] * Qs[r * ks + j], dOs[r * us + cc], acc);
-                acc = fmaf(-Ws[r * ks + j], dVs[r * us + cc], acc);
-            }
-            dH[i] = fmaf(decay, dH[i], acc);
+        for (int task = warp; task < ntask; task += kThreads / 32) {
+            const int j0 = 16 * (task >> 1), th = task & 1;
+            float acc[4][4];
+            mma::zero(acc);
+            mma::warp_gemm<4, SPLIT>(
+                acc, [&](int m, int k) { return m < dk ? Qs[k * ldk + m] * gm[k] : 0.f; },
+                [&](int k, int nn) { return dOs[k * kLdc + nn]; }, j0, th, 2, kDvm, kChunk, lane);
+            mma::warp_gemm<4, SPLIT>(
+                acc, [&](int m, int k) { return m < dk ? -Ws[k * ldk + m] : 0.f; },
+                [&](int k, int nn) { return dVs[k * kLdc + nn]; }, j0, th, 2, kDvm, kChunk, lane);
+            mma::for_each(acc, j0, th, 2, kDvm, lane, [&](int j, int cc, float &x) {
+                if (j < dk) dH[j * kLdh + cc] = fmaf(decay, dH[j * kLdh + cc], x);
+            });
         }
     }
     __syncthreads();
     if (b.dh0) {
-        for (int i = tid; i < dk * kDvt; i += kThreads) {
-            const int j = i / kDvt, cc = i - j * kDvt;
-            if (cc < nv) b.dh0[(sbase + dv0 + cc) * dk + j] = dH[i];
+        for (int i = tid; i < dk * kDvm; i += kThreads) {
+            const int j = i / kDvm, cc = i - j * kDvm;
+            if (cc < nv) b.dh0[(sbase + dv0 + cc) * dk + j] = dH[j * kLdh + cc];
         }
     }
 }
 
 // ------------------------------------------------------------ chunk kernel
 //
-// One CTA per (chunk, head).  Phase 1 rebuilds A and T from K, beta and the
-// gates.  Phase 2 walks d_v in 32-wide tiles and accumulates the d_v
-// contractions: dO S0 and V' dSC in registers (thread (r, j mod 4) owns
-// row r, key columns j = j0 + 4m), dV' S0 in shared memory, dO V'^T and
-// dV' (diag(beta) V)^T as C x C tiles; it also writes dV and collects the
-// U part of dbeta.  Phase 3 forms dQ, dK, dbeta and dlog_alpha.
+// One CTA per (chunk, head), 8 warps; every product runs on the tensor
+// cores through mma.sync tf32 (gdn_mma.cuh; three products per step for fp32
+// I/O, one for bf16 I/O).  Warp w owns rows 16 (w / 2) .. +15 of every
+// 64-row output and the 8-column tiles w % 2, w % 2 + 2, ... of it.
+// Phase 1 rebuilds A and T from K, beta and the gates.  Phase 2 walks d_v in
+// 32-wide tiles: dO S0, V' dSC and dV' S0 (64 x d_k) and dO V'^T,
+// dV' V^T (64 x 64) accumulate in registers; dV = diag(beta) T^T dV' and the
+// U part of dbeta are written per tile.  Phase 3 forms dQ, dK, dbeta and
+// dlog_alpha.
+
+constexpr int kNtK = 8;            // 8-column tiles per warp of a 64 x d_k output (d_k <= 128)
+constexpr int kNtC = 4;            // ... of a 64 x 64 output
+constexpr int kNtV = 2;            // ... of a 64 x 32 output
 
 struct ChunkLay {
-    int ks, region;
+    int ldk, region;
     int oK, oR, oWm, oT, oB1, oB2, oB3, oV;
     size_t bytes;
 };
 
 __host__ __device__ inline ChunkLay chunk_lay(int dk) {
     ChunkLay l;
-    l.ks = dk + 1;
-    const int tiles = 4 * kChunk * (kDvt + 1) + 2 * dk * (kDvt + 1);
-    const int qsz = kChunk * l.ks;
+    l.ldk = dk + 4;
+    const int tiles = 4 * kChunk * kLdt + 2 * dk * kLdt;
+    const int qsz = kChunk * l.ldk;
     l.region = tiles > qsz ? tiles : qsz;
     l.oK = 0;
-    l.oR = l.oK + kChunk * l.ks;
+    l.oR = l.oK + kChunk * l.ldk;
     l.oWm = l.oR + l.region;
-    l.oT = l.oWm + kChunk * l.ks;
-    l.oB1 = l.oT + kChunk * 65;
-    l.oB2 = l.oB1 + kChunk * 65;
-    l.oB3 = l.oB2 + kChunk * 65;
-    l.oV = l.oB3 + kChunk * 65;
+    l.oT = l.oWm + kChunk * l.ldk;
+    l.oB1 = l.oT + kChunk * kLdc;
+    l.oB2 = l.oB1 + kChunk * kLdc;
+    l.oB3 = l.oB2 + kChunk * kLdc;
+    l.oV = l.oB3 + kChunk * kLdc;
     l.bytes = sizeof(float) * ((size_t)l.oV + 12 * kChunk + 32);
     return l;
 }
 
-template <typename TIn>
+// Row sums (over this thread's columns and the four lanes of a row) of an
+// accumulator block, added to v[row] with weight w(row).
+template <int NT, typename F, typename W>
+__device__ __forceinline__ void add_row_sums(float (&acc)[NT][4], int m0, int nt0, int nstep,
+                                             int n_end, int lane, F value, float *v, W w) {
+    float r0 = 0.f, r1 = 0.f;
+    mma::for_each(acc, m0, nt0, nstep, n_end, lane, [&](int m, int n, float &x) {
+        const float y = value(m, n, x);
+        if (((m - m0) >> 3) == 0) r0 += y; else r1 += y;
+    });
+    r0 += __shfl_xor_sync(0xffffffffu, r0, 1);
+    r0 += __shfl_xor_sync(0xffffffffu, r0, 2);
+    r1 += __shfl_xor_sync(0xffffffffu, r1, 1);
+    r1 += __shfl_xor_sync(0xffffffffu, r1, 2);
+    if ((lane & 3) == 0) {
+        const int m = m0 + (lane >> 2);
+        atomicAdd(v + m, w(m) * r0);
+        atomicAdd(v + m + 8, w(m + 8) * r1);
+    }
+}
+
+// Column sums (over the 16 rows of the block) added to v[col] times scale.
+template <int NT, typename F>
+__device__ __forceinline__ void add_col_sums(float (&acc)[NT][4], int m0, int nt0, int nstep,
+                                             int n_end, int lane, F value, float *v,
+                                             float scale) {
+    const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int i = 0; i < NT; ++i) {
+        const int n = 8 * (nt0 + i * nstep);
+        if (n < n_end) {
+            float c0 = value(m0 + g, n + 2 * t, acc[i][0]) + value(m0 + g + 8, n + 2 * t, acc[i][2]);
+            float c1 = value(m0 + g, n + 2 * t + 1, acc[i][1]) +
+                       value(m0 + g + 8, n + 2 * t + 1, acc[i][3]);
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) {
+                c0 += __shfl_xor_sync(0xffffffffu, c0, o);
+                c1 += __shfl_xor_sync(0xffffffffu, c1, o);
+            }
+            if (g == 0) {
+                atomicAdd(v + n + 2 * t, scale * c0);
+                atomicAdd(v + n + 2 * t + 1, scale * c1);
+            }
+        }
+    }
+}
+
+template <typename TIn, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
 k_bwd_chunk(FwdArgs a, BwdArgs b, const int2 *__restrict__ table, const float *__restrict__ Hst,
             const float *__restrict__ dHc, const float *__restrict__ Vn,
@@ -242,14 +333,14 @@ k_bwd_chunk(FwdArgs a, BwdArgs b, const int2 *__restrict__ table, const float *_
     const long long st_off = ((long long)h * a.chunk_slots + a.chunk_slot(n, c)) * dk * dv;
 
     const ChunkLay ly = chunk_lay(dk);
-    const int ks = ly.ks, us = kDvt + 1;
-    float *Ks = smem + ly.oK;     // [64][dk+1]
+    const int ldk = ly.ldk;
+    float *Ks = smem + ly.oK;     // [64][ldk]
     float *Rg = smem + ly.oR;     // phase 2 tiles, then Q
-    float *Wm = smem + ly.oWm;    // [64][dk+1]  dV' S0 (= -dW)
-    float *Tm = smem + ly.oT;     // [64][65]    T
-    float *B1 = smem + ly.oB1;    // [64][65]    dO V'^T, then dP, then dT T^T
-    float *B2 = smem + ly.oB2;    // [64][65]    dV'(diag(beta)V)^T, then dT, then dA
-    float *B3 = smem + ly.oB3;    // [64][65]    A, then dP * (Q K^T), then dA * G * K K^T
+    float *Wm = smem + ly.oWm;    // [64][ldk]  dV' S0 (= -dW)
+    float *Tm = smem + ly.oT;     // [64][68]   T
+    float *B1 = smem + ly.oB1;    // [64][68]   A, then dP, then dT T^T
+    float *B2 = smem + ly.oB2;    // [64][68]   dV' (diag(beta) V)^T, then dT, then X = dA * G
+    float *B3 = smem + ly.oB3;    // [64][68]   K K^T
     float *g = smem + ly.oV;      // [64] gate cumsum
     float *bb = g + kChunk;       // [64] beta
     float *gm = bb + kChunk;      // [64] exp(g)
@@ -263,35 +354,32 @@ k_bwd_chunk(FwdArgs a, BwdArgs b, const int2 *__restrict__ table, const float *_
     float *dbA = dgA + kChunk;    // [64] dbeta from A
     float *dlv = dbA + kChunk;    // [64] dg total
     float *red = dlv + kChunk;    // [32]
-    // phase 2 tiles
-    float *dOs = Rg;                       // [64][33]
-    float *Vns = dOs + kChunk * us;        // [64][33]  V'
-    float *dVs = Vns + kChunk * us;        // [64][33]  dV'
-    float *Vs = dVs + kChunk * us;         // [64][33]  V
-    float *S0t = Vs + kChunk * us;         // [dk][33]  S0^T tile
-    float *dSt = S0t + dk * us;            // [dk][33]  dSC^T tile
-    float *Qs = Rg;                        // phase 3: [64][dk+1]
+    float *dOs = Rg;                       // [64][36]
+    float *Vns = dOs + kChunk * kLdt;      // [64][36]  V'
+    float *dVs = Vns + kChunk * kLdt;      // [64][36]  dV'
+    float *Vs = dVs + kChunk * kLdt;       // [64][36]  V
+    float *S0t = Vs + kChunk * kLdt;       // [dk][36]  S0^T tile
+    float *dSt = S0t + dk * kLdt;          // [dk][36]  dSC^T tile
+    float *Qs = Rg;                        // phase 3: [64][ldk]
 
     const TIn *qp = static_cast<const TIn *>(a.q);
     const TIn *kp = static_cast<const TIn *>(a.k);
     const TIn *vp = static_cast<const TIn *>(a.v);
     const TIn *dop = static_cast<const TIn *>(b.dout);
 
+    const int m0 = 16 * (warp >> 1), nh = warp & 1;
+
     // ---- phase 1: K, gates, A, T
-    for (int i = tid; i < kChunk * dk; i += kThreads) {
-        const int r = i / dk, j = i - r * dk;
-        Ks[r * ks + j] = r < L ? ld_in(kp + (r0 + r) * dk + j) : 0.f;
-        Wm[r * ks + j] = 0.f;
+    {
+        TileRegs<4> rk;
+        rk.load(kp + r0 * dk, dk, dk, L, dk, tid);
+        rk.store(Ks, ldk, dk, tid);
     }
     if (tid < kChunk) {
         const bool ok = tid < L;
         g[tid] = ok ? __ldg(a.log_alpha + r0 + tid) : 0.f;
         bb[tid] = ok ? __ldg(a.beta + r0 + tid) : 0.f;
-        dbU[tid] = 0.f;
-    }
-    for (int i = tid; i < kChunk * 65; i += kThreads) {
-        B1[i] = 0.f;
-        B2[i] = 0.f;
+        dbU[tid] = dgE[tid] = dgQ[tid] = Fv[tid] = tv[tid] = dgA[tid] = dbA[tid] = 0.f;
     }
     __syncthreads();
     if (tid == 0) {
@@ -301,6 +389,15 @@ k_bwd_chunk(FwdArgs a, BwdArgs b, const int2 *__restrict__ table, const float *_
             g[r] = s;
         }
     }
+    if (erase) {   // K K^T
+        float acc[kNtC][4];
+        mma::zero(acc);
+        mma::warp_gemm<kNtC, SPLIT>(
+            acc, [&](int m, int k) { return Ks[m * ldk + k]; },
+            [&](int k, int nn) { return Ks[nn * ldk + k]; }, m0, nh, 2, kChunk, dk, lane);
+        mma::for_each(acc, m0, nh, 2, kChunk, lane,
+                      [&](int m, int nn, float &x) { B3[m * kLdc + nn] = x; });
+    }
     __syncthreads();
     const float gC = g[L - 1];
     if (tid < kChunk) {
@@ -309,252 +406,252 @@ k_bwd_chunk(FwdArgs a, BwdArgs b, const int2 *__restrict__ table, const float *_
     }
     for (int i = tid; i < kChunk * kChunk; i += kThreads) {
         const int r = i >> 6, s = i & 63;
-        float val = 0.f;
-        if (s < r && erase) {
-            float acc = 0.f;
-            for (int j = 0; j < dk; ++j) acc = fmaf(Ks[r * ks + j], Ks[s * ks + j], acc);
-            val = bb[r] * expf(g[r] - g[s]) * acc;
-        }
-        B3[r * 65 + s] = val;
+        B1[r * kLdc + s] = (s < r && erase) ? bb[r] * expf(g[r] - g[s]) * B3[r * kLdc + s] : 0.f;
     }
     __syncthreads();
     if (tid < kChunk) {  // column tid of T = (I + A)^{-1}
         const int cc = tid;
-        for (int r = 0; r <= cc; ++r) Tm[r * 65 + cc] = (r == cc) ? 1.f : 0.f;
+        for (int r = 0; r <= cc; ++r) Tm[r * kLdc + cc] = (r == cc) ? 1.f : 0.f;
         for (int r = cc + 1; r < kChunk; ++r) {
             float acc = 0.f;
-            for (int s = cc; s < r; ++s) acc = fmaf(B3[r * 65 + s], Tm[s * 65 + cc], acc);
-            Tm[r * 65 + cc] = -acc;
+            for (int s = cc; s < r; ++s) acc = fmaf(B1[r * kLdc + s], Tm[s * kLdc + cc], acc);
+            Tm[r * kLdc + cc] = -acc;
         }
     }
 
     // ---- phase 2: the d_v contractions, tile by tile
-    const int rr = tid >> 2, jq = tid & 3;
-    float aQ[kRegJ], aK[kRegJ];
-#pragma unroll
-    for (int m = 0; m < kRegJ; ++m) {
-        aQ[m] = 0.f;
-        aK[m] = 0.f;
-    }
+    float aQ[kNtK][4], aK[kNtK][4], aW[kNtK][4], aP[kNtC][4], aT[kNtC][4];
+    mma::zero(aQ);
+    mma::zero(aK);
+    mma::zero(aW);
+    mma::zero(aP);
+    mma::zero(aT);
     float sC = 0.f;
+    const int gl = lane >> 2, tl = lane & 3;
     for (int dv0 = 0; dv0 < dv; dv0 += kDvt) {
         const int nv = min(kDvt, dv - dv0);
-        __syncthreads();  // T ready / the previous tile consumed
-        for (int i = tid; i < kChunk * kDvt; i += kThreads) {
-            const int r = i / kDvt, cc = i - r * kDvt;
-            const bool ok = r < L && cc < nv;
-            const long long o = (r0 + r) * dv + dv0 + cc;
-            dOs[r * us + cc] = ok ? ld_in(dop + o) : 0.f;
-            Vns[r * us + cc] = ok ? __ldg(Vn + o) : 0.f;
-            dVs[r * us + cc] = ok ? __ldg(dVn + o) : 0.f;
-            Vs[r * us + cc] = ok ? ld_in(vp + o) : 0.f;
-        }
-        for (int i = tid; i < dk * kDvt; i += kThreads) {
-            const int j = i / kDvt, cc = i - j * kDvt;
-            const bool ok = cc < nv;
-            const long long o = st_off + (long long)j * dv + dv0 + cc;
-            const float s0 = ok ? __ldg(Hst + o) : 0.f;
-            const float ds = ok ? __ldg(dHc + o) : 0.f;
-            S0t[j * us + cc] = s0;
-            dSt[j * us + cc] = ds;
-            sC = fmaf(s0, ds, sC);
+        {   // all of this tile's loads in flight at once
+            TileRegs<1> t1, t2, t3, t4, s0a, s0b, dsa, dsb;
+            const long long o = r0 * dv + dv0;
+            t1.load(dop + o, dv, kDvt, L, nv, tid);
+            t2.load(Vn + o, dv, kDvt, L, nv, tid);
+            t3.load(dVn + o, dv, kDvt, L, nv, tid);
+            t4.load(vp + o, dv, kDvt, L, nv, tid);
+            const float *hs = Hst + st_off + dv0, *hd = dHc + st_off + dv0;
+            s0a.load(hs, dv, kDvt, dk, nv, tid);
+            dsa.load(hd, dv, kDvt, dk, nv, tid);
+            s0b.load(hs + 64LL * dv, dv, kDvt, dk - 64, nv, tid);
+            dsb.load(hd + 64LL * dv, dv, kDvt, dk - 64, nv, tid);
+            __syncthreads();  // T ready / the previous tile consumed
+            t1.store(dOs, kLdt, kDvt, tid);
+            t2.store(Vns, kLdt, kDvt, tid);
+            t3.store(dVs, kLdt, kDvt, tid);
+            t4.store(Vs, kLdt, kDvt, tid);
+            s0a.store(S0t, kLdt, kDvt, tid, dk);
+            dsa.store(dSt, kLdt, kDvt, tid, dk);
+            if (dk > 64) {
+                s0b.store(S0t + 64 * kLdt, kLdt, kDvt, tid, dk - 64);
+                dsb.store(dSt + 64 * kLdt, kLdt, kDvt, tid, dk - 64);
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                sC = fmaf(s0a.v[0][e], dsa.v[0][e], fmaf(s0b.v[0][e], dsb.v[0][e], sC));
         }
         __syncthreads();
-        // dO S0 and V' dSC (registers), dV' S0 (shared, thread-owned elements)
+        // dO S0, V' dSC, dV' S0 sharing the S0 / dSC fragments
+#pragma unroll 1
+        for (int k0 = 0; k0 < kDvt; k0 += 8) {
+            mma::AFrag<SPLIT> fo, fv, fd;
+            fo.load([&](int m, int k) { return dOs[m * kLdt + k]; }, m0, k0, gl, tl);
+            fv.load([&](int m, int k) { return Vns[m * kLdt + k]; }, m0, k0, gl, tl);
+            if (erase) fd.load([&](int m, int k) { return dVs[m * kLdt + k]; }, m0, k0, gl, tl);
 #pragma unroll
-        for (int m = 0; m < kRegJ; ++m) {
-            const int j = jq + 4 * m;
-            if (j < dk) {
-                float q1 = 0.f, k1 = 0.f, w1 = 0.f;
-                #pragma unroll 4
-                for (int cc = 0; cc < kDvt; ++cc) {
-                    const float s0 = S0t[j * us + cc];
-                    q1 = fmaf(dOs[rr * us + cc], s0, q1);
-                    k1 = fmaf(Vns[rr * us + cc], dSt[j * us + cc], k1);
-                    if (erase) w1 = fmaf(dVs[rr * us + cc], s0, w1);
+            for (int i = 0; i < kNtK; ++i) {
+                const int nn = 8 * (nh + 2 * i);
+                if (nn < dk) {
+                    const float s0a = S0t[(nn + gl) * kLdt + k0 + tl];
+                    const float s0b = S0t[(nn + gl) * kLdt + k0 + tl + 4];
+                    mma::mma_step<SPLIT>(aQ[i], fo, s0a, s0b);
+                    mma::mma_step<SPLIT>(aK[i], fv, dSt[(nn + gl) * kLdt + k0 + tl],
+                                         dSt[(nn + gl) * kLdt + k0 + tl + 4]);
+                    if (erase) mma::mma_step<SPLIT>(aW[i], fd, s0a, s0b);
                 }
-                aQ[m] += q1;
-                aK[m] += k1;
-                if (erase) Wm[rr * ks + j] += w1;
             }
-        }
-        // dO V'^T and dV' (diag(beta) V)^T
-        for (int i = tid; i < kChunk * kChunk; i += kThreads) {
-            const int r = i >> 6, s = i & 63;
-            float p1 = 0.f, p2 = 0.f;
-            for (int cc = 0; cc < kDvt; ++cc) {
-                p1 = fmaf(dOs[r * us + cc], Vns[s * us + cc], p1);
-                if (erase) p2 = fmaf(dVs[r * us + cc], Vs[s * us + cc], p2);
-            }
-            B1[r * 65 + s] += p1;
-            if (erase) B2[r * 65 + s] += bb[s] * p2;
-        }
-        // dV = diag(beta) T^T dV'  and the U part of dbeta (one warp per row s)
-        for (int i = tid; i < kChunk * kDvt; i += kThreads) {
-            const int s = i / kDvt, cc = i - s * kDvt;
-            float acc = 0.f;
-            for (int r = s; r < kChunk; ++r) acc = fmaf(Tm[r * 65 + s], dVs[r * us + cc], acc);
-            if (s < L && cc < nv)
-                st_out(static_cast<TIn *>(b.dv) + (r0 + s) * dv + dv0 + cc, bb[s] * acc);
-            float x = acc * Vs[s * us + cc];
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-            if (lane == 0) dbU[s] += x;
+            for (int i = 0; i < kNtC; ++i) {
+                const int nn = 8 * (nh + 2 * i);
+                mma::mma_step<SPLIT>(aP[i], fo, Vns[(nn + gl) * kLdt + k0 + tl],
+                                     Vns[(nn + gl) * kLdt + k0 + tl + 4]);
+                if (erase)
+                    mma::mma_step<SPLIT>(aT[i], fd, Vs[(nn + gl) * kLdt + k0 + tl],
+                                         Vs[(nn + gl) * kLdt + k0 + tl + 4]);
+            }
+        }
+        // dV = diag(beta) T^T dV' and the U part of dbeta
+        {
+            float acc[kNtV][4];
+            mma::zero(acc);
+            mma::warp_gemm<kNtV, SPLIT>(
+                acc, [&](int m, int k) { return Tm[k * kLdc + m]; },
+                [&](int k, int nn) { return dVs[k * kLdt + nn]; }, m0, nh, 2, kDvt, kChunk, lane);
+            TIn *dvp = static_cast<TIn *>(b.dv);
+            mma::for_each(acc, m0, nh, 2, kDvt, lane, [&](int s, int cc, float &x) {
+                if (s < L && cc < nv) st_out(dvp + (r0 + s) * dv + dv0 + cc, bb[s] * x);
+            });
+            add_row_sums(acc, m0, nh, 2, kDvt, lane,
+                         [&](int s, int cc, float x) { return x * Vs[s * kLdt + cc]; }, dbU,
+                         [](int) { return 1.f; });
         }
     }
-    // <dSC, S0> over the block
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) sC += __shfl_xor_sync(0xffffffffu, sC, o);
-    __syncthreads();  // tiles consumed; Rg becomes Q
+    __syncthreads();  // tiles consumed; B1 (A) no longer needed; Rg becomes Q
     if (lane == 0) red[warp] = sC;
-    for (int i = tid; i < kChunk * dk; i += kThreads) {
-        const int r = i / dk, j = i - r * dk;
-        Qs[r * ks + j] = r < L ? ld_in(qp + (r0 + r) * dk + j) : 0.f;
+    if (erase)
+        mma::for_each(aW, m0, nh, 2, dk, lane,
+                      [&](int m, int j, float &x) { Wm[m * ldk + j] = x; });
+    mma::for_each(aP, m0, nh, 2, kChunk, lane, [&](int r, int s, float &x) {
+        B1[r * kLdc + s] = s <= r ? x * expf(g[r] - g[s]) : 0.f;   // dP
+    });
+    if (erase)
+        mma::for_each(aT, m0, nh, 2, kChunk, lane,
+                      [&](int r, int s, float &x) { B2[r * kLdc + s] = s < r ? x * bb[s] : 0.f; });
+    {
+        TileRegs<4> rq;
+        rq.load(qp + r0 * dk, dk, dk, L, dk, tid);
+        rq.store(Qs, ldk, dk, tid);
     }
     __syncthreads();
 
     // ---- phase 3
-    // dP = mask * G * (dO V'^T) in B1; E = dP * (Q K^T) in B3
-    for (int i = tid; i < kChunk * kChunk; i += kThreads) {
-        const int r = i >> 6, s = i & 63;
-        float dp = 0.f, ev = 0.f;
-        if (s <= r) {
-            dp = B1[r * 65 + s] * expf(g[r] - g[s]);
-            float acc = 0.f;
-            for (int j = 0; j < dk; ++j) acc = fmaf(Qs[r * ks + j], Ks[s * ks + j], acc);
-            ev = dp * acc;
-        }
-        B1[r * 65 + s] = dp;
-        B3[r * 65 + s] = ev;
+    {   // E = dP * (Q K^T): row sums into dg_r, column sums out of dg_s
+        float acc[kNtC][4];
+        mma::zero(acc);
+        mma::warp_gemm<kNtC, SPLIT>(
+            acc, [&](int m, int k) { return Qs[m * ldk + k]; },
+            [&](int k, int nn) { return Ks[nn * ldk + k]; }, m0, nh, 2, kChunk, dk, lane);
+        auto ev = [&](int r, int s, float x) { return B1[r * kLdc + s] * x; };
+        add_row_sums(acc, m0, nh, 2, kChunk, lane, ev, dgE, [](int) { return 1.f; });
+        add_col_sums(acc, m0, nh, 2, kChunk, lane, ev, dgE, -1.f);
     }
-    __syncthreads();
-    if (tid < kChunk) {
-        float x = 0.f;
-        for (int s = 0; s < kChunk; ++s) x += B3[tid * 65 + s] - B3[s * 65 + tid];
-        dgE[tid] = x;
-    }
-    // dQ = diag(gamma) dO S0 + dP K;  dg_r += gamma_r q_r . (dO S0)_r
-    {
-        float part = 0.f;
+    float tmp[kNtK][4];
+    {   // dQ = diag(gamma) dO S0 + dP K;  dg_r += gamma_r q_r . (dO S0)_r
+        mma::zero(tmp);
+        mma::warp_gemm<kNtK, SPLIT>(
+            tmp, [&](int m, int k) { return B1[m * kLdc + k]; },
+            [&](int k, int nn) { return Ks[k * ldk + nn]; }, m0, nh, 2, dk, kChunk, lane);
+        TIn *dqp = static_cast<TIn *>(b.dq);
 #pragma unroll
-        for (int m = 0; m < kRegJ; ++m) {
-            const int j = jq + 4 * m;
-            if (j < dk) {
-                float acc = 0.f;
-                #pragma unroll 4
-                for (int s = 0; s <= rr; ++s) acc = fmaf(B1[rr * 65 + s], Ks[s * ks + j], acc);
-                part = fmaf(Qs[rr * ks + j], aQ[m], part);
-                if (rr < L)
-                    st_out(static_cast<TIn *>(b.dq) + (r0 + rr) * dk + j,
-                           fmaf(gm[rr], aQ[m], acc));
-            }
-        }
-        part += __shfl_xor_sync(0xffffffffu, part, 1);
-        part += __shfl_xor_sync(0xffffffffu, part, 2);
-        if (jq == 0) dgQ[rr] = gm[rr] * part;
-    }
-    // dK (registers aK, row s = rr) = e_s (V' dSC)_s + (dP^T Q)_s + beta_s gamma_s (T^T dW)_s
-    {
-        float fpart = 0.f, tpart = 0.f;
+        for (int i = 0; i < kNtK; ++i)
 #pragma unroll
-        for (int m = 0; m < kRegJ; ++m) {
-            const int j = jq + 4 * m;
-            if (j < dk) {
-                const float kd = aK[m];
-                fpart = fmaf(Ks[rr * ks + j], kd, fpart);
-                float acc = ed[rr] * kd;
-                #pragma unroll 4
-                for (int r = rr; r < kChunk; ++r) acc = fmaf(B1[r * 65 + rr], Qs[r * ks + j], acc);
-                if (erase) {
-                    float tw = 0.f;   // (T^T dW)_sj = -sum_r T_rs Wm_rj
-                    #pragma unroll 4
-                    for (int r = rr; r < kChunk; ++r) tw = fmaf(-Tm[r * 65 + rr], Wm[r * ks + j], tw);
-                    acc = fmaf(bb[rr] * gm[rr], tw, acc);
-                    tpart = fmaf(Ks[rr * ks + j], tw, tpart);
-                }
-                aK[m] = acc;
+            for (int e = 0; e < 4; ++e) {
+                const int r = m0 + gl + 8 * (e >> 1), j = 8 * (nh + 2 * i) + 2 * tl + (e & 1);
+                if (8 * (nh + 2 * i) < dk && r < L)
+                    st_out(dqp + (r0 + r) * dk + j, fmaf(gm[r], aQ[i][e], tmp[i][e]));
             }
-        }
-        fpart += __shfl_xor_sync(0xffffffffu, fpart, 1);
-        fpart += __shfl_xor_sync(0xffffffffu, fpart, 2);
-        tpart += __shfl_xor_sync(0xffffffffu, tpart, 1);
-        tpart += __shfl_xor_sync(0xffffffffu, tpart, 2);
-        if (jq == 0) {
-            Fv[rr] = ed[rr] * fpart;
-            tv[rr] = gm[rr] * tpart;
+        add_row_sums(aQ, m0, nh, 2, dk, lane,
+                     [&](int r, int j, float x) { return Qs[r * ldk + j] * x; }, dgQ,
+                     [&](int r) { return gm[r]; });
+    }
+    {   // dK = e_s (V' dSC)_s + (dP^T Q)_s + beta_s gamma_s (T^T dW)_s
+        add_row_sums(aK, m0, nh, 2, dk, lane,
+                     [&](int s, int j, float x) { return Ks[s * ldk + j] * x; }, Fv,
+                     [&](int s) { return ed[s]; });
+        mma::for_each(aK, m0, nh, 2, dk, lane, [&](int s, int, float &x) { x *= ed[s]; });
+        mma::zero(tmp);
+        mma::warp_gemm<kNtK, SPLIT>(
+            tmp, [&](int m, int k) { return B1[k * kLdc + m]; },
+            [&](int k, int nn) { return Qs[k * ldk + nn]; }, m0, nh, 2, dk, kChunk, lane);
+#pragma unroll
+        for (int i = 0; i < kNtK; ++i)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) aK[i][e] += tmp[i][e];
+        if (erase) {
+            mma::zero(tmp);
+            mma::warp_gemm<kNtK, SPLIT>(
+                tmp, [&](int m, int k) { return Tm[k * kLdc + m]; },
+                [&](int k, int nn) { return Wm[k * ldk + nn]; }, m0, nh, 2, dk, kChunk, lane);
+            // T^T dW = -tmp
+            add_row_sums(tmp, m0, nh, 2, dk, lane,
+                         [&](int s, int j, float x) { return -Ks[s * ldk + j] * x; }, tv,
+                         [&](int s) { return gm[s]; });
+            mma::for_each(tmp, m0, nh, 2, dk, lane, [&](int s, int, float &x) {
+                x *= -bb[s] * gm[s];
+            });
+#pragma unroll
+            for (int i = 0; i < kNtK; ++i)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) aK[i][e] += tmp[i][e];
         }
     }
-    if (tid < kChunk) {
-        dgA[tid] = 0.f;
-        dbA[tid] = 0.f;
-    }
-    __syncthreads();  // B1 (dP) and B3 (E) consumed
+    __syncthreads();  // B1 (dP) consumed
     if (erase) {
-        // dT = dV'(diag(beta)V)^T - Wm (diag(beta gamma) K)^T, strictly lower part
-        for (int i = tid; i < kChunk * kChunk; i += kThreads) {
-            const int r = i >> 6, s = i & 63;
-            float val = 0.f;
-            if (s < r) {
-                float acc = 0.f;
-                for (int j = 0; j < dk; ++j) acc = fmaf(Wm[r * ks + j], Ks[s * ks + j], acc);
-                val = B2[r * 65 + s] - bb[s] * gm[s] * acc;
-            }
-            B2[r * 65 + s] = val;
+        {   // dT = dV'(diag(beta)V)^T - Wm (diag(beta gamma) K)^T, strictly lower part
+            float acc[kNtC][4];
+            mma::zero(acc);
+            mma::warp_gemm<kNtC, SPLIT>(
+                acc, [&](int m, int k) { return Wm[m * ldk + k]; },
+                [&](int k, int nn) { return Ks[nn * ldk + k]; }, m0, nh, 2, kChunk, dk, lane);
+            mma::for_each(acc, m0, nh, 2, kChunk, lane, [&](int r, int s, float &x) {
+                B2[r * kLdc + s] = s < r ? B2[r * kLdc + s] - bb[s] * gm[s] * x : 0.f;
+            });
         }
         __syncthreads();
-        // Z = dT T^T  (B1)
-        for (int i = tid; i < kChunk * kChunk; i += kThreads) {
-            const int r = i >> 6, s = i & 63;
-            float acc = 0.f;
-            const int mmax = min(r - 1, s);
-            for (int m = 0; m <= mmax; ++m) acc = fmaf(B2[r * 65 + m], Tm[s * 65 + m], acc);
-            B1[r * 65 + s] = acc;
+        {   // Z = dT T^T  (B1)
+            float acc[kNtC][4];
+            mma::zero(acc);
+            mma::warp_gemm<kNtC, SPLIT>(
+                acc, [&](int m, int k) { return B2[m * kLdc + k]; },
+                [&](int k, int nn) { return Tm[nn * kLdc + k]; }, m0, nh, 2, kChunk, kChunk,
+                lane);
+            mma::for_each(acc, m0, nh, 2, kChunk, lane,
+                          [&](int r, int s, float &x) { B1[r * kLdc + s] = x; });
         }
         __syncthreads();
-        // dA = -T^T Z, strictly lower, times G  (B2);  B3 = that times K K^T
-        for (int i = tid; i < kChunk * kChunk; i += kThreads) {
-            const int r = i >> 6, s = i & 63;
-            float x = 0.f, y = 0.f;
-            if (s < r) {
-                float acc = 0.f;
-                for (int m = r; m < kChunk; ++m) acc = fmaf(Tm[m * 65 + r], B1[m * 65 + s], acc);
-                x = -acc * expf(g[r] - g[s]);
-                float kk = 0.f;
-                for (int j = 0; j < dk; ++j) kk = fmaf(Ks[r * ks + j], Ks[s * ks + j], kk);
-                y = x * kk;
-            }
-            B2[r * 65 + s] = x;
-            B3[r * 65 + s] = y;
+        {   // X = dA * G with dA = -T^T Z (strictly lower), into B2; Y = X * K K^T
+            float acc[kNtC][4];
+            mma::zero(acc);
+            mma::warp_gemm<kNtC, SPLIT>(
+                acc, [&](int m, int k) { return Tm[k * kLdc + m]; },
+                [&](int k, int nn) { return B1[k * kLdc + nn]; }, m0, nh, 2, kChunk, kChunk,
+                lane);
+            mma::for_each(acc, m0, nh, 2, kChunk, lane, [&](int r, int s, float &x) {
+                x = s < r ? -x * expf(g[r] - g[s]) : 0.f;
+                B2[r * kLdc + s] = x;
+            });
+            auto yv = [&](int r, int s, float x) { return x * B3[r * kLdc + s]; };
+            add_row_sums(acc, m0, nh, 2, kChunk, lane, yv, dbA, [](int) { return 1.f; });
+            add_row_sums(acc, m0, nh, 2, kChunk, lane, yv, dgA, [&](int r) { return bb[r]; });
+            add_col_sums(acc, m0, nh, 2, kChunk, lane,
+                         [&](int r, int s, float x) { return bb[r] * x * B3[r * kLdc + s]; },
+                         dgA, -1.f);
         }
         __syncthreads();
-        if (tid < kChunk) {
-            float row = 0.f, col = 0.f;
-            for (int s = 0; s < kChunk; ++s) {
-                row += B3[tid * 65 + s];
-                col += bb[s] * B3[s * 65 + tid];
-            }
-            dbA[tid] = row;
-            dgA[tid] = bb[tid] * row - col;
-        }
-        // dK_r += beta_r sum_s X_rs k_s + sum_r' X_r'r beta_r' k_r'
+        {   // dK_r += beta_r (X K)_r + ((X * beta_row)^T K)_r
+            mma::zero(tmp);
+            mma::warp_gemm<kNtK, SPLIT>(
+                tmp, [&](int m, int k) { return B2[m * kLdc + k]; },
+                [&](int k, int nn) { return Ks[k * ldk + nn]; }, m0, nh, 2, dk, kChunk, lane);
+            mma::for_each(tmp, m0, nh, 2, dk, lane, [&](int r, int, float &x) { x *= bb[r]; });
 #pragma unroll
-        for (int m = 0; m < kRegJ; ++m) {
-            const int j = jq + 4 * m;
-            if (j < dk) {
-                float a1 = 0.f, a2 = 0.f;
-                #pragma unroll 4
-                for (int s = 0; s < rr; ++s) a1 = fmaf(B2[rr * 65 + s], Ks[s * ks + j], a1);
-                #pragma unroll 4
-                for (int r = rr + 1; r < kChunk; ++r)
-                    a2 = fmaf(B2[r * 65 + rr] * bb[r], Ks[r * ks + j], a2);
-                aK[m] += fmaf(bb[rr], a1, a2);
-            }
+            for (int i = 0; i < kNtK; ++i)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) aK[i][e] += tmp[i][e];
+            mma::zero(tmp);
+            mma::warp_gemm<kNtK, SPLIT>(
+                tmp, [&](int m, int k) { return B2[k * kLdc + m] * bb[k]; },
+                [&](int k, int nn) { return Ks[k * ldk + nn]; }, m0, nh, 2, dk, kChunk, lane);
+#pragma unroll
+            for (int i = 0; i < kNtK; ++i)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) aK[i][e] += tmp[i][e];
         }
     }
-#pragma unroll
-    for (int m = 0; m < kRegJ; ++m) {
-        const int j = jq + 4 * m;
-        if (j < dk && rr < L) st_out(static_cast<TIn *>(b.dk) + (r0 + rr) * dk + j, aK[m]);
+    {
+        TIn *dkp = static_cast<TIn *>(b.dk);
+        mma::for_each(aK, m0, nh, 2, dk, lane, [&](int r, int j, float &x) {
+            if (r < L) st_out(dkp + (r0 + r) * dk + j, x);
+        });
     }
     __syncthreads();
     // dg and dbeta per row; dlog_alpha is the reverse cumsum of dg
@@ -585,9 +682,12 @@ gdn_status launch_bwd(const FwdArgs &a, const BwdArgs &b) {
     const size_t states = (size_t)a.sm.H * (size_t)a.chunk_slots * a.dk * a.dv;
     const size_t dsm = dstate_smem(a.dk);
     const ChunkLay ly = chunk_lay(a.dk);
-    if (cudaFuncSetAttribute(k_bwd_dstate<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    constexpr bool kSplit = std::is_same<TIn, float>::value;   // fp32 I/O: 3xTF32
+    if (cudaFuncSetAttribute(k_bwd_dstate<TIn, kSplit>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)dsm) != cudaSuccess ||
-        cudaFuncSetAttribute(k_bwd_chunk<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaFuncSetAttribute(k_bwd_chunk<TIn, kSplit>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)ly.bytes) != cudaSuccess)
         return GDN_ERR_CUDA;
     float *W = nullptr, *U = nullptr, *G = nullptr, *Vn = nullptr, *dVn = nullptr;
@@ -615,13 +715,13 @@ gdn_status launch_bwd(const FwdArgs &a, const BwdArgs &b) {
         rc = enqueue_simt_state(f, W, U, G, Hst, Vn);
     }
     if (rc == GDN_OK && a.sm.N > 0 && a.sm.H > 0) {
-        dim3 grid(a.sm.N, a.sm.H, (a.dv + kDvt - 1) / kDvt);
-        k_bwd_dstate<TIn><<<grid, kThreads, dsm, st>>>(a, b, W, G, dVn, dHc, err);
+        dim3 grid(a.sm.N, a.sm.H, (a.dv + kDvm - 1) / kDvm);
+        k_bwd_dstate<TIn, kSplit><<<grid, kThreads, dsm, st>>>(a, b, W, G, dVn, dHc, err);
         count_launch();
     }
     if (rc == GDN_OK && a.chunk_slots > 0 && a.sm.H > 0) {
         const int slot = timer_begin(st, "k_bwd_chunk");
-        k_bwd_chunk<TIn><<<dim3(a.chunk_slots, a.sm.H), kThreads, ly.bytes, st>>>(
+        k_bwd_chunk<TIn, kSplit><<<dim3(a.chunk_slots, a.sm.H), kThreads, ly.bytes, st>>>(
             a, b, table, Hst, dHc, Vn, dVn, err);
         timer_end(slot, st);
         count_launch();

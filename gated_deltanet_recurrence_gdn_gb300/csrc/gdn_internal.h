@@ -94,8 +94,6 @@ gdn_status simt_forward(const FwdArgs &a);
 // pass: with Hst non-null it also stores each chunk's starting state
 // H = S^T as [H][chunk_slots][d_k][d_v] and with Vn non-null the rows of
 // V' = U - W H as [rows][d_v]; with a.o null it writes no output.
-size_t simt_prep_smem(const FwdArgs &a);
-size_t simt_state_smem(const FwdArgs &a);
 gdn_status enqueue_simt_prep(const FwdArgs &a, const int2 *table, float *W, float *U, float *G);
 gdn_status enqueue_simt_state(const FwdArgs &a, const float *W, const float *U, const float *G,
                               float *Hst, float *Vn);

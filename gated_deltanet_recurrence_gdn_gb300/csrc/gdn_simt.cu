@@ -28,8 +28,11 @@
 #include <cuda_bf16.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "gdn_internal.h"
+#include "gdn_mma.cuh"
+#include "gdn_tile.cuh"
 
 namespace gdn {
 namespace {
@@ -362,6 +365,165 @@ k_simt_state(FwdArgs a, const float *__restrict__ W, const float *__restrict__ U
     }
 }
 
+// The state pass for a scalar gate with its products on the tensor cores
+// (mma.sync tf32, gdn_mma.cuh: three products per step for fp32 I/O, one for
+// bf16 I/O).  Same chunk algebra and outputs as k_simt_state, but one CTA per
+// (sequence, head, 64-wide d_v tile), and the next chunk's K, W, Q and U are
+// loaded into registers while the current chunk is computed.  P and O are
+// skipped when no output is wanted (the backward pass's recomputation).
+constexpr int kDvm = 64;           // d_v columns per CTA
+constexpr int kLdh = kDvm + 8;     // d_k x 64 state tile: transposed reads conflict-free
+constexpr int kLdc = kChunk + 4;   // 64 x 64 tiles
+
+size_t state_mma_smem(int dk, bool out) {
+    const size_t ldk = dk + 4;
+    return sizeof(float) * ((size_t)dk * kLdh + 2 * kChunk * ldk + 2 * kChunk * kLdc +
+                            3 * kChunk + (out ? kChunk * ldk + kChunk * kLdc : 0));
+}
+
+template <typename TIn, bool SPLIT>
+__global__ void __launch_bounds__(kThreads, 1)
+k_state_mma(FwdArgs a, const float *__restrict__ W, const float *__restrict__ U,
+            const float *__restrict__ G, float *__restrict__ Hst, float *__restrict__ Vout,
+            int *err) {
+    extern __shared__ float smem[];
+    const int dk = a.dk, dv = a.dv, tid = threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5;
+    const int n = blockIdx.x, h = blockIdx.y, dv0 = blockIdx.z * kDvm;
+    const int nv = min(kDvm, dv - dv0);
+    if (!seq_ok(a.sm, n)) {
+        if (tid == 0) set_error(err, kErrBadIndex);
+        return;
+    }
+    long long row0;
+    int len;
+    a.sm.get(n, h, row0, len);
+    const int ldk = dk + 4;
+    const TIn *qp = static_cast<const TIn *>(a.q);
+    const TIn *kp = static_cast<const TIn *>(a.k);
+    TIn *op = static_cast<TIn *>(a.o);
+    float *Hs = smem;                    // [dk][72]   H = S^T tile
+    float *Ks = Hs + dk * kLdh;          // [64][dk+4]
+    float *Ws = Ks + kChunk * ldk;       // [64][dk+4]
+    float *Us = Ws + kChunk * ldk;       // [64][68]
+    float *Vn = Us + kChunk * kLdc;      // [64][68]
+    float *g = Vn + kChunk * kLdc;       // [64]
+    float *e = g + kChunk;               // [64] exp(g_C - g_r)
+    float *gm = e + kChunk;              // [64] exp(g_r)
+    float *Qs = gm + kChunk;             // [64][dk+4]  (with an output only)
+    float *P = Qs + kChunk * ldk;        // [64][68]    (with an output only)
+    const long long sbase = ((long long)n * a.sm.H + h) * dv;
+    const int m0 = 16 * (warp >> 1), nh = warp & 1;
+    const int ntask = 2 * ((dk + 15) / 16);
+
+    for (int i = tid; i < dk * kDvm; i += kThreads) {
+        const int j = i / kDvm, cc = i - j * kDvm;
+        Hs[j * kLdh + cc] = (a.h0 && cc < nv) ? __ldg(a.h0 + (sbase + dv0 + cc) * dk + j) : 0.f;
+    }
+    TileRegs<4> rk, rw, rq;
+    TileRegs<2> ru;
+    float gnext = 0.f;
+    auto issue = [&](int c) {
+        const int L = min(kChunk, len - c * kChunk);
+        const long long r0 = row0 + (long long)c * kChunk;
+        rk.load(kp + r0 * dk, dk, dk, L, dk, tid);
+        rw.load(W + r0 * dk, dk, dk, L, dk, tid);
+        if (op) rq.load(qp + r0 * dk, dk, dk, L, dk, tid);
+        ru.load(U + r0 * dv + dv0, dv, kDvm, L, nv, tid);
+        if (tid < kChunk) gnext = __ldg(G + r0 + min(tid, L - 1));
+    };
+    const int nch = (len + kChunk - 1) / kChunk;
+    if (nch > 0) issue(0);
+    for (int c = 0; c < nch; ++c) {
+        const int t0 = c * kChunk, L = min(kChunk, len - t0);
+        const long long r0 = row0 + t0;
+        __syncthreads();  // previous chunk fully consumed
+        if (Hst) {
+            float *dst = Hst + ((long long)h * a.chunk_slots + a.chunk_slot(n, c)) * dk * dv;
+            for (int i = tid; i < dk * kDvm; i += kThreads) {
+                const int j = i / kDvm, cc = i - j * kDvm;
+                if (cc < nv) dst[(long long)j * dv + dv0 + cc] = Hs[j * kLdh + cc];
+            }
+        }
+        rk.store(Ks, ldk, dk, tid);
+        rw.store(Ws, ldk, dk, tid);
+        if (op) rq.store(Qs, ldk, dk, tid);
+        ru.store(Us, kLdc, kDvm, tid);
+        if (tid < kChunk) g[tid] = gnext;
+        if (c + 1 < nch) issue(c + 1);
+        __syncthreads();
+        const float gl = g[kChunk - 1];
+        if (tid < kChunk) {
+            e[tid] = expf(gl - g[tid]);
+            gm[tid] = expf(g[tid]);
+        }
+        if (op) {   // P_rs = G_rs q_r . k_s, s <= r
+            float acc[4][4];
+            mma::zero(acc);
+            mma::warp_gemm<4, SPLIT>(
+                acc, [&](int m, int k) { return Qs[m * ldk + k]; },
+                [&](int k, int nn) { return Ks[nn * ldk + k]; }, m0, nh, 2, kChunk, dk, lane);
+            mma::for_each(acc, m0, nh, 2, kChunk, lane, [&](int r, int s, float &x) {
+                P[r * kLdc + s] = s <= r ? expf(g[r] - g[s]) * x : 0.f;
+            });
+        }
+        {   // V' = U - W H
+            float acc[4][4];
+            mma::zero(acc);
+            mma::warp_gemm<4, SPLIT>(
+                acc, [&](int m, int k) { return Ws[m * ldk + k]; },
+                [&](int k, int nn) { return Hs[k * kLdh + nn]; }, m0, nh, 2, kDvm, dk, lane);
+            mma::for_each(acc, m0, nh, 2, kDvm, lane, [&](int r, int cc, float &x) {
+                const float val = Us[r * kLdc + cc] - x;
+                Vn[r * kLdc + cc] = val;
+                if (Vout && r < L && cc < nv) Vout[(r0 + r) * dv + dv0 + cc] = val;
+            });
+        }
+        __syncthreads();
+        if (op) {   // O = diag(gamma) Q H + P V'
+            float a1[4][4], a2[4][4];
+            mma::zero(a1);
+            mma::zero(a2);
+            mma::warp_gemm<4, SPLIT>(
+                a1, [&](int m, int k) { return Qs[m * ldk + k]; },
+                [&](int k, int nn) { return Hs[k * kLdh + nn]; }, m0, nh, 2, kDvm, dk, lane);
+            mma::warp_gemm<4, SPLIT>(
+                a2, [&](int m, int k) { return P[m * kLdc + k]; },
+                [&](int k, int nn) { return Vn[k * kLdc + nn]; }, m0, nh, 2, kDvm, kChunk, lane);
+            const int gq = lane >> 2, tq = lane & 3;
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int r = m0 + gq + 8 * (q >> 1), cc = 8 * (nh + 2 * i) + 2 * tq + (q & 1);
+                    if (r < L && cc < nv)
+                        st_out(op + (r0 + r) * dv + dv0 + cc, fmaf(gm[r], a1[i][q], a2[i][q]));
+                }
+            __syncthreads();  // every read of H for this chunk is done
+        }
+        // H <- exp(g_C) H + K^T diag(exp(g_C - g)) V'
+        const float decay = expf(gl);
+        for (int task = warp; task < ntask; task += kThreads / 32) {
+            const int j0 = 16 * (task >> 1), th = task & 1;
+            float acc[4][4];
+            mma::zero(acc);
+            mma::warp_gemm<4, SPLIT>(
+                acc, [&](int m, int k) { return m < dk ? Ks[k * ldk + m] * e[k] : 0.f; },
+                [&](int k, int nn) { return Vn[k * kLdc + nn]; }, j0, th, 2, kDvm, kChunk, lane);
+            mma::for_each(acc, j0, th, 2, kDvm, lane, [&](int j, int cc, float &x) {
+                if (j < dk) Hs[j * kLdh + cc] = fmaf(decay, Hs[j * kLdh + cc], x);
+            });
+        }
+    }
+    __syncthreads();
+    if (a.hT) {
+        for (int i = tid; i < dk * kDvm; i += kThreads) {
+            const int j = i / kDvm, cc = i - j * kDvm;
+            if (cc < nv) a.hT[(sbase + dv0 + cc) * dk + j] = Hs[j * kLdh + cc];
+        }
+    }
+}
+
 size_t prep_smem(int dk, int dv, bool vg) {
     return sizeof(float) * ((size_t)kChunk * (dk + 1) + (size_t)kChunk * (dv + 1) +
                             2 * kChunk * 65 + 3 * kChunk + (vg ? (size_t)kChunk * (dk + 1) : 0));
@@ -372,16 +534,44 @@ size_t state_smem(int dk, bool vg) {
                             (vg ? (size_t)kChunk * (dk + 1) : 0));
 }
 
+// Launches the state pass: the tensor-core kernel for a scalar gate, the
+// CUDA-core one for a gate per key dimension.
+template <typename TIn>
+cudaError_t run_state(const FwdArgs &a, const float *W, const float *U, const float *G,
+                      float *Hst, float *Vn, int *err) {
+    const dim3 grid(a.sm.N, a.sm.H, (a.dv + kDvt - 1) / kDvt);
+    cudaError_t e;
+    if (a.vector_gate) {
+        const size_t ssm = state_smem(a.dk, true);
+        e = cudaFuncSetAttribute(k_simt_state<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)ssm);
+        if (e != cudaSuccess) return e;
+        const int slot = timer_begin(a.stream, "k_simt_state");
+        k_simt_state<TIn><<<grid, kThreads, ssm, a.stream>>>(a, W, U, G, Hst, Vn, err);
+        timer_end(slot, a.stream);
+    } else {
+        constexpr bool kSplit = std::is_same<TIn, float>::value;   // fp32 I/O: 3xTF32
+        const size_t ssm = state_mma_smem(a.dk, a.o != nullptr);
+        e = cudaFuncSetAttribute(k_state_mma<TIn, kSplit>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)state_mma_smem(a.dk, true));
+        if (e != cudaSuccess) return e;
+        const dim3 gm(a.sm.N, a.sm.H, (a.dv + kDvm - 1) / kDvm);
+        const int slot = timer_begin(a.stream, "k_state_mma");
+        k_state_mma<TIn, kSplit><<<gm, kThreads, ssm, a.stream>>>(a, W, U, G, Hst, Vn, err);
+        timer_end(slot, a.stream);
+    }
+    count_launch();
+    return cudaGetLastError();
+}
+
 template <typename TIn>
 gdn_status launch(const FwdArgs &a) {
     int *err = device_error_word();
     cudaStream_t st = a.stream;
-    const size_t psm = prep_smem(a.dk, a.dv, a.vector_gate),
-                 ssm = state_smem(a.dk, a.vector_gate);
+    const size_t psm = prep_smem(a.dk, a.dv, a.vector_gate);
     if (cudaFuncSetAttribute(k_simt_prep<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)psm) != cudaSuccess ||
-        cudaFuncSetAttribute(k_simt_state<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)ssm) != cudaSuccess)
+                             (int)psm) != cudaSuccess)
         return GDN_ERR_CUDA;
     float *W = nullptr, *U = nullptr, *G = nullptr;
     int2 *table = nullptr;
@@ -412,13 +602,9 @@ gdn_status launch(const FwdArgs &a) {
             count_launch();
         }
     }
-    if (rc == GDN_OK && a.sm.N > 0 && a.sm.H > 0) {
-        dim3 grid(a.sm.N, a.sm.H, (a.dv + kDvt - 1) / kDvt);
-        const int slot = timer_begin(st, "k_simt_state");
-        k_simt_state<TIn><<<grid, kThreads, ssm, st>>>(a, W, U, G, nullptr, nullptr, err);
-        timer_end(slot, st);
-        count_launch();
-    }
+    if (rc == GDN_OK && a.sm.N > 0 && a.sm.H > 0 &&
+        run_state<TIn>(a, W, U, G, nullptr, nullptr, err) != cudaSuccess)
+        rc = GDN_ERR_CUDA;
     if (rc == GDN_OK && cudaGetLastError() != cudaSuccess) rc = GDN_ERR_CUDA;
     scratch_free(W, st);
     scratch_free(U, st);
@@ -433,8 +619,6 @@ gdn_status simt_forward(const FwdArgs &a) {
     return a.dt == GDN_F32 ? launch<float>(a) : launch<__nv_bfloat16>(a);
 }
 
-size_t simt_prep_smem(const FwdArgs &a) { return prep_smem(a.dk, a.dv, a.vector_gate); }
-size_t simt_state_smem(const FwdArgs &a) { return state_smem(a.dk, a.vector_gate); }
 
 template <typename TIn>
 gdn_status enqueue_prep_t(const FwdArgs &a, const int2 *table, float *W, float *U, float *G) {
@@ -453,15 +637,9 @@ gdn_status enqueue_prep_t(const FwdArgs &a, const int2 *table, float *W, float *
 template <typename TIn>
 gdn_status enqueue_state_t(const FwdArgs &a, const float *W, const float *U, const float *G,
                            float *Hst, float *Vn) {
-    const size_t ssm = state_smem(a.dk, a.vector_gate);
-    if (cudaFuncSetAttribute(k_simt_state<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)ssm) != cudaSuccess)
+    if (a.sm.N > 0 && a.sm.H > 0 &&
+        run_state<TIn>(a, W, U, G, Hst, Vn, device_error_word()) != cudaSuccess)
         return GDN_ERR_CUDA;
-    if (a.sm.N > 0 && a.sm.H > 0) {
-        k_simt_state<TIn><<<dim3(a.sm.N, a.sm.H, (a.dv + kDvt - 1) / kDvt), kThreads, ssm,
-                            a.stream>>>(a, W, U, G, Hst, Vn, device_error_word());
-        count_launch();
-    }
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
@@ -526,12 +704,9 @@ template <typename TIn>
 gdn_status launch_noalloc(const FwdArgs &a, float *scratch) {
     int *err = device_error_word();
     cudaStream_t st = a.stream;
-    const size_t psm = prep_smem(a.dk, a.dv, a.vector_gate),
-                 ssm = state_smem(a.dk, a.vector_gate);
+    const size_t psm = prep_smem(a.dk, a.dv, a.vector_gate);
     if (cudaFuncSetAttribute(k_simt_prep<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)psm) != cudaSuccess ||
-        cudaFuncSetAttribute(k_simt_state<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)ssm) != cudaSuccess)
+                             (int)psm) != cudaSuccess)
         return GDN_ERR_CUDA;
     const size_t rows = (size_t)a.rows;
     float *W = scratch;
@@ -542,9 +717,7 @@ gdn_status launch_noalloc(const FwdArgs &a, float *scratch) {
         k_simt_prep<TIn><<<grid, kThreads, psm, st>>>(a, nullptr, W, U, G, err);
         count_launch();
     }
-    dim3 grid(a.sm.N, a.sm.H, (a.dv + kDvt - 1) / kDvt);
-    k_simt_state<TIn><<<grid, kThreads, ssm, st>>>(a, W, U, G, nullptr, nullptr, err);
-    count_launch();
+    if (run_state<TIn>(a, W, U, G, nullptr, nullptr, err) != cudaSuccess) return GDN_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
