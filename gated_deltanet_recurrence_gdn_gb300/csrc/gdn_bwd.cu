@@ -218,7 +218,7 @@ k_bwd_dstate(FwdArgs a, BwdArgs b, const float *__restrict__ W, const float *__r
 // cores through mma.sync tf32 (gdn_mma.cuh; three products per step for fp32
 // I/O, one for bf16 I/O).  Warp w owns rows 16 (w / 2) .. +15 of every
 // 64-row output and the 8-column tiles w % 2, w % 2 + 2, ... of it.
-// Phase 1 rebuilds A and T from K, beta and the gates.  Phase 2 walks d_v in
+// Phase 1 loads T (written by the prep) and forms K K^T.  Phase 2 walks d_v in
 // 32-wide tiles: dO S0, V' dSC and dV' S0 (64 x d_k) and dO V'^T,
 // dV' V^T (64 x 64) accumulate in registers; dV = diag(beta) T^T dV' and the
 // U part of dbeta are written per tile.  Phase 3 forms dQ, dK, dbeta and
@@ -301,9 +301,9 @@ __device__ __forceinline__ void add_col_sums(float (&acc)[NT][4], int m0, int nt
 
 template <typename TIn, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
-k_bwd_chunk(FwdArgs a, BwdArgs b, const int2 *__restrict__ table, const float *__restrict__ Hst,
-            const float *__restrict__ dHc, const float *__restrict__ Vn,
-            const float *__restrict__ dVn, int *err) {
+k_bwd_chunk(FwdArgs a, BwdArgs b, const int2 *__restrict__ table, const float *__restrict__ Tg,
+            const float *__restrict__ Hst, const float *__restrict__ dHc,
+            const float *__restrict__ Vn, const float *__restrict__ dVn, int *err) {
     extern __shared__ float smem[];
     const int dk = a.dk, dv = a.dv, tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
@@ -338,7 +338,7 @@ k_bwd_chunk(FwdArgs a, BwdArgs b, const int2 *__restrict__ table, const float *_
     float *Rg = smem + ly.oR;     // phase 2 tiles, then Q
     float *Wm = smem + ly.oWm;    // [64][ldk]  dV' S0 (= -dW)
     float *Tm = smem + ly.oT;     // [64][68]   T
-    float *B1 = smem + ly.oB1;    // [64][68]   A, then dP, then dT T^T
+    float *B1 = smem + ly.oB1;    // [64][68]   dP, then dT T^T
     float *B2 = smem + ly.oB2;    // [64][68]   dV' (diag(beta) V)^T, then dT, then X = dA * G
     float *B3 = smem + ly.oB3;    // [64][68]   K K^T
     float *g = smem + ly.oV;      // [64] gate cumsum
@@ -369,11 +369,18 @@ k_bwd_chunk(FwdArgs a, BwdArgs b, const int2 *__restrict__ table, const float *_
 
     const int m0 = 16 * (warp >> 1), nh = warp & 1;
 
-    // ---- phase 1: K, gates, A, T
+    // ---- phase 1: K, gates, T (from the prep), K K^T
     {
         TileRegs<4> rk;
+        TileRegs<2> rt;
         rk.load(kp + r0 * dk, dk, dk, L, dk, tid);
+        rt.load(Tg + r0 * kChunk, kChunk, kChunk, L, kChunk, tid);
         rk.store(Ks, ldk, dk, tid);
+        rt.store(Tm, kLdc, kChunk, tid, L);
+    }
+    for (int i = tid; i < kChunk * kChunk; i += kThreads) {   // rows past L: identity
+        const int r = i >> 6, s = i & 63;
+        if (r >= L) Tm[r * kLdc + s] = r == s ? 1.f : 0.f;
     }
     if (tid < kChunk) {
         const bool ok = tid < L;
@@ -403,20 +410,6 @@ k_bwd_chunk(FwdArgs a, BwdArgs b, const int2 *__restrict__ table, const float *_
     if (tid < kChunk) {
         gm[tid] = expf(g[tid]);
         ed[tid] = expf(gC - g[tid]);
-    }
-    for (int i = tid; i < kChunk * kChunk; i += kThreads) {
-        const int r = i >> 6, s = i & 63;
-        B1[r * kLdc + s] = (s < r && erase) ? bb[r] * expf(g[r] - g[s]) * B3[r * kLdc + s] : 0.f;
-    }
-    __syncthreads();
-    if (tid < kChunk) {  // column tid of T = (I + A)^{-1}
-        const int cc = tid;
-        for (int r = 0; r <= cc; ++r) Tm[r * kLdc + cc] = (r == cc) ? 1.f : 0.f;
-        for (int r = cc + 1; r < kChunk; ++r) {
-            float acc = 0.f;
-            for (int s = cc; s < r; ++s) acc = fmaf(B1[r * kLdc + s], Tm[s * kLdc + cc], acc);
-            Tm[r * kLdc + cc] = -acc;
-        }
     }
 
     // ---- phase 2: the d_v contractions, tile by tile
@@ -691,13 +684,13 @@ gdn_status launch_bwd(const FwdArgs &a, const BwdArgs &b) {
                              (int)ly.bytes) != cudaSuccess)
         return GDN_ERR_CUDA;
     float *W = nullptr, *U = nullptr, *G = nullptr, *Vn = nullptr, *dVn = nullptr;
-    float *Hst = nullptr, *dHc = nullptr;
+    float *Hst = nullptr, *dHc = nullptr, *Tg = nullptr;
     int2 *table = nullptr;
-    float **bufs[] = {&W, &U, &G, &Vn, &dVn, &Hst, &dHc};
+    float **bufs[] = {&W, &U, &G, &Vn, &dVn, &Hst, &dHc, &Tg};
     const size_t sizes[] = {rows * a.dk, rows * a.dv, rows, rows * a.dv, rows * a.dv,
-                            states > 0 ? states : 1, states > 0 ? states : 1};
+                            states > 0 ? states : 1, states > 0 ? states : 1, rows * kChunk};
     gdn_status rc = GDN_OK;
-    for (int i = 0; i < 7 && rc == GDN_OK; ++i)
+    for (int i = 0; i < 8 && rc == GDN_OK; ++i)
         if (scratch_alloc((void **)bufs[i], sizes[i] * sizeof(float), st) != cudaSuccess)
             rc = GDN_ERR_CUDA;
     if (rc == GDN_OK && a.sm.cu && a.chunk_slots > 0) {
@@ -707,7 +700,7 @@ gdn_status launch_bwd(const FwdArgs &a, const BwdArgs &b) {
         else
             rc = enqueue_chunk_table(a, table);
     }
-    if (rc == GDN_OK) rc = enqueue_simt_prep(a, table, W, U, G);
+    if (rc == GDN_OK) rc = enqueue_simt_prep(a, table, W, U, G, Tg);
     if (rc == GDN_OK) {
         FwdArgs f = a;
         f.o = nullptr;
@@ -722,7 +715,7 @@ gdn_status launch_bwd(const FwdArgs &a, const BwdArgs &b) {
     if (rc == GDN_OK && a.chunk_slots > 0 && a.sm.H > 0) {
         const int slot = timer_begin(st, "k_bwd_chunk");
         k_bwd_chunk<TIn, kSplit><<<dim3(a.chunk_slots, a.sm.H), kThreads, ly.bytes, st>>>(
-            a, b, table, Hst, dHc, Vn, dVn, err);
+            a, b, table, Tg, Hst, dHc, Vn, dVn, err);
         timer_end(slot, st);
         count_launch();
     }

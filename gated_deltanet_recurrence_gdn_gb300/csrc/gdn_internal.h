@@ -89,12 +89,14 @@ long long option(int key);
 // SIMT (CUDA-core, fp32 arithmetic) path: every supported shape and dtype.
 gdn_status simt_forward(const FwdArgs &a);
 
-// Pieces of that path the backward pass reuses.  Prep: W [rows][d_k], U
-// [rows][d_v], gate cumsum G [rows] (table: packed batches only).  State
-// pass: with Hst non-null it also stores each chunk's starting state
-// H = S^T as [H][chunk_slots][d_k][d_v] and with Vn non-null the rows of
-// V' = U - W H as [rows][d_v]; with a.o null it writes no output.
-gdn_status enqueue_simt_prep(const FwdArgs &a, const int2 *table, float *W, float *U, float *G);
+// Pieces of that path the backward pass reuses.  Prep: W [rows][d_k],
+// U [rows][d_v], gate cumsum G [rows] and, with Tout non-null (scalar gates
+// only), T = (I + A)^{-1} of every chunk as [rows][64] (table: packed
+// batches only).  State pass: with Hst non-null it also stores each chunk's
+// starting state H = S^T as [H][chunk_slots][d_k][d_v] and with Vn non-null
+// the rows of V' = U - W H as [rows][d_v]; with a.o null it writes no output.
+gdn_status enqueue_simt_prep(const FwdArgs &a, const int2 *table, float *W, float *U, float *G,
+                             float *Tout);
 gdn_status enqueue_simt_state(const FwdArgs &a, const float *W, const float *U, const float *G,
                               float *Hst, float *Vn);
 

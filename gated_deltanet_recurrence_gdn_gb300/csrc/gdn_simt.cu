@@ -524,6 +524,184 @@ k_state_mma(FwdArgs a, const float *__restrict__ W, const float *__restrict__ U,
     }
 }
 
+// Chunk prep for a scalar gate with its products on the tensor cores
+// (mma.sync tf32; three products per step for fp32 I/O).  One CTA per
+// (chunk, head): the gate cumsum, A = strictly_lower(diag(beta) G * K K^T),
+// T = (I + A)^{-1} by blocks -- the four 16 x 16 diagonal blocks by forward
+// substitution, then T21 = -T22 A21 T11 merges 16 -> 32 -> 64 -- and
+// W = T diag(beta gamma) K, U = T diag(beta) V.  With Tout non-null it also
+// stores T as [rows][64] (the backward pass reads it).
+size_t prep_mma_smem(int dk, int dv) {
+    return sizeof(float) * ((size_t)kChunk * (dk + 4) + (size_t)kChunk * (dv + 4) +
+                            2 * kChunk * kLdc + 32 * 36 + 3 * kChunk);
+}
+
+template <typename TIn, bool SPLIT>
+__global__ void __launch_bounds__(kThreads, 2)
+k_prep_mma(FwdArgs a, const int2 *__restrict__ table, float *__restrict__ W,
+           float *__restrict__ U, float *__restrict__ G, float *__restrict__ Tout, int *err) {
+    extern __shared__ float smem[];
+    const int dk = a.dk, dv = a.dv, tid = threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5;
+    int n, c;
+    if (table) {
+        int2 e = table[blockIdx.x];
+        n = e.x;
+        c = e.y;
+        if (n < 0) return;
+    } else {
+        n = blockIdx.x / a.max_chunks;
+        c = blockIdx.x % a.max_chunks;
+    }
+    const int h = blockIdx.y;
+    if (!seq_ok(a.sm, n)) {
+        if (tid == 0) set_error(err, kErrBadIndex);
+        return;
+    }
+    long long row0;
+    int len;
+    a.sm.get(n, h, row0, len);
+    const int t0 = c * kChunk;
+    if (t0 >= len) return;
+    const int L = min(kChunk, len - t0);
+    const long long r0 = row0 + t0;
+    const bool erase = !a.no_erase;
+    const int ldk = dk + 4, ldv = dv + 4;
+    float *Ks = smem;                 // [64][dk+4]
+    float *Vs = Ks + kChunk * ldk;    // [64][dv+4]
+    float *A = Vs + kChunk * ldv;     // [64][68]
+    float *Tm = A + kChunk * kLdc;    // [64][68]
+    float *X = Tm + kChunk * kLdc;    // [32][36] merge scratch
+    float *g = X + 32 * 36;           // [64] gate cumsum
+    float *bb = g + kChunk;           // [64] beta
+    float *wb = bb + kChunk;          // [64] beta * exp(g)
+    const int m0 = 16 * (warp >> 1), nh = warp & 1;
+    {
+        TileRegs<4> rk;
+        TileRegs<8> rv;
+        rk.load(static_cast<const TIn *>(a.k) + r0 * dk, dk, dk, L, dk, tid);
+        rv.load(static_cast<const TIn *>(a.v) + r0 * dv, dv, dv, L, dv, tid);
+        if (tid < kChunk) {
+            const bool ok = tid < L;
+            g[tid] = ok ? __ldg(a.log_alpha + r0 + tid) : 0.f;
+            bb[tid] = ok ? __ldg(a.beta + r0 + tid) : 0.f;
+        }
+        for (int i = tid; i < kChunk * kLdc; i += kThreads) Tm[i] = 0.f;
+        rk.store(Ks, ldk, dk, tid);
+        rv.store(Vs, ldv, dv, tid);
+    }
+    __syncthreads();
+    if (tid == 0) {
+        float s = 0.f;
+        for (int r = 0; r < kChunk; ++r) {
+            s += g[r];
+            g[r] = s;
+        }
+    }
+    __syncthreads();
+    if (tid < kChunk) wb[tid] = bb[tid] * expf(g[tid]);
+    if (erase) {   // A = strictly_lower(diag(beta) G * K K^T)
+        float acc[4][4];
+        mma::zero(acc);
+        mma::warp_gemm<4, SPLIT>(
+            acc, [&](int m, int k) { return Ks[m * ldk + k]; },
+            [&](int k, int nn) { return Ks[nn * ldk + k]; }, m0, nh, 2, kChunk, dk, lane);
+        mma::for_each(acc, m0, nh, 2, kChunk, lane, [&](int r, int s, float &x) {
+            A[r * kLdc + s] = s < r ? bb[r] * expf(g[r] - g[s]) * x : 0.f;
+        });
+    } else {
+        for (int i = tid; i < kChunk * kLdc; i += kThreads) A[i] = 0.f;
+    }
+    __syncthreads();
+    if (tid < kChunk) {   // the 16 x 16 diagonal blocks, one column per thread
+        const int o = 16 * (tid >> 4), cc = tid & 15;
+        Tm[(o + cc) * kLdc + o + cc] = 1.f;
+        for (int r = cc + 1; r < 16; ++r) {
+            float acc = 0.f;
+            for (int s = cc; s < r; ++s)
+                acc = fmaf(A[(o + r) * kLdc + o + s], Tm[(o + s) * kLdc + o + cc], acc);
+            Tm[(o + r) * kLdc + o + cc] = -acc;
+        }
+    }
+    __syncthreads();
+    // 16 -> 32: T21 = -T22 (A21 T11) for the blocks at 0 and 32
+    if (warp < 2) {
+        const int o = 32 * warp;
+        float acc[2][4];
+        mma::zero(acc);
+        mma::warp_gemm<2, SPLIT>(
+            acc, [&](int m, int k) { return A[(o + 16 + m) * kLdc + o + k]; },
+            [&](int k, int nn) { return Tm[(o + k) * kLdc + o + nn]; }, 0, 0, 1, 16, 16, lane);
+        mma::for_each(acc, 0, 0, 1, 16, lane,
+                      [&](int m, int nn, float &x) { X[(16 * warp + m) * 36 + nn] = x; });
+    }
+    __syncthreads();
+    if (warp < 2) {
+        const int o = 32 * warp;
+        float acc[2][4];
+        mma::zero(acc);
+        mma::warp_gemm<2, SPLIT>(
+            acc, [&](int m, int k) { return Tm[(o + 16 + m) * kLdc + o + 16 + k]; },
+            [&](int k, int nn) { return X[(16 * warp + k) * 36 + nn]; }, 0, 0, 1, 16, 16, lane);
+        mma::for_each(acc, 0, 0, 1, 16, lane,
+                      [&](int m, int nn, float &x) { Tm[(o + 16 + m) * kLdc + o + nn] = -x; });
+    }
+    __syncthreads();
+    // 32 -> 64: T21 = -T22 (A21 T11), 32 x 32 blocks
+    if (warp < 4) {
+        float acc[2][4];
+        mma::zero(acc);
+        mma::warp_gemm<2, SPLIT>(
+            acc, [&](int m, int k) { return A[(32 + m) * kLdc + k]; },
+            [&](int k, int nn) { return Tm[k * kLdc + nn]; }, 16 * (warp >> 1), warp & 1, 2, 32,
+            32, lane);
+        mma::for_each(acc, 16 * (warp >> 1), warp & 1, 2, 32, lane,
+                      [&](int m, int nn, float &x) { X[m * 36 + nn] = x; });
+    }
+    __syncthreads();
+    if (warp < 4) {
+        float acc[2][4];
+        mma::zero(acc);
+        mma::warp_gemm<2, SPLIT>(
+            acc, [&](int m, int k) { return Tm[(32 + m) * kLdc + 32 + k]; },
+            [&](int k, int nn) { return X[k * 36 + nn]; }, 16 * (warp >> 1), warp & 1, 2, 32, 32,
+            lane);
+        mma::for_each(acc, 16 * (warp >> 1), warp & 1, 2, 32, lane,
+                      [&](int m, int nn, float &x) { Tm[(32 + m) * kLdc + nn] = -x; });
+    }
+    __syncthreads();
+    {   // W = T diag(beta gamma) K (zero without the erase term)
+        float acc[8][4];
+        mma::zero(acc);
+        if (erase)
+            mma::warp_gemm<8, SPLIT>(
+                acc, [&](int m, int k) { return Tm[m * kLdc + k]; },
+                [&](int k, int nn) { return Ks[k * ldk + nn] * wb[k]; }, m0, nh, 2, dk, kChunk,
+                lane);
+        mma::for_each(acc, m0, nh, 2, dk, lane, [&](int r, int j, float &x) {
+            if (r < L) W[(r0 + r) * dk + j] = x;
+        });
+    }
+    for (int c0 = 0; c0 < dv; c0 += 128) {   // U = T diag(beta) V
+        float acc[8][4];
+        mma::zero(acc);
+        const int ne = min(dv, c0 + 128);
+        mma::warp_gemm<8, SPLIT>(
+            acc, [&](int m, int k) { return Tm[m * kLdc + k]; },
+            [&](int k, int nn) { return Vs[k * ldv + nn] * bb[k]; }, m0, c0 / 8 + nh, 2, ne,
+            kChunk, lane);
+        mma::for_each(acc, m0, c0 / 8 + nh, 2, ne, lane, [&](int r, int j, float &x) {
+            if (r < L) U[(r0 + r) * dv + j] = x;
+        });
+    }
+    if (tid < L) G[r0 + tid] = g[tid];
+    if (Tout)
+        for (int i = tid; i < kChunk * kChunk; i += kThreads) {
+            const int r = i >> 6, s = i & 63;
+            if (r < L) Tout[(r0 + r) * kChunk + s] = Tm[r * kLdc + s];
+        }
+}
+
 size_t prep_smem(int dk, int dv, bool vg) {
     return sizeof(float) * ((size_t)kChunk * (dk + 1) + (size_t)kChunk * (dv + 1) +
                             2 * kChunk * 65 + 3 * kChunk + (vg ? (size_t)kChunk * (dk + 1) : 0));
@@ -532,6 +710,31 @@ size_t state_smem(int dk, bool vg) {
     return sizeof(float) * ((size_t)dk * kDvt + 3 * (size_t)kChunk * (dk + 1) +
                             2 * kChunk * (kDvt + 1) + kChunk * 65 + 2 * kChunk +
                             (vg ? (size_t)kChunk * (dk + 1) : 0));
+}
+
+// Launches the chunk prep: the tensor-core kernel for a scalar gate, the
+// CUDA-core one for a gate per key dimension (which writes no T).
+template <typename TIn>
+cudaError_t run_prep(const FwdArgs &a, const int2 *table, float *W, float *U, float *G,
+                     float *Tout, int *err) {
+    const dim3 grid(a.chunk_slots, a.sm.H);
+    cudaError_t e;
+    if (a.vector_gate) {
+        const size_t psm = prep_smem(a.dk, a.dv, true);
+        e = cudaFuncSetAttribute(k_simt_prep<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)psm);
+        if (e != cudaSuccess) return e;
+        k_simt_prep<TIn><<<grid, kThreads, psm, a.stream>>>(a, table, W, U, G, err);
+    } else {
+        constexpr bool kSplit = std::is_same<TIn, float>::value;   // fp32 I/O: 3xTF32
+        const size_t psm = prep_mma_smem(a.dk, a.dv);
+        e = cudaFuncSetAttribute(k_prep_mma<TIn, kSplit>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psm);
+        if (e != cudaSuccess) return e;
+        k_prep_mma<TIn, kSplit><<<grid, kThreads, psm, a.stream>>>(a, table, W, U, G, Tout, err);
+    }
+    count_launch();
+    return cudaGetLastError();
 }
 
 // Launches the state pass: the tensor-core kernel for a scalar gate, the
@@ -569,10 +772,6 @@ template <typename TIn>
 gdn_status launch(const FwdArgs &a) {
     int *err = device_error_word();
     cudaStream_t st = a.stream;
-    const size_t psm = prep_smem(a.dk, a.dv, a.vector_gate);
-    if (cudaFuncSetAttribute(k_simt_prep<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)psm) != cudaSuccess)
-        return GDN_ERR_CUDA;
     float *W = nullptr, *U = nullptr, *G = nullptr;
     int2 *table = nullptr;
     const size_t rows = (size_t)a.rows > 0 ? (size_t)a.rows : 1;
@@ -596,11 +795,9 @@ gdn_status launch(const FwdArgs &a) {
                 count_launch();
             }
         }
-        if (rc == GDN_OK) {
-            dim3 grid(a.chunk_slots, a.sm.H);
-            k_simt_prep<TIn><<<grid, kThreads, psm, st>>>(a, table, W, U, G, err);
-            count_launch();
-        }
+        if (rc == GDN_OK && a.sm.H > 0 &&
+            run_prep<TIn>(a, table, W, U, G, nullptr, err) != cudaSuccess)
+            rc = GDN_ERR_CUDA;
     }
     if (rc == GDN_OK && a.sm.N > 0 && a.sm.H > 0 &&
         run_state<TIn>(a, W, U, G, nullptr, nullptr, err) != cudaSuccess)
@@ -619,21 +816,6 @@ gdn_status simt_forward(const FwdArgs &a) {
     return a.dt == GDN_F32 ? launch<float>(a) : launch<__nv_bfloat16>(a);
 }
 
-
-template <typename TIn>
-gdn_status enqueue_prep_t(const FwdArgs &a, const int2 *table, float *W, float *U, float *G) {
-    const size_t psm = prep_smem(a.dk, a.dv, a.vector_gate);
-    if (cudaFuncSetAttribute(k_simt_prep<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)psm) != cudaSuccess)
-        return GDN_ERR_CUDA;
-    if (a.chunk_slots > 0 && a.sm.H > 0) {
-        k_simt_prep<TIn><<<dim3(a.chunk_slots, a.sm.H), kThreads, psm, a.stream>>>(
-            a, table, W, U, G, device_error_word());
-        count_launch();
-    }
-    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
-}
-
 template <typename TIn>
 gdn_status enqueue_state_t(const FwdArgs &a, const float *W, const float *U, const float *G,
                            float *Hst, float *Vn) {
@@ -643,9 +825,20 @@ gdn_status enqueue_state_t(const FwdArgs &a, const float *W, const float *U, con
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
-gdn_status enqueue_simt_prep(const FwdArgs &a, const int2 *table, float *W, float *U, float *G) {
-    return a.dt == GDN_F32 ? enqueue_prep_t<float>(a, table, W, U, G)
-                           : enqueue_prep_t<__nv_bfloat16>(a, table, W, U, G);
+template <typename TIn>
+gdn_status enqueue_prep_t(const FwdArgs &a, const int2 *table, float *W, float *U, float *G,
+                          float *Tout) {
+    if (a.chunk_slots > 0 && a.sm.H > 0 &&
+        run_prep<TIn>(a, table, W, U, G, Tout, device_error_word()) != cudaSuccess)
+        return GDN_ERR_CUDA;
+    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+gdn_status enqueue_simt_prep(const FwdArgs &a, const int2 *table, float *W, float *U, float *G,
+                             float *Tout) {
+    if (Tout && a.vector_gate) return GDN_ERR_UNSUPPORTED;
+    return a.dt == GDN_F32 ? enqueue_prep_t<float>(a, table, W, U, G, Tout)
+                           : enqueue_prep_t<__nv_bfloat16>(a, table, W, U, G, Tout);
 }
 
 gdn_status enqueue_simt_state(const FwdArgs &a, const float *W, const float *U, const float *G,
@@ -703,20 +896,12 @@ gdn_status noalloc_scratch(float **out) {
 template <typename TIn>
 gdn_status launch_noalloc(const FwdArgs &a, float *scratch) {
     int *err = device_error_word();
-    cudaStream_t st = a.stream;
-    const size_t psm = prep_smem(a.dk, a.dv, a.vector_gate);
-    if (cudaFuncSetAttribute(k_simt_prep<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)psm) != cudaSuccess)
-        return GDN_ERR_CUDA;
     const size_t rows = (size_t)a.rows;
     float *W = scratch;
     float *U = W + rows * a.dk;
     float *G = U + rows * a.dv;
-    if (a.chunk_slots > 0) {
-        dim3 grid(a.chunk_slots, a.sm.H);
-        k_simt_prep<TIn><<<grid, kThreads, psm, st>>>(a, nullptr, W, U, G, err);
-        count_launch();
-    }
+    if (a.chunk_slots > 0 && run_prep<TIn>(a, nullptr, W, U, G, nullptr, err) != cudaSuccess)
+        return GDN_ERR_CUDA;
     if (run_state<TIn>(a, W, U, G, nullptr, nullptr, err) != cudaSuccess) return GDN_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
