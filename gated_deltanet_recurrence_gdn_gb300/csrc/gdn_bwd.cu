@@ -156,9 +156,8 @@ k_bwd_dstate(FwdArgs a, BwdArgs b, const float *__restrict__ W, const float *__r
         {
             float acc[4][4];
             mma::zero(acc);
-            mma::warp_gemm<4, SPLIT>(
-                acc, [&](int m, int k) { return Qs[m * ldk + k]; },
-                [&](int k, int nn) { return Ks[nn * ldk + k]; }, m0, nh, 2, kChunk, dk, lane);
+            mma::gemm_s<4, SPLIT>(acc, Qs, ldk, 1, nullptr, Ks, 1, ldk, m0, nh, 2, kChunk, dk,
+                                  lane);
             mma::for_each(acc, m0, nh, 2, kChunk, lane, [&](int r, int s, float &x) {
                 P[r * kLdc + s] = s <= r ? expf(g[r] - g[s]) * x : 0.f;
             });
@@ -168,12 +167,10 @@ k_bwd_dstate(FwdArgs a, BwdArgs b, const float *__restrict__ W, const float *__r
             float a1[4][4], a2[4][4];
             mma::zero(a1);
             mma::zero(a2);
-            mma::warp_gemm<4, SPLIT>(
-                a1, [&](int m, int k) { return P[k * kLdc + m]; },
-                [&](int k, int nn) { return dOs[k * kLdc + nn]; }, m0, nh, 2, kDvm, kChunk, lane);
-            mma::warp_gemm<4, SPLIT>(
-                a2, [&](int m, int k) { return Ks[m * ldk + k]; },
-                [&](int k, int nn) { return dH[k * kLdh + nn]; }, m0, nh, 2, kDvm, dk, lane);
+            mma::gemm_s<4, SPLIT>(a1, P, 1, kLdc, nullptr, dOs, kLdc, 1, m0, nh, 2, kDvm, kChunk,
+                                  lane);
+            mma::gemm_s<4, SPLIT>(a2, Ks, ldk, 1, nullptr, dH, kLdh, 1, m0, nh, 2, kDvm, dk,
+                                  lane);
             const int gl4 = lane >> 2, tl = lane & 3;
 #pragma unroll
             for (int i = 0; i < 4; ++i)
@@ -190,14 +187,17 @@ k_bwd_dstate(FwdArgs a, BwdArgs b, const float *__restrict__ W, const float *__r
         const float decay = expf(gl);
         for (int task = warp; task < ntask; task += kThreads / 32) {
             const int j0 = 16 * (task >> 1), th = task & 1;
-            float acc[4][4];
+            float acc[4][4], acw[4][4];
             mma::zero(acc);
-            mma::warp_gemm<4, SPLIT>(
-                acc, [&](int m, int k) { return m < dk ? Qs[k * ldk + m] * gm[k] : 0.f; },
-                [&](int k, int nn) { return dOs[k * kLdc + nn]; }, j0, th, 2, kDvm, kChunk, lane);
-            mma::warp_gemm<4, SPLIT>(
-                acc, [&](int m, int k) { return m < dk ? -Ws[k * ldk + m] : 0.f; },
-                [&](int k, int nn) { return dVs[k * kLdc + nn]; }, j0, th, 2, kDvm, kChunk, lane);
+            mma::zero(acw);
+            mma::gemm_s<4, SPLIT>(acc, Qs, 1, ldk, gm, dOs, kLdc, 1, j0, th, 2, kDvm, kChunk,
+                                  lane);
+            mma::gemm_s<4, SPLIT>(acw, Ws, 1, ldk, nullptr, dVs, kLdc, 1, j0, th, 2, kDvm,
+                                  kChunk, lane);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) acc[i][q] -= acw[i][q];
             mma::for_each(acc, j0, th, 2, kDvm, lane, [&](int j, int cc, float &x) {
                 if (j < dk) dH[j * kLdh + cc] = fmaf(decay, dH[j * kLdh + cc], x);
             });
@@ -399,9 +399,8 @@ k_bwd_chunk(FwdArgs a, BwdArgs b, const int2 *__restrict__ table, const float *_
     if (erase) {   // K K^T
         float acc[kNtC][4];
         mma::zero(acc);
-        mma::warp_gemm<kNtC, SPLIT>(
-            acc, [&](int m, int k) { return Ks[m * ldk + k]; },
-            [&](int k, int nn) { return Ks[nn * ldk + k]; }, m0, nh, 2, kChunk, dk, lane);
+        mma::gemm_s<kNtC, SPLIT>(acc, Ks, ldk, 1, nullptr, Ks, 1, ldk, m0, nh, 2, kChunk, dk,
+                                 lane);
         mma::for_each(acc, m0, nh, 2, kChunk, lane,
                       [&](int m, int nn, float &x) { B3[m * kLdc + nn] = x; });
     }
@@ -452,7 +451,7 @@ k_bwd_chunk(FwdArgs a, BwdArgs b, const int2 *__restrict__ table, const float *_
         }
         __syncthreads();
         // dO S0, V' dSC, dV' S0 sharing the S0 / dSC fragments
-#pragma unroll 1
+#pragma unroll
         for (int k0 = 0; k0 < kDvt; k0 += 8) {
             mma::AFrag<SPLIT> fo, fv, fd;
             fo.load([&](int m, int k) { return dOs[m * kLdt + k]; }, m0, k0, gl, tl);
@@ -484,9 +483,8 @@ k_bwd_chunk(FwdArgs a, BwdArgs b, const int2 *__restrict__ table, const float *_
         {
             float acc[kNtV][4];
             mma::zero(acc);
-            mma::warp_gemm<kNtV, SPLIT>(
-                acc, [&](int m, int k) { return Tm[k * kLdc + m]; },
-                [&](int k, int nn) { return dVs[k * kLdt + nn]; }, m0, nh, 2, kDvt, kChunk, lane);
+            mma::gemm_s<kNtV, SPLIT>(acc, Tm, 1, kLdc, nullptr, dVs, kLdt, 1, m0, nh, 2, kDvt,
+                                     kChunk, lane);
             TIn *dvp = static_cast<TIn *>(b.dv);
             mma::for_each(acc, m0, nh, 2, kDvt, lane, [&](int s, int cc, float &x) {
                 if (s < L && cc < nv) st_out(dvp + (r0 + s) * dv + dv0 + cc, bb[s] * x);
@@ -520,9 +518,8 @@ k_bwd_chunk(FwdArgs a, BwdArgs b, const int2 *__restrict__ table, const float *_
     {   // E = dP * (Q K^T): row sums into dg_r, column sums out of dg_s
         float acc[kNtC][4];
         mma::zero(acc);
-        mma::warp_gemm<kNtC, SPLIT>(
-            acc, [&](int m, int k) { return Qs[m * ldk + k]; },
-            [&](int k, int nn) { return Ks[nn * ldk + k]; }, m0, nh, 2, kChunk, dk, lane);
+        mma::gemm_s<kNtC, SPLIT>(acc, Qs, ldk, 1, nullptr, Ks, 1, ldk, m0, nh, 2, kChunk, dk,
+                                 lane);
         auto ev = [&](int r, int s, float x) { return B1[r * kLdc + s] * x; };
         add_row_sums(acc, m0, nh, 2, kChunk, lane, ev, dgE, [](int) { return 1.f; });
         add_col_sums(acc, m0, nh, 2, kChunk, lane, ev, dgE, -1.f);
@@ -530,9 +527,8 @@ k_bwd_chunk(FwdArgs a, BwdArgs b, const int2 *__restrict__ table, const float *_
     float tmp[kNtK][4];
     {   // dQ = diag(gamma) dO S0 + dP K;  dg_r += gamma_r q_r . (dO S0)_r
         mma::zero(tmp);
-        mma::warp_gemm<kNtK, SPLIT>(
-            tmp, [&](int m, int k) { return B1[m * kLdc + k]; },
-            [&](int k, int nn) { return Ks[k * ldk + nn]; }, m0, nh, 2, dk, kChunk, lane);
+        mma::gemm_s<kNtK, SPLIT>(tmp, B1, kLdc, 1, nullptr, Ks, ldk, 1, m0, nh, 2, dk, kChunk,
+                                 lane);
         TIn *dqp = static_cast<TIn *>(b.dq);
 #pragma unroll
         for (int i = 0; i < kNtK; ++i)
@@ -552,18 +548,16 @@ k_bwd_chunk(FwdArgs a, BwdArgs b, const int2 *__restrict__ table, const float *_
                      [&](int s) { return ed[s]; });
         mma::for_each(aK, m0, nh, 2, dk, lane, [&](int s, int, float &x) { x *= ed[s]; });
         mma::zero(tmp);
-        mma::warp_gemm<kNtK, SPLIT>(
-            tmp, [&](int m, int k) { return B1[k * kLdc + m]; },
-            [&](int k, int nn) { return Qs[k * ldk + nn]; }, m0, nh, 2, dk, kChunk, lane);
+        mma::gemm_s<kNtK, SPLIT>(tmp, B1, 1, kLdc, nullptr, Qs, ldk, 1, m0, nh, 2, dk, kChunk,
+                                 lane);
 #pragma unroll
         for (int i = 0; i < kNtK; ++i)
 #pragma unroll
             for (int e = 0; e < 4; ++e) aK[i][e] += tmp[i][e];
         if (erase) {
             mma::zero(tmp);
-            mma::warp_gemm<kNtK, SPLIT>(
-                tmp, [&](int m, int k) { return Tm[k * kLdc + m]; },
-                [&](int k, int nn) { return Wm[k * ldk + nn]; }, m0, nh, 2, dk, kChunk, lane);
+            mma::gemm_s<kNtK, SPLIT>(tmp, Tm, 1, kLdc, nullptr, Wm, ldk, 1, m0, nh, 2, dk, kChunk,
+                                     lane);
             // T^T dW = -tmp
             add_row_sums(tmp, m0, nh, 2, dk, lane,
                          [&](int s, int j, float x) { return -Ks[s * ldk + j] * x; }, tv,
@@ -582,9 +576,8 @@ k_bwd_chunk(FwdArgs a, BwdArgs b, const int2 *__restrict__ table, const float *_
         {   // dT = dV'(diag(beta)V)^T - Wm (diag(beta gamma) K)^T, strictly lower part
             float acc[kNtC][4];
             mma::zero(acc);
-            mma::warp_gemm<kNtC, SPLIT>(
-                acc, [&](int m, int k) { return Wm[m * ldk + k]; },
-                [&](int k, int nn) { return Ks[nn * ldk + k]; }, m0, nh, 2, kChunk, dk, lane);
+            mma::gemm_s<kNtC, SPLIT>(acc, Wm, ldk, 1, nullptr, Ks, 1, ldk, m0, nh, 2, kChunk, dk,
+                                     lane);
             mma::for_each(acc, m0, nh, 2, kChunk, lane, [&](int r, int s, float &x) {
                 B2[r * kLdc + s] = s < r ? B2[r * kLdc + s] - bb[s] * gm[s] * x : 0.f;
             });
@@ -593,10 +586,8 @@ k_bwd_chunk(FwdArgs a, BwdArgs b, const int2 *__restrict__ table, const float *_
         {   // Z = dT T^T  (B1)
             float acc[kNtC][4];
             mma::zero(acc);
-            mma::warp_gemm<kNtC, SPLIT>(
-                acc, [&](int m, int k) { return B2[m * kLdc + k]; },
-                [&](int k, int nn) { return Tm[nn * kLdc + k]; }, m0, nh, 2, kChunk, kChunk,
-                lane);
+            mma::gemm_s<kNtC, SPLIT>(acc, B2, kLdc, 1, nullptr, Tm, 1, kLdc, m0, nh, 2, kChunk,
+                                     kChunk, lane);
             mma::for_each(acc, m0, nh, 2, kChunk, lane,
                           [&](int r, int s, float &x) { B1[r * kLdc + s] = x; });
         }
@@ -604,10 +595,8 @@ k_bwd_chunk(FwdArgs a, BwdArgs b, const int2 *__restrict__ table, const float *_
         {   // X = dA * G with dA = -T^T Z (strictly lower), into B2; Y = X * K K^T
             float acc[kNtC][4];
             mma::zero(acc);
-            mma::warp_gemm<kNtC, SPLIT>(
-                acc, [&](int m, int k) { return Tm[k * kLdc + m]; },
-                [&](int k, int nn) { return B1[k * kLdc + nn]; }, m0, nh, 2, kChunk, kChunk,
-                lane);
+            mma::gemm_s<kNtC, SPLIT>(acc, Tm, 1, kLdc, nullptr, B1, kLdc, 1, m0, nh, 2, kChunk,
+                                     kChunk, lane);
             mma::for_each(acc, m0, nh, 2, kChunk, lane, [&](int r, int s, float &x) {
                 x = s < r ? -x * expf(g[r] - g[s]) : 0.f;
                 B2[r * kLdc + s] = x;
@@ -622,18 +611,16 @@ k_bwd_chunk(FwdArgs a, BwdArgs b, const int2 *__restrict__ table, const float *_
         __syncthreads();
         {   // dK_r += beta_r (X K)_r + ((X * beta_row)^T K)_r
             mma::zero(tmp);
-            mma::warp_gemm<kNtK, SPLIT>(
-                tmp, [&](int m, int k) { return B2[m * kLdc + k]; },
-                [&](int k, int nn) { return Ks[k * ldk + nn]; }, m0, nh, 2, dk, kChunk, lane);
+            mma::gemm_s<kNtK, SPLIT>(tmp, B2, kLdc, 1, nullptr, Ks, ldk, 1, m0, nh, 2, dk, kChunk,
+                                     lane);
             mma::for_each(tmp, m0, nh, 2, dk, lane, [&](int r, int, float &x) { x *= bb[r]; });
 #pragma unroll
             for (int i = 0; i < kNtK; ++i)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) aK[i][e] += tmp[i][e];
             mma::zero(tmp);
-            mma::warp_gemm<kNtK, SPLIT>(
-                tmp, [&](int m, int k) { return B2[k * kLdc + m] * bb[k]; },
-                [&](int k, int nn) { return Ks[k * ldk + nn]; }, m0, nh, 2, dk, kChunk, lane);
+            mma::gemm_s<kNtK, SPLIT>(tmp, B2, 1, kLdc, bb, Ks, ldk, 1, m0, nh, 2, dk, kChunk,
+                                     lane);
 #pragma unroll
             for (int i = 0; i < kNtK; ++i)
 #pragma unroll

@@ -9,12 +9,15 @@
 // (g + 8, t + 4); B holds (t, g), (t + 4, g); the accumulator holds
 // (g, 2t), (g, 2t + 1), (g + 8, 2t), (g + 8, 2t + 1).
 //
-// SPLIT = true keeps fp32 accuracy with three tf32 products per step: each
-// operand is split into its tf32 rounding hi and the tf32 rounding of the
-// remainder lo, and hi*hi + hi*lo + lo*hi is accumulated (the lo*lo term,
-// about 2^-22 relative, is dropped) -- the "3xTF32" emulation of an fp32
-// product on tf32 tensor cores.  SPLIT = false takes hi*hi alone (about
-// 2^-11 relative per product), which is enough for bf16 outputs.
+// The tensor cores read a tf32 operand from the upper 19 bits of an fp32
+// register (sign, exponent, 10 mantissa bits), so an fp32 value passed as is
+// is truncated to tf32.  SPLIT = true keeps fp32 accuracy with three tf32
+// products per step: each operand x is split into hi = x with its low 13
+// bits cleared (exact) and lo = x - hi (exact in fp32, truncated to tf32 by
+// the hardware), and hi*hi + hi*lo + lo*hi is accumulated -- the "3xTF32"
+// emulation of an fp32 product on tf32 tensor cores (the dropped lo*lo term
+// and the truncation of lo are about 2^-20 relative).  SPLIT = false takes x
+// alone (about 2^-10 relative per operand), which is enough for bf16 outputs.
 //
 // Shared-memory strides: row-wise operand reads (A(m, k) = S[m * ld + k],
 // B(k, n) = S[n * ld + k]) are free of bank conflicts when ld is 4 modulo 8;
@@ -24,12 +27,6 @@
 
 namespace gdn {
 namespace mma {
-
-__device__ __forceinline__ float to_tf32(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return __uint_as_float(r);
-}
 
 __device__ __forceinline__ void mma8(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
                                      uint32_t b1) {
@@ -44,9 +41,13 @@ template <bool SPLIT>
 struct Op {
     uint32_t hi, lo;
     __device__ __forceinline__ explicit Op(float x) {
-        const float h = to_tf32(x);
-        hi = __float_as_uint(h);
-        lo = SPLIT ? __float_as_uint(to_tf32(x - h)) : 0u;
+        if (SPLIT) {
+            hi = __float_as_uint(x) & 0xffffe000u;
+            lo = __float_as_uint(x - __uint_as_float(hi));
+        } else {
+            hi = __float_as_uint(x);
+            lo = 0u;
+        }
     }
 };
 
@@ -92,6 +93,46 @@ __device__ __forceinline__ void warp_gemm(float (&acc)[NT][4], FA A, FB B, int m
             const int n = 8 * (nt0 + i * nstep);
             if (n < n_end) mma_step<SPLIT>(acc[i], a, B(k0 + t, n + g), B(k0 + t + 4, n + g));
         }
+    }
+}
+
+// The same product with strided operands: A(m, k) = pa[m * sam + k * sak]
+// (times ascale[k] when ascale is non-null) and B(k, n) = pb[k * sbk + n * sbn];
+// the per-thread element pointers are formed once, the k loop only adds.
+template <int NT, bool SPLIT>
+__device__ __forceinline__ void gemm_s(float (&acc)[NT][4], const float *pa, int sam, int sak,
+                                       const float *ascale, const float *pb, int sbk, int sbn,
+                                       int m0, int nt0, int nstep, int n_end, int K, int lane) {
+    const int g = lane >> 2, t = lane & 3;
+    const float *a0 = pa + (m0 + g) * sam + t * sak;
+    const float *a1 = a0 + 8 * sam;
+    const float *bp[NT];
+#pragma unroll
+    for (int i = 0; i < NT; ++i) bp[i] = pb + t * sbk + (8 * (nt0 + i * nstep) + g) * sbn;
+    const int ak4 = 4 * sak, bk4 = 4 * sbk, ak8 = 8 * sak, bk8 = 8 * sbk;
+#pragma unroll 2
+    for (int k0 = 0; k0 < K; k0 += 8) {
+        float v0 = a0[0], v1 = a1[0], v2 = a0[ak4], v3 = a1[ak4];
+        if (ascale) {
+            const float s0 = ascale[k0 + t], s1 = ascale[k0 + t + 4];
+            v0 *= s0;
+            v1 *= s0;
+            v2 *= s1;
+            v3 *= s1;
+        }
+        AFrag<SPLIT> a;
+        {
+            const Op<SPLIT> o0(v0), o1(v1), o2(v2), o3(v3);
+            a.hi[0] = o0.hi; a.hi[1] = o1.hi; a.hi[2] = o2.hi; a.hi[3] = o3.hi;
+            a.lo[0] = o0.lo; a.lo[1] = o1.lo; a.lo[2] = o2.lo; a.lo[3] = o3.lo;
+        }
+#pragma unroll
+        for (int i = 0; i < NT; ++i) {
+            if (8 * (nt0 + i * nstep) < n_end) mma_step<SPLIT>(acc[i], a, bp[i][0], bp[i][bk4]);
+            bp[i] += bk8;
+        }
+        a0 += ak8;
+        a1 += ak8;
     }
 }
 

@@ -460,9 +460,8 @@ k_state_mma(FwdArgs a, const float *__restrict__ W, const float *__restrict__ U,
         if (op) {   // P_rs = G_rs q_r . k_s, s <= r
             float acc[4][4];
             mma::zero(acc);
-            mma::warp_gemm<4, SPLIT>(
-                acc, [&](int m, int k) { return Qs[m * ldk + k]; },
-                [&](int k, int nn) { return Ks[nn * ldk + k]; }, m0, nh, 2, kChunk, dk, lane);
+            mma::gemm_s<4, SPLIT>(acc, Qs, ldk, 1, nullptr, Ks, 1, ldk, m0, nh, 2, kChunk, dk,
+                                  lane);
             mma::for_each(acc, m0, nh, 2, kChunk, lane, [&](int r, int s, float &x) {
                 P[r * kLdc + s] = s <= r ? expf(g[r] - g[s]) * x : 0.f;
             });
@@ -470,9 +469,8 @@ k_state_mma(FwdArgs a, const float *__restrict__ W, const float *__restrict__ U,
         {   // V' = U - W H
             float acc[4][4];
             mma::zero(acc);
-            mma::warp_gemm<4, SPLIT>(
-                acc, [&](int m, int k) { return Ws[m * ldk + k]; },
-                [&](int k, int nn) { return Hs[k * kLdh + nn]; }, m0, nh, 2, kDvm, dk, lane);
+            mma::gemm_s<4, SPLIT>(acc, Ws, ldk, 1, nullptr, Hs, kLdh, 1, m0, nh, 2, kDvm, dk,
+                                  lane);
             mma::for_each(acc, m0, nh, 2, kDvm, lane, [&](int r, int cc, float &x) {
                 const float val = Us[r * kLdc + cc] - x;
                 Vn[r * kLdc + cc] = val;
@@ -484,12 +482,10 @@ k_state_mma(FwdArgs a, const float *__restrict__ W, const float *__restrict__ U,
             float a1[4][4], a2[4][4];
             mma::zero(a1);
             mma::zero(a2);
-            mma::warp_gemm<4, SPLIT>(
-                a1, [&](int m, int k) { return Qs[m * ldk + k]; },
-                [&](int k, int nn) { return Hs[k * kLdh + nn]; }, m0, nh, 2, kDvm, dk, lane);
-            mma::warp_gemm<4, SPLIT>(
-                a2, [&](int m, int k) { return P[m * kLdc + k]; },
-                [&](int k, int nn) { return Vn[k * kLdc + nn]; }, m0, nh, 2, kDvm, kChunk, lane);
+            mma::gemm_s<4, SPLIT>(a1, Qs, ldk, 1, nullptr, Hs, kLdh, 1, m0, nh, 2, kDvm, dk,
+                                  lane);
+            mma::gemm_s<4, SPLIT>(a2, P, kLdc, 1, nullptr, Vn, kLdc, 1, m0, nh, 2, kDvm, kChunk,
+                                  lane);
             const int gq = lane >> 2, tq = lane & 3;
 #pragma unroll
             for (int i = 0; i < 4; ++i)
@@ -507,9 +503,8 @@ k_state_mma(FwdArgs a, const float *__restrict__ W, const float *__restrict__ U,
             const int j0 = 16 * (task >> 1), th = task & 1;
             float acc[4][4];
             mma::zero(acc);
-            mma::warp_gemm<4, SPLIT>(
-                acc, [&](int m, int k) { return m < dk ? Ks[k * ldk + m] * e[k] : 0.f; },
-                [&](int k, int nn) { return Vn[k * kLdc + nn]; }, j0, th, 2, kDvm, kChunk, lane);
+            mma::gemm_s<4, SPLIT>(acc, Ks, 1, ldk, e, Vn, kLdc, 1, j0, th, 2, kDvm, kChunk,
+                                  lane);
             mma::for_each(acc, j0, th, 2, kDvm, lane, [&](int j, int cc, float &x) {
                 if (j < dk) Hs[j * kLdh + cc] = fmaf(decay, Hs[j * kLdh + cc], x);
             });
@@ -603,9 +598,7 @@ k_prep_mma(FwdArgs a, const int2 *__restrict__ table, float *__restrict__ W,
     if (erase) {   // A = strictly_lower(diag(beta) G * K K^T)
         float acc[4][4];
         mma::zero(acc);
-        mma::warp_gemm<4, SPLIT>(
-            acc, [&](int m, int k) { return Ks[m * ldk + k]; },
-            [&](int k, int nn) { return Ks[nn * ldk + k]; }, m0, nh, 2, kChunk, dk, lane);
+        mma::gemm_s<4, SPLIT>(acc, Ks, ldk, 1, nullptr, Ks, 1, ldk, m0, nh, 2, kChunk, dk, lane);
         mma::for_each(acc, m0, nh, 2, kChunk, lane, [&](int r, int s, float &x) {
             A[r * kLdc + s] = s < r ? bb[r] * expf(g[r] - g[s]) * x : 0.f;
         });
@@ -674,10 +667,7 @@ k_prep_mma(FwdArgs a, const int2 *__restrict__ table, float *__restrict__ W,
         float acc[8][4];
         mma::zero(acc);
         if (erase)
-            mma::warp_gemm<8, SPLIT>(
-                acc, [&](int m, int k) { return Tm[m * kLdc + k]; },
-                [&](int k, int nn) { return Ks[k * ldk + nn] * wb[k]; }, m0, nh, 2, dk, kChunk,
-                lane);
+            mma::gemm_s<8, SPLIT>(acc, Tm, kLdc, 1, wb, Ks, ldk, 1, m0, nh, 2, dk, kChunk, lane);
         mma::for_each(acc, m0, nh, 2, dk, lane, [&](int r, int j, float &x) {
             if (r < L) W[(r0 + r) * dk + j] = x;
         });
@@ -686,10 +676,8 @@ k_prep_mma(FwdArgs a, const int2 *__restrict__ table, float *__restrict__ W,
         float acc[8][4];
         mma::zero(acc);
         const int ne = min(dv, c0 + 128);
-        mma::warp_gemm<8, SPLIT>(
-            acc, [&](int m, int k) { return Tm[m * kLdc + k]; },
-            [&](int k, int nn) { return Vs[k * ldv + nn] * bb[k]; }, m0, c0 / 8 + nh, 2, ne,
-            kChunk, lane);
+        mma::gemm_s<8, SPLIT>(acc, Tm, kLdc, 1, bb, Vs, ldv, 1, m0, c0 / 8 + nh, 2, ne, kChunk,
+                              lane);
         mma::for_each(acc, m0, c0 / 8 + nh, 2, ne, lane, [&](int r, int j, float &x) {
             if (r < L) U[(r0 + r) * dv + j] = x;
         });
