@@ -47,8 +47,8 @@ GLA_METRIC = ("gated linear attention (no erase term) chunked fwd tokens/s (B·H
               "roofline, bf16, d=128, 1×GB300")
 BWD_METRIC = "GDN chunked bwd tokens/s (B·H·T/s) and % of roofline, bf16, d=128, 1×GB300"
 DEFAULT_WORKLOAD = "gdn_fwd_b4_h16_t4096_d128_bf16"
-# fp32 FMA rate of the CUDA cores: 152 SMs x 128 lanes x 2 FLOP x 2.07 GHz
-ALU_FP32_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+# tf32 tensor rate relative to bf16 (nominal dense figures: 1.1 vs 2.25 PFLOP/s)
+TF32_PER_BF16 = 1.1 / 2.25
 L2_FLUSH_BYTES = 256 << 20
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
@@ -152,8 +152,8 @@ def algorithmic(shape):
 
 
 def algorithmic_bwd(shape):
-    """Compulsory HBM bytes of one backward call and the FLOPs its per-chunk
-    gradient kernel issues.
+    """Compulsory HBM bytes of one backward call and the FLOPs of its per-chunk
+    gradient kernel (one tf32 product each; fp32 I/O issues three).
 
     Bytes: q, k, v, dO read and dq, dk, dv written once at the I/O width, the
     two gates read and their two gradients written (fp32), h0 and dhT read and
@@ -188,7 +188,8 @@ KERNEL_SOURCES = {
     "k_gdn_tc": ["gdn_tc.cu", "tc_ptx.cuh", "gdn_internal.h"],
     "k_gdn_prep": ["gdn_prep.cu", "tc_ptx.cuh", "gdn_internal.h"],
     "k_gdn_decode": ["gdn_decode.cu", "gdn_internal.h"],
-    "k_bwd_chunk": ["gdn_bwd.cu", "gdn_internal.h"],
+    "k_bwd_chunk": ["gdn_bwd.cu", "gdn_internal.h", "gdn_mma.cuh", "gdn_tile.cuh"],
+    "k_state_mma": ["gdn_simt.cu", "gdn_internal.h", "gdn_mma.cuh", "gdn_tile.cuh"],
 }
 
 
@@ -491,15 +492,19 @@ def run_ours(args, world, rank, local):
                      {1: "simt", 2: "tc"}.get(gdn.last_impl(), "none"),
     }
     if BACKWARD:
-        # CUDA-core fp32 kernels: the roof of the dominant one is the fp32 FMA rate
-        alu = flops / (kern_ms * 1e-3) / 1e12
+        # the dominant kernel's products run on tf32 tensor cores (mma.sync):
+        # its roof is the tf32 rate, the measured bf16 peak times the nominal ratio
+        tf32 = tf * TF32_PER_BF16
+        ach = flops / (kern_ms * 1e-3) / 1e12
         res["roofline"] = {
-            "bound": "alu", "achieved": alu, "peak": ALU_FP32_TFLOPS, "unit": "TFLOP/s",
-            "frac": alu / ALU_FP32_TFLOPS,
-            "peak_source": "fp32 FMA: 152 SMs x 128 lanes x 2 FLOP x 2.07 GHz (nominal)",
+            "bound": "tensor", "achieved": ach, "peak": tf32, "unit": "TFLOP/s",
+            "frac": ach / tf32,
+            "peak_source": "tf32 = %s bf16 peak %.1f TFLOP/s x 1.1/2.25 (nominal ratio)"
+                           % (src, tf),
             "traffic": recorded_traffic(k_name, args.workload),
             "kernel": k_name, "kernel_ms": kern_ms, "algorithmic_flops": flops,
             "algorithmic_bytes": by,
+            "issued_tf32_products": 3 if shape["io"] == "f32" else 1,
             "step_hbm_frac": by / (step_ms * 1e-3) / 1e9 / hbm,
         }
         res["config"]["pass"] = "backward (state recomputed)"
