@@ -224,7 +224,7 @@ gdn_status gdn_fwd_varlen_ex(const void *q, const void *k, const void *v,
  *          h0 is NULL), or NULL to skip it.
  *   flags  GDN_FLAG_NO_ERASE differentiates gated linear attention;
  *          GDN_FLAG_VECTOR_GATE gives GDN_ERR_UNSUPPORTED (not built).
- * Device memory, caller-owned; scratch (about 4 (d_k + 3 d_v + 1) bytes
+ * Device memory, caller-owned; scratch (about 4 (d_k + 3 d_v + 65) bytes
  * per token-head plus 8 d_k d_v bytes per chunk-head) comes from the
  * library's pool.  Errors as gdn_fwd; with GDN_IMPL_TC forced the call
  * returns GDN_ERR_UNSUPPORTED (there is no tensor-core backward).
