@@ -156,9 +156,11 @@ k_bwd_dstate(FwdArgs a, BwdArgs b, const float *__restrict__ W, const float *__r
         {
             float acc[4][4];
             mma::zero(acc);
-            mma::gemm_s<4, SPLIT>(acc, Qs, ldk, 1, nullptr, Ks, 1, ldk, m0, nh, 2, kChunk, dk,
+            // tiles right of this warp's diagonal block are masked: not formed
+            // (the P^T dO below reads rows s >= r only, which are)
+            mma::gemm_s<4, SPLIT>(acc, Qs, ldk, 1, nullptr, Ks, 1, ldk, m0, nh, 2, m0 + 16, dk,
                                   lane);
-            mma::for_each(acc, m0, nh, 2, kChunk, lane, [&](int r, int s, float &x) {
+            mma::for_each(acc, m0, nh, 2, m0 + 16, lane, [&](int r, int s, float &x) {
                 P[r * kLdc + s] = s <= r ? expf(g[r] - g[s]) * x : 0.f;
             });
         }
@@ -168,7 +170,7 @@ k_bwd_dstate(FwdArgs a, BwdArgs b, const float *__restrict__ W, const float *__r
             mma::zero(a1);
             mma::zero(a2);
             mma::gemm_s<4, SPLIT>(a1, P, 1, kLdc, nullptr, dOs, kLdc, 1, m0, nh, 2, kDvm, kChunk,
-                                  lane);
+                                  lane, m0);
             mma::gemm_s<4, SPLIT>(a2, Ks, ldk, 1, nullptr, dH, kLdh, 1, m0, nh, 2, kDvm, dk,
                                   lane);
             const int gl4 = lane >> 2, tl = lane & 3;
@@ -399,9 +401,11 @@ k_bwd_chunk(FwdArgs a, BwdArgs b, const int2 *__restrict__ table, const float *_
     if (erase) {   // K K^T
         float acc[kNtC][4];
         mma::zero(acc);
-        mma::gemm_s<kNtC, SPLIT>(acc, Ks, ldk, 1, nullptr, Ks, 1, ldk, m0, nh, 2, kChunk, dk,
+        // K K^T is read below the diagonal only: tiles right of this warp's
+        // diagonal block are not formed
+        mma::gemm_s<kNtC, SPLIT>(acc, Ks, ldk, 1, nullptr, Ks, 1, ldk, m0, nh, 2, m0 + 16, dk,
                                  lane);
-        mma::for_each(acc, m0, nh, 2, kChunk, lane,
+        mma::for_each(acc, m0, nh, 2, m0 + 16, lane,
                       [&](int m, int nn, float &x) { B3[m * kLdc + nn] = x; });
     }
     __syncthreads();
@@ -484,7 +488,7 @@ k_bwd_chunk(FwdArgs a, BwdArgs b, const int2 *__restrict__ table, const float *_
             float acc[kNtV][4];
             mma::zero(acc);
             mma::gemm_s<kNtV, SPLIT>(acc, Tm, 1, kLdc, nullptr, dVs, kLdt, 1, m0, nh, 2, kDvt,
-                                     kChunk, lane);
+                                     kChunk, lane, m0);
             TIn *dvp = static_cast<TIn *>(b.dv);
             mma::for_each(acc, m0, nh, 2, kDvt, lane, [&](int s, int cc, float &x) {
                 if (s < L && cc < nv) st_out(dvp + (r0 + s) * dv + dv0 + cc, bb[s] * x);
@@ -518,16 +522,16 @@ k_bwd_chunk(FwdArgs a, BwdArgs b, const int2 *__restrict__ table, const float *_
     {   // E = dP * (Q K^T): row sums into dg_r, column sums out of dg_s
         float acc[kNtC][4];
         mma::zero(acc);
-        mma::gemm_s<kNtC, SPLIT>(acc, Qs, ldk, 1, nullptr, Ks, 1, ldk, m0, nh, 2, kChunk, dk,
+        mma::gemm_s<kNtC, SPLIT>(acc, Qs, ldk, 1, nullptr, Ks, 1, ldk, m0, nh, 2, m0 + 16, dk,
                                  lane);
         auto ev = [&](int r, int s, float x) { return B1[r * kLdc + s] * x; };
-        add_row_sums(acc, m0, nh, 2, kChunk, lane, ev, dgE, [](int) { return 1.f; });
-        add_col_sums(acc, m0, nh, 2, kChunk, lane, ev, dgE, -1.f);
+        add_row_sums(acc, m0, nh, 2, m0 + 16, lane, ev, dgE, [](int) { return 1.f; });
+        add_col_sums(acc, m0, nh, 2, m0 + 16, lane, ev, dgE, -1.f);
     }
     float tmp[kNtK][4];
     {   // dQ = diag(gamma) dO S0 + dP K;  dg_r += gamma_r q_r . (dO S0)_r
         mma::zero(tmp);
-        mma::gemm_s<kNtK, SPLIT>(tmp, B1, kLdc, 1, nullptr, Ks, ldk, 1, m0, nh, 2, dk, kChunk,
+        mma::gemm_s<kNtK, SPLIT>(tmp, B1, kLdc, 1, nullptr, Ks, ldk, 1, m0, nh, 2, dk, m0 + 16,
                                  lane);
         TIn *dqp = static_cast<TIn *>(b.dq);
 #pragma unroll
@@ -549,7 +553,7 @@ k_bwd_chunk(FwdArgs a, BwdArgs b, const int2 *__restrict__ table, const float *_
         mma::for_each(aK, m0, nh, 2, dk, lane, [&](int s, int, float &x) { x *= ed[s]; });
         mma::zero(tmp);
         mma::gemm_s<kNtK, SPLIT>(tmp, B1, 1, kLdc, nullptr, Qs, ldk, 1, m0, nh, 2, dk, kChunk,
-                                 lane);
+                                 lane, m0);
 #pragma unroll
         for (int i = 0; i < kNtK; ++i)
 #pragma unroll
@@ -557,7 +561,7 @@ k_bwd_chunk(FwdArgs a, BwdArgs b, const int2 *__restrict__ table, const float *_
         if (erase) {
             mma::zero(tmp);
             mma::gemm_s<kNtK, SPLIT>(tmp, Tm, 1, kLdc, nullptr, Wm, ldk, 1, m0, nh, 2, dk, kChunk,
-                                     lane);
+                                     lane, m0);
             // T^T dW = -tmp
             add_row_sums(tmp, m0, nh, 2, dk, lane,
                          [&](int s, int j, float x) { return -Ks[s * ldk + j] * x; }, tv,
@@ -576,9 +580,10 @@ k_bwd_chunk(FwdArgs a, BwdArgs b, const int2 *__restrict__ table, const float *_
         {   // dT = dV'(diag(beta)V)^T - Wm (diag(beta gamma) K)^T, strictly lower part
             float acc[kNtC][4];
             mma::zero(acc);
-            mma::gemm_s<kNtC, SPLIT>(acc, Wm, ldk, 1, nullptr, Ks, 1, ldk, m0, nh, 2, kChunk, dk,
+            // strictly lower part only; B2 is already zero right of the diagonal
+            mma::gemm_s<kNtC, SPLIT>(acc, Wm, ldk, 1, nullptr, Ks, 1, ldk, m0, nh, 2, m0 + 16, dk,
                                      lane);
-            mma::for_each(acc, m0, nh, 2, kChunk, lane, [&](int r, int s, float &x) {
+            mma::for_each(acc, m0, nh, 2, m0 + 16, lane, [&](int r, int s, float &x) {
                 B2[r * kLdc + s] = s < r ? B2[r * kLdc + s] - bb[s] * gm[s] * x : 0.f;
             });
         }
@@ -587,7 +592,7 @@ k_bwd_chunk(FwdArgs a, BwdArgs b, const int2 *__restrict__ table, const float *_
             float acc[kNtC][4];
             mma::zero(acc);
             mma::gemm_s<kNtC, SPLIT>(acc, B2, kLdc, 1, nullptr, Tm, 1, kLdc, m0, nh, 2, kChunk,
-                                     kChunk, lane);
+                                     m0 + 16, lane);
             mma::for_each(acc, m0, nh, 2, kChunk, lane,
                           [&](int r, int s, float &x) { B1[r * kLdc + s] = x; });
         }
@@ -595,23 +600,24 @@ k_bwd_chunk(FwdArgs a, BwdArgs b, const int2 *__restrict__ table, const float *_
         {   // X = dA * G with dA = -T^T Z (strictly lower), into B2; Y = X * K K^T
             float acc[kNtC][4];
             mma::zero(acc);
-            mma::gemm_s<kNtC, SPLIT>(acc, Tm, 1, kLdc, nullptr, B1, kLdc, 1, m0, nh, 2, kChunk,
-                                     kChunk, lane);
-            mma::for_each(acc, m0, nh, 2, kChunk, lane, [&](int r, int s, float &x) {
+            // strictly lower part only; B2 (dT) is already zero right of the diagonal
+            mma::gemm_s<kNtC, SPLIT>(acc, Tm, 1, kLdc, nullptr, B1, kLdc, 1, m0, nh, 2, m0 + 16,
+                                     kChunk, lane, m0);
+            mma::for_each(acc, m0, nh, 2, m0 + 16, lane, [&](int r, int s, float &x) {
                 x = s < r ? -x * expf(g[r] - g[s]) : 0.f;
                 B2[r * kLdc + s] = x;
             });
             auto yv = [&](int r, int s, float x) { return x * B3[r * kLdc + s]; };
-            add_row_sums(acc, m0, nh, 2, kChunk, lane, yv, dbA, [](int) { return 1.f; });
-            add_row_sums(acc, m0, nh, 2, kChunk, lane, yv, dgA, [&](int r) { return bb[r]; });
-            add_col_sums(acc, m0, nh, 2, kChunk, lane,
+            add_row_sums(acc, m0, nh, 2, m0 + 16, lane, yv, dbA, [](int) { return 1.f; });
+            add_row_sums(acc, m0, nh, 2, m0 + 16, lane, yv, dgA, [&](int r) { return bb[r]; });
+            add_col_sums(acc, m0, nh, 2, m0 + 16, lane,
                          [&](int r, int s, float x) { return bb[r] * x * B3[r * kLdc + s]; },
                          dgA, -1.f);
         }
         __syncthreads();
         {   // dK_r += beta_r (X K)_r + ((X * beta_row)^T K)_r
             mma::zero(tmp);
-            mma::gemm_s<kNtK, SPLIT>(tmp, B2, kLdc, 1, nullptr, Ks, ldk, 1, m0, nh, 2, dk, kChunk,
+            mma::gemm_s<kNtK, SPLIT>(tmp, B2, kLdc, 1, nullptr, Ks, ldk, 1, m0, nh, 2, dk, m0 + 16,
                                      lane);
             mma::for_each(tmp, m0, nh, 2, dk, lane, [&](int r, int, float &x) { x *= bb[r]; });
 #pragma unroll
@@ -620,7 +626,7 @@ k_bwd_chunk(FwdArgs a, BwdArgs b, const int2 *__restrict__ table, const float *_
                 for (int e = 0; e < 4; ++e) aK[i][e] += tmp[i][e];
             mma::zero(tmp);
             mma::gemm_s<kNtK, SPLIT>(tmp, B2, 1, kLdc, bb, Ks, ldk, 1, m0, nh, 2, dk, kChunk,
-                                     lane);
+                                     lane, m0);
 #pragma unroll
             for (int i = 0; i < kNtK; ++i)
 #pragma unroll

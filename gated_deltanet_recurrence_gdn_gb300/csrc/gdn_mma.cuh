@@ -97,21 +97,24 @@ __device__ __forceinline__ void warp_gemm(float (&acc)[NT][4], FA A, FB B, int m
 }
 
 // The same product with strided operands: A(m, k) = pa[m * sam + k * sak]
-// (times ascale[k] when ascale is non-null) and B(k, n) = pb[k * sbk + n * sbn];
-// the per-thread element pointers are formed once, the k loop only adds.
+// (times ascale[k] when ascale is non-null) and B(k, n) = pb[k * sbk + n * sbn],
+// k over [kb, K) (both multiples of 8: a triangular operand skips its zero
+// blocks); the per-thread element pointers are formed once, the k loop only
+// adds.
 template <int NT, bool SPLIT>
 __device__ __forceinline__ void gemm_s(float (&acc)[NT][4], const float *pa, int sam, int sak,
                                        const float *ascale, const float *pb, int sbk, int sbn,
-                                       int m0, int nt0, int nstep, int n_end, int K, int lane) {
+                                       int m0, int nt0, int nstep, int n_end, int K, int lane,
+                                       int kb = 0) {
     const int g = lane >> 2, t = lane & 3;
-    const float *a0 = pa + (m0 + g) * sam + t * sak;
+    const float *a0 = pa + (m0 + g) * sam + (kb + t) * sak;
     const float *a1 = a0 + 8 * sam;
     const float *bp[NT];
 #pragma unroll
-    for (int i = 0; i < NT; ++i) bp[i] = pb + t * sbk + (8 * (nt0 + i * nstep) + g) * sbn;
+    for (int i = 0; i < NT; ++i) bp[i] = pb + (kb + t) * sbk + (8 * (nt0 + i * nstep) + g) * sbn;
     const int ak4 = 4 * sak, bk4 = 4 * sbk, ak8 = 8 * sak, bk8 = 8 * sbk;
 #pragma unroll 2
-    for (int k0 = 0; k0 < K; k0 += 8) {
+    for (int k0 = kb; k0 < K; k0 += 8) {
         float v0 = a0[0], v1 = a1[0], v2 = a0[ak4], v3 = a1[ak4];
         if (ascale) {
             const float s0 = ascale[k0 + t], s1 = ascale[k0 + t + 4];

@@ -460,9 +460,10 @@ k_state_mma(FwdArgs a, const float *__restrict__ W, const float *__restrict__ U,
         if (op) {   // P_rs = G_rs q_r . k_s, s <= r
             float acc[4][4];
             mma::zero(acc);
-            mma::gemm_s<4, SPLIT>(acc, Qs, ldk, 1, nullptr, Ks, 1, ldk, m0, nh, 2, kChunk, dk,
+            // tiles right of this warp's diagonal block are masked: not formed
+            mma::gemm_s<4, SPLIT>(acc, Qs, ldk, 1, nullptr, Ks, 1, ldk, m0, nh, 2, m0 + 16, dk,
                                   lane);
-            mma::for_each(acc, m0, nh, 2, kChunk, lane, [&](int r, int s, float &x) {
+            mma::for_each(acc, m0, nh, 2, m0 + 16, lane, [&](int r, int s, float &x) {
                 P[r * kLdc + s] = s <= r ? expf(g[r] - g[s]) * x : 0.f;
             });
         }
@@ -484,7 +485,7 @@ k_state_mma(FwdArgs a, const float *__restrict__ W, const float *__restrict__ U,
             mma::zero(a2);
             mma::gemm_s<4, SPLIT>(a1, Qs, ldk, 1, nullptr, Hs, kLdh, 1, m0, nh, 2, kDvm, dk,
                                   lane);
-            mma::gemm_s<4, SPLIT>(a2, P, kLdc, 1, nullptr, Vn, kLdc, 1, m0, nh, 2, kDvm, kChunk,
+            mma::gemm_s<4, SPLIT>(a2, P, kLdc, 1, nullptr, Vn, kLdc, 1, m0, nh, 2, kDvm, m0 + 16,
                                   lane);
             const int gq = lane >> 2, tq = lane & 3;
 #pragma unroll
@@ -598,8 +599,10 @@ k_prep_mma(FwdArgs a, const int2 *__restrict__ table, float *__restrict__ W,
     if (erase) {   // A = strictly_lower(diag(beta) G * K K^T)
         float acc[4][4];
         mma::zero(acc);
-        mma::gemm_s<4, SPLIT>(acc, Ks, ldk, 1, nullptr, Ks, 1, ldk, m0, nh, 2, kChunk, dk, lane);
-        mma::for_each(acc, m0, nh, 2, kChunk, lane, [&](int r, int s, float &x) {
+        // only the strictly lower part of A is ever read: tiles right of this
+        // warp's diagonal block are not formed
+        mma::gemm_s<4, SPLIT>(acc, Ks, ldk, 1, nullptr, Ks, 1, ldk, m0, nh, 2, m0 + 16, dk, lane);
+        mma::for_each(acc, m0, nh, 2, m0 + 16, lane, [&](int r, int s, float &x) {
             A[r * kLdc + s] = s < r ? bb[r] * expf(g[r] - g[s]) * x : 0.f;
         });
     } else {
@@ -667,7 +670,7 @@ k_prep_mma(FwdArgs a, const int2 *__restrict__ table, float *__restrict__ W,
         float acc[8][4];
         mma::zero(acc);
         if (erase)
-            mma::gemm_s<8, SPLIT>(acc, Tm, kLdc, 1, wb, Ks, ldk, 1, m0, nh, 2, dk, kChunk, lane);
+            mma::gemm_s<8, SPLIT>(acc, Tm, kLdc, 1, wb, Ks, ldk, 1, m0, nh, 2, dk, m0 + 16, lane);
         mma::for_each(acc, m0, nh, 2, dk, lane, [&](int r, int j, float &x) {
             if (r < L) W[(r0 + r) * dk + j] = x;
         });
@@ -676,7 +679,7 @@ k_prep_mma(FwdArgs a, const int2 *__restrict__ table, float *__restrict__ W,
         float acc[8][4];
         mma::zero(acc);
         const int ne = min(dv, c0 + 128);
-        mma::gemm_s<8, SPLIT>(acc, Tm, kLdc, 1, bb, Vs, ldv, 1, m0, c0 / 8 + nh, 2, ne, kChunk,
+        mma::gemm_s<8, SPLIT>(acc, Tm, kLdc, 1, bb, Vs, ldv, 1, m0, c0 / 8 + nh, 2, ne, m0 + 16,
                               lane);
         mma::for_each(acc, m0, c0 / 8 + nh, 2, ne, lane, [&](int r, int j, float &x) {
             if (r < L) U[(r0 + r) * dv + j] = x;
