@@ -42,6 +42,9 @@ WORKLOADS = {
     "gdn_fwd_varlen_n64_h32_dk128_dv256_bf16": dict(N=64, len_min=128, len_max=16384, H=32,
                                                     dk=128, dv=256, io="bf16", decay="fast",
                                                     h0_std=0.02, seed=5),
+    # the headline batch at a quarter of its length: the case ncu captures run on
+    "gdn_fwd_b4_h16_t1024_d128_bf16": dict(B=4, H=16, T=1024, dk=128, dv=128, io="bf16",
+                                           decay="fast", h0_std=0.0, seed=7),
     # one decode step over 256 sequences x 32 heads: 537 MB of fp32 state
     "gdn_decode_b256_h32_d128_bf16": dict(kind="decode", B=256, H=32, dk=128, dv=128,
                                           io="bf16", decay="fast", state_std=0.02, seed=6),
