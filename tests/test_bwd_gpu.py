@@ -137,3 +137,33 @@ def test_bwd_vector_gate_and_forced_tc_are_unsupported():
         with pytest.raises(gdn.GdnError) as e:
             gdn.gdn_bwd(x.q, x.k, x.v, x.log_alpha, x.beta, None, dout, dhT)
     assert e.value.status == gdn.GDN_ERR_UNSUPPORTED
+
+
+def test_bwd_long_sequence_adjoint_identity():
+    # 256 chunks per head: the state adjoint crosses many chunk boundaries.
+    # <dO, O> + <dhT, hT> = <dV, V> + <dh0, h0> and <dO, O> = <dq, q> hold for
+    # the exact gradient at any length (the fp64 oracle, which keeps every
+    # state, would need 17 GB per head here).
+    x = synth.make_dense(1, 2, 16384, 128, 128, io="bf16", decay="slow", h0_std=0.05, seed=81,
+                         device="cuda")
+    dout, dhT = _weights(x, 82)
+    o, hT = gdn.gdn_fwd(x.q, x.k, x.v, x.log_alpha, x.beta, x.h0)
+    dq, _, dv, _, _, dh0 = gdn.gdn_bwd(x.q, x.k, x.v, x.log_alpha, x.beta, x.h0, dout, dhT,
+                                       check=True)
+    U.sync()
+    f = lambda a, b: float((a.double() * b.double()).sum())
+    L_o, L_h = f(dout, o), f(dhT, hT)
+    assert abs(L_o + L_h - f(dv, x.v) - f(dh0, x.h0)) <= 2e-2 * (abs(L_o) + abs(L_h))
+    assert abs(L_o - f(dq, x.q)) <= 2e-2 * abs(L_o)
+
+
+def test_bwd_varlen_without_h0_or_dhT_fp32():
+    y = synth.make_varlen([5, 64, 0, 150], 3, 64, 32, io="f32", seed=83, device="cuda")
+    dout = torch.randn(y.v.shape, generator=torch.Generator(device="cuda").manual_seed(84),
+                       device="cuda")
+    got = gdn.gdn_bwd_varlen(y.q, y.k, y.v, y.log_alpha, y.beta, y.cu_seqlens, None, dout,
+                             None, check=True)
+    U.sync()
+    ref = oracle.gdn_bwd_varlen(U.f64(y.q), U.f64(y.k), U.f64(y.v), U.f64(y.log_alpha),
+                                U.f64(y.beta), y.cu_seqlens.cpu().numpy(), None, U.f64(dout))
+    _compare(got, ref, "f32")

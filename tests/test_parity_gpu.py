@@ -200,6 +200,16 @@ def test_workload_b4_h16_t4096_d128_full(impl):
     check(o, hT, o_ref.reshape(o.shape), h_ref.reshape(hT.shape), "bf16")
 
 
+def test_fp32_io_b4_h16_t1024_d128_full():
+    # the general path with fp32 I/O (three tf32 products per step) at the
+    # headline batch's width over 16 chunks per head, every head and token
+    x = synth.make_dense(4, 16, 1024, 128, 128, io="f32", h0_std=0.02, seed=29, device="cuda")
+    o, hT = run_dense(x, "auto")
+    assert gdn.load().gdn_last_impl() == gdn.GDN_IMPL_SIMT
+    o_ref, h_ref = U.oracle_dense(x)
+    check(o, hT, o_ref.reshape(o.shape), h_ref.reshape(hT.shape), "f32")
+
+
 def test_workload_b8_h8_t8192_d64_h0_full():
     x = synth.make_workload("gdn_fwd_b8_h8_t8192_d64_bf16_h0", device="cuda")
     o, hT = run_dense(x, "auto")
