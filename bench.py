@@ -2,6 +2,7 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload NAME] [--no-cpu-baseline] [--no-erase] [--backward]
+                    [--vector-gate]
 
 One step = one gdn_fwd call (every stage of the chunked forward pass) over the
 whole synthetic batch of the workload (default: B=4, H=16, T=4096,
@@ -16,8 +17,9 @@ slowest rank's time is reported.
 workload on the host cores (rank 0 only).
 
 --no-erase times gated linear attention (the recurrence without the erase
-term); --backward times the backward pass (gdn_bwd: the gradient of
-sum(dO * o) + sum(dhT * hT) for fixed seeded weights dO, dhT) instead.
+term); --vector-gate draws a forget gate per key dimension; --backward times
+the backward pass (gdn_bwd: the gradient of sum(dO * o) + sum(dhT * hT) for
+fixed seeded weights dO, dhT) instead.
 """
 from __future__ import annotations
 
@@ -45,6 +47,8 @@ UNIT = "tokens/s"
 DECODE_METRIC = "GDN decode step tokens/s (B·H/s) and % of roofline, bf16, d=128, 1×GB300"
 GLA_METRIC = ("gated linear attention (no erase term) chunked fwd tokens/s (B·H·T/s) and % of "
               "roofline, bf16, d=128, 1×GB300")
+VG_METRIC = ("GDN chunked fwd with a forget gate per key dimension tokens/s (B·H·T/s) and % of "
+             "roofline, bf16, d=128, 1×GB300")
 BWD_METRIC = "GDN chunked bwd tokens/s (B·H·T/s) and % of roofline, bf16, d=128, 1×GB300"
 DEFAULT_WORKLOAD = "gdn_fwd_b4_h16_t4096_d128_bf16"
 # tf32 tensor rate relative to bf16 (nominal dense figures: 1.1 vs 2.25 PFLOP/s)
@@ -62,6 +66,8 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--vector-gate", action="store_true",
+                    help="a forget gate per key dimension (log_alpha [.., T, d_k])")
     ap.add_argument("--backward", action="store_true",
                     help="time the backward pass (gdn_bwd) instead of the forward")
     ap.add_argument("--no-erase", action="store_true",
@@ -146,7 +152,8 @@ def algorithmic(shape):
         return th * ((2 * dk + 2 * dv) * io + 8 + 2 * dk * dv * 4), th * 6 * dk * dv
     seqheads = shape["N"] * shape["H"]
     state = seqheads * dk * dv * 4
-    by = th * ((2 * dk + 2 * dv) * io + 8) + state * (2 if shape["h0"] else 1)
+    gates = 4 * (1 + dk) if VECTOR_GATE else 8
+    by = th * ((2 * dk + 2 * dv) * io + gates) + state * (2 if shape["h0"] else 1)
     flops = th * (6 * C * dk + 4 * C * dv + 6 * dk * dv)
     return by, flops
 
@@ -190,6 +197,7 @@ KERNEL_SOURCES = {
     "k_gdn_decode": ["gdn_decode.cu", "gdn_internal.h"],
     "k_bwd_chunk": ["gdn_bwd.cu", "gdn_internal.h", "gdn_mma.cuh", "gdn_tile.cuh"],
     "k_state_mma": ["gdn_simt.cu", "gdn_internal.h", "gdn_mma.cuh", "gdn_tile.cuh"],
+    "k_state_vg": ["gdn_simt.cu", "gdn_internal.h", "gdn_mma.cuh", "gdn_tile.cuh"],
 }
 
 
@@ -283,6 +291,8 @@ class ClockSampler:
 
 
 def make_inputs(name, device):
+    if VECTOR_GATE:
+        return synth.make_workload(name, device=device, vector_gate=True)
     return synth.make_workload(name, device=device)
 
 
@@ -293,6 +303,8 @@ def is_decode(x):
 def metric_for(shape):
     if BACKWARD:
         return BWD_METRIC
+    if VECTOR_GATE:
+        return VG_METRIC
     if NO_ERASE:
         return GLA_METRIC
     return DECODE_METRIC if shape["kind"] == "decode" else METRIC
@@ -300,6 +312,7 @@ def metric_for(shape):
 
 NO_ERASE = False   # set from --no-erase
 BACKWARD = False   # set from --backward
+VECTOR_GATE = False   # set from --vector-gate
 _BWD_WEIGHTS = {}
 
 
@@ -404,7 +417,7 @@ def run_ours(args, world, rank, local):
         d2h = sum(t.numel() * t.element_size() for t in g_host)
     e2e_steps = max(3, min(args.steps, 10))
 
-    dense = shape["kind"] == "dense" and not NO_ERASE and not BACKWARD
+    dense = shape["kind"] == "dense" and not (NO_ERASE or BACKWARD or VECTOR_GATE)
 
     def e2e_step():
         if BACKWARD:
@@ -491,7 +504,7 @@ def run_ours(args, world, rank, local):
         "impl_used": "decode" if shape["kind"] == "decode" else
                      {1: "simt", 2: "tc"}.get(gdn.last_impl(), "none"),
     }
-    if BACKWARD:
+    if BACKWARD or VECTOR_GATE:
         # the dominant kernel's products run on tf32 tensor cores (mma.sync):
         # its roof is the tf32 rate, the measured bf16 peak times the nominal ratio
         tf32 = tf * TF32_PER_BF16
@@ -507,7 +520,8 @@ def run_ours(args, world, rank, local):
             "issued_tf32_products": 3 if shape["io"] == "f32" else 1,
             "step_hbm_frac": by / (step_ms * 1e-3) / 1e9 / hbm,
         }
-        res["config"]["pass"] = "backward (state recomputed)"
+        res["config"]["pass"] = ("backward (state recomputed)" if BACKWARD
+                                 else "forward, a forget gate per key dimension")
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(args.workload, x, args.cpu_seconds)
     elif rank == 0 and world == 1:
@@ -562,7 +576,7 @@ def oracle_sample(name, x, budget_s, max_heads=None):
                 oracle.gdn_bwd(*args, h0, f64(dout[s])[None, None], f64(dhT[n, h])[None, None],
                                erase=not NO_ERASE)
             else:
-                oracle.gdn_fwd(*args, h0, erase=not NO_ERASE)
+                oracle.gdn_fwd(*args, h0, erase=not NO_ERASE, vector_gate=VECTOR_GATE)
             return b - a, time.perf_counter() - t0
     else:
         units = [(b, h) for b in range(x.q.shape[0]) for h in range(x.q.shape[1])]
@@ -572,7 +586,7 @@ def oracle_sample(name, x, budget_s, max_heads=None):
             args = [f64(t[b, h])[None, None] for t in (x.q, x.k, x.v, x.log_alpha, x.beta)]
             h0 = None if x.h0 is None else f64(x.h0[b, h])[None, None]
             t0 = time.perf_counter()
-            oracle.gdn_fwd(*args, h0, erase=not NO_ERASE)
+            oracle.gdn_fwd(*args, h0, erase=not NO_ERASE, vector_gate=VECTOR_GATE)
             return x.q.shape[2], time.perf_counter() - t0
 
     toks, secs, used = 0, 0.0, 0
@@ -626,10 +640,13 @@ def run_reference(args, world, rank):
 
 
 def main():
-    global NO_ERASE, BACKWARD
+    global NO_ERASE, BACKWARD, VECTOR_GATE
     args = parse()
     NO_ERASE = args.no_erase
     BACKWARD = args.backward
+    VECTOR_GATE = args.vector_gate
+    if VECTOR_GATE and (BACKWARD or synth.WORKLOADS[args.workload].get("kind") == "decode"):
+        raise SystemExit("--vector-gate times the chunked forward only")
     if BACKWARD and synth.WORKLOADS[args.workload].get("kind") == "decode":
         raise SystemExit("--backward needs a chunked workload")
     world, rank, local = dist_setup(args.gpus)

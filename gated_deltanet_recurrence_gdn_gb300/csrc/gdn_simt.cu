@@ -1,16 +1,19 @@
-// gdn_simt.cu -- chunked gated delta rule on CUDA cores, fp32 arithmetic.
+// gdn_simt.cu -- the general path: fp32 I/O, widths the tcgen05 kernels do
+// not cover, the allocation-free entry point, gates per key dimension, and
+// the backward pass's recomputation.
 //
-// This is the path for fp32 I/O and for shapes the tensor-core kernels do not
-// cover.  It follows the chunked method of "Gated DeltaNet GPU并行实现"
-// section 3.2: inside a chunk everything is a small dense product, across
-// chunks a serial pass carries the state.  Two kernels:
+// It follows the chunked method of "Gated DeltaNet GPU并行实现" section 3.2:
+// inside a chunk everything is a small dense product, across chunks a serial
+// pass carries the state.  The products run on the tensor cores as warp-level
+// tf32 mma.sync (gdn_mma.cuh; three products per step, the 3xTF32 split, for
+// fp32 I/O).  Two kernels per gate kind:
 //
 //   prep  (one CTA per (chunk, head), all chunks in parallel):
 //         g_r   = sum_{i<=r} log_alpha_i inside the chunk        (gate cumsum)
 //         A_rs  = beta_r exp(g_r - g_s) (k_r . k_s),  s < r        (decayed Gram)
-//         T     = (I + A)^{-1}  by column-wise forward substitution
+//         T     = (I + A)^{-1}  (16 x 16 blocks, then merged)
 //         W     = T diag(beta exp(g)) K,   U = T diag(beta) V       (WY factors)
-//   state (one CTA per (sequence, head, 32-wide d_v tile), chunks in order):
+//   state (one CTA per (sequence, head, 64-wide d_v tile), chunks in order):
 //         with H = S^T (d_k x d_v) at the chunk start,
 //         V'    = U - W H
 //         O     = diag(exp(g)) Q H + [mask_{s<=r} exp(g_r - g_s) Q K^T] V'
@@ -27,6 +30,7 @@
 // and log_alpha = 0, which leaves every real row unchanged.
 #include <cuda_bf16.h>
 
+#include <algorithm>
 #include <mutex>
 #include <type_traits>
 
@@ -38,10 +42,7 @@ namespace gdn {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kDvt = 32;  // d_v columns per state-pass CTA
 
-__device__ __forceinline__ float ld_in(const float *p) { return __ldg(p); }
-__device__ __forceinline__ float ld_in(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
 __device__ __forceinline__ void st_out(float *p, float x) { *p = x; }
 __device__ __forceinline__ void st_out(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
 
@@ -95,282 +96,12 @@ __global__ void k_chunk_table(const int32_t *cu, int N, int T_total, int2 *table
     if (tid == 0 && s_bad) set_error(err, kErrBadIndex);
 }
 
-template <typename TIn>
-__global__ void __launch_bounds__(kThreads)
-k_simt_prep(FwdArgs a, const int2 *__restrict__ table, float *__restrict__ W,
-            float *__restrict__ U, float *__restrict__ G, int *err) {
-    extern __shared__ float smem[];
-    const int dk = a.dk, dv = a.dv, tid = threadIdx.x;
-    int n, c;
-    if (table) {
-        int2 e = table[blockIdx.x];
-        n = e.x;
-        c = e.y;
-        if (n < 0) return;
-    } else {
-        n = blockIdx.x / a.max_chunks;
-        c = blockIdx.x % a.max_chunks;
-    }
-    const int h = blockIdx.y;
-    if (!seq_ok(a.sm, n)) {
-        if (tid == 0) set_error(err, kErrBadIndex);
-        return;
-    }
-    long long row0;
-    int len;
-    a.sm.get(n, h, row0, len);
-    const int t0 = c * kChunk;
-    if (t0 >= len) return;
-    const int L = min(kChunk, len - t0);
-    const long long r0 = row0 + t0;
-    const int ks = dk + 1, vs = dv + 1;
-    float *Ks = smem;                 // [64][dk+1]
-    float *Vs = Ks + kChunk * ks;     // [64][dv+1]
-    float *A = Vs + kChunk * vs;      // [64][65]
-    float *Tm = A + kChunk * 65;      // [64][65]
-    float *g = Tm + kChunk * 65;      // [64] gate cumsum
-    float *bb = g + kChunk;           // [64] beta
-    float *wb = bb + kChunk;          // [64] beta * exp(g)
-    float *Gv = wb + kChunk;          // [64][dk+1] per-dimension gate cumsum (vector gate)
-    const bool vg = a.vector_gate;
-    const TIn *kp = static_cast<const TIn *>(a.k);
-    const TIn *vp = static_cast<const TIn *>(a.v);
-
-    if (tid < kChunk) {
-        const bool ok = tid < L;
-        g[tid] = (ok && !vg) ? __ldg(a.log_alpha + r0 + tid) : 0.f;
-        bb[tid] = ok ? __ldg(a.beta + r0 + tid) : 0.f;
-    }
-    if (vg)
-        for (int i = tid; i < kChunk * dk; i += kThreads) {
-            const int r = i / dk, j = i - r * dk;
-            Gv[r * ks + j] = r < L ? __ldg(a.log_alpha + (r0 + r) * dk + j) : 0.f;
-        }
-    for (int i = tid; i < kChunk * dk; i += kThreads) {
-        const int r = i / dk, j = i - r * dk;
-        Ks[r * ks + j] = r < L ? ld_in(kp + (r0 + r) * dk + j) : 0.f;
-    }
-    for (int i = tid; i < kChunk * dv; i += kThreads) {
-        const int r = i / dv, j = i - r * dv;
-        Vs[r * vs + j] = r < L ? ld_in(vp + (r0 + r) * dv + j) : 0.f;
-    }
-    __syncthreads();
-    if (tid == 0) {
-        float s = 0.f;
-        for (int r = 0; r < kChunk; ++r) {
-            s += g[r];
-            g[r] = s;
-        }
-    }
-    if (vg && tid < dk) {   // column tid of the per-dimension cumsum
-        float s = 0.f;
-        for (int r = 0; r < kChunk; ++r) {
-            s += Gv[r * ks + tid];
-            Gv[r * ks + tid] = s;
-        }
-    }
-    __syncthreads();
-    // A: the beta-weighted decayed Gram of the erase term (zero without it,
-    // which leaves T = I, U = diag(beta) V and W = 0)
-    for (int i = tid; i < kChunk * kChunk; i += kThreads) {
-        const int r = i >> 6, s = i & 63;
-        float val = 0.f;
-        if (s < r && !a.no_erase) {
-            float acc = 0.f;
-            if (vg) {   // the decay from s to r taken per key dimension
-                for (int j = 0; j < dk; ++j)
-                    acc = fmaf(Ks[r * ks + j] * expf(Gv[r * ks + j] - Gv[s * ks + j]),
-                               Ks[s * ks + j], acc);
-                val = bb[r] * acc;
-            } else {
-                for (int j = 0; j < dk; ++j) acc = fmaf(Ks[r * ks + j], Ks[s * ks + j], acc);
-                val = bb[r] * expf(g[r] - g[s]) * acc;  // s < r: g_r <= g_s, no overflow
-            }
-        }
-        A[r * 65 + s] = val;
-    }
-    if (tid < kChunk) wb[tid] = bb[tid] * expf(g[tid]);
-    __syncthreads();
-    if (tid < kChunk) {  // column tid of T = (I + A)^{-1}
-        const int cc = tid;
-        for (int r = 0; r <= cc; ++r) Tm[r * 65 + cc] = (r == cc) ? 1.f : 0.f;
-        for (int r = cc + 1; r < kChunk; ++r) {
-            float acc = 0.f;
-            for (int s = cc; s < r; ++s) acc = fmaf(A[r * 65 + s], Tm[s * 65 + cc], acc);
-            Tm[r * 65 + cc] = -acc;
-        }
-    }
-    __syncthreads();
-    for (int i = tid; i < L * dk; i += kThreads) {
-        const int r = i / dk, j = i - r * dk;
-        float acc = 0.f;
-        if (!a.no_erase) {
-            if (vg)   // W = T diag(beta) (K * gamma), gamma per key dimension
-                for (int s = 0; s <= r; ++s)
-                    acc = fmaf(Tm[r * 65 + s] * bb[s] * expf(Gv[s * ks + j]), Ks[s * ks + j], acc);
-            else
-                for (int s = 0; s <= r; ++s)
-                    acc = fmaf(Tm[r * 65 + s] * wb[s], Ks[s * ks + j], acc);
-        }
-        W[(r0 + r) * dk + j] = acc;
-    }
-    for (int i = tid; i < L * dv; i += kThreads) {
-        const int r = i / dv, j = i - r * dv;
-        float acc = 0.f;
-        for (int s = 0; s <= r; ++s) acc = fmaf(Tm[r * 65 + s] * bb[s], Vs[s * vs + j], acc);
-        U[(r0 + r) * dv + j] = acc;
-    }
-    if (vg) {
-        for (int i = tid; i < L * dk; i += kThreads) {
-            const int r = i / dk, j = i - r * dk;
-            G[(r0 + r) * dk + j] = Gv[r * ks + j];
-        }
-    } else if (tid < L) {
-        G[r0 + tid] = g[tid];
-    }
-}
-
-template <typename TIn>
-__global__ void __launch_bounds__(kThreads)
-k_simt_state(FwdArgs a, const float *__restrict__ W, const float *__restrict__ U,
-             const float *__restrict__ G, float *__restrict__ Hst, float *__restrict__ Vout,
-             int *err) {
-    extern __shared__ float smem[];
-    const int dk = a.dk, dv = a.dv, tid = threadIdx.x;
-    const int n = blockIdx.x, h = blockIdx.y, dv0 = blockIdx.z * kDvt;
-    const int nv = min(kDvt, dv - dv0);
-    if (!seq_ok(a.sm, n)) {
-        if (tid == 0) set_error(err, kErrBadIndex);
-        return;
-    }
-    long long row0;
-    int len;
-    a.sm.get(n, h, row0, len);
-    const int ks = dk + 1, us = kDvt + 1;
-    float *Hs = smem;                    // [dk][32]   H = S^T tile
-    float *Ks = Hs + dk * kDvt;          // [64][dk+1]
-    float *Qs = Ks + kChunk * ks;        // [64][dk+1]
-    float *Ws = Qs + kChunk * ks;        // [64][dk+1]
-    float *Us = Ws + kChunk * ks;        // [64][33]
-    float *Vn = Us + kChunk * us;        // [64][33]
-    float *P = Vn + kChunk * us;         // [64][65]
-    float *g = P + kChunk * 65;          // [64]
-    float *e = g + kChunk;               // [64] exp(g_C - g_r)
-    float *Gv = e + kChunk;              // [64][dk+1] per-dimension cumsum (vector gate)
-    const bool vg = a.vector_gate;
-    const TIn *qp = static_cast<const TIn *>(a.q);
-    const TIn *kp = static_cast<const TIn *>(a.k);
-    TIn *op = static_cast<TIn *>(a.o);
-    const long long sbase = ((long long)n * a.sm.H + h) * dv;  // state row of (n, h)
-
-    for (int i = tid; i < dk * kDvt; i += kThreads) {
-        const int j = i / kDvt, cc = i - j * kDvt;
-        Hs[i] = (a.h0 && cc < nv) ? __ldg(a.h0 + (sbase + dv0 + cc) * dk + j) : 0.f;
-    }
-    const int nch = (len + kChunk - 1) / kChunk;
-    for (int c = 0; c < nch; ++c) {
-        const int t0 = c * kChunk, L = min(kChunk, len - t0);
-        const long long r0 = row0 + t0;
-        __syncthreads();  // previous chunk fully consumed
-        if (Hst) {   // the chunk's starting state, [d_k][d_v] per chunk slot
-            float *dst = Hst + ((long long)h * a.chunk_slots + a.chunk_slot(n, c)) * dk * dv;
-            for (int i = tid; i < dk * kDvt; i += kThreads) {
-                const int j = i / kDvt, cc = i - j * kDvt;
-                if (cc < nv) dst[(long long)j * dv + dv0 + cc] = Hs[i];
-            }
-        }
-        for (int i = tid; i < kChunk * dk; i += kThreads) {
-            const int r = i / dk, j = i - r * dk;
-            const bool ok = r < L;
-            Ks[r * ks + j] = ok ? ld_in(kp + (r0 + r) * dk + j) : 0.f;
-            Qs[r * ks + j] = ok ? ld_in(qp + (r0 + r) * dk + j) : 0.f;
-            Ws[r * ks + j] = ok ? __ldg(W + (r0 + r) * dk + j) : 0.f;
-        }
-        for (int i = tid; i < kChunk * kDvt; i += kThreads) {
-            const int r = i / kDvt, cc = i - r * kDvt;
-            Us[r * us + cc] = (r < L && cc < nv) ? __ldg(U + (r0 + r) * dv + dv0 + cc) : 0.f;
-        }
-        if (vg) {   // rows past the sequence repeat its last cumulative gate
-            for (int i = tid; i < kChunk * dk; i += kThreads) {
-                const int r = i / dk, j = i - r * dk;
-                Gv[r * ks + j] = __ldg(G + (r0 + min(r, L - 1)) * dk + j);
-            }
-        } else if (tid < kChunk) {
-            g[tid] = __ldg(G + r0 + min(tid, L - 1));
-        }
-        __syncthreads();
-        const float gl = vg ? 0.f : g[kChunk - 1];
-        if (tid < kChunk && !vg) e[tid] = expf(gl - g[tid]);
-        for (int i = tid; i < kChunk * kChunk; i += kThreads) {
-            const int r = i >> 6, s = i & 63;
-            float val = 0.f;
-            if (s <= r) {
-                float acc = 0.f;
-                if (vg) {
-                    for (int j = 0; j < dk; ++j)
-                        acc = fmaf(Qs[r * ks + j] * expf(Gv[r * ks + j] - Gv[s * ks + j]),
-                                   Ks[s * ks + j], acc);
-                    val = acc;
-                } else {
-                    for (int j = 0; j < dk; ++j) acc = fmaf(Qs[r * ks + j], Ks[s * ks + j], acc);
-                    val = expf(g[r] - g[s]) * acc;
-                }
-            }
-            P[r * 65 + s] = val;
-        }
-        for (int i = tid; i < kChunk * kDvt; i += kThreads) {
-            const int r = i / kDvt, cc = i - r * kDvt;
-            float acc = Us[r * us + cc];
-            for (int j = 0; j < dk; ++j) acc = fmaf(-Ws[r * ks + j], Hs[j * kDvt + cc], acc);
-            Vn[r * us + cc] = acc;
-            if (Vout && r < L && cc < nv) Vout[(r0 + r) * dv + dv0 + cc] = acc;
-        }
-        __syncthreads();
-        for (int i = tid; i < kChunk * kDvt; i += kThreads) {
-            const int r = i / kDvt, cc = i - r * kDvt;
-            if (op && r < L && cc < nv) {
-                float a1 = 0.f, a2 = 0.f;
-                if (vg)   // (Q * gamma) H with gamma per key dimension
-                    for (int j = 0; j < dk; ++j)
-                        a1 = fmaf(Qs[r * ks + j] * expf(Gv[r * ks + j]), Hs[j * kDvt + cc], a1);
-                else
-                    for (int j = 0; j < dk; ++j) a1 = fmaf(Qs[r * ks + j], Hs[j * kDvt + cc], a1);
-                for (int s = 0; s <= r; ++s) a2 = fmaf(P[r * 65 + s], Vn[s * us + cc], a2);
-                st_out(op + (r0 + r) * dv + dv0 + cc, (vg ? a1 : expf(g[r]) * a1) + a2);
-            }
-        }
-        __syncthreads();  // every read of H for this chunk is done
-        const float decay = expf(gl);
-        for (int i = tid; i < dk * kDvt; i += kThreads) {
-            const int j = i / kDvt, cc = i - j * kDvt;
-            float acc = 0.f;
-            if (vg) {   // row j of H decays by its own dimension's gate
-                const float glj = Gv[(kChunk - 1) * ks + j];
-                for (int s = 0; s < kChunk; ++s)
-                    acc = fmaf(Ks[s * ks + j] * expf(glj - Gv[s * ks + j]), Vn[s * us + cc], acc);
-                Hs[i] = fmaf(expf(glj), Hs[i], acc);
-            } else {
-                for (int s = 0; s < kChunk; ++s)
-                    acc = fmaf(Ks[s * ks + j] * e[s], Vn[s * us + cc], acc);
-                Hs[i] = fmaf(decay, Hs[i], acc);
-            }
-        }
-    }
-    __syncthreads();
-    if (a.hT) {
-        for (int i = tid; i < dk * kDvt; i += kThreads) {
-            const int j = i / kDvt, cc = i - j * kDvt;
-            if (cc < nv) a.hT[(sbase + dv0 + cc) * dk + j] = Hs[i];
-        }
-    }
-}
-
 // The state pass for a scalar gate with its products on the tensor cores
 // (mma.sync tf32, gdn_mma.cuh: three products per step for fp32 I/O, one for
-// bf16 I/O).  Same chunk algebra and outputs as k_simt_state, but one CTA per
-// (sequence, head, 64-wide d_v tile), and the next chunk's K, W, Q and U are
-// loaded into registers while the current chunk is computed.  P and O are
-// skipped when no output is wanted (the backward pass's recomputation).
+// bf16 I/O).  One CTA per (sequence, head, 64-wide d_v tile); the next
+// chunk's K, W, Q and U are loaded into registers while the current chunk is
+// computed.  P and O are skipped when no output is wanted (the backward
+// pass's recomputation).
 constexpr int kDvm = 64;           // d_v columns per CTA
 constexpr int kLdh = kDvm + 8;     // d_k x 64 state tile: transposed reads conflict-free
 constexpr int kLdc = kChunk + 4;   // 64 x 64 tiles
@@ -693,31 +424,379 @@ k_prep_mma(FwdArgs a, const int2 *__restrict__ table, float *__restrict__ W,
         }
 }
 
-size_t prep_smem(int dk, int dv, bool vg) {
-    return sizeof(float) * ((size_t)kChunk * (dk + 1) + (size_t)kChunk * (dv + 1) +
-                            2 * kChunk * 65 + 3 * kChunk + (vg ? (size_t)kChunk * (dk + 1) : 0));
-}
-size_t state_smem(int dk, bool vg) {
-    return sizeof(float) * ((size_t)dk * kDvt + 3 * (size_t)kChunk * (dk + 1) +
-                            2 * kChunk * (kDvt + 1) + kChunk * 65 + 2 * kChunk +
-                            (vg ? (size_t)kChunk * (dk + 1) : 0));
+// ------------------------------------------------ a gate per key dimension
+//
+// With log alpha a d_k-vector the decay between rows s <= r of a chunk is
+// exp(G_rj - G_sj) per key dimension j (G the in-chunk cumsum), inside every
+// contraction.  On the tensor cores it is split at 16-row blocks: for s and r
+// in the same block the pair terms are formed directly; for s in an earlier
+// block than r, with m the first row of r's block,
+//     exp(G_rj - G_sj) = exp(G_rj - G_mj) exp(G_mj - G_sj),
+// both factors <= 1 (G only decreases down the chunk), so
+//     sum_j x_rj k_sj exp(G_rj - G_sj) = (x_r * exp(G_r - G_m)) . (k_s * exp(G_m - G_s))
+// is a product of two bounded operands and nothing can overflow whatever the
+// decay.  The other contractions take one bounded factor each:
+// W = T diag(beta) (K * exp(G)), O = (Q * exp(G)) H + P V',
+// H_j <- exp(G_Cj) H_j + sum_s k_sj exp(G_Cj - G_sj) V'_s.
+
+// Prep: G [rows][d_k], A and T, W, U, and P [rows][64] (s <= r, zero above).
+size_t prep_vg_smem(int dk, int dv) {
+    const size_t ldk = dk + 4, ldv = dv + 4;
+    const size_t region = std::max(64 * ldk + 32 * ldk + 48 * ldk, 64 * ldv);
+    return sizeof(float) * (2 * 64 * ldk + 3 * (size_t)kChunk * kLdc + 32 * 36 + kChunk + region);
 }
 
-// Launches the chunk prep: the tensor-core kernel for a scalar gate, the
-// CUDA-core one for a gate per key dimension (which writes no T).
+template <typename TIn, bool SPLIT>
+__global__ void __launch_bounds__(kThreads, 1)
+k_prep_vg(FwdArgs a, const int2 *__restrict__ table, float *__restrict__ W,
+          float *__restrict__ U, float *__restrict__ G, float *__restrict__ Pout, int *err) {
+    extern __shared__ float smem[];
+    const int dk = a.dk, dv = a.dv, tid = threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5;
+    int n, c;
+    if (table) {
+        int2 e = table[blockIdx.x];
+        n = e.x;
+        c = e.y;
+        if (n < 0) return;
+    } else {
+        n = blockIdx.x / a.max_chunks;
+        c = blockIdx.x % a.max_chunks;
+    }
+    const int h = blockIdx.y;
+    if (!seq_ok(a.sm, n)) {
+        if (tid == 0) set_error(err, kErrBadIndex);
+        return;
+    }
+    long long row0;
+    int len;
+    a.sm.get(n, h, row0, len);
+    const int t0 = c * kChunk;
+    if (t0 >= len) return;
+    const int L = min(kChunk, len - t0);
+    const long long r0 = row0 + t0;
+    const bool erase = !a.no_erase;
+    const int ldk = dk + 4, ldv = dv + 4;
+    float *Ks = smem;                   // [64][dk+4]  K, later K * exp(G)
+    float *Gs = Ks + kChunk * ldk;      // [64][dk+4]  in-chunk cumsum of log alpha
+    float *A = Gs + kChunk * ldk;       // [64][68]
+    float *Tm = A + kChunk * kLdc;      // [64][68]
+    float *Pm = Tm + kChunk * kLdc;     // [64][68]
+    float *X = Pm + kChunk * kLdc;      // [32][36] merge scratch
+    float *bb = X + 32 * 36;            // [64] beta
+    float *Rg = bb + kChunk;            // Q and the staging tiles, then V
+    float *Qs = Rg;                     // [64][dk+4]
+    float *Xr = Qs + kChunk * ldk;      // [32][dk+4] rows of r's block: k-side 0..15, q-side 16..31
+    float *Xs = Xr + 32 * ldk;          // [48][dk+4] rows s of the earlier blocks
+    float *Vs = Rg;                     // [64][dv+4] (after the products above)
+    const int m0 = 16 * (warp >> 1), nh = warp & 1;
+    const bool want_p = Pout != nullptr;
+    {
+        TileRegs<4> rk, rq, rg;
+        rk.load(static_cast<const TIn *>(a.k) + r0 * dk, dk, dk, L, dk, tid);
+        if (want_p) rq.load(static_cast<const TIn *>(a.q) + r0 * dk, dk, dk, L, dk, tid);
+        rg.load(a.log_alpha + r0 * dk, dk, dk, L, dk, tid);
+        if (tid < kChunk) bb[tid] = tid < L ? __ldg(a.beta + r0 + tid) : 0.f;
+        for (int i = tid; i < kChunk * kLdc; i += kThreads) {
+            Tm[i] = 0.f;
+            A[i] = 0.f;
+            Pm[i] = 0.f;
+        }
+        rk.store(Ks, ldk, dk, tid);
+        if (want_p) rq.store(Qs, ldk, dk, tid);
+        rg.store(Gs, ldk, dk, tid);
+    }
+    __syncthreads();
+    for (int j = tid; j < dk; j += kThreads) {   // column cumsums
+        float acc = 0.f;
+        for (int r = 0; r < kChunk; ++r) {
+            acc += Gs[r * ldk + j];
+            Gs[r * ldk + j] = acc;
+        }
+    }
+    __syncthreads();
+    // pairs inside the 16-row diagonal blocks, formed directly
+    for (int i = tid; i < 2 * 4 * 136; i += kThreads) {
+        const int which = i / (4 * 136), rem = i - which * 4 * 136;   // 0: A, 1: P
+        const int blk = rem / 136;
+        int p = rem - blk * 136, rl = 0;
+        while (p > rl) {   // pair index -> (rl, sl) with sl <= rl
+            p -= rl + 1;
+            ++rl;
+        }
+        const int r = 16 * blk + rl, sc = 16 * blk + p;
+        if (which == 0 && (sc == r || !erase)) continue;
+        if (which == 1 && !want_p) continue;
+        const float *xr = which == 0 ? Ks + r * ldk : Qs + r * ldk;
+        float acc = 0.f;
+        for (int j = 0; j < dk; ++j)
+            acc = fmaf(xr[j] * expf(Gs[r * ldk + j] - Gs[sc * ldk + j]), Ks[sc * ldk + j], acc);
+        if (which == 0) A[r * kLdc + sc] = bb[r] * acc;
+        else Pm[r * kLdc + sc] = acc;
+    }
+    // earlier blocks, through the first row m of r's block
+    for (int m = 16; m < kChunk; m += 16) {
+        __syncthreads();   // staging free
+        for (int i = tid; i < (32 + m) * dk; i += kThreads) {
+            const int row = i / dk, j = i - row * dk;
+            const float gm_ = Gs[m * ldk + j];
+            if (row < 16) {
+                Xr[row * ldk + j] = Ks[(m + row) * ldk + j] * expf(Gs[(m + row) * ldk + j] - gm_);
+            } else if (row < 32) {
+                const int rr = m + row - 16;
+                Xr[row * ldk + j] = want_p ? Qs[rr * ldk + j] * expf(Gs[rr * ldk + j] - gm_) : 0.f;
+            } else {
+                const int sr = row - 32;
+                Xs[sr * ldk + j] = Ks[sr * ldk + j] * expf(gm_ - Gs[sr * ldk + j]);
+            }
+        }
+        __syncthreads();
+        const int ntile = m / 8;
+        for (int task = warp; task < 2 * ntile; task += kThreads / 32) {
+            const int which = task / ntile, tile = task - which * ntile;
+            if ((which == 0 && !erase) || (which == 1 && !want_p)) continue;
+            float acc[1][4];
+            mma::zero(acc);
+            mma::gemm_s<1, SPLIT>(acc, Xr + 16 * which * ldk, ldk, 1, nullptr, Xs, 1, ldk, 0,
+                                  tile, 1, m, dk, lane);
+            mma::for_each(acc, 0, tile, 1, m, lane, [&](int i, int sc, float &x) {
+                if (which == 0) A[(m + i) * kLdc + sc] = bb[m + i] * x;
+                else Pm[(m + i) * kLdc + sc] = x;
+            });
+        }
+    }
+    __syncthreads();
+    // T = (I + A)^{-1}: 16 x 16 diagonal blocks, then 16 -> 32 -> 64 merges
+    if (tid < kChunk) {
+        const int o = 16 * (tid >> 4), cc = tid & 15;
+        Tm[(o + cc) * kLdc + o + cc] = 1.f;
+        for (int r = cc + 1; r < 16; ++r) {
+            float acc = 0.f;
+            for (int q = cc; q < r; ++q)
+                acc = fmaf(A[(o + r) * kLdc + o + q], Tm[(o + q) * kLdc + o + cc], acc);
+            Tm[(o + r) * kLdc + o + cc] = -acc;
+        }
+    }
+    __syncthreads();
+    if (warp < 2) {
+        const int o = 32 * warp;
+        float acc[2][4];
+        mma::zero(acc);
+        mma::gemm_s<2, SPLIT>(acc, A + (o + 16) * kLdc + o, kLdc, 1, nullptr, Tm + o * kLdc + o,
+                              kLdc, 1, 0, 0, 1, 16, 16, lane);
+        mma::for_each(acc, 0, 0, 1, 16, lane,
+                      [&](int i, int nn, float &x) { X[(16 * warp + i) * 36 + nn] = x; });
+    }
+    __syncthreads();
+    if (warp < 2) {
+        const int o = 32 * warp;
+        float acc[2][4];
+        mma::zero(acc);
+        mma::gemm_s<2, SPLIT>(acc, Tm + (o + 16) * kLdc + o + 16, kLdc, 1, nullptr,
+                              X + 16 * warp * 36, 36, 1, 0, 0, 1, 16, 16, lane);
+        mma::for_each(acc, 0, 0, 1, 16, lane,
+                      [&](int i, int nn, float &x) { Tm[(o + 16 + i) * kLdc + o + nn] = -x; });
+    }
+    __syncthreads();
+    if (warp < 4) {
+        float acc[2][4];
+        mma::zero(acc);
+        mma::gemm_s<2, SPLIT>(acc, A + 32 * kLdc, kLdc, 1, nullptr, Tm, kLdc, 1,
+                              16 * (warp >> 1), warp & 1, 2, 32, 32, lane);
+        mma::for_each(acc, 16 * (warp >> 1), warp & 1, 2, 32, lane,
+                      [&](int i, int nn, float &x) { X[i * 36 + nn] = x; });
+    }
+    __syncthreads();
+    if (warp < 4) {
+        float acc[2][4];
+        mma::zero(acc);
+        mma::gemm_s<2, SPLIT>(acc, Tm + 32 * kLdc + 32, kLdc, 1, nullptr, X, 36, 1,
+                              16 * (warp >> 1), warp & 1, 2, 32, 32, lane);
+        mma::for_each(acc, 16 * (warp >> 1), warp & 1, 2, 32, lane,
+                      [&](int i, int nn, float &x) { Tm[(32 + i) * kLdc + nn] = -x; });
+    }
+    // K * exp(G) (each factor <= 1)
+    for (int i = tid; i < kChunk * dk; i += kThreads) {
+        const int r = i / dk, j = i - r * dk;
+        Ks[r * ldk + j] *= expf(Gs[r * ldk + j]);
+    }
+    __syncthreads();
+    {   // W = T diag(beta) (K * exp(G)) (zero without the erase term)
+        float acc[8][4];
+        mma::zero(acc);
+        if (erase)
+            mma::gemm_s<8, SPLIT>(acc, Tm, kLdc, 1, bb, Ks, ldk, 1, m0, nh, 2, dk, m0 + 16, lane);
+        mma::for_each(acc, m0, nh, 2, dk, lane, [&](int r, int j, float &x) {
+            if (r < L) W[(r0 + r) * dk + j] = x;
+        });
+    }
+    {
+        TileRegs<8> rv;
+        rv.load(static_cast<const TIn *>(a.v) + r0 * dv, dv, dv, L, dv, tid);
+        rv.store(Vs, ldv, dv, tid);
+    }
+    __syncthreads();
+    for (int c0 = 0; c0 < dv; c0 += 128) {   // U = T diag(beta) V
+        float acc[8][4];
+        mma::zero(acc);
+        const int ne = min(dv, c0 + 128);
+        mma::gemm_s<8, SPLIT>(acc, Tm, kLdc, 1, bb, Vs, ldv, 1, m0, c0 / 8 + nh, 2, ne, m0 + 16,
+                              lane);
+        mma::for_each(acc, m0, c0 / 8 + nh, 2, ne, lane, [&](int r, int j, float &x) {
+            if (r < L) U[(r0 + r) * dv + j] = x;
+        });
+    }
+    for (int i = tid; i < L * dk; i += kThreads) {
+        const int r = i / dk, j = i - r * dk;
+        G[(r0 + r) * dk + j] = Gs[r * ldk + j];
+    }
+    if (want_p)
+        for (int i = tid; i < L * kChunk; i += kThreads) {
+            const int r = i >> 6, sc = i & 63;
+            Pout[(r0 + r) * kChunk + sc] = Pm[r * kLdc + sc];
+        }
+}
+
+// State pass with a gate per key dimension: one CTA per (sequence, head,
+// 64-wide d_v tile), chunks in order, reading P from the prep.
+size_t state_vg_smem(int dk) {
+    const size_t ldk = dk + 4;
+    return sizeof(float) * ((size_t)dk * kLdh + 4 * (size_t)kChunk * ldk +
+                            3 * (size_t)kChunk * kLdc + 128);
+}
+
+template <typename TIn, bool SPLIT>
+__global__ void __launch_bounds__(kThreads, 1)
+k_state_vg(FwdArgs a, const float *__restrict__ W, const float *__restrict__ U,
+           const float *__restrict__ G, const float *__restrict__ Pg, int *err) {
+    extern __shared__ float smem[];
+    const int dk = a.dk, dv = a.dv, tid = threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5;
+    const int n = blockIdx.x, h = blockIdx.y, dv0 = blockIdx.z * kDvm;
+    const int nv = min(kDvm, dv - dv0);
+    if (!seq_ok(a.sm, n)) {
+        if (tid == 0) set_error(err, kErrBadIndex);
+        return;
+    }
+    long long row0;
+    int len;
+    a.sm.get(n, h, row0, len);
+    const int ldk = dk + 4;
+    const TIn *qp = static_cast<const TIn *>(a.q);
+    const TIn *kp = static_cast<const TIn *>(a.k);
+    TIn *op = static_cast<TIn *>(a.o);
+    float *Hs = smem;                    // [dk][72]   H = S^T tile
+    float *Ks = Hs + dk * kLdh;          // [64][dk+4] K * exp(G_C - G)
+    float *Ws = Ks + kChunk * ldk;       // [64][dk+4]
+    float *Qs = Ws + kChunk * ldk;       // [64][dk+4] Q * exp(G)
+    float *Gt = Qs + kChunk * ldk;       // [64][dk+4] cumulative gates
+    float *Us = Gt + kChunk * ldk;       // [64][68]
+    float *Vn = Us + kChunk * kLdc;      // [64][68]
+    float *P = Vn + kChunk * kLdc;       // [64][68]
+    float *gce = P + kChunk * kLdc;      // [128] exp(G_C)
+    const long long sbase = ((long long)n * a.sm.H + h) * dv;
+    const int m0 = 16 * (warp >> 1), nh = warp & 1;
+
+    for (int i = tid; i < dk * kDvm; i += kThreads) {
+        const int j = i / kDvm, cc = i - j * kDvm;
+        Hs[j * kLdh + cc] = (a.h0 && cc < nv) ? __ldg(a.h0 + (sbase + dv0 + cc) * dk + j) : 0.f;
+    }
+    const int nch = (len + kChunk - 1) / kChunk;
+    for (int c = 0; c < nch; ++c) {
+        const int t0 = c * kChunk, L = min(kChunk, len - t0);
+        const long long r0 = row0 + t0;
+        __syncthreads();  // previous chunk fully consumed
+        {
+            TileRegs<4> t;
+            t.load(kp + r0 * dk, dk, dk, L, dk, tid);
+            t.store(Ks, ldk, dk, tid);
+            t.load(W + r0 * dk, dk, dk, L, dk, tid);
+            t.store(Ws, ldk, dk, tid);
+            t.load(qp + r0 * dk, dk, dk, L, dk, tid);
+            t.store(Qs, ldk, dk, tid);
+            t.load(G + r0 * dk, dk, dk, L, dk, tid);
+            t.store(Gt, ldk, dk, tid);
+        }
+        {
+            TileRegs<2> t;
+            t.load(U + r0 * dv + dv0, dv, kDvm, L, nv, tid);
+            t.store(Us, kLdc, kDvm, tid);
+            t.load(Pg + r0 * kChunk, kChunk, kChunk, L, kChunk, tid);
+            t.store(P, kLdc, kChunk, tid);
+        }
+        __syncthreads();
+        // rows past L hold zeros (K = Q = 0), so their factors do not matter
+        for (int i = tid; i < kChunk * dk; i += kThreads) {
+            const int r = i / dk, j = i - r * dk;
+            const float gr = Gt[r * ldk + j], gc = Gt[(L - 1) * ldk + j];
+            Qs[r * ldk + j] *= expf(gr);
+            Ks[r * ldk + j] *= expf(gc - gr);
+        }
+        for (int j = tid; j < dk; j += kThreads) gce[j] = expf(Gt[(L - 1) * ldk + j]);
+        {   // V' = U - W H
+            float acc[4][4];
+            mma::zero(acc);
+            mma::gemm_s<4, SPLIT>(acc, Ws, ldk, 1, nullptr, Hs, kLdh, 1, m0, nh, 2, kDvm, dk,
+                                  lane);
+            mma::for_each(acc, m0, nh, 2, kDvm, lane, [&](int r, int cc, float &x) {
+                Vn[r * kLdc + cc] = Us[r * kLdc + cc] - x;
+            });
+        }
+        __syncthreads();
+        {   // O = (Q * exp(G)) H + P V'
+            float a1[4][4], a2[4][4];
+            mma::zero(a1);
+            mma::zero(a2);
+            mma::gemm_s<4, SPLIT>(a1, Qs, ldk, 1, nullptr, Hs, kLdh, 1, m0, nh, 2, kDvm, dk,
+                                  lane);
+            mma::gemm_s<4, SPLIT>(a2, P, kLdc, 1, nullptr, Vn, kLdc, 1, m0, nh, 2, kDvm, m0 + 16,
+                                  lane);
+            const int gq = lane >> 2, tq = lane & 3;
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int r = m0 + gq + 8 * (q >> 1), cc = 8 * (nh + 2 * i) + 2 * tq + (q & 1);
+                    if (r < L && cc < nv) st_out(op + (r0 + r) * dv + dv0 + cc, a1[i][q] + a2[i][q]);
+                }
+        }
+        __syncthreads();  // every read of H for this chunk is done
+        // H_j <- exp(G_Cj) H_j + sum_s k_sj exp(G_Cj - G_sj) V'_s
+        for (int j0 = 16 * warp; j0 < dk; j0 += 16 * (kThreads / 32)) {
+            float acc[8][4];
+            mma::zero(acc);
+            mma::gemm_s<8, SPLIT>(acc, Ks, 1, ldk, nullptr, Vn, kLdc, 1, j0, 0, 1, kDvm, kChunk,
+                                  lane);
+            mma::for_each(acc, j0, 0, 1, kDvm, lane, [&](int j, int cc, float &x) {
+                if (j < dk) Hs[j * kLdh + cc] = fmaf(gce[j], Hs[j * kLdh + cc], x);
+            });
+        }
+    }
+    __syncthreads();
+    if (a.hT) {
+        for (int i = tid; i < dk * kDvm; i += kThreads) {
+            const int j = i / kDvm, cc = i - j * kDvm;
+            if (cc < nv) a.hT[(sbase + dv0 + cc) * dk + j] = Hs[j * kLdh + cc];
+        }
+    }
+}
+
+
+// Launches the chunk prep (P: the intra-chunk P rows a gate per key
+// dimension needs, else unused).
 template <typename TIn>
 cudaError_t run_prep(const FwdArgs &a, const int2 *table, float *W, float *U, float *G,
-                     float *Tout, int *err) {
+                     float *Tout, float *P, int *err) {
+    constexpr bool kSplit = std::is_same<TIn, float>::value;   // fp32 I/O: 3xTF32
     const dim3 grid(a.chunk_slots, a.sm.H);
     cudaError_t e;
     if (a.vector_gate) {
-        const size_t psm = prep_smem(a.dk, a.dv, true);
-        e = cudaFuncSetAttribute(k_simt_prep<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)psm);
+        const size_t psm = prep_vg_smem(a.dk, a.dv);
+        e = cudaFuncSetAttribute(k_prep_vg<TIn, kSplit>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psm);
         if (e != cudaSuccess) return e;
-        k_simt_prep<TIn><<<grid, kThreads, psm, a.stream>>>(a, table, W, U, G, err);
+        k_prep_vg<TIn, kSplit><<<grid, kThreads, psm, a.stream>>>(a, table, W, U, G, P, err);
     } else {
-        constexpr bool kSplit = std::is_same<TIn, float>::value;   // fp32 I/O: 3xTF32
         const size_t psm = prep_mma_smem(a.dk, a.dv);
         e = cudaFuncSetAttribute(k_prep_mma<TIn, kSplit>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psm);
@@ -728,31 +807,29 @@ cudaError_t run_prep(const FwdArgs &a, const int2 *table, float *W, float *U, fl
     return cudaGetLastError();
 }
 
-// Launches the state pass: the tensor-core kernel for a scalar gate, the
-// CUDA-core one for a gate per key dimension.
+// Launches the state pass (P as for run_prep).
 template <typename TIn>
 cudaError_t run_state(const FwdArgs &a, const float *W, const float *U, const float *G,
-                      float *Hst, float *Vn, int *err) {
-    const dim3 grid(a.sm.N, a.sm.H, (a.dv + kDvt - 1) / kDvt);
+                      float *Hst, float *Vn, const float *P, int *err) {
+    constexpr bool kSplit = std::is_same<TIn, float>::value;   // fp32 I/O: 3xTF32
+    const dim3 grid(a.sm.N, a.sm.H, (a.dv + kDvm - 1) / kDvm);
     cudaError_t e;
     if (a.vector_gate) {
-        const size_t ssm = state_smem(a.dk, true);
-        e = cudaFuncSetAttribute(k_simt_state<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)ssm);
+        const size_t ssm = state_vg_smem(a.dk);
+        e = cudaFuncSetAttribute(k_state_vg<TIn, kSplit>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ssm);
         if (e != cudaSuccess) return e;
-        const int slot = timer_begin(a.stream, "k_simt_state");
-        k_simt_state<TIn><<<grid, kThreads, ssm, a.stream>>>(a, W, U, G, Hst, Vn, err);
+        const int slot = timer_begin(a.stream, "k_state_vg");
+        k_state_vg<TIn, kSplit><<<grid, kThreads, ssm, a.stream>>>(a, W, U, G, P, err);
         timer_end(slot, a.stream);
     } else {
-        constexpr bool kSplit = std::is_same<TIn, float>::value;   // fp32 I/O: 3xTF32
         const size_t ssm = state_mma_smem(a.dk, a.o != nullptr);
         e = cudaFuncSetAttribute(k_state_mma<TIn, kSplit>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)state_mma_smem(a.dk, true));
         if (e != cudaSuccess) return e;
-        const dim3 gm(a.sm.N, a.sm.H, (a.dv + kDvm - 1) / kDvm);
         const int slot = timer_begin(a.stream, "k_state_mma");
-        k_state_mma<TIn, kSplit><<<gm, kThreads, ssm, a.stream>>>(a, W, U, G, Hst, Vn, err);
+        k_state_mma<TIn, kSplit><<<grid, kThreads, ssm, a.stream>>>(a, W, U, G, Hst, Vn, err);
         timer_end(slot, a.stream);
     }
     count_launch();
@@ -763,15 +840,18 @@ template <typename TIn>
 gdn_status launch(const FwdArgs &a) {
     int *err = device_error_word();
     cudaStream_t st = a.stream;
-    float *W = nullptr, *U = nullptr, *G = nullptr;
+    float *W = nullptr, *U = nullptr, *G = nullptr, *P = nullptr;
     int2 *table = nullptr;
     const size_t rows = (size_t)a.rows > 0 ? (size_t)a.rows : 1;
     if (scratch_alloc((void **)&W, rows * a.dk * sizeof(float), st) != cudaSuccess ||
         scratch_alloc((void **)&U, rows * a.dv * sizeof(float), st) != cudaSuccess ||
         scratch_alloc((void **)&G, rows * (a.vector_gate ? a.dk : 1) * sizeof(float), st) !=
-            cudaSuccess) {
+            cudaSuccess ||
+        (a.vector_gate &&
+         scratch_alloc((void **)&P, rows * kChunk * sizeof(float), st) != cudaSuccess)) {
         if (W) scratch_free(W, st);
         if (U) scratch_free(U, st);
+        if (G) scratch_free(G, st);
         return GDN_ERR_CUDA;
     }
     gdn_status rc = GDN_OK;
@@ -787,16 +867,17 @@ gdn_status launch(const FwdArgs &a) {
             }
         }
         if (rc == GDN_OK && a.sm.H > 0 &&
-            run_prep<TIn>(a, table, W, U, G, nullptr, err) != cudaSuccess)
+            run_prep<TIn>(a, table, W, U, G, nullptr, P, err) != cudaSuccess)
             rc = GDN_ERR_CUDA;
     }
     if (rc == GDN_OK && a.sm.N > 0 && a.sm.H > 0 &&
-        run_state<TIn>(a, W, U, G, nullptr, nullptr, err) != cudaSuccess)
+        run_state<TIn>(a, W, U, G, nullptr, nullptr, P, err) != cudaSuccess)
         rc = GDN_ERR_CUDA;
     if (rc == GDN_OK && cudaGetLastError() != cudaSuccess) rc = GDN_ERR_CUDA;
     scratch_free(W, st);
     scratch_free(U, st);
     scratch_free(G, st);
+    if (P) scratch_free(P, st);
     if (table) scratch_free(table, st);
     return rc;
 }
@@ -811,7 +892,7 @@ template <typename TIn>
 gdn_status enqueue_state_t(const FwdArgs &a, const float *W, const float *U, const float *G,
                            float *Hst, float *Vn) {
     if (a.sm.N > 0 && a.sm.H > 0 &&
-        run_state<TIn>(a, W, U, G, Hst, Vn, device_error_word()) != cudaSuccess)
+        run_state<TIn>(a, W, U, G, Hst, Vn, nullptr, device_error_word()) != cudaSuccess)
         return GDN_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
@@ -820,20 +901,21 @@ template <typename TIn>
 gdn_status enqueue_prep_t(const FwdArgs &a, const int2 *table, float *W, float *U, float *G,
                           float *Tout) {
     if (a.chunk_slots > 0 && a.sm.H > 0 &&
-        run_prep<TIn>(a, table, W, U, G, Tout, device_error_word()) != cudaSuccess)
+        run_prep<TIn>(a, table, W, U, G, Tout, nullptr, device_error_word()) != cudaSuccess)
         return GDN_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
 gdn_status enqueue_simt_prep(const FwdArgs &a, const int2 *table, float *W, float *U, float *G,
                              float *Tout) {
-    if (Tout && a.vector_gate) return GDN_ERR_UNSUPPORTED;
+    if (a.vector_gate) return GDN_ERR_UNSUPPORTED;
     return a.dt == GDN_F32 ? enqueue_prep_t<float>(a, table, W, U, G, Tout)
                            : enqueue_prep_t<__nv_bfloat16>(a, table, W, U, G, Tout);
 }
 
 gdn_status enqueue_simt_state(const FwdArgs &a, const float *W, const float *U, const float *G,
                               float *Hst, float *Vn) {
+    if (a.vector_gate) return GDN_ERR_UNSUPPORTED;
     return a.dt == GDN_F32 ? enqueue_state_t<float>(a, W, U, G, Hst, Vn)
                            : enqueue_state_t<__nv_bfloat16>(a, W, U, G, Hst, Vn);
 }
@@ -891,9 +973,11 @@ gdn_status launch_noalloc(const FwdArgs &a, float *scratch) {
     float *W = scratch;
     float *U = W + rows * a.dk;
     float *G = U + rows * a.dv;
-    if (a.chunk_slots > 0 && run_prep<TIn>(a, nullptr, W, U, G, nullptr, err) != cudaSuccess)
+    if (a.chunk_slots > 0 &&
+        run_prep<TIn>(a, nullptr, W, U, G, nullptr, nullptr, err) != cudaSuccess)
         return GDN_ERR_CUDA;
-    if (run_state<TIn>(a, W, U, G, nullptr, nullptr, err) != cudaSuccess) return GDN_ERR_CUDA;
+    if (run_state<TIn>(a, W, U, G, nullptr, nullptr, nullptr, err) != cudaSuccess)
+        return GDN_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 

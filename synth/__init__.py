@@ -179,10 +179,10 @@ def make_workload(name, device="cpu", **override) -> Inputs:
             lengths = varlen_lengths(cfg["N"], cfg["len_min"], cfg["len_max"], cfg["seed"])
         return make_varlen(lengths, cfg["H"], cfg["dk"], cfg["dv"], io=cfg["io"],
                            decay=cfg["decay"], h0_std=cfg["h0_std"], seed=cfg["seed"],
-                           device=device)
+                           device=device, vector_gate=cfg.get("vector_gate", False))
     return make_dense(cfg["B"], cfg["H"], cfg["T"], cfg["dk"], cfg["dv"], io=cfg["io"],
                       decay=cfg["decay"], h0_std=cfg["h0_std"], seed=cfg["seed"],
-                      device=device)
+                      device=device, vector_gate=cfg.get("vector_gate", False))
 
 
 def to_f64(t):
