@@ -1,5 +1,5 @@
-// gdn_bwd.cu -- backward pass of the chunked gated delta rule, CUDA cores,
-// fp32 arithmetic.
+// gdn_bwd.cu -- backward pass of the chunked gated delta rule on warp-level
+// tf32 mma.sync products (three per step for fp32 I/O), fp32 accumulation.
 //
 // The gradient of L = sum dO . o + <dhT, hT> with respect to q, k, v,
 // log_alpha, beta and h0.  The recurrent state is recomputed, not stored by

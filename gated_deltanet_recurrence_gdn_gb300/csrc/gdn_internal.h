@@ -86,7 +86,8 @@ void timer_end(int slot, cudaStream_t st);
 void count_launch(int n = 1);
 long long option(int key);
 
-// SIMT (CUDA-core, fp32 arithmetic) path: every supported shape and dtype.
+// The general path (GDN_IMPL_SIMT): every supported shape and dtype, warp-level
+// tf32 mma.sync products with fp32 accumulation.
 gdn_status simt_forward(const FwdArgs &a);
 
 // Pieces of that path the backward pass reuses.  Prep: W [rows][d_k],
@@ -101,7 +102,7 @@ gdn_status enqueue_simt_state(const FwdArgs &a, const float *W, const float *U, 
                               float *Hst, float *Vn);
 
 // Backward pass of the scalar-gate recurrence (with or without the erase
-// term) on CUDA cores, fp32 arithmetic; defined in gdn_bwd.cu.
+// term) on the general path's products; defined in gdn_bwd.cu.
 gdn_status simt_backward(const FwdArgs &a, const BwdArgs &b);
 
 // The same path on a dense batch with its scratch in a fixed device array of

@@ -1,4 +1,4 @@
-// gdn_mma.cuh -- warp-level tf32 tensor-core products for the CUDA-core
+// gdn_mma.cuh -- warp-level tf32 tensor-core products for the general path's
 // kernels (mma.sync m16n8k8, fp32 operands in shared memory, fp32 accumulate).
 //
 // A warp computes a 16-row block of an output C (M x N) over NT 8-column

@@ -931,7 +931,7 @@ gdn_status enqueue_chunk_table(const FwdArgs &a, int2 *table) {
 
 // ------------------------------------------------- allocation-free variant
 //
-// gdn_fwd_noalloc runs the same two CUDA-core kernels (prep, state pass) on a
+// gdn_fwd_noalloc runs the same two kernels (prep, state pass) on a
 // dense batch, but its W / U / gate-cumsum scratch lives in this fixed device
 // array instead of the library's scratch pool.  The array belongs to every
 // GPU that loads the library, for as long as the library stays loaded.  All

@@ -1,5 +1,5 @@
-// gdn_tile.cuh -- register-staged loads of 64-row chunk tiles for the
-// CUDA-core kernels.
+// gdn_tile.cuh -- register-staged loads of 64-row chunk tiles for the general
+// path's kernels.
 //
 // A chunk tile is 64 rows of `width` consecutive elements (width a multiple
 // of 8) at a row stride of `stride` elements.  A block of 256 threads loads it

@@ -108,8 +108,8 @@ gdn_status gdn_fwd_varlen(const void *q, const void *k, const void *v,
  *
  *   Limit: B*H*T*(d_k + d_v + 1)*4 bytes must not exceed 32 MiB (for
  *   d_k = d_v = 128, about 32 000 token-heads), otherwise GDN_ERR_TOO_LARGE
- *   is returned and nothing is enqueued.  It always runs the fp32 CUDA-core
- *   kernels (bf16 or fp32 I/O).
+ *   is returned and nothing is enqueued.  It always runs the general path's
+ *   kernels (GDN_IMPL_SIMT; bf16 or fp32 I/O).
  *   Set-up: the first call on each device looks up the array's device address
  *   with that device current; make that first call before any stream capture.
  *   Sharing: every call uses the same array.  Calls whose kernels overlap on
@@ -134,8 +134,10 @@ gdn_status gdn_sync_check(void *stream);
 
 /*
  * Implementation selection (process-wide; for tests and benchmarks).
- *   GDN_OPT_IMPL:      GDN_IMPL_AUTO (default), GDN_IMPL_SIMT (fp32 CUDA-core
- *                      kernels, every supported shape), GDN_IMPL_TC (tcgen05
+ *   GDN_OPT_IMPL:      GDN_IMPL_AUTO (default), GDN_IMPL_SIMT (the general
+ *                      path: every supported shape; warp-level tf32 mma.sync
+ *                      products, three per step for fp32 I/O so they keep
+ *                      fp32 accuracy), GDN_IMPL_TC (tcgen05
  *                      tensor-core kernels; GDN_ERR_UNSUPPORTED when the call
  *                      does not fit them).
  *   GDN_OPT_SEGMENTS:  0 = automatic; s > 0 forces s sequence segments per
@@ -188,7 +190,7 @@ int gdn_last_impl(void);
  *       S_t = (S_{t-1} diag(alpha_t)) (I - beta_t k_t k_t^T) + beta_t v_t k_t^T.
  *   With all d_k entries of a row equal this is the scalar-gate recurrence.
  *   Both flags together give gated linear attention with a vector gate.
- *   Vector gates run on the CUDA-core path only: with GDN_IMPL_TC forced the
+ *   Vector gates run on the general path only: with GDN_IMPL_TC forced the
  *   call returns GDN_ERR_UNSUPPORTED, with GDN_IMPL_AUTO it takes that path.
  * Unknown flag bits give GDN_ERR_INVALID_ARG.
  */
@@ -214,7 +216,8 @@ gdn_status gdn_fwd_varlen_ex(const void *q, const void *k, const void *v,
  * in the backward pass rather than storing it, and so does this call: it
  * reruns the chunked forward (without writing o), carries the adjoint of the
  * state backwards chunk by chunk, then forms every chunk's gradients in
- * parallel.  CUDA cores, fp32 arithmetic.
+ * parallel.  Warp-level tf32 mma.sync products (three per step for fp32 I/O),
+ * fp32 accumulation.
  *   q, k, v, log_alpha, beta, h0, B, H, T, d_k, d_v, chunk, dt: as gdn_fwd.
  *   dout   [B][H][T][d_v] dtype dt: the weights dO of the outputs.
  *   dhT    [B][H][d_v][d_k] fp32, or NULL for zero weight on the final state.
