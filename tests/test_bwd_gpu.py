@@ -42,6 +42,7 @@ def _compare(got, ref, io, skip=()):
 
 @pytest.mark.parametrize("erase", [True, False])
 @pytest.mark.parametrize("B,H,T,dk,dv,io", [(1, 2, 130, 64, 64, "f32"),
+                                            (2, 2, 257, 64, 64, "bf16"),
                                             (2, 2, 300, 128, 128, "bf16"),
                                             (1, 3, 200, 64, 128, "bf16"),
                                             (2, 1, 150, 32, 48, "f32"),

@@ -403,3 +403,35 @@ def test_vector_gate_not_on_tensor_core_path():
         with pytest.raises(gdn.GdnError) as e:
             gdn.gdn_fwd(x.q, x.k, x.v, x.log_alpha, x.beta, None)
     assert e.value.status == gdn.GDN_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("B,H,T,dk,dv,io,decay", [(1, 2, 200, 128, 256, "bf16", "fast"),
+                                                  (2, 2, 150, 64, 64, "f32", "slow"),
+                                                  (1, 3, 130, 128, 128, "f32", "fast")])
+def test_vector_gate_wide_and_fp32(B, H, T, dk, dv, io, decay):
+    # the widest tiles (d_v = 256) and fp32 I/O (three tf32 products per step)
+    x = synth.make_dense(B, H, T, dk, dv, io=io, decay=decay, h0_std=0.05, seed=T + 7,
+                         device="cuda", vector_gate=True)
+    o, hT = gdn.gdn_fwd(x.q, x.k, x.v, x.log_alpha, x.beta, x.h0, check=True)
+    U.sync()
+    import oracle
+    o_ref, h_ref = oracle.gdn_fwd(U.f64(x.q), U.f64(x.k), U.f64(x.v), U.f64(x.log_alpha),
+                                  U.f64(x.beta), U.f64(x.h0), threads=U.ORACLE_THREADS,
+                                  vector_gate=True)
+    check(o, hT, o_ref, h_ref, io)
+
+
+def test_vector_gate_steep_decay_stays_finite():
+    # log gates of -20 per step in some dimensions: exp(G_r - G_s) spans far
+    # below fp32's range inside one chunk; the factored products must neither
+    # overflow nor lose the near-diagonal terms
+    x = synth.make_dense(1, 2, 192, 64, 64, io="f32", seed=37, device="cuda", vector_gate=True)
+    la = x.log_alpha.clone()
+    la[..., ::3] = -20.0
+    o, hT = gdn.gdn_fwd(x.q, x.k, x.v, la, x.beta, None, check=True)
+    U.sync()
+    assert torch.isfinite(o).all() and torch.isfinite(hT).all()
+    import oracle
+    o_ref, h_ref = oracle.gdn_fwd(U.f64(x.q), U.f64(x.k), U.f64(x.v), U.f64(la), U.f64(x.beta),
+                                  None, vector_gate=True)
+    check(o, hT, o_ref, h_ref, "f32")
