@@ -48,8 +48,6 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kDvt = 32;     // d_v columns per tile
 
-__device__ __forceinline__ float ld_in(const float *p) { return __ldg(p); }
-__device__ __forceinline__ float ld_in(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
 __device__ __forceinline__ void st_out(float *p, float x) { *p = x; }
 __device__ __forceinline__ void st_out(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
 __device__ __forceinline__ void set_error(int *err, int code) { atomicCAS(err, 0, code); }
