@@ -389,6 +389,10 @@ def run_ours(args, world, rank, local):
     launches = gdn.kernel_launches() - launches0
     k_ms, k_n, k_name = gdn.kernel_timer_read()
     gdn.kernel_timer(False)
+    if k_n != args.steps:
+        # one timed launch of the dominant kernel per call, or the mean mixes kernels
+        raise RuntimeError("kernel timer: %d launches of %s in %d steps" % (k_n, k_name,
+                                                                          args.steps))
     gdn.sync_check(dev)
     step_ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / args.steps
     step_ms = max_over_ranks(step_ms, world)

@@ -828,7 +828,9 @@ cudaError_t run_state(const FwdArgs &a, const float *W, const float *U, const fl
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)state_mma_smem(a.dk, true));
         if (e != cudaSuccess) return e;
-        const int slot = timer_begin(a.stream, "k_state_mma");
+        // timed only as a forward call's dominant kernel: the backward pass's
+        // recomputation (no output) is not its most expensive launch
+        const int slot = a.o ? timer_begin(a.stream, "k_state_mma") : -1;
         k_state_mma<TIn, kSplit><<<grid, kThreads, ssm, a.stream>>>(a, W, U, G, Hst, Vn, err);
         timer_end(slot, a.stream);
     }
