@@ -4,6 +4,7 @@
 #include <mutex>
 #include <vector>
 
+#include "gdn_bwd_tc.h"
 #include "gdn_internal.h"
 
 namespace gdn {
@@ -257,7 +258,6 @@ gdn_status check_bwd(const void *dout, const float *dhT, const void *dq, const v
                      bool tokens, unsigned flags) {
     if (flags & ~(unsigned)(GDN_FLAG_NO_ERASE | GDN_FLAG_VECTOR_GATE)) return GDN_ERR_INVALID_ARG;
     if (flags & GDN_FLAG_VECTOR_GATE) return GDN_ERR_UNSUPPORTED;
-    if (g_opt_impl.load() == GDN_IMPL_TC) return GDN_ERR_UNSUPPORTED;
     if (tokens && (!dout || !dq || !dk || !dv || !dla || !dbeta)) return GDN_ERR_INVALID_ARG;
     const void *ptrs[] = {dout, dhT, dq, dk, dv, dla, dbeta, dh0};
     for (const void *p : ptrs)
@@ -270,8 +270,9 @@ gdn_status run_bwd(FwdArgs &a, const void *dout, const float *dhT, void *dq, voi
     BwdArgs b{};
     b.dout = dout; b.dhT = dhT; b.dq = dq; b.dk = dk; b.dv = dv;
     b.dlog_alpha = dla; b.dbeta = dbeta; b.dh0 = dh0;
-    const gdn_status rc = simt_backward(a, b);
-    if (rc == GDN_OK) g_last_impl.store(GDN_IMPL_SIMT);
+    int used = 0;
+    const gdn_status rc = run_backward(a, b, g_opt_impl.load(), &used);
+    if (rc == GDN_OK) g_last_impl.store(used);
     return rc;
 }
 }  // namespace

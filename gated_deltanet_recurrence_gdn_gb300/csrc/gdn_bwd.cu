@@ -32,12 +32,15 @@
 //
 // Kernels: the forward prep and state pass (gdn_simt.cu) recompute W, U, the
 // gate cumsum, every chunk's starting state and V'; k_bwd_dstate carries the
-// state adjoint backwards; k_bwd_chunk forms every gradient of one chunk.
+// state adjoint backwards (for bf16 I/O on shapes it takes, the tcgen05
+// kernel of gdn_bwd_tc.cu does instead); k_bwd_chunk forms every gradient of
+// one chunk.
 // Without the erase term A = 0, T = I and W = 0, and the A and W terms drop.
 #include <cuda_bf16.h>
 
 #include <type_traits>
 
+#include "gdn_bwd_tc.h"
 #include "gdn_internal.h"
 #include "gdn_mma.cuh"
 #include "gdn_tile.cuh"
@@ -659,7 +662,7 @@ k_bwd_chunk(FwdArgs a, BwdArgs b, const int2 *__restrict__ table, const float *_
 }
 
 template <typename TIn>
-gdn_status launch_bwd(const FwdArgs &a, const BwdArgs &b) {
+gdn_status launch_bwd(const FwdArgs &a, const BwdArgs &b, bool tc_dstate) {
     cudaStream_t st = a.stream;
     int *err = device_error_word();
     const size_t rows = (size_t)a.rows > 0 ? (size_t)a.rows : 1;
@@ -676,6 +679,7 @@ gdn_status launch_bwd(const FwdArgs &a, const BwdArgs &b) {
         return GDN_ERR_CUDA;
     float *W = nullptr, *U = nullptr, *G = nullptr, *Vn = nullptr, *dVn = nullptr;
     float *Hst = nullptr, *dHc = nullptr, *Tg = nullptr;
+    __nv_bfloat16 *Wb = nullptr;   // bf16 W, the tensor-core state adjoint's input
     int2 *table = nullptr;
     float **bufs[] = {&W, &U, &G, &Vn, &dVn, &Hst, &dHc, &Tg};
     const size_t sizes[] = {rows * a.dk, rows * a.dv, rows, rows * a.dv, rows * a.dv,
@@ -684,6 +688,9 @@ gdn_status launch_bwd(const FwdArgs &a, const BwdArgs &b) {
     for (int i = 0; i < 8 && rc == GDN_OK; ++i)
         if (scratch_alloc((void **)bufs[i], sizes[i] * sizeof(float), st) != cudaSuccess)
             rc = GDN_ERR_CUDA;
+    if (rc == GDN_OK && tc_dstate &&
+        scratch_alloc((void **)&Wb, rows * a.dk * sizeof(__nv_bfloat16), st) != cudaSuccess)
+        rc = GDN_ERR_CUDA;
     if (rc == GDN_OK && a.sm.cu && a.chunk_slots > 0) {
         if (scratch_alloc((void **)&table, sizeof(int2) * (size_t)a.chunk_slots, st) !=
             cudaSuccess)
@@ -691,14 +698,18 @@ gdn_status launch_bwd(const FwdArgs &a, const BwdArgs &b) {
         else
             rc = enqueue_chunk_table(a, table);
     }
-    if (rc == GDN_OK) rc = enqueue_simt_prep(a, table, W, U, G, Tg);
+    if (rc == GDN_OK)
+        rc = tc_dstate ? enqueue_simt_prep_w16(a, table, W, U, G, Tg, Wb)
+                       : enqueue_simt_prep(a, table, W, U, G, Tg);
     if (rc == GDN_OK) {
         FwdArgs f = a;
         f.o = nullptr;
         f.hT = nullptr;
         rc = enqueue_simt_state(f, W, U, G, Hst, Vn);
     }
-    if (rc == GDN_OK && a.sm.N > 0 && a.sm.H > 0) {
+    if (rc == GDN_OK && tc_dstate) {
+        rc = tc_bwd_dstate(a, b, Wb, G, dVn, dHc);
+    } else if (rc == GDN_OK && a.sm.N > 0 && a.sm.H > 0) {
         dim3 grid(a.sm.N, a.sm.H, (a.dv + kDvm - 1) / kDvm);
         k_bwd_dstate<TIn, kSplit><<<grid, kThreads, dsm, st>>>(a, b, W, G, dVn, dHc, err);
         count_launch();
@@ -713,17 +724,27 @@ gdn_status launch_bwd(const FwdArgs &a, const BwdArgs &b) {
     if (rc == GDN_OK && cudaGetLastError() != cudaSuccess) rc = GDN_ERR_CUDA;
     for (float **p : bufs)
         if (*p) scratch_free(*p, st);
+    if (Wb) scratch_free(Wb, st);
     if (table) scratch_free(table, st);
     return rc;
 }
 
 }  // namespace
 
-gdn_status simt_backward(const FwdArgs &a, const BwdArgs &b) {
+gdn_status run_backward(const FwdArgs &a, const BwdArgs &b, long long impl, int *used) {
     if (a.vector_gate) return GDN_ERR_UNSUPPORTED;
     if (chunk_lay(a.dk).bytes > 227 * 1024 || dstate_smem(a.dk) > 227 * 1024)
         return GDN_ERR_UNSUPPORTED;
-    return a.dt == GDN_F32 ? launch_bwd<float>(a, b) : launch_bwd<__nv_bfloat16>(a, b);
+    const bool tc = impl != GDN_IMPL_SIMT && tc_bwd_supported(a);
+    if (impl == GDN_IMPL_TC && !tc) return GDN_ERR_UNSUPPORTED;
+    const gdn_status rc = a.dt == GDN_F32 ? launch_bwd<float>(a, b, false)
+                                          : launch_bwd<__nv_bfloat16>(a, b, tc);
+    if (used) *used = tc ? GDN_IMPL_TC : GDN_IMPL_SIMT;
+    return rc;
+}
+
+gdn_status simt_backward(const FwdArgs &a, const BwdArgs &b) {
+    return run_backward(a, b, GDN_IMPL_SIMT, nullptr);
 }
 
 }  // namespace gdn

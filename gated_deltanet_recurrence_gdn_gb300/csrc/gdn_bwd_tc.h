@@ -1,0 +1,35 @@
+// gdn_bwd_tc.h -- entry points of the backward pass's tensor-core state
+// adjoint (gdn_bwd_tc.cu) and of the prep variant that feeds it.
+#pragma once
+#include <cuda_bf16.h>
+
+#include "gdn_internal.h"
+
+namespace gdn {
+
+// The general path's chunk prep (as enqueue_simt_prep, bf16 I/O only) that
+// also writes W as bf16 rows [rows][d_k] into Wb, the bulk-copy source of the
+// tensor-core state adjoint.
+gdn_status enqueue_simt_prep_w16(const FwdArgs &a, const int2 *table, float *W, float *U,
+                                 float *G, float *Tout, __nv_bfloat16 *Wb);
+
+// Whether the tensor-core state adjoint takes this call: bf16 I/O, a scalar
+// gate, d_k 64 or 128, d_v a multiple of 64 (at most 256), an sm_10x device.
+bool tc_bwd_supported(const FwdArgs &a);
+
+// The state adjoint dS carried backwards through every sequence's chunks on
+// tcgen05 products (bf16 operands, fp32 accumulation): stores the adjoint of
+// each chunk's end state as dHc [H][chunk_slots][d_k][d_v] (transposed, dH =
+// dS^T) and the rows of dV' as dVn [rows][d_v] (fp32), and dh0 when the
+// backward arguments ask for it.  G is the in-chunk gate cumsum [rows] and Wb
+// the bf16 W of the prep.
+gdn_status tc_bwd_dstate(const FwdArgs &a, const BwdArgs &b, const __nv_bfloat16 *Wb,
+                         const float *G, float *dVn, float *dHc);
+
+// The backward pass (gdn_bwd.cu) under an implementation choice: GDN_IMPL_SIMT
+// keeps every kernel on warp-level mma.sync; GDN_IMPL_AUTO takes the
+// tensor-core state adjoint where it fits; GDN_IMPL_TC requires it
+// (GDN_ERR_UNSUPPORTED otherwise).  *used (optional) gets the choice taken.
+gdn_status run_backward(const FwdArgs &a, const BwdArgs &b, long long impl, int *used);
+
+}  // namespace gdn

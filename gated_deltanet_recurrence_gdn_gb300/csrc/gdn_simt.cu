@@ -34,6 +34,7 @@
 #include <mutex>
 #include <type_traits>
 
+#include "gdn_bwd_tc.h"
 #include "gdn_internal.h"
 #include "gdn_mma.cuh"
 #include "gdn_tile.cuh"
@@ -257,7 +258,8 @@ k_state_mma(FwdArgs a, const float *__restrict__ W, const float *__restrict__ U,
 // T = (I + A)^{-1} by blocks -- the four 16 x 16 diagonal blocks by forward
 // substitution, then T21 = -T22 A21 T11 merges 16 -> 32 -> 64 -- and
 // W = T diag(beta gamma) K, U = T diag(beta) V.  With Tout non-null it also
-// stores T as [rows][64] (the backward pass reads it).
+// stores T as [rows][64], with Wb non-null a bf16 copy of W (the backward
+// pass reads them).
 size_t prep_mma_smem(int dk, int dv) {
     return sizeof(float) * ((size_t)kChunk * (dk + 4) + (size_t)kChunk * (dv + 4) +
                             2 * kChunk * kLdc + 32 * 36 + 3 * kChunk);
@@ -266,7 +268,8 @@ size_t prep_mma_smem(int dk, int dv) {
 template <typename TIn, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 2)
 k_prep_mma(FwdArgs a, const int2 *__restrict__ table, float *__restrict__ W,
-           float *__restrict__ U, float *__restrict__ G, float *__restrict__ Tout, int *err) {
+           float *__restrict__ U, float *__restrict__ G, float *__restrict__ Tout,
+           __nv_bfloat16 *__restrict__ Wb, int *err) {
     extern __shared__ float smem[];
     const int dk = a.dk, dv = a.dv, tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
@@ -403,7 +406,10 @@ k_prep_mma(FwdArgs a, const int2 *__restrict__ table, float *__restrict__ W,
         if (erase)
             mma::gemm_s<8, SPLIT>(acc, Tm, kLdc, 1, wb, Ks, ldk, 1, m0, nh, 2, dk, m0 + 16, lane);
         mma::for_each(acc, m0, nh, 2, dk, lane, [&](int r, int j, float &x) {
-            if (r < L) W[(r0 + r) * dk + j] = x;
+            if (r < L) {
+                W[(r0 + r) * dk + j] = x;
+                if (Wb) Wb[(r0 + r) * dk + j] = __float2bfloat16_rn(x);
+            }
         });
     }
     for (int c0 = 0; c0 < dv; c0 += 128) {   // U = T diag(beta) V
@@ -786,7 +792,7 @@ k_state_vg(FwdArgs a, const float *__restrict__ W, const float *__restrict__ U,
 // dimension needs, else unused).
 template <typename TIn>
 cudaError_t run_prep(const FwdArgs &a, const int2 *table, float *W, float *U, float *G,
-                     float *Tout, float *P, int *err) {
+                     float *Tout, float *P, int *err, __nv_bfloat16 *Wb = nullptr) {
     constexpr bool kSplit = std::is_same<TIn, float>::value;   // fp32 I/O: 3xTF32
     const dim3 grid(a.chunk_slots, a.sm.H);
     cudaError_t e;
@@ -801,7 +807,8 @@ cudaError_t run_prep(const FwdArgs &a, const int2 *table, float *W, float *U, fl
         e = cudaFuncSetAttribute(k_prep_mma<TIn, kSplit>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psm);
         if (e != cudaSuccess) return e;
-        k_prep_mma<TIn, kSplit><<<grid, kThreads, psm, a.stream>>>(a, table, W, U, G, Tout, err);
+        k_prep_mma<TIn, kSplit><<<grid, kThreads, psm, a.stream>>>(a, table, W, U, G, Tout, Wb,
+                                                                  err);
     }
     count_launch();
     return cudaGetLastError();
@@ -901,9 +908,9 @@ gdn_status enqueue_state_t(const FwdArgs &a, const float *W, const float *U, con
 
 template <typename TIn>
 gdn_status enqueue_prep_t(const FwdArgs &a, const int2 *table, float *W, float *U, float *G,
-                          float *Tout) {
+                          float *Tout, __nv_bfloat16 *Wb = nullptr) {
     if (a.chunk_slots > 0 && a.sm.H > 0 &&
-        run_prep<TIn>(a, table, W, U, G, Tout, nullptr, device_error_word()) != cudaSuccess)
+        run_prep<TIn>(a, table, W, U, G, Tout, nullptr, device_error_word(), Wb) != cudaSuccess)
         return GDN_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
@@ -913,6 +920,12 @@ gdn_status enqueue_simt_prep(const FwdArgs &a, const int2 *table, float *W, floa
     if (a.vector_gate) return GDN_ERR_UNSUPPORTED;
     return a.dt == GDN_F32 ? enqueue_prep_t<float>(a, table, W, U, G, Tout)
                            : enqueue_prep_t<__nv_bfloat16>(a, table, W, U, G, Tout);
+}
+
+gdn_status enqueue_simt_prep_w16(const FwdArgs &a, const int2 *table, float *W, float *U,
+                                 float *G, float *Tout, __nv_bfloat16 *Wb) {
+    if (a.vector_gate || a.dt != GDN_BF16) return GDN_ERR_UNSUPPORTED;
+    return enqueue_prep_t<__nv_bfloat16>(a, table, W, U, G, Tout, Wb);
 }
 
 gdn_status enqueue_simt_state(const FwdArgs &a, const float *W, const float *U, const float *G,

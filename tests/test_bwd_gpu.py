@@ -40,6 +40,14 @@ def _compare(got, ref, io, skip=()):
     return errs
 
 
+def _expected_impl(io, dk, dv, impl):
+    """The state adjoint the backward takes: the tcgen05 kernel for bf16 I/O
+    with d_k 64 or 128 and d_v a multiple of 64, unless mma.sync is forced."""
+    tc_fits = io == "bf16" and dk in (64, 128) and dv % 64 == 0
+    return gdn.GDN_IMPL_TC if (tc_fits and impl != gdn.GDN_IMPL_SIMT) else gdn.GDN_IMPL_SIMT
+
+
+@pytest.mark.parametrize("impl", [gdn.GDN_IMPL_AUTO, gdn.GDN_IMPL_SIMT], ids=["auto", "simt"])
 @pytest.mark.parametrize("erase", [True, False])
 @pytest.mark.parametrize("B,H,T,dk,dv,io", [(1, 2, 130, 64, 64, "f32"),
                                             (2, 2, 257, 64, 64, "bf16"),
@@ -47,26 +55,31 @@ def _compare(got, ref, io, skip=()):
                                             (1, 3, 200, 64, 128, "bf16"),
                                             (2, 1, 150, 32, 48, "f32"),
                                             (1, 1, 64, 128, 256, "bf16")])
-def test_bwd_matches_oracle(erase, B, H, T, dk, dv, io):
+def test_bwd_matches_oracle(impl, erase, B, H, T, dk, dv, io):
     x = synth.make_dense(B, H, T, dk, dv, io=io, h0_std=0.1, seed=T + 61, device="cuda")
     dout, dhT = _weights(x, T + 62)
-    got = gdn.gdn_bwd(x.q, x.k, x.v, x.log_alpha, x.beta, x.h0, dout, dhT, erase=erase,
-                      check=True)
-    U.sync()
+    with gdn.use_impl(impl):
+        got = gdn.gdn_bwd(x.q, x.k, x.v, x.log_alpha, x.beta, x.h0, dout, dhT, erase=erase,
+                          check=True)
+        U.sync()
+    assert gdn.last_impl() == _expected_impl(io, dk, dv, impl)
     ref = oracle.gdn_bwd(U.f64(x.q), U.f64(x.k), U.f64(x.v), U.f64(x.log_alpha),
                          U.f64(x.beta), U.f64(x.h0), U.f64(dout), U.f64(dhT),
                          threads=U.ORACLE_THREADS, erase=erase)
     _compare(got, ref, io)
 
 
+@pytest.mark.parametrize("impl", [gdn.GDN_IMPL_AUTO, gdn.GDN_IMPL_SIMT], ids=["auto", "simt"])
 @pytest.mark.parametrize("erase", [True, False])
-def test_bwd_varlen_matches_oracle(erase):
+def test_bwd_varlen_matches_oracle(impl, erase):
     y = synth.make_varlen([1, 63, 64, 65, 200, 0, 129], 2, 128, 128, io="bf16", h0_std=0.1,
                           seed=71, device="cuda")
     dout, dhT = _weights(y, 72, packed=True)
-    got = gdn.gdn_bwd_varlen(y.q, y.k, y.v, y.log_alpha, y.beta, y.cu_seqlens, y.h0, dout,
-                             dhT, erase=erase, check=True)
-    U.sync()
+    with gdn.use_impl(impl):
+        got = gdn.gdn_bwd_varlen(y.q, y.k, y.v, y.log_alpha, y.beta, y.cu_seqlens, y.h0, dout,
+                                 dhT, erase=erase, check=True)
+        U.sync()
+    assert gdn.last_impl() == _expected_impl("bf16", 128, 128, impl)
     ref = oracle.gdn_bwd_varlen(U.f64(y.q), U.f64(y.k), U.f64(y.v), U.f64(y.log_alpha),
                                 U.f64(y.beta), y.cu_seqlens.cpu().numpy(), U.f64(y.h0),
                                 U.f64(dout), U.f64(dhT), erase=erase)
@@ -123,7 +136,7 @@ def test_bwd_full_size_sampled_heads():
         _compare([t[b:b + 1, h:h + 1] for t in got], ref, "bf16")
 
 
-def test_bwd_vector_gate_and_forced_tc_are_unsupported():
+def test_bwd_vector_gate_and_forced_tc_outside_its_shapes_are_unsupported():
     x = synth.make_dense(1, 1, 64, 64, 64, io="bf16", seed=79, device="cuda")
     dout, dhT = _weights(x, 80)
     lib = gdn.load()
@@ -134,10 +147,37 @@ def test_bwd_vector_gate_and_forced_tc_are_unsupported():
                      ptr(dout), ptr(dhT), *(ptr(t) for t in g), None, 1, 1, 64, 64, 64, 64,
                      gdn.GDN_BF16, gdn.GDN_FLAG_VECTOR_GATE, stream)
     assert rc == gdn.GDN_ERR_UNSUPPORTED
+    # the tcgen05 state adjoint takes bf16 I/O only: forced on fp32 I/O it refuses
+    xf = synth.make_dense(1, 1, 64, 64, 64, io="f32", seed=79, device="cuda")
+    doutf, dhTf = _weights(xf, 80)
     with gdn.use_impl(gdn.GDN_IMPL_TC):
         with pytest.raises(gdn.GdnError) as e:
-            gdn.gdn_bwd(x.q, x.k, x.v, x.log_alpha, x.beta, None, dout, dhT)
-    assert e.value.status == gdn.GDN_ERR_UNSUPPORTED
+            gdn.gdn_bwd(xf.q, xf.k, xf.v, xf.log_alpha, xf.beta, None, doutf, dhTf)
+        assert e.value.status == gdn.GDN_ERR_UNSUPPORTED
+        # and runs where it fits
+        gdn.gdn_bwd(x.q, x.k, x.v, x.log_alpha, x.beta, None, dout, dhT, check=True)
+        U.sync()
+    assert gdn.last_impl() == gdn.GDN_IMPL_TC
+
+
+@pytest.mark.parametrize("impl", [gdn.GDN_IMPL_AUTO, gdn.GDN_IMPL_SIMT], ids=["auto", "simt"])
+def test_bwd_steep_decay_matches_oracle(impl):
+    # log gates of -3 per step in the second and fourth chunks: their total log
+    # decay is below -80, where exp(-g_s) would overflow, so those chunks take
+    # the unscaled-dO branch of the tensor-core state adjoint; the others the
+    # gamma dO one
+    x = synth.make_dense(1, 2, 256, 128, 128, io="bf16", h0_std=0.1, seed=83, device="cuda")
+    la = x.log_alpha.clone()
+    la[..., 64:128] = -3.0
+    la[..., 192:256] = -3.0
+    dout, dhT = _weights(x, 84)
+    with gdn.use_impl(impl):
+        got = gdn.gdn_bwd(x.q, x.k, x.v, la, x.beta, x.h0, dout, dhT, check=True)
+        U.sync()
+    assert gdn.last_impl() == _expected_impl("bf16", 128, 128, impl)
+    ref = oracle.gdn_bwd(U.f64(x.q), U.f64(x.k), U.f64(x.v), U.f64(la), U.f64(x.beta),
+                         U.f64(x.h0), U.f64(dout), U.f64(dhT))
+    _compare(got, ref, "bf16")
 
 
 def test_bwd_long_sequence_adjoint_identity():
