@@ -192,7 +192,7 @@ def load_peaks():
 
 # the sources each timed kernel is built from (its file and the headers it includes)
 KERNEL_SOURCES = {
-    "k_gdn_tc": ["gdn_tc.cu", "tc_common.cuh", "tc_ptx.cuh", "gdn_internal.h"],
+    "k_gdn_tc": ["gdn_tc.cu", "gdn_bwd_tc.h", "tc_common.cuh", "tc_ptx.cuh", "gdn_internal.h"],
     "k_bwd_dstate_tc": ["gdn_bwd_tc.cu", "gdn_bwd_tc.h", "tc_common.cuh", "tc_ptx.cuh",
                         "gdn_internal.h"],
     "k_gdn_prep": ["gdn_prep.cu", "tc_ptx.cuh", "gdn_internal.h"],

@@ -679,7 +679,8 @@ gdn_status launch_bwd(const FwdArgs &a, const BwdArgs &b, bool tc_dstate) {
         return GDN_ERR_CUDA;
     float *W = nullptr, *U = nullptr, *G = nullptr, *Vn = nullptr, *dVn = nullptr;
     float *Hst = nullptr, *dHc = nullptr, *Tg = nullptr;
-    __nv_bfloat16 *Wb = nullptr;   // bf16 W, the tensor-core state adjoint's input
+    // bf16 T diag(beta) [rows][64] then W [rows][d_k]: the tensor-core kernels' input
+    __nv_bfloat16 *Tb = nullptr;
     int2 *table = nullptr;
     float **bufs[] = {&W, &U, &G, &Vn, &dVn, &Hst, &dHc, &Tg};
     const size_t sizes[] = {rows * a.dk, rows * a.dv, rows, rows * a.dv, rows * a.dv,
@@ -689,8 +690,10 @@ gdn_status launch_bwd(const FwdArgs &a, const BwdArgs &b, bool tc_dstate) {
         if (scratch_alloc((void **)bufs[i], sizes[i] * sizeof(float), st) != cudaSuccess)
             rc = GDN_ERR_CUDA;
     if (rc == GDN_OK && tc_dstate &&
-        scratch_alloc((void **)&Wb, rows * a.dk * sizeof(__nv_bfloat16), st) != cudaSuccess)
+        scratch_alloc((void **)&Tb, rows * (kChunk + a.dk) * sizeof(__nv_bfloat16), st) !=
+            cudaSuccess)
         rc = GDN_ERR_CUDA;
+    __nv_bfloat16 *Wb = Tb ? Tb + rows * kChunk : nullptr;
     if (rc == GDN_OK && a.sm.cu && a.chunk_slots > 0) {
         if (scratch_alloc((void **)&table, sizeof(int2) * (size_t)a.chunk_slots, st) !=
             cudaSuccess)
@@ -699,13 +702,16 @@ gdn_status launch_bwd(const FwdArgs &a, const BwdArgs &b, bool tc_dstate) {
             rc = enqueue_chunk_table(a, table);
     }
     if (rc == GDN_OK)
-        rc = tc_dstate ? enqueue_simt_prep_w16(a, table, W, U, G, Tg, Wb)
+        rc = tc_dstate ? enqueue_simt_prep_tc(a, table, W, U, G, Tg, Tb, Wb)
                        : enqueue_simt_prep(a, table, W, U, G, Tg);
     if (rc == GDN_OK) {
         FwdArgs f = a;
         f.o = nullptr;
         f.hT = nullptr;
-        rc = enqueue_simt_state(f, W, U, G, Hst, Vn);
+        // the states and V' from the forward's fused kernel where the
+        // tensor-core adjoint runs (the same bf16-operand products), else
+        // from the general path's state pass
+        rc = tc_dstate ? tc_state_pass(f, Tb, Hst, Vn) : enqueue_simt_state(f, W, U, G, Hst, Vn);
     }
     if (rc == GDN_OK && tc_dstate) {
         rc = tc_bwd_dstate(a, b, Wb, G, dVn, dHc);
@@ -724,7 +730,7 @@ gdn_status launch_bwd(const FwdArgs &a, const BwdArgs &b, bool tc_dstate) {
     if (rc == GDN_OK && cudaGetLastError() != cudaSuccess) rc = GDN_ERR_CUDA;
     for (float **p : bufs)
         if (*p) scratch_free(*p, st);
-    if (Wb) scratch_free(Wb, st);
+    if (Tb) scratch_free(Tb, st);
     if (table) scratch_free(table, st);
     return rc;
 }
@@ -735,7 +741,7 @@ gdn_status run_backward(const FwdArgs &a, const BwdArgs &b, long long impl, int 
     if (a.vector_gate) return GDN_ERR_UNSUPPORTED;
     if (chunk_lay(a.dk).bytes > 227 * 1024 || dstate_smem(a.dk) > 227 * 1024)
         return GDN_ERR_UNSUPPORTED;
-    const bool tc = impl != GDN_IMPL_SIMT && tc_bwd_supported(a);
+    const bool tc = impl != GDN_IMPL_SIMT && tc_bwd_supported(a) && tc_supported(a);
     if (impl == GDN_IMPL_TC && !tc) return GDN_ERR_UNSUPPORTED;
     const gdn_status rc = a.dt == GDN_F32 ? launch_bwd<float>(a, b, false)
                                           : launch_bwd<__nv_bfloat16>(a, b, tc);

@@ -8,10 +8,17 @@
 namespace gdn {
 
 // The general path's chunk prep (as enqueue_simt_prep, bf16 I/O only) that
-// also writes W as bf16 rows [rows][d_k] into Wb, the bulk-copy source of the
-// tensor-core state adjoint.
-gdn_status enqueue_simt_prep_w16(const FwdArgs &a, const int2 *table, float *W, float *U,
-                                 float *G, float *Tout, __nv_bfloat16 *Wb);
+// also writes, for the tensor-core kernels, T diag(beta) as bf16 rows
+// [rows][64] into Tub and W as bf16 rows [rows][d_k] into Wb.
+gdn_status enqueue_simt_prep_tc(const FwdArgs &a, const int2 *table, float *W, float *U,
+                                float *G, float *Tout, __nv_bfloat16 *Tub, __nv_bfloat16 *Wb);
+
+// The forward's fused tcgen05 kernel as the backward's state pass: no output,
+// every chunk's starting state H = S^T into Hst [H][chunk_slots][d_k][d_v] and
+// the rows of V' into Vst [rows][d_v] (fp32).  Tbuf holds T diag(beta) then W
+// (bf16, as enqueue_simt_prep_tc writes them, Wb = Tbuf + rows * 64).
+// GDN_ERR_UNSUPPORTED where the fused kernel does not take the call.
+gdn_status tc_state_pass(const FwdArgs &a, const __nv_bfloat16 *Tbuf, float *Hst, float *Vst);
 
 // Whether the tensor-core state adjoint takes this call: bf16 I/O, a scalar
 // gate, d_k 64 or 128, d_v a multiple of 64 (at most 256), an sm_10x device.

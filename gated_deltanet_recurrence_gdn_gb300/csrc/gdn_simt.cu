@@ -258,8 +258,8 @@ k_state_mma(FwdArgs a, const float *__restrict__ W, const float *__restrict__ U,
 // T = (I + A)^{-1} by blocks -- the four 16 x 16 diagonal blocks by forward
 // substitution, then T21 = -T22 A21 T11 merges 16 -> 32 -> 64 -- and
 // W = T diag(beta gamma) K, U = T diag(beta) V.  With Tout non-null it also
-// stores T as [rows][64], with Wb non-null a bf16 copy of W (the backward
-// pass reads them).
+// stores T as [rows][64], with Tub and Wb non-null T diag(beta) and W as bf16
+// rows (the backward pass reads them).
 size_t prep_mma_smem(int dk, int dv) {
     return sizeof(float) * ((size_t)kChunk * (dk + 4) + (size_t)kChunk * (dv + 4) +
                             2 * kChunk * kLdc + 32 * 36 + 3 * kChunk);
@@ -269,7 +269,7 @@ template <typename TIn, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 2)
 k_prep_mma(FwdArgs a, const int2 *__restrict__ table, float *__restrict__ W,
            float *__restrict__ U, float *__restrict__ G, float *__restrict__ Tout,
-           __nv_bfloat16 *__restrict__ Wb, int *err) {
+           __nv_bfloat16 *__restrict__ Tub, __nv_bfloat16 *__restrict__ Wb, int *err) {
     extern __shared__ float smem[];
     const int dk = a.dk, dv = a.dv, tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
@@ -405,12 +405,26 @@ k_prep_mma(FwdArgs a, const int2 *__restrict__ table, float *__restrict__ W,
         mma::zero(acc);
         if (erase)
             mma::gemm_s<8, SPLIT>(acc, Tm, kLdc, 1, wb, Ks, ldk, 1, m0, nh, 2, dk, m0 + 16, lane);
-        mma::for_each(acc, m0, nh, 2, dk, lane, [&](int r, int j, float &x) {
-            if (r < L) {
-                W[(r0 + r) * dk + j] = x;
-                if (Wb) Wb[(r0 + r) * dk + j] = __float2bfloat16_rn(x);
+        // adjacent column pairs of the accumulator, stored as pairs
+        const int gq = lane >> 2, tq = lane & 3;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int n8 = 8 * (nh + 2 * i);
+            if (n8 < dk) {
+#pragma unroll
+                for (int hr = 0; hr < 2; ++hr) {
+                    const int r = m0 + gq + 8 * hr;
+                    if (r < L) {
+                        const long long o = (r0 + r) * dk + n8 + 2 * tq;
+                        const float x0 = acc[i][2 * hr], x1 = acc[i][2 * hr + 1];
+                        *reinterpret_cast<float2 *>(W + o) = make_float2(x0, x1);
+                        if (Wb)
+                            *reinterpret_cast<__nv_bfloat162 *>(Wb + o) =
+                                __floats2bfloat162_rn(x0, x1);
+                    }
+                }
             }
-        });
+        }
     }
     for (int c0 = 0; c0 < dv; c0 += 128) {   // U = T diag(beta) V
         float acc[8][4];
@@ -427,6 +441,13 @@ k_prep_mma(FwdArgs a, const int2 *__restrict__ table, float *__restrict__ W,
         for (int i = tid; i < kChunk * kChunk; i += kThreads) {
             const int r = i >> 6, s = i & 63;
             if (r < L) Tout[(r0 + r) * kChunk + s] = Tm[r * kLdc + s];
+        }
+    if (Tub)   // T diag(beta), column pairs
+        for (int i = tid; i < kChunk * kChunk / 2; i += kThreads) {
+            const int r = i >> 5, s = 2 * (i & 31);
+            if (r < L)
+                *reinterpret_cast<__nv_bfloat162 *>(Tub + (r0 + r) * kChunk + s) =
+                    __floats2bfloat162_rn(Tm[r * kLdc + s] * bb[s], Tm[r * kLdc + s + 1] * bb[s + 1]);
         }
 }
 
@@ -792,7 +813,8 @@ k_state_vg(FwdArgs a, const float *__restrict__ W, const float *__restrict__ U,
 // dimension needs, else unused).
 template <typename TIn>
 cudaError_t run_prep(const FwdArgs &a, const int2 *table, float *W, float *U, float *G,
-                     float *Tout, float *P, int *err, __nv_bfloat16 *Wb = nullptr) {
+                     float *Tout, float *P, int *err, __nv_bfloat16 *Tub = nullptr,
+                     __nv_bfloat16 *Wb = nullptr) {
     constexpr bool kSplit = std::is_same<TIn, float>::value;   // fp32 I/O: 3xTF32
     const dim3 grid(a.chunk_slots, a.sm.H);
     cudaError_t e;
@@ -807,8 +829,8 @@ cudaError_t run_prep(const FwdArgs &a, const int2 *table, float *W, float *U, fl
         e = cudaFuncSetAttribute(k_prep_mma<TIn, kSplit>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psm);
         if (e != cudaSuccess) return e;
-        k_prep_mma<TIn, kSplit><<<grid, kThreads, psm, a.stream>>>(a, table, W, U, G, Tout, Wb,
-                                                                  err);
+        k_prep_mma<TIn, kSplit><<<grid, kThreads, psm, a.stream>>>(a, table, W, U, G, Tout, Tub,
+                                                                  Wb, err);
     }
     count_launch();
     return cudaGetLastError();
@@ -908,9 +930,10 @@ gdn_status enqueue_state_t(const FwdArgs &a, const float *W, const float *U, con
 
 template <typename TIn>
 gdn_status enqueue_prep_t(const FwdArgs &a, const int2 *table, float *W, float *U, float *G,
-                          float *Tout, __nv_bfloat16 *Wb = nullptr) {
+                          float *Tout, __nv_bfloat16 *Tub = nullptr, __nv_bfloat16 *Wb = nullptr) {
     if (a.chunk_slots > 0 && a.sm.H > 0 &&
-        run_prep<TIn>(a, table, W, U, G, Tout, nullptr, device_error_word(), Wb) != cudaSuccess)
+        run_prep<TIn>(a, table, W, U, G, Tout, nullptr, device_error_word(), Tub, Wb) !=
+            cudaSuccess)
         return GDN_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
@@ -922,10 +945,10 @@ gdn_status enqueue_simt_prep(const FwdArgs &a, const int2 *table, float *W, floa
                            : enqueue_prep_t<__nv_bfloat16>(a, table, W, U, G, Tout);
 }
 
-gdn_status enqueue_simt_prep_w16(const FwdArgs &a, const int2 *table, float *W, float *U,
-                                 float *G, float *Tout, __nv_bfloat16 *Wb) {
+gdn_status enqueue_simt_prep_tc(const FwdArgs &a, const int2 *table, float *W, float *U,
+                                float *G, float *Tout, __nv_bfloat16 *Tub, __nv_bfloat16 *Wb) {
     if (a.vector_gate || a.dt != GDN_BF16) return GDN_ERR_UNSUPPORTED;
-    return enqueue_prep_t<__nv_bfloat16>(a, table, W, U, G, Tout, Wb);
+    return enqueue_prep_t<__nv_bfloat16>(a, table, W, U, G, Tout, Tub, Wb);
 }
 
 gdn_status enqueue_simt_state(const FwdArgs &a, const float *W, const float *U, const float *G,

@@ -41,6 +41,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include "gdn_bwd_tc.h"
 #include "gdn_internal.h"
 #include "tc_common.cuh"
 #include "tc_ptx.cuh"
@@ -141,9 +142,18 @@ struct TcParams {
     // h0 = identity (d_k x d_k state), final state into hT2 with width dv2.
     int xsplit, dv2;
     float *hT2;
+    // State pass for the backward (no segments): every chunk's starting state
+    // H = S^T as [H][chunk_slots][d_k][d_v] and the rows of V' as [rows][d_v],
+    // fp32; null: not stored.  Chunk slot: dense n * max_chunks + c, packed
+    // floor(cu[n] / 64) + n + c.
+    float *Hst, *Vst;
+    long long chunk_slots;
+    int max_chunks;
 };
 
-template <int DK>
+// STATES: the backward's state pass (stores Hst / Vst); a separate
+// instantiation, so the forward's kernel carries none of it.
+template <int DK, bool STATES>
 __global__ void __launch_bounds__(kThreadsTC, 1)
 k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
          const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_t,
@@ -199,6 +209,7 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
     const int dvs = lin ? p.dv2 : p.dv;                  // width of this CTA's state
     float *hTp = lin ? p.hT2 : p.hT;
     const long long srow = ((long long)n * p.sm.H + h) * dvs;   // state row of (n, h)
+    const long long slot0 = p.sm.cu ? (long long)(ytok0 / kC) + n : (long long)n * p.max_chunks;
 
     if (warp == 9) {
         tmem_alloc(misc, 512);
@@ -274,6 +285,14 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
             TRACE(0, j, 0, t == 0);
             // (i) publish H as the bf16 B operand of the chain MMA
             if (t < DK) put_row64(Hs, t, hreg);
+            if (STATES && t < DK) {   // the chunk's starting state, for the backward
+                float4 *dst = reinterpret_cast<float4 *>(
+                    p.Hst + ((h * p.chunk_slots + slot0 + j) * DK + t) * (long long)p.dv + dv0);
+#pragma unroll
+                for (int q = 0; q < 16; ++q)
+                    dst[q] = make_float4(hreg[4 * q], hreg[4 * q + 1], hreg[4 * q + 2],
+                                         hreg[4 * q + 3]);
+            }
             fence_proxy_async_smem();
             tc_fence_before();
             named_bar(1, 128);
@@ -315,6 +334,14 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
                     for (int i = 0; i < 32; ++i) {
                         vn[i] = f32(u[i]) - f32(wh[i]);
                         vt[i] = vn[i] * ev;
+                    }
+                    if (STATES && t < min(kC, len - j * kC)) {
+                        float4 *dst = reinterpret_cast<float4 *>(
+                            p.Vst + (row0 + (long long)j * kC + t) * p.dv + dv0 + 32 * half);
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            dst[q] = make_float4(vn[4 * q], vn[4 * q + 1], vn[4 * q + 2],
+                                                 vn[4 * q + 3]);
                     }
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
@@ -691,6 +718,7 @@ struct LaunchCfg {
     int lin_tiles;
     float *hT2;
     bool timed;
+    float *Hst = nullptr, *Vst = nullptr;   // the backward's state pass
 };
 
 template <int DK>
@@ -706,7 +734,9 @@ gdn_status launch_tc(const FwdArgs &a, const __nv_bfloat16 *Tin, const LaunchCfg
         return GDN_ERR_CUDA;
     static bool attr_set = false;
     if (!attr_set) {
-        if (cudaFuncSetAttribute(k_gdn_tc<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(k_gdn_tc<DK, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 L::ALLOC) != cudaSuccess ||
+            cudaFuncSetAttribute(k_gdn_tc<DK, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  L::ALLOC) != cudaSuccess)
             return GDN_ERR_CUDA;
         attr_set = true;
@@ -728,6 +758,10 @@ gdn_status launch_tc(const FwdArgs &a, const __nv_bfloat16 *Tin, const LaunchCfg
     p.xsplit = a.dv / kNV;
     p.dv2 = DK;
     p.hT2 = c.hT2;
+    p.Hst = c.Hst;
+    p.Vst = c.Vst;
+    p.chunk_slots = a.chunk_slots;
+    p.max_chunks = a.max_chunks;
     dim3 grid(a.dv / kNV + c.lin_tiles, a.sm.H, c.nseq);
     const int slot = c.timed ? timer_begin(a.stream, "k_gdn_tc") : -1;
     // launched as a programmatic dependent of the previous kernel: its
@@ -742,7 +776,9 @@ gdn_status launch_tc(const FwdArgs &a, const __nv_bfloat16 *Tin, const LaunchCfg
     cfg.stream = a.stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t le = cudaLaunchKernelEx(&cfg, k_gdn_tc<DK>, mq, mk, mv, mt, mw, p);
+    const cudaError_t le =
+        c.Hst ? cudaLaunchKernelEx(&cfg, k_gdn_tc<DK, true>, mq, mk, mv, mt, mw, p)
+              : cudaLaunchKernelEx(&cfg, k_gdn_tc<DK, false>, mq, mk, mv, mt, mw, p);
     timer_end(slot, a.stream);
     if (le != cudaSuccess) return GDN_ERR_CUDA;
     count_launch();
@@ -921,6 +957,12 @@ gdn_status tc_forward(const FwdArgs &a) {
     scratch_free(Tbuf, st);
     if (table) scratch_free(table, st);
     return rc;
+}
+
+gdn_status tc_state_pass(const FwdArgs &a, const __nv_bfloat16 *Tbuf, float *Hst, float *Vst) {
+    if (!tc_supported(a)) return GDN_ERR_UNSUPPORTED;
+    LaunchCfg c{a.sm.N, 0, 0, 1, a.h0, nullptr, 0, nullptr, false, Hst, Vst};
+    return a.dk == 128 ? launch_tc<128>(a, Tbuf, c) : launch_tc<64>(a, Tbuf, c);
 }
 
 }  // namespace gdn
