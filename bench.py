@@ -195,7 +195,7 @@ KERNEL_SOURCES = {
     "k_gdn_tc": ["gdn_tc.cu", "gdn_bwd_tc.h", "tc_common.cuh", "tc_ptx.cuh", "gdn_internal.h"],
     "k_bwd_dstate_tc": ["gdn_bwd_tc.cu", "gdn_bwd_tc.h", "tc_common.cuh", "tc_ptx.cuh",
                         "gdn_internal.h"],
-    "k_gdn_prep": ["gdn_prep.cu", "tc_ptx.cuh", "gdn_internal.h"],
+    "k_gdn_prep": ["gdn_prep.cu", "gdn_bwd_tc.h", "tc_ptx.cuh", "gdn_internal.h"],
     "k_gdn_decode": ["gdn_decode.cu", "gdn_internal.h"],
     "k_bwd_chunk": ["gdn_bwd.cu", "gdn_internal.h", "gdn_mma.cuh", "gdn_tile.cuh"],
     "k_state_mma": ["gdn_simt.cu", "gdn_internal.h", "gdn_mma.cuh", "gdn_tile.cuh"],

@@ -682,11 +682,14 @@ gdn_status launch_bwd(const FwdArgs &a, const BwdArgs &b, bool tc_dstate) {
     // bf16 T diag(beta) [rows][64] then W [rows][d_k]: the tensor-core kernels' input
     __nv_bfloat16 *Tb = nullptr;
     int2 *table = nullptr;
+    // with the erase term the tensor-core path's prep (gdn_prep.cu) gives
+    // every input the tensor-core kernels and k_bwd_chunk read: no fp32 W, U
+    const bool tc_prep = tc_dstate && !a.no_erase;
     float **bufs[] = {&W, &U, &G, &Vn, &dVn, &Hst, &dHc, &Tg};
     const size_t sizes[] = {rows * a.dk, rows * a.dv, rows, rows * a.dv, rows * a.dv,
                             states > 0 ? states : 1, states > 0 ? states : 1, rows * kChunk};
     gdn_status rc = GDN_OK;
-    for (int i = 0; i < 8 && rc == GDN_OK; ++i)
+    for (int i = tc_prep ? 2 : 0; i < 8 && rc == GDN_OK; ++i)
         if (scratch_alloc((void **)bufs[i], sizes[i] * sizeof(float), st) != cudaSuccess)
             rc = GDN_ERR_CUDA;
     if (rc == GDN_OK && tc_dstate &&
@@ -702,8 +705,9 @@ gdn_status launch_bwd(const FwdArgs &a, const BwdArgs &b, bool tc_dstate) {
             rc = enqueue_chunk_table(a, table);
     }
     if (rc == GDN_OK)
-        rc = tc_dstate ? enqueue_simt_prep_tc(a, table, W, U, G, Tg, Tb, Wb)
-                       : enqueue_simt_prep(a, table, W, U, G, Tg);
+        rc = tc_prep     ? enqueue_tc_prep_bwd(a, table, Tb, Wb, Tg, G)
+             : tc_dstate ? enqueue_simt_prep_tc(a, table, W, U, G, Tg, Tb, Wb)
+                         : enqueue_simt_prep(a, table, W, U, G, Tg);
     if (rc == GDN_OK) {
         FwdArgs f = a;
         f.o = nullptr;

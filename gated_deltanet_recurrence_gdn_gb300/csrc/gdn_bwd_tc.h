@@ -13,6 +13,14 @@ namespace gdn {
 gdn_status enqueue_simt_prep_tc(const FwdArgs &a, const int2 *table, float *W, float *U,
                                 float *G, float *Tout, __nv_bfloat16 *Tub, __nv_bfloat16 *Wb);
 
+// The tensor-core path's chunk prep (gdn_prep.cu) for the backward pass with
+// the erase term: T diag(beta) and W as bf16 rows into Tu and W (as for the
+// forward), T itself as fp32 rows [rows][64] into T_out and the in-chunk gate
+// cumsum [rows] into G_out.  GDN_ERR_UNSUPPORTED without the erase term or
+// outside bf16 I/O with d_k 64 or 128.
+gdn_status enqueue_tc_prep_bwd(const FwdArgs &a, const int2 *table, __nv_bfloat16 *Tu,
+                               __nv_bfloat16 *W, float *T_out, float *G_out);
+
 // The forward's fused tcgen05 kernel as the backward's state pass: no output,
 // every chunk's starting state H = S^T into Hst [H][chunk_slots][d_k][d_v] and
 // the rows of V' into Vst [rows][d_v] (fp32).  Tbuf holds T diag(beta) then W

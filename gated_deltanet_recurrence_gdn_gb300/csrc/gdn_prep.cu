@@ -14,7 +14,8 @@
 // serial).  The kernel writes T_u = T diag(beta) ([rows][64]) and
 // W = T diag(beta gamma) K ([rows][d_k]) as bf16 rows indexed like the token
 // rows of the inputs, so the fused kernel loads them with the same kind of
-// bulk tensor copy as K.
+// bulk tensor copy as K.  For the backward pass it can also write T itself
+// ([rows][64], fp32) and the gate cumsum g ([rows], fp32).
 //
 // Arithmetic: the Gram and W run on bf16 mma.sync tiles (fragments by
 // ldmatrix) with fp32 accumulation (the inputs are bf16 already); the inverse
@@ -30,6 +31,7 @@
 // current one.
 #include <cuda_bf16.h>
 
+#include "gdn_bwd_tc.h"
 #include "gdn_internal.h"
 #include "tc_ptx.cuh"
 
@@ -153,7 +155,8 @@ __global__ void __launch_bounds__(128, 4)
 k_gdn_prep(const __nv_bfloat16 *__restrict__ k, const float *__restrict__ log_alpha,
            const float *__restrict__ beta, SeqMap sm, const int2 *__restrict__ table,
            int max_chunks, int slots, int units, __nv_bfloat16 *__restrict__ Tu_out,
-           __nv_bfloat16 *__restrict__ W_out, int *err) {
+           __nv_bfloat16 *__restrict__ W_out, float *__restrict__ T_out,
+           float *__restrict__ G_out, int *err) {
     using L = PrepLay<DK>;
     extern __shared__ __align__(16) uint8_t smem[];
     __nv_bfloat16 *Ks = reinterpret_cast<__nv_bfloat16 *>(smem + L::OFF_K);
@@ -257,6 +260,10 @@ k_gdn_prep(const __nv_bfloat16 *__restrict__ k, const float *__restrict__ log_al
             gs[160 + lane] = b1 * __expf(la1);
             gs[192 + lane] = __expf(-la0);
             gs[224 + lane] = __expf(-la1);
+            if (G_out) {
+                if (lane < Lc) G_out[r0 + lane] = la0;
+                if (lane + 32 < Lc) G_out[r0 + lane + 32] = la1;
+            }
         }
         __syncthreads();
         long long r0n;
@@ -408,9 +415,11 @@ k_gdn_prep(const __nv_bfloat16 *__restrict__ k, const float *__restrict__ log_al
                     const int r = 16 * w + i;
                     float2 tv = *reinterpret_cast<const float2 *>(Tb + r * LDA + s);
                     if (r < 32 && s >= 32) tv = make_float2(0.f, 0.f);   // T's upper-right block
-                    if (r < Lc)
+                    if (r < Lc) {
                         *reinterpret_cast<uint32_t *>(Tu_out + (r0 + r) * kCp + s) =
                             pack2(tv.x * bs.x, tv.y * bs.y);
+                        if (T_out) *reinterpret_cast<float2 *>(T_out + (r0 + r) * kCp + s) = tv;
+                    }
                     *reinterpret_cast<uint32_t *>(Tw + r * LDT + s) = pack2(tv.x * bg.x, tv.y * bg.y);
                 }
             }
@@ -531,7 +540,7 @@ size_t tc_prep_smem(int dk) {
 namespace {
 template <int DK>
 gdn_status launch_prep(const FwdArgs &a, const int2 *table, __nv_bfloat16 *Tu,
-                       __nv_bfloat16 *W) {
+                       __nv_bfloat16 *W, float *T_out, float *G_out) {
     static int blocks_per_sm[64] = {};   // per device, filled on first use
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return GDN_ERR_CUDA;
@@ -552,7 +561,7 @@ gdn_status launch_prep(const FwdArgs &a, const int2 *table, __nv_bfloat16 *Tu,
     const int grid = (int)(units < blocks_per_sm[dev] ? units : (long long)blocks_per_sm[dev]);
     k_gdn_prep<DK><<<grid, 128, smem, a.stream>>>(
         static_cast<const __nv_bfloat16 *>(a.k), a.log_alpha, a.beta, a.sm, table, a.max_chunks,
-        a.chunk_slots, (int)units, Tu, W, device_error_word());
+        a.chunk_slots, (int)units, Tu, W, T_out, G_out, device_error_word());
     count_launch();
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
@@ -572,7 +581,17 @@ gdn_status enqueue_tc_prep(const FwdArgs &a, const int2 *table, __nv_bfloat16 *T
         count_launch();
         return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
     }
-    return a.dk == 128 ? launch_prep<128>(a, table, Tu, W) : launch_prep<64>(a, table, Tu, W);
+    return a.dk == 128 ? launch_prep<128>(a, table, Tu, W, nullptr, nullptr)
+                       : launch_prep<64>(a, table, Tu, W, nullptr, nullptr);
+}
+
+gdn_status enqueue_tc_prep_bwd(const FwdArgs &a, const int2 *table, __nv_bfloat16 *Tu,
+                               __nv_bfloat16 *W, float *T_out, float *G_out) {
+    if (a.no_erase || a.vector_gate || a.dt != GDN_BF16 || (a.dk != 64 && a.dk != 128))
+        return GDN_ERR_UNSUPPORTED;
+    if (a.chunk_slots <= 0 || a.sm.H <= 0) return GDN_OK;
+    return a.dk == 128 ? launch_prep<128>(a, table, Tu, W, T_out, G_out)
+                       : launch_prep<64>(a, table, Tu, W, T_out, G_out);
 }
 
 }  // namespace gdn
