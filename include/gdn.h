@@ -169,8 +169,10 @@ gdn_status gdn_kernel_timer_read(double *total_ms, long long *launches, const ch
 /* Number of kernels this library has launched since it was loaded. */
 uint64_t gdn_kernel_launches(void);
 
-/* Implementation the last successful gdn_fwd / gdn_fwd_varlen call used
- * (GDN_IMPL_SIMT or GDN_IMPL_TC), 0 before the first call. */
+/* Implementation the last successful gdn_fwd / gdn_fwd_varlen / gdn_bwd /
+ * gdn_bwd_varlen call used (GDN_IMPL_SIMT or GDN_IMPL_TC; for the backward,
+ * GDN_IMPL_TC when its state adjoint ran on tcgen05), 0 before the first
+ * call. */
 int gdn_last_impl(void);
 
 /*
@@ -216,8 +218,12 @@ gdn_status gdn_fwd_varlen_ex(const void *q, const void *k, const void *v,
  * in the backward pass rather than storing it, and so does this call: it
  * reruns the chunked forward (without writing o), carries the adjoint of the
  * state backwards chunk by chunk, then forms every chunk's gradients in
- * parallel.  Warp-level tf32 mma.sync products (three per step for fp32 I/O),
- * fp32 accumulation.
+ * parallel.  For bf16 I/O with d_k 64 or 128 and d_v a multiple of 64 the
+ * chunk prep, the state pass and the state adjoint run on the tcgen05 kernels
+ * (bf16 operands, fp32 accumulation and fp32 states; the state pass is the
+ * forward's fused kernel); the per-chunk gradients, and every step of other
+ * shapes and of fp32 I/O, on warp-level tf32 mma.sync products (three per
+ * step for fp32 I/O), fp32 accumulation.
  *   q, k, v, log_alpha, beta, h0, B, H, T, d_k, d_v, chunk, dt: as gdn_fwd.
  *   dout   [B][H][T][d_v] dtype dt: the weights dO of the outputs.
  *   dhT    [B][H][d_v][d_k] fp32, or NULL for zero weight on the final state.
@@ -229,8 +235,9 @@ gdn_status gdn_fwd_varlen_ex(const void *q, const void *k, const void *v,
  *          GDN_FLAG_VECTOR_GATE gives GDN_ERR_UNSUPPORTED (not built).
  * Device memory, caller-owned; scratch (about 4 (d_k + 3 d_v + 65) bytes
  * per token-head plus 8 d_k d_v bytes per chunk-head) comes from the
- * library's pool.  Errors as gdn_fwd; with GDN_IMPL_TC forced the call
- * returns GDN_ERR_UNSUPPORTED (there is no tensor-core backward).
+ * library's pool.  Errors as gdn_fwd.  GDN_IMPL_SIMT forces the mma.sync
+ * kernels throughout; GDN_IMPL_TC forced returns GDN_ERR_UNSUPPORTED where
+ * the tcgen05 kernels do not take the call.
  */
 gdn_status gdn_bwd(const void *q, const void *k, const void *v,
                    const float *log_alpha, const float *beta, const float *h0,
