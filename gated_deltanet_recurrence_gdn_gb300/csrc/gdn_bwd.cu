@@ -455,33 +455,62 @@ k_bwd_chunk(FwdArgs a, BwdArgs b, const int2 *__restrict__ table, const float *_
                 sC = fmaf(s0a.v[0][e], dsa.v[0][e], fmaf(s0b.v[0][e], dsb.v[0][e], sC));
         }
         __syncthreads();
-        // dO S0, V' dSC, dV' S0 sharing the S0 / dSC fragments
+        // dO S0, V' dSC, dV' S0 sharing the S0 / dSC fragments; every operand
+        // here is row-wise in the d_v index, so fragments load by ldmatrix
+        // (B tiles in pairs 16 columns apart; past d_k the pair repeats its
+        // first tile, whose second products are skipped)
+        {
+            const int ao = (m0 + (lane & 15)) * kLdt + 4 * (lane >> 4);
+            const uint32_t a_o = mma::smem_addr(dOs + ao), a_v = mma::smem_addr(Vns + ao),
+                           a_d = mma::smem_addr(dVs + ao);
 #pragma unroll
-        for (int k0 = 0; k0 < kDvt; k0 += 8) {
-            mma::AFrag<SPLIT> fo, fv, fd;
-            fo.load([&](int m, int k) { return dOs[m * kLdt + k]; }, m0, k0, gl, tl);
-            fv.load([&](int m, int k) { return Vns[m * kLdt + k]; }, m0, k0, gl, tl);
-            if (erase) fd.load([&](int m, int k) { return dVs[m * kLdt + k]; }, m0, k0, gl, tl);
+            for (int k0 = 0; k0 < kDvt; k0 += 8) {
+                mma::AFrag<SPLIT> fo, fv, fd;
+                mma::lda_ldsm(fo, a_o + 4 * k0);
+                mma::lda_ldsm(fv, a_v + 4 * k0);
+                if (erase) mma::lda_ldsm(fd, a_d + 4 * k0);
 #pragma unroll
-            for (int i = 0; i < kNtK; ++i) {
-                const int nn = 8 * (nh + 2 * i);
-                if (nn < dk) {
-                    const float s0a = S0t[(nn + gl) * kLdt + k0 + tl];
-                    const float s0b = S0t[(nn + gl) * kLdt + k0 + tl + 4];
-                    mma::mma_step<SPLIT>(aQ[i], fo, s0a, s0b);
-                    mma::mma_step<SPLIT>(aK[i], fv, dSt[(nn + gl) * kLdt + k0 + tl],
-                                         dSt[(nn + gl) * kLdt + k0 + tl + 4]);
-                    if (erase) mma::mma_step<SPLIT>(aW[i], fd, s0a, s0b);
+                for (int i = 0; i < kNtK; i += 2) {
+                    const int n0 = 8 * (nh + 2 * i), n1 = 8 * (nh + 2 * i + 2);
+                    if (n0 < dk) {
+                        const int n1c = n1 < dk ? n1 : n0;
+                        uint32_t bs[4], bd[4];
+                        mma::ldsm4(bs, mma::smem_addr(mma::ldb_pair_ptr(S0t, kLdt, n0, n1c, k0,
+                                                                         lane)));
+                        mma::ldsm4(bd, mma::smem_addr(mma::ldb_pair_ptr(dSt, kLdt, n0, n1c, k0,
+                                                                         lane)));
+                        const float s0[4] = {__uint_as_float(bs[0]), __uint_as_float(bs[1]),
+                                             __uint_as_float(bs[2]), __uint_as_float(bs[3])};
+                        const float d0[4] = {__uint_as_float(bd[0]), __uint_as_float(bd[1]),
+                                             __uint_as_float(bd[2]), __uint_as_float(bd[3])};
+                        mma::mma_step<SPLIT>(aQ[i], fo, s0[0], s0[1]);
+                        mma::mma_step<SPLIT>(aK[i], fv, d0[0], d0[1]);
+                        if (erase) mma::mma_step<SPLIT>(aW[i], fd, s0[0], s0[1]);
+                        if (n1 < dk) {
+                            mma::mma_step<SPLIT>(aQ[i + 1], fo, s0[2], s0[3]);
+                            mma::mma_step<SPLIT>(aK[i + 1], fv, d0[2], d0[3]);
+                            if (erase) mma::mma_step<SPLIT>(aW[i + 1], fd, s0[2], s0[3]);
+                        }
+                    }
                 }
-            }
 #pragma unroll
-            for (int i = 0; i < kNtC; ++i) {
-                const int nn = 8 * (nh + 2 * i);
-                mma::mma_step<SPLIT>(aP[i], fo, Vns[(nn + gl) * kLdt + k0 + tl],
-                                     Vns[(nn + gl) * kLdt + k0 + tl + 4]);
-                if (erase)
-                    mma::mma_step<SPLIT>(aT[i], fd, Vs[(nn + gl) * kLdt + k0 + tl],
-                                         Vs[(nn + gl) * kLdt + k0 + tl + 4]);
+                for (int i = 0; i < kNtC; i += 2) {
+                    const int n0 = 8 * (nh + 2 * i), n1 = 8 * (nh + 2 * i + 2);
+                    uint32_t bv[4];
+                    mma::ldsm4(bv, mma::smem_addr(mma::ldb_pair_ptr(Vns, kLdt, n0, n1, k0, lane)));
+                    mma::mma_step<SPLIT>(aP[i], fo, __uint_as_float(bv[0]), __uint_as_float(bv[1]));
+                    mma::mma_step<SPLIT>(aP[i + 1], fo, __uint_as_float(bv[2]),
+                                         __uint_as_float(bv[3]));
+                    if (erase) {
+                        uint32_t bw[4];
+                        mma::ldsm4(bw, mma::smem_addr(mma::ldb_pair_ptr(Vs, kLdt, n0, n1, k0,
+                                                                         lane)));
+                        mma::mma_step<SPLIT>(aT[i], fd, __uint_as_float(bw[0]),
+                                             __uint_as_float(bw[1]));
+                        mma::mma_step<SPLIT>(aT[i + 1], fd, __uint_as_float(bw[2]),
+                                             __uint_as_float(bw[3]));
+                    }
+                }
             }
         }
         // dV = diag(beta) T^T dV' and the U part of dbeta

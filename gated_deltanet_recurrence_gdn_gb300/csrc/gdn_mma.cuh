@@ -22,6 +22,12 @@
 // Shared-memory strides: row-wise operand reads (A(m, k) = S[m * ld + k],
 // B(k, n) = S[n * ld + k]) are free of bank conflicts when ld is 4 modulo 8;
 // transposed reads then see two-way conflicts.
+//
+// Row-wise operands also load by ldmatrix: an 8 x 8 matrix of 16-bit
+// elements is an 8 x 4 block of fp32 values, which ldmatrix hands out so that
+// thread (g, t) holds element (g, t) -- the tf32 fragment layout.  One x4 load
+// gives a whole A fragment, or the B fragments of two 8-column tiles, where
+// the scalar path takes four loads.
 #pragma once
 #include <cstdint>
 
@@ -67,6 +73,41 @@ struct AFrag {
     }
 };
 
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// Four 8 x 8 b16 matrices; lanes 8i .. 8i + 7 give the 16-byte row addresses
+// of matrix i.
+__device__ __forceinline__ void ldsm4(uint32_t (&r)[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr)
+                 : "memory");
+}
+
+// A fragment of rows m0 .. m0 + 15, k0 .. k0 + 7 of a row-major fp32 tile:
+// `addr` = address of element (m0 + (lane & 15), k0 + 4 (lane >> 4)).
+template <bool SPLIT>
+__device__ __forceinline__ void lda_ldsm(AFrag<SPLIT> &a, uint32_t addr) {
+    uint32_t r[4];
+    ldsm4(r, addr);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const Op<SPLIT> o(__uint_as_float(r[i]));
+        a.hi[i] = o.hi;
+        a.lo[i] = o.lo;
+    }
+}
+
+// Lane address for the B fragments of the 8-column tiles n0 and n1 of a
+// column-wise tile (B(k, n) = S[n * ld + k]) at k0: the x4 load then gives
+// (b0, b1) of tile n0 in r[0], r[1] and of tile n1 in r[2], r[3].
+__device__ __forceinline__ const float *ldb_pair_ptr(const float *S, int ld, int n0, int n1,
+                                                     int k0, int lane) {
+    return S + ((lane >> 4 ? n1 : n0) + (lane & 7)) * ld + k0 + 4 * ((lane >> 3) & 1);
+}
+
 template <bool SPLIT>
 __device__ __forceinline__ void mma_step(float (&d)[4], const AFrag<SPLIT> &a, float b0,
                                          float b1) {
@@ -107,6 +148,54 @@ __device__ __forceinline__ void gemm_s(float (&acc)[NT][4], const float *pa, int
                                        int m0, int nt0, int nstep, int n_end, int K, int lane,
                                        int kb = 0) {
     const int g = lane >> 2, t = lane & 3;
+    if (sak == 1 && sbk == 1 && ((sam | sbn) & 3) == 0 &&
+        ((smem_addr(pa) | smem_addr(pb)) & 15) == 0) {
+        // rows of A and columns of B contiguous in k, 16-byte aligned: fragments
+        // by ldmatrix; B tiles in pairs (the second of an odd count repeats the
+        // first, its products skipped)
+        constexpr int NP = (NT + 1) / 2;
+        const uint32_t a_addr = smem_addr(pa + (m0 + (lane & 15)) * sam + kb + 4 * (lane >> 4));
+        uint32_t b_addr[NP];
+#pragma unroll
+        for (int q = 0; q < NP; ++q) {
+            const int n0 = 8 * (nt0 + 2 * q * nstep), n1 = 8 * (nt0 + (2 * q + 1) * nstep);
+            const bool second = 2 * q + 1 < NT && n1 < n_end;
+            b_addr[q] = smem_addr(ldb_pair_ptr(pb, sbn, n0, second ? n1 : n0, kb, lane));
+        }
+#pragma unroll 2
+        for (int k0 = kb; k0 < K; k0 += 8) {
+            const uint32_t ko = 4u * (uint32_t)(k0 - kb);
+            AFrag<SPLIT> a;
+            if (ascale) {
+                uint32_t r[4];
+                ldsm4(r, a_addr + ko);
+                const float s0 = ascale[k0 + t], s1 = ascale[k0 + t + 4];
+                const float v[4] = {__uint_as_float(r[0]) * s0, __uint_as_float(r[1]) * s0,
+                                    __uint_as_float(r[2]) * s1, __uint_as_float(r[3]) * s1};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const Op<SPLIT> o(v[i]);
+                    a.hi[i] = o.hi;
+                    a.lo[i] = o.lo;
+                }
+            } else {
+                lda_ldsm(a, a_addr + ko);
+            }
+#pragma unroll
+            for (int q = 0; q < NP; ++q) {
+                const int n0 = 8 * (nt0 + 2 * q * nstep), n1 = 8 * (nt0 + (2 * q + 1) * nstep);
+                if (n0 < n_end) {
+                    uint32_t b[4];
+                    ldsm4(b, b_addr[q] + ko);
+                    mma_step<SPLIT>(acc[2 * q], a, __uint_as_float(b[0]), __uint_as_float(b[1]));
+                    if (2 * q + 1 < NT && n1 < n_end)
+                        mma_step<SPLIT>(acc[2 * q + 1 < NT ? 2 * q + 1 : 2 * q], a,
+                                        __uint_as_float(b[2]), __uint_as_float(b[3]));
+                }
+            }
+        }
+        return;
+    }
     const float *a0 = pa + (m0 + g) * sam + (kb + t) * sak;
     const float *a1 = a0 + 8 * sam;
     const float *bp[NT];
