@@ -117,15 +117,20 @@ struct BLay {
     static constexpr int OFF_P = kNS * STAGE;           // two P buffers
     static constexpr int OFF_VN = OFF_P + 2 * 8192;     // -dV' (bf16)
     static constexpr int OFF_H = OFF_VN + 8192;         // dH (bf16), DK rows
+    // fp32 staging of the stored dH (DK rows) and dV' (64 rows) for bulk
+    // tensor stores: two 32-column halves of 128-byte rows each
+    static constexpr int OFF_SH = OFF_H + DK * 128;
+    static constexpr int OFF_SV = OFF_SH + DK * 256;
     static constexpr int GSZ = 4 * 64;                  // g, gamma, e, 1 / gamma
-    static constexpr int OFF_G = OFF_H + DK * 128;      // 2 x GSZ floats
+    static constexpr int OFF_G = OFF_SV + 64 * 256;     // 2 x GSZ floats
     static constexpr int OFF_GS = OFF_G + 2 * GSZ * 4;  // per stage: raw gate cumsum
     static constexpr int OFF_BAR = OFF_GS + kNS * 64 * 4;
     static constexpr int OFF_MISC = OFF_BAR + B_COUNT * 8;
     static constexpr int TOTAL = OFF_MISC + 64;
     static constexpr int ALLOC = TOTAL + 1024;
     static_assert(STAGE % 1024 == 0 && OFF_P % 1024 == 0 && OFF_VN % 1024 == 0 &&
-                      OFF_H % 1024 == 0 && OFF_BAR % 8 == 0,
+                      OFF_H % 1024 == 0 && OFF_SH % 1024 == 0 && OFF_SV % 1024 == 0 &&
+                      OFF_BAR % 8 == 0,
                   "align");
     // the second 64-row half of an M = 128 operand read past its tile stays
     // inside the allocation: [P^T; x] ends at OFF_VN + 8 KiB, (gamma Q)^T and
@@ -167,6 +172,7 @@ template <int DK>
 __global__ void __launch_bounds__(kThreadsB, 1)
 k_bwd_dstate_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_do,
+                const __grid_constant__ CUtensorMap tm_dh, const __grid_constant__ CUtensorMap tm_dv,
                 BwdTcParams p) {
     using L = BLay<DK>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -237,6 +243,7 @@ k_bwd_dstate_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         for (int c = 0; c < kNV; ++c)
             hreg[c] = (t < DK && p.dhT) ? __ldg(p.dhT + (srow + dv0 + c) * DK + t) : 0.f;
         uint8_t *Hs = sm + L::OFF_H, *VNs = sm + L::OFF_VN;
+        uint8_t *SH = sm + L::OFF_SH, *SV = sm + L::OFF_SV;
         bool alive = true;
         for (int j = 0; j < nch; ++j) {
             const int c = nch - 1 - j, s = j % kNS, bsel = j & 1;
@@ -248,16 +255,21 @@ k_bwd_dstate_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if (t < DK) put_row64(Hs, t, hreg);
             fence_proxy_async_smem();
             tc_fence_before();
+            if (t == 0) bulk_wait_read();   // the staging tiles' last stores have read them
             named_bar(1, 128);
             if (t == 0) st_release_cta(h_flag, (uint32_t)j + 1);
             BTRACE(0, j, 1, t == 0);
-            if (t < DK) {
-                float4 *dst = reinterpret_cast<float4 *>(
-                    p.dHc + ((h * p.chunk_slots + slot0 + c) * DK + t) * (long long)p.dv + dv0);
-#pragma unroll
-                for (int q = 0; q < 16; ++q)
-                    dst[q] = make_float4(hreg[4 * q], hreg[4 * q + 1], hreg[4 * q + 2],
-                                         hreg[4 * q + 3]);
+            // out through the staging tile and two bulk tensor stores (a
+            // thread's own 256-byte row scattered across the warp's stores
+            // would touch 32 rows per instruction)
+            if (t < DK) put_row64_f32(SH, DK, t, hreg);
+            fence_proxy_async_smem();
+            named_bar(1, 128);
+            if (t == 0) {
+                const int y = (int)((h * p.chunk_slots + slot0 + c) * DK);
+                tma_store_2d(&tm_dh, SH, dv0, y);
+                tma_store_2d(&tm_dh, SH + DK * 128, dv0 + 32, y);
+                bulk_commit();
             }
             // (ii) dV' = X + diag(e) Z; -dV' is the bf16 B operand of the update
             {
@@ -274,9 +286,13 @@ k_bwd_dstate_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             // kept in a register: the gate buffer is refilled once this chunk's
             // update MMA has been issued
             const float decayC = gj[64 + 63];
+            // dV' rows by bulk tensor store where the box holds this sequence's
+            // rows only (dense batches: rows past T are clipped; a packed
+            // batch's partial chunk is followed by the next sequence's rows)
+            const bool bulk_dv = !p.sm.cu || Lc == kC;
             if (t < kC) {
                 const float ev = gj[128 + t];
-                float *dvp = t < Lc ? p.dVn + (r0 + t) * p.dv + dv0 : nullptr;
+                float *dvp = (!bulk_dv && t < Lc) ? p.dVn + (r0 + t) * p.dv + dv0 : nullptr;
                 const uint32_t ax = tmem + lane_base + TM_X + bsel * 64;
                 const uint32_t az = tmem + lane_base + TM_Z;
 #pragma unroll
@@ -286,7 +302,14 @@ k_bwd_dstate_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     tmem_ld16f(az + 16 * qt, zv);
 #pragma unroll
                     for (int i = 0; i < 16; ++i) xv[i] = fmaf(ev, zv[i], xv[i]);
-                    if (dvp) {
+                    if (bulk_dv) {
+                        uint8_t *sv = SV + (qt >> 1) * 8192;
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+                            *reinterpret_cast<float4 *>(sv + sw128_offset(t, (qt & 1) * 4 + u)) =
+                                make_float4(xv[4 * u], xv[4 * u + 1], xv[4 * u + 2],
+                                            xv[4 * u + 3]);
+                    } else if (dvp) {
                         float4 *d4 = reinterpret_cast<float4 *>(dvp + 16 * qt);
 #pragma unroll
                         for (int q = 0; q < 4; ++q)
@@ -302,7 +325,15 @@ k_bwd_dstate_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             fence_proxy_async_smem();
             tc_fence_before();
             named_bar(1, 128);
-            if (t == 0) st_release_cta(vn_flag, (uint32_t)j + 1);
+            if (t == 0) {
+                st_release_cta(vn_flag, (uint32_t)j + 1);
+                if (bulk_dv) {
+                    const int y = ytok0 + c * kC;
+                    tma_store_3d(&tm_dv, SV, dv0, y, zcoord);
+                    tma_store_3d(&tm_dv, SV + 8192, dv0 + 32, y, zcoord);
+                    bulk_commit();
+                }
+            }
             BTRACE(0, j, 3, t == 0);
             // (iii) dH <- exp(g_C) dH + (Y - W^T dV')
             if (!named_bar_and(1, 128, ctl.wait(B_U, j & 1))) {
@@ -329,6 +360,7 @@ k_bwd_dstate_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
             for (int c = 0; c < kNV; ++c) p.dh0[(srow + dv0 + c) * DK + t] = hreg[c];
         }
+        if (t == 0) bulk_wait_all();   // every store done before the CTA leaves
     } else if (warp < 6) {
         // ======================================================= gate warps
         const int t = tid - 128;   // row of the chunk
@@ -602,9 +634,11 @@ gdn_status launch_bwd_tc(const FwdArgs &a, const BwdArgs &b, const __nv_bfloat16
     using L = BLay<DK>;
     const long long ydim = a.sm.cu ? a.sm.T_total : a.sm.T;
     const long long zdim = a.sm.cu ? a.sm.H : (long long)a.sm.N * a.sm.H;
-    CUtensorMap mq, mk, mw, mdo;
+    CUtensorMap mq, mk, mw, mdo, mdh, mdv;
     if (!make_map(&mq, a.q, DK, ydim, zdim) || !make_map(&mk, a.k, DK, ydim, zdim) ||
-        !make_map(&mw, Wb, DK, ydim, zdim) || !make_map(&mdo, b.dout, a.dv, ydim, zdim))
+        !make_map(&mw, Wb, DK, ydim, zdim) || !make_map(&mdo, b.dout, a.dv, ydim, zdim) ||
+        !make_map_f32(&mdh, dHc, a.dv, (long long)a.sm.H * a.chunk_slots * DK, DK) ||
+        !make_map_f32_3d(&mdv, dVn, a.dv, ydim, zdim))
         return GDN_ERR_CUDA;
     static bool attr_set = false;
     if (!attr_set) {
@@ -627,7 +661,7 @@ gdn_status launch_bwd_tc(const FwdArgs &a, const BwdArgs &b, const __nv_bfloat16
     const long long lim = option(GDN_OPT_WAIT_LIMIT);
     p.wait_limit = lim > 0 ? (uint32_t)(lim > 0x7fffffffLL ? 0x7fffffffLL : lim) : (1u << 22);
     const dim3 grid(a.dv / kNV, a.sm.H, a.sm.N);
-    k_bwd_dstate_tc<DK><<<grid, kThreadsB, L::ALLOC, a.stream>>>(mq, mk, mw, mdo, p);
+    k_bwd_dstate_tc<DK><<<grid, kThreadsB, L::ALLOC, a.stream>>>(mq, mk, mw, mdo, mdh, mdv, p);
     count_launch();
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }

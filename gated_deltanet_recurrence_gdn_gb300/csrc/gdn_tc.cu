@@ -117,6 +117,12 @@ struct Lay {
     static constexpr int OFF_MISC = OFF_BAR + B_COUNT * 8;
     static constexpr int TOTAL = OFF_MISC + 64;
     static constexpr int ALLOC = TOTAL + 1024;
+    // the backward's state pass only: an fp32 staging tile for bulk tensor
+    // stores of each chunk's starting state (DK rows) and then of its V'
+    // rows (64), two 32-column halves of 128-byte rows
+    static constexpr int OFF_STG = (TOTAL + 1023) / 1024 * 1024;
+    static constexpr int ALLOC_S = OFF_STG + DK * 256 + 1024;
+    static_assert(ALLOC_S <= 227 * 1024, "shared memory budget (state pass)");
     static_assert(OFF_WQ % 1024 == 0 && OFF_TU % 1024 == 0 && STAGE % 1024 == 0, "align");
     static_assert(OFF_H % 1024 == 0 && OFF_R0 % 1024 == 0 && OFF_G % 16 == 0, "align");
     static_assert(ALLOC <= 227 * 1024, "shared memory budget");
@@ -157,7 +163,8 @@ template <int DK, bool STATES>
 __global__ void __launch_bounds__(kThreadsTC, 1)
 k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
          const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_t,
-         const __grid_constant__ CUtensorMap tm_w, TcParams p) {
+         const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_hst,
+         const __grid_constant__ CUtensorMap tm_vst, TcParams p) {
     using L = Lay<DK>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -285,25 +292,30 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
             TRACE(0, j, 0, t == 0);
             // (i) publish H as the bf16 B operand of the chain MMA
             if (t < DK) put_row64(Hs, t, hreg);
-            if (STATES && t < DK) {   // the chunk's starting state, for the backward
-                float4 *dst = reinterpret_cast<float4 *>(
-                    p.Hst + ((h * p.chunk_slots + slot0 + j) * DK + t) * (long long)p.dv + dv0);
-#pragma unroll
-                for (int q = 0; q < 16; ++q)
-                    dst[q] = make_float4(hreg[4 * q], hreg[4 * q + 1], hreg[4 * q + 2],
-                                         hreg[4 * q + 3]);
-            }
             fence_proxy_async_smem();
             tc_fence_before();
+            if (STATES && t == 0) bulk_wait_read();   // the staging tile is free
             named_bar(1, 128);
             if (t == 0) st_release_cta(h_flag, (uint32_t)j + 1);
             TRACE(0, j, 1, t == 0);
+            if (STATES) {   // the chunk's starting state, for the backward
+                if (t < DK) put_row64_f32(sm + L::OFF_STG, DK, t, hreg);
+                fence_proxy_async_smem();
+                named_bar(1, 128);
+                if (t == 0) {
+                    const int y = (int)((h * p.chunk_slots + slot0 + j) * DK);
+                    tma_store_2d(&tm_hst, sm + L::OFF_STG, dv0, y);
+                    tma_store_2d(&tm_hst, sm + L::OFF_STG + DK * 128, dv0 + 32, y);
+                    bulk_commit();
+                }
+            }
             // (i') previous chunk's output rows, off the state's critical path
             if (j > 0 && t >= 64 && !p.no_output && !lin) store_o(j - 1);
             TRACE(0, j, 2, t == 64);
             // (ii) V' = U - W H, and its decayed copy for the state update
             {
                 // READY orders this chunk's gates; UW and M2 bring U and W H
+                if (STATES && t == 0) bulk_wait_read();   // staging free for V'
                 bool ok = ctl.wait(B_READY + (j % kNS), (j / kNS) & 1);
                 ok = ok && ctl.wait(B_UW, j & 1) && ctl.wait(B_M2, j & 1);
                 if (!named_bar_and(1, 128, ok)) {
@@ -319,6 +331,9 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
             // this chunk's output scale, kept in a register: its gate buffer
             // may be refilled before the rows are stored during chunk j + 1
             const float osc_j = (t >= 64 && gC > -80.f) ? gj[128 + t - 64] : 1.f;
+            // V' rows by bulk tensor store where the box holds this sequence's
+            // rows only (dense: rows past T are clipped)
+            const bool bulk_v = !p.sm.cu || len - j * kC >= kC;
             if (t < 64) {
                 const float ev = __expf(gC - gj[t]);
                 const uint32_t acc = tmem + lane_base + TM_M2 + (j & 1) * 64;
@@ -335,7 +350,14 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
                         vn[i] = f32(u[i]) - f32(wh[i]);
                         vt[i] = vn[i] * ev;
                     }
-                    if (STATES && t < min(kC, len - j * kC)) {
+                    if (STATES && bulk_v) {   // staged for two bulk tensor stores
+                        uint8_t *sv = sm + L::OFF_STG + half * 8192;
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            *reinterpret_cast<float4 *>(sv + sw128_offset(t, q)) =
+                                make_float4(vn[4 * q], vn[4 * q + 1], vn[4 * q + 2],
+                                            vn[4 * q + 3]);
+                    } else if (STATES && t < min(kC, len - j * kC)) {
                         float4 *dst = reinterpret_cast<float4 *>(
                             p.Vst + (row0 + (long long)j * kC + t) * p.dv + dv0 + 32 * half);
 #pragma unroll
@@ -356,6 +378,12 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
             if (t == 0) {
                 st_release_cta(vn_flag, (uint32_t)j + 1);
                 mbar_arrive(bar + B_VN);
+                if (STATES && bulk_v) {
+                    const int y = ytok0 + j * kC;
+                    tma_store_3d(&tm_vst, sm + L::OFF_STG, dv0, y, zcoord);
+                    tma_store_3d(&tm_vst, sm + L::OFF_STG + 8192, dv0 + 32, y, zcoord);
+                    bulk_commit();
+                }
             }
             TRACE(0, j, 4, t == 0);
             // (iii) H <- exp(g_C) H + dH
@@ -384,6 +412,7 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
 #pragma unroll
             for (int c = 0; c < kNV; ++c) hTp[(srow + dv0 + c) * DK + t] = hreg[c];
         }
+        if (STATES && t == 0) bulk_wait_all();   // every store done before the CTA leaves
     } else if (warp < 8) {
         // ================================================== prep warpgroups
         // Two independent 64-thread pipelines over the chunks:
@@ -737,10 +766,15 @@ gdn_status launch_tc(const FwdArgs &a, const __nv_bfloat16 *Tin, const LaunchCfg
         if (cudaFuncSetAttribute(k_gdn_tc<DK, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  L::ALLOC) != cudaSuccess ||
             cudaFuncSetAttribute(k_gdn_tc<DK, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 L::ALLOC) != cudaSuccess)
+                                 L::ALLOC_S) != cudaSuccess)
             return GDN_ERR_CUDA;
         attr_set = true;
     }
+    // the state pass's outputs (the forward's instantiation never reads these)
+    CUtensorMap mh = mq, mvs = mq;
+    if (c.Hst && (!make_map_f32(&mh, c.Hst, a.dv, (long long)a.sm.H * a.chunk_slots * DK, DK) ||
+                  !make_map_f32_3d(&mvs, c.Vst, a.dv, ydim, zdim)))
+        return GDN_ERR_CUDA;
     TcParams p;
     p.sm = a.sm;
     p.log_alpha = a.log_alpha;
@@ -772,13 +806,13 @@ gdn_status launch_tc(const FwdArgs &a, const __nv_bfloat16 *Tin, const LaunchCfg
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(kThreadsTC);
-    cfg.dynamicSmemBytes = L::ALLOC;
+    cfg.dynamicSmemBytes = c.Hst ? L::ALLOC_S : L::ALLOC;
     cfg.stream = a.stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     const cudaError_t le =
-        c.Hst ? cudaLaunchKernelEx(&cfg, k_gdn_tc<DK, true>, mq, mk, mv, mt, mw, p)
-              : cudaLaunchKernelEx(&cfg, k_gdn_tc<DK, false>, mq, mk, mv, mt, mw, p);
+        c.Hst ? cudaLaunchKernelEx(&cfg, k_gdn_tc<DK, true>, mq, mk, mv, mt, mw, mh, mvs, p)
+              : cudaLaunchKernelEx(&cfg, k_gdn_tc<DK, false>, mq, mk, mv, mt, mw, mh, mvs, p);
     timer_end(slot, a.stream);
     if (le != cudaSuccess) return GDN_ERR_CUDA;
     count_launch();

@@ -56,6 +56,47 @@ __device__ __forceinline__ void put_row64(uint8_t *tile, int row, const float (&
 
 __device__ __forceinline__ float f32(uint32_t u) { return __uint_as_float(u); }
 
+// Bulk tensor stores (shared -> global) of a 128-byte-swizzled fp32 tile,
+// tracked by this thread's bulk groups.  The tile's writers make it visible
+// to the async proxy (fence.proxy.async) before the storing thread issues.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void *src, int x,
+                                             int y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::
+                     "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(src)), "r"(x), "r"(y)
+                 : "memory");
+}
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, const void *src, int x,
+                                             int y, int z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Until every committed store has read its shared-memory source.
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Until every committed store has completed.
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// Row `row` of a 64-column fp32 tile staged for bulk stores: two 32-column
+// halves, each `rows` rows of 128 bytes, 128-byte swizzled.
+__device__ __forceinline__ void put_row64_f32(uint8_t *tile, int rows, int row,
+                                              const float (&x)[64]) {
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+        float4 *d = reinterpret_cast<float4 *>(tile + (q >> 3) * rows * 128 +
+                                               sw128_offset(row, q & 7));
+        *d = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+    }
+}
+
 // -------------------------------------------------------------------- host
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
@@ -88,6 +129,35 @@ inline bool make_map(CUtensorMap *m, const void *base, int d, long long ydim, lo
     cuuint32_t box[3] = {64, 64, 1};
     cuuint32_t es[3] = {1, 1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
+              es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
+// Views of an fp32 row-major tensor with rows of `d` elements for bulk tensor
+// stores of 32-column, 128-byte-swizzled boxes: 2-D [ydim][d] with boxes of
+// `box_rows` rows, or 3-D [zdim][ydim][d] with boxes of 64 rows.
+inline bool make_map_f32(CUtensorMap *m, const void *base, int d, long long ydim, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)ydim};
+    cuuint64_t strides[1] = {(cuuint64_t)d * 4};
+    cuuint32_t box[2] = {32, (cuuint32_t)box_rows};
+    cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void *>(base), dims, strides, box,
+              es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+inline bool make_map_f32_3d(CUtensorMap *m, const void *base, int d, long long ydim,
+                            long long zdim) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)ydim, (cuuint64_t)zdim};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)d * 4 * (cuuint64_t)ydim};
+    cuuint32_t box[3] = {32, 64, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void *>(base), dims, strides, box,
               es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
            CUDA_SUCCESS;
