@@ -157,14 +157,14 @@ struct TcParams {
     int max_chunks;
 };
 
-// STATES: the backward's state pass (stores Hst / Vst); a separate
-// instantiation, so the forward's kernel carries none of it.
+// The kernel body.  STATES: the backward's state pass (stores Hst / Vst),
+// a separate kernel (k_gdn_tc_states), so the forward's k_gdn_tc carries
+// none of it.  The tensor maps are the kernels' __grid_constant__ parameters.
 template <int DK, bool STATES>
-__global__ void __launch_bounds__(kThreadsTC, 1)
-k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-         const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_t,
-         const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_hst,
-         const __grid_constant__ CUtensorMap tm_vst, TcParams p) {
+__device__ __forceinline__ void gdn_tc_body(const CUtensorMap *tm_q, const CUtensorMap *tm_k,
+                                            const CUtensorMap *tm_v, const CUtensorMap *tm_t,
+                                            const CUtensorMap *tm_w, const CUtensorMap *tm_hst,
+                                            const CUtensorMap *tm_vst, const TcParams &p) {
     using L = Lay<DK>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -304,8 +304,8 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
                 named_bar(1, 128);
                 if (t == 0) {
                     const int y = (int)((h * p.chunk_slots + slot0 + j) * DK);
-                    tma_store_2d(&tm_hst, sm + L::OFF_STG, dv0, y);
-                    tma_store_2d(&tm_hst, sm + L::OFF_STG + DK * 128, dv0 + 32, y);
+                    tma_store_2d(tm_hst, sm + L::OFF_STG, dv0, y);
+                    tma_store_2d(tm_hst, sm + L::OFF_STG + DK * 128, dv0 + 32, y);
                     bulk_commit();
                 }
             }
@@ -380,8 +380,8 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
                 mbar_arrive(bar + B_VN);
                 if (STATES && bulk_v) {
                     const int y = ytok0 + j * kC;
-                    tma_store_3d(&tm_vst, sm + L::OFF_STG, dv0, y, zcoord);
-                    tma_store_3d(&tm_vst, sm + L::OFF_STG + 8192, dv0 + 32, y, zcoord);
+                    tma_store_3d(tm_vst, sm + L::OFF_STG, dv0, y, zcoord);
+                    tma_store_3d(tm_vst, sm + L::OFF_STG + 8192, dv0 + 32, y, zcoord);
                     bulk_commit();
                 }
             }
@@ -587,11 +587,11 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
         // lane 0 issues the bulk tensor copies; all lanes stage the chunk's
         // gates (log_alpha, beta; zero past the sequence) next to them
         if (lane == 0) {
-            prefetch_tmap(&tm_q);
-            prefetch_tmap(&tm_k);
-            prefetch_tmap(&tm_v);
-            prefetch_tmap(&tm_t);
-            prefetch_tmap(&tm_w);
+            prefetch_tmap(tm_q);
+            prefetch_tmap(tm_k);
+            prefetch_tmap(tm_v);
+            prefetch_tmap(tm_t);
+            prefetch_tmap(tm_w);
         }
         int issued = 0;
         // gates of the next chunk, loaded one chunk ahead so their latency hides
@@ -618,13 +618,13 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
                 mbar_arrive_expect_tx(fb, (uint32_t)(L::STAGE - (lin ? 8192 : 0)));
 #pragma unroll
                 for (int blk = 0; blk < L::KB; ++blk) {
-                    tma_load_3d(stg + blk * 8192, &tm_k, fb, blk * 64, y, zcoord);
-                    tma_load_3d(stg + L::OFF_WQ + blk * 16384, &tm_w, fb, blk * 64, y, zcoord);
-                    tma_load_3d(stg + L::OFF_WQ + blk * 16384 + 8192, &tm_q, fb, blk * 64, y,
+                    tma_load_3d(stg + blk * 8192, tm_k, fb, blk * 64, y, zcoord);
+                    tma_load_3d(stg + L::OFF_WQ + blk * 16384, tm_w, fb, blk * 64, y, zcoord);
+                    tma_load_3d(stg + L::OFF_WQ + blk * 16384 + 8192, tm_q, fb, blk * 64, y,
                                 zcoord);
                 }
-                if (!lin) tma_load_3d(stg + L::OFF_V, &tm_v, fb, dv0, y, zcoord);
-                tma_load_3d(stg + L::OFF_TU, &tm_t, fb, 0, y, zcoord);
+                if (!lin) tma_load_3d(stg + L::OFF_V, tm_v, fb, dv0, y, zcoord);
+                tma_load_3d(stg + L::OFF_TU, tm_t, fb, 0, y, zcoord);
             }
             {
                 float *gs = reinterpret_cast<float *>(sm + L::OFF_GS) + s * 128;
@@ -733,6 +733,23 @@ k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
     if (warp == 9) tmem_dealloc(tmem, 512);
 }
 
+template <int DK>
+__global__ void __launch_bounds__(kThreadsTC, 1)
+k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+         const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_t,
+         const __grid_constant__ CUtensorMap tm_w, TcParams p) {
+    gdn_tc_body<DK, false>(&tm_q, &tm_k, &tm_v, &tm_t, &tm_w, nullptr, nullptr, p);
+}
+
+template <int DK>
+__global__ void __launch_bounds__(kThreadsTC, 1)
+k_gdn_tc_states(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_t,
+                const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_hst,
+                const __grid_constant__ CUtensorMap tm_vst, TcParams p) {
+    gdn_tc_body<DK, true>(&tm_q, &tm_k, &tm_v, &tm_t, &tm_w, &tm_hst, &tm_vst, p);
+}
+
 // -------------------------------------------------------------------- host
 
 // One launch of the fused kernel.  `seq` says how the grid's z axis maps to
@@ -763,9 +780,9 @@ gdn_status launch_tc(const FwdArgs &a, const __nv_bfloat16 *Tin, const LaunchCfg
         return GDN_ERR_CUDA;
     static bool attr_set = false;
     if (!attr_set) {
-        if (cudaFuncSetAttribute(k_gdn_tc<DK, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(k_gdn_tc<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  L::ALLOC) != cudaSuccess ||
-            cudaFuncSetAttribute(k_gdn_tc<DK, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            cudaFuncSetAttribute(k_gdn_tc_states<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  L::ALLOC_S) != cudaSuccess)
             return GDN_ERR_CUDA;
         attr_set = true;
@@ -811,8 +828,8 @@ gdn_status launch_tc(const FwdArgs &a, const __nv_bfloat16 *Tin, const LaunchCfg
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     const cudaError_t le =
-        c.Hst ? cudaLaunchKernelEx(&cfg, k_gdn_tc<DK, true>, mq, mk, mv, mt, mw, mh, mvs, p)
-              : cudaLaunchKernelEx(&cfg, k_gdn_tc<DK, false>, mq, mk, mv, mt, mw, mh, mvs, p);
+        c.Hst ? cudaLaunchKernelEx(&cfg, k_gdn_tc_states<DK>, mq, mk, mv, mt, mw, mh, mvs, p)
+              : cudaLaunchKernelEx(&cfg, k_gdn_tc<DK>, mq, mk, mv, mt, mw, p);
     timer_end(slot, a.stream);
     if (le != cudaSuccess) return GDN_ERR_CUDA;
     count_launch();
