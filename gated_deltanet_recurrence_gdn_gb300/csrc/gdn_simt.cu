@@ -554,29 +554,42 @@ k_prep_vg(FwdArgs a, const int2 *__restrict__ table, float *__restrict__ W,
         const int r = 16 * blk + rl, sc = 16 * blk + p;
         if (which == 0 && (sc == r || !erase)) continue;
         if (which == 1 && !want_p) continue;
-        const float *xr = which == 0 ? Ks + r * ldk : Qs + r * ldk;
+        // four key dimensions per shared-memory load (rows are 16-byte
+        // aligned: ldk is a multiple of 4)
+        const float4 *xr = reinterpret_cast<const float4 *>(which == 0 ? Ks + r * ldk
+                                                                       : Qs + r * ldk);
+        const float4 *gr = reinterpret_cast<const float4 *>(Gs + r * ldk);
+        const float4 *gs = reinterpret_cast<const float4 *>(Gs + sc * ldk);
+        const float4 *ks = reinterpret_cast<const float4 *>(Ks + sc * ldk);
         float acc = 0.f;
-        for (int j = 0; j < dk; ++j)
-            acc = fmaf(xr[j] * expf(Gs[r * ldk + j] - Gs[sc * ldk + j]), Ks[sc * ldk + j], acc);
+        for (int j4 = 0; j4 < dk / 4; ++j4) {
+            const float4 x = xr[j4], a = gr[j4], b = gs[j4], k = ks[j4];
+            acc = fmaf(x.x * __expf(a.x - b.x), k.x, acc);
+            acc = fmaf(x.y * __expf(a.y - b.y), k.y, acc);
+            acc = fmaf(x.z * __expf(a.z - b.z), k.z, acc);
+            acc = fmaf(x.w * __expf(a.w - b.w), k.w, acc);
+        }
         if (which == 0) A[r * kLdc + sc] = bb[r] * acc;
         else Pm[r * kLdc + sc] = acc;
     }
     // earlier blocks, through the first row m of r's block
     for (int m = 16; m < kChunk; m += 16) {
         __syncthreads();   // staging free
-        for (int i = tid; i < (32 + m) * dk; i += kThreads) {
-            const int row = i / dk, j = i - row * dk;
-            const float gm_ = Gs[m * ldk + j];
-            if (row < 16) {
-                Xr[row * ldk + j] = Ks[(m + row) * ldk + j] * expf(Gs[(m + row) * ldk + j] - gm_);
-            } else if (row < 32) {
-                const int rr = m + row - 16;
-                Xr[row * ldk + j] = want_p ? Qs[rr * ldk + j] * expf(Gs[rr * ldk + j] - gm_) : 0.f;
-            } else {
-                const int sr = row - 32;
-                Xs[sr * ldk + j] = Ks[sr * ldk + j] * expf(gm_ - Gs[sr * ldk + j]);
+        for (int row = warp; row < 32 + m; row += kThreads / 32)   // a warp per row
+            for (int j = lane; j < dk; j += 32) {
+                const float gm_ = Gs[m * ldk + j];
+                if (row < 16) {
+                    Xr[row * ldk + j] =
+                        Ks[(m + row) * ldk + j] * __expf(Gs[(m + row) * ldk + j] - gm_);
+                } else if (row < 32) {
+                    const int rr = m + row - 16;
+                    Xr[row * ldk + j] =
+                        want_p ? Qs[rr * ldk + j] * __expf(Gs[rr * ldk + j] - gm_) : 0.f;
+                } else {
+                    const int sr = row - 32;
+                    Xs[sr * ldk + j] = Ks[sr * ldk + j] * __expf(gm_ - Gs[sr * ldk + j]);
+                }
             }
-        }
         __syncthreads();
         const int ntile = m / 8;
         for (int task = warp; task < 2 * ntile; task += kThreads / 32) {
@@ -643,10 +656,8 @@ k_prep_vg(FwdArgs a, const int2 *__restrict__ table, float *__restrict__ W,
                       [&](int i, int nn, float &x) { Tm[(32 + i) * kLdc + nn] = -x; });
     }
     // K * exp(G) (each factor <= 1)
-    for (int i = tid; i < kChunk * dk; i += kThreads) {
-        const int r = i / dk, j = i - r * dk;
-        Ks[r * ldk + j] *= expf(Gs[r * ldk + j]);
-    }
+    for (int r = warp; r < kChunk; r += kThreads / 32)
+        for (int j = lane; j < dk; j += 32) Ks[r * ldk + j] *= __expf(Gs[r * ldk + j]);
     __syncthreads();
     {   // W = T diag(beta) (K * exp(G)) (zero without the erase term)
         float acc[8][4];
@@ -673,10 +684,8 @@ k_prep_vg(FwdArgs a, const int2 *__restrict__ table, float *__restrict__ W,
             if (r < L) U[(r0 + r) * dv + j] = x;
         });
     }
-    for (int i = tid; i < L * dk; i += kThreads) {
-        const int r = i / dk, j = i - r * dk;
-        G[(r0 + r) * dk + j] = Gs[r * ldk + j];
-    }
+    for (int r = warp; r < L; r += kThreads / 32)
+        for (int j = lane; j < dk; j += 32) G[(r0 + r) * dk + j] = Gs[r * ldk + j];
     if (want_p)
         for (int i = tid; i < L * kChunk; i += kThreads) {
             const int r = i >> 6, sc = i & 63;
@@ -753,13 +762,13 @@ k_state_vg(FwdArgs a, const float *__restrict__ W, const float *__restrict__ U,
         }
         __syncthreads();
         // rows past L hold zeros (K = Q = 0), so their factors do not matter
-        for (int i = tid; i < kChunk * dk; i += kThreads) {
-            const int r = i / dk, j = i - r * dk;
-            const float gr = Gt[r * ldk + j], gc = Gt[(L - 1) * ldk + j];
-            Qs[r * ldk + j] *= expf(gr);
-            Ks[r * ldk + j] *= expf(gc - gr);
-        }
-        for (int j = tid; j < dk; j += kThreads) gce[j] = expf(Gt[(L - 1) * ldk + j]);
+        for (int r = warp; r < kChunk; r += kThreads / 32)
+            for (int j = lane; j < dk; j += 32) {
+                const float gr = Gt[r * ldk + j], gc = Gt[(L - 1) * ldk + j];
+                Qs[r * ldk + j] *= __expf(gr);
+                Ks[r * ldk + j] *= __expf(gc - gr);
+            }
+        for (int j = tid; j < dk; j += kThreads) gce[j] = __expf(Gt[(L - 1) * ldk + j]);
         {   // V' = U - W H
             float acc[4][4];
             mma::zero(acc);
