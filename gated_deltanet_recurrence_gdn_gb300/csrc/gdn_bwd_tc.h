@@ -1,5 +1,7 @@
-// gdn_bwd_tc.h -- entry points of the backward pass's tensor-core state
-// adjoint (gdn_bwd_tc.cu) and of the prep variant that feeds it.
+// gdn_bwd_tc.h -- the backward pass's tcgen05 stages and its implementation
+// choice: the preps' extra outputs for it (gdn_simt.cu, gdn_prep.cu), the
+// forward's fused kernel as its state pass (gdn_tc.cu), the state adjoint
+// (gdn_bwd_tc.cu) and the backward's entry (gdn_bwd.cu).
 #pragma once
 #include <cuda_bf16.h>
 
