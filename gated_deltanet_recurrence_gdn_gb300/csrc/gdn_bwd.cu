@@ -51,8 +51,13 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kDvt = 32;     // d_v columns per tile
 
-__device__ __forceinline__ void st_out(float *p, float x) { *p = x; }
-__device__ __forceinline__ void st_out(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
+// Two adjacent outputs (columns c, c + 1 of a row, c even) in one store.
+__device__ __forceinline__ void st_out2(float *p, float x, float y) {
+    *reinterpret_cast<float2 *>(p) = make_float2(x, y);
+}
+__device__ __forceinline__ void st_out2(__nv_bfloat16 *p, float x, float y) {
+    *reinterpret_cast<__nv_bfloat162 *>(p) = __floats2bfloat162_rn(x, y);
+}
 __device__ __forceinline__ void set_error(int *err, int code) { atomicCAS(err, 0, code); }
 
 __device__ __forceinline__ bool seq_ok(const SeqMap &sm, int n) {
@@ -520,9 +525,20 @@ k_bwd_chunk(FwdArgs a, BwdArgs b, const int2 *__restrict__ table, const float *_
             mma::gemm_s<kNtV, SPLIT>(acc, Tm, 1, kLdc, nullptr, dVs, kLdt, 1, m0, nh, 2, kDvt,
                                      kChunk, lane, m0);
             TIn *dvp = static_cast<TIn *>(b.dv);
-            mma::for_each(acc, m0, nh, 2, kDvt, lane, [&](int s, int cc, float &x) {
-                if (s < L && cc < nv) st_out(dvp + (r0 + s) * dv + dv0 + cc, bb[s] * x);
-            });
+            // the accumulator's adjacent column pairs, one store each
+#pragma unroll
+            for (int i = 0; i < kNtV; ++i) {
+                const int cc = 8 * (nh + 2 * i) + 2 * tl;
+                if (8 * (nh + 2 * i) < kDvt && cc < nv) {
+#pragma unroll
+                    for (int hr = 0; hr < 2; ++hr) {
+                        const int s = m0 + gl + 8 * hr;
+                        if (s < L)
+                            st_out2(dvp + (r0 + s) * dv + dv0 + cc, bb[s] * acc[i][2 * hr],
+                                    bb[s] * acc[i][2 * hr + 1]);
+                    }
+                }
+            }
             add_row_sums(acc, m0, nh, 2, kDvt, lane,
                          [&](int s, int cc, float x) { return x * Vs[s * kLdt + cc]; }, dbU,
                          [](int) { return 1.f; });
@@ -565,13 +581,19 @@ k_bwd_chunk(FwdArgs a, BwdArgs b, const int2 *__restrict__ table, const float *_
                                  lane);
         TIn *dqp = static_cast<TIn *>(b.dq);
 #pragma unroll
-        for (int i = 0; i < kNtK; ++i)
+        for (int i = 0; i < kNtK; ++i) {
+            const int j = 8 * (nh + 2 * i) + 2 * tl;
+            if (8 * (nh + 2 * i) < dk) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int r = m0 + gl + 8 * (e >> 1), j = 8 * (nh + 2 * i) + 2 * tl + (e & 1);
-                if (8 * (nh + 2 * i) < dk && r < L)
-                    st_out(dqp + (r0 + r) * dk + j, fmaf(gm[r], aQ[i][e], tmp[i][e]));
+                for (int hr = 0; hr < 2; ++hr) {
+                    const int r = m0 + gl + 8 * hr;
+                    if (r < L)
+                        st_out2(dqp + (r0 + r) * dk + j,
+                                fmaf(gm[r], aQ[i][2 * hr], tmp[i][2 * hr]),
+                                fmaf(gm[r], aQ[i][2 * hr + 1], tmp[i][2 * hr + 1]));
+                }
             }
+        }
         add_row_sums(aQ, m0, nh, 2, dk, lane,
                      [&](int r, int j, float x) { return Qs[r * ldk + j] * x; }, dgQ,
                      [&](int r) { return gm[r]; });
@@ -665,9 +687,17 @@ k_bwd_chunk(FwdArgs a, BwdArgs b, const int2 *__restrict__ table, const float *_
     }
     {
         TIn *dkp = static_cast<TIn *>(b.dk);
-        mma::for_each(aK, m0, nh, 2, dk, lane, [&](int r, int j, float &x) {
-            if (r < L) st_out(dkp + (r0 + r) * dk + j, x);
-        });
+#pragma unroll
+        for (int i = 0; i < kNtK; ++i) {
+            const int j = 8 * (nh + 2 * i) + 2 * tl;
+            if (8 * (nh + 2 * i) < dk) {
+#pragma unroll
+                for (int hr = 0; hr < 2; ++hr) {
+                    const int r = m0 + gl + 8 * hr;
+                    if (r < L) st_out2(dkp + (r0 + r) * dk + j, aK[i][2 * hr], aK[i][2 * hr + 1]);
+                }
+            }
+        }
     }
     __syncthreads();
     // dg and dbeta per row; dlog_alpha is the reverse cumsum of dg
