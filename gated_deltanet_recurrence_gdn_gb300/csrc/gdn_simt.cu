@@ -44,8 +44,32 @@ namespace {
 
 constexpr int kThreads = 256;
 
-__device__ __forceinline__ void st_out(float *p, float x) { *p = x; }
-__device__ __forceinline__ void st_out(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
+// Two adjacent outputs (columns c, c + 1 of a row, c even) in one store.
+__device__ __forceinline__ void st_out2(float *p, float x, float y) {
+    *reinterpret_cast<float2 *>(p) = make_float2(x, y);
+}
+__device__ __forceinline__ void st_out2(__nv_bfloat16 *p, float x, float y) {
+    *reinterpret_cast<__nv_bfloat162 *>(p) = __floats2bfloat162_rn(x, y);
+}
+
+// The accumulator block's column pairs (2t, 2t + 1 of each 8-column tile
+// below n_end) into rows r < L of dst (row stride ld), one store a pair.
+template <int NT, typename T>
+__device__ __forceinline__ void store_pairs(const float (&acc)[NT][4], int m0, int nt0, int nstep,
+                                            int n_end, int lane, int L, T *dst, long long ld) {
+    const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int i = 0; i < NT; ++i) {
+        const int n = 8 * (nt0 + i * nstep);
+        if (n < n_end) {
+#pragma unroll
+            for (int hr = 0; hr < 2; ++hr) {
+                const int r = m0 + g + 8 * hr;
+                if (r < L) st_out2(dst + r * ld + n + 2 * t, acc[i][2 * hr], acc[i][2 * hr + 1]);
+            }
+        }
+    }
+}
 
 __device__ __forceinline__ void set_error(int *err, int code) { atomicCAS(err, 0, code); }
 
@@ -219,15 +243,13 @@ k_state_mma(FwdArgs a, const float *__restrict__ W, const float *__restrict__ U,
                                   lane);
             mma::gemm_s<4, SPLIT>(a2, P, kLdc, 1, nullptr, Vn, kLdc, 1, m0, nh, 2, kDvm, m0 + 16,
                                   lane);
-            const int gq = lane >> 2, tq = lane & 3;
+            const int gq = lane >> 2;   // accumulator rows m0 + gq and m0 + gq + 8
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int r = m0 + gq + 8 * (q >> 1), cc = 8 * (nh + 2 * i) + 2 * tq + (q & 1);
-                    if (r < L && cc < nv)
-                        st_out(op + (r0 + r) * dv + dv0 + cc, fmaf(gm[r], a1[i][q], a2[i][q]));
-                }
+                for (int q = 0; q < 4; ++q)
+                    a1[i][q] = fmaf(gm[m0 + gq + 8 * (q >> 1)], a1[i][q], a2[i][q]);
+            store_pairs(a1, m0, nh, 2, nv, lane, L, op + r0 * dv + dv0, dv);
             __syncthreads();  // every read of H for this chunk is done
         }
         // H <- exp(g_C) H + K^T diag(exp(g_C - g)) V'
@@ -432,9 +454,7 @@ k_prep_mma(FwdArgs a, const int2 *__restrict__ table, float *__restrict__ W,
         const int ne = min(dv, c0 + 128);
         mma::gemm_s<8, SPLIT>(acc, Tm, kLdc, 1, bb, Vs, ldv, 1, m0, c0 / 8 + nh, 2, ne, m0 + 16,
                               lane);
-        mma::for_each(acc, m0, c0 / 8 + nh, 2, ne, lane, [&](int r, int j, float &x) {
-            if (r < L) U[(r0 + r) * dv + j] = x;
-        });
+        store_pairs(acc, m0, c0 / 8 + nh, 2, ne, lane, L, U + r0 * dv, dv);
     }
     if (tid < L) G[r0 + tid] = g[tid];
     if (Tout)
@@ -664,9 +684,7 @@ k_prep_vg(FwdArgs a, const int2 *__restrict__ table, float *__restrict__ W,
         mma::zero(acc);
         if (erase)
             mma::gemm_s<8, SPLIT>(acc, Tm, kLdc, 1, bb, Ks, ldk, 1, m0, nh, 2, dk, m0 + 16, lane);
-        mma::for_each(acc, m0, nh, 2, dk, lane, [&](int r, int j, float &x) {
-            if (r < L) W[(r0 + r) * dk + j] = x;
-        });
+        store_pairs(acc, m0, nh, 2, dk, lane, L, W + r0 * dk, dk);
     }
     {
         TileRegs<8> rv;
@@ -680,9 +698,7 @@ k_prep_vg(FwdArgs a, const int2 *__restrict__ table, float *__restrict__ W,
         const int ne = min(dv, c0 + 128);
         mma::gemm_s<8, SPLIT>(acc, Tm, kLdc, 1, bb, Vs, ldv, 1, m0, c0 / 8 + nh, 2, ne, m0 + 16,
                               lane);
-        mma::for_each(acc, m0, c0 / 8 + nh, 2, ne, lane, [&](int r, int j, float &x) {
-            if (r < L) U[(r0 + r) * dv + j] = x;
-        });
+        store_pairs(acc, m0, c0 / 8 + nh, 2, ne, lane, L, U + r0 * dv, dv);
     }
     for (int r = warp; r < L; r += kThreads / 32)
         for (int j = lane; j < dk; j += 32) G[(r0 + r) * dk + j] = Gs[r * ldk + j];
@@ -787,14 +803,11 @@ k_state_vg(FwdArgs a, const float *__restrict__ W, const float *__restrict__ U,
                                   lane);
             mma::gemm_s<4, SPLIT>(a2, P, kLdc, 1, nullptr, Vn, kLdc, 1, m0, nh, 2, kDvm, m0 + 16,
                                   lane);
-            const int gq = lane >> 2, tq = lane & 3;
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int r = m0 + gq + 8 * (q >> 1), cc = 8 * (nh + 2 * i) + 2 * tq + (q & 1);
-                    if (r < L && cc < nv) st_out(op + (r0 + r) * dv + dv0 + cc, a1[i][q] + a2[i][q]);
-                }
+                for (int q = 0; q < 4; ++q) a1[i][q] += a2[i][q];
+            store_pairs(a1, m0, nh, 2, nv, lane, L, op + r0 * dv + dv0, dv);
         }
         __syncthreads();  // every read of H for this chunk is done
         // H_j <- exp(G_Cj) H_j + sum_s k_sj exp(G_Cj - G_sj) V'_s
