@@ -20,8 +20,9 @@ tests/test_oracle_pins.py (beta = 0 decay, exact recall S k = v for
 alpha = beta = 1, affine-map bracketing, the T = 1 closed form, reduction to
 (gated) linear attention, linearity, continuation, varlen splitting; for the
 gradient: central finite differences of the forward loop, the exact adjoint
-identities of its linear arguments) and by planted-mistake checks that each
-of those pins catches.
+identities of its linear arguments), by examples worked by hand
+(tests/golden/, checked in tests/test_golden.py), and by planted-mistake
+checks that each of those pins catches.
 """
 from __future__ import annotations
 

@@ -61,7 +61,8 @@
  *
  * Parity pins for this file (closed forms, invariants, reductions to linear
  * attention, finite differences, planted-mistake checks) live in
- * tests/test_oracle_pins.py.
+ * tests/test_oracle_pins.py; examples worked by hand are in tests/golden/,
+ * checked by tests/test_golden.py.
  */
 #include <math.h>
 #include <stddef.h>
