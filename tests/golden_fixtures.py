@@ -90,3 +90,30 @@ def oracle_gradient_errors(lib) -> dict:
     got = oracle.gdn_bwd(one(g["q"]), one(g["k"]), one(g["v"]), one(g["log_alpha"]),
                          one(g["beta"]), one(g["h0"]), one(g["dO"]), one(g["dhT"]), lib=lib)
     return {n: rel(a[0, 0], g[n]) for n, a in zip(GRAD_NAMES, got)}
+
+
+def oracle_packed_gradient_errors(lib) -> dict:
+    """The gradient fixture packed as two sequences x two heads.  Head 1 has
+    v and h0 doubled: every state doubles (the states are linear in (h0, v)
+    jointly), so dq, dk, dlog_alpha and dbeta double while dv and dh0, which
+    depend only on dO, dhT, q and the gates, stay as they are.  Distinct
+    heads make a mix-up of the (sequence, head) state offsets visible."""
+    import oracle
+    g = load(GRADIENT)
+    scale = {"dq": 2.0, "dk": 2.0, "dv": 1.0, "dlog_alpha": 2.0, "dbeta": 2.0, "dh0": 1.0}
+    heads = lambda a, b: np.stack([np.concatenate([a, a]), np.concatenate([b, b])])  # noqa: E731
+    same = lambda n: heads(g[n], g[n])  # noqa: E731
+    h0 = np.stack([np.stack([g["h0"], 2 * g["h0"]])] * 2)          # [N=2][H=2]
+    dhT = np.stack([np.stack([g["dhT"], g["dhT"]])] * 2)
+    got = oracle.gdn_bwd_varlen(same("q"), same("k"), heads(g["v"], 2 * g["v"]),
+                                same("log_alpha"), same("beta"), np.array([0, 1, 2]), h0,
+                                same("dO"), dhT, lib=lib)
+    errs = {}
+    for n, a in zip(GRAD_NAMES, got):
+        for h in range(2):
+            want = g[n] * (scale[n] if h else 1.0)
+            if n == "dh0":
+                errs["dh0[h%d]" % h] = max(rel(a[s, h], want) for s in range(2))
+            else:
+                errs["%s[h%d]" % (n, h)] = rel(a[h], np.concatenate([want, want]))
+    return errs

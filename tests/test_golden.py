@@ -33,6 +33,11 @@ def test_oracle_matches_hand_worked_gradient(lib):
     assert max(errs.values()) <= ORACLE_TOL, errs
 
 
+def test_oracle_matches_hand_worked_gradient_packed(lib):
+    errs = G.oracle_packed_gradient_errors(lib)
+    assert max(errs.values()) <= ORACLE_TOL, errs
+
+
 def test_fixture_derivations_are_consistent():
     # what the derivations lean on: recall at beta = 1 (S_2 k_2 = v_2 for the
     # hand-derived S_2), and the gradient fixture's forward is the first
@@ -49,9 +54,7 @@ def test_fixture_derivations_are_consistent():
 
 def _planted():
     from tests.test_oracle_pins import MUTANTS
-    # a packed gradient with one head cannot tell the state offsets apart;
-    # the packed-split pin catches that mistake
-    return sorted(n for n in MUTANTS if n != "bwd_varlen_state_offset")
+    return sorted(MUTANTS)
 
 
 @pytest.fixture(scope="module")
@@ -74,6 +77,7 @@ def test_hand_worked_values_catch_planted_mistake(mutant_dir, name):
     for fx in G.FORWARD:
         errs.update({fx + ":" + k: v for k, v in G.oracle_forward_errors(mlib, fx).items()})
     errs.update(G.oracle_gradient_errors(mlib))
+    errs.update({"packed:" + k: v for k, v in G.oracle_packed_gradient_errors(mlib).items()})
     assert max(errs.values()) > 1e-6, errs
 
 
