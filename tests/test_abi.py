@@ -1,6 +1,5 @@
 """The C-ABI library loads and exports every function include/gdn.h declares,
 and its host-side argument checks answer without touching a GPU (CPU)."""
-import ctypes
 import os
 import re
 
