@@ -69,6 +69,7 @@ ABI = [
     ("gdn_kernel_launches", ctypes.c_uint64, []),
     ("gdn_last_impl", _i, []),
     ("gdn_release_scratch", _i, []),
+    ("gdn_selftest_wait", _i, [_i, ctypes.c_longlong, ctypes.POINTER(_i), _vp]),
 ]
 
 
@@ -403,6 +404,19 @@ def release_scratch(device=None) -> None:
     the current one) back to the driver."""
     with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
         _check(load().gdn_release_scratch(), "gdn_release_scratch")
+
+
+def selftest_wait(complete: bool, limit: int, device=None):
+    """Device self-test of the bounded waits (include/gdn_selftest.h): one CTA
+    waits on an mbarrier phase and a counter that it completes itself
+    (complete=True) or that nothing completes (each wait then gives up after
+    `limit` polls and records a timeout, which the next sync_check reports).
+    Returns (mbarrier wait succeeded, counter wait succeeded)."""
+    ok = (_i * 2)()
+    with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
+        _check(load().gdn_selftest_wait(1 if complete else 0, int(limit), ok, _stream(device)),
+               "gdn_selftest_wait")
+    return bool(ok[0]), bool(ok[1])
 
 
 class use_impl:

@@ -134,3 +134,9 @@ def test_decode_host_checks(lib):
 def test_binding_fails_loudly_without_library(tmp_path):
     with pytest.raises(ImportError):
         gdn.load(str(tmp_path / "missing.so"))
+
+
+def test_selftest_argument_checks(lib):
+    # rejected on the host, before any CUDA call
+    for complete, limit in ((2, 10), (-1, 10), (0, 0), (1, -5), (0, (1 << 22) + 1)):
+        assert lib.gdn_selftest_wait(complete, limit, None, None) == gdn.GDN_ERR_INVALID_ARG
