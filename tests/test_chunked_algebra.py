@@ -131,3 +131,94 @@ def test_no_erase_makes_the_inverse_the_identity(lib):
         S = np.exp(g[-1]) * S + Vn.T @ (kk[sl] * np.exp(g[-1] - g)[:, None])
     assert P._rel(o, o_ref[0, 0]) <= TOL
     assert P._rel(S, h_ref[0, 0]) <= TOL
+
+
+# ------------------------------------------------- a forget gate per key dimension
+#
+# With alpha_t a d_k-vector ("Gated DeltaNet GPU并行实现", section 2.2, the
+# diagonal gate acting on the old state first) the same unrolling gives, with
+# G_r the running sum of the log-gate vectors and Gamma_r = e^{G_r}:
+#   A_rs = beta_r sum_j k_rj k_sj e^{G_rj - G_sj}       (s < r)
+#   W = T diag(beta) (K * Gamma),  U = T diag(beta) V,  V' = U - W S_0^T
+#   O = (Q * Gamma) S_0^T + P V',  P_rs = sum_j q_rj k_sj e^{G_rj - G_sj}  (s <= r)
+#   S_C = S_0 diag(Gamma_C) + V'^T (K * e^{G_C - G})
+# The decay inside A and P is taken block by block (16 rows): for a row block
+# after a key block, e^{G_r - G_s} = e^{G_r - G_m} e^{G_m - G_s} with m the key
+# block's last row, so both factors are at most 1 and nothing overflows.
+
+BLK = 16
+
+
+def decayed_products(X, K, G, inclusive):
+    """sum_j X_rj K_sj e^{G_rj - G_sj} for s < r (s <= r when inclusive), by
+    16-row blocks with every exponent <= 0."""
+    L = len(G)
+    out = np.zeros((L, L))
+    for b0 in range(0, L, BLK):
+        rows = slice(b0, min(b0 + BLK, L))
+        for c0 in range(0, b0 + 1, BLK):
+            cols = slice(c0, min(c0 + BLK, L))
+            if c0 < b0:
+                m = cols.stop - 1                  # the key block's last row
+                fr, fs = G[rows] - G[m], G[m] - G[cols]
+                assert fr.max() <= 0 and fs.max() <= 0
+                out[rows, cols] = (X[rows] * np.exp(fr)) @ (K[cols] * np.exp(fs)).T
+            else:                                  # diagonal block: pairwise
+                for r in range(rows.start, rows.stop):
+                    last = r + 1 if inclusive else r
+                    for s in range(cols.start, last):
+                        assert (G[r] - G[s]).max() <= 0
+                        out[r, s] = X[r] @ (K[s] * np.exp(G[r] - G[s]))
+    return out
+
+
+def chunked_forward_vg(q, k, v, la, be, h0, C, erase=True):
+    T, dk = k.shape
+    dv = v.shape[1]
+    S = np.zeros((dv, dk)) if h0 is None else h0.copy()
+    o = np.zeros((T, dv))
+    for t0 in range(0, T, C):
+        sl = slice(t0, min(t0 + C, T))
+        qc, kc, vc, bc = q[sl], k[sl], v[sl], be[sl]
+        G = np.cumsum(la[sl], axis=0)
+        Gam = np.exp(G)
+        L = len(bc)
+        A = (bc[:, None] * decayed_products(kc, kc, G, inclusive=False) if erase
+             else np.zeros((L, L)))
+        inv = np.linalg.solve(np.eye(L) + A, np.eye(L))
+        W = inv @ (bc[:, None] * kc * Gam) if erase else np.zeros((L, dk))
+        U = inv @ (bc[:, None] * vc)
+        Vn = U - W @ S.T
+        Pm = decayed_products(qc, kc, G, inclusive=True)
+        o[sl] = (qc * Gam) @ S.T + Pm @ Vn
+        S = S * Gam[-1][None, :] + Vn.T @ (kc * np.exp(G[-1] - G))
+    return o, S
+
+
+@pytest.mark.parametrize("erase", [True, False])
+@pytest.mark.parametrize("T,C", [(1, 64), (40, 16), (64, 64), (100, 64), (131, 32)])
+def test_vector_gate_chunked_form_equals_token_loop(lib, T, C, erase):
+    rng = np.random.default_rng(500 + T + C)
+    dk, dv = 6, 5
+    q, k, v, _, be = P._rand_inputs(rng, 1, 1, T, dk, dv)
+    la = -0.5 * np.log1p(np.exp(rng.standard_normal((1, 1, T, dk))))
+    h0 = rng.standard_normal((1, 1, dv, dk))
+    o_ref, h_ref = oracle.gdn_fwd(q, k, v, la, be, h0, lib=lib, erase=erase, vector_gate=True)
+    o, S = chunked_forward_vg(q[0, 0], k[0, 0], v[0, 0], la[0, 0], be[0, 0], h0[0, 0], C,
+                              erase=erase)
+    assert P._rel(o, o_ref[0, 0]) <= TOL
+    assert P._rel(S, h_ref[0, 0]) <= TOL
+
+
+def test_vector_gate_blocks_survive_steep_decay(lib):
+    # decays far beyond fp32's exponent range over one chunk: the blocked
+    # factors stay <= 1, so the chunked form still matches the token loop
+    rng = np.random.default_rng(77)
+    T, dk, dv = 64, 4, 3
+    q, k, v, _, be = P._rand_inputs(rng, 1, 1, T, dk, dv)
+    la = -rng.uniform(2.0, 6.0, (1, 1, T, dk))
+    h0 = rng.standard_normal((1, 1, dv, dk))
+    o_ref, h_ref = oracle.gdn_fwd(q, k, v, la, be, h0, lib=lib, vector_gate=True)
+    o, S = chunked_forward_vg(q[0, 0], k[0, 0], v[0, 0], la[0, 0], be[0, 0], h0[0, 0], 64)
+    assert np.isfinite(o).all() and np.isfinite(S).all()
+    assert P._rel(o, o_ref[0, 0]) <= TOL
