@@ -222,3 +222,122 @@ def test_vector_gate_blocks_survive_steep_decay(lib):
     o, S = chunked_forward_vg(q[0, 0], k[0, 0], v[0, 0], la[0, 0], be[0, 0], h0[0, 0], 64)
     assert np.isfinite(o).all() and np.isfinite(S).all()
     assert P._rel(o, o_ref[0, 0]) <= TOL
+
+
+# ------------------------------------------------------------- backward pass
+#
+# The chunked adjoint the backward kernels compute (scalar gates), for
+# L = sum dO . o + <dhT, hT>.  Per chunk, with M = strictly_lower(G * K K^T),
+# A = diag(beta) M, P = mask * G * Q K^T (mask: s <= r) and dSC the adjoint of
+# the chunk's end state, in reverse over the chunks:
+#   dV' = P^T dO + diag(e) K dSC^T
+#   dS0 = gamma_C dSC + dO^T diag(gamma) Q - dV'^T W
+# and then, chunk by chunk with no order:
+#   dQ = diag(gamma) dO S0 + dP K,   dP = mask * G * (dO V'^T)
+#   dW = -dV' S0,  dV = diag(beta) T^T dV',  dT = dV' (diag(beta) V)^T + dW (diag(beta gamma) K)^T
+#   dA = strictly_lower(-T^T dT T^T),  dM = diag(beta) dA
+#   dK = dP^T Q + diag(e) V' dSC + diag(beta gamma) T^T dW + (N + N^T) K,  N = dM * G
+#   dbeta_r = v_r . (T^T dV')_r + gamma_r k_r . (T^T dW)_r + sum_s dA_rs M_rs
+#   dg      = gamma * rowdot(dO S0, Q) + rowsum - colsum of (P * dO V'^T) and of (dM * M)
+#             + beta gamma rowdot(T^T dW, K), plus at the chunk's end
+#             gamma_C <dSC, S0> + sum_r e_r v'_r . dSC k_r, minus e_r v'_r . dSC k_r at r
+#   dlog_alpha = the reverse running sum of dg inside the chunk.
+
+
+def _chunk_fwd(k, v, la, be, S0, erase):
+    g = np.cumsum(la)
+    gam = np.exp(g)
+    L = len(la)
+    diff = g[:, None] - g[None, :]
+    G = np.exp(np.tril(diff))                      # e^{g_r - g_s}, 1 above the diagonal
+    M = np.tril(G * (k @ k.T), -1) if erase else np.zeros((L, L))
+    T = np.linalg.solve(np.eye(L) + be[:, None] * M, np.eye(L))
+    W = T @ ((be * gam)[:, None] * k) if erase else np.zeros_like(k)
+    U = T @ (be[:, None] * v)
+    Vn = U - W @ S0.T
+    e = np.exp(g[-1] - g)
+    SC = gam[-1] * S0 + Vn.T @ (e[:, None] * k)
+    return dict(g=g, gam=gam, G=G, M=M, T=T, W=W, Vn=Vn, e=e, SC=SC)
+
+
+def chunked_backward(q, k, v, la, be, h0, dO, dhT, C, erase=True):
+    """One (sequence, head): (dq, dk, dv, dlog_alpha, dbeta, dh0)."""
+    Tn, dk = k.shape
+    dv = v.shape[1]
+    chunks = [slice(t0, min(t0 + C, Tn)) for t0 in range(0, Tn, C)]
+    # forward: every chunk's starting state and factors
+    S = np.zeros((dv, dk)) if h0 is None else h0.copy()
+    fw = []
+    for sl in chunks:
+        f = _chunk_fwd(k[sl], v[sl], la[sl], be[sl], S, erase)
+        f["S0"] = S
+        fw.append(f)
+        S = f["SC"]
+    # reverse over chunks: the adjoint of each chunk's end state
+    dSC = np.zeros((dv, dk)) if dhT is None else dhT.copy()
+    for sl, f in zip(reversed(chunks), reversed(fw)):
+        f["dSC"] = dSC
+        P = np.tril(f["G"] * (q[sl] @ k[sl].T))
+        f["P"] = P
+        f["dVn"] = P.T @ dO[sl] + (f["e"][:, None] * k[sl]) @ dSC.T
+        dSC = (f["gam"][-1] * dSC + dO[sl].T @ (f["gam"][:, None] * q[sl])
+               - f["dVn"].T @ f["W"])
+    dh0 = dSC
+    out = [np.zeros_like(q), np.zeros_like(k), np.zeros_like(v), np.zeros_like(la),
+           np.zeros_like(be)]
+    for sl, f in zip(chunks, fw):
+        for i, grad in enumerate(_chunk_grads(q[sl], k[sl], v[sl], be[sl], dO[sl], f, erase)):
+            out[i][sl] = grad
+    return (*out, dh0)
+
+
+def _chunk_grads(q, k, v, be, dO, f, erase):
+    g, gam, G, M, T, Vn, e = (f[n] for n in ("g", "gam", "G", "M", "T", "Vn", "e"))
+    S0, dSC, dVn, P = f["S0"], f["dSC"], f["dVn"], f["P"]
+    dOV = dO @ Vn.T
+    dP = np.tril(G * dOV)
+    TdU = T.T @ dVn
+    # W = T diag(beta gamma) K only exists with the erase term
+    dW = -dVn @ S0
+    TdW = T.T @ dW if erase else np.zeros_like(k)
+    dq = gam[:, None] * (dO @ S0) + dP @ k
+    dv = be[:, None] * TdU
+    dk = dP.T @ q + e[:, None] * (Vn @ dSC) + (be * gam)[:, None] * TdW
+    dbeta = np.sum(v * TdU, axis=1) + gam * np.sum(k * TdW, axis=1)
+    dg = gam * np.sum((dO @ S0) * q, axis=1) + be * gam * np.sum(TdW * k, axis=1)
+    Y = P * dOV
+    dg += Y.sum(axis=1) - Y.sum(axis=0)
+    if erase:
+        dT = dVn @ (be[:, None] * v).T + dW @ ((be * gam)[:, None] * k).T
+        dA = np.tril(-T.T @ dT @ T.T, -1)
+        dM = be[:, None] * dA
+        N = dM * G
+        dk += (N + N.T) @ k
+        dbeta += np.sum(dA * M, axis=1)
+        Z = dM * M
+        dg += Z.sum(axis=1) - Z.sum(axis=0)
+    # the chunk's end state: gamma_C S0 and e_r = e^{g_C - g_r}
+    de = np.einsum("ri,ij,rj->r", Vn, dSC, k)      # v'_r . dSC k_r
+    dg[-1] += gam[-1] * np.sum(dSC * S0) + np.sum(e * de)
+    dg -= e * de
+    dla = np.cumsum(dg[::-1])[::-1]
+    return dq, dk, dv, dla, dbeta
+
+
+BWD_NAMES = ("dq", "dk", "dv", "dlog_alpha", "dbeta", "dh0")
+
+
+@pytest.mark.parametrize("erase", [True, False])
+@pytest.mark.parametrize("T,C", [(1, 64), (17, 16), (64, 64), (100, 64), (130, 32)])
+def test_chunked_adjoint_equals_oracle_gradient(lib, T, C, erase):
+    rng = np.random.default_rng(900 + T + C)
+    dk, dv = 6, 5
+    q, k, v, la, be = P._rand_inputs(rng, 1, 1, T, dk, dv)
+    h0 = rng.standard_normal((1, 1, dv, dk))
+    dO = rng.standard_normal((1, 1, T, dv))
+    dhT = rng.standard_normal((1, 1, dv, dk))
+    ref = oracle.gdn_bwd(q, k, v, la, be, h0, dO, dhT, lib=lib, erase=erase)
+    got = chunked_backward(q[0, 0], k[0, 0], v[0, 0], la[0, 0], be[0, 0], h0[0, 0],
+                           dO[0, 0], dhT[0, 0], C, erase=erase)
+    errs = {n: P._rel(a, b[0, 0]) for n, a, b in zip(BWD_NAMES, got, ref)}
+    assert max(errs.values()) <= TOL, errs
