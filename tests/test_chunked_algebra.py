@@ -341,3 +341,30 @@ def test_chunked_adjoint_equals_oracle_gradient(lib, T, C, erase):
                            dO[0, 0], dhT[0, 0], C, erase=erase)
     errs = {n: P._rel(a, b[0, 0]) for n, a, b in zip(BWD_NAMES, got, ref)}
     assert max(errs.values()) <= TOL, errs
+
+
+def test_factorised_decay_holds_in_fp32_up_to_the_span_guard():
+    # P^T dO with P_rs = e^{g_r - g_s} (q_r . k_s) equals P'^T (gamma * dO),
+    # P'_rs = e^{-g_s} (q_r . k_s): the backward's tensor-core adjoint forms the
+    # latter while the chunk's total log-decay g_C stays >= -80, where e^{-g_s}
+    # is finite in fp32 (its exponent range ends near 88.7); past that bound
+    # it forms P directly
+    rng = np.random.default_rng(11)
+    L, dk, dv = 64, 8, 4
+    q = rng.standard_normal((L, dk)).astype(np.float32)
+    k = rng.standard_normal((L, dk)).astype(np.float32)
+    dO = rng.standard_normal((L, dv)).astype(np.float32)
+    mask = np.tril(np.ones((L, L), dtype=np.float32))
+    for gC, finite in ((-20.0, True), (-80.0, True), (-95.0, False)):
+        g = np.linspace(gC / L, gC, L).astype(np.float32)
+        with np.errstate(over="ignore", invalid="ignore"):
+            direct = (mask * np.exp(np.tril(g[:, None] - g[None, :])) * (q @ k.T)).T @ dO
+            Pp = mask * np.exp(-g)[None, :] * (q @ k.T)
+            fact = Pp.T @ (np.exp(g)[:, None] * dO)
+        ref = (np.tril(np.exp(np.float64(g)[:, None] - np.float64(g)[None, :]))
+               * (q.astype(np.float64) @ k.T.astype(np.float64))).T @ dO
+        assert np.isfinite(direct).all()
+        assert P._rel(direct, ref) <= 1e-5
+        assert np.isfinite(fact).all() == finite
+        if finite:
+            assert P._rel(fact, ref) <= 1e-5
