@@ -368,3 +368,33 @@ def test_factorised_decay_holds_in_fp32_up_to_the_span_guard():
         assert np.isfinite(fact).all() == finite
         if finite:
             assert P._rel(fact, ref) <= 1e-5
+
+
+def test_decode_row_form_equals_one_token(lib):
+    # the decode kernel's form of one step: S' = alpha S + d k^T with
+    # d = beta (v - alpha S k), and o = alpha S q + d (k . q); each row of the
+    # new state needs only the same row of the old one
+    rng = np.random.default_rng(13)
+    dk, dv = 7, 5
+    q, k, v, la, be = P._rand_inputs(rng, 1, 1, 1, dk, dv)
+    S = rng.standard_normal((1, 1, dv, dk))
+    o_ref, h_ref = oracle.gdn_fwd(q, k, v, la, be, S, lib=lib)
+    a, b = np.exp(la[0, 0, 0]), be[0, 0, 0]
+    qq, kk, vv, SS = q[0, 0, 0], k[0, 0, 0], v[0, 0, 0], S[0, 0]
+    d = b * (vv - a * SS @ kk)
+    assert P._rel(a * SS + np.outer(d, kk), h_ref[0, 0]) <= TOL
+    assert P._rel(a * SS @ qq + d * (kk @ qq), o_ref[0, 0, 0]) <= TOL
+
+
+def test_segment_map_from_the_forward_itself(lib):
+    # a segment's affine map S -> S A + B read off two forward runs: A is the
+    # final state from h0 = I with v = 0 (d_v taken as d_k), B the final
+    # state from h0 = 0 with the real v; then any h0 gives h0 A + B
+    rng = np.random.default_rng(17)
+    T, dk, dv = 90, 5, 3
+    q, k, v, la, be = P._rand_inputs(rng, 1, 1, T, dk, dv)
+    _, A = oracle.gdn_fwd(q, k, np.zeros((1, 1, T, dk)), la, be, np.eye(dk)[None, None], lib=lib)
+    _, B = oracle.gdn_fwd(q, k, v, la, be, None, lib=lib)
+    h0 = rng.standard_normal((1, 1, dv, dk))
+    _, h_ref = oracle.gdn_fwd(q, k, v, la, be, h0, lib=lib)
+    assert P._rel(h0[0, 0] @ A[0, 0] + B[0, 0], h_ref[0, 0]) <= TOL
