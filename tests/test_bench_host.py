@@ -1,6 +1,7 @@
-"""The benchmark's host-side arithmetic on CPU: compulsory bytes and FLOPs
-behind the roofline figures, the clock-record summary, the peaks file and the
-rule that a DRAM-traffic record counts only at the sources it was taken on."""
+"""The benchmark's host side on CPU: compulsory bytes and FLOPs behind the
+roofline figures, the clock-record summary, the peaks file, the rule that a
+DRAM-traffic record counts only at the sources it was taken on, and the
+reference arm's JSON line (the oracle timed on the host)."""
 import os
 
 import pytest
@@ -114,3 +115,22 @@ def test_every_timed_kernel_names_existing_sources():
     for kernel, files in bench.KERNEL_SOURCES.items():
         for f in files:
             assert os.path.exists(os.path.join(csrc, f)), (kernel, f)
+
+
+def test_reference_arm_line_keeps_the_contract():
+    # the oracle timed on the host cores, on a bounded sample (rank 0 only)
+    args = type("A", (), {"workload": "gdn_fwd_b1_h1_t256_d64_fp32", "steps": 1,
+                          "warmup": 0, "cpu_seconds": 1.0})()
+    assert bench.run_reference(args, 2, 1) is None          # other ranks: no work
+    line = bench.run_reference(args, 1, 0)
+    assert line["impl"] == "reference" and line["value"] > 0
+    assert line["unit"] == bench.UNIT and line["higher_is_better"] is True
+    assert line["metric"] == bench.METRIC and line["dtype"] == "f64"
+    assert line["config"]["workload"] == "gdn_fwd_b1_h1_t256_d64_fp32"
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] == 1 and cb["value"] == line["value"]
+    assert cb["unit"] == line["unit"] and cb["sample"]
+    e2e = line["e2e"]
+    assert e2e["value"] == line["value"] and e2e["unit"] == line["unit"]
+    assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+    assert line["steps"] == 1 and line["warmup"] == 0 and line["n_gpus"] == 1
