@@ -401,7 +401,7 @@ def last_impl() -> int:
 
 def release_scratch(device=None) -> None:
     """Hand the scratch memory the library's pool keeps on `device` (default:
-    the current one) back to the driver."""
+    the current one) back to the CUDA driver."""
     with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
         _check(load().gdn_release_scratch(), "gdn_release_scratch")
 
