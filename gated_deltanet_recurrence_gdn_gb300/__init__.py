@@ -409,8 +409,9 @@ def release_scratch(device=None) -> None:
 def selftest_wait(complete: bool, limit: int, device=None):
     """Device self-test of the bounded waits (include/gdn_selftest.h): one CTA
     waits on an mbarrier phase and a counter that it completes itself
-    (complete=True) or that nothing completes (each wait then gives up after
-    `limit` polls and records a timeout, which the next sync_check reports).
+    (complete=True) or that nothing completes (the mbarrier wait then gives
+    up after `limit` suspending polls, the counter wait after 4 * limit loads,
+    and a timeout is recorded that the next sync_check reports).
     Returns (mbarrier wait succeeded, counter wait succeeded)."""
     ok = (_i * 2)()
     with torch.cuda.device(device if device is not None else torch.cuda.current_device()):

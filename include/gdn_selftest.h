@@ -24,12 +24,13 @@ extern "C" {
  * counter.
  *   complete    1: the CTA completes the phase and sets the counter before
  *               waiting, so both waits succeed and no error is recorded;
- *               0: nothing completes them, so both waits give up after
- *               `limit` polls and a timeout is recorded in the device error
- *               word (read and cleared by gdn_sync_check).
- *   limit       polls per wait, 1 <= limit <= 1 << 22 (each poll suspends
- *               for at most a hardware-defined interval, so this bounds the
- *               kernel's run time).
+ *               0: nothing completes them, so both waits give up and a
+ *               timeout is recorded in the device error word (read and
+ *               cleared by gdn_sync_check).
+ *   limit       the poll bound, 1 <= limit <= 1 << 22: the mbarrier wait
+ *               gives up after `limit` suspending polls (each suspends for at
+ *               most a hardware-defined interval), the counter wait after
+ *               4 * limit acquire loads, so the kernel's run time is bounded.
  *   waits_ok    host pointer to 2 ints or NULL: whether the mbarrier wait and
  *               the counter wait succeeded (1) or gave up (0).
  *   stream      cudaStream_t to enqueue on; the call synchronises it.
