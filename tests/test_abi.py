@@ -140,3 +140,20 @@ def test_selftest_argument_checks(lib):
     # rejected on the host, before any CUDA call
     for complete, limit in ((2, 10), (-1, 10), (0, 0), (1, -5), (0, (1 << 22) + 1)):
         assert lib.gdn_selftest_wait(complete, limit, None, None) == gdn.GDN_ERR_INVALID_ARG
+
+
+def test_build_targets_sm103a_only():
+    flags = _build.ARCH
+    assert flags == ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def test_binding_refuses_host_tensors(lib):
+    # no CPU fallback: host tensors are rejected before anything runs
+    import torch
+    x = torch.zeros(1, 1, 4, 8)
+    g = torch.zeros(1, 1, 4)
+    with pytest.raises(ValueError):
+        gdn.gdn_fwd(x, x, x, g, g)
+    with pytest.raises(ValueError):
+        gdn.gdn_decode(x[:, :, 0], x[:, :, 0], x[:, :, 0], g[:, :, 0], g[:, :, 0],
+                       torch.zeros(1, 1, 8, 8))
