@@ -39,6 +39,7 @@ GDN_OPT_POISON_SCRATCH = 3
 GDN_IMPL_AUTO = 0
 GDN_IMPL_SIMT = 1
 GDN_IMPL_TC = 2
+GDN_IMPL_TC_FUSED = 3
 
 CHUNK = 64
 
@@ -421,7 +422,7 @@ def selftest_wait(complete: bool, limit: int, device=None):
 
 
 class use_impl:
-    """Context manager forcing GDN_IMPL_SIMT / GDN_IMPL_TC / GDN_IMPL_AUTO."""
+    """Context manager forcing GDN_IMPL_SIMT / GDN_IMPL_TC / GDN_IMPL_TC_FUSED / GDN_IMPL_AUTO."""
 
     def __init__(self, impl: int, segments: int | None = None):
         self.impl, self.segments = impl, segments

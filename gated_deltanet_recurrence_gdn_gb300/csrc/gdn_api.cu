@@ -55,6 +55,10 @@ gdn_status dispatch(FwdArgs &a) {
     if (impl == GDN_IMPL_SIMT || (impl == GDN_IMPL_AUTO && !tc_supported(a))) {
         rc = simt_forward(a);
         used = GDN_IMPL_SIMT;
+    } else if (impl == GDN_IMPL_TC_FUSED) {
+        if (!tc_supported(a) || !fused_supported(a)) return GDN_ERR_UNSUPPORTED;
+        rc = fused_forward(a);
+        used = GDN_IMPL_TC_FUSED;
     } else {
         if (!tc_supported(a)) return GDN_ERR_UNSUPPORTED;
         rc = tc_forward(a);
@@ -361,7 +365,7 @@ gdn_status gdn_sync_check(void *stream) {
 gdn_status gdn_set_option(int key, long long value) {
     switch (key) {
         case GDN_OPT_IMPL:
-            if (value < GDN_IMPL_AUTO || value > GDN_IMPL_TC) return GDN_ERR_INVALID_ARG;
+            if (value < GDN_IMPL_AUTO || value > GDN_IMPL_TC_FUSED) return GDN_ERR_INVALID_ARG;
             g_opt_impl.store(value);
             return GDN_OK;
         case GDN_OPT_SEGMENTS:

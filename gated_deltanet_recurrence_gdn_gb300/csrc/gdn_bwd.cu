@@ -805,7 +805,7 @@ gdn_status run_backward(const FwdArgs &a, const BwdArgs &b, long long impl, int 
     if (chunk_lay(a.dk).bytes > 227 * 1024 || dstate_smem(a.dk) > 227 * 1024)
         return GDN_ERR_UNSUPPORTED;
     const bool tc = impl != GDN_IMPL_SIMT && tc_bwd_supported(a) && tc_supported(a);
-    if (impl == GDN_IMPL_TC && !tc) return GDN_ERR_UNSUPPORTED;
+    if ((impl == GDN_IMPL_TC || impl == GDN_IMPL_TC_FUSED) && !tc) return GDN_ERR_UNSUPPORTED;
     const gdn_status rc = a.dt == GDN_F32 ? launch_bwd<float>(a, b, false)
                                           : launch_bwd<__nv_bfloat16>(a, b, tc);
     if (used) *used = tc ? GDN_IMPL_TC : GDN_IMPL_SIMT;

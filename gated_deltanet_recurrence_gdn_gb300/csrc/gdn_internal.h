@@ -122,6 +122,16 @@ size_t tc_prep_smem(int dk);
 gdn_status enqueue_tc_prep(const FwdArgs &a, const int2 *table, __nv_bfloat16 *Tu,
                            __nv_bfloat16 *W);
 
+// Chunk-prep kernel of the fused forward (gdn_ut.cu): T_u = (I + A)^{-1} diag(beta)
+// and T_w = (I + A)^{-1} diag(beta gamma) of every chunk as bf16
+// [H][chunk_slots][T_u | T_w][64][64] (slot of chunk c of sequence n: dense
+// n * max_chunks + c, packed floor(cu[n] / 64) + n + c; table: packed batches
+// only).  The fused forward (gdn_fused.cu) reads it and forms W, U,
+// the state pass and the output in one kernel per (sequence, head, d_v tile).
+gdn_status enqueue_ut(const FwdArgs &a, const int2 *table, __nv_bfloat16 *Tu);
+bool fused_supported(const FwdArgs &a);
+gdn_status fused_forward(const FwdArgs &a);
+
 // tcgen05 tensor-core path (bf16 I/O).  Returns GDN_ERR_UNSUPPORTED when the
 // call does not fit it; the caller then decides whether to fall back.
 bool tc_supported(const FwdArgs &a);

@@ -33,15 +33,19 @@
 
 #include "gdn_bwd_tc.h"
 #include "gdn_internal.h"
+#include "gdn_inv.cuh"
 #include "tc_ptx.cuh"
 
 namespace gdn {
 namespace {
 
 using ptx::griddep_launch_dependents;
+using inv::LDA;
+using inv::ldsm4;
+using inv::saddr;
+using inv::tf32;
 
 constexpr int kCp = 64;
-constexpr int LDA = 68;   // fp32 row stride of A / T
 constexpr int LDT = 72;   // bf16 row stride of the T_w tile
 
 template <int DK>
@@ -63,22 +67,6 @@ struct PrepLay {
     static_assert(kCp * LDT * 2 <= TBYTES && kCp * LDK * 2 <= TBYTES, "staging fits");
 };
 
-__device__ __forceinline__ float tf32(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return __uint_as_float(r);
-}
-
-// D += A(16x8, row) * B(8x8, col), tf32 inputs, fp32 accumulate.
-__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], const float (&b)[2]) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(__float_as_uint(b[0])),
-          "r"(__float_as_uint(b[1])));
-}
-
 // D += A(16x16, row) * B(16x8, col), bf16 inputs (two per register), fp32 accumulate.
 __device__ __forceinline__ void mma_bf16x16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
                                             uint32_t b1) {
@@ -89,56 +77,11 @@ __device__ __forceinline__ void mma_bf16x16(float (&d)[4], const uint32_t (&a)[4
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ uint32_t saddr(const void *p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-// Four 8x8 bf16 matrices from shared memory (lanes 8i..8i+7 give the row
-// addresses of matrix i); .trans hands each thread a column pair instead.
-__device__ __forceinline__ void ldsm4(uint32_t (&r)[4], uint32_t addr) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(addr)
-                 : "memory");
-}
 __device__ __forceinline__ void ldsm4t(uint32_t (&r)[4], uint32_t addr) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                  : "r"(addr)
                  : "memory");
-}
-
-// One 16x8 output tile of  Y = Am * Bm  over the 8-wide k steps [kb, ke),
-// operands tf32 values stored as fp32 in smem (row-major, strides lda / ldb;
-// Am 16-byte aligned with lda a multiple of 4).  The A fragment of a k step is
-// one ldmatrix: its 8x8 b16 matrices are 8x4 fp32 blocks, which hand thread
-// (g, t) element (g, t) -- the tf32 fragment layout.
-template <int K>
-__device__ __forceinline__ void tile_mma(float (&c)[4], const float *Am, int lda, const float *Bm,
-                                         int ldb, int lane, int kb = 0, int ke = K / 8) {
-    const int g = lane >> 2, t = lane & 3;
-    c[0] = c[1] = c[2] = c[3] = 0.f;
-    const uint32_t a_addr = saddr(Am + (lane & 15) * lda + 4 * (lane >> 4));
-#pragma unroll
-    for (int ks = 0; ks < K / 8; ++ks) {
-        if (ks < kb || ks >= ke) continue;
-        const int k0 = 8 * ks;
-        uint32_t a[4];
-        ldsm4(a, a_addr + 4 * k0);
-        const float b[2] = {Bm[(k0 + t) * ldb + g], Bm[(k0 + t + 4) * ldb + g]};
-        mma_tf32(c, a, b);
-    }
-}
-
-// Stores scale * C rounded to tf32 (every fp32 matrix in smem holds tf32
-// values, so the products read it without conversion).
-__device__ __forceinline__ void store_tile(float *D, int ldd, const float (&c)[4], int lane,
-                                           float scale) {
-    const int g = lane >> 2, t = lane & 3;
-    *reinterpret_cast<float2 *>(D + g * ldd + 2 * t) =
-        make_float2(tf32(scale * c[0]), tf32(scale * c[1]));
-    *reinterpret_cast<float2 *>(D + (g + 8) * ldd + 2 * t) =
-        make_float2(tf32(scale * c[2]), tf32(scale * c[3]));
 }
 
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
@@ -331,77 +274,14 @@ k_gdn_prep(const __nv_bfloat16 *__restrict__ k, const float *__restrict__ log_al
                     }
                 }
         } else if (live) {
-            for (int i = lane; i < 2 * 256; i += 32) {
-                const int b = i >> 8, e = i & 255;
-                Tb[(32 * b + (e >> 4)) * LDA + 32 * b + 16 + (e & 15)] = 0.f;
-            }
+            inv::clear_upper16(Tb, lane, 32);
         }
         fetch(r0n, Lcn);   // next unit's loads fly during the rest of this one
         if (live) {
             __syncthreads();
 
             // ---- T = (I + A)^{-1}
-            if (w < 2) {
-                // 16x16 diagonal blocks, one column cc per thread: row by row,
-                // x_r = delta_{r,cc} - sum_{s<r} A_rs x_s, A's rows read as
-                // float4 broadcasts
-                const int blk = tid >> 4, cc = tid & 15, o = blk * 16;
-                float x[16];
-#pragma unroll
-                for (int r = 0; r < 16; ++r) {
-                    const float4 *row = reinterpret_cast<const float4 *>(Ab + (o + r) * LDA + o);
-                    float acc = (r == cc) ? 1.f : 0.f;
-#pragma unroll
-                    for (int q = 0; 4 * q < r; ++q) {
-                        const float4 a4 = row[q];
-                        const float av[4] = {a4.x, a4.y, a4.z, a4.w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            if (4 * q + e < r) acc = fmaf(-av[e], x[4 * q + e], acc);
-                    }
-                    x[r] = acc;
-                }
-#pragma unroll
-                for (int r = 0; r < 16; ++r) Tb[(o + r) * LDA + o + cc] = tf32(x[r]);
-            }
-            __syncthreads();
-            {
-                // 16 -> 32: T_{2p+1,2p} = -D_{2p+1} A_{2p+1,2p} D_{2p}  (D_{2p} is
-                // lower triangular: its columns 8-15 have zero rows 0-7)
-                const int pr = w >> 1, nh = w & 1;
-                const int ro = 32 * pr + 16, co = 32 * pr;
-                float *Xw = Tb + (16 * pr) * LDA + 32 + 8 * nh;
-                float c4[4];
-                tile_mma<16>(c4, Ab + ro * LDA + co, LDA, Tb + co * LDA + co + 8 * nh, LDA, lane, nh);
-                store_tile(Xw, LDA, c4, lane, 1.f);
-                __syncwarp();
-                tile_mma<16>(c4, Tb + ro * LDA + ro, LDA, Xw, LDA, lane);
-                store_tile(Tb + ro * LDA + co + 8 * nh, LDA, c4, lane, -1.f);
-            }
-            __syncthreads();
-            {
-                // 32 -> 64: T_{1,0} = -E1 (A_{1,0} E0), 32x32 blocks; E0 and E1
-                // are lower triangular, so k steps of zero operand rows or
-                // columns are skipped
-                float *Xb = Tb + 32;
-                const int mt = w >> 1, nt0 = 2 * (w & 1);
-#pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    float c4[4];
-                    tile_mma<32>(c4, Ab + (32 + 16 * mt) * LDA, LDA, Tb + 8 * (nt0 + q), LDA, lane,
-                                 nt0 + q);
-                    store_tile(Xb + 16 * mt * LDA + 8 * (nt0 + q), LDA, c4, lane, 1.f);
-                }
-                __syncthreads();
-#pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    float c4[4];
-                    tile_mma<32>(c4, Tb + (32 + 16 * mt) * LDA + 32, LDA, Xb + 8 * (nt0 + q), LDA,
-                                 lane, 0, 2 + 2 * mt);
-                    store_tile(Tb + (32 + 16 * mt) * LDA + 8 * (nt0 + q), LDA, c4, lane, -1.f);
-                }
-            }
-            __syncthreads();
+            inv::invert64(Ab, Tb, tid, [] { __syncthreads(); });
 
             // ---- T_u = T diag(beta) rows out (bf16), and T_w = T diag(beta gamma)
             //      as the bf16 A operand of W = T_w K (in A's space): lane l

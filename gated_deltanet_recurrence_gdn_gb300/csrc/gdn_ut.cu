@@ -1,0 +1,444 @@
+// gdn_ut.cu -- chunk-prep kernel of the forward pass: for every chunk of C = 64
+// tokens of every (sequence, head), with g_r = sum_{i<=r} log_alpha_i inside
+// the chunk,
+//
+//   A_rs = beta_r exp(g_r - g_s) (k_r . k_s)   for s < r, else 0
+//   T_u  = (I + A)^{-1} diag(beta),   T_w = (I + A)^{-1} diag(beta gamma)
+//
+// ("Gated DeltaNet GPU并行实现", section 3.2: everything inside a chunk is
+// parallel; the serial state pass needs only the chunk's WY factors
+// U = T_u V and W = T_w K, which the fused kernel forms on its own tensor
+// cores.)  Both are written as bf16 in a per-chunk layout
+// [H][chunk_slots][T_u | T_w][64][64] (dense: slot n * max_chunks + c; packed:
+// floor(cu[n] / 64) + n + c), so each is one bulk-copy box for the fused
+// kernel.  Rows and columns of tokens past a sequence's end are zero, because
+// beta and log_alpha are zero there.
+//
+// Per unit (chunk, head): the K tile arrives by bulk tensor copy (128-byte
+// swizzle), one thread issues the Gram K K^T as tcgen05 MMAs into tensor
+// memory (M = 128: rows 64-127 of the operand are whatever follows the tile and
+// are never read), four warps read its rows, form A and invert I + A
+// (gdn_inv.cuh).  Persistent: each CTA walks units b, b + grid, ... with two K
+// buffers and two Gram accumulators in flight.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "gdn_internal.h"
+#include "gdn_inv.cuh"
+#include "tc_common.cuh"
+#include "tc_ptx.cuh"
+
+// Optional per-CTA timing for profiling builds (-DGDN_TRACE_TIMELINE):
+// start and end clock64(), SM and units of every CTA, read back with
+// gdn_ut_trace_read().  Compiled out otherwise.
+#ifdef GDN_TRACE_TIMELINE
+__device__ long long g_ut_cta[2048][4];
+__device__ long long g_ut_phase[16][8];   // CTA 0: per local unit, phase stamps
+extern "C" int gdn_ut_trace_read(long long *out) {
+    return (int)cudaMemcpyFromSymbol(out, g_ut_cta, sizeof(g_ut_cta));
+}
+extern "C" int gdn_ut_phase_read(long long *out) {
+    return (int)cudaMemcpyFromSymbol(out, g_ut_phase, sizeof(g_ut_phase));
+}
+#define UTRACE(i, ev)                                                       \
+    do {                                                                    \
+        if (blockIdx.x == 0 && tid == 0 && (i) < 16) g_ut_phase[i][ev] = clock64(); \
+    } while (0)
+#else
+#define UTRACE(i, ev) \
+    do {              \
+    } while (0)
+extern "C" int gdn_ut_debug_ctas();
+#endif
+
+namespace gdn {
+namespace {
+
+using namespace ptx;
+using namespace tcx;
+using inv::LDA;
+
+constexpr int kU = 64;
+constexpr int kThreadsU = 160;   // warps 0-3 compute, warp 4 copies and issues the Gram
+
+enum {
+    U_FULL = 0,        // + buffer: K tile landed, raw gates staged (TMA tx + 32 lanes)
+    U_EMPTY = 2,       // + buffer: Gram read the tile (commit) and the gates were copied
+    U_GDONE = 4,       // + buffer: Gram in tensor memory (commit)
+    U_GFREE = 6,       // + buffer: A formed from it
+    U_DRAIN = 8,
+    U_COUNT
+};
+
+template <int DK>
+struct ULay {
+    static constexpr int KB = DK / 64;
+    static constexpr int SZ_K = KB * 8192;
+    static constexpr int OFF_K = 0;                       // + b * SZ_K
+    // the Gram's 128-row operand of the last tile's last block reads the 8 KB
+    // after the tiles (A's buffer) as its unused rows
+    static constexpr int OFF_A = 2 * SZ_K;                // fp32 [64][LDA]
+    static constexpr int OFF_T = OFF_A + kU * LDA * 4;    // fp32 [64][LDA]
+    static constexpr int OFF_RG = OFF_T + kU * LDA * 4;   // + b * 512: raw log_alpha[64], beta[64]
+    static constexpr int OFF_GS = OFF_RG + 2 * 512;       // g, beta, gamma, 1/gamma [64]
+    static constexpr int OFF_BAR = OFF_GS + 1024;
+    static constexpr int OFF_MISC = OFF_BAR + U_COUNT * 8;
+    static constexpr int TOTAL = OFF_MISC + 16;
+    static constexpr int ALLOC = TOTAL + 1024;
+    static_assert(kU * LDA * 4 >= 8192, "the last tile's unused operand rows stay in bounds");
+    static_assert(OFF_A % 1024 == 0 && OFF_RG % 16 == 0, "align");
+};
+
+struct UtParams {
+    SeqMap sm;
+    const float *log_alpha, *beta;
+    const int2 *table;        // packed batches: (sequence, chunk) of every chunk slot
+    __nv_bfloat16 *Tu;        // [H][chunk_slots][2][64][64]: T_u, T_w
+    int *err;
+    int max_chunks;
+    int chunk_slots;
+    long long units;          // H * chunk_slots
+    uint32_t wait_limit;
+};
+
+// Where unit u lives: its output block, the copy coordinates of its first
+// token row, its first row in the [rows] gate arrays and its token count
+// (0: a slot with no chunk; its output block is never read).
+struct Unit {
+    long long out_row;   // first row of the unit's [2][64][64] block
+    long long row0;
+    int y, z, len;
+};
+
+__device__ __forceinline__ Unit decode(const UtParams &p, long long u) {
+    Unit r{0, 0, 0, 0, 0};
+    const int slot = (int)(u % p.chunk_slots), h = (int)(u / p.chunk_slots);
+    int n, c;
+    if (p.table) {
+        const int2 e = p.table[slot];
+        n = e.x;
+        c = e.y;
+        if (n < 0) return r;
+    } else {
+        n = slot / p.max_chunks;
+        c = slot % p.max_chunks;
+    }
+    if (p.sm.cu) {
+        const int a = __ldg(p.sm.cu + n), b = __ldg(p.sm.cu + n + 1);
+        if (!(a >= 0 && a <= b && b <= p.sm.T_total)) return r;   // reported by the table kernel
+        const int t0 = c * kU;
+        if (t0 >= b - a) return r;
+        r.len = min(kU, b - a - t0);
+        // storage slot of (n, c): floor(cu[n] / 64) + n + c, unique per sequence chunk
+        r.out_row = ((long long)h * p.chunk_slots + a / kU + n + c) * 2 * kU;
+        r.row0 = (long long)h * p.sm.T_total + a + t0;
+        r.y = a + t0;
+        r.z = h;
+    } else {
+        const int t0 = c * kU;
+        if (t0 >= p.sm.T) return r;
+        r.len = min(kU, p.sm.T - t0);
+        r.out_row = u * 2 * kU;
+        r.row0 = ((long long)n * p.sm.H + h) * (long long)p.sm.T + t0;
+        r.y = t0;
+        r.z = n * p.sm.H + h;
+    }
+    return r;
+}
+
+template <int DK>
+__global__ void __launch_bounds__(kThreadsU, 3)
+k_gdn_ut(const __grid_constant__ CUtensorMap tm_k, UtParams p) {
+    using L = ULay<DK>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + L::OFF_BAR);
+    uint32_t *misc = reinterpret_cast<uint32_t *>(sm + L::OFF_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(misc + 1);
+    float *Ab = reinterpret_cast<float *>(sm + L::OFF_A);
+    float *Tb = reinterpret_cast<float *>(sm + L::OFF_T);
+    float *gs = reinterpret_cast<float *>(sm + L::OFF_GS);
+
+    // the fused kernel that follows may start its own prologue now (it waits
+    // for this grid before it reads T_u)
+    griddep_launch_dependents();
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+#ifdef GDN_TRACE_TIMELINE
+    if (tid == 0 && blockIdx.x < 2048) {
+        uint32_t smid;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+        g_ut_cta[blockIdx.x][0] = clock64();
+        g_ut_cta[blockIdx.x][2] = smid;
+    }
+#endif
+    const long long nunits =
+        blockIdx.x < p.units ? (p.units - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+
+    if (warp == 4) {
+        tmem_alloc(misc, 128);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        for (int i = 0; i < U_COUNT; ++i) mbar_init(bar + i, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar + U_FULL + b, 33);
+            mbar_init(bar + U_EMPTY + b, 2);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = misc[0];
+    const Ctl ctl{bar, abort_flag, p.err, p.wait_limit};
+
+    if (warp == 4) {
+        // ================================ copies (all lanes) and Gram (lane 0)
+        if (lane == 0) prefetch_tmap(&tm_k);
+        constexpr uint32_t idG = make_idesc_bf16(128, 64, false, false);
+        const uint32_t sb = smem_u32(sm);
+        auto load = [&](long long i) -> bool {
+            const int b = (int)(i & 1);
+            const bool ok = i < 2 || ctl.wait(U_EMPTY + b, (uint32_t)(((i >> 1) - 1) & 1));
+            if (!__all_sync(0xffffffffu, ok)) return false;
+            const Unit un = decode(p, blockIdx.x + i * gridDim.x);
+            if (lane == 0) {
+                mbar_arrive_expect_tx(bar + U_FULL + b, (uint32_t)L::SZ_K);
+#pragma unroll
+                for (int kb = 0; kb < L::KB; ++kb)
+                    tma_load_3d(sm + L::OFF_K + b * L::SZ_K + kb * 8192, &tm_k, bar + U_FULL + b,
+                                kb * 64, un.y, un.z);
+            }
+            float *rg = reinterpret_cast<float *>(sm + L::OFF_RG + b * 512);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int r = lane + 32 * h;
+                const bool in = r < un.len;
+                rg[r] = in ? __ldg(p.log_alpha + un.row0 + r) : 0.f;
+                rg[64 + r] = in ? __ldg(p.beta + un.row0 + r) : 0.f;
+            }
+            mbar_arrive(bar + U_FULL + b);
+            return true;
+        };
+        auto gram = [&](long long i) -> bool {
+            const int b = (int)(i & 1);
+            bool ok = ctl.wait(U_FULL + b, (uint32_t)((i >> 1) & 1));
+            if (ok && i >= 2) ok = ctl.wait(U_GFREE + b, (uint32_t)(((i >> 1) - 1) & 1));
+            if (!ok) return false;
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < DK / 16; ++kk) {
+                const uint32_t off = L::OFF_K + b * L::SZ_K + (kk >> 2) * 8192 + (kk & 3) * 32;
+                const uint64_t d = make_sdesc(sb + off, 16, 1024, kSwizzle128B);
+                mma_bf16(tmem + 64 * b, d, d, idG, kk > 0);
+            }
+            mma_commit(bar + U_GDONE + b);
+            mma_commit(bar + U_EMPTY + b);
+            return true;
+        };
+        long long loaded = 0;
+        bool ok = true;
+        for (long long i = 0; ok && i < nunits && i < 2; ++i) ok = load(i), loaded = i + 1;
+        for (long long i = 0; ok && i < nunits; ++i) {
+            int okg = 1;
+            if (lane == 0) okg = gram(i);
+            ok = __shfl_sync(0xffffffffu, okg, 0) != 0;
+            if (ok && i + 2 < nunits) ok = load(i + 2), loaded = i + 3;
+        }
+        if (lane == 0) {
+            // every issued MMA and copy has finished before the CTA leaves
+            mma_commit(bar + U_DRAIN);
+            mbar_wait(bar + U_DRAIN, 0, ctl.limit);
+            if (*abort_flag)
+                for (long long i = loaded > 2 ? loaded - 2 : 0; i < loaded; ++i)
+                    mbar_wait(bar + U_FULL + (i & 1), (uint32_t)((i >> 1) & 1), ctl.limit);
+        }
+    } else {
+        // ============================================= compute (warps 0-3)
+        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        auto bar128 = [] { named_bar(1, 128); };
+        for (long long i = 0; i < nunits; ++i) {
+            const int b = (int)(i & 1);
+            const Unit un = decode(p, blockIdx.x + i * gridDim.x);
+            // ---- gates: g = in-chunk cumsum of log_alpha, beta (zero past the end)
+            if (!named_bar_and(1, 128, ctl.wait(U_FULL + b, (uint32_t)((i >> 1) & 1)))) break;
+            UTRACE(i, 0);
+            if (warp == 0) {
+                const float *rg = reinterpret_cast<const float *>(sm + L::OFF_RG + b * 512);
+                float x0 = rg[lane], x1 = rg[32 + lane];
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const float y0 = __shfl_up_sync(0xffffffffu, x0, off);
+                    const float y1 = __shfl_up_sync(0xffffffffu, x1, off);
+                    if (lane >= off) {
+                        x0 += y0;
+                        x1 += y1;
+                    }
+                }
+                x1 += __shfl_sync(0xffffffffu, x0, 31);
+                gs[lane] = x0;
+                gs[32 + lane] = x1;
+                gs[64 + lane] = rg[64 + lane];
+                gs[96 + lane] = rg[96 + lane];
+                gs[128 + lane] = __expf(x0);
+                gs[160 + lane] = __expf(x1);
+                // used only when the chunk's decay span is moderate (g_C > -80)
+                gs[192 + lane] = __expf(-x0);
+                gs[224 + lane] = __expf(-x1);
+            }
+            // ---- A from the Gram rows (lanes 0-63): warps 0-1; warps 2-3 clear
+            //      T's upper diagonal blocks.  Every thread finished reading the
+            //      previous unit's T before this barrier.
+            const bool okg = ctl.wait(U_GDONE + b, (uint32_t)((i >> 1) & 1));
+            if (!named_bar_and(1, 128, okg)) break;
+            UTRACE(i, 1);
+            if (tid == 0) mbar_arrive(bar + U_EMPTY + b);   // gates copied
+            __syncwarp();
+            tc_fence_after();
+            if (warp < 2) {
+                const int r = tid;
+                uint32_t g0[32], g1[32];
+                tmem_ld32(tmem + lane_base + 64 * b, g0);
+                tmem_ld32(tmem + lane_base + 64 * b + 32, g1);
+                const float gr = gs[r], br = gs[64 + r];
+                tmem_wait32(g0);
+                tmem_wait32(g1);
+                // A_rs = beta_r exp(g_r - g_s) G_rs for s < r: as
+                // (beta_r gamma_r) exp(-g_s) G_rs when the chunk's decay span
+                // is moderate, else one exponential per entry (never above 1).
+                // Entries outside the 16x16 diagonal blocks are rounded to tf32
+                // for the merges.
+                const bool span_ok = gs[63] > -80.f;
+                const float bgr = br * gs[128 + r];
+#pragma unroll
+                for (int q = 0; q < 16; ++q) {
+                    float v[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int s = 4 * q + e;
+                        const float gv = f32(s < 32 ? g0[s] : g1[s - 32]);
+                        const float f = span_ok ? bgr * gs[192 + s] : br * __expf(gr - gs[s]);
+                        const float x = s < r ? f * gv : 0.f;
+                        const float xt = inv::tf32(x);
+                        v[e] = (r >> 4) != (s >> 4) ? xt : x;
+                    }
+                    *reinterpret_cast<float4 *>(Ab + r * LDA + 4 * q) =
+                        make_float4(v[0], v[1], v[2], v[3]);
+                }
+            } else {
+                inv::clear_upper16(Tb, tid - 64, 64);
+            }
+            tc_fence_before();
+            bar128();
+            if (tid == 0) mbar_arrive(bar + U_GFREE + b);
+            __syncwarp();
+            UTRACE(i, 2);
+            // ---- T = (I + A)^{-1}
+            inv::invert64(Ab, Tb, tid, bar128);
+            UTRACE(i, 3);
+            // ---- T_u = T diag(beta) and T_w = T diag(beta gamma), bf16 rows:
+            //      thread t takes row t/2, columns 32 (t & 1) .. + 31 of both
+            if (un.len > 0) {
+                const int r = tid >> 1, c0 = 32 * (tid & 1);
+                uint4 *du = reinterpret_cast<uint4 *>(p.Tu + (un.out_row + r) * kU + c0);
+                uint4 *dw = reinterpret_cast<uint4 *>(p.Tu + (un.out_row + kU + r) * kU + c0);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    uint32_t wu[4], ww[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int s = c0 + 8 * q + 2 * e;
+                        const float t0 = inv::t_at(Tb, r, s) * gs[64 + s];
+                        const float t1 = inv::t_at(Tb, r, s + 1) * gs[64 + s + 1];
+                        wu[e] = pack_bf16(t0, t1);
+                        ww[e] = pack_bf16(t0 * gs[128 + s], t1 * gs[128 + s + 1]);
+                    }
+                    du[q] = make_uint4(wu[0], wu[1], wu[2], wu[3]);
+                    dw[q] = make_uint4(ww[0], ww[1], ww[2], ww[3]);
+                }
+            }
+            UTRACE(i, 4);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 4) tmem_dealloc(tmem, 128);
+#ifdef GDN_TRACE_TIMELINE
+    if (tid == 0 && blockIdx.x < 2048) {
+        g_ut_cta[blockIdx.x][1] = clock64();
+        g_ut_cta[blockIdx.x][3] = nunits;
+    }
+#endif
+}
+
+#ifdef GDN_TRACE_TIMELINE
+int g_ut_ctas_seen = 0;
+#endif
+
+template <int DK>
+gdn_status launch_ut(const FwdArgs &a, const int2 *table, __nv_bfloat16 *Tu) {
+    using L = ULay<DK>;
+    static int ctas[64] = {};   // CTAs the device holds at once, per device (benign race:
+                                // every thread computes the same value)
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return GDN_ERR_CUDA;
+    if (cudaFuncSetAttribute(k_gdn_ut<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             L::ALLOC) != cudaSuccess ||
+        cudaFuncSetAttribute(k_gdn_ut<DK>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             100) != cudaSuccess)
+        return GDN_ERR_CUDA;
+    if (ctas[dev] == 0) {
+        // CTAs per SM: what shared memory holds (1 KB reserved per CTA), at most
+        // three (the launch bounds' register budget; 128 of the 512 tensor-memory
+        // columns each)
+        int smem_sm = 0, nsm = 0;
+        if (cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) !=
+                cudaSuccess ||
+            cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return GDN_ERR_CUDA;
+        const int fit = smem_sm / (L::ALLOC + 1024);
+        ctas[dev] = max(1, min(fit, 3)) * max(1, nsm);
+    }
+#ifdef GDN_TRACE_TIMELINE
+    g_ut_ctas_seen = ctas[dev];
+#endif
+    const long long units = (long long)a.chunk_slots * a.sm.H;
+    if (units <= 0) return GDN_OK;
+    const long long ydim = a.sm.cu ? a.sm.T_total : a.sm.T;
+    const long long zdim = a.sm.cu ? a.sm.H : (long long)a.sm.N * a.sm.H;
+    CUtensorMap mk;
+    if (!make_map(&mk, a.k, DK, ydim, zdim)) return GDN_ERR_CUDA;
+    UtParams p;
+    p.sm = a.sm;
+    p.log_alpha = a.log_alpha;
+    p.beta = a.beta;
+    p.table = table;
+    p.Tu = Tu;
+    p.err = device_error_word();
+    p.max_chunks = a.max_chunks;
+    p.chunk_slots = a.chunk_slots;
+    p.units = units;
+    const long long lim = option(GDN_OPT_WAIT_LIMIT);
+    p.wait_limit = lim > 0 ? (uint32_t)(lim > 0x7fffffffLL ? 0x7fffffffLL : lim) : (1u << 22);
+    const int grid = (int)(units < ctas[dev] ? units : (long long)ctas[dev]);
+    k_gdn_ut<DK><<<grid, kThreadsU, L::ALLOC, a.stream>>>(mk, p);
+    count_launch();
+    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+}  // namespace
+
+#ifdef GDN_TRACE_TIMELINE
+extern "C" int gdn_ut_debug_ctas() { return g_ut_ctas_seen; }
+#endif
+
+gdn_status enqueue_ut(const FwdArgs &a, const int2 *table, __nv_bfloat16 *Tu) {
+    if (a.no_erase || a.vector_gate || a.dt != GDN_BF16) return GDN_ERR_UNSUPPORTED;
+    if (a.dk == 128) return launch_ut<128>(a, table, Tu);
+    if (a.dk == 64) return launch_ut<64>(a, table, Tu);
+    return GDN_ERR_UNSUPPORTED;
+}
+
+}  // namespace gdn

@@ -139,7 +139,14 @@ gdn_status gdn_sync_check(void *stream);
  *                      products, three per step for fp32 I/O so they keep
  *                      fp32 accuracy), GDN_IMPL_TC (tcgen05
  *                      tensor-core kernels; GDN_ERR_UNSUPPORTED when the call
- *                      does not fit them).
+ *                      does not fit them), GDN_IMPL_TC_FUSED (the
+ *                      alternative tcgen05 forward: a warp-specialised
+ *                      chunk-prep kernel, then one kernel per (sequence, head,
+ *                      64-wide d_v tile) that runs the whole chunk recurrence
+ *                      with H in registers and every product on tcgen05;
+ *                      bf16 I/O, scalar gates with erase, d_k 64 or 128,
+ *                      d_v a multiple of 64 up to 256, else
+ *                      GDN_ERR_UNSUPPORTED).  AUTO never picks it.
  *   GDN_OPT_SEGMENTS:  0 = automatic; s > 0 forces s sequence segments per
  *                      (sequence, head) in the tensor-core path's segment scan;
  *                      1 disables the scan.
@@ -151,7 +158,7 @@ gdn_status gdn_sync_check(void *stream);
  * Returns GDN_ERR_INVALID_ARG for an unknown key or value.
  */
 enum { GDN_OPT_IMPL = 0, GDN_OPT_SEGMENTS = 1, GDN_OPT_WAIT_LIMIT = 2, GDN_OPT_POISON_SCRATCH = 3 };
-enum { GDN_IMPL_AUTO = 0, GDN_IMPL_SIMT = 1, GDN_IMPL_TC = 2 };
+enum { GDN_IMPL_AUTO = 0, GDN_IMPL_SIMT = 1, GDN_IMPL_TC = 2, GDN_IMPL_TC_FUSED = 3 };
 gdn_status gdn_set_option(int key, long long value);
 long long gdn_get_option(int key);
 
@@ -170,9 +177,10 @@ gdn_status gdn_kernel_timer_read(double *total_ms, long long *launches, const ch
 uint64_t gdn_kernel_launches(void);
 
 /* Implementation the last successful gdn_fwd / gdn_fwd_varlen / gdn_bwd /
- * gdn_bwd_varlen call used (GDN_IMPL_SIMT or GDN_IMPL_TC; for the backward,
- * GDN_IMPL_TC when its state adjoint ran on tcgen05), 0 before the first
- * call. */
+ * gdn_bwd_varlen call used (GDN_IMPL_SIMT, GDN_IMPL_TC or GDN_IMPL_TC_FUSED;
+ * for the backward, GDN_IMPL_TC when its state adjoint ran on tcgen05, where
+ * GDN_IMPL_TC_FUSED selects the same backward as GDN_IMPL_TC), 0 before the
+ * first call. */
 int gdn_last_impl(void);
 
 /*

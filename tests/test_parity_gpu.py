@@ -15,7 +15,8 @@ from tests import gpu_util as U
 
 pytestmark = pytest.mark.gpu
 
-IMPLS = {"simt": gdn.GDN_IMPL_SIMT, "tc": gdn.GDN_IMPL_TC, "auto": gdn.GDN_IMPL_AUTO}
+IMPLS = {"simt": gdn.GDN_IMPL_SIMT, "tc": gdn.GDN_IMPL_TC, "fused": gdn.GDN_IMPL_TC_FUSED,
+         "auto": gdn.GDN_IMPL_AUTO}
 
 
 def run_dense(x, impl, **kw):
@@ -23,7 +24,7 @@ def run_dense(x, impl, **kw):
         try:
             o, hT = gdn.gdn_fwd(x.q, x.k, x.v, x.log_alpha, x.beta, x.h0, check=True, **kw)
         except gdn.GdnError as e:
-            if e.status == gdn.GDN_ERR_UNSUPPORTED and impl == "tc":
+            if e.status == gdn.GDN_ERR_UNSUPPORTED and impl in ("tc", "fused"):
                 pytest.skip("shape not covered by the tensor-core path")
             raise
         used = gdn.last_impl()
@@ -39,7 +40,7 @@ def run_varlen(y, impl, **kw):
             o, hT = gdn.gdn_fwd_varlen(y.q, y.k, y.v, y.log_alpha, y.beta, y.cu_seqlens, y.h0,
                                        check=True, **kw)
         except gdn.GdnError as e:
-            if e.status == gdn.GDN_ERR_UNSUPPORTED and impl == "tc":
+            if e.status == gdn.GDN_ERR_UNSUPPORTED and impl in ("tc", "fused"):
                 pytest.skip("shape not covered by the tensor-core path")
             raise
     U.sync()
@@ -70,7 +71,7 @@ DENSE_CASES = [
 ]
 
 
-@pytest.mark.parametrize("impl", ["simt", "tc"])
+@pytest.mark.parametrize("impl", ["simt", "tc", "fused"])
 @pytest.mark.parametrize("case", DENSE_CASES, ids=lambda c: "b%dh%dt%d_k%dv%d_%s_%s" % (
     c[0], c[1], c[2], c[3], c[4], c[5], c[7]))
 def test_dense_small(impl, case):
@@ -90,7 +91,7 @@ VARLEN_CASES = [
 ]
 
 
-@pytest.mark.parametrize("impl", ["simt", "tc"])
+@pytest.mark.parametrize("impl", ["simt", "tc", "fused"])
 @pytest.mark.parametrize("case", VARLEN_CASES, ids=lambda c: "n%d_k%dv%d_%s" % (
     len(c[0]), c[2], c[3], c[4]))
 def test_varlen_small(impl, case):
@@ -105,7 +106,7 @@ def test_varlen_small(impl, case):
     check(o, hT, o_ref, h_ref, io)
 
 
-@pytest.mark.parametrize("impl", ["simt", "tc"])
+@pytest.mark.parametrize("impl", ["simt", "tc", "fused"])
 def test_varlen_equals_dense(impl):
     # equal lengths: the packed call must reproduce the dense call bit for bit
     # up to the different memory layout
@@ -121,7 +122,7 @@ def test_varlen_equals_dense(impl):
     assert torch.equal(ov, pack(od)) and torch.equal(hv, hd)
 
 
-@pytest.mark.parametrize("impl", ["simt", "tc"])
+@pytest.mark.parametrize("impl", ["simt", "tc", "fused"])
 def test_continuation(impl):
     B, H, T1, T2, dk, dv = 1, 4, 192, 137, 128, 128
     x = synth.make_dense(B, H, T1 + T2, dk, dv, io="bf16", h0_std=0.02, seed=9, device="cuda")
@@ -143,7 +144,7 @@ def test_empty_sequence_gives_h0(impl):
     assert o.numel() == 0 and torch.equal(hT, x.h0)
 
 
-@pytest.mark.parametrize("impl", ["simt", "tc"])
+@pytest.mark.parametrize("impl", ["simt", "tc", "fused"])
 def test_scratch_pool_release_and_reuse(impl):
     # scratch comes from the library's own pool: results do not depend on
     # whether the pool was just emptied or still holds the previous call's
@@ -192,7 +193,7 @@ def test_workload_fp32_small_full():
     check(o, hT, o_ref.reshape(o.shape), h_ref.reshape(hT.shape), "f32")
 
 
-@pytest.mark.parametrize("impl", ["auto", "simt"])
+@pytest.mark.parametrize("impl", ["auto", "fused", "simt"])
 def test_workload_b4_h16_t4096_d128_full(impl):
     x = synth.make_workload("gdn_fwd_b4_h16_t4096_d128_bf16", device="cuda")
     o, hT = run_dense(x, impl)
@@ -280,7 +281,7 @@ def test_bad_cu_seqlens_reported(impl):
         try:
             gdn.gdn_fwd_varlen(y.q, y.k, y.v, y.log_alpha, y.beta, bad, None)
         except gdn.GdnError as e:
-            if e.status == gdn.GDN_ERR_UNSUPPORTED and impl == "tc":
+            if e.status == gdn.GDN_ERR_UNSUPPORTED and impl in ("tc", "fused"):
                 pytest.skip("shape not covered by the tensor-core path")
             raise
     lib = gdn.load()
@@ -303,7 +304,7 @@ def test_no_erase_matches_oracle(impl, B, H, T, dk, dv, io):
         try:
             o, hT = gdn.gdn_fwd(x.q, x.k, x.v, x.log_alpha, x.beta, x.h0, check=True, erase=False)
         except gdn.GdnError as e:
-            if e.status == gdn.GDN_ERR_UNSUPPORTED and impl == "tc":
+            if e.status == gdn.GDN_ERR_UNSUPPORTED and impl in ("tc", "fused"):
                 pytest.skip("shape not covered by the tensor-core path")
             raise
     U.sync()
