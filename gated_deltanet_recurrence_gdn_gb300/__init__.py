@@ -68,6 +68,7 @@ ABI = [
                                    ctypes.POINTER(ctypes.c_longlong),
                                    ctypes.POINTER(ctypes.c_char_p)]),
     ("gdn_kernel_launches", ctypes.c_uint64, []),
+    ("gdn_scratch_stats", _i, [ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(ctypes.c_uint64), _i]),
     ("gdn_last_impl", _i, []),
     ("gdn_release_scratch", _i, []),
     ("gdn_selftest_wait", _i, [_i, ctypes.c_longlong, ctypes.POINTER(_i), _vp]),
@@ -380,6 +381,16 @@ def get_option(key: int) -> int:
 
 def kernel_launches() -> int:
     return int(load().gdn_kernel_launches())
+
+
+def scratch_stats(reset_high: bool = False):
+    """(bytes in use, high-water mark) of the current device's scratch pool;
+    reset_high restarts the high-water mark from the current use afterwards."""
+    cur = ctypes.c_uint64(0)
+    high = ctypes.c_uint64(0)
+    _check(load().gdn_scratch_stats(ctypes.byref(cur), ctypes.byref(high), 1 if reset_high else 0),
+           "gdn_scratch_stats")
+    return int(cur.value), int(high.value)
 
 
 def kernel_timer(enable: bool):

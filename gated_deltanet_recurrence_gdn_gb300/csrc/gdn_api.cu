@@ -415,6 +415,23 @@ gdn_status gdn_kernel_timer_read(double *total_ms, long long *launches, const ch
 
 uint64_t gdn_kernel_launches(void) { return g_launches.load(); }
 
+gdn_status gdn_scratch_stats(uint64_t *used_current, uint64_t *used_high, int reset_high) {
+    cudaMemPool_t pool;
+    if (scratch_pool(&pool) != cudaSuccess) return GDN_ERR_CUDA;
+    uint64_t cur = 0, high = 0;
+    if (cudaMemPoolGetAttribute(pool, cudaMemPoolAttrUsedMemCurrent, &cur) != cudaSuccess ||
+        cudaMemPoolGetAttribute(pool, cudaMemPoolAttrUsedMemHigh, &high) != cudaSuccess)
+        return GDN_ERR_CUDA;
+    if (used_current) *used_current = cur;
+    if (used_high) *used_high = high;
+    if (reset_high) {
+        uint64_t zero = 0;   // restarts the high-water mark at the current use
+        if (cudaMemPoolSetAttribute(pool, cudaMemPoolAttrUsedMemHigh, &zero) != cudaSuccess)
+            return GDN_ERR_CUDA;
+    }
+    return GDN_OK;
+}
+
 int gdn_last_impl(void) { return g_last_impl.load(); }
 
 gdn_status gdn_release_scratch(void) {

@@ -640,13 +640,10 @@ gdn_status launch_bwd_tc(const FwdArgs &a, const BwdArgs &b, const __nv_bfloat16
         !make_map_f32(&mdh, dHc, a.dv, (long long)a.sm.H * a.chunk_slots * DK, DK) ||
         !make_map_f32_3d(&mdv, dVn, a.dv, ydim, zdim))
         return GDN_ERR_CUDA;
-    static bool attr_set = false;
-    if (!attr_set) {
-        if (cudaFuncSetAttribute(k_bwd_dstate_tc<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 L::ALLOC) != cudaSuccess)
-            return GDN_ERR_CUDA;
-        attr_set = true;
-    }
+    // a per-function attribute of the current device: cheap, set on every launch
+    if (cudaFuncSetAttribute(k_bwd_dstate_tc<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             L::ALLOC) != cudaSuccess)
+        return GDN_ERR_CUDA;
     BwdTcParams p;
     p.sm = a.sm;
     p.G = G;
@@ -673,9 +670,10 @@ bool tc_bwd_supported(const FwdArgs &a) {
     if (a.dk != 64 && a.dk != 128) return false;
     if (a.dv % kNV != 0) return false;
     if (a.sm.N > 65535 || a.sm.H > 65535 || a.rows <= 0) return false;
-    static int ok = -1;
-    if (ok < 0) ok = (device_is_sm10x() && encode_fn() != nullptr) ? 1 : 0;
-    return ok == 1;
+    static std::atomic<int> memo[kMaxDeviceMemo];
+    return per_device(
+               memo, [](int) { return (device_is_sm10x() && encode_fn() != nullptr) ? 1 : 0; },
+               0) == 1;
 }
 
 gdn_status tc_bwd_dstate(const FwdArgs &a, const BwdArgs &b, const __nv_bfloat16 *Wb,

@@ -165,13 +165,18 @@ extern "C" gdn_status gdn_fwd_host(const void *q, const void *k, const void *v,
     if (rc == GDN_OK && hT)
         chk(cudaMemcpyAsync(hT, state + (size_t)(S & 1) * (nst / 4), nst, cudaMemcpyDeviceToHost,
                             hs.out));
-    // the caller's stream resumes after everything; the buffers go back to the
-    // pool in its order
+    // the caller's stream resumes after all three internal streams (after an
+    // error, copies or kernels already queued on any of them may still use the
+    // buffers); the buffers then go back to the pool in its order, and the
+    // internal streams' next work comes after it
     if (ok) {
-        cudaEventRecord(ev_end, hs.out);
-        cudaStreamWaitEvent(hs.in, ev_end, 0);
-        cudaStreamWaitEvent(hs.comp, ev_end, 0);
-        cudaStreamWaitEvent(ust, ev_end, 0);
+        const cudaStream_t internal[3] = {hs.in, hs.comp, hs.out};
+        for (cudaStream_t s2 : internal) {
+            cudaEventRecord(ev_end, s2);
+            cudaStreamWaitEvent(ust, ev_end, 0);
+        }
+        cudaEventRecord(ev_end, ust);
+        for (cudaStream_t s2 : internal) cudaStreamWaitEvent(s2, ev_end, 0);
     }
     scratch_free(sets, ust);
     scratch_free(state, ust);

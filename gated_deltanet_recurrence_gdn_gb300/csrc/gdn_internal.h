@@ -1,6 +1,8 @@
 // gdn_internal.h -- shared host/device declarations of libgdn (not installed).
 #pragma once
 
+#include <atomic>
+
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -38,6 +40,24 @@ struct SeqMap {
         }
     }
 };
+
+// Per-device memo of a small non-negative host-side value: compute(dev) runs
+// until it succeeds once per device (two threads racing on a first use both
+// compute the same value).  A negative result is a failure: it is returned as
+// `fallback` and not remembered.  `fallback` also covers a current device
+// that is unknown or past the table.
+constexpr int kMaxDeviceMemo = 64;
+template <typename F>
+inline int per_device(std::atomic<int> (&memo)[kMaxDeviceMemo], F compute, int fallback) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDeviceMemo) return fallback;
+    const int v = memo[dev].load(std::memory_order_acquire);   // value + 1; 0 = not yet known
+    if (v > 0) return v - 1;
+    const int c = compute(dev);
+    if (c < 0) return fallback;
+    memo[dev].store(c + 1, std::memory_order_release);
+    return c;
+}
 
 struct FwdArgs {
     const void *q, *k, *v;

@@ -421,24 +421,27 @@ namespace {
 template <int DK>
 gdn_status launch_prep(const FwdArgs &a, const int2 *table, __nv_bfloat16 *Tu,
                        __nv_bfloat16 *W, float *T_out, float *G_out) {
-    static int blocks_per_sm[64] = {};   // per device, filled on first use
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return GDN_ERR_CUDA;
     const int smem = PrepLay<DK>::TOTAL;
     if (cudaFuncSetAttribute(k_gdn_prep<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
         cudaSuccess)
         return GDN_ERR_CUDA;
-    if (blocks_per_sm[dev] == 0) {
-        int nb = 0, nsm = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, k_gdn_prep<DK>, 128, smem) !=
-                cudaSuccess ||
-            cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-            return GDN_ERR_CUDA;
-        blocks_per_sm[dev] = max(1, nb) * max(1, nsm);
-    }
+    // resident CTAs of the whole device, per device
+    static std::atomic<int> memo[kMaxDeviceMemo];
+    const int resident = per_device(
+        memo,
+        [smem](int dev) {
+            int nb = 0, nsm = 0;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, k_gdn_prep<DK>, 128, smem) !=
+                    cudaSuccess ||
+                cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+                return -1;
+            return max(1, nb) * max(1, nsm);
+        },
+        0);
+    if (resident <= 0) return GDN_ERR_CUDA;
     const long long units = (long long)a.chunk_slots * a.sm.H;
     if (units > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
-    const int grid = (int)(units < blocks_per_sm[dev] ? units : (long long)blocks_per_sm[dev]);
+    const int grid = (int)(units < resident ? units : (long long)resident);
     k_gdn_prep<DK><<<grid, 128, smem, a.stream>>>(
         static_cast<const __nv_bfloat16 *>(a.k), a.log_alpha, a.beta, a.sm, table, a.max_chunks,
         a.chunk_slots, (int)units, Tu, W, T_out, G_out, device_error_word());

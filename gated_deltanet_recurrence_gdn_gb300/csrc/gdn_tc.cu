@@ -48,7 +48,8 @@
 
 // Optional per-phase timeline of CTA (0,0,0) for profiling builds
 // (-DGDN_TRACE_TIMELINE): clock64() stamps by role, chunk and event, read back
-// with gdn_trace_read().  Compiled out otherwise.
+// with gdn_trace_read(), and every CTA's start and end, read back with
+// gdn_cta_trace_read().  Compiled out otherwise.
 #ifdef GDN_TRACE_TIMELINE
 __device__ long long g_gdn_trace[4][128][16];
 extern "C" int gdn_trace_read(long long *out) {
@@ -59,9 +60,36 @@ extern "C" int gdn_trace_read(long long *out) {
         if ((cond) && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && (jj) < 128) \
             g_gdn_trace[role][jj][ev] = clock64();                                         \
     } while (0)
+// per CTA (linear index < 4096): global-timer start and end (ns), SM id
+__device__ long long g_gdn_cta[4096][3];
+extern "C" int gdn_cta_trace_read(long long *out) {
+    return (int)cudaMemcpyFromSymbol(out, g_gdn_cta, sizeof(g_gdn_cta));
+}
+__device__ __forceinline__ long long gtimer() {
+    long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ int smid() {
+    int r;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(r));
+    return r;
+}
+#define CTA_SPAN(slot)                                                                     \
+    do {                                                                                   \
+        const long long lin_ = ((long long)blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + \
+                               blockIdx.x;                                                 \
+        if (threadIdx.x == 0 && lin_ < 4096) {                                             \
+            g_gdn_cta[lin_][slot] = gtimer();                                              \
+            g_gdn_cta[lin_][2] = smid();                                                   \
+        }                                                                                  \
+    } while (0)
 #else
 #define TRACE(role, jj, ev, cond) \
     do {                          \
+    } while (0)
+#define CTA_SPAN(slot) \
+    do {               \
     } while (0)
 #endif
 
@@ -239,6 +267,7 @@ __device__ __forceinline__ void gdn_tc_body(const CUtensorMap *tm_q, const CUten
     // data written by the previous kernel in the stream (T_u / W, segment
     // initial states) is read only from here on
     griddep_wait();
+    if (!STATES) CTA_SPAN(0);
     const Ctl ctl{bar, abort_flag, p.err, p.wait_limit};
 
     if (warp < 4) {
@@ -730,6 +759,7 @@ __device__ __forceinline__ void gdn_tc_body(const CUtensorMap *tm_q, const CUten
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if (!STATES) CTA_SPAN(1);
     if (warp == 9) tmem_dealloc(tmem, 512);
 }
 
@@ -778,15 +808,12 @@ gdn_status launch_tc(const FwdArgs &a, const __nv_bfloat16 *Tin, const LaunchCfg
         !make_map(&mv, a.v, a.dv, ydim, zdim) || !make_map(&mt, Tin, 64, ydim, zdim) ||
         !make_map(&mw, Win, DK, ydim, zdim))
         return GDN_ERR_CUDA;
-    static bool attr_set = false;
-    if (!attr_set) {
-        if (cudaFuncSetAttribute(k_gdn_tc<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 L::ALLOC) != cudaSuccess ||
-            cudaFuncSetAttribute(k_gdn_tc_states<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 L::ALLOC_S) != cudaSuccess)
-            return GDN_ERR_CUDA;
-        attr_set = true;
-    }
+    // per-function attributes of the current device: cheap, set on every launch
+    if (cudaFuncSetAttribute(k_gdn_tc<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             L::ALLOC) != cudaSuccess ||
+        cudaFuncSetAttribute(k_gdn_tc_states<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             L::ALLOC_S) != cudaSuccess)
+        return GDN_ERR_CUDA;
     // the state pass's outputs (the forward's instantiation never reads these)
     CUtensorMap mh = mq, mvs = mq;
     if (c.Hst && (!make_map_f32(&mh, c.Hst, a.dv, (long long)a.sm.H * a.chunk_slots * DK, DK) ||
@@ -885,14 +912,17 @@ k_seg_fold(const float *__restrict__ h0, const float *__restrict__ Aseg,
 }
 
 int sm_count() {
-    static int n = 0;
-    if (n == 0) {
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-            n = 148;
-    }
-    return n;
+    static std::atomic<int> memo[kMaxDeviceMemo];
+    return per_device(
+        memo,
+        [](int dev) {
+            int n = 0;
+            if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+                n <= 0)
+                n = 148;
+            return n;
+        },
+        148);
 }
 
 // Number of sequence segments for the segment scan (1 = none).  Automatic:
@@ -974,9 +1004,10 @@ bool tc_supported(const FwdArgs &a) {
     if (a.dv % kNV != 0 || a.dv > 256) return false;
     if (a.sm.N > 65535 || a.sm.H > 65535) return false;
     if (a.rows <= 0) return false;   // nothing but h0 -> hT: the plain path covers it
-    static int ok = -1;
-    if (ok < 0) ok = (device_is_sm10x() && encode_fn() != nullptr) ? 1 : 0;
-    return ok == 1;
+    static std::atomic<int> memo[kMaxDeviceMemo];
+    return per_device(
+               memo, [](int) { return (device_is_sm10x() && encode_fn() != nullptr) ? 1 : 0; },
+               0) == 1;
 }
 
 gdn_status tc_forward(const FwdArgs &a) {

@@ -380,29 +380,30 @@ int g_ut_ctas_seen = 0;
 template <int DK>
 gdn_status launch_ut(const FwdArgs &a, const int2 *table, __nv_bfloat16 *Tu) {
     using L = ULay<DK>;
-    static int ctas[64] = {};   // CTAs the device holds at once, per device (benign race:
-                                // every thread computes the same value)
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return GDN_ERR_CUDA;
     if (cudaFuncSetAttribute(k_gdn_ut<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              L::ALLOC) != cudaSuccess ||
         cudaFuncSetAttribute(k_gdn_ut<DK>, cudaFuncAttributePreferredSharedMemoryCarveout,
                              100) != cudaSuccess)
         return GDN_ERR_CUDA;
-    if (ctas[dev] == 0) {
-        // CTAs per SM: what shared memory holds (1 KB reserved per CTA), at most
-        // three (the launch bounds' register budget; 128 of the 512 tensor-memory
-        // columns each)
-        int smem_sm = 0, nsm = 0;
-        if (cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) !=
-                cudaSuccess ||
-            cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-            return GDN_ERR_CUDA;
-        const int fit = smem_sm / (L::ALLOC + 1024);
-        ctas[dev] = max(1, min(fit, 3)) * max(1, nsm);
-    }
+    // CTAs the device holds at once, per device.  CTAs per SM: what shared
+    // memory holds (1 KB reserved per CTA), at most three (the launch bounds'
+    // register budget; 128 of the 512 tensor-memory columns each)
+    static std::atomic<int> memo[kMaxDeviceMemo];
+    const int ctas = per_device(
+        memo,
+        [](int dev) {
+            int smem_sm = 0, nsm = 0;
+            if (cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor,
+                                       dev) != cudaSuccess ||
+                cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+                return -1;
+            const int fit = smem_sm / (L::ALLOC + 1024);
+            return max(1, min(fit, 3)) * max(1, nsm);
+        },
+        0);
+    if (ctas <= 0) return GDN_ERR_CUDA;
 #ifdef GDN_TRACE_TIMELINE
-    g_ut_ctas_seen = ctas[dev];
+    g_ut_ctas_seen = ctas;
 #endif
     const long long units = (long long)a.chunk_slots * a.sm.H;
     if (units <= 0) return GDN_OK;
@@ -422,7 +423,7 @@ gdn_status launch_ut(const FwdArgs &a, const int2 *table, __nv_bfloat16 *Tu) {
     p.units = units;
     const long long lim = option(GDN_OPT_WAIT_LIMIT);
     p.wait_limit = lim > 0 ? (uint32_t)(lim > 0x7fffffffLL ? 0x7fffffffLL : lim) : (1u << 22);
-    const int grid = (int)(units < ctas[dev] ? units : (long long)ctas[dev]);
+    const int grid = (int)(units < ctas ? units : (long long)ctas);
     k_gdn_ut<DK><<<grid, kThreadsU, L::ALLOC, a.stream>>>(mk, p);
     count_launch();
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;

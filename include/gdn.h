@@ -103,15 +103,21 @@ gdn_status gdn_fwd_varlen(const void *q, const void *k, const void *v,
  * allocation afterwards, or a latency-critical loop in which an allocation
  * that stalls or fails is not acceptable.  gdn_fwd_noalloc takes the same
  * arguments and has the same layouts as gdn_fwd, but keeps its scratch in a
- * fixed 32 MiB array that the library places in every GPU's memory when it
- * is loaded; it never calls an allocator.
+ * fixed 32 MiB array that is part of the library's device code; it never
+ * calls an allocator and never takes memory from the scratch pool.
+ *
+ *   When the 32 MiB are taken: the CUDA driver loads a library's device code
+ *   onto a device lazily, at its first use there (the default since CUDA
+ *   12.2), so the array is mapped on a device by the first gdn_fwd_noalloc
+ *   call there (or by an earlier general-path call, which shares that code).
+ *   That first call therefore needs 32 MiB of free device memory: make one
+ *   call on each device before the process reserves its device memory for
+ *   itself, and before any stream capture.  Later calls map nothing.
  *
  *   Limit: B*H*T*(d_k + d_v + 1)*4 bytes must not exceed 32 MiB (for
  *   d_k = d_v = 128, about 32 000 token-heads), otherwise GDN_ERR_TOO_LARGE
  *   is returned and nothing is enqueued.  It always runs the general path's
  *   kernels (GDN_IMPL_SIMT; bf16 or fp32 I/O).
- *   Set-up: the first call on each device looks up the array's device address
- *   with that device current; make that first call before any stream capture.
  *   Sharing: every call uses the same array.  Calls whose kernels overlap on
  *   the GPU (other streams, other host threads) race on it and give wrong
  *   results; serialise them.
@@ -175,6 +181,16 @@ gdn_status gdn_kernel_timer_read(double *total_ms, long long *launches, const ch
 
 /* Number of kernels this library has launched since it was loaded. */
 uint64_t gdn_kernel_launches(void);
+
+/*
+ * The current device's scratch pool (the stream-ordered pool every entry point
+ * but gdn_fwd_noalloc takes its temporary buffers from): bytes in use now and
+ * the high-water mark of bytes in use (either pointer may be null).  With
+ * reset_high != 0 the high-water mark then restarts from the current use.
+ * Creates the pool if the device had none.  GDN_ERR_CUDA if the pool cannot be
+ * queried.
+ */
+gdn_status gdn_scratch_stats(uint64_t *used_current, uint64_t *used_high, int reset_high);
 
 /* Implementation the last successful gdn_fwd / gdn_fwd_varlen / gdn_bwd /
  * gdn_bwd_varlen call used (GDN_IMPL_SIMT, GDN_IMPL_TC or GDN_IMPL_TC_FUSED;

@@ -4,11 +4,15 @@ Some users cannot let a library allocate device memory while they run: a
 serving process that gives all of the GPU's memory to its own pool at start-up
 and forbids other allocations, or a latency-critical loop in which an
 allocation that stalls or fails is not acceptable.  gdn_fwd_noalloc keeps its
-scratch in a fixed 32 MiB device array instead.  This test calls it through
-the C ABI and checks it against gdn_fwd, the allocating entry point, on two
-calls in a row (the second call finds the first call's data in the shared
-scratch and must not be affected by it).  It lives in its own file, collected
-last, and passes both alone in a fresh process and after the other tests.
+scratch in a fixed 32 MiB device array instead.
+
+These tests call it through the C ABI and compare every output element with
+the fp64 oracle, for bf16 and fp32 I/O, on two calls in a row: the first call
+on a device maps the array (the driver loads the library's device code
+lazily), and the second call must succeed, find the first call's data in the
+shared scratch without being affected by it, and take nothing from the
+library's scratch pool.  The file is collected last and passes both alone in
+a fresh process and after the other tests.
 """
 import ctypes
 
@@ -32,21 +36,35 @@ def _call_noalloc(lib, x, o, hT):
                                ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
 
 
-def test_noalloc_matches_gdn_fwd_on_two_calls():
+def _run_and_check(lib, x, io):
+    B, H, T, dk = x.q.shape
+    dv = x.v.shape[-1]
+    o = torch.full_like(x.v, float("nan"))
+    hT = torch.full((B, H, dv, dk), float("nan"), dtype=torch.float32, device="cuda")
+    assert _call_noalloc(lib, x, o, hT) == gdn.GDN_OK
+    assert lib.gdn_sync_check(ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)) == gdn.GDN_OK
+    torch.cuda.synchronize()
+    o_ref, h_ref = U.oracle_dense(x)
+    to, th = U.TOL[io]
+    eo = U.rel(U.f64(o), o_ref.reshape(o.shape))
+    eh = U.rel(U.f64(hT), h_ref.reshape(hT.shape))
+    assert eo <= to and eh <= th, (io, eo, eh)
+
+
+@pytest.mark.parametrize("io", ["bf16", "f32"])
+def test_noalloc_two_calls_match_oracle(io):
     lib = gdn.load()
-    stream = torch.cuda.current_stream().cuda_stream
-    cases = [(2, 3, 200, 128, 128, 0.02, 31), (1, 4, 3 * 64 + 5, 64, 64, 0.0, 32)]
-    for B, H, T, dk, dv, h0s, seed in cases:
-        x = synth.make_dense(B, H, T, dk, dv, io="bf16", h0_std=h0s, seed=seed, device="cuda")
-        o_ref, h_ref = gdn.gdn_fwd(x.q, x.k, x.v, x.log_alpha, x.beta, x.h0, check=True)
-        o = torch.full_like(o_ref, float("nan"))
-        hT = torch.full_like(h_ref, float("nan"))
-        assert _call_noalloc(lib, x, o, hT) == gdn.GDN_OK
-        assert lib.gdn_sync_check(stream) == gdn.GDN_OK
-        torch.cuda.synchronize()
-        eo = U.rel(U.f64(o), U.f64(o_ref))
-        eh = U.rel(U.f64(hT), U.f64(h_ref))
-        assert eo <= U.TOL["bf16"][0] and eh <= U.TOL["bf16"][1], (eo, eh)
+    first = synth.make_dense(2, 3, 200, 128, 128, io=io, h0_std=0.02, seed=31, device="cuda")
+    second = synth.make_dense(1, 4, 3 * 64 + 5, 64, 64, io=io, h0_std=0.0, seed=32,
+                              device="cuda")
+    # first call on this device: maps the fixed array if nothing has yet
+    _run_and_check(lib, first, io)
+    # second call: must succeed and draw nothing from the scratch pool
+    torch.cuda.synchronize()
+    cur0, _ = gdn.scratch_stats(reset_high=True)
+    _run_and_check(lib, second, io)
+    cur1, high1 = gdn.scratch_stats()
+    assert high1 <= cur0 and cur1 <= cur0, (cur0, cur1, high1)
 
 
 def test_noalloc_rejects_calls_beyond_its_scratch():
