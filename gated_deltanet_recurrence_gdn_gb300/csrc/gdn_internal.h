@@ -149,6 +149,12 @@ gdn_status enqueue_tc_prep(const FwdArgs &a, const int2 *table, __nv_bfloat16 *T
 // only).  The fused forward (gdn_fused.cu) reads it and forms W, U,
 // the state pass and the output in one kernel per (sequence, head, d_v tile).
 gdn_status enqueue_ut(const FwdArgs &a, const int2 *table, __nv_bfloat16 *Tu);
+// The same chunk prep (bf16, scalar gates, erase; d_k 64 or 128) in the layout
+// of enqueue_tc_prep: T_u as [rows][64] and W = T_w K (formed on tcgen05 from
+// the staged K tile) as [rows][d_k], rows indexed like the token rows of the
+// inputs.  GDN_ERR_UNSUPPORTED outside those shapes.
+gdn_status enqueue_ut_w(const FwdArgs &a, const int2 *table, __nv_bfloat16 *Tu,
+                        __nv_bfloat16 *W);
 bool fused_supported(const FwdArgs &a);
 gdn_status fused_forward(const FwdArgs &a);
 

@@ -1028,7 +1028,12 @@ gdn_status tc_forward(const FwdArgs &a) {
         else
             rc = enqueue_chunk_table(a, table);
     }
-    if (rc == GDN_OK) rc = enqueue_tc_prep(a, table, Tbuf, Tbuf + (size_t)a.rows * 64);
+    if (rc == GDN_OK) {
+        // the tcgen05 chunk prep (gdn_ut.cu) where it applies, else gdn_prep.cu's
+        __nv_bfloat16 *Wbuf = Tbuf + (size_t)a.rows * 64;
+        rc = enqueue_ut_w(a, table, Tbuf, Wbuf);
+        if (rc == GDN_ERR_UNSUPPORTED) rc = enqueue_tc_prep(a, table, Tbuf, Wbuf);
+    }
     const int S = choose_segments(a);
     if (rc == GDN_OK && S > 1) {
         rc = tc_segmented(a, Tbuf, S);

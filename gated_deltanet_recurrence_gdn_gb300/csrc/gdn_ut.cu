@@ -7,19 +7,27 @@
 //
 // ("Gated DeltaNet GPU并行实现", section 3.2: everything inside a chunk is
 // parallel; the serial state pass needs only the chunk's WY factors
-// U = T_u V and W = T_w K, which the fused kernel forms on its own tensor
-// cores.)  Both are written as bf16 in a per-chunk layout
-// [H][chunk_slots][T_u | T_w][64][64] (dense: slot n * max_chunks + c; packed:
-// floor(cu[n] / 64) + n + c), so each is one bulk-copy box for the fused
-// kernel.  Rows and columns of tokens past a sequence's end are zero, because
-// beta and log_alpha are zero there.
+// U = T_u V and W = T_w K.)  Two output forms:
+//   - T_u and T_w as bf16 in a per-chunk layout [H][chunk_slots][T_u | T_w]
+//     [64][64] (dense: slot n * max_chunks + c; packed: floor(cu[n] / 64) +
+//     n + c), one bulk-copy box each, for the fused kernel (gdn_fused.cu),
+//     which forms W and U on its own tensor cores;
+//   - "W out", the forward's default: T_u as [rows][64] and W = T_w K as
+//     [rows][d_k], bf16, rows indexed like the token rows of the inputs, for
+//     the chain kernel (gdn_tc.cu).  W comes from a second tcgen05 product on
+//     the staged K tile.
+// Rows and columns of tokens past a sequence's end are zero, because beta and
+// log_alpha are zero there.
 //
 // Per unit (chunk, head): the K tile arrives by bulk tensor copy (128-byte
 // swizzle), one thread issues the Gram K K^T as tcgen05 MMAs into tensor
 // memory (M = 128: rows 64-127 of the operand are whatever follows the tile and
 // are never read), four warps read its rows, form A and invert I + A
-// (gdn_inv.cuh).  Persistent: each CTA walks units b, b + grid, ... with two K
-// buffers and two Gram accumulators in flight.
+// (gdn_inv.cuh).  With W out, the warps then stage T_w (bf16, swizzled) and
+// the same thread issues W^T = K^T T_w^T (M = d_k lanes, N = 64 tokens) into
+// the unit's Gram columns; the warps read it back, transpose it through shared
+// memory and store W rows.  Persistent: each CTA walks units b, b + grid, ...
+// with two K buffers and two accumulators in flight.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -63,10 +71,14 @@ constexpr int kThreadsU = 160;   // warps 0-3 compute, warp 4 copies and issues 
 
 enum {
     U_FULL = 0,        // + buffer: K tile landed, raw gates staged (TMA tx + 32 lanes)
-    U_EMPTY = 2,       // + buffer: Gram read the tile (commit) and the gates were copied
+    U_EMPTY = 2,       // + buffer: the tile's MMAs are done (commits) and the gates
+                       //   were copied
     U_GDONE = 4,       // + buffer: Gram in tensor memory (commit)
-    U_GFREE = 6,       // + buffer: A formed from it
-    U_DRAIN = 8,
+    U_GFREE = 6,       // + buffer: its tensor-memory columns read (A formed; with W
+                       //   out, W^T read as well)
+    U_TW = 8,          // + buffer: T_w staged as the bf16 operand of W^T (W out)
+    U_WDONE = 10,      // + buffer: W^T in tensor memory (commit; W out)
+    U_DRAIN = 12,
     U_COUNT
 };
 
@@ -93,7 +105,10 @@ struct UtParams {
     SeqMap sm;
     const float *log_alpha, *beta;
     const int2 *table;        // packed batches: (sequence, chunk) of every chunk slot
-    __nv_bfloat16 *Tu;        // [H][chunk_slots][2][64][64]: T_u, T_w
+    // per-chunk blocks [H][chunk_slots][2][64][64] of T_u, T_w; or, with W out,
+    // T_u as [rows][64] indexed like the token rows of the inputs
+    __nv_bfloat16 *Tu;
+    __nv_bfloat16 *W;         // W out: W = T_w K as [rows][d_k]
     int *err;
     int max_chunks;
     int chunk_slots;
@@ -146,7 +161,7 @@ __device__ __forceinline__ Unit decode(const UtParams &p, long long u) {
     return r;
 }
 
-template <int DK>
+template <int DK, bool WOUT>
 __global__ void __launch_bounds__(kThreadsU, 3)
 k_gdn_ut(const __grid_constant__ CUtensorMap tm_k, UtParams p) {
     using L = ULay<DK>;
@@ -182,7 +197,7 @@ k_gdn_ut(const __grid_constant__ CUtensorMap tm_k, UtParams p) {
         for (int i = 0; i < U_COUNT; ++i) mbar_init(bar + i, 1);
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar + U_FULL + b, 33);
-            mbar_init(bar + U_EMPTY + b, 2);
+            mbar_init(bar + U_EMPTY + b, WOUT ? 3 : 2);
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -237,12 +252,40 @@ k_gdn_ut(const __grid_constant__ CUtensorMap tm_k, UtParams p) {
             mma_commit(bar + U_EMPTY + b);
             return true;
         };
+        // W^T = K^T T_w^T (M = d_k lanes, N = 64 tokens) into the unit's Gram
+        // columns: A is K read d_k-major, B the staged T_w tile (K-major)
+        constexpr uint32_t idW = make_idesc_bf16(128, 64, true, false);
+        auto wmma = [&](long long i) -> bool {
+            const int b = (int)(i & 1);
+            if (!ctl.wait(U_TW + b, (uint32_t)((i >> 1) & 1))) return false;
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < kU / 16; ++kk) {
+                const uint64_t da =
+                    make_sdesc(sb + L::OFF_K + b * L::SZ_K + kk * 2048, 8192, 1024, kSwizzle128B);
+                const uint64_t dbw = make_sdesc(sb + L::OFF_A + kk * 32, 16, 1024, kSwizzle128B);
+                mma_bf16(tmem + 64 * b, da, dbw, idW, kk > 0);
+            }
+            mma_commit(bar + U_WDONE + b);
+            mma_commit(bar + U_EMPTY + b);
+            return true;
+        };
         long long loaded = 0;
         bool ok = true;
         for (long long i = 0; ok && i < nunits && i < 2; ++i) ok = load(i), loaded = i + 1;
         for (long long i = 0; ok && i < nunits; ++i) {
             int okg = 1;
-            if (lane == 0) okg = gram(i);
+            if (lane == 0) {
+                if (!WOUT) {
+                    okg = gram(i);
+                } else {
+                    // the next unit's Gram goes ahead of this unit's W^T, which
+                    // waits for the inverse
+                    if (i == 0) okg = gram(0);
+                    if (okg && i + 1 < nunits) okg = gram(i + 1);
+                    if (okg) okg = wmma(i);
+                }
+            }
             ok = __shfl_sync(0xffffffffu, okg, 0) != 0;
             if (ok && i + 2 < nunits) ok = load(i + 2), loaded = i + 3;
         }
@@ -309,34 +352,125 @@ k_gdn_ut(const __grid_constant__ CUtensorMap tm_k, UtParams p) {
                 // is moderate, else one exponential per entry (never above 1).
                 // Entries outside the 16x16 diagonal blocks are rounded to tf32
                 // for the merges.
+                // (a uniform branch: the common case computes no exponential)
                 const bool span_ok = gs[63] > -80.f;
                 const float bgr = br * gs[128 + r];
+                auto form = [&](auto factor) {
 #pragma unroll
-                for (int q = 0; q < 16; ++q) {
-                    float v[4];
+                    for (int q = 0; q < 16; ++q) {
+                        float v[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int s = 4 * q + e;
-                        const float gv = f32(s < 32 ? g0[s] : g1[s - 32]);
-                        const float f = span_ok ? bgr * gs[192 + s] : br * __expf(gr - gs[s]);
-                        const float x = s < r ? f * gv : 0.f;
-                        const float xt = inv::tf32(x);
-                        v[e] = (r >> 4) != (s >> 4) ? xt : x;
+                        for (int e = 0; e < 4; ++e) {
+                            const int s = 4 * q + e;
+                            const float gv = f32(s < 32 ? g0[s] : g1[s - 32]);
+                            const float x = s < r ? factor(s) * gv : 0.f;
+                            v[e] = (r >> 4) != (s >> 4) ? inv::tf32(x) : x;
+                        }
+                        *reinterpret_cast<float4 *>(Ab + r * LDA + 4 * q) =
+                            make_float4(v[0], v[1], v[2], v[3]);
                     }
-                    *reinterpret_cast<float4 *>(Ab + r * LDA + 4 * q) =
-                        make_float4(v[0], v[1], v[2], v[3]);
-                }
+                };
+                if (span_ok)
+                    form([&](int s) { return bgr * gs[192 + s]; });
+                else
+                    form([&](int s) { return br * __expf(s < r ? gr - gs[s] : 0.f); });
             } else {
                 inv::clear_upper16(Tb, tid - 64, 64);
             }
             tc_fence_before();
             bar128();
-            if (tid == 0) mbar_arrive(bar + U_GFREE + b);
+            if (!WOUT && tid == 0) mbar_arrive(bar + U_GFREE + b);
             __syncwarp();
             UTRACE(i, 2);
             // ---- T = (I + A)^{-1}
             inv::invert64(Ab, Tb, tid, bar128);
             UTRACE(i, 3);
+            if (WOUT) {
+                // ---- T_u = T diag(beta) rows out, and T_w = T diag(beta gamma)
+                //      staged (bf16, 128-byte swizzled, in A's space) as the
+                //      operand of W^T.  Item (row r, 8-column chunk ch), four per
+                //      thread: eight consecutive threads read one row of T
+                //      (conflict-free) and write 128 contiguous bytes of T_u.
+                {
+                    uint8_t *Tw = sm + L::OFF_A;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int item = tid + 128 * k, r = item >> 3, ch = item & 7;
+                        const int c = 8 * ch;
+                        const float4 ta = *reinterpret_cast<const float4 *>(Tb + r * LDA + c);
+                        const float4 tb = *reinterpret_cast<const float4 *>(Tb + r * LDA + c + 4);
+                        float tv[8] = {ta.x, ta.y, ta.z, ta.w, tb.x, tb.y, tb.z, tb.w};
+                        uint32_t wu[4], ww[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int s2 = c + 2 * e;
+                            // zero above the diagonal and in the scratch block
+                            const bool z0 = s2 > r || (r < 32 && s2 >= 32);
+                            const bool z1 = s2 + 1 > r || (r < 32 && s2 + 1 >= 32);
+                            const float t0 = z0 ? 0.f : tv[2 * e] * gs[64 + s2];
+                            const float t1 = z1 ? 0.f : tv[2 * e + 1] * gs[64 + s2 + 1];
+                            wu[e] = pack_bf16(t0, t1);
+                            ww[e] = pack_bf16(t0 * gs[128 + s2], t1 * gs[128 + s2 + 1]);
+                        }
+                        if (r < un.len)
+                            *reinterpret_cast<uint4 *>(p.Tu + (un.row0 + r) * kU + c) =
+                                make_uint4(wu[0], wu[1], wu[2], wu[3]);
+                        st16(Tw + sw128_offset(r, ch), ww[0], ww[1], ww[2], ww[3]);
+                    }
+                }
+                fence_proxy_async_smem();
+                bar128();
+                if (tid == 0) mbar_arrive(bar + U_TW + b);
+                // ---- W rows: W^T from tensor memory (lane = d_k index), through
+                //      a padded shared-memory tile over A's and T's space (both
+                //      done with: the W^T MMA has read the T_w tile), out as rows.
+                //      Row stride = 16 words mod 32, so the even lanes' row 2m and
+                //      the odd lanes' row 2m + 1 fill different banks.
+                constexpr int LDW = DK + 32;   // bf16 row stride of the staging tile
+                static_assert(kU * LDW * 2 <= 2 * kU * LDA * 4, "staging fits A's and T's space");
+                __nv_bfloat16 *Ws = reinterpret_cast<__nv_bfloat16 *>(sm + L::OFF_A);
+                if (!named_bar_and(1, 128, ctl.wait(U_WDONE + b, (uint32_t)((i >> 1) & 1))))
+                    break;
+                tc_fence_after();
+                if (tid < DK) {
+                    uint32_t w0[32], w1[32];
+                    tmem_ld32(tmem + lane_base + 64 * b, w0);
+                    tmem_ld32(tmem + lane_base + 64 * b + 32, w1);
+                    tmem_wait32(w0);
+                    tmem_wait32(w1);
+                    // lanes t and t ^ 1 hold columns t and t ^ 1 of every row:
+                    // the even lane writes the pair for rows 2m, the odd lane
+                    // for rows 2m + 1, as one 32-bit word each
+                    const bool odd = tid & 1;
+                    const int cpair = tid & ~1;
+#pragma unroll
+                    for (int m = 0; m < 32; ++m) {
+                        const int r0 = 2 * m;   // rows r0 (even lane) and r0 + 1 (odd lane)
+                        const float a0 = f32(r0 < 32 ? w0[r0] : w1[r0 - 32]);
+                        const float a1 = f32(r0 + 1 < 32 ? w0[r0 + 1] : w1[r0 - 31]);
+                        // even lane: needs the odd lane's value of row r0; odd
+                        // lane: the even lane's value of row r0 + 1
+                        const float give = odd ? a0 : a1;
+                        const float got = __shfl_xor_sync(0xffffffffu, give, 1);
+                        const int row = odd ? r0 + 1 : r0;
+                        const uint32_t word = odd ? pack_bf16(got, a1) : pack_bf16(a0, got);
+                        *reinterpret_cast<uint32_t *>(Ws + row * LDW + cpair) = word;
+                    }
+                }
+                tc_fence_before();
+                bar128();
+                if (tid == 0) mbar_arrive(bar + U_GFREE + b);
+                constexpr int VPR = DK / 8;   // 16-byte vectors per W row
+#pragma unroll
+                for (int j = 0; j < kU * VPR / 128; ++j) {
+                    const int idx = tid + 128 * j, r = idx / VPR, q = idx % VPR;
+                    if (r < un.len)
+                        *reinterpret_cast<uint4 *>(p.W + (un.row0 + r) * DK + 8 * q) =
+                            *reinterpret_cast<const uint4 *>(Ws + r * LDW + 8 * q);
+                }
+                UTRACE(i, 4);
+                continue;
+            }
             // ---- T_u = T diag(beta) and T_w = T diag(beta gamma), bf16 rows:
             //      thread t takes row t/2, columns 32 (t & 1) .. + 31 of both
             if (un.len > 0) {
@@ -377,12 +511,12 @@ k_gdn_ut(const __grid_constant__ CUtensorMap tm_k, UtParams p) {
 int g_ut_ctas_seen = 0;
 #endif
 
-template <int DK>
-gdn_status launch_ut(const FwdArgs &a, const int2 *table, __nv_bfloat16 *Tu) {
+template <int DK, bool WOUT>
+gdn_status launch_ut(const FwdArgs &a, const int2 *table, __nv_bfloat16 *Tu, __nv_bfloat16 *W) {
     using L = ULay<DK>;
-    if (cudaFuncSetAttribute(k_gdn_ut<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(k_gdn_ut<DK, WOUT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              L::ALLOC) != cudaSuccess ||
-        cudaFuncSetAttribute(k_gdn_ut<DK>, cudaFuncAttributePreferredSharedMemoryCarveout,
+        cudaFuncSetAttribute(k_gdn_ut<DK, WOUT>, cudaFuncAttributePreferredSharedMemoryCarveout,
                              100) != cudaSuccess)
         return GDN_ERR_CUDA;
     // CTAs the device holds at once, per device.  CTAs per SM: what shared
@@ -417,6 +551,7 @@ gdn_status launch_ut(const FwdArgs &a, const int2 *table, __nv_bfloat16 *Tu) {
     p.beta = a.beta;
     p.table = table;
     p.Tu = Tu;
+    p.W = W;
     p.err = device_error_word();
     p.max_chunks = a.max_chunks;
     p.chunk_slots = a.chunk_slots;
@@ -424,7 +559,7 @@ gdn_status launch_ut(const FwdArgs &a, const int2 *table, __nv_bfloat16 *Tu) {
     const long long lim = option(GDN_OPT_WAIT_LIMIT);
     p.wait_limit = lim > 0 ? (uint32_t)(lim > 0x7fffffffLL ? 0x7fffffffLL : lim) : (1u << 22);
     const int grid = (int)(units < ctas ? units : (long long)ctas);
-    k_gdn_ut<DK><<<grid, kThreadsU, L::ALLOC, a.stream>>>(mk, p);
+    k_gdn_ut<DK, WOUT><<<grid, kThreadsU, L::ALLOC, a.stream>>>(mk, p);
     count_launch();
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
@@ -437,8 +572,16 @@ extern "C" int gdn_ut_debug_ctas() { return g_ut_ctas_seen; }
 
 gdn_status enqueue_ut(const FwdArgs &a, const int2 *table, __nv_bfloat16 *Tu) {
     if (a.no_erase || a.vector_gate || a.dt != GDN_BF16) return GDN_ERR_UNSUPPORTED;
-    if (a.dk == 128) return launch_ut<128>(a, table, Tu);
-    if (a.dk == 64) return launch_ut<64>(a, table, Tu);
+    if (a.dk == 128) return launch_ut<128, false>(a, table, Tu, nullptr);
+    if (a.dk == 64) return launch_ut<64, false>(a, table, Tu, nullptr);
+    return GDN_ERR_UNSUPPORTED;
+}
+
+gdn_status enqueue_ut_w(const FwdArgs &a, const int2 *table, __nv_bfloat16 *Tu,
+                        __nv_bfloat16 *W) {
+    if (a.no_erase || a.vector_gate || a.dt != GDN_BF16) return GDN_ERR_UNSUPPORTED;
+    if (a.dk == 128) return launch_ut<128, true>(a, table, Tu, W);
+    if (a.dk == 64) return launch_ut<64, true>(a, table, Tu, W);
     return GDN_ERR_UNSUPPORTED;
 }
 
