@@ -30,6 +30,7 @@ GDN_ERR_ALIGNMENT = 3
 GDN_ERR_CUDA = 4
 GDN_ERR_DEVICE_TIMEOUT = 5
 GDN_ERR_TOO_LARGE = 6
+GDN_ERR_BOUNDS = 7
 GDN_F32 = 0
 GDN_BF16 = 1
 GDN_OPT_IMPL = 0
@@ -69,6 +70,7 @@ ABI = [
                                    ctypes.POINTER(ctypes.c_char_p)]),
     ("gdn_kernel_launches", ctypes.c_uint64, []),
     ("gdn_scratch_stats", _i, [ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(ctypes.c_uint64), _i]),
+    ("gdn_bounds_violation", _i, [_i]),
     ("gdn_last_impl", _i, []),
     ("gdn_release_scratch", _i, []),
     ("gdn_selftest_wait", _i, [_i, ctypes.c_longlong, ctypes.POINTER(_i), _vp]),

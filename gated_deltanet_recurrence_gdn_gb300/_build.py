@@ -31,14 +31,26 @@ def _stale(out, deps):
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, extra=()) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+# Build variants: name -> extra nvcc flags.  "check" is the debug
+# bounds-check build (csrc/gdn_check.cuh); its objects and library sit beside
+# the normal ones under their own names.
+VARIANTS = {"check": ["-DGDN_BOUNDS_CHECK"]}
+
+
+def build_variant(name: str, force: bool = False, verbose: bool = False) -> str:
+    return build(force=force, verbose=verbose, extra=VARIANTS[name], variant=name)
+
+
+def build(force: bool = False, verbose: bool = False, extra=(), variant=None) -> str:
+    build_dir = BUILD if variant is None else os.path.join(PKG, "_build_" + variant)
+    lib_path = LIB if variant is None else os.path.join(PKG, "libgdn_%s.so" % variant)
+    os.makedirs(build_dir, exist_ok=True)
     headers = glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(CSRC, "*.cuh")) + \
         glob.glob(os.path.join(ROOT, "include", "*.h"))
     objs = []
     jobs = []
     for src in sources():
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         objs.append(obj)
         if force or _stale(obj, [src] + headers):
             jobs.append([NVCC] + _flags() + list(extra) + ["-c", src, "-o", obj])
@@ -54,11 +66,11 @@ def build(force: bool = False, verbose: bool = False, extra=()) -> str:
 
     with ThreadPoolExecutor(max_workers=max(1, min(len(jobs), os.cpu_count() or 4))) as ex:
         list(ex.map(run, jobs))
-    if force or jobs or _stale(LIB, objs):
-        tmp = LIB + ".tmp%d" % os.getpid()
+    if force or jobs or _stale(lib_path, objs):
+        tmp = lib_path + ".tmp%d" % os.getpid()
         run([NVCC] + ARCH + ["-shared", "-o", tmp] + objs)
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

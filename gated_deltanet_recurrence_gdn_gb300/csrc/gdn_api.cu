@@ -156,6 +156,33 @@ long long option(int key) {
     }
 }
 
+// Readers of the violation words of the translation units built with
+// GDN_BOUNDS_CHECK (gdn_check.cuh); empty in a normal build.
+namespace {
+std::mutex g_bounds_mu;
+std::vector<int (*)(bool)> &bounds_readers() {
+    static std::vector<int (*)(bool)> v;
+    return v;
+}
+}  // namespace
+
+void register_bounds_word(int (*read_clear)(bool clear)) {
+    std::lock_guard<std::mutex> lk(g_bounds_mu);
+    bounds_readers().push_back(read_clear);
+}
+
+// Source line of the first failed bounds check on the current device in any
+// translation unit (0: none); clears every word if asked.
+int bounds_line(bool clear) {
+    std::lock_guard<std::mutex> lk(g_bounds_mu);
+    int first = 0;
+    for (auto fn : bounds_readers()) {
+        const int v = fn(clear);
+        if (first == 0) first = v;
+    }
+    return first;
+}
+
 }  // namespace gdn
 
 using namespace gdn;
@@ -346,6 +373,7 @@ const char *gdn_status_string(gdn_status s) {
         case GDN_ERR_CUDA: return "GDN_ERR_CUDA: CUDA runtime error";
         case GDN_ERR_DEVICE_TIMEOUT: return "GDN_ERR_DEVICE_TIMEOUT: bounded device wait gave up";
         case GDN_ERR_TOO_LARGE: return "GDN_ERR_TOO_LARGE: call needs more than the fixed scratch of gdn_fwd_noalloc (32 MiB)";
+        case GDN_ERR_BOUNDS: return "GDN_ERR_BOUNDS: a check of the bounds-check build failed (see gdn_bounds_violation)";
         default: return "unknown gdn_status";
     }
 }
@@ -357,9 +385,21 @@ gdn_status gdn_sync_check(void *stream) {
     if (cudaMemcpyFromSymbol(&word, g_error_word, sizeof(int)) != cudaSuccess) return GDN_ERR_CUDA;
     if (word != 0 && cudaMemcpyToSymbol(g_error_word, &zero, sizeof(int)) != cudaSuccess)
         return GDN_ERR_CUDA;
+    // the debug bounds-check build: the first failed check (kept for
+    // gdn_bounds_violation until it clears it)
+    if (bounds_line(false) != 0) return GDN_ERR_BOUNDS;
     if (word == kErrTimeout) return GDN_ERR_DEVICE_TIMEOUT;
     if (word == kErrBadIndex) return GDN_ERR_INVALID_ARG;
     return word == 0 ? GDN_OK : GDN_ERR_CUDA;
+}
+
+int gdn_bounds_violation(int clear) {
+#ifdef GDN_BOUNDS_CHECK
+    return bounds_line(clear != 0);
+#else
+    (void)clear;
+    return -1;
+#endif
 }
 
 gdn_status gdn_set_option(int key, long long value) {

@@ -12,6 +12,8 @@
 #pragma once
 #include <cstdint>
 
+#include "gdn_check.cuh"
+
 namespace gdn {
 namespace inv {
 
@@ -73,10 +75,12 @@ __device__ __forceinline__ void tile_mma(float (&c)[4], const float *Am, int lda
 __device__ __forceinline__ void store_tile(float *D, int ldd, const float (&c)[4], int lane,
                                            float scale) {
     const int g = lane >> 2, t = lane & 3;
-    *reinterpret_cast<float2 *>(D + g * ldd + 2 * t) =
-        make_float2(tf32(scale * c[0]), tf32(scale * c[1]));
-    *reinterpret_cast<float2 *>(D + (g + 8) * ldd + 2 * t) =
-        make_float2(tf32(scale * c[2]), tf32(scale * c[3]));
+    if (GDN_SMEM_OK(saddr(D + g * ldd + 2 * t), 8))
+        *reinterpret_cast<float2 *>(D + g * ldd + 2 * t) =
+            make_float2(tf32(scale * c[0]), tf32(scale * c[1]));
+    if (GDN_SMEM_OK(saddr(D + (g + 8) * ldd + 2 * t), 8))
+        *reinterpret_cast<float2 *>(D + (g + 8) * ldd + 2 * t) =
+            make_float2(tf32(scale * c[2]), tf32(scale * c[3]));
 }
 
 // Zeroes the upper 16x16 blocks inside T's two diagonal 32x32 blocks (the
@@ -84,7 +88,8 @@ __device__ __forceinline__ void store_tile(float *D, int ldd, const float (&c)[4
 __device__ __forceinline__ void clear_upper16(float *Tb, int i, int n) {
     for (int e = i; e < 2 * 256; e += n) {
         const int b = e >> 8, x = e & 255;
-        Tb[(32 * b + (x >> 4)) * LDA + 32 * b + 16 + (x & 15)] = 0.f;
+        float *d = Tb + (32 * b + (x >> 4)) * LDA + 32 * b + 16 + (x & 15);
+        if (GDN_SMEM_OK(saddr(d), 4)) *d = 0.f;
     }
 }
 
@@ -117,7 +122,9 @@ __device__ __forceinline__ void invert64(const float *Ab, float *Tb, int tid, Ba
             x[r] = acc;
         }
 #pragma unroll
-        for (int r = 0; r < 16; ++r) Tb[(o + r) * LDA + o + cc] = tf32(x[r]);
+        for (int r = 0; r < 16; ++r)
+            if (GDN_SMEM_OK(saddr(Tb + (o + r) * LDA + o + cc), 4))
+                Tb[(o + r) * LDA + o + cc] = tf32(x[r]);
     }
     bar();
     {

@@ -152,6 +152,10 @@ k_gdn_prep(const __nv_bfloat16 *__restrict__ k, const float *__restrict__ log_al
         r0 = row0 + t0;
     };
 
+    // token rows of the inputs (element counts for the bounds-check build)
+    const long long nrows =
+        sm.cu ? (long long)sm.H * sm.T_total : (long long)sm.N * sm.H * sm.T;
+    (void)nrows;
     uint4 kr[L::KV];
     float la0 = 0.f, la1 = 0.f, b0 = 0.f, b1 = 0.f;
     // K rows past the chunk and the gates there read as zero
@@ -159,14 +163,17 @@ k_gdn_prep(const __nv_bfloat16 *__restrict__ k, const float *__restrict__ log_al
 #pragma unroll
         for (int j = 0; j < L::KV; ++j) {
             const int i = tid + 128 * j, r = i / VPR, q = i % VPR;
-            kr[j] = r < Lc ? __ldg(reinterpret_cast<const uint4 *>(k + (r0 + r) * DK) + q)
+            kr[j] = (r < Lc && GDN_IDX_OK((r0 + r) * DK + 8 * q, 8, nrows * DK))
+                        ? __ldg(reinterpret_cast<const uint4 *>(k + (r0 + r) * DK) + q)
                            : make_uint4(0u, 0u, 0u, 0u);
         }
         if (w == 0) {
-            la0 = lane < Lc ? __ldg(log_alpha + r0 + lane) : 0.f;
-            la1 = lane + 32 < Lc ? __ldg(log_alpha + r0 + lane + 32) : 0.f;
-            b0 = lane < Lc ? __ldg(beta + r0 + lane) : 0.f;
-            b1 = lane + 32 < Lc ? __ldg(beta + r0 + lane + 32) : 0.f;
+            const bool in0 = lane < Lc && GDN_IDX_OK(r0 + lane, 1, nrows);
+            const bool in1 = lane + 32 < Lc && GDN_IDX_OK(r0 + lane + 32, 1, nrows);
+            la0 = in0 ? __ldg(log_alpha + r0 + lane) : 0.f;
+            la1 = in1 ? __ldg(log_alpha + r0 + lane + 32) : 0.f;
+            b0 = in0 ? __ldg(beta + r0 + lane) : 0.f;
+            b1 = in1 ? __ldg(beta + r0 + lane + 32) : 0.f;
         }
     };
 
@@ -204,8 +211,9 @@ k_gdn_prep(const __nv_bfloat16 *__restrict__ k, const float *__restrict__ log_al
             gs[192 + lane] = __expf(-la0);
             gs[224 + lane] = __expf(-la1);
             if (G_out) {
-                if (lane < Lc) G_out[r0 + lane] = la0;
-                if (lane + 32 < Lc) G_out[r0 + lane + 32] = la1;
+                if (lane < Lc && GDN_IDX_OK(r0 + lane, 1, nrows)) G_out[r0 + lane] = la0;
+                if (lane + 32 < Lc && GDN_IDX_OK(r0 + lane + 32, 1, nrows))
+                    G_out[r0 + lane + 32] = la1;
             }
         }
         __syncthreads();
@@ -295,7 +303,7 @@ k_gdn_prep(const __nv_bfloat16 *__restrict__ k, const float *__restrict__ log_al
                     const int r = 16 * w + i;
                     float2 tv = *reinterpret_cast<const float2 *>(Tb + r * LDA + s);
                     if (r < 32 && s >= 32) tv = make_float2(0.f, 0.f);   // T's upper-right block
-                    if (r < Lc) {
+                    if (r < Lc && GDN_IDX_OK((r0 + r) * kCp + s, 2, nrows * kCp)) {
                         *reinterpret_cast<uint32_t *>(Tu_out + (r0 + r) * kCp + s) =
                             pack2(tv.x * bs.x, tv.y * bs.y);
                         if (T_out) *reinterpret_cast<float2 *>(T_out + (r0 + r) * kCp + s) = tv;
@@ -351,7 +359,7 @@ k_gdn_prep(const __nv_bfloat16 *__restrict__ k, const float *__restrict__ log_al
 #pragma unroll
             for (int j = 0; j < L::KV; ++j) {
                 const int i = tid + 128 * j, r = i / VPR, q = i % VPR;
-                if (r < Lc)
+                if (r < Lc && GDN_IDX_OK((r0 + r) * DK + 8 * q, 8, nrows * DK))
                     *reinterpret_cast<uint4 *>(W_out + (r0 + r) * DK + 8 * q) =
                         *reinterpret_cast<const uint4 *>(Ws + r * L::LDK + 8 * q);
             }

@@ -269,6 +269,13 @@ __device__ __forceinline__ void gdn_tc_body(const CUtensorMap *tm_q, const CUten
     griddep_wait();
     if (!STATES) CTA_SPAN(0);
     const Ctl ctl{bar, abort_flag, p.err, p.wait_limit};
+    // element counts of the global arrays, for the bounds-check build: token
+    // rows of the inputs, and the states of this launch's grid
+    const long long nrows =
+        p.sm.cu ? (long long)p.sm.H * p.sm.T_total : (long long)p.sm.N * p.sm.H * p.sm.T;
+    const long long nstate = (long long)gridDim.z * p.sm.H * dvs * DK;
+    (void)nrows;
+    (void)nstate;
 
     if (warp < 4) {
         // ================================================= chain warpgroup
@@ -278,7 +285,9 @@ __device__ __forceinline__ void gdn_tc_body(const CUtensorMap *tm_q, const CUten
 #pragma unroll
         for (int c = 0; c < kNV; ++c)
             hreg[c] = lin ? ((t < DK && dv0 + c == t) ? 1.f : 0.f)
-                          : ((t < DK && p.h0) ? __ldg(p.h0 + (srow + dv0 + c) * DK + t) : 0.f);
+                          : ((t < DK && p.h0 && GDN_IDX_OK((srow + dv0 + c) * DK + t, 1, nstate))
+                                 ? __ldg(p.h0 + (srow + dv0 + c) * DK + t)
+                                 : 0.f);
         uint8_t *Hs = sm + L::OFF_H;
         uint8_t *VT = sm + L::OFF_R0, *VN = sm + L::OFF_R1;
         // Output rows of chunk jj (lanes 64-127 of its accumulator) to global,
@@ -299,7 +308,8 @@ __device__ __forceinline__ void gdn_tc_body(const CUtensorMap *tm_q, const CUten
                 o0[i] = __float_as_uint(f32(o0[i]) * osc);
                 o1[i] = __float_as_uint(f32(o1[i]) * osc);
             }
-            if (r < Lj) {
+            if (r < Lj && GDN_IDX_OK((row0 + (long long)jj * kC + r) * p.dv + dv0, kNV,
+                                     nrows * p.dv)) {
                 uint4 *dst = reinterpret_cast<uint4 *>(p.o + (row0 + (long long)jj * kC + r) *
                                                                  p.dv + dv0);
 #pragma unroll
@@ -383,10 +393,13 @@ __device__ __forceinline__ void gdn_tc_body(const CUtensorMap *tm_q, const CUten
                         uint8_t *sv = sm + L::OFF_STG + half * 8192;
 #pragma unroll
                         for (int q = 0; q < 8; ++q)
-                            *reinterpret_cast<float4 *>(sv + sw128_offset(t, q)) =
-                                make_float4(vn[4 * q], vn[4 * q + 1], vn[4 * q + 2],
-                                            vn[4 * q + 3]);
-                    } else if (STATES && t < min(kC, len - j * kC)) {
+                            if (GDN_SMEM_OK(smem_u32(sv + sw128_offset(t, q)), 16))
+                                *reinterpret_cast<float4 *>(sv + sw128_offset(t, q)) =
+                                    make_float4(vn[4 * q], vn[4 * q + 1], vn[4 * q + 2],
+                                                vn[4 * q + 3]);
+                    } else if (STATES && t < min(kC, len - j * kC) &&
+                               GDN_IDX_OK((row0 + (long long)j * kC + t) * p.dv + dv0 + 32 * half,
+                                          32, nrows * p.dv)) {
                         float4 *dst = reinterpret_cast<float4 *>(
                             p.Vst + (row0 + (long long)j * kC + t) * p.dv + dv0 + 32 * half);
 #pragma unroll
@@ -439,7 +452,9 @@ __device__ __forceinline__ void gdn_tc_body(const CUtensorMap *tm_q, const CUten
         if (alive && nch > 0 && t >= 64 && !p.no_output && !lin) store_o(nch - 1);
         if (alive && hTp && t < DK) {
 #pragma unroll
-            for (int c = 0; c < kNV; ++c) hTp[(srow + dv0 + c) * DK + t] = hreg[c];
+            for (int c = 0; c < kNV; ++c)
+                if (GDN_IDX_OK((srow + dv0 + c) * DK + t, 1, nstate))
+                    hTp[(srow + dv0 + c) * DK + t] = hreg[c];
         }
         if (STATES && t == 0) bulk_wait_all();   // every store done before the CTA leaves
     } else if (warp < 8) {
@@ -629,10 +644,12 @@ __device__ __forceinline__ void gdn_tc_body(const CUtensorMap *tm_q, const CUten
         auto load_gates = [&](int jj) {
             const long long r0 = row0 + (long long)jj * kC;
             const int Lj = min(kC, len - jj * kC);
-            pla0 = lane < Lj ? __ldg(p.log_alpha + r0 + lane) : 0.f;
-            pla1 = lane + 32 < Lj ? __ldg(p.log_alpha + r0 + lane + 32) : 0.f;
-            pb0 = lane < Lj ? __ldg(p.beta + r0 + lane) : 0.f;
-            pb1 = lane + 32 < Lj ? __ldg(p.beta + r0 + lane + 32) : 0.f;
+            const bool in0 = lane < Lj && GDN_IDX_OK(r0 + lane, 1, nrows);
+            const bool in1 = lane + 32 < Lj && GDN_IDX_OK(r0 + lane + 32, 1, nrows);
+            pla0 = in0 ? __ldg(p.log_alpha + r0 + lane) : 0.f;
+            pla1 = in1 ? __ldg(p.log_alpha + r0 + lane + 32) : 0.f;
+            pb0 = in0 ? __ldg(p.beta + r0 + lane) : 0.f;
+            pb1 = in1 ? __ldg(p.beta + r0 + lane + 32) : 0.f;
         };
         if (nch > 0) load_gates(0);
         for (int j = 0; j < nch; ++j) {

@@ -207,6 +207,10 @@ k_gdn_ut(const __grid_constant__ CUtensorMap tm_k, UtParams p) {
     tc_fence_after();
     const uint32_t tmem = misc[0];
     const Ctl ctl{bar, abort_flag, p.err, p.wait_limit};
+    // token rows of the inputs (element counts for the bounds-check build)
+    const long long nrows =
+        p.sm.cu ? (long long)p.sm.H * p.sm.T_total : (long long)p.sm.N * p.sm.H * p.sm.T;
+    (void)nrows;
 
     if (warp == 4) {
         // ================================ copies (all lanes) and Gram (lane 0)
@@ -229,7 +233,7 @@ k_gdn_ut(const __grid_constant__ CUtensorMap tm_k, UtParams p) {
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const int r = lane + 32 * h;
-                const bool in = r < un.len;
+                const bool in = r < un.len && GDN_IDX_OK(un.row0 + r, 1, nrows);
                 rg[r] = in ? __ldg(p.log_alpha + un.row0 + r) : 0.f;
                 rg[64 + r] = in ? __ldg(p.beta + un.row0 + r) : 0.f;
             }
@@ -366,8 +370,9 @@ k_gdn_ut(const __grid_constant__ CUtensorMap tm_k, UtParams p) {
                             const float x = s < r ? factor(s) * gv : 0.f;
                             v[e] = (r >> 4) != (s >> 4) ? inv::tf32(x) : x;
                         }
-                        *reinterpret_cast<float4 *>(Ab + r * LDA + 4 * q) =
-                            make_float4(v[0], v[1], v[2], v[3]);
+                        if (GDN_SMEM_OK(smem_u32(Ab + r * LDA + 4 * q), 16))
+                            *reinterpret_cast<float4 *>(Ab + r * LDA + 4 * q) =
+                                make_float4(v[0], v[1], v[2], v[3]);
                     }
                 };
                 if (span_ok)
@@ -412,7 +417,7 @@ k_gdn_ut(const __grid_constant__ CUtensorMap tm_k, UtParams p) {
                             wu[e] = pack_bf16(t0, t1);
                             ww[e] = pack_bf16(t0 * gs[128 + s2], t1 * gs[128 + s2 + 1]);
                         }
-                        if (r < un.len)
+                        if (r < un.len && GDN_IDX_OK((un.row0 + r) * kU + c, 8, nrows * kU))
                             *reinterpret_cast<uint4 *>(p.Tu + (un.row0 + r) * kU + c) =
                                 make_uint4(wu[0], wu[1], wu[2], wu[3]);
                         st16(Tw + sw128_offset(r, ch), ww[0], ww[1], ww[2], ww[3]);
@@ -454,7 +459,8 @@ k_gdn_ut(const __grid_constant__ CUtensorMap tm_k, UtParams p) {
                         const float got = __shfl_xor_sync(0xffffffffu, give, 1);
                         const int row = odd ? r0 + 1 : r0;
                         const uint32_t word = odd ? pack_bf16(got, a1) : pack_bf16(a0, got);
-                        *reinterpret_cast<uint32_t *>(Ws + row * LDW + cpair) = word;
+                        if (GDN_SMEM_OK(smem_u32(Ws + row * LDW + cpair), 4))
+                            *reinterpret_cast<uint32_t *>(Ws + row * LDW + cpair) = word;
                     }
                 }
                 tc_fence_before();
@@ -464,7 +470,8 @@ k_gdn_ut(const __grid_constant__ CUtensorMap tm_k, UtParams p) {
 #pragma unroll
                 for (int j = 0; j < kU * VPR / 128; ++j) {
                     const int idx = tid + 128 * j, r = idx / VPR, q = idx % VPR;
-                    if (r < un.len)
+                    if (r < un.len && GDN_IDX_OK((un.row0 + r) * DK + 8 * q, 8, nrows * DK) &&
+                        GDN_SMEM_OK(smem_u32(Ws + r * LDW + 8 * q), 16))
                         *reinterpret_cast<uint4 *>(p.W + (un.row0 + r) * DK + 8 * q) =
                             *reinterpret_cast<const uint4 *>(Ws + r * LDW + 8 * q);
                 }
@@ -473,7 +480,8 @@ k_gdn_ut(const __grid_constant__ CUtensorMap tm_k, UtParams p) {
             }
             // ---- T_u = T diag(beta) and T_w = T diag(beta gamma), bf16 rows:
             //      thread t takes row t/2, columns 32 (t & 1) .. + 31 of both
-            if (un.len > 0) {
+            if (un.len > 0 && GDN_IDX_OK((un.out_row + (tid >> 1)) * kU, kU * kU + kU,
+                                         p.units * 2 * kU * kU)) {
                 const int r = tid >> 1, c0 = 32 * (tid & 1);
                 uint4 *du = reinterpret_cast<uint4 *>(p.Tu + (un.out_row + r) * kU + c0);
                 uint4 *dw = reinterpret_cast<uint4 *>(p.Tu + (un.out_row + kU + r) * kU + c0);

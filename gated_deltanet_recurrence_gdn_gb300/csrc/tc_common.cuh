@@ -38,7 +38,9 @@ struct Ctl {
     }
 };
 
+// 16-byte store to shared memory
 __device__ __forceinline__ void st16(uint8_t *p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    if (!GDN_SMEM_OK(smem_u32(p), 16)) return;
     *reinterpret_cast<uint4 *>(p) = make_uint4(a, b, c, d);
 }
 
@@ -61,12 +63,14 @@ __device__ __forceinline__ float f32(uint32_t u) { return __uint_as_float(u); }
 // to the async proxy (fence.proxy.async) before the storing thread issues.
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void *src, int x,
                                              int y) {
+    if (!GDN_SMEM_OK(smem_u32(src), 8192)) return;   // the box's first 8 KiB
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::
                      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(src)), "r"(x), "r"(y)
                  : "memory");
 }
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, const void *src, int x,
                                              int y, int z) {
+    if (!GDN_SMEM_OK(smem_u32(src), 8192)) return;
     asm volatile(
         "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
             reinterpret_cast<uint64_t>(map)),
@@ -93,6 +97,7 @@ __device__ __forceinline__ void put_row64_f32(uint8_t *tile, int rows, int row,
     for (int q = 0; q < 16; ++q) {
         float4 *d = reinterpret_cast<float4 *>(tile + (q >> 3) * rows * 128 +
                                                sw128_offset(row, q & 7));
+        if (!GDN_SMEM_OK(smem_u32(d), 16)) continue;
         *d = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
     }
 }

@@ -6,6 +6,8 @@
 #include <cuda.h>
 #include <stdint.h>
 
+#include "gdn_check.cuh"
+
 namespace gdn {
 namespace ptx {
 
@@ -16,6 +18,7 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
 // ------------------------------------------------------------------ mbarrier
 
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    if (!GDN_SMEM_OK(smem_u32(bar), 8)) return;
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
                  : "memory");
 }
@@ -26,16 +29,19 @@ __device__ __forceinline__ void fence_mbar_init() {
 }
 
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    if (!GDN_SMEM_OK(smem_u32(bar), 8)) return;
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    if (!GDN_SMEM_OK(smem_u32(bar), 8)) return;
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
                  "r"(bytes)
                  : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    if (!GDN_SMEM_OK(smem_u32(bar), 8)) return true;   // recorded; never wait on it
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
@@ -48,6 +54,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 }
 
 __device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+    if (!GDN_SMEM_OK(smem_u32(bar), 8)) return true;   // recorded; never wait on it
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
@@ -148,6 +155,8 @@ __device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t count, bool 
 
 __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, uint64_t *bar,
                                             int x, int y, int z) {
+    // the first 8 KiB of the box (every load map of this library has 8 KiB boxes)
+    if (!GDN_SMEM_OK(smem_u32(dst), 8192) || !GDN_SMEM_OK(smem_u32(bar), 8)) return;
     asm volatile(
         "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
@@ -157,6 +166,7 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, u
 
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar,
                                             int x, int y) {
+    if (!GDN_SMEM_OK(smem_u32(dst), 8192) || !GDN_SMEM_OK(smem_u32(bar), 8)) return;
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
@@ -190,6 +200,7 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
 // 32 lanes x 32 bit, 16 consecutive columns: thread i of the warp gets lane
 // (base lane + i), columns col..col+15.  taddr = (lane << 16) | column.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    if (!GDN_TMEM_OK(taddr, 16)) return;   // the address is warp-uniform
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
         "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
@@ -208,6 +219,7 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
 // 32 lanes x 32 bit, 32 consecutive columns.  The registers are valid only
 // after tmem_wait32 on them (several loads may be in flight before it).
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    if (!GDN_TMEM_OK(taddr, 32)) return;   // the address is warp-uniform
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 " GDN_OPS32 ", [%32];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
                    "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
@@ -258,6 +270,12 @@ enum : uint32_t { kSwizzleNone = 0, kSwizzle128B = 2, kSwizzle64B = 4, kSwizzle3
 
 __device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr, uint32_t lbo_bytes,
                                                uint32_t sbo_bytes, uint32_t swizzle) {
+#ifdef GDN_BOUNDS_CHECK
+    // an operand starts at least one 64-row tile of 128-byte rows before the
+    // end of the CTA's shared memory; else it is recorded and re-pointed there
+    if (!GDN_SMEM_OK(saddr, 8192))
+        saddr = static_cast<uint32_t>(__cvta_generic_to_shared(::gdn::chk::gdn_chk_dyn_smem));
+#endif
     uint64_t d = 0;
     d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
     d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16;

@@ -55,7 +55,8 @@ typedef enum {
     GDN_ERR_ALIGNMENT = 3,      /* a pointer is not 16-byte aligned */
     GDN_ERR_CUDA = 4,           /* a CUDA runtime call or launch failed */
     GDN_ERR_DEVICE_TIMEOUT = 5, /* a bounded device-side wait gave up */
-    GDN_ERR_TOO_LARGE = 6       /* gdn_fwd_noalloc: the call needs more than its fixed scratch */
+    GDN_ERR_TOO_LARGE = 6,      /* gdn_fwd_noalloc: the call needs more than its fixed scratch */
+    GDN_ERR_BOUNDS = 7          /* bounds-check build only: an index check failed */
 } gdn_status;
 
 typedef enum {
@@ -134,9 +135,22 @@ const char *gdn_status_string(gdn_status s);
 /*
  * Synchronises `stream`, then reads and clears the device error word of the
  * current device.  Returns GDN_OK, GDN_ERR_DEVICE_TIMEOUT, GDN_ERR_INVALID_ARG
- * (bad cu_seqlens seen by a kernel) or GDN_ERR_CUDA.
+ * (bad cu_seqlens seen by a kernel), GDN_ERR_BOUNDS (a library built with
+ * -DGDN_BOUNDS_CHECK recorded a failed index check; see gdn_bounds_violation)
+ * or GDN_ERR_CUDA.
  */
 gdn_status gdn_sync_check(void *stream);
+
+/*
+ * The debug bounds-check build (-DGDN_BOUNDS_CHECK): the tcgen05 and
+ * chunk-prep kernels check their shared-memory, tensor-memory and global
+ * indices, skip any access that fails and record the source line of the first
+ * failure ("Gated DeltaNet GPU并行实现", section 5.2, second pitfall: index and
+ * alignment errors in bulk-copy inputs are otherwise silent).  Returns that
+ * line on the current device (0: no failure; the caller synchronises first),
+ * clearing it if `clear` != 0; -1 in a normal build, which checks nothing.
+ */
+int gdn_bounds_violation(int clear);
 
 /*
  * Implementation selection (process-wide; for tests and benchmarks).

@@ -42,7 +42,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings(lib):
-    for s in range(7):
+    for s in range(8):
         assert lib.gdn_status_string(s).decode().startswith("GDN_")
     assert lib.gdn_status_string(99) == b"unknown gdn_status"
 
