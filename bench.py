@@ -74,6 +74,9 @@ def parse():
                     help="gated linear attention: the recurrence without the erase term")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle sample")
+    ap.add_argument("--host-link", action="store_true",
+                    help="measure the host <-> device copy rates that bound the e2e figure "
+                         "(pinned and pageable, one and several streams) and exit")
     return ap.parse_args()
 
 
@@ -201,12 +204,12 @@ def load_peaks():
 
 # the sources each timed kernel is built from (its file and the headers it includes)
 KERNEL_SOURCES = {
-    "k_gdn_fused": ["gdn_fused.cu", "tc_common.cuh", "tc_ptx.cuh", "gdn_internal.h"],
-    "k_gdn_ut": ["gdn_ut.cu", "gdn_inv.cuh", "tc_common.cuh", "tc_ptx.cuh", "gdn_internal.h"],
-    "k_gdn_tc": ["gdn_tc.cu", "gdn_bwd_tc.h", "tc_common.cuh", "tc_ptx.cuh", "gdn_internal.h"],
-    "k_bwd_dstate_tc": ["gdn_bwd_tc.cu", "gdn_bwd_tc.h", "tc_common.cuh", "tc_ptx.cuh",
+    "k_gdn_fused": ["gdn_fused.cu", "tc_common.cuh", "tc_ptx.cuh", "gdn_check.cuh", "gdn_internal.h"],
+    "k_gdn_ut": ["gdn_ut.cu", "gdn_inv.cuh", "tc_common.cuh", "tc_ptx.cuh", "gdn_check.cuh", "gdn_internal.h"],
+    "k_gdn_tc": ["gdn_tc.cu", "gdn_bwd_tc.h", "tc_common.cuh", "tc_ptx.cuh", "gdn_check.cuh", "gdn_internal.h"],
+    "k_bwd_dstate_tc": ["gdn_bwd_tc.cu", "gdn_bwd_tc.h", "tc_common.cuh", "tc_ptx.cuh", "gdn_check.cuh",
                         "gdn_internal.h"],
-    "k_gdn_prep": ["gdn_prep.cu", "gdn_inv.cuh", "gdn_bwd_tc.h", "tc_ptx.cuh",
+    "k_gdn_prep": ["gdn_prep.cu", "gdn_inv.cuh", "gdn_bwd_tc.h", "tc_ptx.cuh", "gdn_check.cuh",
                    "gdn_internal.h"],
     "k_gdn_decode": ["gdn_decode.cu", "gdn_internal.h"],
     "k_bwd_chunk": ["gdn_bwd.cu", "gdn_internal.h", "gdn_mma.cuh", "gdn_tile.cuh"],
@@ -659,9 +662,80 @@ def run_reference(args, world, rank):
     }
 
 
+def host_link(nbytes=256 << 20, reps=5):
+    """Copy rates between host and device memory (GB/s, best of `reps`, CUDA
+    events on the copying streams): what bounds `e2e`, whose timed region
+    moves the step's inputs up and its outputs down."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    d = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    d2 = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    pin = torch.ones(nbytes, dtype=torch.uint8).pin_memory()
+    pin2 = torch.ones(nbytes, dtype=torch.uint8).pin_memory()
+    pag = torch.ones(nbytes, dtype=torch.uint8)
+
+    def rate(fn, moved):
+        fn()
+        torch.cuda.synchronize()
+        best = float("inf")
+        for _ in range(reps):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            best = min(best, a.elapsed_time(b))
+        return moved / (best * 1e-3) / 1e9
+
+    def split(n, pairs):
+        # n streams, each copying its share of every (dst, src) pair
+        cur = torch.cuda.current_stream()
+        streams = [torch.cuda.Stream() for _ in range(n)]
+
+        def run():
+            ev = cur.record_event()
+            for i, st in enumerate(streams):
+                st.wait_event(ev)
+                with torch.cuda.stream(st):
+                    for dst, src in pairs:
+                        part = dst.numel() // n
+                        dst[i * part:(i + 1) * part].copy_(src[i * part:(i + 1) * part],
+                                                           non_blocking=True)
+            for st in streams:
+                cur.wait_stream(st)
+        return run
+
+    out = {"bytes_per_copy": nbytes}
+    out["h2d_pinned_gbs"] = rate(lambda: d.copy_(pin, non_blocking=True), nbytes)
+    out["d2h_pinned_gbs"] = rate(lambda: pin.copy_(d, non_blocking=True), nbytes)
+    out["h2d_pageable_gbs"] = rate(lambda: d.copy_(pag), nbytes)
+    out["d2h_pageable_gbs"] = rate(lambda: pag.copy_(d), nbytes)
+    for n in (2, 4, 8):
+        out["h2d_pinned_%d_streams_gbs" % n] = rate(split(n, [(d, pin)]), nbytes)
+    both = [torch.cuda.Stream(), torch.cuda.Stream()]
+
+    def up_and_down():
+        cur = torch.cuda.current_stream()
+        ev = cur.record_event()
+        for st in both:
+            st.wait_event(ev)
+        with torch.cuda.stream(both[0]):
+            d.copy_(pin, non_blocking=True)
+        with torch.cuda.stream(both[1]):
+            pin2.copy_(d2, non_blocking=True)
+        for st in both:
+            cur.wait_stream(st)
+    out["h2d_plus_d2h_at_once_gbs"] = rate(up_and_down, 2 * nbytes)
+    return {k: (round(v, 1) if isinstance(v, float) else v) for k, v in out.items()}
+
+
 def main():
     global NO_ERASE, BACKWARD, VECTOR_GATE
     args = parse()
+    if args.host_link:
+        torch.cuda.set_device(0)
+        print(json.dumps({"host_link": host_link()}), flush=True)
+        return
     NO_ERASE = args.no_erase
     BACKWARD = args.backward
     VECTOR_GATE = args.vector_gate
