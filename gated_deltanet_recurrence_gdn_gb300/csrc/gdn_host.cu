@@ -74,7 +74,9 @@ extern "C" gdn_status gdn_fwd_host(const void *q, const void *k, const void *v,
     const long long BH = (long long)B * H;
     const size_t es = dt == GDN_BF16 ? 2 : 4;
     // slices: chunk-aligned lengths, the last one possibly shorter
-    int S = T == 0 ? 1 : (T + kSliceTarget - 1) / kSliceTarget;
+    const long long opt_slice = option(GDN_OPT_HOST_SLICE);
+    const int target = opt_slice > 0 ? (int)((opt_slice + kChunk - 1) / kChunk * kChunk) : kSliceTarget;
+    int S = T == 0 ? 1 : (T + target - 1) / target;
     S = S < 1 ? 1 : (S > kMaxSlices ? kMaxSlices : S);
     const int Ts = T == 0 ? 0 : ((T + S - 1) / S + kChunk - 1) / kChunk * kChunk;
     S = T == 0 ? 1 : (T + Ts - 1) / Ts;

@@ -175,9 +175,19 @@ int gdn_bounds_violation(int clear);
  *                      in bf16 and fp32) when it is handed out, so that a read
  *                      of scratch no kernel wrote shows up in the results; 0
  *                      (default) leaves it as the pool returns it.
+ *   GDN_OPT_HOST_SLICE: target tokens per time slice of gdn_fwd_host (0 =
+ *                      default; rounded up to a multiple of the chunk).
+ *                      Shorter slices overlap the copies of neighbouring
+ *                      slices better and cost more launches.
  * Returns GDN_ERR_INVALID_ARG for an unknown key or value.
  */
-enum { GDN_OPT_IMPL = 0, GDN_OPT_SEGMENTS = 1, GDN_OPT_WAIT_LIMIT = 2, GDN_OPT_POISON_SCRATCH = 3 };
+enum {
+    GDN_OPT_IMPL = 0,
+    GDN_OPT_SEGMENTS = 1,
+    GDN_OPT_WAIT_LIMIT = 2,
+    GDN_OPT_POISON_SCRATCH = 3,
+    GDN_OPT_HOST_SLICE = 4
+};
 enum { GDN_IMPL_AUTO = 0, GDN_IMPL_SIMT = 1, GDN_IMPL_TC = 2, GDN_IMPL_TC_FUSED = 3 };
 gdn_status gdn_set_option(int key, long long value);
 long long gdn_get_option(int key);
