@@ -206,6 +206,7 @@ def load_peaks():
 KERNEL_SOURCES = {
     "k_gdn_fused": ["gdn_fused.cu", "tc_common.cuh", "tc_ptx.cuh", "gdn_check.cuh", "gdn_internal.h"],
     "k_gdn_ut": ["gdn_ut.cu", "gdn_inv.cuh", "tc_common.cuh", "tc_ptx.cuh", "gdn_check.cuh", "gdn_internal.h"],
+    "k_gdn_utw": ["gdn_ut.cu", "gdn_inv.cuh", "tc_common.cuh", "tc_ptx.cuh", "gdn_check.cuh", "gdn_internal.h"],
     "k_gdn_tc": ["gdn_tc.cu", "gdn_bwd_tc.h", "tc_common.cuh", "tc_ptx.cuh", "gdn_check.cuh", "gdn_internal.h"],
     "k_bwd_dstate_tc": ["gdn_bwd_tc.cu", "gdn_bwd_tc.h", "tc_common.cuh", "tc_ptx.cuh", "gdn_check.cuh",
                         "gdn_internal.h"],

@@ -165,6 +165,75 @@ __device__ __forceinline__ void invert64(const float *Ab, float *Tb, int tid, Ba
     bar();
 }
 
+// T = (I + A)^{-1} in place: on entry AT holds A with every row written in
+// full (zeros on and above the diagonal, entries outside the 16x16 diagonal
+// blocks rounded to tf32); on exit it holds T's lower triangle, and its
+// upper-right 32x32 block (rows 0-31, columns 32-63: zeros of A) holds the
+// merges' scratch, as invert64 leaves it.  Each step overwrites only entries
+// of A that no later step reads: a diagonal block's 16 threads (one warp)
+// sync before writing T over it, and the 16 -> 32 merge completes every
+// X = A_10 T_00 before any T_10 = -T_11 X lands on A_10.
+template <typename Bar>
+__device__ __forceinline__ void invert64_inplace(float *AT, int tid, Bar bar) {
+    const int w = tid >> 5, lane = tid & 31;
+    if (w < 2) {
+        const int blk = tid >> 4, cc = tid & 15, o = blk * 16;
+        float x[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            const float4 *row = reinterpret_cast<const float4 *>(AT + (o + r) * LDA + o);
+            float acc = (r == cc) ? 1.f : 0.f;
+#pragma unroll
+            for (int q = 0; 4 * q < r; ++q) {
+                const float4 a4 = row[q];
+                const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (4 * q + e < r) acc = fmaf(-av[e], x[4 * q + e], acc);
+            }
+            x[r] = acc;
+        }
+        __syncwarp();   // the block's 16 threads (this warp) have read it
+#pragma unroll
+        for (int r = 0; r < 16; ++r)
+            if (GDN_SMEM_OK(saddr(AT + (o + r) * LDA + o + cc), 4))
+                AT[(o + r) * LDA + o + cc] = tf32(x[r]);
+    }
+    bar();
+    {
+        const int pr = w >> 1, nh = w & 1;
+        const int ro = 32 * pr + 16, co = 32 * pr;
+        float *Xw = AT + (16 * pr) * LDA + 32 + 8 * nh;
+        float c4[4];
+        tile_mma<16>(c4, AT + ro * LDA + co, LDA, AT + co * LDA + co + 8 * nh, LDA, lane, nh);
+        store_tile(Xw, LDA, c4, lane, 1.f);
+        bar();   // both halves of X read all of A_10
+        tile_mma<16>(c4, AT + ro * LDA + ro, LDA, Xw, LDA, lane);
+        store_tile(AT + ro * LDA + co + 8 * nh, LDA, c4, lane, -1.f);
+    }
+    bar();
+    {
+        float *Xb = AT + 32;
+        const int mt = w >> 1, nt0 = 2 * (w & 1);
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            float c4[4];
+            tile_mma<32>(c4, AT + (32 + 16 * mt) * LDA, LDA, AT + 8 * (nt0 + q), LDA, lane,
+                         nt0 + q);
+            store_tile(Xb + 16 * mt * LDA + 8 * (nt0 + q), LDA, c4, lane, 1.f);
+        }
+        bar();
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            float c4[4];
+            tile_mma<32>(c4, AT + (32 + 16 * mt) * LDA + 32, LDA, Xb + 8 * (nt0 + q), LDA, lane,
+                         0, 2 + 2 * mt);
+            store_tile(AT + (32 + 16 * mt) * LDA + 8 * (nt0 + q), LDA, c4, lane, -1.f);
+        }
+    }
+    bar();
+}
+
 // Element (r, s) of T from the buffer invert64 leaves (zero above the diagonal
 // and in the scratch block).
 __device__ __forceinline__ float t_at(const float *Tb, int r, int s) {

@@ -58,6 +58,11 @@ def test_options_roundtrip(lib):
     assert lib.gdn_get_option(gdn.GDN_OPT_POISON_SCRATCH) == 1
     assert lib.gdn_set_option(gdn.GDN_OPT_POISON_SCRATCH, 2) == gdn.GDN_ERR_INVALID_ARG
     assert lib.gdn_set_option(gdn.GDN_OPT_POISON_SCRATCH, prev) == gdn.GDN_OK
+    prev = lib.gdn_get_option(gdn.GDN_OPT_HOST_SLICE)
+    assert lib.gdn_set_option(gdn.GDN_OPT_HOST_SLICE, 1024) == gdn.GDN_OK
+    assert lib.gdn_get_option(gdn.GDN_OPT_HOST_SLICE) == 1024
+    assert lib.gdn_set_option(gdn.GDN_OPT_HOST_SLICE, -1) == gdn.GDN_ERR_INVALID_ARG
+    assert lib.gdn_set_option(gdn.GDN_OPT_HOST_SLICE, prev) == gdn.GDN_OK
 
 
 # Host-only validation: these calls must return before any CUDA call, so fake

@@ -60,3 +60,19 @@ def test_host_empty_sequence_gives_h0():
     x = synth.make_dense(2, 3, 0, 64, 64, io="bf16", h0_std=0.3, seed=1, device="cuda")
     o, hT = gdn.gdn_fwd_host(*host_inputs(x))
     assert o.numel() == 0 and torch.equal(hT, x.h0.cpu())
+
+
+@pytest.mark.parametrize("slice_tokens", [64, 100, 320, 4096])
+def test_host_slice_lengths_equal_device_call(slice_tokens):
+    # GDN_OPT_HOST_SLICE changes only how the pipeline cuts T (rounded up to a
+    # chunk multiple; at most 32 slices): the result stays bit-identical
+    x = synth.make_dense(2, 2, 1000, 128, 128, io="bf16", h0_std=0.02, seed=21, device="cuda")
+    prev = gdn.get_option(gdn.GDN_OPT_HOST_SLICE)
+    try:
+        with gdn.use_impl(gdn.GDN_IMPL_AUTO, 1):
+            o_d, h_d = gdn.gdn_fwd(x.q, x.k, x.v, x.log_alpha, x.beta, x.h0, check=True)
+            gdn.set_option(gdn.GDN_OPT_HOST_SLICE, slice_tokens)
+            o_h, h_h = gdn.gdn_fwd_host(*host_inputs(x))
+    finally:
+        gdn.set_option(gdn.GDN_OPT_HOST_SLICE, prev)
+    assert torch.equal(o_h, o_d.cpu()) and torch.equal(h_h, h_d.cpu())
