@@ -120,6 +120,7 @@ enum {
     B_M34,                      // dH and O done
     B_DRAIN,                    // chain MMA issuer drained
     B_DRAIN2,                   // prep MMA issuer drained
+    B_M34I,                     // K^T V~ and the output MMA of the chunk issued
     B_COUNT
 };
 
@@ -729,6 +730,7 @@ __device__ __forceinline__ void gdn_tc_body(const CUtensorMap *tm_q, const CUten
                 mma_commit(bar + B_M34);
                 mma_commit(bar + B_PFREE + (j & 1));
                 mma_commit(bar + B_FREE + (j % kNS));
+                mbar_arrive(bar + B_M34I);
                 TRACE(2, j, 3, true);
             }
             // every issued MMA has finished before TMEM is released
@@ -747,6 +749,10 @@ __device__ __forceinline__ void gdn_tc_body(const CUtensorMap *tm_q, const CUten
                 const uint32_t soff = s * L::STAGE;
                 if (!ctl.wait(B_READY + s, (j / kNS) & 1)) break;
                 if (j > 0 && !ctl.wait(B_GFREE, (j - 1) & 1)) break;   // G of j-1 consumed
+                // the tensor pipe runs MMAs in issue order: this chunk's Gram
+                // and U go behind the previous chunk's state and output MMAs
+                // (K^T V~, P' V'), which the chain waits for, not ahead of them
+                if (j > 0 && !ctl.wait(B_M34I, (j - 1) & 1)) break;
                 TRACE(3, j, 0, true);
                 tc_fence_after();
                 // the Gram first: P is the longer path to the output MMA
