@@ -121,6 +121,7 @@ enum {
     B_DRAIN,                    // chain MMA issuer drained
     B_DRAIN2,                   // prep MMA issuer drained
     B_M34I,                     // K^T V~ and the output MMA of the chunk issued
+    B_HPUB,                     // bf16 H of the chunk in smem (chain -> chain MMA issuer)
     B_COUNT
 };
 
@@ -200,9 +201,6 @@ __device__ __forceinline__ void gdn_tc_body(const CUtensorMap *tm_q, const CUten
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + L::OFF_BAR);
     uint32_t *misc = reinterpret_cast<uint32_t *>(sm + L::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(misc + 1);
-    // chunk index + 1 of the last H / V' the chain published (read by the
-    // output MMA issuer)
-    uint32_t *h_flag = misc + 2, *vn_flag = misc + 3;
     float *gb = reinterpret_cast<float *>(sm + L::OFF_G);   // [2][GSZ]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -256,8 +254,6 @@ __device__ __forceinline__ void gdn_tc_body(const CUtensorMap *tm_q, const CUten
         for (int s = 0; s < kNS; ++s) mbar_init(bar + B_FREE + s, 3);   // chain MMA + 2 prep groups
         for (int s = 0; s < kNS; ++s) mbar_init(bar + B_FULL + s, 33);   // TMA tx + 32 gate lanes
         *abort_flag = 0;
-        *h_flag = 0;
-        *vn_flag = 0;
         fence_mbar_init();
     }
     tc_fence_before();
@@ -336,7 +332,7 @@ __device__ __forceinline__ void gdn_tc_body(const CUtensorMap *tm_q, const CUten
             tc_fence_before();
             if (STATES && t == 0) bulk_wait_read();   // the staging tile is free
             named_bar(1, 128);
-            if (t == 0) st_release_cta(h_flag, (uint32_t)j + 1);
+            if (t == 0) mbar_arrive(bar + B_HPUB);
             TRACE(0, j, 1, t == 0);
             if (STATES) {   // the chunk's starting state, for the backward
                 if (t < DK) put_row64_f32(sm + L::OFF_STG, DK, t, hreg);
@@ -419,7 +415,6 @@ __device__ __forceinline__ void gdn_tc_body(const CUtensorMap *tm_q, const CUten
             tc_fence_before();
             named_bar(1, 128);
             if (t == 0) {
-                st_release_cta(vn_flag, (uint32_t)j + 1);
                 mbar_arrive(bar + B_VN);
                 if (STATES && bulk_v) {
                     const int y = ytok0 + j * kC;
@@ -706,7 +701,7 @@ __device__ __forceinline__ void gdn_tc_body(const CUtensorMap *tm_q, const CUten
             for (int j = 0; j < nch; ++j) {
                 const uint32_t soff = (j % kNS) * L::STAGE;
                 const uint32_t acc = tmem + TM_M2 + (j & 1) * 64;
-                if (!ctl.wait(B_WQ, j & 1) || !ctl.flag(h_flag, (uint32_t)j + 1)) break;
+                if (!ctl.wait(B_WQ, j & 1) || !ctl.wait(B_HPUB, j & 1)) break;
                 TRACE(2, j, 0, true);
                 tc_fence_after();
 #pragma unroll
@@ -717,7 +712,7 @@ __device__ __forceinline__ void gdn_tc_body(const CUtensorMap *tm_q, const CUten
                 mma_commit(bar + B_M2);
                 TRACE(2, j, 1, true);
                 if (!ctl.wait(B_PREADY + (j & 1), (j >> 1) & 1)) break;   // P of this chunk
-                if (!ctl.flag(vn_flag, (uint32_t)j + 1)) break;
+                if (!ctl.wait(B_VN, j & 1)) break;   // V' of this chunk
                 TRACE(2, j, 2, true);
                 tc_fence_after();
                 const uint64_t dP = (j & 1) ? dVN : dVT;   // [x; P] starts at the region base
