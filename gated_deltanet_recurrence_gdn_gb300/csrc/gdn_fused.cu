@@ -212,6 +212,10 @@ k_gdn_fused(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + L::OFF_BAR);
     uint32_t *misc = reinterpret_cast<uint32_t *>(sm + L::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(misc + 1);
+    // chunks whose Gram warps 6-7 have seen complete: a count, so that the
+    // wide-span branch of warps 4-5, which waits for the Gram only in some
+    // chunks, cannot mistake an older phase of its mbarrier for this one
+    uint32_t *g_seen = misc + 2;
     auto GA = [&](int s) { return reinterpret_cast<float *>(sm + L::OFF_GA + s * 1024); };
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -264,6 +268,7 @@ k_gdn_fused(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             mbar_init(bar + E_KQ + s, 3);
         }
         *abort_flag = 0;
+        *g_seen = 0;
         fence_mbar_init();
     }
     tc_fence_before();
@@ -403,7 +408,7 @@ k_gdn_fused(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             //      in place once the Gram has read Q; otherwise the output rows
             //      take gamma_r when stored
             if (ga[63] <= -80.f) {
-                if (!named_bar_and(2, 64, ctl.wait(B_GDONE, j & 1))) break;
+                if (!named_bar_and(2, 64, ctl.flag(g_seen, (uint32_t)j + 1))) break;
                 const float gr = ga[64 + r];
                 const float f[8] = {gr, gr, gr, gr, gr, gr, gr, gr};
 #pragma unroll
@@ -485,6 +490,7 @@ k_gdn_fused(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 alive = false;
                 break;
             }
+            if (r == 0) st_release_cta(g_seen, (uint32_t)j + 1);
             if (r == 0) FTRACE(2, j, 0);
             tc_fence_after();
             {

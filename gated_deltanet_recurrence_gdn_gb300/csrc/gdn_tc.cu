@@ -201,6 +201,10 @@ __device__ __forceinline__ void gdn_tc_body(const CUtensorMap *tm_q, const CUten
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + L::OFF_BAR);
     uint32_t *misc = reinterpret_cast<uint32_t *>(sm + L::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(misc + 1);
+    // chunks whose Gram warps 6-7 have seen complete: a count, so that the
+    // wide-span branch of warps 4-5, which waits for the Gram only in some
+    // chunks, cannot mistake an older phase of its mbarrier for this one
+    uint32_t *g_seen = misc + 2;
     float *gb = reinterpret_cast<float *>(sm + L::OFF_G);   // [2][GSZ]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -254,6 +258,7 @@ __device__ __forceinline__ void gdn_tc_body(const CUtensorMap *tm_q, const CUten
         for (int s = 0; s < kNS; ++s) mbar_init(bar + B_FREE + s, 3);   // chain MMA + 2 prep groups
         for (int s = 0; s < kNS; ++s) mbar_init(bar + B_FULL + s, 33);   // TMA tx + 32 gate lanes
         *abort_flag = 0;
+        *g_seen = 0;
         fence_mbar_init();
     }
     tc_fence_before();
@@ -562,7 +567,7 @@ __device__ __forceinline__ void gdn_tc_body(const CUtensorMap *tm_q, const CUten
                 TRACE(1, j, 7, t == 0);
                 if (!span_ok) {
                     // the Gram must read the unscaled Q first
-                    if (!named_bar_and(4, 64, ctl.wait(B_G, j & 1))) break;
+                    if (!named_bar_and(4, 64, ctl.flag(g_seen, (uint32_t)j + 1))) break;
                     scale_q();
                     fence_proxy_async_smem();
                     named_bar(4, 64);
@@ -583,6 +588,7 @@ __device__ __forceinline__ void gdn_tc_body(const CUtensorMap *tm_q, const CUten
                 okg = okg && ctl.wait(B_G, j & 1);
                 if (j >= 2) okg = okg && ctl.wait(B_PFREE + (j & 1), ((j - 2) >> 1) & 1);
                 if (!named_bar_and(3, 64, okg)) break;
+                if (t == 64) st_release_cta(g_seen, (uint32_t)j + 1);
                 TRACE(1, j, 3, t == 64);
                 tc_fence_after();
                 const int r = t - 64;

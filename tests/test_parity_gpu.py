@@ -5,6 +5,8 @@ cases run at full size in the launch configuration the benchmark times and
 compare either every output (when the oracle finishes in seconds) or a
 sampled subset of heads / sequences / a causal prefix.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -156,6 +158,54 @@ def test_scratch_pool_release_and_reuse(impl):
     o3, h3 = run_dense(x, impl)
     assert torch.equal(o1, o2) and torch.equal(h1, h2)
     assert torch.equal(o1, o3) and torch.equal(h1, h3)
+
+
+# ------------------------------------------------------------ steep decay
+#
+# Where a chunk's total log decay g_C is below -80, exp(-g_s) could overflow:
+# the chunk-prep kernels then form A with one exponential per entry, and the
+# chunk loop scales Q by gamma in place and forms P exactly.  The synthetic
+# gates never reach that (about -25 per chunk), so these cases set log gates
+# of -3 per step (g_C about -190) and -1.3 (about -83, just past the switch)
+# in some chunks and keep the synthetic ones elsewhere.
+
+
+def _steep(la, T):
+    la = la.clone()
+    la[..., 64:min(T, 128)] = -3.0
+    if T > 128:
+        la[..., 128:min(T, 192)] = -1.3
+    if T > 192:
+        la[..., 192:min(T, 256)] = -3.0
+    return la
+
+
+@pytest.mark.parametrize("impl", ["simt", "tc", "fused"])
+@pytest.mark.parametrize("dk,dv", [(128, 128), (64, 64), (128, 256)])
+def test_steep_decay_matches_oracle(impl, dk, dv):
+    x = synth.make_dense(1, 2, 4 * 64 + 9, dk, dv, io="bf16", h0_std=0.1, seed=91 + dk + dv,
+                         device="cuda")
+    x = dataclasses.replace(x, log_alpha=_steep(x.log_alpha, x.log_alpha.shape[-1]))
+    o, hT = run_dense(x, impl)
+    o_ref, h_ref = U.oracle_dense(x)
+    check(o, hT, o_ref.reshape(o.shape), h_ref.reshape(hT.shape), "bf16")
+
+
+@pytest.mark.parametrize("impl", ["simt", "tc", "fused"])
+def test_steep_decay_varlen_matches_oracle(impl):
+    import oracle
+    y = synth.make_varlen([300, 40, 200], 2, 128, 128, io="bf16", h0_std=0.1, seed=97,
+                          device="cuda")
+    # steep chunks inside the first and the third sequence
+    la = y.log_alpha.clone()
+    la[..., 64:128] = -3.0
+    la[..., 340 + 64:340 + 128] = -1.3
+    y = dataclasses.replace(y, log_alpha=la)
+    o, hT = run_varlen(y, impl)
+    o_ref, h_ref = oracle.gdn_fwd_varlen(U.f64(y.q), U.f64(y.k), U.f64(y.v), U.f64(y.log_alpha),
+                                         U.f64(y.beta), y.cu_seqlens.cpu().numpy(),
+                                         U.f64(y.h0))
+    check(o, hT, o_ref, h_ref, "bf16")
 
 
 # ------------------------------------------------------------ segment scan
