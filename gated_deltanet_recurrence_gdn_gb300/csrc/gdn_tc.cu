@@ -201,7 +201,7 @@ __device__ __forceinline__ void gdn_tc_body(const CUtensorMap *tm_q, const CUten
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + L::OFF_BAR);
     uint32_t *misc = reinterpret_cast<uint32_t *>(sm + L::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(misc + 1);
-    // chunks whose Gram warps 6-7 have seen complete: a count, so that the
+    // chunks whose Gram warps 6-7 have read (P formed): a count, so that the
     // wide-span branch of warps 4-5, which waits for the Gram only in some
     // chunks, cannot mistake an older phase of its mbarrier for this one
     uint32_t *g_seen = misc + 2;
@@ -588,7 +588,6 @@ __device__ __forceinline__ void gdn_tc_body(const CUtensorMap *tm_q, const CUten
                 okg = okg && ctl.wait(B_G, j & 1);
                 if (j >= 2) okg = okg && ctl.wait(B_PFREE + (j & 1), ((j - 2) >> 1) & 1);
                 if (!named_bar_and(3, 64, okg)) break;
-                if (t == 64) st_release_cta(g_seen, (uint32_t)j + 1);
                 TRACE(1, j, 3, t == 64);
                 tc_fence_after();
                 const int r = t - 64;
@@ -624,6 +623,7 @@ __device__ __forceinline__ void gdn_tc_body(const CUtensorMap *tm_q, const CUten
                     mbar_arrive(bar + B_PREADY + (j & 1));
                     mbar_arrive(bar + B_GFREE);
                     mbar_arrive(bar + B_FREE + s);
+                    st_release_cta(g_seen, (uint32_t)j + 1);   // off the P path
                 }
                 TRACE(1, j, 4, t == 64);
             }
