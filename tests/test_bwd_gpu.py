@@ -161,15 +161,16 @@ def test_bwd_vector_gate_and_forced_tc_outside_its_shapes_are_unsupported():
 
 
 @pytest.mark.parametrize("impl", [gdn.GDN_IMPL_AUTO, gdn.GDN_IMPL_SIMT], ids=["auto", "simt"])
-def test_bwd_steep_decay_matches_oracle(impl):
-    # log gates of -3 per step in the second and fourth chunks: their total log
-    # decay is below -80, where exp(-g_s) would overflow, so those chunks take
-    # the unscaled-dO branch of the tensor-core state adjoint; the others the
-    # gamma dO one
+@pytest.mark.parametrize("steep", [(1, 3), (1, 2, 3)], ids=["apart", "consecutive"])
+def test_bwd_steep_decay_matches_oracle(impl, steep):
+    # log gates of -3 per step in some chunks: their total log decay is below
+    # -80, where exp(-g_s) would overflow, so those chunks take the
+    # unscaled-dO branch of the tensor-core state adjoint (and the wide-span
+    # branch of the state pass); the others the gamma dO one
     x = synth.make_dense(1, 2, 256, 128, 128, io="bf16", h0_std=0.1, seed=83, device="cuda")
     la = x.log_alpha.clone()
-    la[..., 64:128] = -3.0
-    la[..., 192:256] = -3.0
+    for c in steep:
+        la[..., 64 * c:64 * (c + 1)] = -3.0
     dout, dhT = _weights(x, 84)
     with gdn.use_impl(impl):
         got = gdn.gdn_bwd(x.q, x.k, x.v, la, x.beta, x.h0, dout, dhT, check=True)
