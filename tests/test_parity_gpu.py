@@ -191,6 +191,31 @@ def test_steep_decay_matches_oracle(impl, dk, dv):
     check(o, hT, o_ref.reshape(o.shape), h_ref.reshape(hT.shape), "bf16")
 
 
+def test_steep_decay_fp32_io_matches_oracle():
+    # the general path with fp32 I/O (3xTF32 products) through the same chunks
+    x = synth.make_dense(1, 2, 4 * 64 + 9, 64, 64, io="f32", h0_std=0.1, seed=95, device="cuda")
+    x = dataclasses.replace(x, log_alpha=_steep(x.log_alpha, x.log_alpha.shape[-1]))
+    o, hT = run_dense(x, "simt")
+    o_ref, h_ref = U.oracle_dense(x)
+    check(o, hT, o_ref.reshape(o.shape), h_ref.reshape(hT.shape), "f32")
+
+
+@pytest.mark.parametrize("impl", ["simt", "tc"])
+def test_steep_decay_no_erase_matches_oracle(impl):
+    # gated linear attention (no erase term) through the same chunks
+    import oracle
+    x = synth.make_dense(1, 2, 4 * 64 + 9, 128, 128, io="bf16", h0_std=0.1, seed=96,
+                         device="cuda")
+    x = dataclasses.replace(x, log_alpha=_steep(x.log_alpha, x.log_alpha.shape[-1]))
+    with gdn.use_impl(IMPLS[impl]):
+        o, hT = gdn.gdn_fwd(x.q, x.k, x.v, x.log_alpha, x.beta, x.h0, check=True, erase=False)
+    U.sync()
+    o_ref, h_ref = oracle.gdn_fwd(U.f64(x.q), U.f64(x.k), U.f64(x.v), U.f64(x.log_alpha),
+                                  U.f64(x.beta), U.f64(x.h0), threads=U.ORACLE_THREADS,
+                                  erase=False)
+    check(o, hT, o_ref, h_ref, "bf16")
+
+
 @pytest.mark.parametrize("impl", ["simt", "tc", "fused"])
 def test_steep_decay_varlen_matches_oracle(impl):
     import oracle
