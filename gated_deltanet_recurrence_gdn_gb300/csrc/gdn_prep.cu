@@ -109,9 +109,6 @@ k_gdn_prep(const __nv_bfloat16 *__restrict__ k, const float *__restrict__ log_al
     __nv_bfloat16 *Tw = reinterpret_cast<__nv_bfloat16 *>(smem + L::OFF_A);
     __nv_bfloat16 *Ws = reinterpret_cast<__nv_bfloat16 *>(smem + L::OFF_T);
 
-    // the fused kernel that follows may be scheduled on SMs this grid leaves
-    // (it waits for this grid's completion before reading T_u / W)
-    griddep_launch_dependents();
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, t = lane & 3;
     constexpr int VPR = DK / 8;   // 16-byte vectors per K row
@@ -367,6 +364,11 @@ k_gdn_prep(const __nv_bfloat16 *__restrict__ k, const float *__restrict__ log_al
         r0 = r0n;
         Lc = Lcn;
     }
+    // the chunk loop that follows may launch once every CTA is here (it waits
+    // for this grid's completion before reading T_u / W); triggered at the
+    // start, its CTAs were placed on SMs as this grid's left them, which
+    // measured slower than the launch's own placement
+    griddep_launch_dependents();
 }
 
 // Gated linear attention (no erase term): A = 0, so T = I, T_u = diag(beta)

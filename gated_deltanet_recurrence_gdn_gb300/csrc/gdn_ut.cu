@@ -171,9 +171,6 @@ k_gdn_ut(const __grid_constant__ CUtensorMap tm_k, UtParams p) {
     float *Tb = reinterpret_cast<float *>(sm + L::OFF_T);
     float *gs = reinterpret_cast<float *>(sm + L::OFF_GS);
 
-    // the fused kernel that follows may start its own prologue now (it waits
-    // for this grid before it reads T_u)
-    griddep_launch_dependents();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 #ifdef GDN_TRACE_TIMELINE
     if (tid == 0 && blockIdx.x < 2048) {
@@ -388,6 +385,10 @@ k_gdn_ut(const __grid_constant__ CUtensorMap tm_k, UtParams p) {
     __syncthreads();
     tc_fence_after();
     if (warp == 4) tmem_dealloc(tmem, 128);
+    // the fused kernel that follows may launch once every CTA is here (it
+    // waits for this grid before it reads T_u): triggered at the start, its
+    // CTAs were placed on SMs as this grid's left them, which measured slower
+    griddep_launch_dependents();
 #ifdef GDN_TRACE_TIMELINE
     if (tid == 0 && blockIdx.x < 2048) {
         g_ut_cta[blockIdx.x][1] = clock64();
@@ -444,9 +445,6 @@ k_gdn_utw(const __grid_constant__ CUtensorMap tm_k, UtParams p) {
     float *AT = reinterpret_cast<float *>(sm + L::OFF_AT);
     float *gs = reinterpret_cast<float *>(sm + L::OFF_GS);
 
-    // the chain kernel that follows may start its own prologue now (it waits
-    // for this grid before it reads T_u and W)
-    griddep_launch_dependents();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 #ifdef GDN_TRACE_TIMELINE
     if (tid == 0 && blockIdx.x < 2048) {
@@ -728,6 +726,11 @@ k_gdn_utw(const __grid_constant__ CUtensorMap tm_k, UtParams p) {
     __syncthreads();
     tc_fence_after();
     if (warp == 0) tmem_dealloc(tmem, 128);
+    // the chain kernel that follows may launch once every CTA is here (it
+    // waits for this grid before it reads T_u and W).  Triggered at the start,
+    // its CTAs were placed on SMs as this grid's left them: 0.215 against
+    // 0.200 ms per call at B4 H16 T4096 d128
+    griddep_launch_dependents();
 #ifdef GDN_TRACE_TIMELINE
     if (tid == 0 && blockIdx.x < 2048) {
         g_ut_cta[blockIdx.x][1] = clock64();
