@@ -866,8 +866,9 @@ gdn_status launch_tc(const FwdArgs &a, const __nv_bfloat16 *Tin, const LaunchCfg
     p.max_chunks = a.max_chunks;
     dim3 grid(a.dv / kNV + c.lin_tiles, a.sm.H, c.nseq);
     const int slot = c.timed ? timer_begin(a.stream, "k_gdn_tc") : -1;
-    // launched as a programmatic dependent of the previous kernel: its
-    // prologue (barriers, TMEM) overlaps that kernel's tail
+    // launched as a programmatic dependent of the previous kernel, which
+    // releases it as its CTAs finish (the chunk-prep kernels do so at their
+    // end): the prologue (barriers, TMEM) may overlap that kernel's tail
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
