@@ -18,6 +18,7 @@ std::atomic<long long> g_opt_segments{0};
 std::atomic<long long> g_opt_wait_limit{0};
 std::atomic<long long> g_opt_poison{0};
 std::atomic<long long> g_opt_host_slice{0};
+std::atomic<long long> g_opt_prep_lead{0};
 std::atomic<int> g_last_impl{0};
 
 struct TimerState {
@@ -154,6 +155,7 @@ long long option(int key) {
         case GDN_OPT_WAIT_LIMIT: return g_opt_wait_limit.load();
         case GDN_OPT_POISON_SCRATCH: return g_opt_poison.load();
         case GDN_OPT_HOST_SLICE: return g_opt_host_slice.load();
+        case GDN_OPT_PREP_LEAD: return g_opt_prep_lead.load();
         default: return -1;
     }
 }
@@ -425,6 +427,10 @@ gdn_status gdn_set_option(int key, long long value) {
         case GDN_OPT_HOST_SLICE:
             if (value < 0 || value > (1LL << 24)) return GDN_ERR_INVALID_ARG;
             g_opt_host_slice.store(value);
+            return GDN_OK;
+        case GDN_OPT_PREP_LEAD:
+            if (value < -1 || value > (1LL << 30)) return GDN_ERR_INVALID_ARG;
+            g_opt_prep_lead.store(value);
             return GDN_OK;
         default:
             return GDN_ERR_INVALID_ARG;

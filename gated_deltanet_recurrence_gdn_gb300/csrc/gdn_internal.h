@@ -155,6 +155,13 @@ gdn_status enqueue_ut(const FwdArgs &a, const int2 *table, __nv_bfloat16 *Tu);
 // inputs.  GDN_ERR_UNSUPPORTED outside those shapes.
 gdn_status enqueue_ut_w(const FwdArgs &a, const int2 *table, __nv_bfloat16 *Tu,
                         __nv_bfloat16 *W);
+// The same over chunks 0 .. lead - 1 of every (sequence, head) of a dense
+// batch only (the chain kernel's overlapped launch prepares the rest); it
+// first clears the n_done ready flags at `done` that the overlapped launch
+// sets.  GDN_ERR_UNSUPPORTED where enqueue_ut_w is, for packed batches and
+// for lead outside 1 .. max_chunks.
+gdn_status enqueue_ut_w_lead(const FwdArgs &a, __nv_bfloat16 *Tu, __nv_bfloat16 *W, int lead,
+                             uint32_t *done, long long n_done);
 bool fused_supported(const FwdArgs &a);
 gdn_status fused_forward(const FwdArgs &a);
 

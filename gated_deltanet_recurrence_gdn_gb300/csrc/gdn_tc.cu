@@ -41,6 +41,8 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include <cmath>
+
 #include "gdn_bwd_tc.h"
 #include "gdn_internal.h"
 #include "tc_common.cuh"
@@ -92,6 +94,8 @@ __device__ __forceinline__ int smid() {
     do {               \
     } while (0)
 #endif
+
+#include "gdn_utw.cuh"   // the chunk prep's pipeline, run beside the chain by k_gdn_tc_ov
 
 namespace gdn {
 namespace {
@@ -185,6 +189,12 @@ struct TcParams {
     float *Hst, *Vst;
     long long chunk_slots;
     int max_chunks;
+    // Chunk prep beside the chain (k_gdn_tc_ov; dense batches, no segments):
+    // chunk j >= prep_c0 of (n, h) waits for its ready flag
+    // done[h * chunk_slots + n * max_chunks + j] before its W and T_u tiles
+    // are copied.  Null: no wait.
+    const uint32_t *done;
+    int prep_c0;
 };
 
 // The kernel body.  STATES: the backward's state pass (stores Hst / Vst),
@@ -194,7 +204,9 @@ template <int DK, bool STATES>
 __device__ __forceinline__ void gdn_tc_body(const CUtensorMap *tm_q, const CUtensorMap *tm_k,
                                             const CUtensorMap *tm_v, const CUtensorMap *tm_t,
                                             const CUtensorMap *tm_w, const CUtensorMap *tm_hst,
-                                            const CUtensorMap *tm_vst, const TcParams &p) {
+                                            const CUtensorMap *tm_vst, const TcParams &p,
+                                            const int bx, const int h, const int n,
+                                            const int nseq) {
     using L = Lay<DK>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -208,9 +220,8 @@ __device__ __forceinline__ void gdn_tc_body(const CUtensorMap *tm_q, const CUten
     float *gb = reinterpret_cast<float *>(sm + L::OFF_G);   // [2][GSZ]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int dv0 = ((int)blockIdx.x >= p.xsplit ? (int)blockIdx.x - p.xsplit : (int)blockIdx.x) *
-                    kNV;
-    const int h = blockIdx.y, n = blockIdx.z;
+    // this CTA: d_v tile bx (or linear-part tile bx - xsplit) of (sequence n, head h)
+    const int dv0 = (bx >= p.xsplit ? bx - p.xsplit : bx) * kNV;
 
     // ---- sequence bounds (validated; an invalid packed range is an error)
     long long row0 = 0;
@@ -243,7 +254,7 @@ __device__ __forceinline__ void gdn_tc_body(const CUtensorMap *tm_q, const CUten
         return;  // before any barrier or TMEM use
     }
     const int nch = (len + kC - 1) / kC;
-    const bool lin = (int)blockIdx.x >= p.xsplit;        // linear-part CTA (v = 0, h0 = I)
+    const bool lin = bx >= p.xsplit;                     // linear-part CTA (v = 0, h0 = I)
     const int dvs = lin ? p.dv2 : p.dv;                  // width of this CTA's state
     float *hTp = lin ? p.hT2 : p.hT;
     const long long srow = ((long long)n * p.sm.H + h) * dvs;   // state row of (n, h)
@@ -275,7 +286,7 @@ __device__ __forceinline__ void gdn_tc_body(const CUtensorMap *tm_q, const CUten
     // rows of the inputs, and the states of this launch's grid
     const long long nrows =
         p.sm.cu ? (long long)p.sm.H * p.sm.T_total : (long long)p.sm.N * p.sm.H * p.sm.T;
-    const long long nstate = (long long)gridDim.z * p.sm.H * dvs * DK;
+    const long long nstate = (long long)nseq * p.sm.H * dvs * DK;
     (void)nrows;
     (void)nstate;
 
@@ -656,6 +667,15 @@ __device__ __forceinline__ void gdn_tc_body(const CUtensorMap *tm_q, const CUten
         if (nch > 0) load_gates(0);
         for (int j = 0; j < nch; ++j) {
             const int s = j % kNS;
+            if (p.done && j >= p.prep_c0) {
+                // this chunk's T_u and W rows come from the prep CTAs of the
+                // same launch: their ready flag (usually set long before;
+                // polled ahead of the wait for a free stage)
+                const bool okp =
+                    ctl.gflag(p.done + (long long)h * p.chunk_slots + slot0 + j, 1u);
+                if (!__all_sync(0xffffffffu, okp)) break;
+                fence_proxy_async_global();
+            }
             const bool ok = j < kNS || ctl.wait(B_FREE + s, ((j / kNS) - 1) & 1);
             if (!__all_sync(0xffffffffu, ok)) break;
             uint8_t *stg = sm + L::OFF_STAGE + s * L::STAGE;
@@ -738,7 +758,7 @@ __device__ __forceinline__ void gdn_tc_body(const CUtensorMap *tm_q, const CUten
             mma_commit(bar + B_DRAIN);
             mbar_wait(bar + B_DRAIN, 0, ctl.limit);
         }
-    } else {
+    } else if (warp == 10) {
         // ============================================== prep MMA issuer
         if (lane == 0 && nch > 0) {
             constexpr uint32_t idG = make_idesc_bf16(128, 64, false, false);   // [W;Q] K^T
@@ -792,7 +812,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
 k_gdn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
          const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_t,
          const __grid_constant__ CUtensorMap tm_w, TcParams p) {
-    gdn_tc_body<DK, false>(&tm_q, &tm_k, &tm_v, &tm_t, &tm_w, nullptr, nullptr, p);
+    gdn_tc_body<DK, false>(&tm_q, &tm_k, &tm_v, &tm_t, &tm_w, nullptr, nullptr, p, blockIdx.x,
+                           blockIdx.y, blockIdx.z, gridDim.z);
 }
 
 template <int DK>
@@ -801,7 +822,85 @@ k_gdn_tc_states(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_t,
                 const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_hst,
                 const __grid_constant__ CUtensorMap tm_vst, TcParams p) {
-    gdn_tc_body<DK, true>(&tm_q, &tm_k, &tm_v, &tm_t, &tm_w, &tm_hst, &tm_vst, p);
+    gdn_tc_body<DK, true>(&tm_q, &tm_k, &tm_v, &tm_t, &tm_w, &tm_hst, &tm_vst, p, blockIdx.x,
+                          blockIdx.y, blockIdx.z, gridDim.z);
+}
+
+// The chain with the chunk prep beside it, one cooperative launch of one CTA
+// per SM.  CTAs 0 .. nchain - 1 run the chain of (sequence, head, d_v tile)
+// (tile fastest, then head); from chunk prep_c0 on, each chunk's W and T_u
+// tiles wait for the chunk's ready flag.  Every other CTA runs kPrepPipes
+// prep pipelines (gdn_utw.cuh) over the units of chunks prep_c0 ..
+// max_chunks - 1, chunk by chunk, and sets those flags; the prep launch
+// before this one has prepared the earlier chunks and cleared the flags.
+// The chain CTAs, latency-bound on their serial chunk pass, leave the other
+// SMs idle otherwise.  A cooperative launch has every CTA resident at once,
+// so a chain CTA's wait on a prep CTA always ends.
+constexpr int kPrepPipes = 3;
+constexpr int kThreadsOV = 128 * kPrepPipes > kThreadsTC ? 128 * kPrepPipes : kThreadsTC;
+
+template <int DK>
+struct OvLay {
+    static constexpr int PIPE = (VLay<DK>::TOTAL + 1023) / 1024 * 1024;   // per pipeline
+    static constexpr int OFF_MISC = kPrepPipes * PIPE;                       // TMEM address
+    static constexpr int ALLOC_PREP = OFF_MISC + 16 + 1024;
+    static constexpr int ALLOC = ALLOC_PREP > Lay<DK>::ALLOC ? ALLOC_PREP : Lay<DK>::ALLOC;
+    static_assert(ALLOC <= 227 * 1024, "shared memory budget (overlapped launch)");
+};
+
+template <int DK>
+__global__ void __launch_bounds__(kThreadsOV, 1)
+k_gdn_tc_ov(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+            const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_t,
+            const __grid_constant__ CUtensorMap tm_w, TcParams p, UtParams up, int nchain,
+            int by_sm) {
+    // Role by SM: with one CTA per SM (by_sm) and SM ids 0 .. SMs - 1, the CTA on
+    // SM s takes role s, so the chain CTAs sit on the lowest-numbered SMs, as
+    // a plain launch of the chain alone places them (measured: 139 µs for the
+    // chain at B4 H16 T4096 d128 there, against 152 µs when the roles follow
+    // the launch's own placement, which spreads the chain CTAs over every
+    // GPC).  Otherwise the role is the CTA index.
+    uint32_t sm_id, n_smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(sm_id));
+    asm volatile("mov.u32 %0, %%nsmid;" : "=r"(n_smid));
+    const int role = by_sm && n_smid == gridDim.x ? (int)sm_id : (int)blockIdx.x;
+    if (role < nchain) {
+        const int ci = role, tiles = p.xsplit, hn = ci / tiles;
+        gdn_tc_body<DK, false>(&tm_q, &tm_k, &tm_v, &tm_t, &tm_w, nullptr, nullptr, p,
+                               ci - hn * tiles, hn % p.sm.H, hn / p.sm.H, p.sm.N);
+        return;
+    }
+    using O = OvLay<DK>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint32_t *misc = reinterpret_cast<uint32_t *>(sm + O::OFF_MISC);
+    const int tid = threadIdx.x, warp = tid >> 5, pipe = tid >> 7, ptid = tid & 127;
+    const bool in_pipe = pipe < kPrepPipes;   // warps past the pipelines only join the barriers
+    CTA_SPAN(0);
+    uint8_t *psm = sm + pipe * O::PIPE;
+    if (warp == 0) {
+        tmem_alloc(misc, 512);
+        tmem_relinquish();
+    }
+    if (in_pipe) utw_init<DK>(psm, ptid);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = misc[0];
+    // the prep launch before this one cleared the ready flags
+    griddep_wait();
+    // pipelines of all prep CTAs walk the units round robin, so the chunks
+    // are finished roughly in order
+    const long long stride = (long long)kPrepPipes * (gridDim.x - nchain);
+    const long long first = (long long)(role - nchain) * kPrepPipes + pipe;
+    const long long nun = first < up.units ? (up.units - 1 - first) / stride + 1 : 0;
+    if (in_pipe && nun > 0)
+        utw_run<DK>(psm, tmem + 128 * pipe, ptid, 1 + pipe, &tm_k, up, first, stride, nun);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    CTA_SPAN(1);
+    if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
 // -------------------------------------------------------------------- host
@@ -821,29 +920,19 @@ struct LaunchCfg {
     float *Hst = nullptr, *Vst = nullptr;   // the backward's state pass
 };
 
-template <int DK>
-gdn_status launch_tc(const FwdArgs &a, const __nv_bfloat16 *Tin, const LaunchCfg &c) {
-    using L = Lay<DK>;
+// The bulk-copy maps of a chain launch: q, k, v, T_u, W (T_u's rows, then W's,
+// at Tin).
+bool tc_maps(const FwdArgs &a, int dk, const __nv_bfloat16 *Tin, CUtensorMap (&m)[5]) {
     const long long ydim = a.sm.cu ? a.sm.T_total : a.sm.T;
     const long long zdim = a.sm.cu ? a.sm.H : (long long)a.sm.N * a.sm.H;
-    CUtensorMap mq, mk, mv, mt, mw;
     const __nv_bfloat16 *Win = Tin + (size_t)a.rows * 64;
-    if (!make_map(&mq, a.q, DK, ydim, zdim) || !make_map(&mk, a.k, DK, ydim, zdim) ||
-        !make_map(&mv, a.v, a.dv, ydim, zdim) || !make_map(&mt, Tin, 64, ydim, zdim) ||
-        !make_map(&mw, Win, DK, ydim, zdim))
-        return GDN_ERR_CUDA;
-    // per-function attributes of the current device: cheap, set on every launch
-    if (cudaFuncSetAttribute(k_gdn_tc<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             L::ALLOC) != cudaSuccess ||
-        cudaFuncSetAttribute(k_gdn_tc_states<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             L::ALLOC_S) != cudaSuccess)
-        return GDN_ERR_CUDA;
-    // the state pass's outputs (the forward's instantiation never reads these)
-    CUtensorMap mh = mq, mvs = mq;
-    if (c.Hst && (!make_map_f32(&mh, c.Hst, a.dv, (long long)a.sm.H * a.chunk_slots * DK, DK) ||
-                  !make_map_f32_3d(&mvs, c.Vst, a.dv, ydim, zdim)))
-        return GDN_ERR_CUDA;
-    TcParams p;
+    return make_map(&m[0], a.q, dk, ydim, zdim) && make_map(&m[1], a.k, dk, ydim, zdim) &&
+           make_map(&m[2], a.v, a.dv, ydim, zdim) && make_map(&m[3], Tin, 64, ydim, zdim) &&
+           make_map(&m[4], Win, dk, ydim, zdim);
+}
+
+TcParams tc_params(const FwdArgs &a, int dk, const LaunchCfg &c) {
+    TcParams p{};
     p.sm = a.sm;
     p.log_alpha = a.log_alpha;
     p.beta = a.beta;
@@ -858,12 +947,36 @@ gdn_status launch_tc(const FwdArgs &a, const __nv_bfloat16 *Tin, const LaunchCfg
     p.seglen = c.seglen;
     p.no_output = c.no_output;
     p.xsplit = a.dv / kNV;
-    p.dv2 = DK;
+    p.dv2 = dk;
     p.hT2 = c.hT2;
     p.Hst = c.Hst;
     p.Vst = c.Vst;
     p.chunk_slots = a.chunk_slots;
     p.max_chunks = a.max_chunks;
+    p.done = nullptr;
+    p.prep_c0 = 0;
+    return p;
+}
+
+template <int DK>
+gdn_status launch_tc(const FwdArgs &a, const __nv_bfloat16 *Tin, const LaunchCfg &c) {
+    using L = Lay<DK>;
+    const long long ydim = a.sm.cu ? a.sm.T_total : a.sm.T;
+    const long long zdim = a.sm.cu ? a.sm.H : (long long)a.sm.N * a.sm.H;
+    CUtensorMap m[5];
+    if (!tc_maps(a, DK, Tin, m)) return GDN_ERR_CUDA;
+    // per-function attributes of the current device: cheap, set on every launch
+    if (cudaFuncSetAttribute(k_gdn_tc<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             L::ALLOC) != cudaSuccess ||
+        cudaFuncSetAttribute(k_gdn_tc_states<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             L::ALLOC_S) != cudaSuccess)
+        return GDN_ERR_CUDA;
+    // the state pass's outputs (the forward's instantiation never reads these)
+    CUtensorMap mh = m[0], mvs = m[0];
+    if (c.Hst && (!make_map_f32(&mh, c.Hst, a.dv, (long long)a.sm.H * a.chunk_slots * DK, DK) ||
+                  !make_map_f32_3d(&mvs, c.Vst, a.dv, ydim, zdim)))
+        return GDN_ERR_CUDA;
+    const TcParams p = tc_params(a, DK, c);
     dim3 grid(a.dv / kNV + c.lin_tiles, a.sm.H, c.nseq);
     const int slot = c.timed ? timer_begin(a.stream, "k_gdn_tc") : -1;
     // launched as a programmatic dependent of the previous kernel, which
@@ -880,10 +993,75 @@ gdn_status launch_tc(const FwdArgs &a, const __nv_bfloat16 *Tin, const LaunchCfg
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     const cudaError_t le =
-        c.Hst ? cudaLaunchKernelEx(&cfg, k_gdn_tc_states<DK>, mq, mk, mv, mt, mw, mh, mvs, p)
-              : cudaLaunchKernelEx(&cfg, k_gdn_tc<DK>, mq, mk, mv, mt, mw, p);
+        c.Hst ? cudaLaunchKernelEx(&cfg, k_gdn_tc_states<DK>, m[0], m[1], m[2], m[3], m[4], mh,
+                                   mvs, p)
+              : cudaLaunchKernelEx(&cfg, k_gdn_tc<DK>, m[0], m[1], m[2], m[3], m[4], p);
     timer_end(slot, a.stream);
     if (le != cudaSuccess) return GDN_ERR_CUDA;
+    count_launch();
+    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+// The overlapped launch (k_gdn_tc_ov): nchain chain CTAs and nprep prep CTAs
+// over a dense batch whose chunks 0 .. lead - 1 are prepared.
+// GDN_ERR_UNSUPPORTED when the device cannot hold the grid at once (the launch
+// did not start; the caller runs the plain path).
+template <int DK>
+gdn_status launch_tc_ov(const FwdArgs &a, __nv_bfloat16 *Tbuf, uint32_t *done, int lead,
+                        int nchain, int nprep) {
+    using O = OvLay<DK>;
+    CUtensorMap m[5];
+    if (!tc_maps(a, DK, Tbuf, m)) return GDN_ERR_CUDA;
+    if (cudaFuncSetAttribute(k_gdn_tc_ov<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             O::ALLOC) != cudaSuccess)
+        return GDN_ERR_CUDA;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_gdn_tc_ov<DK>, kThreadsOV,
+                                                      O::ALLOC) != cudaSuccess ||
+        per_sm < 1)
+        return GDN_ERR_UNSUPPORTED;
+    // the grid is one CTA per SM (nchain + nprep SMs): with at most one per SM
+    // every SM holds exactly one, and the roles may follow SM ids
+    const int by_sm = per_sm == 1 ? 1 : 0;
+    const LaunchCfg c{a.sm.N, 0, 0, 0, a.h0, a.hT, 0, nullptr, true};
+    TcParams p = tc_params(a, DK, c);
+    p.done = done;
+    p.prep_c0 = lead;
+    UtParams up;
+    ut_params(a, nullptr, Tbuf, Tbuf + (size_t)a.rows * 64, &up);
+    up.c0 = lead;
+    up.nc = a.max_chunks - lead;
+    up.units = (long long)a.sm.N * a.sm.H * up.nc;
+    up.done = done;
+    // cooperative (every CTA resident at once), and a programmatic dependent
+    // of the prep launch where the runtime takes both
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(nchain + nprep);
+    cfg.blockDim = dim3(kThreadsOV);
+    cfg.dynamicSmemBytes = O::ALLOC;
+    cfg.stream = a.stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    const int slot = timer_begin(a.stream, "k_gdn_tc");
+    cudaError_t le =
+        cudaLaunchKernelEx(&cfg, k_gdn_tc_ov<DK>, m[0], m[1], m[2], m[3], m[4], p, up, nchain,
+                           by_sm);
+    if (le != cudaSuccess) {
+        (void)cudaGetLastError();
+        cfg.numAttrs = 1;
+        le = cudaLaunchKernelEx(&cfg, k_gdn_tc_ov<DK>, m[0], m[1], m[2], m[3], m[4], p, up,
+                                nchain, by_sm);
+    }
+    timer_end(slot, a.stream);
+    if (le != cudaSuccess) {
+        (void)cudaGetLastError();   // a launch that did not start leaves no sticky error
+        return GDN_ERR_UNSUPPORTED;
+    }
     count_launch();
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
@@ -970,6 +1148,67 @@ int choose_segments(const FwdArgs &a) {
     return S;
 }
 
+bool coop_supported() {
+    static std::atomic<int> memo[kMaxDeviceMemo];
+    return per_device(
+               memo,
+               [](int dev) {
+                   int v = 0;
+                   return cudaDeviceGetAttribute(&v, cudaDevAttrCooperativeLaunch, dev) ==
+                                      cudaSuccess &&
+                                  v
+                              ? 1
+                              : 0;
+               },
+               0) == 1;
+}
+
+// Chunks per sequence that the prep launch covers before the overlapped
+// launch prepares the rest beside the chain, or -1: no overlap.  Automatic:
+// the prep CTAs finish a chunk of every (sequence, head) in
+// S = N H u / (prep CTAs x kPrepPipes) cycles and the chain takes tau cycles
+// per chunk, so chunk lead + j is ready in time when (j + 1) S <= (lead + j)
+// tau; the lead is the smallest that keeps this for every j, plus one.  With
+// a lead past half the chunks the prep SMs take too small a share to pay for
+// the overlapped launch (measured at B4 H16 T4096 d128: 24 prep SMs, best
+// lead 48 of 64, no faster than the plain path), so the overlap is off.
+// Cycle counts measured on GB300 inside the overlapped launch: tau 4.5 k /
+// 3.9 k (d_k 128 / 64), u 19.5 k / 18 k per unit and pipeline (three
+// pipelines on an SM, beside the chain's memory traffic).
+int choose_prep_lead(const FwdArgs &a, int nchain) {
+    if (a.sm.cu || a.dt != GDN_BF16 || a.no_erase || a.vector_gate) return -1;
+    if (a.dk != 64 && a.dk != 128) return -1;
+    const long long opt = option(GDN_OPT_PREP_LEAD);
+    const int M = a.max_chunks;
+    const int nprep = sm_count() - nchain;
+    if (opt < 0 || M < 2 || nprep < 1 || !coop_supported()) return -1;
+    if (opt > 0) return opt < M ? (int)opt : -1;
+    const double tau = a.dk == 128 ? 4500.0 : 3900.0;
+    const double u = a.dk == 128 ? 19500.0 : 18000.0;
+    const double S = (double)a.sm.N * a.sm.H * u / ((double)nprep * kPrepPipes);
+    const double need = S <= tau ? S / tau : M - (M - 1) * tau / S;
+    const int lead = max(1, (int)ceil(need) + 1);
+    return 2 * lead > M ? -1 : lead;
+}
+
+// The forward with the chunk prep overlapped: the prep launch over chunks
+// 0 .. lead - 1 (it also clears the ready flags), then k_gdn_tc_ov.
+// GDN_ERR_UNSUPPORTED when the overlapped launch could not start.
+gdn_status tc_overlapped(const FwdArgs &a, __nv_bfloat16 *Tbuf, int lead, int nchain) {
+    const long long nd = (long long)a.sm.H * a.chunk_slots;
+    uint32_t *done = nullptr;
+    if (scratch_alloc((void **)&done, sizeof(uint32_t) * (size_t)nd, a.stream) != cudaSuccess)
+        return GDN_ERR_CUDA;
+    gdn_status rc = enqueue_ut_w_lead(a, Tbuf, Tbuf + (size_t)a.rows * 64, lead, done, nd);
+    if (rc == GDN_OK) {
+        const int nprep = sm_count() - nchain;
+        rc = a.dk == 128 ? launch_tc_ov<128>(a, Tbuf, done, lead, nchain, nprep)
+                         : launch_tc_ov<64>(a, Tbuf, done, lead, nchain, nprep);
+    }
+    scratch_free(done, a.stream);
+    return rc;
+}
+
 gdn_status tc_segmented(const FwdArgs &a, const __nv_bfloat16 *Tbuf, int S) {
     cudaStream_t st = a.stream;
     const int nch = a.max_chunks;
@@ -1053,16 +1292,24 @@ gdn_status tc_forward(const FwdArgs &a) {
         else
             rc = enqueue_chunk_table(a, table);
     }
-    if (rc == GDN_OK) {
+    const int S = choose_segments(a);
+    const int nchain = (a.dv / kNV) * a.sm.H * a.sm.N;
+    const int lead = rc == GDN_OK && S <= 1 ? choose_prep_lead(a, nchain) : -1;
+    bool done = false;
+    if (lead > 0) {
+        rc = tc_overlapped(a, Tbuf, lead, nchain);
+        done = rc == GDN_OK;
+        if (rc == GDN_ERR_UNSUPPORTED) rc = GDN_OK;   // the plain path below
+    }
+    if (rc == GDN_OK && !done) {
         // the tcgen05 chunk prep (gdn_ut.cu) where it applies, else gdn_prep.cu's
         __nv_bfloat16 *Wbuf = Tbuf + (size_t)a.rows * 64;
         rc = enqueue_ut_w(a, table, Tbuf, Wbuf);
         if (rc == GDN_ERR_UNSUPPORTED) rc = enqueue_tc_prep(a, table, Tbuf, Wbuf);
     }
-    const int S = choose_segments(a);
-    if (rc == GDN_OK && S > 1) {
+    if (rc == GDN_OK && !done && S > 1) {
         rc = tc_segmented(a, Tbuf, S);
-    } else if (rc == GDN_OK) {
+    } else if (rc == GDN_OK && !done) {
         LaunchCfg c{a.sm.N, 0, 0, 0, a.h0, a.hT, 0, nullptr, true};
         rc = a.dk == 128 ? launch_tc<128>(a, Tbuf, c) : launch_tc<64>(a, Tbuf, c);
     }

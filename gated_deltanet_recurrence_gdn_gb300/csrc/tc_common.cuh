@@ -36,6 +36,14 @@ struct Ctl {
         atomicCAS(err, 0, kErrTimeout);
         return false;
     }
+    // The same on a global flag that another CTA sets (gpu scope).
+    __device__ __forceinline__ bool gflag(const uint32_t *f, uint32_t target) const {
+        if (*abort) return false;
+        if (gflag_wait(f, target, limit)) return true;
+        *abort = 1;
+        atomicCAS(err, 0, kErrTimeout);
+        return false;
+    }
 };
 
 // 16-byte store to shared memory

@@ -104,6 +104,26 @@ __device__ __forceinline__ bool flag_wait(const uint32_t *p, uint32_t target, ui
     return false;
 }
 
+// The same on a global 32-bit word shared between CTAs (gpu scope): a flag
+// that another CTA of the same launch sets once its stores are done.
+__device__ __forceinline__ void st_release_gpu(uint32_t *p, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+// Bounded poll with a short sleep between reads; false if *p never reached
+// `target`.
+__device__ __forceinline__ bool gflag_wait(const uint32_t *p, uint32_t target, uint32_t limit) {
+    for (uint32_t i = 0; i < limit; ++i) {
+        if (ld_acquire_gpu(p) >= target) return true;
+        __nanosleep(64);
+    }
+    return false;
+}
+
 // Programmatic dependent launch: a kernel launched with programmatic stream
 // serialisation may start while the previous kernel in the stream runs;
 // griddep_wait() blocks until that kernel has completed and its memory is
@@ -120,6 +140,13 @@ __device__ __forceinline__ void griddep_launch_dependents() {
 // (tcgen05.mma operand reads, bulk copies out of shared memory).
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// Orders this thread's generic-proxy accesses to global memory with its
+// async-proxy ones (bulk tensor copies): global data written with plain
+// stores, by this thread or (after an acquire) by another, before a copy
+// reads it.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() {

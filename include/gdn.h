@@ -179,6 +179,14 @@ int gdn_bounds_violation(int clear);
  *                      default; rounded up to a multiple of the chunk).
  *                      Shorter slices overlap the copies of neighbouring
  *                      slices better and cost more launches.
+ *   GDN_OPT_PREP_LEAD: the tensor-core forward's overlap of chunk prep and
+ *                      chain (dense batches without the segment scan, bf16,
+ *                      scalar gates with erase, d_k 64 or 128).  0 =
+ *                      automatic (default); -1 = off (the chunk prep is one
+ *                      launch before the chain); n >= 1: the prep launch
+ *                      covers chunks 0 .. n - 1 of every sequence and the
+ *                      chain's launch prepares the rest on the SMs its chain
+ *                      CTAs leave free (n >= the chunk count: no overlap).
  * Returns GDN_ERR_INVALID_ARG for an unknown key or value.
  */
 enum {
@@ -186,7 +194,8 @@ enum {
     GDN_OPT_SEGMENTS = 1,
     GDN_OPT_WAIT_LIMIT = 2,
     GDN_OPT_POISON_SCRATCH = 3,
-    GDN_OPT_HOST_SLICE = 4
+    GDN_OPT_HOST_SLICE = 4,
+    GDN_OPT_PREP_LEAD = 5
 };
 enum { GDN_IMPL_AUTO = 0, GDN_IMPL_SIMT = 1, GDN_IMPL_TC = 2, GDN_IMPL_TC_FUSED = 3 };
 gdn_status gdn_set_option(int key, long long value);

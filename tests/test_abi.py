@@ -63,6 +63,13 @@ def test_options_roundtrip(lib):
     assert lib.gdn_get_option(gdn.GDN_OPT_HOST_SLICE) == 1024
     assert lib.gdn_set_option(gdn.GDN_OPT_HOST_SLICE, -1) == gdn.GDN_ERR_INVALID_ARG
     assert lib.gdn_set_option(gdn.GDN_OPT_HOST_SLICE, prev) == gdn.GDN_OK
+    prev = lib.gdn_get_option(gdn.GDN_OPT_PREP_LEAD)
+    assert prev == 0   # automatic by default
+    for v in (-1, 1, 48):
+        assert lib.gdn_set_option(gdn.GDN_OPT_PREP_LEAD, v) == gdn.GDN_OK
+        assert lib.gdn_get_option(gdn.GDN_OPT_PREP_LEAD) == v
+    assert lib.gdn_set_option(gdn.GDN_OPT_PREP_LEAD, -2) == gdn.GDN_ERR_INVALID_ARG
+    assert lib.gdn_set_option(gdn.GDN_OPT_PREP_LEAD, prev) == gdn.GDN_OK
 
 
 # Host-only validation: these calls must return before any CUDA call, so fake

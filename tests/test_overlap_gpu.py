@@ -1,0 +1,101 @@
+"""The tensor-core forward with the chunk prep overlapped on the chain's spare
+SMs (k_gdn_tc_ov), against the fp64 oracle and against the same call without
+the overlap.
+
+The prep units are computed by the same pipeline code in either launch and
+the chain's arithmetic does not depend on which CTA prepared a chunk, so the
+overlapped result must equal the plain one bit for bit; a missing or early
+ready flag would hand the chain stale T_u / W rows (the scratch is poisoned
+with NaN in these tests) and show up in both comparisons.  The lead (chunks
+prepared before the chain starts) is swept from 1 (almost every chunk
+prepared beside the chain, the chain waiting on its flags) to the chunk
+count minus one.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import gated_deltanet_recurrence_gdn_gb300 as gdn
+import synth
+from tests import gpu_util as U
+
+pytestmark = pytest.mark.gpu
+
+
+class prep_lead:
+    def __init__(self, lead):
+        self.lead = lead
+
+    def __enter__(self):
+        self.prev = gdn.get_option(gdn.GDN_OPT_PREP_LEAD)
+        gdn.set_option(gdn.GDN_OPT_PREP_LEAD, self.lead)
+
+    def __exit__(self, *exc):
+        gdn.set_option(gdn.GDN_OPT_PREP_LEAD, self.prev)
+
+
+def _run(x, lead):
+    with gdn.use_impl(gdn.GDN_IMPL_TC, 1), prep_lead(lead):
+        o, hT = gdn.gdn_fwd(x.q, x.k, x.v, x.log_alpha, x.beta, x.h0, check=True)
+        assert gdn.last_impl() == gdn.GDN_IMPL_TC
+    U.sync()
+    return o, hT
+
+
+def _steep(la, starts):
+    la = la.clone()
+    for s0, val in starts:
+        la[..., s0:s0 + 64] = val
+    return la
+
+
+@pytest.mark.parametrize("dk,dv", [(128, 128), (64, 64), (128, 256)])
+@pytest.mark.parametrize("lead", [1, 4, 10])
+def test_overlap_matches_oracle_and_plain(dk, dv, lead):
+    # 11 chunks (the last one ragged); steep chunks take the chain's wide-span branch
+    x = synth.make_dense(2, 3, 10 * 64 + 17, dk, dv, io="bf16", h0_std=0.1, seed=601 + dk + dv,
+                         device="cuda")
+    x = dataclasses.replace(x, log_alpha=_steep(x.log_alpha, [(128, -3.0), (448, -1.3)]))
+    o, hT = _run(x, lead)
+    o_ref, h_ref = U.oracle_dense(x)
+    to, th = U.TOL["bf16"]
+    eo = U.rel(U.f64(o), o_ref.reshape(o.shape))
+    eh = U.rel(U.f64(hT), h_ref.reshape(hT.shape))
+    assert eo <= to and eh <= th, (eo, eh)
+    assert np.isfinite(U.f64(o)).all()
+    o1, h1 = _run(x, -1)
+    assert torch.equal(o, o1) and torch.equal(hT, h1)
+
+
+def test_overlap_repeatable():
+    # the chain waits on flags for 15 of 16 chunks; calls with a cold L2 or
+    # another launch in between must all give the same bits
+    x = synth.make_dense(4, 4, 16 * 64, 128, 128, io="bf16", h0_std=0.1, seed=611,
+                         device="cuda")
+    o0, h0 = _run(x, 1)
+    for i in range(5):
+        if i % 2:
+            torch.empty(256 << 20, dtype=torch.uint8, device="cuda").zero_()
+        else:
+            torch.randn(1 << 20, device="cuda").sum()
+        o, h = _run(x, 1)
+        assert torch.equal(o, o0) and torch.equal(h, h0), "call %d differs" % (i + 1)
+    o1, h1 = _run(x, -1)
+    assert torch.equal(o0, o1) and torch.equal(h0, h1)
+
+
+def test_overlap_automatic_lead_workload():
+    # B8 H8 T8192 d64 with h0 (64 chain CTAs, 88 SMs for the prep) and the
+    # automatic lead: every output equals the plain path's, two heads the
+    # oracle's
+    x = synth.make_workload("gdn_fwd_b8_h8_t8192_d64_bf16_h0", device="cuda")
+    o, hT = _run(x, 0)
+    o1, h1 = _run(x, -1)
+    assert torch.equal(o, o1) and torch.equal(hT, h1)
+    heads = [(0, 0), (7, 7)]
+    o_ref, h_ref = U.oracle_dense_heads_gpu(x, heads)
+    for i, (b, h) in enumerate(heads):
+        assert U.rel(U.f64(o[b, h]), o_ref[i]) <= U.TOL["bf16"][0]
+        assert U.rel(U.f64(hT[b, h]), h_ref[i]) <= U.TOL["bf16"][1]
