@@ -209,9 +209,14 @@ KERNEL_TIMING = "a second pass over the timed steps with per-kernel CUDA events"
 # the sources each timed kernel is built from (its file and the headers it includes)
 KERNEL_SOURCES = {
     "k_gdn_fused": ["gdn_fused.cu", "tc_common.cuh", "tc_ptx.cuh", "gdn_check.cuh", "gdn_internal.h"],
-    "k_gdn_ut": ["gdn_ut.cu", "gdn_inv.cuh", "tc_common.cuh", "tc_ptx.cuh", "gdn_check.cuh", "gdn_internal.h"],
-    "k_gdn_utw": ["gdn_ut.cu", "gdn_inv.cuh", "tc_common.cuh", "tc_ptx.cuh", "gdn_check.cuh", "gdn_internal.h"],
-    "k_gdn_tc": ["gdn_tc.cu", "gdn_bwd_tc.h", "tc_common.cuh", "tc_ptx.cuh", "gdn_check.cuh", "gdn_internal.h"],
+    "k_gdn_ut": ["gdn_ut.cu", "gdn_utw.cuh", "gdn_inv.cuh", "tc_common.cuh", "tc_ptx.cuh",
+                 "gdn_check.cuh", "gdn_internal.h"],
+    "k_gdn_utw": ["gdn_ut.cu", "gdn_utw.cuh", "gdn_inv.cuh", "tc_common.cuh", "tc_ptx.cuh",
+                  "gdn_check.cuh", "gdn_internal.h"],
+    "k_gdn_tc": ["gdn_tc.cu", "gdn_utw.cuh", "gdn_inv.cuh", "gdn_bwd_tc.h", "tc_common.cuh",
+                 "tc_ptx.cuh", "gdn_check.cuh", "gdn_internal.h"],
+    "k_gdn_tc_ov": ["gdn_tc.cu", "gdn_utw.cuh", "gdn_inv.cuh", "gdn_bwd_tc.h", "tc_common.cuh",
+                    "tc_ptx.cuh", "gdn_check.cuh", "gdn_internal.h"],
     "k_bwd_dstate_tc": ["gdn_bwd_tc.cu", "gdn_bwd_tc.h", "tc_common.cuh", "tc_ptx.cuh", "gdn_check.cuh",
                         "gdn_internal.h"],
     "k_gdn_prep": ["gdn_prep.cu", "gdn_inv.cuh", "gdn_bwd_tc.h", "tc_ptx.cuh", "gdn_check.cuh",

@@ -139,6 +139,13 @@ int timer_begin(cudaStream_t st, const char *kernel) {
     return slot;
 }
 
+void timer_cancel(int slot) {
+    if (slot < 0) return;
+    TimerState &t = timer();
+    std::lock_guard<std::mutex> lk(t.mu);
+    if ((size_t)slot + 1 == t.used) --t.used;
+}
+
 void timer_end(int slot, cudaStream_t st) {
     if (slot < 0) return;
     TimerState &t = timer();

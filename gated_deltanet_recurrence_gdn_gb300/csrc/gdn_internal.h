@@ -103,6 +103,8 @@ int *device_error_word();
 // dominant-kernel timer: returns a slot (or -1 when timing is off)
 int timer_begin(cudaStream_t st, const char *kernel);
 void timer_end(int slot, cudaStream_t st);
+// Forgets `slot` (the last begun) when its launch did not start.
+void timer_cancel(int slot);
 void count_launch(int n = 1);
 long long option(int key);
 

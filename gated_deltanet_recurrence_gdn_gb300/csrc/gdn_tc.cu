@@ -1047,7 +1047,7 @@ gdn_status launch_tc_ov(const FwdArgs &a, __nv_bfloat16 *Tbuf, uint32_t *done, i
     cfg.stream = a.stream;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    const int slot = timer_begin(a.stream, "k_gdn_tc");
+    const int slot = timer_begin(a.stream, "k_gdn_tc_ov");
     cudaError_t le =
         cudaLaunchKernelEx(&cfg, k_gdn_tc_ov<DK>, m[0], m[1], m[2], m[3], m[4], p, up, nchain,
                            by_sm);
@@ -1057,11 +1057,12 @@ gdn_status launch_tc_ov(const FwdArgs &a, __nv_bfloat16 *Tbuf, uint32_t *done, i
         le = cudaLaunchKernelEx(&cfg, k_gdn_tc_ov<DK>, m[0], m[1], m[2], m[3], m[4], p, up,
                                 nchain, by_sm);
     }
-    timer_end(slot, a.stream);
     if (le != cudaSuccess) {
         (void)cudaGetLastError();   // a launch that did not start leaves no sticky error
+        timer_cancel(slot);
         return GDN_ERR_UNSUPPORTED;
     }
+    timer_end(slot, a.stream);
     count_launch();
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
