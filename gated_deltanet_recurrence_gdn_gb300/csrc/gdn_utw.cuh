@@ -84,7 +84,9 @@ struct Unit {
 
 __device__ __forceinline__ Unit decode(const UtParams &p, long long u) {
     Unit r{0, 0, 0, 0, 0};
-    const int slot = (int)(u % p.chunk_slots), h = (int)(u / p.chunk_slots);
+    // units, one per 64 token rows of a head, number far fewer than 2^31
+    const uint32_t uu = (uint32_t)u, cs = (uint32_t)p.chunk_slots;
+    const int h = (int)(uu / cs), slot = (int)(uu - (uint32_t)h * cs);
     int n, c;
     if (p.table) {
         const int2 e = p.table[slot];
@@ -93,7 +95,7 @@ __device__ __forceinline__ Unit decode(const UtParams &p, long long u) {
         if (n < 0) return r;
     } else {
         n = slot / p.max_chunks;
-        c = slot % p.max_chunks;
+        c = slot - n * p.max_chunks;
     }
     if (p.sm.cu) {
         const int a = __ldg(p.sm.cu + n), b = __ldg(p.sm.cu + n + 1);
@@ -140,7 +142,7 @@ struct VLay {
     // The Gram's unused operand rows of the last tile read its start.
     static constexpr int OFF_AT = 2 * SZ_K;
     static constexpr int OFF_GS = OFF_AT + (kU * LDA * 4 + 1023) / 1024 * 1024;
-    static constexpr int OFF_BAR = OFF_GS + 1024;           // g, beta, gamma, exp(-g)
+    static constexpr int OFF_BAR = OFF_GS + 2048;           // 2 x g, beta, gamma, exp(-g)
     static constexpr int OFF_MISC = OFF_BAR + V_COUNT * 8;
     static constexpr int TOTAL = OFF_MISC + 16;
     static constexpr int ALLOC = TOTAL + 1024;
@@ -176,7 +178,7 @@ __device__ __forceinline__ void utw_run(uint8_t *sm, uint32_t tmem, int tid, uin
     uint32_t *misc = reinterpret_cast<uint32_t *>(sm + L::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(misc + 1);
     float *AT = reinterpret_cast<float *>(sm + L::OFF_AT);
-    float *gs = reinterpret_cast<float *>(sm + L::OFF_GS);
+    float *gsb = reinterpret_cast<float *>(sm + L::OFF_GS);   // unit i's gates at 256 (i & 1)
     const int warp = tid >> 5, lane = tid & 31;
     // token rows of the inputs (element counts for the bounds-check build)
     const long long nrows =
@@ -229,7 +231,36 @@ __device__ __forceinline__ void utw_run(uint8_t *sm, uint32_t tmem, int tid, uin
         be0 = in0 ? __ldg(p.beta + un.row0 + lane) : 0.f;
         be1 = in1 ? __ldg(p.beta + un.row0 + lane + 32) : 0.f;
     };
-    if (warp == 0 && nunits > 0) fetch_gates(0);
+    // ---- warp 3: a unit's g = in-chunk cumsum of log_alpha, gamma = e^g,
+    //      e^{-g} and beta into its gate buffer, from the registers
+    auto scan_gates = [&](float *gs) {
+        float x0 = la0, x1 = la1;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const float y0 = __shfl_up_sync(0xffffffffu, x0, off);
+            const float y1 = __shfl_up_sync(0xffffffffu, x1, off);
+            if (lane >= off) {
+                x0 += y0;
+                x1 += y1;
+            }
+        }
+        x1 += __shfl_sync(0xffffffffu, x0, 31);
+        gs[lane] = x0;
+        gs[32 + lane] = x1;
+        gs[64 + lane] = be0;
+        gs[96 + lane] = be1;
+        gs[128 + lane] = __expf(x0);
+        gs[160 + lane] = __expf(x1);
+        gs[192 + lane] = __expf(-x0);   // used only when the decay span is < 80
+        gs[224 + lane] = __expf(-x1);
+    };
+    // unit 0's gates now; later units' one unit ahead, while warps 0-1 form A
+    // (warp 3 is idle there), so no unit waits for its gate scan
+    if (warp == 3 && nunits > 0) {
+        fetch_gates(0);
+        scan_gates(gsb);
+        if (nunits > 1) fetch_gates(1);
+    }
     if (tid == kIssuer && nunits > 0) {
         prefetch_tmap(&tm_k);
         load(0);
@@ -241,31 +272,8 @@ __device__ __forceinline__ void utw_run(uint8_t *sm, uint32_t tmem, int tid, uin
     for (; i < nunits; ++i) {
         const int b = (int)(i & 1);
         const Unit un = decode(p, uid(i));
+        const float *gs = gsb + 256 * b;   // written by warp 3 before an earlier barrier
         UTRACE(i, 0);
-        // ---- gates: g = in-chunk cumsum of log_alpha, beta; the next unit's
-        //      are fetched meanwhile
-        if (warp == 0) {
-            float x0 = la0, x1 = la1;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const float y0 = __shfl_up_sync(0xffffffffu, x0, off);
-                const float y1 = __shfl_up_sync(0xffffffffu, x1, off);
-                if (lane >= off) {
-                    x0 += y0;
-                    x1 += y1;
-                }
-            }
-            x1 += __shfl_sync(0xffffffffu, x0, 31);
-            gs[lane] = x0;
-            gs[32 + lane] = x1;
-            gs[64 + lane] = be0;
-            gs[96 + lane] = be1;
-            gs[128 + lane] = __expf(x0);
-            gs[160 + lane] = __expf(x1);
-            gs[192 + lane] = __expf(-x0);   // used only when the decay span is < 80
-            gs[224 + lane] = __expf(-x1);
-            if (i + 1 < nunits) fetch_gates(i + 1);
-        }
         // ---- A from the Gram rows (warps 0-1), every row written in full
         if (!named_bar_and(bar_id, 128, ctl.wait(V_GDONE + b, (uint32_t)((i >> 1) & 1)))) break;
         UTRACE(i, 1);
@@ -300,6 +308,11 @@ __device__ __forceinline__ void utw_run(uint8_t *sm, uint32_t tmem, int tid, uin
                 form([&](int s2) { return bgr * gs[192 + s2]; });
             else
                 form([&](int s2) { return br * __expf(s2 < r ? gr - gs[s2] : 0.f); });
+        } else if (warp == 3 && i + 1 < nunits) {
+            // the next unit's gates into the other buffer (unit i - 1, its last
+            // reader, finished before this unit's first barrier)
+            scan_gates(gsb + 256 * (b ^ 1));
+            if (i + 2 < nunits) fetch_gates(i + 2);
         }
         // ---- the next unit's Gram into the other buffer's columns (its W^T
         //      was read in the previous unit): now, while warps 0-1 form A, if
