@@ -69,6 +69,20 @@ def test_overlap_matches_oracle_and_plain(dk, dv, lead):
     assert torch.equal(o, o1) and torch.equal(hT, h1)
 
 
+@pytest.mark.parametrize("B,H,T,dk,dv", [(3, 5, 2000, 128, 128), (1, 2, 700, 64, 192)])
+def test_overlap_automatic_lead_small(B, H, T, dk, dv):
+    # the automatic lead on batches whose chain CTAs leave most SMs to the
+    # prep (ragged last chunk, h0), against the oracle and the plain path
+    x = synth.make_dense(B, H, T, dk, dv, io="bf16", h0_std=0.1, seed=621 + T, device="cuda")
+    o, hT = _run(x, 0)
+    o_ref, h_ref = U.oracle_dense(x)
+    to, th = U.TOL["bf16"]
+    assert U.rel(U.f64(o), o_ref.reshape(o.shape)) <= to
+    assert U.rel(U.f64(hT), h_ref.reshape(hT.shape)) <= th
+    o1, h1 = _run(x, -1)
+    assert torch.equal(o, o1) and torch.equal(hT, h1)
+
+
 def test_overlap_repeatable():
     # the chain waits on flags for 15 of 16 chunks; calls with a cold L2 or
     # another launch in between must all give the same bits
