@@ -39,6 +39,7 @@ GDN_OPT_WAIT_LIMIT = 2
 GDN_OPT_POISON_SCRATCH = 3
 GDN_OPT_HOST_SLICE = 4
 GDN_OPT_PREP_LEAD = 5
+GDN_OPT_WIDE_CHAIN = 6
 GDN_IMPL_AUTO = 0
 GDN_IMPL_SIMT = 1
 GDN_IMPL_TC = 2

@@ -19,6 +19,7 @@ std::atomic<long long> g_opt_wait_limit{0};
 std::atomic<long long> g_opt_poison{0};
 std::atomic<long long> g_opt_host_slice{0};
 std::atomic<long long> g_opt_prep_lead{0};
+std::atomic<long long> g_opt_wide_chain{0};
 std::atomic<int> g_last_impl{0};
 
 struct TimerState {
@@ -163,6 +164,7 @@ long long option(int key) {
         case GDN_OPT_POISON_SCRATCH: return g_opt_poison.load();
         case GDN_OPT_HOST_SLICE: return g_opt_host_slice.load();
         case GDN_OPT_PREP_LEAD: return g_opt_prep_lead.load();
+        case GDN_OPT_WIDE_CHAIN: return g_opt_wide_chain.load();
         default: return -1;
     }
 }
@@ -438,6 +440,10 @@ gdn_status gdn_set_option(int key, long long value) {
         case GDN_OPT_PREP_LEAD:
             if (value < -1 || value > (1LL << 30)) return GDN_ERR_INVALID_ARG;
             g_opt_prep_lead.store(value);
+            return GDN_OK;
+        case GDN_OPT_WIDE_CHAIN:
+            if (value < -1 || value > 1) return GDN_ERR_INVALID_ARG;
+            g_opt_wide_chain.store(value);
             return GDN_OK;
         default:
             return GDN_ERR_INVALID_ARG;

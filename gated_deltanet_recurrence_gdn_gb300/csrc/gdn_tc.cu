@@ -848,34 +848,33 @@ struct OvLay {
     static_assert(ALLOC <= 227 * 1024, "shared memory budget (overlapped launch)");
 };
 
-template <int DK>
-__global__ void __launch_bounds__(kThreadsOV, 1)
-k_gdn_tc_ov(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-            const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_t,
-            const __grid_constant__ CUtensorMap tm_w, TcParams p, UtParams up, int nchain,
-            int by_sm) {
-    // Role by SM: with one CTA per SM (by_sm) and SM ids 0 .. SMs - 1, the CTA on
-    // SM s takes role s, so the chain CTAs sit on the lowest-numbered SMs, as
-    // a plain launch of the chain alone places them (measured: 139 µs for the
-    // chain at B4 H16 T4096 d128 there, against 152 µs when the roles follow
-    // the launch's own placement, which spreads the chain CTAs over every
-    // GPC).  Otherwise the role is the CTA index.
+// The role of this CTA in an overlapped launch.  With one CTA per SM
+// (by_sm) and SM ids 0 .. SMs - 1, the CTA on SM s takes role s, so the chain
+// CTAs sit on the lowest-numbered SMs, as a plain launch of the chain alone
+// places them (measured: 139 µs for the chain at B4 H16 T4096 d128 there,
+// against 152 µs when the roles follow the launch's own placement, which
+// spreads the chain CTAs over every GPC).  Otherwise the role is the CTA
+// index.
+__device__ __forceinline__ int ov_role(int by_sm) {
     uint32_t sm_id, n_smid;
     asm volatile("mov.u32 %0, %%smid;" : "=r"(sm_id));
     asm volatile("mov.u32 %0, %%nsmid;" : "=r"(n_smid));
-    const int role = by_sm && n_smid == gridDim.x ? (int)sm_id : (int)blockIdx.x;
-    if (role < nchain) {
-        const int ci = role, tiles = p.xsplit, hn = ci / tiles;
-        gdn_tc_body<DK, false>(&tm_q, &tm_k, &tm_v, &tm_t, &tm_w, nullptr, nullptr, p,
-                               ci - hn * tiles, hn % p.sm.H, hn / p.sm.H, p.sm.N);
-        return;
-    }
+    return by_sm && n_smid == gridDim.x ? (int)sm_id : (int)blockIdx.x;
+}
+
+// A prep CTA of an overlapped launch (role nchain .. grid - 1): kPrepPipes
+// pipelines of 128 threads (threads past them only join the barriers) over
+// the launch's prep units, round robin over all prep CTAs' pipelines so the
+// chunks finish roughly in order.
+template <int DK>
+__device__ __forceinline__ void ov_prep_role(const CUtensorMap *tm_k, const UtParams &up,
+                                             int role, int nchain) {
     using O = OvLay<DK>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint32_t *misc = reinterpret_cast<uint32_t *>(sm + O::OFF_MISC);
     const int tid = threadIdx.x, warp = tid >> 5, pipe = tid >> 7, ptid = tid & 127;
-    const bool in_pipe = pipe < kPrepPipes;   // warps past the pipelines only join the barriers
+    const bool in_pipe = pipe < kPrepPipes;
     CTA_SPAN(0);
     uint8_t *psm = sm + pipe * O::PIPE;
     if (warp == 0) {
@@ -889,19 +888,36 @@ k_gdn_tc_ov(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     const uint32_t tmem = misc[0];
     // the prep launch before this one cleared the ready flags
     griddep_wait();
-    // pipelines of all prep CTAs walk the units round robin, so the chunks
-    // are finished roughly in order
     const long long stride = (long long)kPrepPipes * (gridDim.x - nchain);
     const long long first = (long long)(role - nchain) * kPrepPipes + pipe;
     const long long nun = first < up.units ? (up.units - 1 - first) / stride + 1 : 0;
     if (in_pipe && nun > 0)
-        utw_run<DK>(psm, tmem + 128 * pipe, ptid, 1 + pipe, &tm_k, up, first, stride, nun);
+        utw_run<DK>(psm, tmem + 128 * pipe, ptid, 1 + pipe, tm_k, up, first, stride, nun);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     CTA_SPAN(1);
     if (warp == 0) tmem_dealloc(tmem, 512);
 }
+
+template <int DK>
+__global__ void __launch_bounds__(kThreadsOV, 1)
+k_gdn_tc_ov(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+            const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_t,
+            const __grid_constant__ CUtensorMap tm_w, TcParams p, UtParams up, int nchain,
+            int by_sm) {
+    const int role = ov_role(by_sm);
+    if (role < nchain) {
+        const int ci = role, tiles = p.xsplit, hn = ci / tiles;
+        gdn_tc_body<DK, false>(&tm_q, &tm_k, &tm_v, &tm_t, &tm_w, nullptr, nullptr, p,
+                               ci - hn * tiles, hn % p.sm.H, hn / p.sm.H, p.sm.N);
+        return;
+    }
+    ov_prep_role<DK>(&tm_k, up, role, nchain);
+}
+
+#include "gdn_tcw.cuh"   // the chunk loop with both d_v halves in one CTA (k_gdn_tcw_ov)
+static_assert(kThreadsW == kThreadsOV, "both overlapped launches share the prep role");
 
 // -------------------------------------------------------------------- host
 
@@ -1002,22 +1018,27 @@ gdn_status launch_tc(const FwdArgs &a, const __nv_bfloat16 *Tin, const LaunchCfg
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
-// The overlapped launch (k_gdn_tc_ov): nchain chain CTAs and nprep prep CTAs
-// over a dense batch whose chunks 0 .. lead - 1 are prepared.
-// GDN_ERR_UNSUPPORTED when the device cannot hold the grid at once (the launch
-// did not start; the caller runs the plain path).
-template <int DK>
+// The overlapped launch (k_gdn_tc_ov, or k_gdn_tcw_ov with WIDE): nchain
+// chain CTAs and nprep prep CTAs over a dense batch whose chunks
+// 0 .. lead - 1 are prepared.  GDN_ERR_UNSUPPORTED when the device cannot
+// hold the grid at once (the launch did not start; the caller runs the plain
+// path).
+template <int DK, bool WIDE>
 gdn_status launch_tc_ov(const FwdArgs &a, __nv_bfloat16 *Tbuf, uint32_t *done, int lead,
                         int nchain, int nprep) {
     using O = OvLay<DK>;
+    constexpr int alloc = WIDE ? (LayW<DK>::ALLOC > O::ALLOC_PREP ? LayW<DK>::ALLOC
+                                                                   : O::ALLOC_PREP)
+                               : O::ALLOC;
+    const auto kern = WIDE ? k_gdn_tcw_ov<DK> : k_gdn_tc_ov<DK>;
     CUtensorMap m[5];
     if (!tc_maps(a, DK, Tbuf, m)) return GDN_ERR_CUDA;
-    if (cudaFuncSetAttribute(k_gdn_tc_ov<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             O::ALLOC) != cudaSuccess)
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, alloc) !=
+        cudaSuccess)
         return GDN_ERR_CUDA;
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_gdn_tc_ov<DK>, kThreadsOV,
-                                                      O::ALLOC) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreadsOV, alloc) !=
+            cudaSuccess ||
         per_sm < 1)
         return GDN_ERR_UNSUPPORTED;
     // the grid is one CTA per SM (nchain + nprep SMs): with at most one per SM
@@ -1043,19 +1064,17 @@ gdn_status launch_tc_ov(const FwdArgs &a, __nv_bfloat16 *Tbuf, uint32_t *done, i
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(nchain + nprep);
     cfg.blockDim = dim3(kThreadsOV);
-    cfg.dynamicSmemBytes = O::ALLOC;
+    cfg.dynamicSmemBytes = alloc;
     cfg.stream = a.stream;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    const int slot = timer_begin(a.stream, "k_gdn_tc_ov");
+    const int slot = timer_begin(a.stream, WIDE ? "k_gdn_tcw_ov" : "k_gdn_tc_ov");
     cudaError_t le =
-        cudaLaunchKernelEx(&cfg, k_gdn_tc_ov<DK>, m[0], m[1], m[2], m[3], m[4], p, up, nchain,
-                           by_sm);
+        cudaLaunchKernelEx(&cfg, kern, m[0], m[1], m[2], m[3], m[4], p, up, nchain, by_sm);
     if (le != cudaSuccess) {
         (void)cudaGetLastError();
         cfg.numAttrs = 1;
-        le = cudaLaunchKernelEx(&cfg, k_gdn_tc_ov<DK>, m[0], m[1], m[2], m[3], m[4], p, up,
-                                nchain, by_sm);
+        le = cudaLaunchKernelEx(&cfg, kern, m[0], m[1], m[2], m[3], m[4], p, up, nchain, by_sm);
     }
     if (le != cudaSuccess) {
         (void)cudaGetLastError();   // a launch that did not start leaves no sticky error
@@ -1176,7 +1195,7 @@ bool coop_supported() {
 // Cycle counts measured on GB300 inside the overlapped launch: tau 4.5 k /
 // 3.9 k (d_k 128 / 64), u 19.5 k / 18 k per unit and pipeline (three
 // pipelines on an SM, beside the chain's memory traffic).
-int choose_prep_lead(const FwdArgs &a, int nchain) {
+int choose_prep_lead(const FwdArgs &a, int nchain, bool wide) {
     if (a.sm.cu || a.dt != GDN_BF16 || a.no_erase || a.vector_gate) return -1;
     if (a.dk != 64 && a.dk != 128) return -1;
     const long long opt = option(GDN_OPT_PREP_LEAD);
@@ -1184,7 +1203,7 @@ int choose_prep_lead(const FwdArgs &a, int nchain) {
     const int nprep = sm_count() - nchain;
     if (opt < 0 || M < 2 || nprep < 1 || !coop_supported()) return -1;
     if (opt > 0) return opt < M ? (int)opt : -1;
-    const double tau = a.dk == 128 ? 4500.0 : 3900.0;
+    const double tau = wide ? (a.dk == 128 ? 4800.0 : 4200.0) : (a.dk == 128 ? 4500.0 : 3900.0);
     const double u = a.dk == 128 ? 19500.0 : 18000.0;
     const double S = (double)a.sm.N * a.sm.H * u / ((double)nprep * kPrepPipes);
     const double need = S <= tau ? S / tau : M - (M - 1) * tau / S;
@@ -1195,7 +1214,8 @@ int choose_prep_lead(const FwdArgs &a, int nchain) {
 // The forward with the chunk prep overlapped: the prep launch over chunks
 // 0 .. lead - 1 (it also clears the ready flags), then k_gdn_tc_ov.
 // GDN_ERR_UNSUPPORTED when the overlapped launch could not start.
-gdn_status tc_overlapped(const FwdArgs &a, __nv_bfloat16 *Tbuf, int lead, int nchain) {
+gdn_status tc_overlapped(const FwdArgs &a, __nv_bfloat16 *Tbuf, int lead, int nchain,
+                         bool wide) {
     const long long nd = (long long)a.sm.H * a.chunk_slots;
     uint32_t *done = nullptr;
     if (scratch_alloc((void **)&done, sizeof(uint32_t) * (size_t)nd, a.stream) != cudaSuccess)
@@ -1203,8 +1223,12 @@ gdn_status tc_overlapped(const FwdArgs &a, __nv_bfloat16 *Tbuf, int lead, int nc
     gdn_status rc = enqueue_ut_w_lead(a, Tbuf, Tbuf + (size_t)a.rows * 64, lead, done, nd);
     if (rc == GDN_OK) {
         const int nprep = sm_count() - nchain;
-        rc = a.dk == 128 ? launch_tc_ov<128>(a, Tbuf, done, lead, nchain, nprep)
-                         : launch_tc_ov<64>(a, Tbuf, done, lead, nchain, nprep);
+        if (wide)
+            rc = a.dk == 128 ? launch_tc_ov<128, true>(a, Tbuf, done, lead, nchain, nprep)
+                             : launch_tc_ov<64, true>(a, Tbuf, done, lead, nchain, nprep);
+        else
+            rc = a.dk == 128 ? launch_tc_ov<128, false>(a, Tbuf, done, lead, nchain, nprep)
+                             : launch_tc_ov<64, false>(a, Tbuf, done, lead, nchain, nprep);
     }
     scratch_free(done, a.stream);
     return rc;
@@ -1295,10 +1319,21 @@ gdn_status tc_forward(const FwdArgs &a) {
     }
     const int S = choose_segments(a);
     const int nchain = (a.dv / kNV) * a.sm.H * a.sm.N;
-    const int lead = rc == GDN_OK && S <= 1 ? choose_prep_lead(a, nchain) : -1;
+    // the overlapped launch: with the wide chunk loop (one CTA per
+    // (sequence, head) at d_v = 128) where it is chosen, else the plain one
+    int lead = -1;
+    bool wide = false;
+    if (rc == GDN_OK && S <= 1) {
+        const long long wopt = option(GDN_OPT_WIDE_CHAIN);
+        if (a.dv == 128 && wopt > 0) {
+            lead = choose_prep_lead(a, a.sm.N * a.sm.H, true);
+            wide = lead > 0;
+        }
+        if (!wide) lead = choose_prep_lead(a, nchain, false);
+    }
     bool done = false;
     if (lead > 0) {
-        rc = tc_overlapped(a, Tbuf, lead, nchain);
+        rc = tc_overlapped(a, Tbuf, lead, wide ? a.sm.N * a.sm.H : nchain, wide);
         done = rc == GDN_OK;
         if (rc == GDN_ERR_UNSUPPORTED) rc = GDN_OK;   // the plain path below
     }

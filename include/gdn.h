@@ -187,6 +187,11 @@ int gdn_bounds_violation(int clear);
  *                      covers chunks 0 .. n - 1 of every sequence and the
  *                      chain's launch prepares the rest on the SMs its chain
  *                      CTAs leave free (n >= the chunk count: no overlap).
+ *   GDN_OPT_WIDE_CHAIN: at d_v = 128, whether the overlapped launch runs the
+ *                      chunk loop with both 64-column halves of d_v in one
+ *                      CTA (one chain CTA per (sequence, head), so more SMs
+ *                      for the chunk prep): 1 = yes where it applies, 0
+ *                      (default) and -1 = no.
  * Returns GDN_ERR_INVALID_ARG for an unknown key or value.
  */
 enum {
@@ -195,7 +200,8 @@ enum {
     GDN_OPT_WAIT_LIMIT = 2,
     GDN_OPT_POISON_SCRATCH = 3,
     GDN_OPT_HOST_SLICE = 4,
-    GDN_OPT_PREP_LEAD = 5
+    GDN_OPT_PREP_LEAD = 5,
+    GDN_OPT_WIDE_CHAIN = 6
 };
 enum { GDN_IMPL_AUTO = 0, GDN_IMPL_SIMT = 1, GDN_IMPL_TC = 2, GDN_IMPL_TC_FUSED = 3 };
 gdn_status gdn_set_option(int key, long long value);

@@ -25,19 +25,21 @@ pytestmark = pytest.mark.gpu
 
 
 class prep_lead:
-    def __init__(self, lead):
-        self.lead = lead
+    def __init__(self, lead, wide=0):
+        self.lead, self.wide = lead, wide
 
     def __enter__(self):
-        self.prev = gdn.get_option(gdn.GDN_OPT_PREP_LEAD)
+        self.prev = (gdn.get_option(gdn.GDN_OPT_PREP_LEAD), gdn.get_option(gdn.GDN_OPT_WIDE_CHAIN))
         gdn.set_option(gdn.GDN_OPT_PREP_LEAD, self.lead)
+        gdn.set_option(gdn.GDN_OPT_WIDE_CHAIN, self.wide)
 
     def __exit__(self, *exc):
-        gdn.set_option(gdn.GDN_OPT_PREP_LEAD, self.prev)
+        gdn.set_option(gdn.GDN_OPT_PREP_LEAD, self.prev[0])
+        gdn.set_option(gdn.GDN_OPT_WIDE_CHAIN, self.prev[1])
 
 
-def _run(x, lead):
-    with gdn.use_impl(gdn.GDN_IMPL_TC, 1), prep_lead(lead):
+def _run(x, lead, wide=0):
+    with gdn.use_impl(gdn.GDN_IMPL_TC, 1), prep_lead(lead, wide):
         o, hT = gdn.gdn_fwd(x.q, x.k, x.v, x.log_alpha, x.beta, x.h0, check=True)
         assert gdn.last_impl() == gdn.GDN_IMPL_TC
     U.sync()
@@ -113,3 +115,43 @@ def test_overlap_automatic_lead_workload():
     for i, (b, h) in enumerate(heads):
         assert U.rel(U.f64(o[b, h]), o_ref[i]) <= U.TOL["bf16"][0]
         assert U.rel(U.f64(hT[b, h]), h_ref[i]) <= U.TOL["bf16"][1]
+
+
+# The chunk loop with both d_v halves in one CTA (GDN_OPT_WIDE_CHAIN): the
+# same products as N = 128 MMAs, the same register arithmetic.
+@pytest.mark.parametrize("dk", [128, 64])
+@pytest.mark.parametrize("lead", [1, 4, 10, 0])
+def test_wide_chain_matches_oracle(dk, lead):
+    x = synth.make_dense(2, 3, 10 * 64 + 17, dk, 128, io="bf16", h0_std=0.1, seed=631 + dk,
+                         device="cuda")
+    x = dataclasses.replace(x, log_alpha=_steep(x.log_alpha, [(128, -3.0), (448, -1.3)]))
+    o, hT = _run(x, lead, wide=1)
+    o_ref, h_ref = U.oracle_dense(x)
+    to, th = U.TOL["bf16"]
+    eo = U.rel(U.f64(o), o_ref.reshape(o.shape))
+    eh = U.rel(U.f64(hT), h_ref.reshape(hT.shape))
+    assert eo <= to and eh <= th, (eo, eh)
+    assert np.isfinite(U.f64(o)).all()
+    # the plain path's products are N = 64 MMAs over the same operands
+    o1, h1 = _run(x, -1)
+    assert U.rel(U.f64(o), U.f64(o1)) <= 1e-3 and U.rel(U.f64(hT), U.f64(h1)) <= 1e-3
+
+
+def test_wide_chain_repeatable_and_workload():
+    # B4 H16 T4096 d128 (64 chain CTAs, 88 prep SMs): repeated calls with a
+    # cold L2 or another launch between them give the same bits; two heads
+    # against the oracle
+    x = synth.make_workload("gdn_fwd_b4_h16_t4096_d128_bf16", device="cuda")
+    o0, h0 = _run(x, 0, wide=1)
+    for i in range(4):
+        if i % 2:
+            torch.empty(256 << 20, dtype=torch.uint8, device="cuda").zero_()
+        else:
+            torch.randn(1 << 20, device="cuda").sum()
+        o, h = _run(x, 0, wide=1)
+        assert torch.equal(o, o0) and torch.equal(h, h0), "call %d differs" % (i + 1)
+    heads = [(0, 0), (3, 15)]
+    o_ref, h_ref = U.oracle_dense_heads_gpu(x, heads)
+    for i, (b, h) in enumerate(heads):
+        assert U.rel(U.f64(o0[b, h]), o_ref[i]) <= U.TOL["bf16"][0]
+        assert U.rel(U.f64(h0[b, h]), h_ref[i]) <= U.TOL["bf16"][1]
