@@ -1,9 +1,13 @@
 // gdn_tcw.cuh -- the chunk loop with both 64-column halves of d_v = 128 in one
-// CTA (one CTA per (sequence, head) instead of two), for the overlapped
-// launch: at B4 H16 T4096 d128 it leaves 88 of the 152 SMs to the chunk prep
-// instead of 24.  Included by gdn_tc.cu inside its namespace (it uses that
-// file's TcParams, kC / kNS, the bounded-wait control block and the
-// overlapped launch's prep role).  Dense batches only, forward only.
+// CTA: one CTA per (sequence, head) instead of two.  Its chunk period is
+// longer (≈ 5.7 k cycles against ≈ 4.0 k: the SM carries both halves' register
+// work), so it pays where the 64-column loop needs more than one wave of
+// CTAs: B8 H16 T4096 d128, 256 CTAs of the 64-column loop against 128 here,
+// 0.388 -> 0.297 ms per call.  As a launch of its own (k_gdn_tcw) or in the
+// overlapped launch with the chunk prep on the SMs it leaves (k_gdn_tcw_ov).
+// Included by gdn_tc.cu inside its namespace (it uses that file's TcParams,
+// kC / kNS, the bounded-wait control block and the overlapped launch's prep
+// role).  Dense batches only, forward only.
 //
 // The algebra is the chain kernel's ("Gated DeltaNet GPU并行实现", sections
 // 3.2-3.3): per chunk, V' = U - W H, O = diag(gamma) Q H + P' V' (P' the
@@ -511,6 +515,17 @@ __device__ __forceinline__ void gdn_tcw_body(const CUtensorMap *tm_q, const CUte
     tc_fence_after();
     CTA_SPAN(1);
     if (warp == 9) tmem_dealloc(tmem, 512);
+}
+
+// The wide chunk loop alone, one CTA per (sequence, head) (the chunk prep
+// ran before it, as one launch).
+template <int DK>
+__global__ void __launch_bounds__(kThreadsW, 1)
+k_gdn_tcw(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+          const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_t,
+          const __grid_constant__ CUtensorMap tm_w, TcParams p) {
+    gdn_tcw_body<DK>(&tm_q, &tm_k, &tm_v, &tm_t, &tm_w, p, (int)blockIdx.x % p.sm.H,
+                     (int)blockIdx.x / p.sm.H);
 }
 
 // The overlapped launch with the wide chunk loop: roles below nchain (one per

@@ -187,11 +187,12 @@ int gdn_bounds_violation(int clear);
  *                      covers chunks 0 .. n - 1 of every sequence and the
  *                      chain's launch prepares the rest on the SMs its chain
  *                      CTAs leave free (n >= the chunk count: no overlap).
- *   GDN_OPT_WIDE_CHAIN: at d_v = 128, whether the overlapped launch runs the
- *                      chunk loop with both 64-column halves of d_v in one
- *                      CTA (one chain CTA per (sequence, head), so more SMs
- *                      for the chunk prep): 1 = yes where it applies, 0
- *                      (default) and -1 = no.
+ *   GDN_OPT_WIDE_CHAIN: at d_v = 128 (dense bf16 batches), whether the
+ *                      tensor-core forward runs the chunk loop with both
+ *                      64-column halves of d_v in one CTA (one CTA per
+ *                      (sequence, head) instead of two, each slower): 0 =
+ *                      automatic (default: where the two-CTA form needs more
+ *                      CTAs than the device has SMs), 1 = always, -1 = never.
  * Returns GDN_ERR_INVALID_ARG for an unknown key or value.
  */
 enum {

@@ -155,3 +155,20 @@ def test_wide_chain_repeatable_and_workload():
     for i, (b, h) in enumerate(heads):
         assert U.rel(U.f64(o0[b, h]), o_ref[i]) <= U.TOL["bf16"][0]
         assert U.rel(U.f64(h0[b, h]), h_ref[i]) <= U.TOL["bf16"][1]
+
+
+@pytest.mark.parametrize("B,H,T,dk,wide", [(8, 20, 200, 128, 0), (8, 20, 200, 64, 1),
+                                           (5, 16, 700, 128, 0)])
+def test_wide_chain_plain_and_automatic(B, H, T, dk, wide):
+    # the wide loop as a launch of its own (B H >= the SMs of a GB300, or forced)
+    # and where the automatic choice takes it (more two-CTA chains than SMs):
+    # the oracle's result, and the 64-column loop's bits
+    x = synth.make_dense(B, H, T, dk, 128, io="bf16", h0_std=0.1, seed=641 + B * H + T,
+                         device="cuda")
+    o, hT = _run(x, 0, wide=wide)
+    o_ref, h_ref = U.oracle_dense(x)
+    to, th = U.TOL["bf16"]
+    assert U.rel(U.f64(o), o_ref.reshape(o.shape)) <= to
+    assert U.rel(U.f64(hT), h_ref.reshape(hT.shape)) <= th
+    o1, h1 = _run(x, -1, wide=-1)
+    assert U.rel(U.f64(o), U.f64(o1)) <= 1e-3 and U.rel(U.f64(hT), U.f64(h1)) <= 1e-3
