@@ -213,10 +213,14 @@ KERNEL_SOURCES = {
                  "gdn_check.cuh", "gdn_internal.h"],
     "k_gdn_utw": ["gdn_ut.cu", "gdn_utw.cuh", "gdn_inv.cuh", "tc_common.cuh", "tc_ptx.cuh",
                   "gdn_check.cuh", "gdn_internal.h"],
-    "k_gdn_tc": ["gdn_tc.cu", "gdn_utw.cuh", "gdn_inv.cuh", "gdn_bwd_tc.h", "tc_common.cuh",
-                 "tc_ptx.cuh", "gdn_check.cuh", "gdn_internal.h"],
-    "k_gdn_tc_ov": ["gdn_tc.cu", "gdn_utw.cuh", "gdn_inv.cuh", "gdn_bwd_tc.h", "tc_common.cuh",
-                    "tc_ptx.cuh", "gdn_check.cuh", "gdn_internal.h"],
+    "k_gdn_tc": ["gdn_tc.cu", "gdn_tcw.cuh", "gdn_utw.cuh", "gdn_inv.cuh", "gdn_bwd_tc.h",
+                 "tc_common.cuh", "tc_ptx.cuh", "gdn_check.cuh", "gdn_internal.h"],
+    "k_gdn_tc_ov": ["gdn_tc.cu", "gdn_tcw.cuh", "gdn_utw.cuh", "gdn_inv.cuh", "gdn_bwd_tc.h",
+                    "tc_common.cuh", "tc_ptx.cuh", "gdn_check.cuh", "gdn_internal.h"],
+    "k_gdn_tcw": ["gdn_tc.cu", "gdn_tcw.cuh", "gdn_utw.cuh", "gdn_inv.cuh", "gdn_bwd_tc.h",
+                  "tc_common.cuh", "tc_ptx.cuh", "gdn_check.cuh", "gdn_internal.h"],
+    "k_gdn_tcw_ov": ["gdn_tc.cu", "gdn_tcw.cuh", "gdn_utw.cuh", "gdn_inv.cuh", "gdn_bwd_tc.h",
+                     "tc_common.cuh", "tc_ptx.cuh", "gdn_check.cuh", "gdn_internal.h"],
     "k_bwd_dstate_tc": ["gdn_bwd_tc.cu", "gdn_bwd_tc.h", "tc_common.cuh", "tc_ptx.cuh", "gdn_check.cuh",
                         "gdn_internal.h"],
     "k_gdn_prep": ["gdn_prep.cu", "gdn_inv.cuh", "gdn_bwd_tc.h", "tc_ptx.cuh", "gdn_check.cuh",
