@@ -1087,7 +1087,7 @@ gdn_status launch_tc_ov(const FwdArgs &a, __nv_bfloat16 *Tbuf, uint32_t *done, i
 }
 
 // The wide chunk loop as a launch of its own (k_gdn_tcw), after the prep
-// launch over every chunk: one CTA per (sequence, head) of a dense batch.
+// launch over every chunk: one CTA per (sequence, head, 128-column d_v tile).
 template <int DK>
 gdn_status launch_tcw(const FwdArgs &a, const __nv_bfloat16 *Tin) {
     using L = LayW<DK>;
@@ -1103,7 +1103,7 @@ gdn_status launch_tcw(const FwdArgs &a, const __nv_bfloat16 *Tin) {
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(a.sm.N * a.sm.H));
+    cfg.gridDim = dim3((unsigned)(a.sm.N * a.sm.H * (a.dv / 128)));
     cfg.blockDim = dim3(kThreadsW);
     cfg.dynamicSmemBytes = L::ALLOC;
     cfg.stream = a.stream;
@@ -1214,15 +1214,16 @@ bool coop_supported() {
                0) == 1;
 }
 
-// Whether the forward runs the wide chunk loop (both halves of d_v = 128 in
-// one CTA): dense bf16 batches with scalar gates and erase, d_k 64 or 128.
+// Whether the forward runs the wide chunk loop (two 64-column halves of d_v
+// in one CTA): bf16 batches with scalar gates and erase, d_k 64 or 128, d_v a
+// multiple of 128.
 // Automatic: where the 64-column loop needs more CTAs than the device has SMs
 // (more than one wave): measured at B8 H16 T4096 d128 (256 CTAs against 128),
 // 0.297 ms against 0.388 ms per call; with one wave the 64-column loop is
 // faster (its chunk period is ≈ 4.0 k cycles against ≈ 5.7 k).
 bool wide_applies(const FwdArgs &a, int nchain) {
-    if (a.sm.cu || a.dt != GDN_BF16 || a.no_erase || a.vector_gate) return false;
-    if (a.dv != 128 || (a.dk != 64 && a.dk != 128)) return false;
+    if (a.dt != GDN_BF16 || a.no_erase || a.vector_gate) return false;
+    if (a.dv % 128 != 0 || (a.dk != 64 && a.dk != 128)) return false;
     const long long opt = option(GDN_OPT_WIDE_CHAIN);
     if (opt < 0) return false;
     return opt > 0 || nchain > sm_count();
@@ -1369,15 +1370,16 @@ gdn_status tc_forward(const FwdArgs &a) {
     // (sequence, head) at d_v = 128) where it is chosen, else the plain one
     int lead = -1;
     bool wide = false;
+    const int nchain_w = a.sm.N * a.sm.H * (a.dv / 128);   // wide CTAs
     if (rc == GDN_OK && S <= 1 && wide_applies(a, nchain)) {
         wide = true;
-        if ((long long)a.sm.N * a.sm.H < sm_count()) lead = choose_prep_lead(a, a.sm.N * a.sm.H, true);
+        if (nchain_w < sm_count()) lead = choose_prep_lead(a, nchain_w, true);
     } else if (rc == GDN_OK && S <= 1) {
         lead = choose_prep_lead(a, nchain, false);
     }
     bool done = false;
     if (lead > 0) {
-        rc = tc_overlapped(a, Tbuf, lead, wide ? a.sm.N * a.sm.H : nchain, wide);
+        rc = tc_overlapped(a, Tbuf, lead, wide ? nchain_w : nchain, wide);
         done = rc == GDN_OK;
         if (rc == GDN_ERR_UNSUPPORTED) rc = GDN_OK;   // the plain path below
     }

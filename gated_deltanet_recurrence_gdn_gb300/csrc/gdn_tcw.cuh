@@ -7,7 +7,8 @@
 // overlapped launch with the chunk prep on the SMs it leaves (k_gdn_tcw_ov).
 // Included by gdn_tc.cu inside its namespace (it uses that file's TcParams,
 // kC / kNS, the bounded-wait control block and the overlapped launch's prep
-// role).  Dense batches only, forward only.
+// role).  Forward only; dense and packed batches (the overlapped form:
+// dense only); d_v a multiple of 128, one CTA per 128-column tile.
 //
 // The algebra is the chain kernel's ("Gated DeltaNet GPU并行实现", sections
 // 3.2-3.3): per chunk, V' = U - W H, O = diag(gamma) Q H + P' V' (P' the
@@ -87,7 +88,7 @@ template <int DK>
 __device__ __forceinline__ void gdn_tcw_body(const CUtensorMap *tm_q, const CUtensorMap *tm_k,
                                              const CUtensorMap *tm_v, const CUtensorMap *tm_t,
                                              const CUtensorMap *tm_w, const TcParams &p,
-                                             const int h, const int n) {
+                                             const int wt, const int h, const int n) {
     using L = LayW<DK>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -97,12 +98,32 @@ __device__ __forceinline__ void gdn_tcw_body(const CUtensorMap *tm_q, const CUte
     float *gb = reinterpret_cast<float *>(sm + L::OFF_G);   // [2][GSZ]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const long long row0 = ((long long)n * p.sm.H + h) * (long long)p.sm.T;
-    const int len = p.sm.T;
-    const int zcoord = n * p.sm.H + h;
+    // this CTA: d_v columns 128 wt .. 128 wt + 127 of (sequence n, head h)
+    long long row0 = 0;
+    int len = 0, ytok0 = 0, zcoord = 0;
+    bool ok_seq = true;
+    if (p.sm.cu) {
+        const int a = __ldg(p.sm.cu + n), b = __ldg(p.sm.cu + n + 1);
+        ok_seq = a >= 0 && a <= b && b <= p.sm.T_total;
+        if (ok_seq) {
+            row0 = (long long)h * p.sm.T_total + a;
+            len = b - a;
+        }
+        ytok0 = a;
+        zcoord = h;
+    } else {
+        row0 = ((long long)n * p.sm.H + h) * (long long)p.sm.T;
+        len = p.sm.T;
+        zcoord = n * p.sm.H + h;
+    }
+    if (!ok_seq) {
+        if (tid == 0) atomicCAS(p.err, 0, kErrBadIndex);
+        return;   // before any barrier or TMEM use
+    }
     const int nch = (len + kC - 1) / kC;
+    const int vx0 = 128 * wt;                                     // first d_v column
     const long long srow = ((long long)n * p.sm.H + h) * p.dv;   // state rows of (n, h)
-    const long long slot0 = (long long)n * p.max_chunks;
+    const long long slot0 = p.sm.cu ? (long long)(ytok0 / kC) + n : (long long)n * p.max_chunks;
 
     if (warp == 9) {
         tmem_alloc(misc, 512);
@@ -124,7 +145,8 @@ __device__ __forceinline__ void gdn_tcw_body(const CUtensorMap *tm_q, const CUte
     CTA_SPAN(0);
     const Ctl ctl{bar, abort_flag, p.err, p.wait_limit};
     // element counts of the global arrays, for the bounds-check build
-    const long long nrows = (long long)p.sm.N * p.sm.H * p.sm.T;
+    const long long nrows =
+        p.sm.cu ? (long long)p.sm.H * p.sm.T_total : (long long)p.sm.N * p.sm.H * p.sm.T;
     const long long nstate = (long long)p.sm.N * p.sm.H * p.dv * DK;
     (void)nrows;
     (void)nstate;
@@ -132,7 +154,7 @@ __device__ __forceinline__ void gdn_tcw_body(const CUtensorMap *tm_q, const CUte
     if (warp < 8) {
         // ====================================== chain: two halves of d_v
         const int hf = warp >> 2, t = tid & 127;   // TMEM lane = H row (d_k index) / output row - 64
-        const int dv0 = 64 * hf;
+        const int dv0 = vx0 + 64 * hf;
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         float hreg[64];
 #pragma unroll
@@ -293,7 +315,7 @@ __device__ __forceinline__ void gdn_tcw_body(const CUtensorMap *tm_q, const CUte
             if (!__all_sync(0xffffffffu, ok)) break;
             uint8_t *stg = sm + s * L::STAGE;
             uint64_t *fb = bar + W_FULL + s;
-            const int y = j * kC;
+            const int y = ytok0 + j * kC;
             if (lane == 0) {
                 mbar_arrive_expect_tx(fb, (uint32_t)L::STAGE);
 #pragma unroll
@@ -303,8 +325,8 @@ __device__ __forceinline__ void gdn_tcw_body(const CUtensorMap *tm_q, const CUte
                     tma_load_3d(stg + L::OFF_WQ + blk * 16384 + 8192, tm_q, fb, blk * 64, y,
                                 zcoord);
                 }
-                tma_load_3d(stg + L::OFF_V, tm_v, fb, 0, y, zcoord);
-                tma_load_3d(stg + L::OFF_V + 8192, tm_v, fb, 64, y, zcoord);
+                tma_load_3d(stg + L::OFF_V, tm_v, fb, vx0, y, zcoord);
+                tma_load_3d(stg + L::OFF_V + 8192, tm_v, fb, vx0 + 64, y, zcoord);
                 tma_load_3d(stg + L::OFF_TU, tm_t, fb, 0, y, zcoord);
             }
             {
@@ -429,6 +451,26 @@ __device__ __forceinline__ void gdn_tcw_body(const CUtensorMap *tm_q, const CUte
                 gj[256 + lane] = b0 * e0;
                 gj[256 + lane + 32] = b1 * e1;
             }
+            const int L_ = min(kC, len - j * kC);
+            if (p.sm.cu && L_ < kC) {
+                // rows past this sequence belong to the next one: clear them in
+                // every tile of the stage (K, W, Q, both V blocks, T_u)
+                constexpr int per_row = 3 * DK / 8 + 24;   // 16-byte pieces per row
+                for (int i = t; i < (kC - L_) * per_row; i += 64) {
+                    const int r = L_ + i / per_row, q = i % per_row;
+                    uint8_t *base;
+                    if (q < DK / 8)   // K
+                        base = stg + (q >> 3) * 8192;
+                    else if (q < 3 * DK / 8)   // W, Q blocks
+                        base = stg + L::OFF_WQ + ((q - DK / 8) >> 3) * 8192;
+                    else if (q < 3 * DK / 8 + 16)   // V blocks
+                        base = stg + L::OFF_V + ((q - 3 * DK / 8) >> 3) * 8192;
+                    else   // T_u
+                        base = stg + L::OFF_TU;
+                    st16(base + sw128_offset(r, q & 7), 0u, 0u, 0u, 0u);
+                }
+                fence_proxy_async_smem();
+            }
             named_bar(4, 64);
             if (t == 0) mbar_arrive(bar + W_READY + s);
             const bool span_ok = gj[63] > -80.f;
@@ -517,15 +559,16 @@ __device__ __forceinline__ void gdn_tcw_body(const CUtensorMap *tm_q, const CUte
     if (warp == 9) tmem_dealloc(tmem, 512);
 }
 
-// The wide chunk loop alone, one CTA per (sequence, head) (the chunk prep
-// ran before it, as one launch).
+// The wide chunk loop alone, one CTA per (sequence, head, 128-column d_v
+// tile) (the chunk prep ran before it, as one launch); dense or packed.
 template <int DK>
 __global__ void __launch_bounds__(kThreadsW, 1)
 k_gdn_tcw(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
           const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_t,
           const __grid_constant__ CUtensorMap tm_w, TcParams p) {
-    gdn_tcw_body<DK>(&tm_q, &tm_k, &tm_v, &tm_t, &tm_w, p, (int)blockIdx.x % p.sm.H,
-                     (int)blockIdx.x / p.sm.H);
+    const int tiles = p.dv / 128, b = (int)blockIdx.x, hn = b / tiles;
+    gdn_tcw_body<DK>(&tm_q, &tm_k, &tm_v, &tm_t, &tm_w, p, b - hn * tiles, hn % p.sm.H,
+                     hn / p.sm.H);
 }
 
 // The overlapped launch with the wide chunk loop: roles below nchain (one per
@@ -538,7 +581,9 @@ k_gdn_tcw_ov(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
              int by_sm) {
     const int role = ov_role(by_sm);
     if (role < nchain) {
-        gdn_tcw_body<DK>(&tm_q, &tm_k, &tm_v, &tm_t, &tm_w, p, role % p.sm.H, role / p.sm.H);
+        const int tiles = p.dv / 128, hn = role / tiles;
+        gdn_tcw_body<DK>(&tm_q, &tm_k, &tm_v, &tm_t, &tm_w, p, role - hn * tiles, hn % p.sm.H,
+                         hn / p.sm.H);
         return;
     }
     ov_prep_role<DK>(&tm_k, up, role, nchain);

@@ -172,3 +172,43 @@ def test_wide_chain_plain_and_automatic(B, H, T, dk, wide):
     assert U.rel(U.f64(hT), h_ref.reshape(hT.shape)) <= th
     o1, h1 = _run(x, -1, wide=-1)
     assert U.rel(U.f64(o), U.f64(o1)) <= 1e-3 and U.rel(U.f64(hT), U.f64(h1)) <= 1e-3
+
+
+@pytest.mark.parametrize("dk,dv", [(128, 128), (64, 256)])
+def test_wide_chain_packed_batch(dk, dv):
+    # packed sequences (chunk tails that the next sequence's rows would fill,
+    # an empty one, h0): the wide loop forced, against the oracle and the
+    # 64-column loop
+    y = synth.make_varlen([300, 1, 64, 200, 0, 129, 700], 3, dk, dv, io="bf16", h0_std=0.1,
+                          seed=651 + dk + dv, device="cuda")
+    y = dataclasses.replace(y, log_alpha=_steep(y.log_alpha, [(64, -3.0), (365, -1.3)]))
+
+    def run(wide):
+        with gdn.use_impl(gdn.GDN_IMPL_TC, 1), prep_lead(0, wide):
+            o, hT = gdn.gdn_fwd_varlen(y.q, y.k, y.v, y.log_alpha, y.beta, y.cu_seqlens, y.h0,
+                                       check=True)
+        U.sync()
+        return o, hT
+
+    o, hT = run(1)
+    import oracle
+    o_ref, h_ref = oracle.gdn_fwd_varlen(U.f64(y.q), U.f64(y.k), U.f64(y.v),
+                                         U.f64(y.log_alpha), U.f64(y.beta),
+                                         y.cu_seqlens.cpu().numpy(), U.f64(y.h0))
+    to, th = U.TOL["bf16"]
+    assert U.rel(U.f64(o), o_ref) <= to
+    assert U.rel(U.f64(hT), h_ref) <= th
+    o1, h1 = run(-1)
+    assert U.rel(U.f64(o), U.f64(o1)) <= 1e-3 and U.rel(U.f64(hT), U.f64(h1)) <= 1e-3
+
+
+def test_wide_chain_dv256_dense():
+    x = synth.make_dense(2, 3, 5 * 64 + 9, 128, 256, io="bf16", h0_std=0.1, seed=661,
+                         device="cuda")
+    o, hT = _run(x, 0, wide=1)
+    o_ref, h_ref = U.oracle_dense(x)
+    to, th = U.TOL["bf16"]
+    assert U.rel(U.f64(o), o_ref.reshape(o.shape)) <= to
+    assert U.rel(U.f64(hT), h_ref.reshape(hT.shape)) <= th
+    o1, h1 = _run(x, -1, wide=-1)
+    assert U.rel(U.f64(o), U.f64(o1)) <= 1e-3 and U.rel(U.f64(hT), U.f64(h1)) <= 1e-3
