@@ -45,6 +45,10 @@ WORKLOADS = {
     # the headline batch at a quarter of its length: the case ncu captures run on
     "gdn_fwd_b4_h16_t1024_d128_bf16": dict(B=4, H=16, T=1024, dk=128, dv=128, io="bf16",
                                            decay="fast", h0_std=0.0, seed=7),
+    # the headline shape at twice the batch: more two-CTA chains than a GB300
+    # has SMs, the case the forward runs with both d_v halves in one CTA
+    "gdn_fwd_b8_h16_t4096_d128_bf16": dict(B=8, H=16, T=4096, dk=128, dv=128, io="bf16",
+                                           decay="fast", h0_std=0.0, seed=8),
     # one decode step over 256 sequences x 32 heads: 537 MB of fp32 state
     "gdn_decode_b256_h32_d128_bf16": dict(kind="decode", B=256, H=32, dk=128, dv=128,
                                           io="bf16", decay="fast", state_std=0.02, seed=6),

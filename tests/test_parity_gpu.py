@@ -293,6 +293,26 @@ def test_workload_b8_h8_t8192_d64_h0_full():
     check(o, hT, o_ref.reshape(o.shape), h_ref.reshape(hT.shape), "bf16")
 
 
+def test_workload_b8_h16_t4096_d128_sampled():
+    # the batch the forward runs with both d_v halves in one CTA (and the chunk
+    # prep beside it): every output equals the 64-column loop's, four heads
+    # the oracle's
+    x = synth.make_workload("gdn_fwd_b8_h16_t4096_d128_bf16", device="cuda")
+    o, hT = run_dense(x, "auto")
+    prev = gdn.get_option(gdn.GDN_OPT_WIDE_CHAIN)
+    gdn.set_option(gdn.GDN_OPT_WIDE_CHAIN, -1)
+    try:
+        o1, h1 = run_dense(x, "auto")
+    finally:
+        gdn.set_option(gdn.GDN_OPT_WIDE_CHAIN, prev)
+    assert U.rel(U.f64(o), U.f64(o1)) <= 1e-3 and U.rel(U.f64(hT), U.f64(h1)) <= 1e-3
+    heads = [(0, 0), (3, 7), (5, 12), (7, 15)]
+    o_ref, h_ref = U.oracle_dense_heads_gpu(x, heads)
+    for i, (b, h) in enumerate(heads):
+        assert U.rel(U.f64(o[b, h]), o_ref[i]) <= U.TOL["bf16"][0]
+        assert U.rel(U.f64(hT[b, h]), h_ref[i]) <= U.TOL["bf16"][1]
+
+
 def test_workload_long_context_sampled():
     name = "gdn_fwd_b1_h16_t131072_d128_bf16"
     x = synth.make_workload(name, device="cuda")
