@@ -21,11 +21,14 @@
 //     U = T_u V, K^T V~ and [x; P'] V' (B operands MN-major, two 64-column
 //     blocks 8 KB or d_k x 128 B apart);
 //   - warp 8 copies (K, W, Q, both V blocks, T_u per stage), warp 9 issues
-//     every MMA (the Gram of the next chunk behind this chunk's state and
-//     output products, as the two issuing warps of the chain kernel order
-//     them), warps 10-11 form the gates and P' (TMEM lanes 64-127) and, in
+//     the state's and the output's products, warps 10-11 form the gates and
+//     P' (TMEM lanes 64-127), issue the chunk's Gram (thread 320, behind the
+//     previous chunk's state and output products in the in-order tensor
+//     pipe, as the two issuing warps of the chain kernel order them) and, in
 //     chunks whose decay span is too wide for exp(-g_s), scale Q by gamma in
-//     place once the Gram has read it.
+//     place once the Gram has read it.  (One issuing thread for everything
+//     put each Gram's issue between H's publication and [W; Q] H: ≈ 5.5 k
+//     cycles per chunk.)
 // U and dH share 128 TMEM columns: U(j) is read before V'(j) is published,
 // dH(j) written after, and U(j + 1) issued only once H(j + 1) is published
 // (after dH(j) was read).  The Gram (64), two [W; Q] H / output accumulators
@@ -42,7 +45,7 @@ enum {
     W_PFREE = W_FREE + kNS,     // P' read by the output product (commit)
     W_PREADY,                   // P' written
     W_G,                        // Gram in TMEM (commit)
-    W_GFREE,                    // Gram read (P' formed)
+    W_M34I,                     // the chunk's K^T V~ and output product issued
     W_UW,                       // U in TMEM (commit)
     W_WQ,                       // [W; Q] (or [W; gamma Q]) final in the stage
     W_M2,                       // [W; Q] H done (commit)
@@ -50,6 +53,7 @@ enum {
     W_M34,                      // dH and the output product done (commit)
     W_HPUB,                     // bf16 H in shared memory, dH read: both halves
     W_DRAIN,                    // MMA issuer drained
+    W_DRAIN2,                   // the Gram's issuer drained
     W_COUNT
 };
 
@@ -200,11 +204,13 @@ __device__ __forceinline__ void gdn_tcw_body(const CUtensorMap *tm_q, const CUte
         for (int j = 0; j < nch; ++j) {
             // (i) publish H as the bf16 B operand of [W; Q] H (dH(j - 1) was
             //     read in the update below: U(j) may now take its columns)
+            TRACE(0, j, 0, tid == 0);
             if (t < DK) put_row64(Hs, t, hreg);
             fence_proxy_async_smem();
             tc_fence_before();
             named_bar(1, 256);
             if (tid == 0) mbar_arrive(bar + W_HPUB);
+            TRACE(0, j, 1, tid == 0);
             // (i') the previous chunk's output rows, off the state's path
             if (j > 0 && t >= 64) store_o(j - 1);
             // (ii) V' = U - W H and its decayed copy V~ for the state update
@@ -216,6 +222,7 @@ __device__ __forceinline__ void gdn_tcw_body(const CUtensorMap *tm_q, const CUte
                     break;
                 }
             }
+            TRACE(0, j, 2, tid == 0);
             tc_fence_after();
             const float *gj = gb + (j & 1) * L::GSZ;
             const float gC = gj[63];
@@ -250,11 +257,13 @@ __device__ __forceinline__ void gdn_tcw_body(const CUtensorMap *tm_q, const CUte
             tc_fence_before();
             named_bar(1, 256);
             if (tid == 0) mbar_arrive(bar + W_VN);
+            TRACE(0, j, 3, tid == 0);
             // (iii) H <- exp(g_C) H + dH
             if (!named_bar_and(1, 256, ctl.wait(W_M34, j & 1))) {
                 alive = false;
                 break;
             }
+            TRACE(0, j, 4, tid == 0);
             tc_fence_after();
             osc = osc_j;
             if (t < DK) {
@@ -348,7 +357,6 @@ __device__ __forceinline__ void gdn_tcw_body(const CUtensorMap *tm_q, const CUte
     } else if (warp == 9) {
         // ======================================== MMA issuer (and TMEM owner)
         if (lane == 0 && nch > 0) {
-            constexpr uint32_t idG = make_idesc_bf16(128, 64, false, false);    // [W;Q] K^T
             constexpr uint32_t idN = make_idesc_bf16(128, 128, false, true);    // [W;Q] H, [T_u;x] V, [x;P'] V'
             constexpr uint32_t idKT = make_idesc_bf16(128, 128, true, true);    // K^T V~
             const uint32_t sbase = smem_u32(sm);
@@ -360,28 +368,12 @@ __device__ __forceinline__ void gdn_tcw_body(const CUtensorMap *tm_q, const CUte
             const uint64_t dVT = make_sdesc(sbase + L::OFF_VT, 8192, 1024, kSwizzle128B);
             const uint64_t dVN = make_sdesc(sbase + L::OFF_VN, 8192, 1024, kSwizzle128B);
             const uint64_t dXP = make_sdesc(sbase + L::OFF_VT + 8192, 16, 1024, kSwizzle128B);
-            // the Gram [W; Q] K^T of chunk jj (its Q rows give P')
-            auto gram = [&](int jj) -> bool {
-                const int s = jj % kNS;
-                const uint32_t soff = s * L::STAGE;
-                if (!ctl.wait(W_READY + s, (jj / kNS) & 1)) return false;
-                if (jj > 0 && !ctl.wait(W_GFREE, (jj - 1) & 1)) return false;   // G(jj-1) read
-                tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < DK / 16; ++kk) {
-                    const uint32_t kof = soff + (kk >> 2) * 8192 + (kk & 3) * 32;
-                    const uint32_t aof = soff + L::OFF_WQ + (kk >> 2) * 16384 + (kk & 3) * 32;
-                    mma_bf16(tmem + TW_G, dS + (aof >> 4), dS + (kof >> 4), idG, kk > 0);
-                }
-                mma_commit(bar + W_G);
-                return true;
-            };
-            bool ok = gram(0);
-            for (int j = 0; ok && j < nch; ++j) {
+            for (int j = 0; j < nch; ++j) {
                 const int s = j % kNS;
                 const uint32_t soff = s * L::STAGE;
                 const uint32_t acc = tmem + TW_M2 + (j & 1) * 128;
                 if (!ctl.wait(W_WQ, j & 1) || !ctl.wait(W_HPUB, j & 1)) break;
+                TRACE(2, j, 0, true);
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < DK / 16; ++kk) {
@@ -396,7 +388,9 @@ __device__ __forceinline__ void gdn_tcw_body(const CUtensorMap *tm_q, const CUte
                     mma_bf16(tmem + TW_UH, dS + ((soff + L::OFF_TU + kk * 32) >> 4),
                              dV + ((soff + kk * 2048) >> 4), idN, kk > 0);
                 mma_commit(bar + W_UW);
+                TRACE(2, j, 1, true);
                 if (!ctl.wait(W_PREADY, j & 1) || !ctl.wait(W_VN, j & 1)) break;
+                TRACE(2, j, 2, true);
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < kC / 16; ++kk) {
@@ -407,9 +401,10 @@ __device__ __forceinline__ void gdn_tcw_body(const CUtensorMap *tm_q, const CUte
                 mma_commit(bar + W_M34);
                 mma_commit(bar + W_PFREE);
                 mma_commit(bar + W_FREE + s);
-                // the next chunk's Gram behind this chunk's state and output
-                // products in the in-order tensor pipe
-                if (j + 1 < nch) ok = gram(j + 1);
+                // the next chunk's Gram (issued by warp 10) goes behind these
+                // in the in-order tensor pipe
+                mbar_arrive(bar + W_M34I);
+                TRACE(2, j, 3, true);
             }
             // every issued MMA has finished before TMEM is released
             mma_commit(bar + W_DRAIN);
@@ -425,6 +420,7 @@ __device__ __forceinline__ void gdn_tcw_body(const CUtensorMap *tm_q, const CUte
             uint8_t *stg = sm + s * L::STAGE;
             float *gj = gb + (j & 1) * L::GSZ;
             if (!named_bar_and(4, 64, ctl.wait(W_FULL + s, (j / kNS) & 1))) break;
+            TRACE(1, j, 0, t == 0);
             if (w == 0) {
                 const float *gs = reinterpret_cast<const float *>(sm + L::OFF_GS) + s * 128;
                 float la0 = gs[lane], la1 = gs[32 + lane];
@@ -482,10 +478,29 @@ __device__ __forceinline__ void gdn_tcw_body(const CUtensorMap *tm_q, const CUte
                 if (!named_bar_and(4, 64, j == 0 || ctl.wait(W_M2, (j - 1) & 1))) break;
                 if (t == 0) mbar_arrive(bar + W_WQ);
             }
+            // this chunk's Gram [W; Q] K^T (its Q rows give P'), behind the
+            // previous chunk's state and output products (the G(j - 1) rows
+            // were read above, before the last barrier)
+            if (t == 0) {
+                if (j == 0 || ctl.wait(W_M34I, (j - 1) & 1)) {
+                    tc_fence_after();
+                    const uint32_t sbase = smem_u32(sm), soff = s * L::STAGE;
+                    const uint64_t dS = make_sdesc(sbase, 16, 1024, kSwizzle128B);
+                    constexpr uint32_t idG = make_idesc_bf16(128, 64, false, false);
+#pragma unroll
+                    for (int kk = 0; kk < DK / 16; ++kk) {
+                        const uint32_t kof = soff + (kk >> 2) * 8192 + (kk & 3) * 32;
+                        const uint32_t aof = soff + L::OFF_WQ + (kk >> 2) * 16384 + (kk & 3) * 32;
+                        mma_bf16(tmem + TW_G, dS + (aof >> 4), dS + (kof >> 4), idG, kk > 0);
+                    }
+                    mma_commit(bar + W_G);
+                }
+            }
             // P' from the Gram's Q rows, once the previous P' was read
             bool okg = ctl.wait(W_G, j & 1);
             if (j > 0) okg = okg && ctl.wait(W_PFREE, (j - 1) & 1);
             if (!named_bar_and(4, 64, okg)) break;
+            TRACE(1, j, 2, t == 0);
             tc_fence_after();
             {
                 const int r = t;
@@ -514,10 +529,8 @@ __device__ __forceinline__ void gdn_tcw_body(const CUtensorMap *tm_q, const CUte
             fence_proxy_async_smem();
             tc_fence_before();
             named_bar(4, 64);
-            if (t == 0) {
-                mbar_arrive(bar + W_PREADY);
-                mbar_arrive(bar + W_GFREE);
-            }
+            if (t == 0) mbar_arrive(bar + W_PREADY);
+            TRACE(1, j, 3, t == 0);
             if (!span_ok) {
                 // the Gram has read Q: gamma Q in place (row t of every Q
                 // block: loads first, then stores), then [W; gamma Q]
@@ -550,6 +563,11 @@ __device__ __forceinline__ void gdn_tcw_body(const CUtensorMap *tm_q, const CUte
                 if (t == 0) mbar_arrive(bar + W_WQ);
             }
             if (t == 0) mbar_arrive(bar + W_FREE + s);
+        }
+        // every Gram issued here has finished before TMEM is released
+        if (t == 0 && nch > 0) {
+            mma_commit(bar + W_DRAIN2);
+            mbar_wait(bar + W_DRAIN2, 0, ctl.limit);
         }
     }
     tc_fence_before();
