@@ -1220,7 +1220,7 @@ bool coop_supported() {
 // Automatic: where the 64-column loop needs more CTAs than the device has SMs
 // (more than one wave): measured at B8 H16 T4096 d128 (256 CTAs against 128),
 // 0.297 ms against 0.388 ms per call; with one wave the 64-column loop is
-// faster (its chunk period is ≈ 4.0 k cycles against ≈ 5.7 k).
+// faster (its chunk period is ≈ 4.0 k cycles against ≈ 5.3 k).
 bool wide_applies(const FwdArgs &a, int nchain) {
     if (a.dt != GDN_BF16 || a.no_erase || a.vector_gate) return false;
     if (a.dv % 128 != 0 || (a.dk != 64 && a.dk != 128)) return false;
@@ -1235,11 +1235,15 @@ bool wide_applies(const FwdArgs &a, int nchain) {
 // S = N H u / (prep CTAs x kPrepPipes) cycles and the chain takes tau cycles
 // per chunk, so chunk lead + j is ready in time when (j + 1) S <= (lead + j)
 // tau; the lead is the smallest that keeps this for every j, plus one.  With
-// a lead past half the chunks the prep SMs take too small a share to pay for
-// the overlapped launch (measured at B4 H16 T4096 d128: 24 prep SMs, best
-// lead 48 of 64, no faster than the plain path), so the overlap is off.
+// the 64-column loop and a lead past half the chunks the prep SMs take too
+// small a share to pay for the overlapped launch (measured at B4 H16 T4096
+// d128: 24 prep SMs, best lead 48 of 64, no faster than the plain path), so
+// the overlap is off; the wide loop's alternative is the same loop after a
+// prep launch over every chunk, so it overlaps whenever lead < chunks.
 // Cycle counts measured on GB300 inside the overlapped launch: tau 4.5 k /
-// 3.9 k (d_k 128 / 64), u 19.5 k / 18 k per unit and pipeline (three
+// 3.9 k (d_k 128 / 64) for the 64-column loop, 5.7 k at d_k 128 for the wide
+// one (fitted to its best lead at B8 H16 T4096 d128, 53 of 64; 5.0 k at
+// d_k 64 is an estimate), u 19.5 k / 18 k per unit and pipeline (three
 // pipelines on an SM, beside the chain's memory traffic).
 int choose_prep_lead(const FwdArgs &a, int nchain, bool wide) {
     if (a.sm.cu || a.dt != GDN_BF16 || a.no_erase || a.vector_gate) return -1;

@@ -1,6 +1,6 @@
 // gdn_tcw.cuh -- the chunk loop with both 64-column halves of d_v = 128 in one
 // CTA: one CTA per (sequence, head) instead of two.  Its chunk period is
-// longer (≈ 5.7 k cycles against ≈ 4.0 k: the SM carries both halves' register
+// longer (≈ 5.3 k cycles against ≈ 4.0 k: the SM carries both halves' register
 // work), so it pays where the 64-column loop needs more than one wave of
 // CTAs: B8 H16 T4096 d128, 256 CTAs of the 64-column loop against 128 here,
 // 0.388 -> 0.297 ms per call.  As a launch of its own (k_gdn_tcw) or in the
