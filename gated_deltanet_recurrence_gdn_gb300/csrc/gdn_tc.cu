@@ -1219,7 +1219,7 @@ bool coop_supported() {
 // multiple of 128.
 // Automatic: where the 64-column loop needs more CTAs than the device has SMs
 // (more than one wave): measured at B8 H16 T4096 d128 (256 CTAs against 128),
-// 0.297 ms against 0.388 ms per call; with one wave the 64-column loop is
+// 0.290 ms against 0.388 ms per call; with one wave the 64-column loop is
 // faster (its chunk period is ≈ 4.0 k cycles against ≈ 5.3 k).
 bool wide_applies(const FwdArgs &a, int nchain) {
     if (a.dt != GDN_BF16 || a.no_erase || a.vector_gate) return false;

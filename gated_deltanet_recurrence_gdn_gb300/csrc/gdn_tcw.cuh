@@ -3,7 +3,7 @@
 // longer (≈ 5.3 k cycles against ≈ 4.0 k: the SM carries both halves' register
 // work), so it pays where the 64-column loop needs more than one wave of
 // CTAs: B8 H16 T4096 d128, 256 CTAs of the 64-column loop against 128 here,
-// 0.388 -> 0.297 ms per call.  As a launch of its own (k_gdn_tcw) or in the
+// 0.388 -> 0.290 ms per call.  As a launch of its own (k_gdn_tcw) or in the
 // overlapped launch with the chunk prep on the SMs it leaves (k_gdn_tcw_ov).
 // Included by gdn_tc.cu inside its namespace (it uses that file's TcParams,
 // kC / kNS, the bounded-wait control block and the overlapped launch's prep
