@@ -212,3 +212,26 @@ def test_wide_chain_dv256_dense():
     assert U.rel(U.f64(hT), h_ref.reshape(hT.shape)) <= th
     o1, h1 = _run(x, -1, wide=-1)
     assert U.rel(U.f64(o), U.f64(o1)) <= 1e-3 and U.rel(U.f64(hT), U.f64(h1)) <= 1e-3
+
+
+@pytest.mark.parametrize("B,H,T,dk,dv,kernel", [
+    (4, 16, 4096, 128, 128, "k_gdn_tc"),       # 128 two-CTA chains, 24 spare SMs: no overlap
+    (8, 8, 8192, 64, 64, "k_gdn_tc_ov"),       # 64 chains, prep beside them on 88 SMs
+    (8, 16, 4096, 128, 128, "k_gdn_tcw_ov"),   # 256 two-CTA chains > SMs: 128 wide ones + prep
+    (8, 20, 256, 128, 128, "k_gdn_tcw"),       # 160 wide chains >= SMs: the wide loop alone
+])
+def test_automatic_path_on_gb300(B, H, T, dk, dv, kernel):
+    # the forward's automatic choice of chunk loop, read from the kernel the
+    # library times for the call; the thresholds follow the SM count, so the
+    # cases are set for GB300's 152
+    if torch.cuda.get_device_properties(0).multi_processor_count != 152:
+        pytest.skip("cases set for a 152-SM GB300")
+    x = synth.make_dense(B, H, T, dk, dv, io="bf16", seed=671, device="cuda")
+    gdn.kernel_timer(True)
+    gdn.kernel_timer_read()
+    try:
+        _run(x, 0)
+        _, n, name = gdn.kernel_timer_read()
+    finally:
+        gdn.kernel_timer(False)
+    assert n == 1 and name == kernel, (n, name)
