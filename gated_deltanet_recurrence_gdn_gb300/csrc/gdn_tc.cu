@@ -182,6 +182,7 @@ struct TcParams {
     // h0 = identity (d_k x d_k state), final state into hT2 with width dv2.
     int xsplit, dv2;
     float *hT2;
+    int lin_tiles;   // the wide chunk loop's launch of its own: linear-part tiles per (n, h)
     // State pass for the backward (no segments): every chunk's starting state
     // H = S^T as [H][chunk_slots][d_k][d_v] and the rows of V' as [rows][d_v],
     // fp32; null: not stored.  Chunk slot: dense n * max_chunks + c, packed
@@ -965,6 +966,7 @@ TcParams tc_params(const FwdArgs &a, int dk, const LaunchCfg &c) {
     p.xsplit = a.dv / kNV;
     p.dv2 = dk;
     p.hT2 = c.hT2;
+    p.lin_tiles = c.lin_tiles;
     p.Hst = c.Hst;
     p.Vst = c.Vst;
     p.chunk_slots = a.chunk_slots;
@@ -1046,6 +1048,7 @@ gdn_status launch_tc_ov(const FwdArgs &a, __nv_bfloat16 *Tbuf, uint32_t *done, i
     const int by_sm = per_sm == 1 ? 1 : 0;
     const LaunchCfg c{a.sm.N, 0, 0, 0, a.h0, a.hT, 0, nullptr, true};
     TcParams p = tc_params(a, DK, c);
+    if (WIDE) p.xsplit = a.dv / 128;   // tiles of the wide loop
     p.done = done;
     p.prep_c0 = lead;
     UtParams up;
@@ -1087,29 +1090,31 @@ gdn_status launch_tc_ov(const FwdArgs &a, __nv_bfloat16 *Tbuf, uint32_t *done, i
 }
 
 // The wide chunk loop as a launch of its own (k_gdn_tcw), after the prep
-// launch over every chunk: one CTA per (sequence, head, 128-column d_v tile).
+// launch over every chunk: one CTA per (sequence, head, 128-column d_v tile),
+// plus c.lin_tiles linear-part tiles per (sequence, head) in a segment scan's
+// first pass.
 template <int DK>
-gdn_status launch_tcw(const FwdArgs &a, const __nv_bfloat16 *Tin) {
+gdn_status launch_tcw(const FwdArgs &a, const __nv_bfloat16 *Tin, const LaunchCfg &c) {
     using L = LayW<DK>;
     CUtensorMap m[5];
     if (!tc_maps(a, DK, Tin, m)) return GDN_ERR_CUDA;
     if (cudaFuncSetAttribute(k_gdn_tcw<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              L::ALLOC) != cudaSuccess)
         return GDN_ERR_CUDA;
-    const LaunchCfg c{a.sm.N, 0, 0, 0, a.h0, a.hT, 0, nullptr, true};
-    const TcParams p = tc_params(a, DK, c);
-    // a programmatic dependent of the prep launch, as the 64-column loop
+    TcParams p = tc_params(a, DK, c);
+    p.xsplit = a.dv / 128;   // tiles of this loop
+    // a programmatic dependent of the previous launch, as the 64-column loop
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(a.sm.N * a.sm.H * (a.dv / 128)));
+    cfg.gridDim = dim3((unsigned)((long long)(p.xsplit + c.lin_tiles) * a.sm.H * c.nseq));
     cfg.blockDim = dim3(kThreadsW);
     cfg.dynamicSmemBytes = L::ALLOC;
     cfg.stream = a.stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const int slot = timer_begin(a.stream, "k_gdn_tcw");
+    const int slot = c.timed ? timer_begin(a.stream, "k_gdn_tcw") : -1;
     const cudaError_t le = cudaLaunchKernelEx(&cfg, k_gdn_tcw<DK>, m[0], m[1], m[2], m[3], m[4], p);
     timer_end(slot, a.stream);
     if (le != cudaSuccess) return GDN_ERR_CUDA;
@@ -1229,6 +1234,44 @@ bool wide_applies(const FwdArgs &a, int nchain) {
     return opt > 0 || nchain > sm_count();
 }
 
+// Whether a segment scan runs the wide chunk loop: dense bf16 batches with
+// scalar gates and erase, d_v a multiple of 128 and d_k = 128 (the linear
+// part is one 128-column tile).  Automatic when the segment count is: per
+// pass, a CTA per (sequence, head) and per map instead of two, so about
+// twice the segments fit one wave (B1 H16 T131072 d128: 5 segments against
+// 3); GDN_OPT_WIDE_CHAIN = 1 also with a forced segment count, -1 never.
+bool seg_wide_applies(const FwdArgs &a) {
+    if (a.sm.cu || a.dt != GDN_BF16 || a.no_erase || a.vector_gate) return false;
+    if (a.dv % 128 != 0 || a.dk != 128) return false;
+    const long long opt = option(GDN_OPT_WIDE_CHAIN);
+    if (opt < 0) return false;
+    return opt > 0 || option(GDN_OPT_SEGMENTS) < 1;
+}
+
+// Segments for the wide segment scan: the count that minimises the chunk
+// periods of its two passes, (waves of pass 1 + waves of pass 3) x chunks per
+// segment, plus the fold's ≈ 10 chunk periods per segment boundary.  Pass 1
+// has B H (d_v / 128 + 1) CTAs per segment but the last, pass 3 B H d_v / 128
+// per segment; a wave is one CTA per SM.  B1 H16 T131072 d128: 9 segments
+// (2.37 ms at 8, 2.49 at 5, 2.96 for the 64-column scan at 3).
+int choose_segments_wide(const FwdArgs &a) {
+    const long long M = a.max_chunks, nsm = sm_count();
+    const long long bh = (long long)a.sm.N * a.sm.H, v = a.dv / 128;
+    int best = 1;
+    long long best_cost = -1;
+    const long long smax = M < 64 ? M : 64;
+    for (long long S = 2; S <= smax; ++S) {
+        const long long w1 = (bh * (v + 1) * (S - 1) + nsm - 1) / nsm;
+        const long long w3 = (bh * v * S + nsm - 1) / nsm;
+        const long long cost = (w1 + w3) * ((M + S - 1) / S) + 10 * (S - 1);
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best = (int)S;
+        }
+    }
+    return best;
+}
+
 // Chunks per sequence that the prep launch covers before the overlapped
 // launch prepares the rest beside the chain, or -1: no overlap.  Automatic:
 // the prep CTAs finish a chunk of every (sequence, head) in
@@ -1285,15 +1328,23 @@ gdn_status tc_overlapped(const FwdArgs &a, __nv_bfloat16 *Tbuf, int lead, int nc
     return rc;
 }
 
-gdn_status tc_segmented(const FwdArgs &a, const __nv_bfloat16 *Tbuf, int S) {
+// The segment scan with the 64-column chunk loop, or with the wide one
+// (both d_v halves of a 128-column tile, and the d_k = 128 linear part, in
+// one CTA each).
+gdn_status tc_segmented(const FwdArgs &a, const __nv_bfloat16 *Tbuf, int S, bool wide) {
     cudaStream_t st = a.stream;
     const int nch = a.max_chunks;
     const int seglen = ((nch + S - 1) / S) * kC;
     S = (a.sm.T + seglen - 1) / seglen;   // no empty segments
     const int B = a.sm.N, H = a.sm.H, dv = a.dv, dk = a.dk;
+    auto pass = [&](const LaunchCfg &c) {
+        if (wide) return dk == 128 ? launch_tcw<128>(a, Tbuf, c) : launch_tcw<64>(a, Tbuf, c);
+        return dk == 128 ? launch_tc<128>(a, Tbuf, c) : launch_tc<64>(a, Tbuf, c);
+    };
+    const int lin_tiles = wide ? dk / 128 : dk / kNV;   // the linear part's tiles
     if (S < 2 || (long long)B * S > 65535) {
         LaunchCfg c{B, 0, 0, 0, a.h0, a.hT, 0, nullptr, true};
-        return dk == 128 ? launch_tc<128>(a, Tbuf, c) : launch_tc<64>(a, Tbuf, c);
+        return pass(c);
     }
     const size_t st_dv = (size_t)H * dv * dk, st_dk = (size_t)H * dk * dk;
     float *Aseg = nullptr, *Bseg = nullptr, *Sin = nullptr, *Hout = nullptr;
@@ -1306,8 +1357,8 @@ gdn_status tc_segmented(const FwdArgs &a, const __nv_bfloat16 *Tbuf, int S) {
     if (rc == GDN_OK) {
         // pass 1: per segment but the last, the map's affine part (final state
         // from zero) and linear part (final state from the identity, v = 0)
-        LaunchCfg c1{B * (S - 1), S - 1, seglen, 1, nullptr, Bseg, dk / kNV, Aseg, false};
-        rc = dk == 128 ? launch_tc<128>(a, Tbuf, c1) : launch_tc<64>(a, Tbuf, c1);
+        LaunchCfg c1{B * (S - 1), S - 1, seglen, 1, nullptr, Bseg, lin_tiles, Aseg, false};
+        rc = pass(c1);
     }
     if (rc == GDN_OK) {
         // pass 2: fold the maps into every segment's initial state
@@ -1320,7 +1371,7 @@ gdn_status tc_segmented(const FwdArgs &a, const __nv_bfloat16 *Tbuf, int S) {
     if (rc == GDN_OK) {
         // pass 3: every segment from its true initial state, with outputs
         LaunchCfg c3{B * S, S, seglen, 0, Sin, Hout, 0, nullptr, true};
-        rc = dk == 128 ? launch_tc<128>(a, Tbuf, c3) : launch_tc<64>(a, Tbuf, c3);
+        rc = pass(c3);
     }
     if (rc == GDN_OK && a.hT) {
         for (int b = 0; b < B && rc == GDN_OK; ++b)
@@ -1368,7 +1419,14 @@ gdn_status tc_forward(const FwdArgs &a) {
         else
             rc = enqueue_chunk_table(a, table);
     }
-    const int S = choose_segments(a);
+    int S = choose_segments(a);
+    // the segment scan with the wide chunk loop: automatic where the scan is
+    // (more segments in one wave of CTAs), or with GDN_OPT_WIDE_CHAIN = 1
+    bool wide_seg = false;
+    if (S > 1 && seg_wide_applies(a)) {
+        wide_seg = true;
+        if (option(GDN_OPT_SEGMENTS) < 1) S = choose_segments_wide(a);
+    }
     const int nchain = (a.dv / kNV) * a.sm.H * a.sm.N;
     // the overlapped launch: with the wide chunk loop (one CTA per
     // (sequence, head) at d_v = 128) where it is chosen, else the plain one
@@ -1394,9 +1452,10 @@ gdn_status tc_forward(const FwdArgs &a) {
         if (rc == GDN_ERR_UNSUPPORTED) rc = enqueue_tc_prep(a, table, Tbuf, Wbuf);
     }
     if (rc == GDN_OK && !done && wide) {
-        rc = a.dk == 128 ? launch_tcw<128>(a, Tbuf) : launch_tcw<64>(a, Tbuf);
+        const LaunchCfg c{a.sm.N, 0, 0, 0, a.h0, a.hT, 0, nullptr, true};
+        rc = a.dk == 128 ? launch_tcw<128>(a, Tbuf, c) : launch_tcw<64>(a, Tbuf, c);
     } else if (rc == GDN_OK && !done && S > 1) {
-        rc = tc_segmented(a, Tbuf, S);
+        rc = tc_segmented(a, Tbuf, S, wide_seg);
     } else if (rc == GDN_OK && !done) {
         LaunchCfg c{a.sm.N, 0, 0, 0, a.h0, a.hT, 0, nullptr, true};
         rc = a.dk == 128 ? launch_tc<128>(a, Tbuf, c) : launch_tc<64>(a, Tbuf, c);

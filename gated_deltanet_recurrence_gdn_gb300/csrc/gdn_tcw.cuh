@@ -92,7 +92,8 @@ template <int DK>
 __device__ __forceinline__ void gdn_tcw_body(const CUtensorMap *tm_q, const CUtensorMap *tm_k,
                                              const CUtensorMap *tm_v, const CUtensorMap *tm_t,
                                              const CUtensorMap *tm_w, const TcParams &p,
-                                             const int wt, const int h, const int n) {
+                                             const int wt, const int h, const int n,
+                                             const int nseq) {
     using L = LayW<DK>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -102,7 +103,9 @@ __device__ __forceinline__ void gdn_tcw_body(const CUtensorMap *tm_q, const CUte
     float *gb = reinterpret_cast<float *>(sm + L::OFF_G);   // [2][GSZ]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // this CTA: d_v columns 128 wt .. 128 wt + 127 of (sequence n, head h)
+    // this CTA: d_v columns 128 wt .. 128 wt + 127 of (sequence n, head h);
+    // tiles wt >= xsplit compute a segment map's linear part instead (v = 0,
+    // h0 = identity, the d_k x d_k final state into hT2)
     long long row0 = 0;
     int len = 0, ytok0 = 0, zcoord = 0;
     bool ok_seq = true;
@@ -115,6 +118,14 @@ __device__ __forceinline__ void gdn_tcw_body(const CUtensorMap *tm_q, const CUte
         }
         ytok0 = a;
         zcoord = h;
+    } else if (p.segs > 0) {
+        // segment scan: sequence n = b * segs + segment
+        const int b = n / p.segs, sg = n - b * p.segs;
+        const int t0 = sg * p.seglen;
+        row0 = ((long long)b * p.sm.H + h) * (long long)p.sm.T + t0;
+        len = max(0, min(p.seglen, p.sm.T - t0));
+        ytok0 = t0;
+        zcoord = b * p.sm.H + h;
     } else {
         row0 = ((long long)n * p.sm.H + h) * (long long)p.sm.T;
         len = p.sm.T;
@@ -125,8 +136,11 @@ __device__ __forceinline__ void gdn_tcw_body(const CUtensorMap *tm_q, const CUte
         return;   // before any barrier or TMEM use
     }
     const int nch = (len + kC - 1) / kC;
-    const int vx0 = 128 * wt;                                     // first d_v column
-    const long long srow = ((long long)n * p.sm.H + h) * p.dv;   // state rows of (n, h)
+    const bool lin = wt >= p.xsplit;                              // linear-part CTA
+    const int vx0 = 128 * (lin ? wt - p.xsplit : wt);             // first state column
+    const int dvs = lin ? p.dv2 : p.dv;                          // width of this CTA's state
+    float *hTp = lin ? p.hT2 : p.hT;
+    const long long srow = ((long long)n * p.sm.H + h) * dvs;    // state rows of (n, h)
     const long long slot0 = p.sm.cu ? (long long)(ytok0 / kC) + n : (long long)n * p.max_chunks;
 
     if (warp == 9) {
@@ -151,7 +165,7 @@ __device__ __forceinline__ void gdn_tcw_body(const CUtensorMap *tm_q, const CUte
     // element counts of the global arrays, for the bounds-check build
     const long long nrows =
         p.sm.cu ? (long long)p.sm.H * p.sm.T_total : (long long)p.sm.N * p.sm.H * p.sm.T;
-    const long long nstate = (long long)p.sm.N * p.sm.H * p.dv * DK;
+    const long long nstate = (long long)nseq * p.sm.H * dvs * DK;
     (void)nrows;
     (void)nstate;
 
@@ -163,9 +177,10 @@ __device__ __forceinline__ void gdn_tcw_body(const CUtensorMap *tm_q, const CUte
         float hreg[64];
 #pragma unroll
         for (int c = 0; c < 64; ++c)
-            hreg[c] = (t < DK && p.h0 && GDN_IDX_OK((srow + dv0 + c) * DK + t, 1, nstate))
-                          ? __ldg(p.h0 + (srow + dv0 + c) * DK + t)
-                          : 0.f;
+            hreg[c] = lin ? ((t < DK && dv0 + c == t) ? 1.f : 0.f)
+                          : ((t < DK && p.h0 && GDN_IDX_OK((srow + dv0 + c) * DK + t, 1, nstate))
+                                 ? __ldg(p.h0 + (srow + dv0 + c) * DK + t)
+                                 : 0.f);
         uint8_t *Hs = sm + L::OFF_H + hf * L::HBLK;
         uint8_t *VT = sm + L::OFF_VT + hf * 8192, *VN = sm + L::OFF_VN + hf * 8192;
         // Output rows of chunk jj (lanes 64-127 of its accumulator, this
@@ -212,7 +227,8 @@ __device__ __forceinline__ void gdn_tcw_body(const CUtensorMap *tm_q, const CUte
             if (tid == 0) mbar_arrive(bar + W_HPUB);
             TRACE(0, j, 1, tid == 0);
             // (i') the previous chunk's output rows, off the state's path
-            if (j > 0 && t >= 64) store_o(j - 1);
+            const bool out = !p.no_output && !lin;
+            if (j > 0 && t >= 64 && out) store_o(j - 1);
             // (ii) V' = U - W H and its decayed copy V~ for the state update
             {
                 bool ok = ctl.wait(W_READY + (j % kNS), (j / kNS) & 1);   // this chunk's gates
@@ -279,12 +295,12 @@ __device__ __forceinline__ void gdn_tcw_body(const CUtensorMap *tm_q, const CUte
                 }
             }
         }
-        if (alive && nch > 0 && t >= 64) store_o(nch - 1);
-        if (alive && p.hT && t < DK) {
+        if (alive && nch > 0 && t >= 64 && !p.no_output && !lin) store_o(nch - 1);
+        if (alive && hTp && t < DK) {
 #pragma unroll
             for (int c = 0; c < 64; ++c)
                 if (GDN_IDX_OK((srow + dv0 + c) * DK + t, 1, nstate))
-                    p.hT[(srow + dv0 + c) * DK + t] = hreg[c];
+                    hTp[(srow + dv0 + c) * DK + t] = hreg[c];
         }
     } else if (warp == 8) {
         // ================================================= TMA producer
@@ -326,7 +342,7 @@ __device__ __forceinline__ void gdn_tcw_body(const CUtensorMap *tm_q, const CUte
             uint64_t *fb = bar + W_FULL + s;
             const int y = ytok0 + j * kC;
             if (lane == 0) {
-                mbar_arrive_expect_tx(fb, (uint32_t)L::STAGE);
+                mbar_arrive_expect_tx(fb, (uint32_t)(L::STAGE - (lin ? 16384 : 0)));
 #pragma unroll
                 for (int blk = 0; blk < L::KB; ++blk) {
                     tma_load_3d(stg + blk * 8192, tm_k, fb, blk * 64, y, zcoord);
@@ -334,8 +350,10 @@ __device__ __forceinline__ void gdn_tcw_body(const CUtensorMap *tm_q, const CUte
                     tma_load_3d(stg + L::OFF_WQ + blk * 16384 + 8192, tm_q, fb, blk * 64, y,
                                 zcoord);
                 }
-                tma_load_3d(stg + L::OFF_V, tm_v, fb, vx0, y, zcoord);
-                tma_load_3d(stg + L::OFF_V + 8192, tm_v, fb, vx0 + 64, y, zcoord);
+                if (!lin) {
+                    tma_load_3d(stg + L::OFF_V, tm_v, fb, vx0, y, zcoord);
+                    tma_load_3d(stg + L::OFF_V + 8192, tm_v, fb, vx0 + 64, y, zcoord);
+                }
                 tma_load_3d(stg + L::OFF_TU, tm_t, fb, 0, y, zcoord);
             }
             {
@@ -415,6 +433,13 @@ __device__ __forceinline__ void gdn_tcw_body(const CUtensorMap *tm_q, const CUte
         const int t = tid - 320, w = warp - 10;
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;   // TMEM lanes 64-127
         uint8_t *Pt = sm + L::OFF_P;
+        if (lin) {
+            // v = 0: the V tiles are never loaded, so clear them once (ordered
+            // before the first U product by this chunk's barriers)
+            for (int i = t; i < kNS * 1024; i += 64)
+                st16(sm + (i >> 10) * L::STAGE + L::OFF_V + (i & 1023) * 16, 0u, 0u, 0u, 0u);
+            fence_proxy_async_smem();
+        }
         for (int j = 0; j < nch; ++j) {
             const int s = j % kNS;
             uint8_t *stg = sm + s * L::STAGE;
@@ -584,9 +609,10 @@ __global__ void __launch_bounds__(kThreadsW, 1)
 k_gdn_tcw(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
           const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_t,
           const __grid_constant__ CUtensorMap tm_w, TcParams p) {
-    const int tiles = p.dv / 128, b = (int)blockIdx.x, hn = b / tiles;
+    // block b: tile b % tiles of head (b / tiles) % H of sequence b / (tiles H)
+    const int tiles = p.xsplit + p.lin_tiles, b = (int)blockIdx.x, hn = b / tiles;
     gdn_tcw_body<DK>(&tm_q, &tm_k, &tm_v, &tm_t, &tm_w, p, b - hn * tiles, hn % p.sm.H,
-                     hn / p.sm.H);
+                     hn / p.sm.H, gridDim.x / (tiles * p.sm.H));
 }
 
 // The overlapped launch with the wide chunk loop: roles below nchain (one per
@@ -599,9 +625,9 @@ k_gdn_tcw_ov(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
              int by_sm) {
     const int role = ov_role(by_sm);
     if (role < nchain) {
-        const int tiles = p.dv / 128, hn = role / tiles;
+        const int tiles = p.xsplit, hn = role / tiles;
         gdn_tcw_body<DK>(&tm_q, &tm_k, &tm_v, &tm_t, &tm_w, p, role - hn * tiles, hn % p.sm.H,
-                         hn / p.sm.H);
+                         hn / p.sm.H, p.sm.N);
         return;
     }
     ov_prep_role<DK>(&tm_k, up, role, nchain);

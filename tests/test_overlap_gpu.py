@@ -235,3 +235,28 @@ def test_automatic_path_on_gb300(B, H, T, dk, dv, kernel):
     finally:
         gdn.kernel_timer(False)
     assert n == 1 and name == kernel, (n, name)
+
+
+@pytest.mark.parametrize("segments", [2, 3, 5])
+@pytest.mark.parametrize("dv", [128, 256])
+def test_wide_segment_scan(segments, dv):
+    # the segment scan with the wide chunk loop (maps from zero and from the
+    # identity, one CTA each, then every segment from its folded state):
+    # against the oracle and the scan with the 64-column loop
+    x = synth.make_dense(2, 2, 9 * 64 + 13, 128, dv, io="bf16", h0_std=0.05,
+                         seed=681 + segments + dv, device="cuda")
+    x = dataclasses.replace(x, log_alpha=_steep(x.log_alpha, [(192, -3.0), (320, -1.3)]))
+
+    def run(wide):
+        with gdn.use_impl(gdn.GDN_IMPL_TC, segments), prep_lead(0, wide):
+            o, hT = gdn.gdn_fwd(x.q, x.k, x.v, x.log_alpha, x.beta, x.h0, check=True)
+        U.sync()
+        return o, hT
+
+    o, hT = run(1)
+    o_ref, h_ref = U.oracle_dense(x)
+    to, th = U.TOL["bf16"]
+    assert U.rel(U.f64(o), o_ref.reshape(o.shape)) <= to
+    assert U.rel(U.f64(hT), h_ref.reshape(hT.shape)) <= th
+    o1, h1 = run(0)
+    assert U.rel(U.f64(o), U.f64(o1)) <= 1e-3 and U.rel(U.f64(hT), U.f64(h1)) <= 1e-3
