@@ -1125,12 +1125,14 @@ gdn_status launch_tcw(const FwdArgs &a, const __nv_bfloat16 *Tin, const LaunchCf
 // Exclusive fold of the segment maps ("Gated DeltaNet GPU并行实现", sections
 // 2.3 and 3.3): with S -> S A_i + B_i the map of segment i (earlier map
 // first), the state entering segment i+1 is S_in[i] A_i + B_i, S_in[0] = h0.
-// One CTA per (batch, head, 16 state rows), fp32.
+// One CTA per (batch, head, 16 state rows), fp32; each map A_i is staged in
+// shared memory (d_k^2 floats) before its product.
 __global__ void __launch_bounds__(256)
 k_seg_fold(const float *__restrict__ h0, const float *__restrict__ Aseg,
            const float *__restrict__ Bseg, float *__restrict__ Sin, int B, int H, int segs,
            int dv, int dk) {
-    extern __shared__ float Sr[];   // [16][dk]
+    extern __shared__ float Sr[];   // [16][dk], then A_m [dk][dk]
+    float *As = Sr + 16 * dk;
     const int tid = threadIdx.x;
     const int bh = blockIdx.x, b = bh / H, h = bh - b * H, r0 = blockIdx.y * 16;
     const int tot = 16 * dk;
@@ -1149,16 +1151,26 @@ k_seg_fold(const float *__restrict__ h0, const float *__restrict__ Aseg,
         const long long m = (long long)b * (segs - 1) + sg;
         const float *Am = Aseg + (m * H + h) * (long long)dk * dk;
         const float *Bm = Bseg + ((m * H + h) * dv + r0) * (long long)dk;
+        // A_m into shared memory (the 16-row blocks of one (batch, head) all
+        // read it), 16-byte pieces
+        for (int i = tid; i < dk * dk / 4; i += 256)
+            reinterpret_cast<float4 *>(As)[i] = __ldg(reinterpret_cast<const float4 *>(Am) + i);
+        __syncthreads();
+        // entry i = tid + 256 e of the 16 x dk block is row tid / dk + e (256 / dk),
+        // column tid % dk (dk divides 256): a thread's entries share their
+        // column, so one read of A per kk feeds all of them, and their eight
+        // sums run side by side (each in the order kk = 0 .. dk - 1)
+        const int cc = tid % dk, rb = tid / dk, rs = 256 / dk, ne = tot / 256;
         float acc[8];   // 16 * dk / 256 <= 8 entries per thread
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const int i = tid + 256 * e;
-            if (i < tot) {
-                const int r = i / dk, cc = i - r * dk;
-                float x = Bm[(long long)r * dk + cc];
-                for (int kk = 0; kk < dk; ++kk) x = fmaf(Sr[r * dk + kk], Am[kk * dk + cc], x);
-                acc[e] = x;
-            }
+        for (int e = 0; e < 8; ++e)
+            acc[e] = e < ne ? Bm[(long long)(rb + rs * e) * dk + cc] : 0.f;
+#pragma unroll 4
+        for (int kk = 0; kk < dk; ++kk) {
+            const float a = As[kk * dk + cc];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                if (e < ne) acc[e] = fmaf(Sr[(rb + rs * e) * dk + kk], a, acc[e]);
         }
         __syncthreads();
 #pragma unroll
@@ -1363,10 +1375,15 @@ gdn_status tc_segmented(const FwdArgs &a, const __nv_bfloat16 *Tbuf, int S, bool
     if (rc == GDN_OK) {
         // pass 2: fold the maps into every segment's initial state
         dim3 grid(B * H, dv / 16);
-        k_seg_fold<<<grid, 256, 16 * dk * sizeof(float), st>>>(a.h0, Aseg, Bseg, Sin, B, H, S,
-                                                               dv, dk);
-        count_launch();
-        if (cudaGetLastError() != cudaSuccess) rc = GDN_ERR_CUDA;
+        const int fsm = (16 * dk + dk * dk) * (int)sizeof(float);   // 72 KB at d_k = 128
+        if (cudaFuncSetAttribute(k_seg_fold, cudaFuncAttributeMaxDynamicSharedMemorySize, fsm) !=
+            cudaSuccess) {
+            rc = GDN_ERR_CUDA;
+        } else {
+            k_seg_fold<<<grid, 256, fsm, st>>>(a.h0, Aseg, Bseg, Sin, B, H, S, dv, dk);
+            count_launch();
+            if (cudaGetLastError() != cudaSuccess) rc = GDN_ERR_CUDA;
+        }
     }
     if (rc == GDN_OK) {
         // pass 3: every segment from its true initial state, with outputs
