@@ -174,10 +174,18 @@ struct TcParams {
     int *err;
     int dv;
     uint32_t wait_limit;
-    // Segment scan (dense batches): sequence n = b * segs + segment, covering
-    // tokens [segment * seglen, min(T, (segment + 1) * seglen)); segs = 0: off.
-    int segs, seglen;
+    // Segment scan (dense batches): sequence n = b * segs + segment; segment 0
+    // covers tokens [0, seglen0), segment s > 0 [seglen0 + (s - 1) seglen, +
+    // seglen), clipped to T; segs = 0: off.  The wide loop's launch covers
+    // segments seg_lo .. segs - 1 of every sequence, segment-major.
+    int segs, seglen, seglen0, seg_lo;
     int no_output;   // 1: skip o (state-only pass)
+    // Wide loop, first pass of a segment scan: segment 0 runs as the final
+    // pass would (from h0x, row b of [N][H][d_v][d_k], with outputs; its
+    // final state into hT like the other segments' affine parts) and has no
+    // linear-part tile.
+    int seg0_full;
+    const float *h0x;
     // CTAs with blockIdx.x >= xsplit run the map's linear part instead: v = 0,
     // h0 = identity (d_k x d_k state), final state into hT2 with width dv2.
     int xsplit, dv2;
@@ -197,6 +205,12 @@ struct TcParams {
     const uint32_t *done;
     int prep_c0;
 };
+
+// Tokens [t0, t0 + len) of segment sg of a segment scan.
+__device__ __forceinline__ void seg_range(const TcParams &p, int sg, int &t0, int &len) {
+    t0 = sg == 0 ? 0 : p.seglen0 + (sg - 1) * p.seglen;
+    len = max(0, min(sg == 0 ? p.seglen0 : p.seglen, p.sm.T - t0));
+}
 
 // The kernel body.  STATES: the backward's state pass (stores Hst / Vst),
 // a separate kernel (k_gdn_tc_states), so the forward's k_gdn_tc carries
@@ -240,9 +254,9 @@ __device__ __forceinline__ void gdn_tc_body(const CUtensorMap *tm_q, const CUten
         zcoord = h;
     } else if (p.segs > 0) {
         const int b = n / p.segs, sg = n - b * p.segs;
-        const int t0 = sg * p.seglen;
+        int t0;
+        seg_range(p, sg, t0, len);
         row0 = ((long long)b * p.sm.H + h) * (long long)p.sm.T + t0;
-        len = max(0, min(p.seglen, p.sm.T - t0));
         ytok0 = t0;
         zcoord = b * p.sm.H + h;
     } else {
@@ -935,6 +949,10 @@ struct LaunchCfg {
     float *hT2;
     bool timed;
     float *Hst = nullptr, *Vst = nullptr;   // the backward's state pass
+    int seglen0 = 0;                        // segment 0's tokens (0: seglen)
+    int seg_lo = 0;                         // first segment launched (wide loop)
+    const float *h0x = nullptr;             // wide loop: segment 0 from h0x with outputs
+    bool seg0_full = false;
 };
 
 // The bulk-copy maps of a chain launch: q, k, v, T_u, W (T_u's rows, then W's,
@@ -962,6 +980,10 @@ TcParams tc_params(const FwdArgs &a, int dk, const LaunchCfg &c) {
     p.wait_limit = lim > 0 ? (uint32_t)(lim > 0x7fffffffLL ? 0x7fffffffLL : lim) : (1u << 22);
     p.segs = c.segs;
     p.seglen = c.seglen;
+    p.seglen0 = c.seglen0 > 0 ? c.seglen0 : c.seglen;
+    p.seg_lo = c.seg_lo;
+    p.seg0_full = c.seg0_full ? 1 : 0;
+    p.h0x = c.h0x;
     p.no_output = c.no_output;
     p.xsplit = a.dv / kNV;
     p.dv2 = dk;
@@ -1126,22 +1148,28 @@ gdn_status launch_tcw(const FwdArgs &a, const __nv_bfloat16 *Tin, const LaunchCf
 // 2.3 and 3.3): with S -> S A_i + B_i the map of segment i (earlier map
 // first), the state entering segment i+1 is S_in[i] A_i + B_i, S_in[0] = h0.
 // One CTA per (batch, head, 16 state rows), fp32; each map A_i is staged in
-// shared memory (d_k^2 floats) before its product.
+// shared memory (d_k^2 floats) before its product.  first_full: segment 0
+// ran from h0 itself, so B_0 is already the state entering segment 1 (and
+// there is no A_0).
 __global__ void __launch_bounds__(256)
 k_seg_fold(const float *__restrict__ h0, const float *__restrict__ Aseg,
            const float *__restrict__ Bseg, float *__restrict__ Sin, int B, int H, int segs,
-           int dv, int dk) {
+           int dv, int dk, int first_full) {
     extern __shared__ float Sr[];   // [16][dk], then A_m [dk][dk]
     float *As = Sr + 16 * dk;
     const int tid = threadIdx.x;
     const int bh = blockIdx.x, b = bh / H, h = bh - b * H, r0 = blockIdx.y * 16;
     const int tot = 16 * dk;
+    // the state entering the first folded segment: rows r0.. of B_0 or h0
+    const float *src = first_full ? Bseg + ((long long)b * (segs - 1) * H + h) * dv * dk
+                       : h0       ? h0 + (long long)bh * dv * dk
+                                  : nullptr;
     for (int i = tid; i < tot; i += 256) {
         const int r = i / dk, cc = i - r * dk;
-        Sr[i] = h0 ? h0[((long long)bh * dv + r0 + r) * dk + cc] : 0.f;
+        Sr[i] = src ? src[(long long)(r0 + r) * dk + cc] : 0.f;
     }
     __syncthreads();
-    for (int sg = 0; sg < segs; ++sg) {
+    for (int sg = first_full ? 1 : 0; sg < segs; ++sg) {
         const long long n = (long long)b * segs + sg;
         for (int i = tid; i < tot; i += 256) {
             const int r = i / dk, cc = i - r * dk;
@@ -1260,25 +1288,71 @@ bool seg_wide_applies(const FwdArgs &a) {
     return opt > 0 || option(GDN_OPT_SEGMENTS) < 1;
 }
 
-// Segments for the wide segment scan: the count that minimises the chunk
-// periods of its two passes, (waves of pass 1 + waves of pass 3) x chunks per
-// segment, plus the fold's ≈ 10 chunk periods per segment boundary.  Pass 1
-// has B H (d_v / 128 + 1) CTAs per segment but the last, pass 3 B H d_v / 128
-// per segment; a wave is one CTA per SM.  B1 H16 T131072 d128: 9 segments
-// (2.37 ms at 8, 2.49 at 5, 2.96 for the 64-column scan at 3).
-int choose_segments_wide(const FwdArgs &a) {
+// The wide segment scan's plan, in chunks.  With head, its first launch runs
+// segment 0 in full (from h0, with outputs) on B H d_v / 128 SMs while the
+// other SMs form the maps of segments 1 .. S - 2 (B H (d_v / 128 + 1) CTAs
+// per segment, w1 waves), and its last launch runs segments 1 .. S - 1 (w3
+// waves).  The maps' pass forms no output, its chunk period r = kMapPeriod /
+// 1000 of the full one (measured at B1 H16 T131072 d128: 2.04 against 2.81
+// us); segment 0 takes as many chunks as the map CTAs' waves take time,
+// L0 = r w1 L, the others L = ceil(M / (r w1 + S - 1)).  Cost, in full chunk
+// periods: max(L0, r w1 L) + w3 L + kFoldPeriods per fold step.  Without
+// head (equal segments, maps of segments 0 .. S - 2, then all S in full):
+// (r w1 + w3) ceil(M / S) + the fold; the cheaper of the two is taken.
+constexpr long long kMapPeriod = 730;
+constexpr long long kFoldPeriods = 4;
+struct SegPlan {
+    int S = 1, L0 = 0, L = 0;   // segments; chunks of segment 0 and of the others
+    bool head = false;
+    double cost = 0.0;
+};
+SegPlan plan_wide(const FwdArgs &a, int S) {
+    SegPlan pl;
     const long long M = a.max_chunks, nsm = sm_count();
-    const long long bh = (long long)a.sm.N * a.sm.H, v = a.dv / 128;
+    const long long bh = (long long)a.sm.N * a.sm.H, v = a.dv / 128, nh = bh * v;
+    if (S < 2 || M < 2) return pl;
+    const double r = kMapPeriod / 1000.0;
+    // equal segments
+    {
+        const long long L = (M + S - 1) / S, Sr = (M + L - 1) / L;
+        const long long w1 = (bh * (v + 1) * (Sr - 1) + nsm - 1) / nsm;
+        const long long w3 = (nh * Sr + nsm - 1) / nsm;
+        pl.S = (int)Sr;
+        pl.L0 = pl.L = (int)L;
+        pl.cost = (r * (double)w1 + (double)w3) * (double)L + (double)(kFoldPeriods * (Sr - 1));
+    }
+    if (nh >= nsm || S < 3) return pl;
+    const long long n1 = bh * (v + 1) * (S - 2);
+    const long long w1 = (n1 + (nsm - nh) - 1) / (nsm - nh);
+    long long L = (long long)std::ceil((double)M / (r * (double)w1 + (double)(S - 1)));
+    L = L < 1 ? 1 : L;
+    long long L0 = M - (S - 1) * L;
+    if (L0 < 1) L0 = std::min<long long>(M - 1, std::max<long long>(1, (long long)(r * w1 * L)));
+    const long long Sr = 1 + (M - L0 + L - 1) / L;   // no empty segments
+    const long long w3 = (nh * (Sr - 1) + nsm - 1) / nsm;
+    const double cost = std::max((double)L0, r * (double)w1 * (double)L) +
+                        (double)(w3 * L) + (double)(kFoldPeriods * (Sr - 1));
+    if (Sr >= 2 && cost < pl.cost) {
+        pl.S = (int)Sr;
+        pl.L0 = (int)L0;
+        pl.L = (int)L;
+        pl.head = true;
+        pl.cost = cost;
+    }
+    return pl;
+}
+
+// Segments for the wide segment scan: the count whose plan costs least.
+int choose_segments_wide(const FwdArgs &a) {
+    const int smax = a.max_chunks < 64 ? a.max_chunks : 64;
     int best = 1;
-    long long best_cost = -1;
-    const long long smax = M < 64 ? M : 64;
-    for (long long S = 2; S <= smax; ++S) {
-        const long long w1 = (bh * (v + 1) * (S - 1) + nsm - 1) / nsm;
-        const long long w3 = (bh * v * S + nsm - 1) / nsm;
-        const long long cost = (w1 + w3) * ((M + S - 1) / S) + 10 * (S - 1);
-        if (best_cost < 0 || cost < best_cost) {
-            best_cost = cost;
-            best = (int)S;
+    double best_cost = -1.0;
+    for (int S = 2; S <= smax; ++S) {
+        const SegPlan pl = plan_wide(a, S);
+        if (pl.S < 2) continue;
+        if (best_cost < 0.0 || pl.cost < best_cost) {
+            best_cost = pl.cost;
+            best = S;
         }
     }
     return best;
@@ -1346,8 +1420,16 @@ gdn_status tc_overlapped(const FwdArgs &a, __nv_bfloat16 *Tbuf, int lead, int nc
 gdn_status tc_segmented(const FwdArgs &a, const __nv_bfloat16 *Tbuf, int S, bool wide) {
     cudaStream_t st = a.stream;
     const int nch = a.max_chunks;
-    const int seglen = ((nch + S - 1) / S) * kC;
+    int seglen = ((nch + S - 1) / S) * kC, seglen0 = seglen;
     S = (a.sm.T + seglen - 1) / seglen;   // no empty segments
+    // the wide loop may run segment 0 in full beside the other segments' maps
+    const SegPlan pl = wide ? plan_wide(a, S) : SegPlan{};
+    const bool head = pl.head;
+    if (head) {
+        S = pl.S;
+        seglen = pl.L * kC;
+        seglen0 = pl.L0 * kC;
+    }
     const int B = a.sm.N, H = a.sm.H, dv = a.dv, dk = a.dk;
     auto pass = [&](const LaunchCfg &c) {
         if (wide) return dk == 128 ? launch_tcw<128>(a, Tbuf, c) : launch_tcw<64>(a, Tbuf, c);
@@ -1368,8 +1450,13 @@ gdn_status tc_segmented(const FwdArgs &a, const __nv_bfloat16 *Tbuf, int S, bool
         rc = GDN_ERR_CUDA;
     if (rc == GDN_OK) {
         // pass 1: per segment but the last, the map's affine part (final state
-        // from zero) and linear part (final state from the identity, v = 0)
+        // from zero) and linear part (final state from the identity, v = 0);
+        // with head, segment 0 instead runs in full, its final state the
+        // true one entering segment 1
         LaunchCfg c1{B * (S - 1), S - 1, seglen, 1, nullptr, Bseg, lin_tiles, Aseg, false};
+        c1.seglen0 = seglen0;
+        c1.seg0_full = head;
+        c1.h0x = a.h0;
         rc = pass(c1);
     }
     if (rc == GDN_OK) {
@@ -1380,14 +1467,18 @@ gdn_status tc_segmented(const FwdArgs &a, const __nv_bfloat16 *Tbuf, int S, bool
             cudaSuccess) {
             rc = GDN_ERR_CUDA;
         } else {
-            k_seg_fold<<<grid, 256, fsm, st>>>(a.h0, Aseg, Bseg, Sin, B, H, S, dv, dk);
+            k_seg_fold<<<grid, 256, fsm, st>>>(a.h0, Aseg, Bseg, Sin, B, H, S, dv, dk,
+                                               head ? 1 : 0);
             count_launch();
             if (cudaGetLastError() != cudaSuccess) rc = GDN_ERR_CUDA;
         }
     }
     if (rc == GDN_OK) {
         // pass 3: every segment from its true initial state, with outputs
-        LaunchCfg c3{B * S, S, seglen, 0, Sin, Hout, 0, nullptr, true};
+        // (from segment 1 on with head)
+        LaunchCfg c3{B * (S - (head ? 1 : 0)), S, seglen, 0, Sin, Hout, 0, nullptr, true};
+        c3.seglen0 = seglen0;
+        c3.seg_lo = head ? 1 : 0;
         rc = pass(c3);
     }
     if (rc == GDN_OK && a.hT) {

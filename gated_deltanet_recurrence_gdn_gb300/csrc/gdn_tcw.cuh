@@ -35,6 +35,9 @@
 // (2 x 128) and U / dH (128) take 448 of the 512 columns; one P' buffer
 // (the next chunk's Gram, which the P' warps wait for, completes after the
 // output product that read it).
+// A state-only pass (the first pass of a segment scan) needs H alone: Q is
+// not copied, and neither the Gram, P' nor the output product is formed, so
+// the tensor pipe carries [W; Q] H, U and K^T V~ per chunk.
 
 constexpr int kThreadsW = 384;   // chain warps 0-7, copy warp 8, MMA warp 9, gate / P' warps 10-11
 
@@ -88,7 +91,8 @@ struct LayW {
 // TMEM columns (512 allocated)
 constexpr uint32_t TW_G = 0, TW_M2 = 64, TW_UH = 320;
 
-template <int DK>
+// SEG: the segment scan's views (k_gdn_tcw); the overlapped launch has none.
+template <int DK, bool SEG>
 __device__ __forceinline__ void gdn_tcw_body(const CUtensorMap *tm_q, const CUtensorMap *tm_k,
                                              const CUtensorMap *tm_v, const CUtensorMap *tm_t,
                                              const CUtensorMap *tm_w, const TcParams &p,
@@ -108,7 +112,8 @@ __device__ __forceinline__ void gdn_tcw_body(const CUtensorMap *tm_q, const CUte
     // h0 = identity, the d_k x d_k final state into hT2)
     long long row0 = 0;
     int len = 0, ytok0 = 0, zcoord = 0;
-    bool ok_seq = true;
+    bool ok_seq = true, head = false;
+    int bseq = n;   // the batch row of (n, h) in h0x
     if (p.sm.cu) {
         const int a = __ldg(p.sm.cu + n), b = __ldg(p.sm.cu + n + 1);
         ok_seq = a >= 0 && a <= b && b <= p.sm.T_total;
@@ -118,14 +123,16 @@ __device__ __forceinline__ void gdn_tcw_body(const CUtensorMap *tm_q, const CUte
         }
         ytok0 = a;
         zcoord = h;
-    } else if (p.segs > 0) {
+    } else if (SEG && p.segs > 0) {
         // segment scan: sequence n = b * segs + segment
         const int b = n / p.segs, sg = n - b * p.segs;
-        const int t0 = sg * p.seglen;
+        int t0;
+        seg_range(p, sg, t0, len);
         row0 = ((long long)b * p.sm.H + h) * (long long)p.sm.T + t0;
-        len = max(0, min(p.seglen, p.sm.T - t0));
         ytok0 = t0;
         zcoord = b * p.sm.H + h;
+        head = p.seg0_full && sg == 0;
+        bseq = b;
     } else {
         row0 = ((long long)n * p.sm.H + h) * (long long)p.sm.T;
         len = p.sm.T;
@@ -137,10 +144,16 @@ __device__ __forceinline__ void gdn_tcw_body(const CUtensorMap *tm_q, const CUte
     }
     const int nch = (len + kC - 1) / kC;
     const bool lin = wt >= p.xsplit;                              // linear-part CTA
+    if (head && lin) return;   // segment 0 from the true h0: no map to form
+    // state-only pass (a segment scan's first): no Q, Gram, P' or output product
+    const bool so = SEG && p.no_output != 0 && !head;
     const int vx0 = 128 * (lin ? wt - p.xsplit : wt);             // first state column
     const int dvs = lin ? p.dv2 : p.dv;                          // width of this CTA's state
     float *hTp = lin ? p.hT2 : p.hT;
     const long long srow = ((long long)n * p.sm.H + h) * dvs;    // state rows of (n, h)
+    // initial state: h0 at (n, h), or for segment 0 run in full h0x at (b, h)
+    const float *h0p = head ? p.h0x : p.h0;
+    const long long srow0 = head ? ((long long)bseq * p.sm.H + h) * dvs : srow;
     const long long slot0 = p.sm.cu ? (long long)(ytok0 / kC) + n : (long long)n * p.max_chunks;
 
     if (warp == 9) {
@@ -166,8 +179,10 @@ __device__ __forceinline__ void gdn_tcw_body(const CUtensorMap *tm_q, const CUte
     const long long nrows =
         p.sm.cu ? (long long)p.sm.H * p.sm.T_total : (long long)p.sm.N * p.sm.H * p.sm.T;
     const long long nstate = (long long)nseq * p.sm.H * dvs * DK;
+    const long long nstate0 = head ? (long long)p.sm.N * p.sm.H * dvs * DK : nstate;
     (void)nrows;
     (void)nstate;
+    (void)nstate0;
 
     if (warp < 8) {
         // ====================================== chain: two halves of d_v
@@ -178,8 +193,9 @@ __device__ __forceinline__ void gdn_tcw_body(const CUtensorMap *tm_q, const CUte
 #pragma unroll
         for (int c = 0; c < 64; ++c)
             hreg[c] = lin ? ((t < DK && dv0 + c == t) ? 1.f : 0.f)
-                          : ((t < DK && p.h0 && GDN_IDX_OK((srow + dv0 + c) * DK + t, 1, nstate))
-                                 ? __ldg(p.h0 + (srow + dv0 + c) * DK + t)
+                          : ((t < DK && h0p &&
+                              GDN_IDX_OK((srow0 + dv0 + c) * DK + t, 1, nstate0))
+                                 ? __ldg(h0p + (srow0 + dv0 + c) * DK + t)
                                  : 0.f);
         uint8_t *Hs = sm + L::OFF_H + hf * L::HBLK;
         uint8_t *VT = sm + L::OFF_VT + hf * 8192, *VN = sm + L::OFF_VN + hf * 8192;
@@ -227,7 +243,7 @@ __device__ __forceinline__ void gdn_tcw_body(const CUtensorMap *tm_q, const CUte
             if (tid == 0) mbar_arrive(bar + W_HPUB);
             TRACE(0, j, 1, tid == 0);
             // (i') the previous chunk's output rows, off the state's path
-            const bool out = !p.no_output && !lin;
+            const bool out = !so && !lin;
             if (j > 0 && t >= 64 && out) store_o(j - 1);
             // (ii) V' = U - W H and its decayed copy V~ for the state update
             {
@@ -295,7 +311,7 @@ __device__ __forceinline__ void gdn_tcw_body(const CUtensorMap *tm_q, const CUte
                 }
             }
         }
-        if (alive && nch > 0 && t >= 64 && !p.no_output && !lin) store_o(nch - 1);
+        if (alive && nch > 0 && t >= 64 && !so && !lin) store_o(nch - 1);
         if (alive && hTp && t < DK) {
 #pragma unroll
             for (int c = 0; c < 64; ++c)
@@ -342,13 +358,15 @@ __device__ __forceinline__ void gdn_tcw_body(const CUtensorMap *tm_q, const CUte
             uint64_t *fb = bar + W_FULL + s;
             const int y = ytok0 + j * kC;
             if (lane == 0) {
-                mbar_arrive_expect_tx(fb, (uint32_t)(L::STAGE - (lin ? 16384 : 0)));
+                mbar_arrive_expect_tx(fb, (uint32_t)(L::STAGE - (lin ? 16384 : 0) -
+                                                     (so ? L::KB * 8192 : 0)));
 #pragma unroll
                 for (int blk = 0; blk < L::KB; ++blk) {
                     tma_load_3d(stg + blk * 8192, tm_k, fb, blk * 64, y, zcoord);
                     tma_load_3d(stg + L::OFF_WQ + blk * 16384, tm_w, fb, blk * 64, y, zcoord);
-                    tma_load_3d(stg + L::OFF_WQ + blk * 16384 + 8192, tm_q, fb, blk * 64, y,
-                                zcoord);
+                    if (!so)
+                        tma_load_3d(stg + L::OFF_WQ + blk * 16384 + 8192, tm_q, fb, blk * 64, y,
+                                    zcoord);
                 }
                 if (!lin) {
                     tma_load_3d(stg + L::OFF_V, tm_v, fb, vx0, y, zcoord);
@@ -414,7 +432,9 @@ __device__ __forceinline__ void gdn_tcw_body(const CUtensorMap *tm_q, const CUte
                 for (int kk = 0; kk < kC / 16; ++kk) {
                     mma_bf16(tmem + TW_UH, dKT + ((soff + kk * 2048) >> 4),
                              dVT + ((kk * 2048) >> 4), idKT, kk > 0);
-                    mma_bf16(acc, dXP + ((kk * 32) >> 4), dVN + ((kk * 2048) >> 4), idN, 1u);
+                    if (!so)
+                        mma_bf16(acc, dXP + ((kk * 32) >> 4), dVN + ((kk * 2048) >> 4), idN,
+                                 1u);
                 }
                 mma_commit(bar + W_M34);
                 mma_commit(bar + W_PFREE);
@@ -438,8 +458,18 @@ __device__ __forceinline__ void gdn_tcw_body(const CUtensorMap *tm_q, const CUte
             // before the first U product by this chunk's barriers)
             for (int i = t; i < kNS * 1024; i += 64)
                 st16(sm + (i >> 10) * L::STAGE + L::OFF_V + (i & 1023) * 16, 0u, 0u, 0u, 0u);
-            fence_proxy_async_smem();
         }
+        if (so) {
+            // Q is never loaded in a state-only pass: clear its blocks once
+            // (ordered before the first [W; Q] H by the W_WQ arrival), so that
+            // the product's unread output rows stay finite
+            for (int i = t; i < kNS * L::KB * 512; i += 64) {
+                const int s = i / (L::KB * 512), r = i - s * (L::KB * 512);
+                st16(sm + s * L::STAGE + L::OFF_WQ + (r >> 9) * 16384 + 8192 + (r & 511) * 16,
+                     0u, 0u, 0u, 0u);
+            }
+        }
+        if (lin || so) fence_proxy_async_smem();
         for (int j = 0; j < nch; ++j) {
             const int s = j % kNS;
             uint8_t *stg = sm + s * L::STAGE;
@@ -499,14 +529,14 @@ __device__ __forceinline__ void gdn_tcw_body(const CUtensorMap *tm_q, const CUte
             // rows take gamma_r at the end, P' is formed divided by gamma_r),
             // once the previous chunk's chain MMA has read its own copy (the
             // mbarrier then never runs two phases ahead of its waiter)
-            if (span_ok) {
+            if (span_ok || so) {
                 if (!named_bar_and(4, 64, j == 0 || ctl.wait(W_M2, (j - 1) & 1))) break;
                 if (t == 0) mbar_arrive(bar + W_WQ);
             }
             // this chunk's Gram [W; Q] K^T (its Q rows give P'), behind the
             // previous chunk's state and output products (the G(j - 1) rows
             // were read above, before the last barrier)
-            if (t == 0) {
+            if (t == 0 && !so) {
                 if (j == 0 || ctl.wait(W_M34I, (j - 1) & 1)) {
                     tc_fence_after();
                     const uint32_t sbase = smem_u32(sm), soff = s * L::STAGE;
@@ -522,12 +552,14 @@ __device__ __forceinline__ void gdn_tcw_body(const CUtensorMap *tm_q, const CUte
                 }
             }
             // P' from the Gram's Q rows, once the previous P' was read
-            bool okg = ctl.wait(W_G, j & 1);
+            // (a state-only pass forms neither: the P' barriers still pace
+            // these warps one chunk ahead of the issuer at most)
+            bool okg = so || ctl.wait(W_G, j & 1);
             if (j > 0) okg = okg && ctl.wait(W_PFREE, (j - 1) & 1);
             if (!named_bar_and(4, 64, okg)) break;
             TRACE(1, j, 2, t == 0);
             tc_fence_after();
-            {
+            if (!so) {
                 const int r = t;
                 uint32_t g0[32], g1[32];
                 tmem_ld32(tmem + lane_base + TW_G, g0);
@@ -556,7 +588,7 @@ __device__ __forceinline__ void gdn_tcw_body(const CUtensorMap *tm_q, const CUte
             named_bar(4, 64);
             if (t == 0) mbar_arrive(bar + W_PREADY);
             TRACE(1, j, 3, t == 0);
-            if (!span_ok) {
+            if (!span_ok && !so) {
                 // the Gram has read Q: gamma Q in place (row t of every Q
                 // block: loads first, then stores), then [W; gamma Q]
                 const float gam = gj[128 + t];
@@ -590,7 +622,7 @@ __device__ __forceinline__ void gdn_tcw_body(const CUtensorMap *tm_q, const CUte
             if (t == 0) mbar_arrive(bar + W_FREE + s);
         }
         // every Gram issued here has finished before TMEM is released
-        if (t == 0 && nch > 0) {
+        if (t == 0 && nch > 0 && !so) {
             mma_commit(bar + W_DRAIN2);
             mbar_wait(bar + W_DRAIN2, 0, ctl.limit);
         }
@@ -609,10 +641,19 @@ __global__ void __launch_bounds__(kThreadsW, 1)
 k_gdn_tcw(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
           const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_t,
           const __grid_constant__ CUtensorMap tm_w, TcParams p) {
-    // block b: tile b % tiles of head (b / tiles) % H of sequence b / (tiles H)
+    // block b: tile b % tiles of head (b / tiles) % H of sequence b / (tiles H);
+    // in a segment scan the sequences run segment-major (segment seg_lo of
+    // every batch row first), so the longest CTAs start in the first wave
     const int tiles = p.xsplit + p.lin_tiles, b = (int)blockIdx.x, hn = b / tiles;
-    gdn_tcw_body<DK>(&tm_q, &tm_k, &tm_v, &tm_t, &tm_w, p, b - hn * tiles, hn % p.sm.H,
-                     hn / p.sm.H, gridDim.x / (tiles * p.sm.H));
+    const int h = hn % p.sm.H, q = hn / p.sm.H;
+    if (p.segs > 0) {
+        const int sg = p.seg_lo + q / p.sm.N, bb = q - (q / p.sm.N) * p.sm.N;
+        gdn_tcw_body<DK, true>(&tm_q, &tm_k, &tm_v, &tm_t, &tm_w, p, b - hn * tiles, h,
+                               bb * p.segs + sg, p.sm.N * p.segs);
+    } else {
+        gdn_tcw_body<DK, true>(&tm_q, &tm_k, &tm_v, &tm_t, &tm_w, p, b - hn * tiles, h, q,
+                               gridDim.x / (tiles * p.sm.H));
+    }
 }
 
 // The overlapped launch with the wide chunk loop: roles below nchain (one per
@@ -626,8 +667,8 @@ k_gdn_tcw_ov(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     const int role = ov_role(by_sm);
     if (role < nchain) {
         const int tiles = p.xsplit, hn = role / tiles;
-        gdn_tcw_body<DK>(&tm_q, &tm_k, &tm_v, &tm_t, &tm_w, p, role - hn * tiles, hn % p.sm.H,
-                         hn / p.sm.H, p.sm.N);
+        gdn_tcw_body<DK, false>(&tm_q, &tm_k, &tm_v, &tm_t, &tm_w, p, role - hn * tiles,
+                                hn % p.sm.H, hn / p.sm.H, p.sm.N);
         return;
     }
     ov_prep_role<DK>(&tm_k, up, role, nchain);

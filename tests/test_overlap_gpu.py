@@ -260,3 +260,27 @@ def test_wide_segment_scan(segments, dv):
     assert U.rel(U.f64(hT), h_ref.reshape(hT.shape)) <= th
     o1, h1 = run(0)
     assert U.rel(U.f64(o), U.f64(o1)) <= 1e-3 and U.rel(U.f64(hT), U.f64(h1)) <= 1e-3
+
+
+@pytest.mark.parametrize("segments", [0, 10])
+def test_wide_segment_scan_first_segment_in_full(segments):
+    # 16 heads x 257 chunks (the last ragged): on a 152-SM device the plan
+    # runs segment 0 in full (from h0, with outputs) beside the maps of
+    # segments 1 .. S - 2, then segments 1 .. S - 1 from their folded states;
+    # against the oracle on three heads and the unsegmented wide loop on all
+    x = synth.make_dense(1, 16, 256 * 64 + 29, 128, 128, io="bf16", h0_std=0.05,
+                         seed=697 + segments, device="cuda")
+    x = dataclasses.replace(x, log_alpha=_steep(x.log_alpha, [(1024, -3.0), (9000, -1.3)]))
+    with gdn.use_impl(gdn.GDN_IMPL_TC, segments), prep_lead(0, 1 if segments else 0):
+        o, hT = gdn.gdn_fwd(x.q, x.k, x.v, x.log_alpha, x.beta, x.h0, check=True)
+    U.sync()
+    heads = [(0, 0), (0, 7), (0, 15)]
+    o_ref, h_ref = U.oracle_dense_heads_gpu(x, heads)
+    to, th = U.TOL["bf16"]
+    for i, (b, h) in enumerate(heads):
+        assert U.rel(U.f64(o[b, h]), o_ref[i]) <= to
+        assert U.rel(U.f64(hT[b, h]), h_ref[i]) <= th
+    with gdn.use_impl(gdn.GDN_IMPL_TC, 1), prep_lead(0, 1):
+        o1, h1 = gdn.gdn_fwd(x.q, x.k, x.v, x.log_alpha, x.beta, x.h0, check=True)
+    U.sync()
+    assert U.rel(U.f64(o), U.f64(o1)) <= 1e-3 and U.rel(U.f64(hT), U.f64(h1)) <= 1e-3
