@@ -437,10 +437,13 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize(dev)
     k_ms, k_n, k_name = gdn.kernel_timer_read()
     gdn.kernel_timer(False)
-    if k_n != args.steps:
-        # one timed launch of the dominant kernel per call, or the mean mixes kernels
+    if k_n == 0 or k_n % args.steps:
+        # the same number of timed launches of the dominant kernel in every call
+        # (two for a segment scan: its map pass and its output pass), or the
+        # mean mixes kernels
         raise RuntimeError("kernel timer: %d launches of %s in %d steps" % (k_n, k_name,
                                                                           args.steps))
+    k_per_call = k_n // args.steps
     gdn.sync_check(dev)
     step_ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / args.steps
     step_ms = max_over_ranks(step_ms, world)
@@ -519,7 +522,9 @@ def run_ours(args, world, rank, local):
 
     by, flops = algorithmic_bwd(shape) if BACKWARD else algorithmic(shape)
     hbm, tf, src = load_peaks()
-    kby = kernel_bytes(k_name, shape, by)
+    # the call's compulsory bytes split over its timed launches: a segment
+    # scan's two chain launches together read every input and write every output
+    kby = kernel_bytes(k_name, shape, by) / k_per_call
     achieved = kby / (kern_ms * 1e-3) / 1e9
     res = {
         "metric": metric_for(shape),
@@ -546,11 +551,11 @@ def run_ours(args, world, rank, local):
                      if src == "measured" else "fallback 6.8 TB/s",
                      "traffic": recorded_traffic(k_name, args.workload),
                      "kernel": k_name, "kernel_ms": kern_ms,
-                     "kernel_timing": KERNEL_TIMING,
+                     "kernel_timing": KERNEL_TIMING, "launches_per_call": k_per_call,
                      "algorithmic_bytes": kby, "algorithmic_flops": flops,
                      "call_bytes": by,
                      "step_frac": by / (step_ms * 1e-3) / 1e9 / hbm,
-                     "tensor_frac_of_peak": flops / (kern_ms * 1e-3) / (tf * 1e12)},
+                     "tensor_frac_of_peak": flops / k_per_call / (kern_ms * 1e-3) / (tf * 1e12)},
         "clocks": clocks.summary(),
         "e2e": {"value": job_throughput(shape["tokens"], world, e2e_ms), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -563,7 +568,7 @@ def run_ours(args, world, rank, local):
         # the dominant kernel's products run on tf32 tensor cores (mma.sync):
         # its roof is the tf32 rate, the measured bf16 peak times the nominal ratio
         tf32 = tf * TF32_PER_BF16
-        ach = flops / (kern_ms * 1e-3) / 1e12
+        ach = flops / k_per_call / (kern_ms * 1e-3) / 1e12
         res["roofline"] = {
             "bound": "tensor", "achieved": ach, "peak": tf32, "unit": "TFLOP/s",
             "frac": ach / tf32,

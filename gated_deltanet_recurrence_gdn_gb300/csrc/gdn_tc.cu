@@ -1147,19 +1147,40 @@ gdn_status launch_tcw(const FwdArgs &a, const __nv_bfloat16 *Tin, const LaunchCf
 // Exclusive fold of the segment maps ("Gated DeltaNet GPU并行实现", sections
 // 2.3 and 3.3): with S -> S A_i + B_i the map of segment i (earlier map
 // first), the state entering segment i+1 is S_in[i] A_i + B_i, S_in[0] = h0.
-// One CTA per (batch, head, 16 state rows), fp32; each map A_i is staged in
-// shared memory (d_k^2 floats) before its product.  first_full: segment 0
-// ran from h0 itself, so B_0 is already the state entering segment 1 (and
-// there is no A_0).
+// One CTA per (batch, head, 16 state rows), fp32; each map A_i is copied into
+// shared memory (d_k^2 floats, two buffers: the next map's copy runs during
+// this one's product).  first_full: segment 0 ran from h0 itself, so B_0 is
+// already the state entering segment 1 (and there is no A_0).
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 __global__ void __launch_bounds__(256)
 k_seg_fold(const float *__restrict__ h0, const float *__restrict__ Aseg,
            const float *__restrict__ Bseg, float *__restrict__ Sin, int B, int H, int segs,
            int dv, int dk, int first_full) {
-    extern __shared__ float Sr[];   // [16][dk], then A_m [dk][dk]
-    float *As = Sr + 16 * dk;
+    extern __shared__ float Sr[];   // [16][dk], then two A_m buffers [dk][dk]
     const int tid = threadIdx.x;
     const int bh = blockIdx.x, b = bh / H, h = bh - b * H, r0 = blockIdx.y * 16;
-    const int tot = 16 * dk;
+    const int tot = 16 * dk, s0 = first_full ? 1 : 0;
+    // A_sg into buffer (sg - s0) & 1, 16-byte pieces (the 16-row blocks of one
+    // (batch, head) all read it)
+    auto fetch = [&](int sg) {
+        const long long m = (long long)b * (segs - 1) + sg;
+        const float *Am = Aseg + (m * H + h) * (long long)dk * dk;
+        float *dst = Sr + 16 * dk + ((sg - s0) & 1) * dk * dk;
+        for (int i = tid; i < dk * dk / 4; i += 256) cp_async16(dst + 4 * i, Am + 4 * i);
+        cp_async_commit();
+    };
+    if (s0 < segs - 1) fetch(s0);
     // the state entering the first folded segment: rows r0.. of B_0 or h0
     const float *src = first_full ? Bseg + ((long long)b * (segs - 1) * H + h) * dv * dk
                        : h0       ? h0 + (long long)bh * dv * dk
@@ -1169,7 +1190,7 @@ k_seg_fold(const float *__restrict__ h0, const float *__restrict__ Aseg,
         Sr[i] = src ? src[(long long)(r0 + r) * dk + cc] : 0.f;
     }
     __syncthreads();
-    for (int sg = first_full ? 1 : 0; sg < segs; ++sg) {
+    for (int sg = s0; sg < segs; ++sg) {
         const long long n = (long long)b * segs + sg;
         for (int i = tid; i < tot; i += 256) {
             const int r = i / dk, cc = i - r * dk;
@@ -1177,13 +1198,7 @@ k_seg_fold(const float *__restrict__ h0, const float *__restrict__ Aseg,
         }
         if (sg == segs - 1) break;
         const long long m = (long long)b * (segs - 1) + sg;
-        const float *Am = Aseg + (m * H + h) * (long long)dk * dk;
         const float *Bm = Bseg + ((m * H + h) * dv + r0) * (long long)dk;
-        // A_m into shared memory (the 16-row blocks of one (batch, head) all
-        // read it), 16-byte pieces
-        for (int i = tid; i < dk * dk / 4; i += 256)
-            reinterpret_cast<float4 *>(As)[i] = __ldg(reinterpret_cast<const float4 *>(Am) + i);
-        __syncthreads();
         // entry i = tid + 256 e of the 16 x dk block is row tid / dk + e (256 / dk),
         // column tid % dk (dk divides 256): a thread's entries share their
         // column, so one read of A per kk feeds all of them, and their eight
@@ -1193,6 +1208,16 @@ k_seg_fold(const float *__restrict__ h0, const float *__restrict__ Aseg,
 #pragma unroll
         for (int e = 0; e < 8; ++e)
             acc[e] = e < ne ? Bm[(long long)(rb + rs * e) * dk + cc] : 0.f;
+        // the next map's copy goes out before this one is awaited (its buffer
+        // was last read by the product two steps back, before a barrier)
+        if (sg + 1 < segs - 1) {
+            fetch(sg + 1);
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
+        }
+        __syncthreads();
+        const float *As = Sr + 16 * dk + ((sg - s0) & 1) * dk * dk;
 #pragma unroll 4
         for (int kk = 0; kk < dk; ++kk) {
             const float a = As[kk * dk + cc];
@@ -1453,7 +1478,7 @@ gdn_status tc_segmented(const FwdArgs &a, const __nv_bfloat16 *Tbuf, int S, bool
         // from zero) and linear part (final state from the identity, v = 0);
         // with head, segment 0 instead runs in full, its final state the
         // true one entering segment 1
-        LaunchCfg c1{B * (S - 1), S - 1, seglen, 1, nullptr, Bseg, lin_tiles, Aseg, false};
+        LaunchCfg c1{B * (S - 1), S - 1, seglen, 1, nullptr, Bseg, lin_tiles, Aseg, true};
         c1.seglen0 = seglen0;
         c1.seg0_full = head;
         c1.h0x = a.h0;
@@ -1462,7 +1487,7 @@ gdn_status tc_segmented(const FwdArgs &a, const __nv_bfloat16 *Tbuf, int S, bool
     if (rc == GDN_OK) {
         // pass 2: fold the maps into every segment's initial state
         dim3 grid(B * H, dv / 16);
-        const int fsm = (16 * dk + dk * dk) * (int)sizeof(float);   // 72 KB at d_k = 128
+        const int fsm = (16 * dk + 2 * dk * dk) * (int)sizeof(float);   // 136 KB at d_k = 128
         if (cudaFuncSetAttribute(k_seg_fold, cudaFuncAttributeMaxDynamicSharedMemorySize, fsm) !=
             cudaSuccess) {
             rc = GDN_ERR_CUDA;

@@ -210,8 +210,10 @@ long long gdn_get_option(int key);
 
 /*
  * Live timing of the dominant kernel, for benchmarks.  While enabled, every
- * forward call records a pair of CUDA events around the launch of its most
- * expensive kernel, on the call's stream.  gdn_kernel_timer_read() waits for
+ * forward call records a pair of CUDA events around each launch of its most
+ * expensive kernel (once per call; twice for a segment scan, whose map pass
+ * and output pass are launches of the same chunk-loop kernel), on the
+ * call's stream.  gdn_kernel_timer_read() waits for
  * those events, returns the summed duration in milliseconds, the number of
  * timed launches and the kernel's name (a static string), and clears the
  * record.  Not thread-safe; meant for one benchmarking thread.
