@@ -186,6 +186,9 @@ struct TcParams {
     // linear-part tile.
     int seg0_full;
     const float *h0x;
+    // Wide loop, packed batch: the CTAs of rank r take sequence seq_order[r]
+    // (null: sequence r).
+    const int *seq_order;
     // CTAs with blockIdx.x >= xsplit run the map's linear part instead: v = 0,
     // h0 = identity (d_k x d_k state), final state into hT2 with width dv2.
     int xsplit, dv2;
@@ -953,6 +956,7 @@ struct LaunchCfg {
     int seg_lo = 0;                         // first segment launched (wide loop)
     const float *h0x = nullptr;             // wide loop: segment 0 from h0x with outputs
     bool seg0_full = false;
+    const int *seq_order = nullptr;         // wide loop, packed batch: sequences by rank
 };
 
 // The bulk-copy maps of a chain launch: q, k, v, T_u, W (T_u's rows, then W's,
@@ -984,6 +988,7 @@ TcParams tc_params(const FwdArgs &a, int dk, const LaunchCfg &c) {
     p.seg_lo = c.seg_lo;
     p.seg0_full = c.seg0_full ? 1 : 0;
     p.h0x = c.h0x;
+    p.seq_order = c.seq_order;
     p.no_output = c.no_output;
     p.xsplit = a.dv / kNV;
     p.dv2 = dk;
@@ -1233,6 +1238,24 @@ k_seg_fold(const float *__restrict__ h0, const float *__restrict__ Aseg,
         }
         __syncthreads();
     }
+}
+
+// Longest sequences first: order[r] = the packed batch's sequence of rank r
+// by length (descending, ties by index: a permutation of 0 .. N - 1).  The
+// wide loop's CTAs run sequence-major, so in this order the longest chains
+// start in the first wave and the last wave holds the shortest.
+constexpr int kMaxOrderSeqs = 4096;   // N^2 comparisons, one thread per sequence
+__global__ void __launch_bounds__(256)
+k_seq_order(const int32_t *__restrict__ cu, int N, int *__restrict__ order) {
+    const int n = blockIdx.x * blockDim.x + threadIdx.x;
+    if (n >= N) return;
+    const int ln = __ldg(cu + n + 1) - __ldg(cu + n);
+    int r = 0;
+    for (int m = 0; m < N; ++m) {
+        const int lm = __ldg(cu + m + 1) - __ldg(cu + m);
+        r += (lm > ln || (lm == ln && m < n)) ? 1 : 0;
+    }
+    order[r] = n;
 }
 
 int sm_count() {
@@ -1578,6 +1601,18 @@ gdn_status tc_forward(const FwdArgs &a) {
         done = rc == GDN_OK;
         if (rc == GDN_ERR_UNSUPPORTED) rc = GDN_OK;   // the plain path below
     }
+    // a packed batch on the wide loop: its sequences longest first (launched
+    // before the prep, which the chain launch follows programmatically)
+    int *order = nullptr;
+    if (rc == GDN_OK && !done && wide && a.sm.cu && a.sm.N <= kMaxOrderSeqs) {
+        if (scratch_alloc((void **)&order, sizeof(int) * (size_t)a.sm.N, st) != cudaSuccess) {
+            rc = GDN_ERR_CUDA;
+        } else {
+            k_seq_order<<<(a.sm.N + 255) / 256, 256, 0, st>>>(a.sm.cu, a.sm.N, order);
+            count_launch();
+            if (cudaGetLastError() != cudaSuccess) rc = GDN_ERR_CUDA;
+        }
+    }
     if (rc == GDN_OK && !done) {
         // the tcgen05 chunk prep (gdn_ut.cu) where it applies, else gdn_prep.cu's
         __nv_bfloat16 *Wbuf = Tbuf + (size_t)a.rows * 64;
@@ -1585,7 +1620,8 @@ gdn_status tc_forward(const FwdArgs &a) {
         if (rc == GDN_ERR_UNSUPPORTED) rc = enqueue_tc_prep(a, table, Tbuf, Wbuf);
     }
     if (rc == GDN_OK && !done && wide) {
-        const LaunchCfg c{a.sm.N, 0, 0, 0, a.h0, a.hT, 0, nullptr, true};
+        LaunchCfg c{a.sm.N, 0, 0, 0, a.h0, a.hT, 0, nullptr, true};
+        c.seq_order = order;
         rc = a.dk == 128 ? launch_tcw<128>(a, Tbuf, c) : launch_tcw<64>(a, Tbuf, c);
     } else if (rc == GDN_OK && !done && S > 1) {
         rc = tc_segmented(a, Tbuf, S, wide_seg);
@@ -1595,6 +1631,7 @@ gdn_status tc_forward(const FwdArgs &a) {
     }
     scratch_free(Tbuf, st);
     if (table) scratch_free(table, st);
+    if (order) scratch_free(order, st);
     return rc;
 }
 

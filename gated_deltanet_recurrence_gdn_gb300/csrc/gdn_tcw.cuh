@@ -651,7 +651,9 @@ k_gdn_tcw(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
         gdn_tcw_body<DK, true>(&tm_q, &tm_k, &tm_v, &tm_t, &tm_w, p, b - hn * tiles, h,
                                bb * p.segs + sg, p.sm.N * p.segs);
     } else {
-        gdn_tcw_body<DK, true>(&tm_q, &tm_k, &tm_v, &tm_t, &tm_w, p, b - hn * tiles, h, q,
+        // a packed batch may run its sequences in a given order (longest first)
+        const int n = p.seq_order ? __ldg(p.seq_order + q) : q;
+        gdn_tcw_body<DK, true>(&tm_q, &tm_k, &tm_v, &tm_t, &tm_w, p, b - hn * tiles, h, n,
                                gridDim.x / (tiles * p.sm.H));
     }
 }

@@ -174,13 +174,16 @@ def test_wide_chain_plain_and_automatic(B, H, T, dk, wide):
     assert U.rel(U.f64(o), U.f64(o1)) <= 1e-3 and U.rel(U.f64(hT), U.f64(h1)) <= 1e-3
 
 
+@pytest.mark.parametrize("lengths", [[300, 1, 64, 200, 0, 129, 700],
+                                     [129, 64, 129, 0, 64, 700, 0, 1]])
 @pytest.mark.parametrize("dk,dv", [(128, 128), (64, 256)])
-def test_wide_chain_packed_batch(dk, dv):
+def test_wide_chain_packed_batch(dk, dv, lengths):
     # packed sequences (chunk tails that the next sequence's rows would fill,
-    # an empty one, h0): the wide loop forced, against the oracle and the
+    # empty ones, h0; the wide loop runs them longest first, the second list
+    # with ties in length): the wide loop forced, against the oracle and the
     # 64-column loop
-    y = synth.make_varlen([300, 1, 64, 200, 0, 129, 700], 3, dk, dv, io="bf16", h0_std=0.1,
-                          seed=651 + dk + dv, device="cuda")
+    y = synth.make_varlen(lengths, 3, dk, dv, io="bf16", h0_std=0.1,
+                          seed=651 + dk + dv + len(lengths), device="cuda")
     y = dataclasses.replace(y, log_alpha=_steep(y.log_alpha, [(64, -3.0), (365, -1.3)]))
 
     def run(wide):
